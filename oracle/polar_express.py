@@ -18,8 +18,13 @@ alternation theorem for Haar spaces on [l, u] with l > 0). The interior extrema 
 error are the roots of p'(x) = a + 3 b x^2 + 5 c x^4, a quadratic in x^2, so each
 exchange finds them in closed form.
 
-Optional ``safety`` > 1 evaluates p_t(x / safety) (coefficients rescaled), a margin
-against rounding pushing singular values above the interval; off by default.
+Each step's polynomial is applied at x / safety (coefficients rescaled: a/s, b/s^3, c/s^5),
+safety = 1.01 by default: our reading of the scheme's safeguard against round-off. The
+polynomials of the middle steps are steep at the top of their interval, so a singular value
+that rounding pushes slightly past it is amplified step after step and the iteration diverges
+in bf16; evaluating at x / 1.01 keeps a 1% overshoot inside the interval the next step was
+designed for. With the margin, step t maps [l_t, u_t] into [q_t(l_t), 1 + E_t], which is the
+next interval (q_t the rescaled polynomial, E_t the minimax error).
 
 Parity of the GPU path never depends on these values (oracle and kernels receive the same
 table). Fidelity to the published table is parity unpinned; the solver itself is pinned
@@ -74,17 +79,14 @@ def minimax_odd_quintic(lo: float, hi: float, iters: int = 100, tol: float = 1e-
     return tuple(float(v) for v in coef), abs(E), pts
 
 
-def polar_express_table(steps: int, l0: float = 1e-3, safety: float = 1.0) -> List[Tuple[float, float, float]]:
+def polar_express_table(steps: int, l0: float = 1e-3, safety: float = 1.01) -> List[Tuple[float, float, float]]:
     lo, hi = l0, 1.0
     table = []
     for _ in range(steps):
         (a, b, c), E, _ = minimax_odd_quintic(lo, hi)
-        if safety != 1.0:
-            a, b, c = a / safety, b / safety ** 3, c / safety ** 5
+        a, b, c = a / safety, b / safety ** 3, c / safety ** 5
         table.append((a, b, c))
-        lo, hi = 1.0 - E, 1.0 + E
-        if safety != 1.0:
-            lo, hi = lo, hi  # the interval bound is kept from the exact minimax step
+        lo, hi = a * lo + b * lo ** 3 + c * lo ** 5, 1.0 + E
     return table
 
 
@@ -97,10 +99,12 @@ def main(argv=None) -> int:
     for steps in (5, 8):
         table = polar_express_table(steps)
         doc = {
-            "source": "oracle/polar_express.py: greedy per-step minimax odd quintics on [l_t, u_t], l_0=1e-3, u_0=1 "
+            "source": "oracle/polar_express.py: greedy per-step minimax odd quintics on [l_t, u_t], l_0=1e-3, u_0=1, "
+                      "each applied at x/1.01 "
                       "(Polar Express scheme, arXiv 2505.16932, named by the dtensor-muon 0.1.0 package description, "
                       "section 'What is Muon?'; the pages print no coefficients)",
             "l0": 1e-3,
+            "safety": 1.01,
             "steps": steps,
             "coeffs": [list(abc) for abc in table],
         }
