@@ -1,0 +1,338 @@
+// Bandwidth-bound kernels of the optimizer step.
+//
+//   nesterov_norm_kernel  momentum M <- mu M + G, Nesterov input U = G + mu M (or M), per-tile sums of
+//                         U^2 for the Frobenius norm, U stored bf16 in the wide orientation
+//                         ("Optimizers: AdamW, Muon and the distributed optimizer", section "Muon:
+//                         orthogonalising the update": the momentum rule and newton_schulz's first lines).
+//   norm_finalize_kernel  s_k = 1 / (sqrt(sum of the tile sums) + eps), one block per matrix, fixed
+//                         summation order (the result does not depend on scheduling).
+//   adamw kernels         AdamW with bias correction and decoupled decay (same page, section "AdamW:
+//                         decoupled weight decay"), 16-byte vector accesses when aligned.
+//   debug_wait_kernel     one bounded wait on a barrier nothing completes.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace muon {
+
+namespace {
+
+__device__ __forceinline__ float ld_f(const float *p, long long i) { return p[i]; }
+__device__ __forceinline__ float ld_f(const __nv_bfloat16 *p, long long i) { return __bfloat162float(p[i]); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Block of 256 threads on one 64 x 64 tile of the stored (A x B) matrix; thread (tx, ty) handles
+// columns 4*tx..4*tx+3 of rows ty, ty+16, ty+32, ty+48.
+template <typename GT, bool MOMENTUM>
+__global__ void __launch_bounds__(256) nesterov_norm_kernel(const NesterovArgs a) {
+  constexpr int T = NESTEROV_TILE;
+  __shared__ __nv_bfloat16 tile[T][T + 8];
+  __shared__ float red[8];
+  const int b = blockIdx.y;
+  const int tr = blockIdx.x / a.tiles_c;
+  const int tc = blockIdx.x - tr * a.tiles_c;
+  const long long mat = static_cast<long long>(a.A) * a.B;
+  const GT *g = a.gptrs != nullptr ? static_cast<const GT *>(a.gptrs[b])
+                                   : static_cast<const GT *>(a.gbase) + static_cast<long long>(b) * mat;
+  float *M = MOMENTUM ? a.momentum + static_cast<long long>(b) * mat : nullptr;
+  __nv_bfloat16 *u = a.u + static_cast<long long>(b) * a.mstride_u;
+
+  const int tx = threadIdx.x & 15;
+  const int ty = threadIdx.x >> 4;
+  const int c0 = tc * T + tx * 4;
+  // vector path: the 4 columns are in range and both rows are 16-byte (M) / 4-element (G) aligned
+  const bool vec = (a.B % 4 == 0) && (c0 + 4 <= a.B) &&
+                   ((reinterpret_cast<uintptr_t>(g) & (4 * sizeof(GT) - 1)) == 0) &&
+                   (!MOMENTUM || (reinterpret_cast<uintptr_t>(M) & 15) == 0);
+  float ss = 0.f;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const int lrow = ty + 16 * p;
+    const int r = tr * T + lrow;
+    float uv[4] = {0.f, 0.f, 0.f, 0.f};
+    if (r < a.A) {
+      const long long base = static_cast<long long>(r) * a.B + c0;
+      float gv[4], mv[4];
+      if (vec) {
+        if constexpr (sizeof(GT) == 4) {
+          const float4 q = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(g) + base);
+          gv[0] = q.x; gv[1] = q.y; gv[2] = q.z; gv[3] = q.w;
+        } else {
+          const uint2 q = *reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(g) + base);
+          const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&q.x));
+          const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&q.y));
+          gv[0] = lo.x; gv[1] = lo.y; gv[2] = hi.x; gv[3] = hi.y;
+        }
+        if constexpr (MOMENTUM) {
+          const float4 q = *reinterpret_cast<const float4 *>(M + base);
+          mv[0] = q.x; mv[1] = q.y; mv[2] = q.z; mv[3] = q.w;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const bool in = c0 + q < a.B;
+          gv[q] = in ? ld_f(g, base + q) : 0.f;
+          mv[q] = (MOMENTUM && in) ? M[base + q] : 0.f;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if constexpr (MOMENTUM) {
+          const float mn = fmaf(a.mu, mv[q], gv[q]);
+          mv[q] = mn;
+          uv[q] = a.nesterov ? fmaf(a.mu, mn, gv[q]) : mn;
+        } else {
+          uv[q] = gv[q];
+        }
+        if (c0 + q >= a.B) uv[q] = 0.f;
+        ss = fmaf(uv[q], uv[q], ss);
+      }
+      if constexpr (MOMENTUM) {
+        if (vec) {
+          *reinterpret_cast<float4 *>(M + base) = make_float4(mv[0], mv[1], mv[2], mv[3]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (c0 + q < a.B) M[base + q] = mv[q];
+        }
+      }
+      if (!a.transposed) {
+        __nv_bfloat16 *dst = u + static_cast<long long>(r) * a.ldu + c0;
+        if (c0 + 4 <= a.B) {
+          __nv_bfloat162 w[2] = {__floats2bfloat162_rn(uv[0], uv[1]), __floats2bfloat162_rn(uv[2], uv[3])};
+          *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<uint2 *>(w);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (c0 + q < a.B) dst[q] = __float2bfloat16_rn(uv[q]);
+        }
+      }
+    }
+    if (a.transposed) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tile[tx * 4 + q][lrow] = __float2bfloat16_rn(uv[q]);
+    }
+  }
+  if (a.transposed) {
+    __syncthreads();
+    // wide row = stored column, wide column = stored row
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const int lc = ty + 16 * p;
+      const int c = tc * T + lc;
+      const int r0 = tr * T + tx * 4;
+      if (c < a.B) {
+        __nv_bfloat16 *dst = u + static_cast<long long>(c) * a.ldu + r0;
+        if (r0 + 4 <= a.A) {
+          *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(&tile[lc][tx * 4]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (r0 + q < a.A) dst[q] = tile[lc][tx * 4 + q];
+        }
+      }
+    }
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += red[w];
+    a.partials[static_cast<long long>(b) * gridDim.x + blockIdx.x] = t;
+  }
+}
+
+__global__ void __launch_bounds__(256) norm_finalize_kernel(const float *partials, int tiles, float *scale,
+                                                            float eps) {
+  __shared__ float red[8];
+  const int b = blockIdx.x;
+  const float *p = partials + static_cast<long long>(b) * tiles;
+  float s = 0.f;
+  for (int i = threadIdx.x; i < tiles; i += 256) s += p[i];
+  s = warp_sum(s);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += red[w];
+    scale[b] = 1.0f / (sqrtf(t) + eps);
+  }
+}
+
+// ------------------------------------------------------------------------------------------ AdamW
+
+__device__ __forceinline__ float adamw_elem(float &pf, float gf, float &mf, float &vf, const AdamwConst &c) {
+  pf *= c.decay;
+  mf = fmaf(c.beta1, mf, c.one_minus_beta1 * gf);
+  vf = fmaf(c.beta2, vf, c.one_minus_beta2 * gf * gf);
+  const float denom = sqrtf(vf) * c.inv_sqrt_bc2 + c.eps;
+  pf = pf - c.step_size * (mf / denom);
+  return pf;
+}
+
+template <typename T>
+__device__ __forceinline__ void load8(const T *p, float *f);
+template <>
+__device__ __forceinline__ void load8<float>(const float *p, float *f) {
+  const float4 a = reinterpret_cast<const float4 *>(p)[0];
+  const float4 b = reinterpret_cast<const float4 *>(p)[1];
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16 *p, float *f) {
+  const uint4 w = reinterpret_cast<const uint4 *>(p)[0];
+  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&w);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 x = __bfloat1622float2(h[e]);
+    f[2 * e] = x.x;
+    f[2 * e + 1] = x.y;
+  }
+}
+template <typename T>
+__device__ __forceinline__ void store8(T *p, const float *f);
+template <>
+__device__ __forceinline__ void store8<float>(float *p, const float *f) {
+  reinterpret_cast<float4 *>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+  reinterpret_cast<float4 *>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+template <>
+__device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16 *p, const float *f) {
+  uint4 w;
+  __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
+  reinterpret_cast<uint4 *>(p)[0] = w;
+}
+
+template <typename T>
+__device__ __forceinline__ float load1(const T *p, long long i);
+template <>
+__device__ __forceinline__ float load1<float>(const float *p, long long i) { return p[i]; }
+template <>
+__device__ __forceinline__ float load1<__nv_bfloat16>(const __nv_bfloat16 *p, long long i) {
+  return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void store1(float *p, long long i, float v) { p[i] = v; }
+__device__ __forceinline__ void store1(__nv_bfloat16 *p, long long i, float v) { p[i] = __float2bfloat16_rn(v); }
+
+// Groups of 8 elements from `first`, then the scalar tail; vec=false runs everything scalar.
+template <typename PT, typename GT>
+__global__ void __launch_bounds__(256) adamw_kernel(PT *__restrict__ p, const GT *__restrict__ g,
+                                                    float *__restrict__ m, float *__restrict__ v, long long n,
+                                                    int vec, AdamwConst c) {
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  long long done = 0;
+  if (vec) {
+    const long long groups = n / 8;
+    for (long long i = tid; i < groups; i += stride) {
+      const long long o = i * 8;
+      float pf[8], gf[8], mf[8], vf[8];
+      load8(p + o, pf);
+      load8(g + o, gf);
+      load8(m + o, mf);
+      load8(v + o, vf);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) adamw_elem(pf[e], gf[e], mf[e], vf[e], c);
+      store8(p + o, pf);
+      store8(m + o, mf);
+      store8(v + o, vf);
+    }
+    done = groups * 8;
+  }
+  for (long long i = done + tid; i < n; i += stride) {
+    float pf = load1(p, i), mf = m[i], vf = v[i];
+    adamw_elem(pf, load1(g, i), mf, vf, c);
+    store1(p, i, pf);
+    m[i] = mf;
+    v[i] = vf;
+  }
+}
+
+__global__ void debug_wait_kernel(uint32_t *err, unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    WaitCtl ctl{&abort_flag, err, timeout_ns};
+    wait_bounded(&bar, 0u, ctl, ERR_WAIT_DEBUG);
+  }
+}
+
+}  // namespace
+
+muon_status launch_nesterov_norm(const NesterovArgs &a, int K, cudaStream_t s) {
+  const dim3 grid(a.tiles_r * a.tiles_c, K);
+  launch_begin(KK_NESTEROV_NORM, s);
+  const bool mom = a.momentum != nullptr;
+  if (a.gdtype == MUON_F32) {
+    if (mom) nesterov_norm_kernel<float, true><<<grid, 256, 0, s>>>(a);
+    else nesterov_norm_kernel<float, false><<<grid, 256, 0, s>>>(a);
+  } else {
+    if (mom) nesterov_norm_kernel<__nv_bfloat16, true><<<grid, 256, 0, s>>>(a);
+    else nesterov_norm_kernel<__nv_bfloat16, false><<<grid, 256, 0, s>>>(a);
+  }
+  launch_end(s);
+  return cudaGetLastError() == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+}
+
+muon_status launch_norm_finalize(const float *partials, int tiles, float *scale, int K, float eps, cudaStream_t s) {
+  launch_begin(KK_NORM_FINALIZE, s);
+  norm_finalize_kernel<<<K, 256, 0, s>>>(partials, tiles, scale, eps);
+  launch_end(s);
+  return cudaGetLastError() == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+}
+
+muon_status launch_adamw(void *p, int pdt, const void *g, int gdt, float *m, float *v, long long n,
+                         const AdamwConst &c, cudaStream_t s) {
+  auto aligned = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
+  const int vec = aligned(p) && aligned(g) && aligned(m) && aligned(v) &&
+                  (pdt == MUON_F32 || (reinterpret_cast<uintptr_t>(p) & 15) == 0);
+  const long long work = vec ? (n / 8 + (n % 8)) : n;
+  const long long sms = device_sm_count();
+  long long blocks = (work + 255) / 256;
+  const long long cap = sms * 8;  // 8 resident 256-thread blocks per SM, grid-stride beyond that
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  launch_begin(KK_ADAMW, s);
+  const int gb = static_cast<int>(blocks);
+  if (pdt == MUON_F32 && gdt == MUON_F32)
+    adamw_kernel<float, float><<<gb, 256, 0, s>>>(static_cast<float *>(p), static_cast<const float *>(g), m, v, n,
+                                                  vec, c);
+  else if (pdt == MUON_F32 && gdt == MUON_BF16)
+    adamw_kernel<float, __nv_bfloat16><<<gb, 256, 0, s>>>(static_cast<float *>(p),
+                                                          static_cast<const __nv_bfloat16 *>(g), m, v, n, vec, c);
+  else if (pdt == MUON_BF16 && gdt == MUON_F32)
+    adamw_kernel<__nv_bfloat16, float><<<gb, 256, 0, s>>>(static_cast<__nv_bfloat16 *>(p),
+                                                          static_cast<const float *>(g), m, v, n, vec, c);
+  else
+    adamw_kernel<__nv_bfloat16, __nv_bfloat16><<<gb, 256, 0, s>>>(
+        static_cast<__nv_bfloat16 *>(p), static_cast<const __nv_bfloat16 *>(g), m, v, n, vec, c);
+  launch_end(s);
+  return cudaGetLastError() == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+}
+
+muon_status launch_debug_wait(uint32_t *err, unsigned long long timeout_ns, cudaStream_t s) {
+  launch_begin(KK_DEBUG_WAIT, s);
+  debug_wait_kernel<<<1, 32, 0, s>>>(err, timeout_ns);
+  launch_end(s);
+  return cudaGetLastError() == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+}
+
+}  // namespace muon

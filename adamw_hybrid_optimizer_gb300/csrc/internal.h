@@ -1,0 +1,128 @@
+// Internal interfaces between the C-ABI layer (libmuon.cu) and the kernels (ns_gemm.cu, elementwise.cu).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/libmuon.h"
+
+namespace muon {
+
+// Kernel kinds, for launch counting and the event trace.
+enum KernelKind : int32_t {
+  KK_ADAMW = 0,
+  KK_NESTEROV_NORM = 1,
+  KK_NORM_FINALIZE = 2,
+  KK_GRAM = 3,
+  KK_POLY = 4,
+  KK_APPLY = 5,
+  KK_FINAL = 6,
+  KK_DEBUG_WAIT = 7,
+  KK_COUNT = 8
+};
+
+// Launch bookkeeping (libmuon.cu): counts launches and, while tracing, records an event pair.
+void launch_begin(int32_t kind, cudaStream_t s);
+void launch_end(cudaStream_t s);
+int device_sm_count();
+
+// ------------------------------------------------------------------------------------------ tensor-core GEMMs
+
+enum EpiKind : int { EPI_GRAM = 0, EPI_POLY = 1, EPI_APPLY = 2, EPI_FINAL = 3 };
+
+// Arguments of one grouped tensor-core launch over a batch of K matrices.
+struct GemmArgs {
+  // tile space of the output (per matrix: rows x cols), 128 x 256 tiles
+  int batch;
+  int rows;
+  int cols;
+  int m_tiles, n_tiles;
+  int tiles_per_matrix;
+  long long total_tiles;
+  int k_iters;      // contraction / 64, rounded up
+  int symmetric;    // 1: only tiles touching the upper triangle; each value also stored mirrored
+  // epilogue coefficients
+  float alpha;            // gram: output = alpha * s^scale_pow * acc
+  float coef_a, coef_b, coef_c;
+  const float *scale;     // per-matrix normalisation s_k (device), or null
+  int scale_pow;
+  // bf16 output of gram / poly / apply
+  __nv_bfloat16 *out;
+  long long ld_out, mstride_out;
+  // second input read by the epilogue: G for poly, X for apply / final
+  const __nv_bfloat16 *aux;
+  long long ld_aux, mstride_aux;
+  // final step: parameter update (params != null) or dense store (out_dense != null)
+  void *const *params;
+  void *out_dense;
+  int out_dtype;          // muon_dtype of params / out_dense
+  int transposed;         // stored matrix is the transpose of the wide iterate
+  int orig_cols;          // columns of the stored matrix
+  int cautious;
+  float lr_wd;            // lr * weight_decay
+  float lr_scale;         // lr * update scale
+  // control
+  uint32_t *err;
+  unsigned long long timeout_ns;
+};
+
+// A bf16 matrix stack in global memory as the GEMMs see it: K matrices of rows x cols,
+// row pitch ld elements (multiple of 8), matrix pitch mstride elements.
+struct Bf16Stack {
+  const void *ptr;
+  long long rows, cols, ld, mstride, batch;
+};
+
+muon_status launch_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long ldg, long long mstride_g, float alpha,
+                        const float *scale, uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
+muon_status launch_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float b, float c,
+                        uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
+muon_status launch_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, float a, const float *scale,
+                         uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
+// Final iteration: u = s*(a*x + h x) in the wide orientation, then either the Muon parameter update
+// or a dense store, transposing back when the stored matrix is tall.
+struct FinalSpec {
+  void *const *params;   // device array of K pointers (update) or null
+  void *out_dense;       // contiguous (K, A, B) (store) or null
+  int dtype;             // muon_dtype
+  int transposed;
+  int orig_cols;
+  int cautious;
+  float lr_wd, lr_scale;
+};
+muon_status launch_final(const Bf16Stack &h, const Bf16Stack &x, float a, const float *scale, const FinalSpec &f,
+                         uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
+
+// ------------------------------------------------------------------------------------------ elementwise
+
+// Momentum + Nesterov + Frobenius partial sums + bf16 store in the wide orientation.
+struct NesterovArgs {
+  const void *const *gptrs;  // device array of K pointers, or null (then gbase is used)
+  const void *gbase;         // contiguous (K, A, B)
+  int gdtype;
+  float *momentum;           // (K, A, B) fp32 or null (plain normalisation, no momentum)
+  __nv_bfloat16 *u;
+  long long ldu, mstride_u;
+  float *partials;           // [K][tiles]
+  int A, B, tiles_r, tiles_c, transposed;
+  float mu;
+  int nesterov;
+};
+constexpr int NESTEROV_TILE = 64;
+muon_status launch_nesterov_norm(const NesterovArgs &a, int K, cudaStream_t s);
+muon_status launch_norm_finalize(const float *partials, int tiles, float *scale, int K, float eps, cudaStream_t s);
+
+struct AdamwConst {
+  float decay;          // 1 - lr*wd
+  float beta1, one_minus_beta1, beta2, one_minus_beta2;
+  float step_size;      // lr / (1 - beta1^t)
+  float inv_sqrt_bc2;   // 1 / sqrt(1 - beta2^t)
+  float eps;
+};
+muon_status launch_adamw(void *p, int pdt, const void *g, int gdt, float *m, float *v, long long n,
+                         const AdamwConst &c, cudaStream_t s);
+
+muon_status launch_debug_wait(uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
+
+}  // namespace muon

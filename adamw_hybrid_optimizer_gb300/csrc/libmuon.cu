@@ -1,0 +1,514 @@
+// libmuon C ABI: argument checks, workspace layout, the order of launches of one optimizer step,
+// launch counting and the optional event trace. See include/libmuon.h for the contract.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+#include <map>
+#include <utility>
+#include <vector>
+
+#include "../../include/libmuon.h"
+#include "internal.h"
+
+namespace muon {
+namespace {
+
+// ------------------------------------------------------------------------------------------ device state
+
+struct DeviceInfo {
+  bool probed = false;
+  bool supported = false;
+  int sms = 0;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return -1;
+  return d;
+}
+
+muon_status check_device() {
+  const int d = current_device();
+  if (d < 0 || d >= 64) return MUON_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo &di = g_dev[d];
+  if (!di.probed) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess)
+      return MUON_ERR_CUDA;
+    di.probed = true;
+    di.supported = (major == 10 && minor == 3);
+    di.sms = sms;
+  }
+  return di.supported ? MUON_OK : MUON_ERR_UNSUPPORTED_DEVICE;
+}
+
+// ------------------------------------------------------------------------------------------ trace
+
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+int64_t g_launches = 0;
+struct TraceRec {
+  int32_t kind;
+  cudaEvent_t start, stop;
+};
+std::vector<TraceRec> g_trace;
+std::vector<cudaEvent_t> g_event_pool;
+constexpr size_t TRACE_CAP = 65536;
+int32_t g_pending_kind = -1;
+cudaEvent_t g_pending_start = nullptr;
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+unsigned long long g_timeout_ns = 2000000000ull;
+
+}  // namespace
+
+void launch_begin(int32_t kind, cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  ++g_launches;
+  g_pending_kind = -1;
+  if (!g_trace_on || g_trace.size() >= TRACE_CAP) return;
+  cudaEvent_t e = take_event();
+  if (e == nullptr) return;
+  cudaEventRecord(e, s);
+  g_pending_kind = kind;
+  g_pending_start = e;
+}
+
+void launch_end(cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (g_pending_kind < 0) return;
+  cudaEvent_t e = take_event();
+  if (e == nullptr) {
+    g_event_pool.push_back(g_pending_start);
+  } else {
+    cudaEventRecord(e, s);
+    g_trace.push_back({g_pending_kind, g_pending_start, e});
+  }
+  g_pending_kind = -1;
+}
+
+int device_sm_count() {
+  const int d = current_device();
+  if (d < 0 || d >= 64) return 1;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  return g_dev[d].sms > 0 ? g_dev[d].sms : 1;
+}
+
+namespace {
+
+// ------------------------------------------------------------------------------------------ workspace
+
+constexpr size_t CTRL_BYTES = 256;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+long long round8(long long v) { return (v + 7) / 8 * 8; }
+
+struct Layout {
+  long long m, n, ldx, ldg, tiles_r, tiles_c;
+  size_t scale, partial, x0, x1, g, h, total;
+};
+
+Layout layout(long long K, long long A, long long B) {
+  Layout L{};
+  L.m = A < B ? A : B;
+  L.n = A < B ? B : A;
+  L.ldx = round8(L.n);
+  L.ldg = round8(L.m);
+  L.tiles_r = (A + NESTEROV_TILE - 1) / NESTEROV_TILE;
+  L.tiles_c = (B + NESTEROV_TILE - 1) / NESTEROV_TILE;
+  size_t off = CTRL_BYTES;
+  off = align_up(off, 1024);
+  L.scale = off;
+  off = align_up(off + static_cast<size_t>(K) * 4, 1024);
+  L.partial = off;
+  off = align_up(off + static_cast<size_t>(K) * L.tiles_r * L.tiles_c * 4, 1024);
+  L.x0 = off;
+  off = align_up(off + static_cast<size_t>(K) * L.m * L.ldx * 2, 1024);
+  L.x1 = off;
+  off = align_up(off + static_cast<size_t>(K) * L.m * L.ldx * 2, 1024);
+  L.g = off;
+  off = align_up(off + static_cast<size_t>(K) * L.m * L.ldg * 2, 1024);
+  L.h = off;
+  off = align_up(off + static_cast<size_t>(K) * L.m * L.ldg * 2, 1024);
+  L.total = off;
+  return L;
+}
+
+bool valid_dtype(int d) { return d == MUON_F32 || d == MUON_BF16; }
+
+muon_status check_stack_dims(int64_t K, int64_t A, int64_t B) {
+  if (K < 1 || A < 1 || B < 1) return MUON_ERR_INVALID_ARG;
+  if (A > 65536 || B > 65536 || K > (1ll << 31)) return MUON_ERR_SHAPE;
+  const long double elems = static_cast<long double>(K) * A * B;
+  if (elems >= static_cast<long double>(1ll << 40)) return MUON_ERR_SHAPE;
+  return MUON_OK;
+}
+
+muon_status check_coeffs(int ns_steps, const float *coeffs) {
+  if (ns_steps < 1 || ns_steps > MUON_MAX_NS_STEPS || coeffs == nullptr) return MUON_ERR_INVALID_ARG;
+  for (int i = 0; i < 3 * ns_steps; ++i)
+    if (!std::isfinite(coeffs[i])) return MUON_ERR_INVALID_ARG;
+  return MUON_OK;
+}
+
+// The Newton-Schulz chain on the wide iterate in x0 (unnormalised U; s_k in `scale`), ending in
+// launch_final. Iteration t reads X from one iterate buffer and writes the other.
+muon_status run_ns_chain(char *ws, const Layout &L, long long K, int ns_steps, const float *coeffs,
+                         const FinalSpec &fin, cudaStream_t s) {
+  uint32_t *err = reinterpret_cast<uint32_t *>(ws);
+  const float *scale = reinterpret_cast<const float *>(ws + L.scale);
+  __nv_bfloat16 *xb[2] = {reinterpret_cast<__nv_bfloat16 *>(ws + L.x0), reinterpret_cast<__nv_bfloat16 *>(ws + L.x1)};
+  __nv_bfloat16 *G = reinterpret_cast<__nv_bfloat16 *>(ws + L.g);
+  __nv_bfloat16 *H = reinterpret_cast<__nv_bfloat16 *>(ws + L.h);
+  const long long mstride_x = L.m * L.ldx;
+  const long long mstride_g = L.m * L.ldg;
+  const unsigned long long to = g_timeout_ns;
+  muon_status st = MUON_OK;
+  for (int t = 0; t < ns_steps; ++t) {
+    const float a = coeffs[3 * t], b = coeffs[3 * t + 1], c = coeffs[3 * t + 2];
+    const float *sc = (t == 0) ? scale : nullptr;
+    Bf16Stack X{xb[t & 1], L.m, L.n, L.ldx, mstride_x, K};
+    if ((st = launch_gram(X, G, L.ldg, mstride_g, 1.0f, sc, err, to, s)) != MUON_OK) return st;
+    Bf16Stack Gs{G, L.m, L.m, L.ldg, mstride_g, K};
+    if ((st = launch_poly(Gs, H, L.ldg, mstride_g, b, c, err, to, s)) != MUON_OK) return st;
+    Bf16Stack Hs{H, L.m, L.m, L.ldg, mstride_g, K};
+    if (t + 1 < ns_steps) {
+      if ((st = launch_apply(Hs, X, xb[(t + 1) & 1], a, sc, err, to, s)) != MUON_OK) return st;
+    } else {
+      if ((st = launch_final(Hs, X, a, sc, fin, err, to, s)) != MUON_OK) return st;
+    }
+  }
+  return MUON_OK;
+}
+
+}  // namespace
+}  // namespace muon
+
+using namespace muon;
+
+extern "C" {
+
+size_t muon_workspace_bytes(int64_t K, int64_t A, int64_t B) {
+  if (K < 1 || A < 1 || B < 1) return 0;
+  return layout(K, A, B).total;
+}
+
+muon_status muon_step_batched(void *const *params, muon_dtype pdt, const void *const *grads, muon_dtype gdt,
+                              float *momentum, int64_t K, int64_t A, int64_t B, const muon_hparams *hp, void *ws,
+                              size_t ws_bytes, muon_stream_t stream) {
+  if (params == nullptr || grads == nullptr || momentum == nullptr || hp == nullptr || ws == nullptr)
+    return MUON_ERR_INVALID_ARG;
+  muon_status st = check_stack_dims(K, A, B);
+  if (st != MUON_OK) return st;
+  if (!valid_dtype(pdt) || !valid_dtype(gdt)) return MUON_ERR_DTYPE;
+  if ((st = check_coeffs(hp->ns_steps, hp->coeffs)) != MUON_OK) return st;
+  if (hp->scale_mode != 0 && hp->scale_mode != 1) return MUON_ERR_INVALID_ARG;
+  if (!std::isfinite(hp->lr) || !std::isfinite(hp->momentum) || !std::isfinite(hp->weight_decay) ||
+      !std::isfinite(hp->eps) || hp->eps < 0.f)
+    return MUON_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MUON_ERR_ALIGNMENT;
+  const Layout L = layout(K, A, B);
+  if (ws_bytes < L.total) return MUON_ERR_WORKSPACE;
+  if ((st = check_device()) != MUON_OK) return st;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char *w = static_cast<char *>(ws);
+  NesterovArgs na{};
+  na.gptrs = grads;
+  na.gbase = nullptr;
+  na.gdtype = gdt;
+  na.momentum = momentum;
+  na.u = reinterpret_cast<__nv_bfloat16 *>(w + L.x0);
+  na.ldu = L.ldx;
+  na.mstride_u = L.m * L.ldx;
+  na.partials = reinterpret_cast<float *>(w + L.partial);
+  na.A = static_cast<int>(A);
+  na.B = static_cast<int>(B);
+  na.tiles_r = static_cast<int>(L.tiles_r);
+  na.tiles_c = static_cast<int>(L.tiles_c);
+  na.transposed = A > B ? 1 : 0;
+  na.mu = hp->momentum;
+  na.nesterov = hp->nesterov ? 1 : 0;
+  if ((st = launch_nesterov_norm(na, static_cast<int>(K), s)) != MUON_OK) return st;
+  if ((st = launch_norm_finalize(na.partials, static_cast<int>(L.tiles_r * L.tiles_c),
+                                 reinterpret_cast<float *>(w + L.scale), static_cast<int>(K), hp->eps, s)) != MUON_OK)
+    return st;
+
+  const double scale = hp->scale_mode == 0 ? 0.2 * std::sqrt(static_cast<double>(A > B ? A : B))
+                                           : std::sqrt(std::max(1.0, static_cast<double>(A) / static_cast<double>(B)));
+  FinalSpec fin{};
+  fin.params = params;
+  fin.out_dense = nullptr;
+  fin.dtype = pdt;
+  fin.transposed = na.transposed;
+  fin.orig_cols = static_cast<int>(B);
+  fin.cautious = hp->cautious_wd ? 1 : 0;
+  fin.lr_wd = static_cast<float>(static_cast<double>(hp->lr) * hp->weight_decay);
+  fin.lr_scale = static_cast<float>(static_cast<double>(hp->lr) * scale);
+  return run_ns_chain(w, L, K, hp->ns_steps, hp->coeffs, fin, s);
+}
+
+muon_status ns_orthogonalize(const void *x, muon_dtype xdt, void *out, muon_dtype odt, int64_t K, int64_t A,
+                             int64_t B, int ns_steps, const float *coeffs, float eps, void *ws, size_t ws_bytes,
+                             muon_stream_t stream) {
+  if (x == nullptr || out == nullptr || ws == nullptr) return MUON_ERR_INVALID_ARG;
+  muon_status st = check_stack_dims(K, A, B);
+  if (st != MUON_OK) return st;
+  if (!valid_dtype(xdt) || !valid_dtype(odt)) return MUON_ERR_DTYPE;
+  if ((st = check_coeffs(ns_steps, coeffs)) != MUON_OK) return st;
+  if (!std::isfinite(eps) || eps < 0.f) return MUON_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MUON_ERR_ALIGNMENT;
+  const Layout L = layout(K, A, B);
+  if (ws_bytes < L.total) return MUON_ERR_WORKSPACE;
+  if ((st = check_device()) != MUON_OK) return st;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char *w = static_cast<char *>(ws);
+  NesterovArgs na{};
+  na.gptrs = nullptr;
+  na.gbase = x;
+  na.gdtype = xdt;
+  na.momentum = nullptr;
+  na.u = reinterpret_cast<__nv_bfloat16 *>(w + L.x0);
+  na.ldu = L.ldx;
+  na.mstride_u = L.m * L.ldx;
+  na.partials = reinterpret_cast<float *>(w + L.partial);
+  na.A = static_cast<int>(A);
+  na.B = static_cast<int>(B);
+  na.tiles_r = static_cast<int>(L.tiles_r);
+  na.tiles_c = static_cast<int>(L.tiles_c);
+  na.transposed = A > B ? 1 : 0;
+  if ((st = launch_nesterov_norm(na, static_cast<int>(K), s)) != MUON_OK) return st;
+  if ((st = launch_norm_finalize(na.partials, static_cast<int>(L.tiles_r * L.tiles_c),
+                                 reinterpret_cast<float *>(w + L.scale), static_cast<int>(K), eps, s)) != MUON_OK)
+    return st;
+  FinalSpec fin{};
+  fin.params = nullptr;
+  fin.out_dense = out;
+  fin.dtype = odt;
+  fin.transposed = na.transposed;
+  fin.orig_cols = static_cast<int>(B);
+  return run_ns_chain(w, L, K, ns_steps, coeffs, fin, s);
+}
+
+muon_status adamw_step(void *param, muon_dtype pdt, const void *grad, muon_dtype gdt, float *exp_avg,
+                       float *exp_avg_sq, int64_t n, const adamw_hparams *hp, muon_stream_t stream) {
+  if (param == nullptr || grad == nullptr || exp_avg == nullptr || exp_avg_sq == nullptr || hp == nullptr)
+    return MUON_ERR_INVALID_ARG;
+  if (n < 1) return MUON_ERR_INVALID_ARG;
+  if (!valid_dtype(pdt) || !valid_dtype(gdt)) return MUON_ERR_DTYPE;
+  if (hp->step < 1 || !std::isfinite(hp->lr) || !std::isfinite(hp->beta1) || !std::isfinite(hp->beta2) ||
+      !std::isfinite(hp->eps) || !std::isfinite(hp->weight_decay) || hp->beta1 < 0.f || hp->beta1 >= 1.f ||
+      hp->beta2 < 0.f || hp->beta2 >= 1.f)
+    return MUON_ERR_INVALID_ARG;
+  muon_status st = check_device();
+  if (st != MUON_OK) return st;
+  const double t = static_cast<double>(hp->step);
+  const double bc1 = 1.0 - std::pow(static_cast<double>(hp->beta1), t);
+  const double bc2 = 1.0 - std::pow(static_cast<double>(hp->beta2), t);
+  AdamwConst c{};
+  c.decay = static_cast<float>(1.0 - static_cast<double>(hp->lr) * hp->weight_decay);
+  c.beta1 = hp->beta1;
+  c.one_minus_beta1 = static_cast<float>(1.0 - hp->beta1);
+  c.beta2 = hp->beta2;
+  c.one_minus_beta2 = static_cast<float>(1.0 - hp->beta2);
+  c.step_size = static_cast<float>(hp->lr / bc1);
+  c.inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(bc2));
+  c.eps = hp->eps;
+  return launch_adamw(param, pdt, grad, gdt, exp_avg, exp_avg_sq, n, c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+static muon_status check_step_stack(const void *p, int64_t K, int64_t m, int64_t n) {
+  if (p == nullptr) return MUON_ERR_INVALID_ARG;
+  muon_status st = check_stack_dims(K, m, n);
+  if (st != MUON_OK) return st;
+  if (m % 8 != 0 || n % 8 != 0) return MUON_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(p) & 255) != 0) return MUON_ERR_ALIGNMENT;
+  return MUON_OK;
+}
+
+static muon_status check_ws_ctrl(void *ws, size_t ws_bytes) {
+  if (ws == nullptr) return MUON_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MUON_ERR_ALIGNMENT;
+  if (ws_bytes < CTRL_BYTES) return MUON_ERR_WORKSPACE;
+  return MUON_OK;
+}
+
+muon_status ns_gram(const void *x, void *g, int64_t K, int64_t m, int64_t n, float alpha, void *ws, size_t ws_bytes,
+                    muon_stream_t stream) {
+  muon_status st;
+  if ((st = check_step_stack(x, K, m, n)) != MUON_OK || (st = check_step_stack(g, K, m, m)) != MUON_OK ||
+      (st = check_ws_ctrl(ws, ws_bytes)) != MUON_OK)
+    return st;
+  if (!std::isfinite(alpha)) return MUON_ERR_INVALID_ARG;
+  if ((st = check_device()) != MUON_OK) return st;
+  Bf16Stack X{x, m, n, n, m * n, K};
+  return launch_gram(X, static_cast<__nv_bfloat16 *>(g), m, m * m, alpha, nullptr, static_cast<uint32_t *>(ws),
+                     g_timeout_ns, reinterpret_cast<cudaStream_t>(stream));
+}
+
+muon_status ns_poly(const void *g, void *h, int64_t K, int64_t m, float b, float c, void *ws, size_t ws_bytes,
+                    muon_stream_t stream) {
+  muon_status st;
+  if ((st = check_step_stack(g, K, m, m)) != MUON_OK || (st = check_step_stack(h, K, m, m)) != MUON_OK ||
+      (st = check_ws_ctrl(ws, ws_bytes)) != MUON_OK)
+    return st;
+  if (!std::isfinite(b) || !std::isfinite(c)) return MUON_ERR_INVALID_ARG;
+  if ((st = check_device()) != MUON_OK) return st;
+  Bf16Stack G{g, m, m, m, m * m, K};
+  return launch_poly(G, static_cast<__nv_bfloat16 *>(h), m, m * m, b, c, static_cast<uint32_t *>(ws), g_timeout_ns,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+muon_status ns_apply(const void *h, const void *x, void *out, int64_t K, int64_t m, int64_t n, float a, void *ws,
+                     size_t ws_bytes, muon_stream_t stream) {
+  muon_status st;
+  if ((st = check_step_stack(h, K, m, m)) != MUON_OK || (st = check_step_stack(x, K, m, n)) != MUON_OK ||
+      (st = check_step_stack(out, K, m, n)) != MUON_OK || (st = check_ws_ctrl(ws, ws_bytes)) != MUON_OK)
+    return st;
+  if (out == x) return MUON_ERR_INVALID_ARG;
+  if (!std::isfinite(a)) return MUON_ERR_INVALID_ARG;
+  if ((st = check_device()) != MUON_OK) return st;
+  Bf16Stack Hs{h, m, m, m, m * m, K};
+  Bf16Stack X{x, m, n, n, m * n, K};
+  // out has x's layout: launch_apply writes with x's pitches
+  return launch_apply(Hs, X, static_cast<__nv_bfloat16 *>(out), a, nullptr, static_cast<uint32_t *>(ws),
+                      g_timeout_ns, reinterpret_cast<cudaStream_t>(stream));
+}
+
+muon_status muon_plan_buckets(int64_t n, const int64_t *rows, const int64_t *cols, int64_t *bucket_id,
+                              int64_t *index_in_bucket, int64_t *n_buckets, int64_t *bucket_shapes, int64_t *bucket_K,
+                              int64_t *momentum_offset) {
+  if (n < 0 || n_buckets == nullptr) return MUON_ERR_INVALID_ARG;
+  if (n > 0 && (rows == nullptr || cols == nullptr || bucket_id == nullptr || index_in_bucket == nullptr ||
+                bucket_shapes == nullptr || bucket_K == nullptr || momentum_offset == nullptr))
+    return MUON_ERR_INVALID_ARG;
+  for (int64_t i = 0; i < n; ++i)
+    if (rows[i] < 1 || cols[i] < 1) return MUON_ERR_INVALID_ARG;
+  // exact (rows, cols) -> bucket; buckets numbered in order of first appearance
+  std::map<std::pair<int64_t, int64_t>, int64_t> seen;
+  int64_t nb = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const auto key = std::make_pair(rows[i], cols[i]);
+    auto it = seen.find(key);
+    int64_t b;
+    if (it == seen.end()) {
+      b = nb++;
+      seen.emplace(key, b);
+      bucket_shapes[2 * b] = rows[i];
+      bucket_shapes[2 * b + 1] = cols[i];
+      bucket_K[b] = 0;
+    } else {
+      b = it->second;
+    }
+    bucket_id[i] = b;
+    index_in_bucket[i] = bucket_K[b]++;
+  }
+  int64_t off = 0;
+  for (int64_t b = 0; b < nb; ++b) {
+    momentum_offset[b] = off;
+    off += bucket_K[b] * bucket_shapes[2 * b] * bucket_shapes[2 * b + 1];
+  }
+  *n_buckets = nb;
+  return MUON_OK;
+}
+
+muon_status muon_check(void *ws, muon_stream_t stream) {
+  if (ws == nullptr) return MUON_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MUON_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return MUON_ERR_CUDA;
+  if (word == 0) return MUON_OK;
+  const uint32_t zero = 0;
+  if (cudaMemcpy(ws, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return MUON_ERR_CUDA;
+  return MUON_ERR_TIMEOUT;
+}
+
+void muon_set_timeout_ns(uint64_t ns) { muon::g_timeout_ns = ns > 0 ? ns : 1; }
+
+muon_status muon_debug_wait_timeout(void *ws, size_t ws_bytes, uint64_t timeout_ns, muon_stream_t stream) {
+  muon_status st = check_ws_ctrl(ws, ws_bytes);
+  if (st != MUON_OK) return st;
+  if (timeout_ns == 0 || timeout_ns > 10000000000ull) return MUON_ERR_INVALID_ARG;
+  if ((st = check_device()) != MUON_OK) return st;
+  return launch_debug_wait(static_cast<uint32_t *>(ws), timeout_ns, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int64_t muon_launch_count(void) {
+  std::lock_guard<std::mutex> lk(muon::g_trace_mu);
+  return muon::g_launches;
+}
+
+void muon_trace_enable(int on) {
+  std::lock_guard<std::mutex> lk(muon::g_trace_mu);
+  muon::g_trace_on = on != 0;
+}
+
+int64_t muon_trace_collect(int32_t *kinds, float *ms, int64_t cap) {
+  std::lock_guard<std::mutex> lk(muon::g_trace_mu);
+  int64_t written = 0;
+  bool failed = false;
+  for (auto &r : muon::g_trace) {
+    if (cudaEventSynchronize(r.stop) != cudaSuccess) failed = true;
+    float t = 0.f;
+    if (!failed && cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess) failed = true;
+    if (written < cap && kinds != nullptr && ms != nullptr) {
+      kinds[written] = r.kind;
+      ms[written] = t;
+      ++written;
+    }
+    muon::g_event_pool.push_back(r.start);
+    muon::g_event_pool.push_back(r.stop);
+  }
+  muon::g_trace.clear();
+  return failed ? -1 : written;
+}
+
+const char *muon_kernel_name(int32_t kind) {
+  switch (kind) {
+    case KK_ADAMW: return "adamw";
+    case KK_NESTEROV_NORM: return "nesterov_norm";
+    case KK_NORM_FINALIZE: return "norm_finalize";
+    case KK_GRAM: return "ns_gram";
+    case KK_POLY: return "ns_poly";
+    case KK_APPLY: return "ns_apply";
+    case KK_FINAL: return "ns_final";
+    case KK_DEBUG_WAIT: return "debug_wait";
+    default: return "unknown";
+  }
+}
+
+const char *muon_status_string(muon_status s) {
+  switch (s) {
+    case MUON_OK: return "MUON_OK";
+    case MUON_ERR_INVALID_ARG: return "MUON_ERR_INVALID_ARG: null pointer, non-positive size or bad hyperparameter";
+    case MUON_ERR_SHAPE: return "MUON_ERR_SHAPE: dimension outside the supported range";
+    case MUON_ERR_DTYPE: return "MUON_ERR_DTYPE: unsupported dtype";
+    case MUON_ERR_ALIGNMENT: return "MUON_ERR_ALIGNMENT: pointer not aligned as required";
+    case MUON_ERR_WORKSPACE: return "MUON_ERR_WORKSPACE: workspace missing or too small";
+    case MUON_ERR_UNSUPPORTED_DEVICE: return "MUON_ERR_UNSUPPORTED_DEVICE: current device is not a GB300 (sm_103)";
+    case MUON_ERR_CUDA: return "MUON_ERR_CUDA: a CUDA call failed";
+    case MUON_ERR_TIMEOUT: return "MUON_ERR_TIMEOUT: a bounded device-side wait ran out";
+    default: return "unknown muon_status";
+  }
+}
+
+}  // extern "C"

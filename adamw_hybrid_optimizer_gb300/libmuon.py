@@ -1,0 +1,241 @@
+"""ctypes binding of libmuon (include/libmuon.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls. Tensors are passed as raw
+device pointers with their sizes and dtypes; the default stream is torch's current stream.
+No computation happens in Python. A missing or unloadable library raises ImportError:
+there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence, Tuple
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "lib", "libmuon.so")
+
+MUON_OK = 0
+MUON_ERR_INVALID_ARG = 1
+MUON_ERR_SHAPE = 2
+MUON_ERR_DTYPE = 3
+MUON_ERR_ALIGNMENT = 4
+MUON_ERR_WORKSPACE = 5
+MUON_ERR_UNSUPPORTED_DEVICE = 6
+MUON_ERR_CUDA = 7
+MUON_ERR_TIMEOUT = 8
+
+MUON_F32 = 0
+MUON_BF16 = 1
+MUON_MAX_NS_STEPS = 32
+
+# the C signatures, checked against include/libmuon.h by tests/test_abi.py
+_c_int64 = ctypes.c_int64
+_vp = ctypes.c_void_p
+
+
+class muon_hparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("momentum", ctypes.c_float), ("weight_decay", ctypes.c_float),
+                ("nesterov", ctypes.c_int), ("cautious_wd", ctypes.c_int), ("scale_mode", ctypes.c_int),
+                ("ns_steps", ctypes.c_int), ("coeffs", ctypes.POINTER(ctypes.c_float)), ("eps", ctypes.c_float)]
+
+
+class adamw_hparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("step", ctypes.c_int64)]
+
+
+SIGNATURES = {
+    "muon_workspace_bytes": (ctypes.c_size_t, [_c_int64, _c_int64, _c_int64]),
+    "muon_step_batched": (ctypes.c_int, [_vp, ctypes.c_int, _vp, ctypes.c_int, _vp, _c_int64, _c_int64, _c_int64,
+                                         ctypes.POINTER(muon_hparams), _vp, ctypes.c_size_t, _vp]),
+    "ns_orthogonalize": (ctypes.c_int, [_vp, ctypes.c_int, _vp, ctypes.c_int, _c_int64, _c_int64, _c_int64,
+                                        ctypes.c_int, ctypes.POINTER(ctypes.c_float), ctypes.c_float, _vp,
+                                        ctypes.c_size_t, _vp]),
+    "adamw_step": (ctypes.c_int, [_vp, ctypes.c_int, _vp, ctypes.c_int, _vp, _vp, _c_int64,
+                                  ctypes.POINTER(adamw_hparams), _vp]),
+    "ns_gram": (ctypes.c_int, [_vp, _vp, _c_int64, _c_int64, _c_int64, ctypes.c_float, _vp, ctypes.c_size_t, _vp]),
+    "ns_poly": (ctypes.c_int, [_vp, _vp, _c_int64, _c_int64, ctypes.c_float, ctypes.c_float, _vp, ctypes.c_size_t,
+                               _vp]),
+    "ns_apply": (ctypes.c_int, [_vp, _vp, _vp, _c_int64, _c_int64, _c_int64, ctypes.c_float, _vp, ctypes.c_size_t,
+                                _vp]),
+    "muon_plan_buckets": (ctypes.c_int, [_c_int64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "muon_check": (ctypes.c_int, [_vp, _vp]),
+    "muon_set_timeout_ns": (None, [ctypes.c_uint64]),
+    "muon_debug_wait_timeout": (ctypes.c_int, [_vp, ctypes.c_size_t, ctypes.c_uint64, _vp]),
+    "muon_launch_count": (ctypes.c_int64, []),
+    "muon_trace_enable": (None, [ctypes.c_int]),
+    "muon_trace_collect": (ctypes.c_int64, [_vp, _vp, _c_int64]),
+    "muon_kernel_name": (ctypes.c_char_p, [ctypes.c_int32]),
+    "muon_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libmuon.so (built by __graft_entry__.build() or adamw_hybrid_optimizer_gb300/_build.py)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libmuon.so is not built ({LIB_PATH}); run `python -c \"import __graft_entry__ as g; "
+                              f"g.build()\"` first. There is no fallback implementation.")
+        try:
+            handle = ctypes.CDLL(LIB_PATH)
+        except OSError as e:
+            raise ImportError(f"libmuon.so failed to load: {e}") from e
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+class MuonError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {muon_status_string(status)}")
+
+
+def muon_status_string(status: int) -> str:
+    return lib().muon_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != MUON_OK:
+        raise MuonError(status, where)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return MUON_F32
+    if t.dtype == torch.bfloat16:
+        return MUON_BF16
+    raise MuonError(MUON_ERR_DTYPE, f"dtype {t.dtype}")
+
+
+def _stream(stream) -> int:
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _coeff_array(coeffs: Sequence[Sequence[float]]):
+    flat = [float(v) for abc in coeffs for v in abc]
+    return (ctypes.c_float * len(flat))(*flat), len(flat) // 3
+
+
+def muon_workspace_bytes(K: int, A: int, B: int) -> int:
+    return int(lib().muon_workspace_bytes(K, A, B))
+
+
+def make_muon_hparams(lr, momentum, weight_decay, nesterov=True, cautious_wd=False, scale_mode=0,
+                      coeffs=((3.4445, -4.7750, 2.0315),) * 5, eps=1e-7):
+    arr, steps = _coeff_array(coeffs)
+    hp = muon_hparams(lr, momentum, weight_decay, int(bool(nesterov)), int(bool(cautious_wd)), int(scale_mode), steps,
+                      ctypes.cast(arr, ctypes.POINTER(ctypes.c_float)), eps)
+    hp._keep = arr  # the coefficient array lives as long as the struct
+    return hp
+
+
+def muon_step_batched(param_ptrs, pdt: int, grad_ptrs, gdt: int, momentum, K: int, A: int, B: int,
+                      hp: muon_hparams, ws, stream=None):
+    """param_ptrs / grad_ptrs: device int64 tensors of K data pointers (see pointer_array)."""
+    st = lib().muon_step_batched(param_ptrs.data_ptr(), pdt, grad_ptrs.data_ptr(), gdt, momentum.data_ptr(), K, A, B,
+                                 ctypes.byref(hp), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "muon_step_batched")
+
+
+def pointer_array(tensors, device):
+    """Device int64 tensor holding each tensor's data pointer (the K-pointer arrays muon_step_batched reads)."""
+    import torch
+    return torch.tensor([t.data_ptr() for t in tensors], dtype=torch.int64, device=device)
+
+
+def ns_orthogonalize(x, out, coeffs, eps: float, ws, stream=None):
+    """x, out: contiguous (K, A, B) float32 or bfloat16 device tensors."""
+    K, A, B = x.shape
+    arr, steps = _coeff_array(coeffs)
+    st = lib().ns_orthogonalize(x.data_ptr(), _dtype_code(x), out.data_ptr(), _dtype_code(out), K, A, B, steps,
+                                arr, eps, ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "ns_orthogonalize")
+
+
+def adamw_step(param, grad, exp_avg, exp_avg_sq, lr, beta1, beta2, eps, weight_decay, step: int, stream=None):
+    hp = adamw_hparams(lr, beta1, beta2, eps, weight_decay, int(step))
+    st = lib().adamw_step(param.data_ptr(), _dtype_code(param), grad.data_ptr(), _dtype_code(grad),
+                          exp_avg.data_ptr(), exp_avg_sq.data_ptr(), param.numel(), ctypes.byref(hp), _stream(stream))
+    _check(st, "adamw_step")
+
+
+def ns_gram(x, g, alpha: float, ws, stream=None):
+    K, m, n = x.shape
+    _check(lib().ns_gram(x.data_ptr(), g.data_ptr(), K, m, n, alpha, ws.data_ptr(), ws.numel() * ws.element_size(),
+                         _stream(stream)), "ns_gram")
+
+
+def ns_poly(g, h, b: float, c: float, ws, stream=None):
+    K, m, _ = g.shape
+    _check(lib().ns_poly(g.data_ptr(), h.data_ptr(), K, m, b, c, ws.data_ptr(), ws.numel() * ws.element_size(),
+                         _stream(stream)), "ns_poly")
+
+
+def ns_apply(h, x, out, a: float, ws, stream=None):
+    K, m, n = x.shape
+    _check(lib().ns_apply(h.data_ptr(), x.data_ptr(), out.data_ptr(), K, m, n, a, ws.data_ptr(),
+                          ws.numel() * ws.element_size(), _stream(stream)), "ns_apply")
+
+
+def muon_plan_buckets(shapes: Sequence[Tuple[int, int]]):
+    n = len(shapes)
+    L = ctypes.c_int64 * max(n, 1)
+    rows = L(*[int(s[0]) for s in shapes])
+    cols = L(*[int(s[1]) for s in shapes])
+    bid, idx, K, off = L(), L(), L(), L()
+    shp = (ctypes.c_int64 * max(2 * n, 2))()
+    nb = ctypes.c_int64(0)
+    _check(lib().muon_plan_buckets(n, rows, cols, bid, idx, ctypes.byref(nb), shp, K, off), "muon_plan_buckets")
+    b = nb.value
+    return {
+        "bucket_id": list(bid)[:n],
+        "index_in_bucket": list(idx)[:n],
+        "bucket_shapes": [(shp[2 * i], shp[2 * i + 1]) for i in range(b)],
+        "bucket_K": list(K)[:b],
+        "momentum_offset": list(off)[:b],
+    }
+
+
+def muon_check(ws, stream=None) -> int:
+    return int(lib().muon_check(ws.data_ptr(), _stream(stream)))
+
+
+def muon_set_timeout_ns(ns: int):
+    lib().muon_set_timeout_ns(int(ns))
+
+
+def muon_debug_wait_timeout(ws, timeout_ns: int, stream=None):
+    _check(lib().muon_debug_wait_timeout(ws.data_ptr(), ws.numel() * ws.element_size(), int(timeout_ns),
+                                         _stream(stream)), "muon_debug_wait_timeout")
+
+
+def muon_launch_count() -> int:
+    return int(lib().muon_launch_count())
+
+
+def muon_trace_enable(on: bool):
+    lib().muon_trace_enable(int(bool(on)))
+
+
+def muon_trace_collect(cap: int = 65536):
+    kinds = (ctypes.c_int32 * cap)()
+    ms = (ctypes.c_float * cap)()
+    n = int(lib().muon_trace_collect(kinds, ms, cap))
+    if n < 0:
+        raise MuonError(MUON_ERR_CUDA, "muon_trace_collect")
+    return [(muon_kernel_name(kinds[i]), float(ms[i])) for i in range(n)]
+
+
+def muon_kernel_name(kind: int) -> str:
+    return lib().muon_kernel_name(int(kind)).decode()

@@ -1,0 +1,147 @@
+"""HybridMuonAdamW: one optimizer for Muon (2-D hidden matrices) and AdamW (everything else).
+
+The user-facing form of the pages' optimizer: ``Opt(param_groups).step()`` with groups tagged
+``"kind": "muon"`` or ``"kind": "adamw"`` ("MuonAdamW vs DistMuonAdamW", sections "Usage
+Examples" and "Do both optimizers support identical hyperparameters?"; "dtensor-muon 0.1.0",
+sections "Usage" and "Key options"). Routing follows "Optimizers: AdamW, Muon and the distributed
+optimizer" (Muon on hidden-layer matrices; embedding, output layer and vectors on AdamW): the
+caller decides by the group's kind, and a Muon group must hold 2-D tensors only.
+
+Muon matrices of one group are bucketed by shape (muon_plan_buckets); each bucket owns one fp32
+(K, A, B) momentum stack and one muon_step_batched call per step. AdamW state is one fp32
+exp_avg / exp_avg_sq pair per tensor and the group's step count. All arithmetic runs in libmuon.
+"""
+from __future__ import annotations
+
+from typing import Dict, List, Sequence
+
+import torch
+
+from . import libmuon as L
+
+CLASSIC = (3.4445, -4.7750, 2.0315)
+
+MUON_DEFAULTS = dict(lr=0.02, momentum=0.95, weight_decay=0.01, nesterov=True, cautious_wd=False, scale_mode=0,
+                     ns_steps=5, ns_coefficients=None, eps=1e-7)
+ADAMW_DEFAULTS = dict(lr=3e-4, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1)
+
+
+class _Bucket:
+    def __init__(self, params: List[torch.Tensor], shape, device):
+        self.params = params
+        self.K = len(params)
+        self.A, self.B = shape
+        self.momentum = torch.zeros((self.K, self.A, self.B), dtype=torch.float32, device=device)
+        self.param_ptrs = L.pointer_array(params, device)
+        self.grad_ptrs = None
+        self._grad_key = None
+
+    def refresh_grads(self, device):
+        grads = [p.grad for p in self.params]
+        key = tuple(g.data_ptr() for g in grads)
+        if key != self._grad_key:
+            self.grad_ptrs = L.pointer_array(grads, device)
+            self._grad_key = key
+        return grads
+
+
+class HybridMuonAdamW:
+    def __init__(self, param_groups: Sequence[Dict]):
+        self.param_groups = []
+        self.state: Dict[torch.Tensor, Dict] = {}
+        self._buckets: List[List[_Bucket]] = []
+        ws_bytes = 0
+        device = None
+        for g in param_groups:
+            kind = g.get("kind", "muon")
+            defaults = MUON_DEFAULTS if kind == "muon" else ADAMW_DEFAULTS
+            if kind not in ("muon", "adamw"):
+                raise ValueError(f"unknown kind {kind!r}")
+            group = dict(defaults)
+            group.update(g)
+            group["kind"] = kind
+            group["params"] = list(g["params"])
+            for p in group["params"]:
+                if not p.is_cuda:
+                    raise ValueError("HybridMuonAdamW runs on the GPU only: parameters must be CUDA tensors")
+                device = p.device
+            buckets = []
+            if kind == "muon":
+                if group["ns_coefficients"] is None:
+                    group["ns_coefficients"] = [CLASSIC] * int(group["ns_steps"])
+                group["ns_steps"] = len(group["ns_coefficients"])
+                for p in group["params"]:
+                    if p.dim() != 2:
+                        raise ValueError("a Muon group holds 2-D matrices only; route vectors to an AdamW group")
+                plan = L.muon_plan_buckets([tuple(p.shape) for p in group["params"]])
+                members = [[] for _ in plan["bucket_K"]]
+                for p, b in zip(group["params"], plan["bucket_id"]):
+                    members[b].append(p)
+                for shape, ps in zip(plan["bucket_shapes"], members):
+                    bk = _Bucket(ps, shape, device)
+                    buckets.append(bk)
+                    ws_bytes = max(ws_bytes, L.muon_workspace_bytes(bk.K, bk.A, bk.B))
+                    for k, p in enumerate(ps):
+                        self.state[p] = {"momentum_buffer": bk.momentum[k]}
+            else:
+                group["step"] = 0
+                for p in group["params"]:
+                    self.state[p] = {"exp_avg": torch.zeros(p.shape, dtype=torch.float32, device=p.device),
+                                     "exp_avg_sq": torch.zeros(p.shape, dtype=torch.float32, device=p.device)}
+            self.param_groups.append(group)
+            self._buckets.append(buckets)
+        self._ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device) if device is not None else None
+
+    @torch.no_grad()
+    def step(self):
+        for group, buckets in zip(self.param_groups, self._buckets):
+            if group["kind"] == "muon":
+                hp = L.make_muon_hparams(group["lr"], group["momentum"], group["weight_decay"], group["nesterov"],
+                                         group["cautious_wd"], group["scale_mode"], group["ns_coefficients"],
+                                         group["eps"])
+                for bk in buckets:
+                    if any(p.grad is None for p in bk.params):
+                        continue
+                    grads = bk.refresh_grads(self._ws.device)
+                    pdt = L._dtype_code(bk.params[0])
+                    gdt = L._dtype_code(grads[0])
+                    for p, gr in zip(bk.params, grads):
+                        if L._dtype_code(p) != pdt or L._dtype_code(gr) != gdt or not p.is_contiguous() \
+                                or not gr.is_contiguous():
+                            raise ValueError("a Muon bucket needs contiguous tensors of one dtype")
+                    L.muon_step_batched(bk.param_ptrs, pdt, bk.grad_ptrs, gdt, bk.momentum, bk.K, bk.A, bk.B, hp,
+                                        self._ws)
+            else:
+                group["step"] += 1
+                b1, b2 = group["betas"]
+                for p in group["params"]:
+                    if p.grad is None:
+                        continue
+                    st = self.state[p]
+                    L.adamw_step(p, p.grad, st["exp_avg"], st["exp_avg_sq"], group["lr"], b1, b2, group["eps"],
+                                 group["weight_decay"], group["step"])
+
+    def zero_grad(self, set_to_none: bool = True):
+        for group in self.param_groups:
+            for p in group["params"]:
+                if p.grad is not None:
+                    if set_to_none:
+                        p.grad = None
+                    else:
+                        p.grad.zero_()
+
+    def state_dict(self):
+        flat = [p for g in self.param_groups for p in g["params"]]
+        return {
+            "state": {i: {k: v.clone() for k, v in self.state[p].items()} for i, p in enumerate(flat)},
+            "steps": [g.get("step", 0) for g in self.param_groups],
+        }
+
+    def load_state_dict(self, sd):
+        flat = [p for g in self.param_groups for p in g["params"]]
+        for i, p in enumerate(flat):
+            for k, v in sd["state"][i].items():
+                self.state[p][k].copy_(v)
+        for g, s in zip(self.param_groups, sd["steps"]):
+            if g["kind"] == "adamw":
+                g["step"] = s

@@ -1,0 +1,174 @@
+/*
+ * libmuon -- the hybrid Muon + AdamW optimizer step on one NVIDIA GB300 (sm_103a).
+ *
+ * C ABI. Plain pointers and sizes; no C++ or framework types cross it.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [P1] "MuonAdamW vs DistMuonAdamW: Key Differences for Single and Multi-GPU Training in nanochat"
+ *   [P2] "Optimizers: AdamW, Muon and the distributed optimizer" (AI-infra handbook)
+ *   [P3] "dtensor-muon 0.1.0" package description
+ *   [P4] "DMuon: Efficient Distributed Muon Training with Near-Adam Overhead" (summary of arXiv 2606.27153)
+ *
+ * Conventions for every call:
+ *   - Matrices are row-major. A stack (K, A, B) is K matrices of A rows and B columns.
+ *   - The caller allocates every buffer: parameters, gradients, optimizer state and the
+ *     workspace. The library never allocates or frees device memory and keeps no pointer
+ *     after a call returns.
+ *   - Device work is enqueued on the caller's stream and is asynchronous: a call returns
+ *     once its kernels are launched. Updates are in place.
+ *   - Argument checks (null pointers, sizes, dtypes, alignment, workspace size, device
+ *     capability) run on the host before anything is launched; a failed check launches
+ *     nothing and changes nothing. A failed launch returns MUON_ERR_CUDA.
+ *   - Every wait inside a kernel is bounded (default 2 s, muon_set_timeout_ns). A wait
+ *     that runs out sets an error word in the workspace and the kernel returns early;
+ *     muon_check() reports it as MUON_ERR_TIMEOUT.
+ *   - Calls on one stream are ordered. Calls on different streams that share a workspace,
+ *     or that touch the same parameters, race.
+ */
+#ifndef LIBMUON_H
+#define LIBMUON_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA stream type (cudaStream_t). NULL is the legacy default stream. */
+typedef struct CUstream_st *muon_stream_t;
+
+typedef enum {
+  MUON_OK = 0,
+  MUON_ERR_INVALID_ARG = 1,        /* null pointer, non-positive size, bad hyperparameter */
+  MUON_ERR_SHAPE = 2,              /* a dimension beyond what the kernels index */
+  MUON_ERR_DTYPE = 3,              /* unsupported dtype or dtype combination */
+  MUON_ERR_ALIGNMENT = 4,          /* a pointer not aligned as the call states */
+  MUON_ERR_WORKSPACE = 5,          /* workspace missing or smaller than muon_workspace_bytes() */
+  MUON_ERR_UNSUPPORTED_DEVICE = 6, /* current device is not compute capability 10.3 (GB300) */
+  MUON_ERR_CUDA = 7,               /* a CUDA runtime/driver call failed */
+  MUON_ERR_TIMEOUT = 8             /* a bounded device-side wait ran out (reported by muon_check) */
+} muon_status;
+
+typedef enum { MUON_F32 = 0, MUON_BF16 = 1 } muon_dtype;
+
+#define MUON_MAX_NS_STEPS 32
+
+/* Muon hyperparameters ([P2] "Muon: orthogonalising the update"; [P3] "Key options"). */
+typedef struct {
+  float lr;            /* eta */
+  float momentum;      /* mu: M <- mu*M + G */
+  float weight_decay;  /* lambda: decoupled decay p <- p - eta*lambda*p (masked if cautious) */
+  int nesterov;        /* 1: orthogonalise G + mu*M (updated M); 0: orthogonalise M */
+  int cautious_wd;     /* 1: decay only where u*p > 0 (u: orthogonalised update, p: pre-update param) */
+  int scale_mode;      /* 0: update scale 0.2*sqrt(max(A,B)); 1: sqrt(max(1, A/B)) */
+  int ns_steps;        /* N, 1..MUON_MAX_NS_STEPS */
+  const float *coeffs; /* HOST array, ns_steps*3 floats: (a_t, b_t, c_t) for step t */
+  float eps;           /* added to the Frobenius norm before dividing, 1e-7 on the pages */
+} muon_hparams;
+
+/* AdamW hyperparameters ([P2] "AdamW: decoupled weight decay"). */
+typedef struct {
+  float lr, beta1, beta2, eps, weight_decay;
+  int64_t step; /* t >= 1, the step count after this update; kept by the caller */
+} adamw_hparams;
+
+/* Bytes of workspace muon_step_batched / ns_orthogonalize need for a (K, A, B) stack.
+ * Layout (all offsets 1024-byte aligned): a 256-byte control block (error word), K fp32
+ * norm scales, per-tile norm partial sums, two bf16 iterates of (K, min, max) with rows
+ * padded to a multiple of 8 elements, and two bf16 (K, min, min) Gram buffers.
+ * Returns 0 if K, A or B is not positive. */
+size_t muon_workspace_bytes(int64_t K, int64_t A, int64_t B);
+
+/* One Muon step on a stack of K same-shape matrices.
+ * [P2] "Muon: orthogonalising the update": M <- mu*M + G; U = G + mu*M (nesterov) or M;
+ * X = U / (||U||_F + eps) per matrix; if A > B work on X^T; N steps of
+ * X <- a_t X + (b_t X X^T + c_t (X X^T)^2) X; transpose back; then
+ * p <- p - lr*wd*p*mask - lr*scale*X with mask = 1, or [X*p > 0] if cautious ([P3] "Features").
+ *   params    DEVICE array of K device pointers; each points to an A x B row-major matrix of pdt.
+ *   grads     DEVICE array of K device pointers; each an A x B row-major matrix of gdt.
+ *   momentum  device, fp32, contiguous (K, A, B); updated in place. Zero before the first step.
+ *   pdt, gdt  MUON_F32 or MUON_BF16 each.
+ *   hp        host struct; hp->coeffs host array of 3*ns_steps floats.
+ *   ws        device workspace of ws_bytes >= muon_workspace_bytes(K, A, B), 256-byte aligned.
+ * Limits: 1 <= A, B <= 65536; K * max(A,B) * min(A,B) < 2^40. */
+muon_status muon_step_batched(void *const *params, muon_dtype pdt, const void *const *grads, muon_dtype gdt,
+                              float *momentum, int64_t K, int64_t A, int64_t B, const muon_hparams *hp, void *ws,
+                              size_t ws_bytes, muon_stream_t stream);
+
+/* Newton-Schulz orthogonalisation of a stack, [P2] "Muon: orthogonalising the update" (newton_schulz):
+ * out_k = NS(x_k) for k < K, with normalisation by ||x_k||_F + eps and transpose-to-wide.
+ *   x    device, contiguous (K, A, B) of xdt (MUON_F32 or MUON_BF16).
+ *   out  device, contiguous (K, A, B) of odt (MUON_F32 or MUON_BF16); may not alias x.
+ *   coeffs HOST array of 3*ns_steps floats. ws as for muon_step_batched. */
+muon_status ns_orthogonalize(const void *x, muon_dtype xdt, void *out, muon_dtype odt, int64_t K, int64_t A,
+                             int64_t B, int ns_steps, const float *coeffs, float eps, void *ws, size_t ws_bytes,
+                             muon_stream_t stream);
+
+/* One AdamW step on n elements, [P2] "AdamW: decoupled weight decay":
+ * p <- p*(1 - lr*wd); m <- b1*m + (1-b1)*g; v <- b2*v + (1-b2)*g^2;
+ * p <- p - lr * (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps).
+ *   param, grad  device, n elements of pdt / gdt (MUON_F32 or MUON_BF16 each).
+ *   exp_avg, exp_avg_sq  device fp32, n elements each; zero before the first step.
+ * Any alignment works; 16-byte aligned pointers take the vectorised path. */
+muon_status adamw_step(void *param, muon_dtype pdt, const void *grad, muon_dtype gdt, float *exp_avg,
+                       float *exp_avg_sq, int64_t n, const adamw_hparams *hp, muon_stream_t stream);
+
+/* The three tensor-core steps of one Newton-Schulz iteration on contiguous bf16 stacks, exposed
+ * one by one ([P2] newton_schulz loop body; [P4] section 2.2 symmetric Gram):
+ *   ns_gram:  g = alpha * x x^T,         x (K, m, n), g (K, m, m); symmetric, both halves written.
+ *   ns_poly:  h = b*g + c*g g,           g, h (K, m, m); g must be symmetric.
+ *   ns_apply: out = a*x + h x,           h (K, m, m), x and out (K, m, n); out may not alias x.
+ * All rows must be 16-byte aligned (m and n multiples of 8), pointers 256-byte aligned.
+ * ws: any workspace of at least 256 bytes (only the control block is used). */
+muon_status ns_gram(const void *x, void *g, int64_t K, int64_t m, int64_t n, float alpha, void *ws, size_t ws_bytes,
+                    muon_stream_t stream);
+muon_status ns_poly(const void *g, void *h, int64_t K, int64_t m, float b, float c, void *ws, size_t ws_bytes,
+                    muon_stream_t stream);
+muon_status ns_apply(const void *h, const void *x, void *out, int64_t K, int64_t m, int64_t n, float a, void *ws,
+                     size_t ws_bytes, muon_stream_t stream);
+
+/* Shape bucketing, host only ([P1] "Parameter Processing and Padding": stacking into (K, ...);
+ * [P4] section 2.2 "Batching"). Groups n matrices by exact (rows, cols), buckets numbered in
+ * order of first appearance; members keep their order.
+ *   rows, cols        host arrays of n.
+ *   bucket_id, index_in_bucket   host outputs of n.
+ *   n_buckets         host output.
+ *   bucket_shapes     host output of 2*n (rows, cols per bucket; first 2*n_buckets used).
+ *   bucket_K          host output of n (first n_buckets used).
+ *   momentum_offset   host output of n: element offset of each bucket's fp32 (K, A, B) momentum
+ *                     block in one concatenated buffer (running sum of K*A*B).
+ * Returns MUON_ERR_INVALID_ARG for a null pointer with n > 0 or a non-positive dimension. */
+muon_status muon_plan_buckets(int64_t n, const int64_t *rows, const int64_t *cols, int64_t *bucket_id,
+                              int64_t *index_in_bucket, int64_t *n_buckets, int64_t *bucket_shapes, int64_t *bucket_K,
+                              int64_t *momentum_offset);
+
+/* Synchronises the stream, then reads and clears the workspace's error word.
+ * Returns MUON_ERR_TIMEOUT if a bounded wait ran out since the last check, else MUON_OK. */
+muon_status muon_check(void *ws, muon_stream_t stream);
+
+/* Per-wait limit for device-side waits, in nanoseconds (default 2e9). Applies to later launches. */
+void muon_set_timeout_ns(uint64_t ns);
+
+/* Launches one kernel that waits on a barrier nothing will complete, with the given limit,
+ * so that the bounded-wait path can be exercised: afterwards muon_check returns MUON_ERR_TIMEOUT. */
+muon_status muon_debug_wait_timeout(void *ws, size_t ws_bytes, uint64_t timeout_ns, muon_stream_t stream);
+
+/* Number of kernels this library has launched since it was loaded. */
+int64_t muon_launch_count(void);
+
+/* Kernel timing with CUDA events. While enabled, every launch is bracketed by an event pair
+ * on its stream (up to 65536 pairs). muon_trace_collect synchronises on the events recorded so far,
+ * writes up to cap (kind, milliseconds) pairs and clears the record; it returns the number written,
+ * or -1 on a CUDA error. Kinds: see muon_kernel_name. */
+void muon_trace_enable(int on);
+int64_t muon_trace_collect(int32_t *kinds, float *ms, int64_t cap);
+const char *muon_kernel_name(int32_t kind);
+
+const char *muon_status_string(muon_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBMUON_H */

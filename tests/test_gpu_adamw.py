@@ -1,0 +1,84 @@
+"""GPU parity of adamw_step against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import adamw as oadamw
+from tests.gpu_common import DEV, bf16_ulp, build_lib, f64
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def L():
+    return build_lib()
+
+
+def _run(L, p, g_list, hp, wd, sample=None, pdt="f32"):
+    """Runs len(g_list) AdamW steps on the GPU and the oracle; compares p, m, v on `sample` indices."""
+    n = p.numel()
+    idx = np.arange(n) if sample is None else sample
+    m = torch.zeros(n, dtype=torch.float32, device=DEV)
+    v = torch.zeros(n, dtype=torch.float32, device=DEV)
+    po, mo, vo = f64(p)[idx], np.zeros(len(idx)), np.zeros(len(idx))
+    for t, g in enumerate(g_list, start=1):
+        L.adamw_step(p, g, m, v, hp.lr, hp.beta1, hp.beta2, hp.eps, wd, t)
+        po_prev, mo_prev = po, mo
+        po, mo, vo = oadamw.adamw_update(po, f64(g)[idx], mo, vo, t, lr=hp.lr, beta1=hp.beta1, beta2=hp.beta2,
+                                         eps=hp.eps, weight_decay=wd, param_dtype=pdt)
+        torch.cuda.synchronize()
+        got_p, got_m, got_v = f64(p)[idx], f64(m)[idx], f64(v)[idx]
+        if pdt == "f32":
+            scale = np.abs(po_prev) + hp.lr * (1 + 1e-3)
+            assert np.max(np.abs(got_p - po) / scale) <= 1e-6, t
+        else:
+            # independent trajectories: each bf16 store may round the other way once
+            terms = np.abs(po_prev) + hp.lr * (1 + 1e-3)
+            assert np.all(np.abs(got_p - po) <= t * bf16_ulp(po) * 1.0001 + 1e-6 * terms), t
+        gi = f64(g)[idx]
+        assert np.all(np.abs(got_m - mo) <= 1e-6 * (hp.beta1 * np.abs(mo_prev) + np.abs(gi)) + 1e-30)
+        assert np.all(np.abs(got_v - vo) <= 1e-6 * (np.abs(vo) + gi * gi) + 1e-30)
+
+
+def test_tiny_vector_three_steps(L):
+    w = workloads.workload("tiny")
+    p = workloads.adamw_param_init(w, 0).to(DEV)
+    gs = [workloads.adamw_grad(w, t, 0).to(DEV) for t in range(1, w.steps + 1)]
+    _run(L, p, gs, w.adamw_hp, w.adamw[0].weight_decay)
+
+
+@pytest.mark.parametrize("n,offset", [(8195, 0), (8195, 1), (7, 0), (1, 0), (100_003, 3)])
+def test_ragged_and_misaligned(L, n, offset):
+    g0 = torch.Generator().manual_seed(n + offset)
+    base_p = torch.randn(n + offset, generator=g0).to(DEV)
+    base_g = torch.randn(n + offset, generator=g0).to(DEV)
+    p, g = base_p[offset:], base_g[offset:]
+    hp = workloads.workload("tiny").adamw_hp
+    _run(L, p, [g, g * 0.5, -g], hp, 0.1)
+
+
+def test_mixed_dtypes(L):
+    hp = workloads.workload("tiny").adamw_hp
+    g0 = torch.Generator().manual_seed(3)
+    p = torch.randn(4099, generator=g0).to(DEV)
+    g = torch.randn(4099, generator=g0).to(torch.bfloat16).to(DEV)
+    _run(L, p, [g, g], hp, 0.1)
+
+
+def test_gpt2_embedding_bf16_full_size_sampled(L):
+    """The 50304 x 768 bf16 embedding at full size, 3 steps; the oracle checks a seeded sample and the tail."""
+    w = workloads.workload("gpt2s")
+    p = workloads.adamw_param_init(w, 0).to(DEV)
+    gs = [workloads.adamw_grad(w, t, 0).to(DEV) for t in range(1, 4)]
+    n = p.numel()
+    rng = np.random.default_rng(0)
+    sample = np.unique(np.concatenate([rng.integers(0, n, 200_000), np.arange(n - 1000, n), np.arange(1000)]))
+    _run(L, p, gs, w.adamw_hp, 0.1, sample=sample, pdt="bf16")
+
+
+def test_layernorm_vectors_no_decay_bf16(L):
+    w = workloads.workload("gpt2s")
+    p = workloads.adamw_param_init(w, 5).to(DEV)
+    gs = [workloads.adamw_grad(w, t, 5).to(DEV) for t in range(1, 4)]
+    _run(L, p, gs, w.adamw_hp, 0.0, pdt="bf16")

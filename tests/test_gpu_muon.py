@@ -1,0 +1,201 @@
+"""GPU parity of ns_orthogonalize and muon_step_batched against the fp64 oracle, through the C ABI.
+
+Inputs come from workloads (seeded); the oracle runs on the same rounded values and its own state
+trajectory. Bar: relative Frobenius error <= 2e-2 for the orthogonalised output and for the
+parameter change; momentum within 1e-6 of its terms' magnitude; bf16 parameters additionally allowed
+their storage rounding (2^-8 of their norm).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import muon as omuon
+from oracle.bf16 import round_to
+from tests.gpu_common import DEV, build_lib, f64, hp_struct, rel_fro, workspace
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+CLASSIC5 = [omuon.CLASSIC] * 5
+
+
+@pytest.fixture(scope="module")
+def L():
+    return build_lib()
+
+
+# ---------------------------------------------------------------------------------------- ns_orthogonalize
+
+@pytest.mark.parametrize("K,A,B,xdt,odt", [
+    (4, 64, 128, torch.float32, torch.float32),
+    (4, 128, 64, torch.float32, torch.float32),       # tall: transpose-to-wide and back
+    (3, 200, 72, torch.bfloat16, torch.float32),      # ragged tiles, tall
+    (2, 72, 200, torch.bfloat16, torch.bfloat16),
+    (2, 1, 40, torch.float32, torch.float32),         # one row
+    (2, 40, 1, torch.float32, torch.float32),         # one column
+    (2, 96, 96, torch.bfloat16, torch.float32),       # square: not transposed
+    (3, 768, 3072, torch.bfloat16, torch.float32),
+])
+def test_ns_orthogonalize_matches_oracle(L, K, A, B, xdt, odt):
+    g = torch.Generator().manual_seed(K * 1000 + A + B)
+    x = torch.randn((K, A, B), generator=g, dtype=torch.float64).to(xdt).to(DEV)
+    out = torch.full((K, A, B), float("nan"), dtype=odt, device=DEV)
+    ws = workspace(L, K, A, B)
+    L.ns_orthogonalize(x, out, CLASSIC5, 1e-7, ws)
+    assert L.muon_check(ws) == L.MUON_OK
+    X = f64(x)
+    got = f64(out)
+    for k in range(K):
+        ref = omuon.newton_schulz(X[k], CLASSIC5, 1e-7)
+        assert rel_fro(got[k], ref) <= 2e-2, k
+
+
+def test_ns_orthogonalize_transpose_symmetry(L):
+    g = torch.Generator().manual_seed(9)
+    x = torch.randn((3, 96, 160), generator=g).to(torch.bfloat16).to(DEV)
+    xt = x.transpose(1, 2).contiguous()
+    o = torch.empty((3, 96, 160), dtype=torch.float32, device=DEV)
+    ot = torch.empty((3, 160, 96), dtype=torch.float32, device=DEV)
+    ws = workspace(L, 3, 96, 160)
+    L.ns_orthogonalize(x, o, CLASSIC5, 1e-7, ws)
+    L.ns_orthogonalize(xt, ot, CLASSIC5, 1e-7, ws)
+    assert L.muon_check(ws) == L.MUON_OK
+    assert torch.equal(o, ot.transpose(1, 2))        # the same wide iterate, bit for bit
+
+
+def test_ns_orthogonalize_zero_matrix(L):
+    x = torch.zeros((2, 64, 128), dtype=torch.float32, device=DEV)
+    out = torch.full((2, 64, 128), 7.0, dtype=torch.float32, device=DEV)
+    ws = workspace(L, 2, 64, 128)
+    L.ns_orthogonalize(x, out, CLASSIC5, 1e-7, ws)
+    assert L.muon_check(ws) == L.MUON_OK
+    assert torch.count_nonzero(out) == 0
+
+
+@pytest.mark.parametrize("n", [512, 1024])
+def test_ns_sweep_small_sizes_sampled(L, n):
+    """Square bf16 stacks, K = 64, 5 classic steps; the oracle checks the first, last and one seeded matrix."""
+    K = workloads.NS_SWEEP_K
+    x = workloads.ns_sweep_input(n, K, 0).to(DEV)
+    out = torch.empty((K, n, n), dtype=torch.bfloat16, device=DEV)
+    ws = workspace(L, K, n, n)
+    L.ns_orthogonalize(x, out, CLASSIC5, 1e-7, ws)
+    assert L.muon_check(ws) == L.MUON_OK
+    for k in workloads.bucket_sample(K, 4, n):
+        ref = omuon.newton_schulz(f64(x[k]), CLASSIC5, 1e-7)
+        assert rel_fro(f64(out[k]), ref) <= 2e-2
+
+
+# ---------------------------------------------------------------------------------------- muon_step_batched
+
+def _run_bucket(L, w, shape, members, steps, sample=None, hp=None):
+    """Runs muon_step_batched on one (K, A, B) bucket for `steps` steps and the oracle on `sample`."""
+    hp = hp or w.muon_hp
+    A, B = shape
+    K = len(members)
+    pdt = "f32" if w.muon_dtype == "f32" else "bf16"
+    tdt = torch.float32 if pdt == "f32" else torch.bfloat16
+    params = [workloads.muon_param_init(w, i).to(DEV) for i in members]
+    p_orc = {k: f64(params[k]) for k in (sample or range(K))}
+    m_orc = {k: np.zeros((A, B)) for k in p_orc}
+    p_first = {k: v.copy() for k, v in p_orc.items()}
+    mom = torch.zeros((K, A, B), dtype=torch.float32, device=DEV)
+    ws = workspace(L, K, A, B)
+    pptr = L.pointer_array(params, DEV)
+    hps = hp_struct(L, hp)
+    code = L.MUON_F32 if pdt == "f32" else L.MUON_BF16
+    for step in range(1, steps + 1):
+        grads = [workloads.muon_grad(w, step, i).to(DEV) for i in members]
+        mom_before = {k: f64(mom[k]) for k in p_orc}
+        L.muon_step_batched(pptr, code, L.pointer_array(grads, DEV), code, mom, K, A, B, hps, ws)
+        assert L.muon_check(ws) == L.MUON_OK
+        for k in p_orc:
+            g = f64(grads[k])
+            p_prev = p_orc[k]
+            p_new, m_new, u = omuon.muon_update(p_prev, g, m_orc[k], lr=hp.lr, momentum=hp.momentum,
+                                                weight_decay=hp.weight_decay, nesterov=hp.nesterov,
+                                                cautious_wd=hp.cautious_wd, coeffs=hp.coeffs, eps=hp.eps,
+                                                scale_mode=hp.scale_mode, param_dtype=pdt)
+            p_orc[k], m_orc[k] = p_new, m_new
+            expect = p_new
+            if hp.cautious_wd:
+                # the decay mask [u*p > 0] is a decision taken on a floating-point u; where |u| is within the
+                # bf16 iteration's error of zero, either decision is correct: take the one the GPU took there
+                ambiguous = np.abs(u) <= 0.1 * np.sqrt(np.mean(u * u))
+                scale = omuon.update_scale(A, B, hp.scale_mode)
+                with_decay = round_to(p_prev - hp.lr * hp.weight_decay * p_prev - hp.lr * scale * u, pdt)
+                without = round_to(p_prev - hp.lr * scale * u, pdt)
+                got_now = f64(params[k])
+                pick = np.where(np.abs(got_now - with_decay) <= np.abs(got_now - without), with_decay, without)
+                expect = np.where(ambiguous, pick, p_new)
+                # outside the ambiguous band the mask is the oracle's
+                assert np.mean(ambiguous) < 0.15
+            got_m = f64(mom[k])
+            terms = np.abs(hp.momentum * mom_before[k]) + np.abs(g)
+            assert np.all(np.abs(got_m - m_new) <= 1e-6 * terms + 1e-30), (step, k)
+            got_p = f64(params[k])
+            moved = np.linalg.norm(p_new - p_first[k])
+            bound = 2e-2 * moved + (2.0 ** -8 * np.linalg.norm(p_new) if pdt == "bf16" else 0.0)
+            assert np.linalg.norm(got_p - expect) <= bound, (step, k, np.linalg.norm(got_p - expect), bound)
+    return params
+
+
+def test_tiny_set_three_steps(L):
+    """4 x (64 x 128) fp32, Nesterov 0.95, lr 0.02, wd 0.01, classic quintic, 3 optimizer steps; every matrix."""
+    w = workloads.workload("tiny")
+    _run_bucket(L, w, (64, 128), list(range(4)), w.steps)
+
+
+@pytest.mark.parametrize("variant", ["no_nesterov", "cautious_big_wd", "scale_mode_1", "tall"])
+def test_step_variants(L, variant):
+    import dataclasses
+    w = workloads.workload("tiny")
+    hp = w.muon_hp
+    shape = (64, 128)
+    if variant == "no_nesterov":
+        hp = dataclasses.replace(hp, nesterov=False)
+    elif variant == "cautious_big_wd":
+        # lr*wd = 0.1 makes the mask visible; one step, since a mask decided the other way on an ambiguous
+        # element moves the independent trajectories apart by 10% of that element
+        hp = dataclasses.replace(hp, cautious_wd=True, weight_decay=5.0)
+        _run_bucket(L, w, shape, list(range(4)), 1, hp=hp)
+        return
+    elif variant == "scale_mode_1":
+        hp = dataclasses.replace(hp, scale_mode=1)
+    elif variant == "tall":
+        w = dataclasses.replace(w, muon=tuple(workloads.MuonTensor(f"t{i}", (128, 64)) for i in range(4)))
+        shape = (128, 64)
+    _run_bucket(L, w, shape, list(range(4)), 3, hp=hp)
+
+
+def test_zero_gradient_step_only_decays(L):
+    K, A, B = 2, 64, 128
+    p = torch.randn((K, A, B), device=DEV)
+    p0 = p.clone()
+    g = torch.zeros((K, A, B), device=DEV)
+    mom = torch.zeros((K, A, B), device=DEV)
+    ws = workspace(L, K, A, B)
+    hp = L.make_muon_hparams(0.02, 0.95, 0.01)
+    L.muon_step_batched(L.pointer_array([p[0], p[1]], DEV), L.MUON_F32, L.pointer_array([g[0], g[1]], DEV),
+                        L.MUON_F32, mom, K, A, B, hp, ws)
+    assert L.muon_check(ws) == L.MUON_OK
+    lr_wd = np.float32(np.float64(np.float32(0.02)) * np.float64(np.float32(0.01)))
+    expect = f64(p0) - np.float64(lr_wd) * f64(p0)
+    assert np.max(np.abs(f64(p) - expect)) <= 1e-7 * np.max(np.abs(expect))
+
+
+def test_gpt2_small_set_sampled(L):
+    """GPT-2-small Muon set (4 buckets x 12, bf16 params/grads), full stacks on the GPU, 2 steps, sampled oracle."""
+    w = workloads.workload("gpt2s")
+    from oracle.buckets import plan_buckets
+    plan = plan_buckets(workloads.shape_list(w))
+    for b, (shape, K) in enumerate(zip(plan["bucket_shapes"], plan["bucket_K"])):
+        members = [i for i, bid in enumerate(plan["bucket_id"]) if bid == b]
+        _run_bucket(L, w, shape, members, 2, sample=workloads.bucket_sample(K, w.cfg_id, b))
+
+
+def test_aspect_polar_express_cautious_sampled(L):
+    """K=16 of 256 x 16384 and K=16 of 16384 x 256, Student-t(3) gradients, 8 Polar Express steps, cautious WD."""
+    w = workloads.workload("aspect")
+    for b, (shape, members) in enumerate([((256, 16384), list(range(16))), ((16384, 256), list(range(16, 32)))]):
+        _run_bucket(L, w, shape, members, 3, sample=workloads.bucket_sample(16, w.cfg_id, b))
