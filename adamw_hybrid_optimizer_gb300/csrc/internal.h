@@ -26,6 +26,9 @@ enum KernelKind : int32_t {
 void launch_begin(int32_t kind, cudaStream_t s);
 void launch_end(cudaStream_t s);
 int device_sm_count();
+// The current device's capability check and the per-wait limit set by muon_set_timeout_ns (libmuon.cu).
+muon_status device_check();
+unsigned long long wait_timeout_ns();
 
 // ------------------------------------------------------------------------------------------ tensor-core GEMMs
 

@@ -104,6 +104,10 @@ void launch_end(cudaStream_t s) {
   g_pending_kind = -1;
 }
 
+muon_status device_check() { return check_device(); }
+
+unsigned long long wait_timeout_ns() { return g_timeout_ns; }
+
 int device_sm_count() {
   const int d = current_device();
   if (d < 0 || d >= 64) return 1;

@@ -51,6 +51,8 @@ SIGNATURES = {
     "ns_orthogonalize": (ctypes.c_int, [_vp, ctypes.c_int, _vp, ctypes.c_int, _c_int64, _c_int64, _c_int64,
                                         ctypes.c_int, ctypes.POINTER(ctypes.c_float), ctypes.c_float, _vp,
                                         ctypes.c_size_t, _vp]),
+    "ns_orthogonalize_noalloc": (ctypes.c_int, [_vp, ctypes.c_int, _vp, ctypes.c_int, _c_int64, _c_int64, _c_int64,
+                                                ctypes.c_int, ctypes.POINTER(ctypes.c_float), ctypes.c_float, _vp]),
     "adamw_step": (ctypes.c_int, [_vp, ctypes.c_int, _vp, ctypes.c_int, _vp, _vp, _c_int64,
                                   ctypes.POINTER(adamw_hparams), _vp]),
     "ns_gram": (ctypes.c_int, [_vp, _vp, _c_int64, _c_int64, _c_int64, ctypes.c_float, _vp, ctypes.c_size_t, _vp]),
@@ -161,6 +163,16 @@ def ns_orthogonalize(x, out, coeffs, eps: float, ws, stream=None):
     st = lib().ns_orthogonalize(x.data_ptr(), _dtype_code(x), out.data_ptr(), _dtype_code(out), K, A, B, steps,
                                 arr, eps, ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream))
     _check(st, "ns_orthogonalize")
+
+
+def ns_orthogonalize_noalloc(x, out, coeffs, eps: float, stream=None):
+    """ns_orthogonalize for callers that cannot allocate device memory: no workspace argument; the library's
+    built-in 64 MiB scratch is used instead (see include/libmuon.h for the limits and the sharing rules)."""
+    K, A, B = x.shape
+    arr, steps = _coeff_array(coeffs)
+    st = lib().ns_orthogonalize_noalloc(x.data_ptr(), _dtype_code(x), out.data_ptr(), _dtype_code(out), K, A, B,
+                                        steps, arr, eps, _stream(stream))
+    _check(st, "ns_orthogonalize_noalloc")
 
 
 def adamw_step(param, grad, exp_avg, exp_avg_sq, lr, beta1, beta2, eps, weight_decay, step: int, stream=None):

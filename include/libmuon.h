@@ -114,6 +114,24 @@ muon_status ns_orthogonalize(const void *x, muon_dtype xdt, void *out, muon_dtyp
 muon_status adamw_step(void *param, muon_dtype pdt, const void *grad, muon_dtype gdt, float *exp_avg,
                        float *exp_avg_sq, int64_t n, const adamw_hparams *hp, muon_stream_t stream);
 
+/* ns_orthogonalize without any device allocation. The pages have no counterpart to this call.
+ * For callers that cannot allocate device memory and so cannot provide a workspace: code running
+ * inside a device-memory allocator's own hooks (allocating there would re-enter the allocator),
+ * plugins whose host program gives them no allocation API, runtimes whose device-memory budget is
+ * fixed at start-up. Same result and arguments as ns_orthogonalize minus the workspace.
+ *   Scratch: a static 64 MiB device array inside the library, held by every GPU that loads the
+ *   library until the process exits. A stack fits if 4*K*A*B + 4*K*min(A,B)^2 bytes plus padding
+ *   (as muon_workspace_bytes(K, A, B) counts it) is at most 64 MiB; larger stacks return
+ *   MUON_ERR_WORKSPACE before anything is launched.
+ *   The first call on a device looks up the array's device address (once per device, with that
+ *   device current); make that first call before any stream capture.
+ *   Every call shares the array: calls whose work overlaps on the GPU (other streams, other host
+ *   threads) race and must be serialised by the caller. Each call clears the array's control block;
+ *   a device-side wait that runs out is not reported by this call (muon_check needs a workspace).
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine. */
+muon_status ns_orthogonalize_noalloc(const void *x, muon_dtype xdt, void *out, muon_dtype odt, int64_t K, int64_t A,
+                                     int64_t B, int ns_steps, const float *coeffs, float eps, muon_stream_t stream);
+
 /* The three tensor-core steps of one Newton-Schulz iteration on contiguous bf16 stacks, exposed
  * one by one ([P2] newton_schulz loop body; [P4] section 2.2 symmetric Gram):
  *   ns_gram:  g = alpha * x x^T,         x (K, m, n), g (K, m, m); symmetric, both halves written.
