@@ -12,6 +12,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -32,6 +34,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 // columns 4*tx..4*tx+3 of rows ty, ty+16, ty+32, ty+48.
 template <typename GT, bool MOMENTUM>
 __global__ void __launch_bounds__(256) nesterov_norm_kernel(const NesterovArgs a) {
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_launch_dependents();
   constexpr int T = NESTEROV_TILE;
   __shared__ __nv_bfloat16 tile[T][T + 8];
   __shared__ float red[8];
@@ -153,6 +157,8 @@ __global__ void __launch_bounds__(256) nesterov_norm_kernel(const NesterovArgs a
 
 __global__ void __launch_bounds__(256) norm_finalize_kernel(const float *partials, int tiles, float *scale,
                                                             float eps) {
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_launch_dependents();
   __shared__ float red[8];
   const int b = blockIdx.x;
   const float *p = partials + static_cast<long long>(b) * tiles;
@@ -231,6 +237,8 @@ template <typename PT, typename GT>
 __global__ void __launch_bounds__(256) adamw_kernel(PT *__restrict__ p, const GT *__restrict__ g,
                                                     float *__restrict__ m, float *__restrict__ v, long long n,
                                                     int vec, AdamwConst c) {
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_launch_dependents();
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   long long done = 0;
@@ -261,6 +269,7 @@ __global__ void __launch_bounds__(256) adamw_kernel(PT *__restrict__ p, const GT
 }
 
 __global__ void debug_wait_kernel(uint32_t *err, unsigned long long timeout_ns) {
+  pdl_wait();
   __shared__ uint64_t bar;
   __shared__ int abort_flag;
   if (threadIdx.x == 0) {
@@ -275,28 +284,45 @@ __global__ void debug_wait_kernel(uint32_t *err, unsigned long long timeout_ns) 
   }
 }
 
+// Launch with programmatic stream serialization (the kernel waits for its predecessor itself).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 }  // namespace
 
 muon_status launch_nesterov_norm(const NesterovArgs &a, int K, cudaStream_t s) {
   const dim3 grid(a.tiles_r * a.tiles_c, K);
   launch_begin(KK_NESTEROV_NORM, s);
   const bool mom = a.momentum != nullptr;
-  if (a.gdtype == MUON_F32) {
-    if (mom) nesterov_norm_kernel<float, true><<<grid, 256, 0, s>>>(a);
-    else nesterov_norm_kernel<float, false><<<grid, 256, 0, s>>>(a);
-  } else {
-    if (mom) nesterov_norm_kernel<__nv_bfloat16, true><<<grid, 256, 0, s>>>(a);
-    else nesterov_norm_kernel<__nv_bfloat16, false><<<grid, 256, 0, s>>>(a);
-  }
+  cudaError_t e;
+  if (a.gdtype == MUON_F32)
+    e = mom ? launch_pdl(nesterov_norm_kernel<float, true>, grid, dim3(256), 0, s, a)
+            : launch_pdl(nesterov_norm_kernel<float, false>, grid, dim3(256), 0, s, a);
+  else
+    e = mom ? launch_pdl(nesterov_norm_kernel<__nv_bfloat16, true>, grid, dim3(256), 0, s, a)
+            : launch_pdl(nesterov_norm_kernel<__nv_bfloat16, false>, grid, dim3(256), 0, s, a);
   launch_end(s);
-  return cudaGetLastError() == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+  return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
 }
 
 muon_status launch_norm_finalize(const float *partials, int tiles, float *scale, int K, float eps, cudaStream_t s) {
   launch_begin(KK_NORM_FINALIZE, s);
-  norm_finalize_kernel<<<K, 256, 0, s>>>(partials, tiles, scale, eps);
+  const cudaError_t e = launch_pdl(norm_finalize_kernel, dim3(K), dim3(256), 0, s, partials, tiles, scale, eps);
   launch_end(s);
-  return cudaGetLastError() == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+  return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
 }
 
 muon_status launch_adamw(void *p, int pdt, const void *g, int gdt, float *m, float *v, long long n,
@@ -311,28 +337,29 @@ muon_status launch_adamw(void *p, int pdt, const void *g, int gdt, float *m, flo
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   launch_begin(KK_ADAMW, s);
-  const int gb = static_cast<int>(blocks);
+  const dim3 gb(static_cast<unsigned>(blocks)), tb(256);
+  cudaError_t e;
   if (pdt == MUON_F32 && gdt == MUON_F32)
-    adamw_kernel<float, float><<<gb, 256, 0, s>>>(static_cast<float *>(p), static_cast<const float *>(g), m, v, n,
-                                                  vec, c);
+    e = launch_pdl(adamw_kernel<float, float>, gb, tb, 0, s, static_cast<float *>(p), static_cast<const float *>(g),
+                   m, v, n, vec, c);
   else if (pdt == MUON_F32 && gdt == MUON_BF16)
-    adamw_kernel<float, __nv_bfloat16><<<gb, 256, 0, s>>>(static_cast<float *>(p),
-                                                          static_cast<const __nv_bfloat16 *>(g), m, v, n, vec, c);
+    e = launch_pdl(adamw_kernel<float, __nv_bfloat16>, gb, tb, 0, s, static_cast<float *>(p),
+                   static_cast<const __nv_bfloat16 *>(g), m, v, n, vec, c);
   else if (pdt == MUON_BF16 && gdt == MUON_F32)
-    adamw_kernel<__nv_bfloat16, float><<<gb, 256, 0, s>>>(static_cast<__nv_bfloat16 *>(p),
-                                                          static_cast<const float *>(g), m, v, n, vec, c);
+    e = launch_pdl(adamw_kernel<__nv_bfloat16, float>, gb, tb, 0, s, static_cast<__nv_bfloat16 *>(p),
+                   static_cast<const float *>(g), m, v, n, vec, c);
   else
-    adamw_kernel<__nv_bfloat16, __nv_bfloat16><<<gb, 256, 0, s>>>(
-        static_cast<__nv_bfloat16 *>(p), static_cast<const __nv_bfloat16 *>(g), m, v, n, vec, c);
+    e = launch_pdl(adamw_kernel<__nv_bfloat16, __nv_bfloat16>, gb, tb, 0, s, static_cast<__nv_bfloat16 *>(p),
+                   static_cast<const __nv_bfloat16 *>(g), m, v, n, vec, c);
   launch_end(s);
-  return cudaGetLastError() == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+  return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
 }
 
 muon_status launch_debug_wait(uint32_t *err, unsigned long long timeout_ns, cudaStream_t s) {
   launch_begin(KK_DEBUG_WAIT, s);
-  debug_wait_kernel<<<1, 32, 0, s>>>(err, timeout_ns);
+  const cudaError_t e = launch_pdl(debug_wait_kernel, dim3(1), dim3(32), 0, s, err, timeout_ns);
   launch_end(s);
-  return cudaGetLastError() == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+  return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
 }
 
 }  // namespace muon

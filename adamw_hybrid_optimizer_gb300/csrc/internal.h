@@ -34,22 +34,22 @@ unsigned long long wait_timeout_ns();
 
 enum EpiKind : int { EPI_GRAM = 0, EPI_POLY = 1, EPI_APPLY = 2, EPI_FINAL = 3 };
 
-// Arguments of one grouped tensor-core launch over a batch of K matrices.
-struct GemmArgs {
-  // tile space of the output (per matrix: rows x cols), 128 x 256 tiles
+constexpr int GEMM_MAX_PROBLEMS = 8;
+
+// One problem of a grouped tensor-core launch: a stack of `batch` matrices whose output is rows x cols
+// (128 x 256 tiles), with its own epilogue inputs and outputs.
+struct GemmProblem {
   int batch;
   int rows;
   int cols;
   int m_tiles, n_tiles;
   int tiles_per_matrix;
-  long long total_tiles;
-  int k_iters;      // contraction / 64, rounded up
-  int symmetric;    // 1: only tiles touching the upper triangle; each value also stored mirrored
+  int k_iters;            // contraction / 64, rounded up
+  long long tile_begin;   // first tile of this problem in the launch's tile space
   // epilogue coefficients
-  float alpha;            // gram: output = alpha * s^scale_pow * acc
+  float alpha;            // gram: output = alpha * s^2 * acc (s from `scale` when given)
   float coef_a, coef_b, coef_c;
   const float *scale;     // per-matrix normalisation s_k (device), or null
-  int scale_pow;
   // bf16 output of gram / poly / apply
   __nv_bfloat16 *out;
   long long ld_out, mstride_out;
@@ -65,9 +65,6 @@ struct GemmArgs {
   int cautious;
   float lr_wd;            // lr * weight_decay
   float lr_scale;         // lr * update scale
-  // control
-  uint32_t *err;
-  unsigned long long timeout_ns;
 };
 
 // A bf16 matrix stack in global memory as the GEMMs see it: K matrices of rows x cols,
@@ -77,12 +74,6 @@ struct Bf16Stack {
   long long rows, cols, ld, mstride, batch;
 };
 
-muon_status launch_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long ldg, long long mstride_g, float alpha,
-                        const float *scale, uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
-muon_status launch_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float b, float c,
-                        uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
-muon_status launch_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, float a, const float *scale,
-                         uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
 // Final iteration: u = s*(a*x + h x) in the wide orientation, then either the Muon parameter update
 // or a dense store, transposing back when the stored matrix is tall.
 struct FinalSpec {
@@ -94,6 +85,37 @@ struct FinalSpec {
   int cautious;
   float lr_wd, lr_scale;
 };
+
+// Collects the problems of one step kind (all grams, all polys, ...) of several stacks and launches
+// them as few grouped kernels (up to GEMM_MAX_PROBLEMS problems per launch), deepest contraction first.
+class GemmBatch {
+ public:
+  GemmBatch(int epi, uint32_t *err, unsigned long long timeout_ns) : epi_(epi), err_(err), timeout_ns_(timeout_ns) {}
+  muon_status add_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long ldg, long long mstride_g, float alpha,
+                       const float *scale);
+  muon_status add_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float b, float c);
+  muon_status add_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, float a, const float *scale);
+  muon_status add_final(const Bf16Stack &h, const Bf16Stack &x, float a, const float *scale, const FinalSpec &f);
+  muon_status launch(cudaStream_t s);
+  ~GemmBatch();
+
+ private:
+  struct Item;
+  int epi_;
+  uint32_t *err_;
+  unsigned long long timeout_ns_;
+  Item *items_ = nullptr;
+  int n_ = 0, cap_ = 0;
+  muon_status push(const Item &it);
+};
+
+// Single-stack conveniences (a batch of one).
+muon_status launch_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long ldg, long long mstride_g, float alpha,
+                        const float *scale, uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
+muon_status launch_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float b, float c,
+                        uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
+muon_status launch_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, float a, const float *scale,
+                         uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
 muon_status launch_final(const Bf16Stack &h, const Bf16Stack &x, float a, const float *scale, const FinalSpec &f,
                          uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
 

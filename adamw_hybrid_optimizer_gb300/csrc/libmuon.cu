@@ -2,6 +2,7 @@
 // launch counting and the optional event trace. See include/libmuon.h for the contract.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 #include <map>
@@ -267,6 +268,118 @@ muon_status muon_step_batched(void *const *params, muon_dtype pdt, const void *c
   fin.lr_wd = static_cast<float>(static_cast<double>(hp->lr) * hp->weight_decay);
   fin.lr_scale = static_cast<float>(static_cast<double>(hp->lr) * scale);
   return run_ns_chain(w, L, K, hp->ns_steps, hp->coeffs, fin, s);
+}
+
+static muon_status check_bucket(const muon_bucket &b) {
+  if (b.params == nullptr || b.grads == nullptr || b.momentum == nullptr) return MUON_ERR_INVALID_ARG;
+  muon_status st = check_stack_dims(b.K, b.A, b.B);
+  if (st != MUON_OK) return st;
+  if (!valid_dtype(b.pdt) || !valid_dtype(b.gdt)) return MUON_ERR_DTYPE;
+  return MUON_OK;
+}
+
+size_t muon_workspace_bytes_grouped(const muon_bucket *buckets, int n) {
+  if (buckets == nullptr || n < 1) return 0;
+  size_t total = 0;
+  for (int i = 0; i < n; ++i) {
+    if (buckets[i].K < 1 || buckets[i].A < 1 || buckets[i].B < 1) return 0;
+    total += layout(buckets[i].K, buckets[i].A, buckets[i].B).total;
+  }
+  return total;
+}
+
+muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hparams *hp, void *ws, size_t ws_bytes,
+                              muon_stream_t stream) {
+  if (buckets == nullptr || hp == nullptr || ws == nullptr || n < 1 || n > 4096) return MUON_ERR_INVALID_ARG;
+  muon_status st;
+  for (int i = 0; i < n; ++i)
+    if ((st = check_bucket(buckets[i])) != MUON_OK) return st;
+  if ((st = check_coeffs(hp->ns_steps, hp->coeffs)) != MUON_OK) return st;
+  if (hp->scale_mode != 0 && hp->scale_mode != 1) return MUON_ERR_INVALID_ARG;
+  if (!std::isfinite(hp->lr) || !std::isfinite(hp->momentum) || !std::isfinite(hp->weight_decay) ||
+      !std::isfinite(hp->eps) || hp->eps < 0.f)
+    return MUON_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MUON_ERR_ALIGNMENT;
+  if (ws_bytes < muon_workspace_bytes_grouped(buckets, n)) return MUON_ERR_WORKSPACE;
+  if ((st = check_device()) != MUON_OK) return st;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char *base = static_cast<char *>(ws);
+  uint32_t *err = reinterpret_cast<uint32_t *>(base);
+  const unsigned long long to = g_timeout_ns;
+  std::vector<Layout> L(n);
+  std::vector<char *> w(n);
+  size_t off = 0;
+  for (int i = 0; i < n; ++i) {
+    L[i] = layout(buckets[i].K, buckets[i].A, buckets[i].B);
+    w[i] = base + off;
+    off += L[i].total;
+  }
+  // momentum, Nesterov input, norm: one pass per bucket
+  for (int i = 0; i < n; ++i) {
+    const muon_bucket &bk = buckets[i];
+    NesterovArgs na{};
+    na.gptrs = bk.grads;
+    na.gdtype = bk.gdt;
+    na.momentum = bk.momentum;
+    na.u = reinterpret_cast<__nv_bfloat16 *>(w[i] + L[i].x0);
+    na.ldu = L[i].ldx;
+    na.mstride_u = L[i].m * L[i].ldx;
+    na.partials = reinterpret_cast<float *>(w[i] + L[i].partial);
+    na.A = static_cast<int>(bk.A);
+    na.B = static_cast<int>(bk.B);
+    na.tiles_r = static_cast<int>(L[i].tiles_r);
+    na.tiles_c = static_cast<int>(L[i].tiles_c);
+    na.transposed = bk.A > bk.B ? 1 : 0;
+    na.mu = hp->momentum;
+    na.nesterov = hp->nesterov ? 1 : 0;
+    if ((st = launch_nesterov_norm(na, static_cast<int>(bk.K), s)) != MUON_OK) return st;
+    if ((st = launch_norm_finalize(na.partials, static_cast<int>(L[i].tiles_r * L[i].tiles_c),
+                                   reinterpret_cast<float *>(w[i] + L[i].scale), static_cast<int>(bk.K), hp->eps,
+                                   s)) != MUON_OK)
+      return st;
+  }
+  // the Newton-Schulz chain, each step kind of all buckets in one grouped launch
+  for (int t = 0; t < hp->ns_steps; ++t) {
+    const float a = hp->coeffs[3 * t], b = hp->coeffs[3 * t + 1], c = hp->coeffs[3 * t + 2];
+    GemmBatch gram(EPI_GRAM, err, to), poly(EPI_POLY, err, to);
+    GemmBatch last(t + 1 < hp->ns_steps ? EPI_APPLY : EPI_FINAL, err, to);
+    for (int i = 0; i < n; ++i) {
+      const Layout &Li = L[i];
+      const float *sc = t == 0 ? reinterpret_cast<const float *>(w[i] + Li.scale) : nullptr;
+      __nv_bfloat16 *xb[2] = {reinterpret_cast<__nv_bfloat16 *>(w[i] + Li.x0),
+                              reinterpret_cast<__nv_bfloat16 *>(w[i] + Li.x1)};
+      __nv_bfloat16 *G = reinterpret_cast<__nv_bfloat16 *>(w[i] + Li.g);
+      __nv_bfloat16 *H = reinterpret_cast<__nv_bfloat16 *>(w[i] + Li.h);
+      const long long K = buckets[i].K, msx = Li.m * Li.ldx, msg = Li.m * Li.ldg;
+      Bf16Stack X{xb[t & 1], Li.m, Li.n, Li.ldx, msx, K};
+      Bf16Stack Gs{G, Li.m, Li.m, Li.ldg, msg, K};
+      Bf16Stack Hs{H, Li.m, Li.m, Li.ldg, msg, K};
+      if ((st = gram.add_gram(X, G, Li.ldg, msg, 1.0f, sc)) != MUON_OK) return st;
+      if ((st = poly.add_poly(Gs, H, Li.ldg, msg, b, c)) != MUON_OK) return st;
+      if (t + 1 < hp->ns_steps) {
+        st = last.add_apply(Hs, X, xb[(t + 1) & 1], a, sc);
+      } else {
+        const muon_bucket &bk = buckets[i];
+        const double scale = hp->scale_mode == 0
+                                 ? 0.2 * std::sqrt(static_cast<double>(bk.A > bk.B ? bk.A : bk.B))
+                                 : std::sqrt(std::max(1.0, static_cast<double>(bk.A) / static_cast<double>(bk.B)));
+        FinalSpec fin{};
+        fin.params = bk.params;
+        fin.dtype = bk.pdt;
+        fin.transposed = bk.A > bk.B ? 1 : 0;
+        fin.orig_cols = static_cast<int>(bk.B);
+        fin.cautious = hp->cautious_wd ? 1 : 0;
+        fin.lr_wd = static_cast<float>(static_cast<double>(hp->lr) * hp->weight_decay);
+        fin.lr_scale = static_cast<float>(static_cast<double>(hp->lr) * scale);
+        st = last.add_final(Hs, X, a, sc, fin);
+      }
+      if (st != MUON_OK) return st;
+    }
+    if ((st = gram.launch(s)) != MUON_OK || (st = poly.launch(s)) != MUON_OK || (st = last.launch(s)) != MUON_OK)
+      return st;
+  }
+  return MUON_OK;
 }
 
 muon_status ns_orthogonalize(const void *x, muon_dtype xdt, void *out, muon_dtype odt, int64_t K, int64_t A,

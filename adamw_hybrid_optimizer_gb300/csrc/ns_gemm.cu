@@ -9,15 +9,19 @@
 //     X' = a X + H X                EPI_APPLY  B operand (X) is read N-major
 //     last step: u = a X + H X, then p <- p - lr*wd*p*mask - lr*scale*u      EPI_FINAL
 //
-// Design (sm_103a): 128 x 256 output tiles, 64-deep k-slices, 4-stage TMA ring with 128-byte
-// swizzle, one tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) per 16-slice issued by one thread,
-// fp32 accumulators in tensor memory (2 x 256 columns, so the epilogue of one tile overlaps the
-// MMAs of the next), persistent CTAs (one per SM) striding over (matrix, tile) of the whole stack.
-// Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner), warps 2-5 = epilogue.
+// Design (sm_103a): 128 x 256 output tiles, 64-deep k-slices, a TMA ring with 128-byte swizzle
+// (4 stages, 3 for the final step), one tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) per 16-slice
+// issued by one thread, fp32 accumulators in tensor memory (2 x 256 columns, so the epilogue of one
+// tile overlaps the MMAs of the next), persistent CTAs (one per SM) striding over the tiles of up to
+// GEMM_MAX_PROBLEMS stacks at once. Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM
+// owner), warps 2-5 = epilogue, warp 6 = epilogue loader: ahead of the epilogue it brings each tile's
+// second input (G or X) and, for bf16 parameters, the parameters into a 2-slot shared-memory ring, so
+// the epilogue never waits for a global-memory round trip.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "internal.h"
@@ -30,30 +34,73 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
+constexpr int MAX_STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int ACC_COLS = BN;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 224;
+
+// Epilogue input ring: a slot holds 64 columns (two 32-column chunks) of a tile's 128 rows.
+constexpr int RING_SLOTS = 2;
+constexpr int RING_AUX_BYTES = BM * 64 * 2;                 // bf16, 128-byte rows, 128B-swizzled (as TMA writes)
+constexpr int PARAM_PITCH_WIDE = 64 * 2 + 16;               // stored row-major: [128 rows][64 cols] + pad
+constexpr int PARAM_PITCH_TALL = BM * 2 + 16;               // stored transposed: [64 stored rows][128] + pad
+constexpr int RING_PARAM_BYTES = BM * PARAM_PITCH_WIDE;     // >= 64 * PARAM_PITCH_TALL
+static_assert(RING_PARAM_BYTES >= 64 * PARAM_PITCH_TALL, "param slot too small");
+
+__host__ __device__ constexpr int stages_of(int epi) { return epi == EPI_FINAL ? 3 : 4; }
+__host__ __device__ constexpr int ring_slot_bytes(int epi) {
+  return epi == EPI_GRAM ? 0 : (epi == EPI_FINAL ? RING_AUX_BYTES + RING_PARAM_BYTES : RING_AUX_BYTES);
+}
 
 struct Ctrl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
+  uint64_t ring_full[RING_SLOTS];
+  uint64_t ring_empty[RING_SLOTS];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  int ring_param_ok[RING_SLOTS];
 };
 
-constexpr size_t SMEM_BYTES = static_cast<size_t>(STAGES) * STAGE_BYTES + sizeof(Ctrl) + 1024;
+__host__ __device__ constexpr size_t smem_bytes(int epi) {
+  return static_cast<size_t>(stages_of(epi)) * STAGE_BYTES + static_cast<size_t>(RING_SLOTS) * ring_slot_bytes(epi) +
+         sizeof(Ctrl) + 1024;
+}
+static_assert(smem_bytes(EPI_APPLY) <= 232448 && smem_bytes(EPI_FINAL) <= 232448, "shared memory over budget");
 
-__device__ __forceinline__ void decode_tile(const GemmArgs &a, long long t, int &b, int &ti, int &tj) {
+// Kernel parameter: up to GEMM_MAX_PROBLEMS problems of one step kind, in order of tile_begin.
+struct GemmGroup {
+  CUtensorMap map_a[GEMM_MAX_PROBLEMS];
+  CUtensorMap map_b[GEMM_MAX_PROBLEMS];
+  GemmProblem prob[GEMM_MAX_PROBLEMS];
+  int nprob;
+  int symmetric;
+  long long total_tiles;
+  uint32_t *err;
+  unsigned long long timeout_ns;
+};
+static_assert(sizeof(GemmGroup) <= 4096, "kernel parameter block too large");
+
+__device__ __forceinline__ int find_problem(const GemmGroup &g, long long t) {
+  int p = 0;
+#pragma unroll 1
+  for (int q = 1; q < g.nprob; ++q)
+    if (t >= g.prob[q].tile_begin) p = q;
+  return p;
+}
+
+// local tile index of one problem -> (matrix, tile row, tile column)
+__device__ __forceinline__ void decode_tile(const GemmProblem &a, int symmetric, long long t, int &b, int &ti,
+                                            int &tj) {
   b = static_cast<int>(t / a.tiles_per_matrix);
   int r = static_cast<int>(t - static_cast<long long>(b) * a.tiles_per_matrix);
-  if (!a.symmetric) {
+  if (!symmetric) {
     tj = r / a.m_tiles;
     ti = r - tj * a.m_tiles;
     return;
@@ -72,63 +119,168 @@ __device__ __forceinline__ void decode_tile(const GemmArgs &a, long long t, int 
   }
 }
 
+// A ring slot pair of chunks is used unless the whole tile lies below the diagonal for those 64 columns.
+__device__ __forceinline__ bool slot_used(int symmetric, int c0, int row0) { return !(symmetric && c0 + 63 < row0); }
+
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
-__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16 *src, float *dst) {
-  const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+__device__ __forceinline__ void unpack8(const uint4 &w, float *dst) {
+  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&w);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 w = s4[q];
-    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&w);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float2 f = __bfloat1622float2(h[e]);
-      dst[q * 8 + 2 * e] = f.x;
-      dst[q * 8 + 2 * e + 1] = f.y;
-    }
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __bfloat1622float2(h[e]);
+    dst[2 * e] = f.x;
+    dst[2 * e + 1] = f.y;
   }
+}
+
+__device__ __forceinline__ uint4 pack8(const float *src) {
+  uint4 w;
+  __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(src[2 * e], src[2 * e + 1]);
+  return w;
 }
 
 __device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const float *src) {
   uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 w;
-    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
+  for (int q = 0; q < 4; ++q) d4[q] = pack8(src + 8 * q);
+}
+
+// 32 bf16 values of tile row r, columns 32*half .. 32*half+31 of a ring slot (128-byte rows, 128B swizzle:
+// the 16-byte chunk q of row r sits at chunk position q ^ (r & 7)).
+__device__ __forceinline__ void ring_aux_row(const uint8_t *slot, int r, int half, float *dst) {
+  const uint8_t *row = slot + r * 128;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(src[q * 8 + 2 * e], src[q * 8 + 2 * e + 1]);
-    d4[q] = w;
+  for (int q = 0; q < 4; ++q) {
+    const int qq = (4 * half + q) ^ (r & 7);
+    unpack8(*reinterpret_cast<const uint4 *>(row + qq * 16), dst + 8 * q);
   }
 }
 
-// Epilogue for one 32-column chunk held by one thread (its row `row`, columns col0..col0+31).
-template <int EPI>
-__device__ __forceinline__ void epilogue_chunk(const GemmArgs &a, int b, int row, int col0, float *v) {
-  if constexpr (EPI == EPI_GRAM || EPI == EPI_POLY) {
-    float sc = a.alpha;
-    if (EPI == EPI_GRAM && a.scale != nullptr) {
-      const float s = a.scale[b];
-      sc *= s * s;
+// Muon parameter update of one element: decoupled decay (masked where u*p <= 0 if cautious), then the
+// scaled orthogonalised step.
+__device__ __forceinline__ float param_update(float pv, float u, const GemmProblem &a) {
+  const float mask = (!a.cautious || u * pv > 0.f) ? 1.f : 0.f;
+  return (pv - a.lr_wd * mask * pv) - a.lr_scale * u;
+}
+
+// Final step for one thread's 32 values of wide row `row`, columns col0..col0+31.
+//   stored wide (row-major A x B): the thread's row segment; parameters from the ring (param_slot, laid out
+//   [128 rows][64 cols] with pitch PARAM_PITCH_WIDE) when the loader staged them, else loaded directly.
+//   stored tall (transposed): element (c, row); for each column the warp's lanes cover 32 consecutive stored
+//   elements; ring layout [64 stored rows][128] with pitch PARAM_PITCH_TALL.
+__device__ __forceinline__ void final_store(const GemmProblem &a, void *base, int row, int rloc, int col0, int half,
+                                            const uint8_t *param_slot, bool staged, float *v) {
+  const bool update = a.params != nullptr;
+  const bool f32 = a.out_dtype == MUON_F32;
+  if (!a.transposed) {
+    const long long idx = static_cast<long long>(row) * a.orig_cols + col0;
+    float pv[32];
+    if (update) {
+      if (staged) {
+        const uint8_t *src = param_slot + rloc * PARAM_PITCH_WIDE + half * 64;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) unpack8(*reinterpret_cast<const uint4 *>(src + 16 * q), pv + 8 * q);
+      } else if (f32) {
+        const float *p = static_cast<const float *>(base) + idx;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pv[j] = (col0 + j < a.cols) ? p[j] : 0.f;
+      } else {
+        const __nv_bfloat16 *p = static_cast<const __nv_bfloat16 *>(base) + idx;
+        const bool vec = col0 + 32 <= a.cols && (reinterpret_cast<uintptr_t>(p) & 15) == 0;
+        if (vec) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) unpack8(reinterpret_cast<const uint4 *>(p)[q], pv + 8 * q);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) pv[j] = (col0 + j < a.cols) ? bf2f(p[j]) : 0.f;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = param_update(pv[j], v[j], a);
     }
+    if (f32) {
+      float *p = static_cast<float *>(base) + idx;
+      const bool vec = col0 + 32 <= a.cols && (reinterpret_cast<uintptr_t>(p) & 15) == 0;
+      if (vec) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          reinterpret_cast<float4 *>(p)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (col0 + j < a.cols) p[j] = v[j];
+      }
+    } else {
+      __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(base) + idx;
+      const bool vec = col0 + 32 <= a.cols && (reinterpret_cast<uintptr_t>(p) & 15) == 0;
+      if (vec) {
+        store_bf16x32(p, v);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (col0 + j < a.cols) p[j] = __float2bfloat16_rn(v[j]);
+      }
+    }
+    return;
+  }
+  // transposed: all loads are issued before the first store
+  if (update) {
+    float pv[32];
+    if (staged) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        pv[j] = bf2f(*reinterpret_cast<const __nv_bfloat16 *>(param_slot + (32 * half + j) * PARAM_PITCH_TALL +
+                                                              2 * rloc));
+    } else if (f32) {
+      const float *p = static_cast<const float *>(base) + row;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) pv[j] = (col0 + j < a.cols) ? p[static_cast<long long>(col0 + j) * a.orig_cols] : 0.f;
+    } else {
+      const __nv_bfloat16 *p = static_cast<const __nv_bfloat16 *>(base) + row;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        pv[j] = (col0 + j < a.cols) ? bf2f(p[static_cast<long long>(col0 + j) * a.orig_cols]) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = param_update(pv[j], v[j], a);
+  }
+  if (f32) {
+    float *p = static_cast<float *>(base) + row;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (col0 + j < a.cols) p[static_cast<long long>(col0 + j) * a.orig_cols] = v[j];
+  } else {
+    __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(base) + row;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (col0 + j < a.cols) p[static_cast<long long>(col0 + j) * a.orig_cols] = __float2bfloat16_rn(v[j]);
+  }
+}
+
+// Epilogue for one 32-column chunk held by one thread (its row `row` = tile row `rloc`, columns
+// col0..col0+31, i.e. half `half` of the ring slot). Called by every lane of the warp.
+template <int EPI>
+__device__ __forceinline__ void epilogue_chunk(const GemmProblem &a, int b, int row, int rloc, int col0, int half,
+                                               const uint8_t *aux_slot, const uint8_t *param_slot, bool param_staged,
+                                               float *v) {
+  if constexpr (EPI == EPI_GRAM || EPI == EPI_POLY) {
     const bool row_ok = row < a.rows;
     const bool full = row_ok && (col0 >= row) && (col0 + 32 <= a.cols);
     __nv_bfloat16 *out_b = a.out + static_cast<long long>(b) * a.mstride_out;
     if constexpr (EPI == EPI_POLY) {
-      const __nv_bfloat16 *g_row = a.aux + static_cast<long long>(b) * a.mstride_aux + static_cast<long long>(row) * a.ld_aux;
-      if (full) {
-        float gv[32];
-        load_bf16x32(g_row + col0, gv);
+      float gv[32];
+      ring_aux_row(aux_slot, rloc, half, gv);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = a.coef_b * gv[j] + a.coef_c * v[j];
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int c = col0 + j;
-          const float gv = (row_ok && c < a.cols && c >= row) ? bf2f(g_row[c]) : 0.f;
-          v[j] = a.coef_b * gv + a.coef_c * v[j];
-        }
-      }
+      for (int j = 0; j < 32; ++j) v[j] = a.coef_b * gv[j] + a.coef_c * v[j];
     } else {
+      float sc = a.alpha;
+      if (a.scale != nullptr) {
+        const float s = a.scale[b];
+        sc *= s * s;
+      }
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] *= sc;
     }
@@ -150,23 +302,15 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &a, int b, int row
       if (row_ok && c < a.cols && c > row) out_b[static_cast<long long>(c) * a.ld_out + row] = __float2bfloat16_rn(v[j]);
     }
   } else {
-    float sc = 1.f;
-    if (a.scale != nullptr) sc = a.scale[b];
-    if (row >= a.rows) return;
-    const __nv_bfloat16 *x_row = a.aux + static_cast<long long>(b) * a.mstride_aux + static_cast<long long>(row) * a.ld_aux;
-    const bool full = (col0 + 32 <= a.cols);
+    const float sc = a.scale != nullptr ? a.scale[b] : 1.f;
     float xv[32];
-    if (full) {
-      load_bf16x32(x_row + col0, xv);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) xv[j] = (col0 + j < a.cols) ? bf2f(x_row[col0 + j]) : 0.f;
-    }
+    ring_aux_row(aux_slot, rloc, half, xv);
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = sc * (a.coef_a * xv[j] + v[j]);
+    if (row >= a.rows) return;
     if constexpr (EPI == EPI_APPLY) {
       __nv_bfloat16 *o_row = a.out + static_cast<long long>(b) * a.mstride_out + static_cast<long long>(row) * a.ld_out;
-      if (full) {
+      if (col0 + 32 <= a.cols) {
         store_bf16x32(o_row + col0, v);
       } else {
 #pragma unroll
@@ -174,51 +318,48 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &a, int b, int row
           if (col0 + j < a.cols) o_row[col0 + j] = __float2bfloat16_rn(v[j]);
       }
     } else {
-      // wide (row, c) is stored element (c, row) when transposed, else (row, c)
       const long long mat_elems = static_cast<long long>(a.rows) * a.cols;
       void *base = a.params != nullptr ? a.params[b]
                                        : static_cast<void *>(static_cast<char *>(a.out_dense) +
                                                              static_cast<long long>(b) * mat_elems *
                                                                  (a.out_dtype == MUON_F32 ? 4 : 2));
-      const bool update = a.params != nullptr;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int c = col0 + j;
-        if (c >= a.cols) continue;
-        const long long idx = a.transposed ? static_cast<long long>(c) * a.orig_cols + row
-                                           : static_cast<long long>(row) * a.orig_cols + c;
-        const float u = v[j];
-        if (a.out_dtype == MUON_F32) {
-          float *p = static_cast<float *>(base) + idx;
-          if (update) {
-            const float pv = *p;
-            const float mask = (!a.cautious || u * pv > 0.f) ? 1.f : 0.f;
-            *p = (pv - a.lr_wd * mask * pv) - a.lr_scale * u;
-          } else {
-            *p = u;
-          }
-        } else {
-          __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(base) + idx;
-          if (update) {
-            const float pv = bf2f(*p);
-            const float mask = (!a.cautious || u * pv > 0.f) ? 1.f : 0.f;
-            *p = __float2bfloat16_rn((pv - a.lr_wd * mask * pv) - a.lr_scale * u);
-          } else {
-            *p = __float2bfloat16_rn(u);
-          }
-        }
-      }
+      final_store(a, base, row, rloc, col0, half, param_slot, param_staged, v);
     }
   }
 }
 
+// Epilogue loader's parameter staging for one slot (64 columns of a tile) of the final step: 1-D bulk
+// copies of the stored rows, when every copy is a whole, 16-byte-aligned bf16 segment. Returns the
+// bytes it will deliver (0: the epilogue loads the parameters itself).
+__device__ __forceinline__ uint32_t stage_params_bytes(const GemmProblem &a, int b, int row0, int c0,
+                                                       const void *&base) {
+  if (a.params == nullptr || a.out_dtype != MUON_BF16) return 0;
+  base = a.params[b];
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (a.orig_cols & 7) != 0) return 0;
+  if (c0 + 64 > a.cols || row0 + BM > a.rows) return 0;
+  return a.transposed ? 64u * BM * 2u : static_cast<uint32_t>(BM) * 64u * 2u;
+}
+
+__device__ __forceinline__ void stage_params_issue(const GemmProblem &a, const void *base, int row0, int c0,
+                                                   uint8_t *dst, uint64_t *bar) {
+  const __nv_bfloat16 *p = static_cast<const __nv_bfloat16 *>(base);
+  if (!a.transposed) {
+    for (int r = 0; r < BM; ++r)
+      bulk_load(dst + r * PARAM_PITCH_WIDE, p + static_cast<long long>(row0 + r) * a.orig_cols + c0, 128, bar);
+  } else {
+    for (int j = 0; j < 64; ++j)
+      bulk_load(dst + j * PARAM_PITCH_TALL, p + static_cast<long long>(c0 + j) * a.orig_cols + row0, BM * 2, bar);
+  }
+}
+
 template <int EPI, bool B_MN>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-    ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                   const GemmArgs args) {
+__global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_constant__ GemmGroup args) {
+  constexpr int STAGES = stages_of(EPI);
+  constexpr int SLOT_BYTES = ring_slot_bytes(EPI);
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + STAGES * STAGE_BYTES);
+  uint8_t *ring = smem + STAGES * STAGE_BYTES;
+  Ctrl *ctrl = reinterpret_cast<Ctrl *>(ring + RING_SLOTS * SLOT_BYTES);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -232,13 +373,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&ctrl->acc_full[s], 1);
       mbar_init(&ctrl->acc_empty[s], 4);
     }
+    for (int s = 0; s < RING_SLOTS; ++s) {
+      mbar_init(&ctrl->ring_full[s], 1);
+      mbar_init(&ctrl->ring_empty[s], 4);
+    }
     mbar_init(&ctrl->drain, 1);
     ctrl->abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&map_a);
-    tma_prefetch_desc(&map_b);
+  if (warp == 0 && lane < 2 * args.nprob) {
+    tma_prefetch_desc(lane & 1 ? &args.map_b[lane >> 1] : &args.map_a[lane >> 1]);
   }
   if (warp == 1) {
     tmem_alloc(&ctrl->tmem_base, TMEM_COLS);
@@ -247,21 +391,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // everything above touched only shared and tensor memory; operands, scales and parameters written by
+  // earlier kernels are read only after the previous grid has completed
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_launch_dependents();
   const uint32_t tmem_base = ctrl->tmem_base;
   WaitCtl ctl{&ctrl->abort_flag, args.err, args.timeout_ns};
-  WaitCtl drain_ctl{&ctrl->abort_flag, args.err, args.timeout_ns};
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------------- TMA producer
       uint32_t stage = 0, phase = 0;
-      int last_parity[STAGES];
-      for (int s = 0; s < STAGES; ++s) last_parity[s] = -1;
+      int last_parity[MAX_STAGES];
+      for (int s = 0; s < MAX_STAGES; ++s) last_parity[s] = -1;
       bool ok = true;
       for (long long t = blockIdx.x; ok && t < args.total_tiles; t += gridDim.x) {
+        // descriptor fields copied to registers: the asm below clobbers memory, which would otherwise force a
+        // reload from parameter space on every use
+        const int pi = find_problem(args, t);
+        const GemmProblem P = args.prob[pi];
+        const CUtensorMap *map_a = &args.map_a[pi];
+        const CUtensorMap *map_b = &args.map_b[pi];
         int b, ti, tj;
-        decode_tile(args, t, b, ti, tj);
-        for (int kk = 0; kk < args.k_iters; ++kk) {
+        decode_tile(P, args.symmetric, t - P.tile_begin, b, ti, tj);
+        const int k_iters = P.k_iters;
+        for (int kk = 0; kk < k_iters; ++kk) {
           if (!wait_bounded(&ctrl->empty[stage], phase ^ 1u, ctl, ERR_WAIT_EMPTY)) {
             ok = false;
             break;
@@ -270,13 +424,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           last_parity[stage] = static_cast<int>(phase);
           uint8_t *sa = smem + stage * STAGE_BYTES;
           uint8_t *sb = sa + A_BYTES;
-          tma_load_3d(sa, &map_a, &ctrl->full[stage], kk * BK, ti * BM, b);
+          tma_load_3d(sa, map_a, &ctrl->full[stage], kk * BK, ti * BM, b);
           if constexpr (!B_MN) {
-            tma_load_3d(sb, &map_b, &ctrl->full[stage], kk * BK, tj * BN, b);
+            tma_load_3d(sb, map_b, &ctrl->full[stage], kk * BK, tj * BN, b);
           } else {
 #pragma unroll
             for (int c = 0; c < BN / 64; ++c)
-              tma_load_3d(sb + c * (64 * BK * 2), &map_b, &ctrl->full[stage], tj * BN + 64 * c, kk * BK, b);
+              tma_load_3d(sb + c * (64 * BK * 2), map_b, &ctrl->full[stage], tj * BN + 64 * c, kk * BK, b);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -285,16 +439,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       // every armed stage's copies have landed before the CTA may exit
-      for (int s = 0; s < STAGES; ++s) {
-        if (last_parity[s] < 0) continue;
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(&ctrl->full[s], static_cast<uint32_t>(last_parity[s]))) {
-          if (globaltimer_ns() - t0 > drain_ctl.timeout_ns) {
-            if (args.err) atomicCAS(args.err, 0u, ERR_WAIT_DRAIN);
-            break;
-          }
-        }
-      }
+      for (int s = 0; s < STAGES; ++s)
+        if (last_parity[s] >= 0) drain_wait(&ctrl->full[s], static_cast<uint32_t>(last_parity[s]), ctl);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -307,7 +453,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!wait_bounded(&ctrl->acc_empty[acc], acc_phase ^ 1u, ctl, ERR_WAIT_ACC_EMPTY)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-        for (int kk = 0; kk < args.k_iters; ++kk) {
+        const int k_iters = args.prob[find_problem(args, t)].k_iters;
+        for (int kk = 0; kk < k_iters; ++kk) {
           if (!wait_bounded(&ctrl->full[stage], phase, ctl, ERR_WAIT_FULL)) {
             ok = false;
             break;
@@ -337,39 +484,115 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // all MMAs this thread issued have completed before TMEM is released
       if (issued) {
         tc_commit(&ctrl->drain);
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(&ctrl->drain, 0)) {
-          if (globaltimer_ns() - t0 > drain_ctl.timeout_ns) {
-            if (args.err) atomicCAS(args.err, 0u, ERR_WAIT_DRAIN);
-            break;
+        drain_wait(&ctrl->drain, 0u, ctl);
+      }
+    }
+  } else if (warp == 6) {
+    if constexpr (EPI != EPI_GRAM) {
+      if (lane == 0) {
+        // ---------------------------------------------------------------- epilogue loader
+        uint32_t slot = 0, rphase = 0;
+        int last_parity[RING_SLOTS];
+        for (int s = 0; s < RING_SLOTS; ++s) last_parity[s] = -1;
+        bool ok = true;
+        for (long long t = blockIdx.x; ok && t < args.total_tiles; t += gridDim.x) {
+          const int pi = find_problem(args, t);
+          const GemmProblem P = args.prob[pi];
+          // POLY reads G through the A-operand map (box 64 x 128); APPLY / FINAL read X through the N-major
+          // B-operand map (box 64 x 64, two loads)
+          const CUtensorMap *aux_map = (EPI == EPI_POLY) ? &args.map_a[pi] : &args.map_b[pi];
+          int b, ti, tj;
+          decode_tile(P, args.symmetric, t - P.tile_begin, b, ti, tj);
+          const int row0 = ti * BM;
+          for (int s = 0; s < BN / 64; ++s) {
+            const int c0 = tj * BN + 64 * s;
+            if (c0 >= P.cols) break;
+            if (!slot_used(args.symmetric, c0, row0)) continue;
+            if (!wait_bounded(&ctrl->ring_empty[slot], rphase ^ 1u, ctl, ERR_WAIT_RING_EMPTY)) {
+              ok = false;
+              break;
+            }
+            uint8_t *dst = ring + slot * SLOT_BYTES;
+            uint32_t pbytes = 0;
+            const void *pbase = nullptr;
+            if constexpr (EPI == EPI_FINAL) pbytes = stage_params_bytes(P, b, row0, c0, pbase);
+            ctrl->ring_param_ok[slot] = pbytes != 0;
+            mbar_arrive_expect_tx(&ctrl->ring_full[slot], RING_AUX_BYTES + pbytes);
+            last_parity[slot] = static_cast<int>(rphase);
+            if constexpr (EPI == EPI_POLY) {
+              tma_load_3d(dst, aux_map, &ctrl->ring_full[slot], c0, row0, b);
+            } else {
+              tma_load_3d(dst, aux_map, &ctrl->ring_full[slot], c0, row0, b);
+              tma_load_3d(dst + 64 * 128, aux_map, &ctrl->ring_full[slot], c0, row0 + 64, b);
+            }
+            if constexpr (EPI == EPI_FINAL) {
+              if (pbytes) stage_params_issue(P, pbase, row0, c0, dst + RING_AUX_BYTES, &ctrl->ring_full[slot]);
+            }
+            if (++slot == RING_SLOTS) {
+              slot = 0;
+              rphase ^= 1u;
+            }
           }
         }
+        for (int s = 0; s < RING_SLOTS; ++s)
+          if (last_parity[s] >= 0) drain_wait(&ctrl->ring_full[s], static_cast<uint32_t>(last_parity[s]), ctl);
       }
     }
   } else {
     // ---------------------------------------------------------------- epilogue (warps 2..5)
     const int lane_base = (warp % 4) * 32;  // TMEM lanes this warp may read
-    uint32_t acc = 0, acc_phase = 0;
+    const int rloc = lane_base + lane;      // this thread's row within the tile
+    uint32_t acc = 0, acc_phase = 0, slot = 0, rphase = 0;
     for (long long t = blockIdx.x; t < args.total_tiles; t += gridDim.x) {
+      // by value: epilogue stores could alias a reference into parameter space and force reloads
+      const GemmProblem P = args.prob[find_problem(args, t)];
       int b, ti, tj;
-      decode_tile(args, t, b, ti, tj);
+      decode_tile(P, args.symmetric, t - P.tile_begin, b, ti, tj);
       // every lane waits; the warp proceeds only if all of them saw the accumulator complete, so the
       // warp-collective TMEM loads below never run with part of the warp gone
-      const bool ok = wait_bounded(&ctrl->acc_full[acc], acc_phase, ctl, ERR_WAIT_ACC_FULL);
+      bool ok = wait_bounded(&ctrl->acc_full[acc], acc_phase, ctl, ERR_WAIT_ACC_FULL);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const int row = ti * BM + lane_base + lane;
-      const int warp_row0 = ti * BM + lane_base;
+      const int row0 = ti * BM;
+      const int row = row0 + rloc;
+      const int warp_row0 = row0 + lane_base;
+      bool aborted = false;
 #pragma unroll 1
-      for (int ch = 0; ch < BN / 32; ++ch) {
-        const int col0 = tj * BN + ch * 32;
-        if (col0 >= args.cols) break;                                    // warp-uniform
-        if (args.symmetric && col0 + 31 < warp_row0) continue;           // chunk below the diagonal for every lane
-        if (warp_row0 >= args.rows) break;                               // whole warp past the last row
-        float v[32];
-        tmem_ld_32x32b_x32(tmem_base + acc * ACC_COLS + (static_cast<uint32_t>(lane_base) << 16) + ch * 32, v);
-        epilogue_chunk<EPI>(args, b, row, col0, v);
+      for (int s = 0; s < BN / 64; ++s) {
+        const int c0 = tj * BN + 64 * s;
+        if (c0 >= P.cols) break;
+        if (EPI != EPI_GRAM && !slot_used(args.symmetric, c0, row0)) continue;
+        const uint8_t *slot_ptr = ring + slot * SLOT_BYTES;
+        bool staged = false;
+        if constexpr (EPI != EPI_GRAM) {
+          ok = wait_bounded(&ctrl->ring_full[slot], rphase, ctl, ERR_WAIT_RING_FULL);
+          if (!__all_sync(0xffffffffu, ok)) {
+            aborted = true;
+            break;
+          }
+          staged = ctrl->ring_param_ok[slot] != 0;
+        }
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          const int col0 = c0 + 32 * half;
+          if (col0 >= P.cols) break;                                     // warp-uniform
+          if (args.symmetric && col0 + 31 < warp_row0) continue;         // chunk below the diagonal for every lane
+          if (warp_row0 >= P.rows) break;                                // whole warp past the last row
+          float v[32];
+          tmem_ld_32x32b_x32(tmem_base + acc * ACC_COLS + (static_cast<uint32_t>(lane_base) << 16) + (col0 - tj * BN),
+                             v);
+          epilogue_chunk<EPI>(P, b, row, rloc, col0, half, slot_ptr, slot_ptr + RING_AUX_BYTES, staged, v);
+        }
+        if constexpr (EPI != EPI_GRAM) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctrl->ring_empty[slot]);
+          if (++slot == RING_SLOTS) {
+            slot = 0;
+            rphase ^= 1u;
+          }
+        }
       }
+      if (aborted) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctrl->acc_empty[acc]);
@@ -422,31 +645,39 @@ bool make_map(CUtensorMap *map, const void *base, long long inner, long long row
 }
 
 template <int EPI, bool B_MN>
-muon_status launch_kernel(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &args, int32_t kind,
-                          cudaStream_t s) {
+muon_status launch_group(const GemmGroup &g, int32_t kind, cudaStream_t s) {
   static std::once_flag attr_once[64];
   int dev = 0;
   cudaGetDevice(&dev);
   std::call_once(attr_once[dev & 63], [] {
     cudaFuncSetAttribute(ns_gemm_kernel<EPI, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(SMEM_BYTES));
+                         static_cast<int>(smem_bytes(EPI)));
   });
-  if (args.total_tiles <= 0) return MUON_OK;
+  if (g.total_tiles <= 0) return MUON_OK;
   const long long sms = device_sm_count();
-  const int grid = static_cast<int>(args.total_tiles < sms ? args.total_tiles : sms);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(g.total_tiles < sms ? g.total_tiles : sms));
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem_bytes(EPI);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   launch_begin(kind, s);
-  ns_gemm_kernel<EPI, B_MN><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ma, mb, args);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<EPI, B_MN>, g);
   launch_end(s);
-  return cudaGetLastError() == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+  return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
 }
 
-void fill_tiles(GemmArgs &a, int batch, int rows, int cols, int contraction, bool symmetric) {
-  a.batch = batch;
-  a.rows = rows;
-  a.cols = cols;
-  a.m_tiles = (rows + BM - 1) / BM;
-  a.n_tiles = (cols + BN - 1) / BN;
-  a.symmetric = symmetric ? 1 : 0;
+void fill_tiles(GemmProblem &a, long long batch, long long rows, long long cols, long long contraction,
+                bool symmetric) {
+  a.batch = static_cast<int>(batch);
+  a.rows = static_cast<int>(rows);
+  a.cols = static_cast<int>(cols);
+  a.m_tiles = static_cast<int>((rows + BM - 1) / BM);
+  a.n_tiles = static_cast<int>((cols + BN - 1) / BN);
   if (symmetric) {
     int cnt = 0;
     for (int j = 0; j < a.n_tiles; ++j) cnt += (a.m_tiles < 2 * j + 2 ? a.m_tiles : 2 * j + 2);
@@ -454,105 +685,174 @@ void fill_tiles(GemmArgs &a, int batch, int rows, int cols, int contraction, boo
   } else {
     a.tiles_per_matrix = a.m_tiles * a.n_tiles;
   }
-  a.total_tiles = static_cast<long long>(a.tiles_per_matrix) * batch;
-  a.k_iters = (contraction + BK - 1) / BK;
+  a.k_iters = static_cast<int>((contraction + BK - 1) / BK);
 }
 
-}  // namespace
-
-muon_status launch_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long ldg, long long mstride_g, float alpha,
-                        const float *scale, uint32_t *err, unsigned long long timeout_ns, cudaStream_t s) {
-  CUtensorMap ma, mb;
-  if (!make_map(&ma, x.ptr, x.cols, x.rows, x.batch, x.ld, x.mstride, BM) ||
-      !make_map(&mb, x.ptr, x.cols, x.rows, x.batch, x.ld, x.mstride, BN))
-    return MUON_ERR_CUDA;
-  GemmArgs a{};
-  fill_tiles(a, static_cast<int>(x.batch), static_cast<int>(x.rows), static_cast<int>(x.rows),
-             static_cast<int>(x.cols), true);
-  a.alpha = alpha;
-  a.scale = scale;
-  a.scale_pow = 2;
-  a.out = g;
-  a.ld_out = ldg;
-  a.mstride_out = mstride_g;
-  a.err = err;
-  a.timeout_ns = timeout_ns;
-  return launch_kernel<EPI_GRAM, false>(ma, mb, a, KK_GRAM, s);
-}
-
-muon_status launch_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float b, float c,
-                        uint32_t *err, unsigned long long timeout_ns, cudaStream_t s) {
-  CUtensorMap ma, mb;
-  if (!make_map(&ma, g.ptr, g.cols, g.rows, g.batch, g.ld, g.mstride, BM) ||
-      !make_map(&mb, g.ptr, g.cols, g.rows, g.batch, g.ld, g.mstride, BN))
-    return MUON_ERR_CUDA;
-  GemmArgs a{};
-  fill_tiles(a, static_cast<int>(g.batch), static_cast<int>(g.rows), static_cast<int>(g.rows),
-             static_cast<int>(g.cols), true);
-  a.alpha = 1.f;
-  a.coef_b = b;
-  a.coef_c = c;
-  a.out = h;
-  a.ld_out = ldh;
-  a.mstride_out = mstride_h;
-  a.aux = static_cast<const __nv_bfloat16 *>(g.ptr);
-  a.ld_aux = g.ld;
-  a.mstride_aux = g.mstride;
-  a.err = err;
-  a.timeout_ns = timeout_ns;
-  return launch_kernel<EPI_POLY, false>(ma, mb, a, KK_POLY, s);
-}
-
-static bool apply_maps(const Bf16Stack &h, const Bf16Stack &x, CUtensorMap *ma, CUtensorMap *mb) {
+bool apply_maps(const Bf16Stack &h, const Bf16Stack &x, CUtensorMap *ma, CUtensorMap *mb) {
   return make_map(ma, h.ptr, h.cols, h.rows, h.batch, h.ld, h.mstride, BM) &&
          make_map(mb, x.ptr, x.cols, x.rows, x.batch, x.ld, x.mstride, BK);
 }
 
-muon_status launch_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, float a_coef,
-                         const float *scale, uint32_t *err, unsigned long long timeout_ns, cudaStream_t s) {
+}  // namespace
+
+struct GemmBatch::Item {
   CUtensorMap ma, mb;
-  if (!apply_maps(h, x, &ma, &mb)) return MUON_ERR_CUDA;
-  GemmArgs a{};
-  fill_tiles(a, static_cast<int>(x.batch), static_cast<int>(x.rows), static_cast<int>(x.cols),
-             static_cast<int>(h.cols), false);
-  a.coef_a = a_coef;
-  a.scale = scale;
-  a.scale_pow = 1;
-  a.out = out;
-  a.ld_out = x.ld;
-  a.mstride_out = x.mstride;
-  a.aux = static_cast<const __nv_bfloat16 *>(x.ptr);
-  a.ld_aux = x.ld;
-  a.mstride_aux = x.mstride;
-  a.err = err;
-  a.timeout_ns = timeout_ns;
-  return launch_kernel<EPI_APPLY, true>(ma, mb, a, KK_APPLY, s);
+  GemmProblem p;
+};
+
+GemmBatch::~GemmBatch() { delete[] items_; }
+
+muon_status GemmBatch::push(const Item &it) {
+  if (n_ == cap_) {
+    const int nc = cap_ ? 2 * cap_ : GEMM_MAX_PROBLEMS;
+    Item *ni = new Item[nc];
+    for (int i = 0; i < n_; ++i) ni[i] = items_[i];
+    delete[] items_;
+    items_ = ni;
+    cap_ = nc;
+  }
+  items_[n_++] = it;
+  return MUON_OK;
 }
 
-muon_status launch_final(const Bf16Stack &h, const Bf16Stack &x, float a_coef, const float *scale, const FinalSpec &f,
+muon_status GemmBatch::add_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long ldg, long long mstride_g, float alpha,
+                                const float *scale) {
+  if (epi_ != EPI_GRAM) return MUON_ERR_INVALID_ARG;
+  Item it{};
+  if (!make_map(&it.ma, x.ptr, x.cols, x.rows, x.batch, x.ld, x.mstride, BM) ||
+      !make_map(&it.mb, x.ptr, x.cols, x.rows, x.batch, x.ld, x.mstride, BN))
+    return MUON_ERR_CUDA;
+  fill_tiles(it.p, x.batch, x.rows, x.rows, x.cols, true);
+  it.p.alpha = alpha;
+  it.p.scale = scale;
+  it.p.out = g;
+  it.p.ld_out = ldg;
+  it.p.mstride_out = mstride_g;
+  return push(it);
+}
+
+muon_status GemmBatch::add_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float b,
+                                float c) {
+  if (epi_ != EPI_POLY) return MUON_ERR_INVALID_ARG;
+  Item it{};
+  if (!make_map(&it.ma, g.ptr, g.cols, g.rows, g.batch, g.ld, g.mstride, BM) ||
+      !make_map(&it.mb, g.ptr, g.cols, g.rows, g.batch, g.ld, g.mstride, BN))
+    return MUON_ERR_CUDA;
+  fill_tiles(it.p, g.batch, g.rows, g.rows, g.cols, true);
+  it.p.alpha = 1.f;
+  it.p.coef_b = b;
+  it.p.coef_c = c;
+  it.p.out = h;
+  it.p.ld_out = ldh;
+  it.p.mstride_out = mstride_h;
+  it.p.aux = static_cast<const __nv_bfloat16 *>(g.ptr);
+  it.p.ld_aux = g.ld;
+  it.p.mstride_aux = g.mstride;
+  return push(it);
+}
+
+muon_status GemmBatch::add_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, float a,
+                                 const float *scale) {
+  if (epi_ != EPI_APPLY) return MUON_ERR_INVALID_ARG;
+  Item it{};
+  if (!apply_maps(h, x, &it.ma, &it.mb)) return MUON_ERR_CUDA;
+  fill_tiles(it.p, x.batch, x.rows, x.cols, h.cols, false);
+  it.p.coef_a = a;
+  it.p.scale = scale;
+  it.p.out = out;
+  it.p.ld_out = x.ld;
+  it.p.mstride_out = x.mstride;
+  it.p.aux = static_cast<const __nv_bfloat16 *>(x.ptr);
+  it.p.ld_aux = x.ld;
+  it.p.mstride_aux = x.mstride;
+  return push(it);
+}
+
+muon_status GemmBatch::add_final(const Bf16Stack &h, const Bf16Stack &x, float a, const float *scale,
+                                 const FinalSpec &f) {
+  if (epi_ != EPI_FINAL) return MUON_ERR_INVALID_ARG;
+  Item it{};
+  if (!apply_maps(h, x, &it.ma, &it.mb)) return MUON_ERR_CUDA;
+  fill_tiles(it.p, x.batch, x.rows, x.cols, h.cols, false);
+  it.p.coef_a = a;
+  it.p.scale = scale;
+  it.p.aux = static_cast<const __nv_bfloat16 *>(x.ptr);
+  it.p.ld_aux = x.ld;
+  it.p.mstride_aux = x.mstride;
+  it.p.params = f.params;
+  it.p.out_dense = f.out_dense;
+  it.p.out_dtype = f.dtype;
+  it.p.transposed = f.transposed;
+  it.p.orig_cols = f.orig_cols;
+  it.p.cautious = f.cautious;
+  it.p.lr_wd = f.lr_wd;
+  it.p.lr_scale = f.lr_scale;
+  return push(it);
+}
+
+muon_status GemmBatch::launch(cudaStream_t s) {
+  // deepest contraction first, so that the longest tiles start in the first wave of the persistent CTAs
+  for (int i = 1; i < n_; ++i)
+    for (int j = i; j > 0 && items_[j].p.k_iters > items_[j - 1].p.k_iters; --j) {
+      Item t = items_[j];
+      items_[j] = items_[j - 1];
+      items_[j - 1] = t;
+    }
+  for (int first = 0; first < n_; first += GEMM_MAX_PROBLEMS) {
+    const int cnt = (n_ - first) < GEMM_MAX_PROBLEMS ? (n_ - first) : GEMM_MAX_PROBLEMS;
+    GemmGroup g;
+    memset(&g, 0, sizeof(g));
+    long long tiles = 0;
+    for (int i = 0; i < cnt; ++i) {
+      g.map_a[i] = items_[first + i].ma;
+      g.map_b[i] = items_[first + i].mb;
+      g.prob[i] = items_[first + i].p;
+      g.prob[i].tile_begin = tiles;
+      tiles += static_cast<long long>(g.prob[i].tiles_per_matrix) * g.prob[i].batch;
+    }
+    g.nprob = cnt;
+    g.symmetric = (epi_ == EPI_GRAM || epi_ == EPI_POLY) ? 1 : 0;
+    g.total_tiles = tiles;
+    g.err = err_;
+    g.timeout_ns = timeout_ns_;
+    muon_status st;
+    switch (epi_) {
+      case EPI_GRAM: st = launch_group<EPI_GRAM, false>(g, KK_GRAM, s); break;
+      case EPI_POLY: st = launch_group<EPI_POLY, false>(g, KK_POLY, s); break;
+      case EPI_APPLY: st = launch_group<EPI_APPLY, true>(g, KK_APPLY, s); break;
+      default: st = launch_group<EPI_FINAL, true>(g, KK_FINAL, s); break;
+    }
+    if (st != MUON_OK) return st;
+  }
+  return MUON_OK;
+}
+
+muon_status launch_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long ldg, long long mstride_g, float alpha,
+                        const float *scale, uint32_t *err, unsigned long long timeout_ns, cudaStream_t s) {
+  GemmBatch bt(EPI_GRAM, err, timeout_ns);
+  muon_status st = bt.add_gram(x, g, ldg, mstride_g, alpha, scale);
+  return st != MUON_OK ? st : bt.launch(s);
+}
+
+muon_status launch_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float b, float c,
+                        uint32_t *err, unsigned long long timeout_ns, cudaStream_t s) {
+  GemmBatch bt(EPI_POLY, err, timeout_ns);
+  muon_status st = bt.add_poly(g, h, ldh, mstride_h, b, c);
+  return st != MUON_OK ? st : bt.launch(s);
+}
+
+muon_status launch_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, float a, const float *scale,
                          uint32_t *err, unsigned long long timeout_ns, cudaStream_t s) {
-  CUtensorMap ma, mb;
-  if (!apply_maps(h, x, &ma, &mb)) return MUON_ERR_CUDA;
-  GemmArgs a{};
-  fill_tiles(a, static_cast<int>(x.batch), static_cast<int>(x.rows), static_cast<int>(x.cols),
-             static_cast<int>(h.cols), false);
-  a.coef_a = a_coef;
-  a.scale = scale;
-  a.scale_pow = 1;
-  a.aux = static_cast<const __nv_bfloat16 *>(x.ptr);
-  a.ld_aux = x.ld;
-  a.mstride_aux = x.mstride;
-  a.params = f.params;
-  a.out_dense = f.out_dense;
-  a.out_dtype = f.dtype;
-  a.transposed = f.transposed;
-  a.orig_cols = f.orig_cols;
-  a.cautious = f.cautious;
-  a.lr_wd = f.lr_wd;
-  a.lr_scale = f.lr_scale;
-  a.err = err;
-  a.timeout_ns = timeout_ns;
-  return launch_kernel<EPI_FINAL, true>(ma, mb, a, KK_FINAL, s);
+  GemmBatch bt(EPI_APPLY, err, timeout_ns);
+  muon_status st = bt.add_apply(h, x, out, a, scale);
+  return st != MUON_OK ? st : bt.launch(s);
+}
+
+muon_status launch_final(const Bf16Stack &h, const Bf16Stack &x, float a, const float *scale, const FinalSpec &f,
+                         uint32_t *err, unsigned long long timeout_ns, cudaStream_t s) {
+  GemmBatch bt(EPI_FINAL, err, timeout_ns);
+  muon_status st = bt.add_final(h, x, a, scale, f);
+  return st != MUON_OK ? st : bt.launch(s);
 }
 
 }  // namespace muon

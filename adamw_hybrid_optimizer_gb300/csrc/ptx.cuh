@@ -16,6 +16,8 @@ enum : uint32_t {
   ERR_WAIT_ACC_FULL = 0x103,  // epilogue waiting for an accumulator
   ERR_WAIT_ACC_EMPTY = 0x104, // MMA issuer waiting for the epilogue to drain an accumulator
   ERR_WAIT_DRAIN = 0x105,     // teardown waiting for in-flight copies / MMAs
+  ERR_WAIT_RING_FULL = 0x106, // epilogue waiting for its staged second input
+  ERR_WAIT_RING_EMPTY = 0x107,// epilogue loader waiting for a free ring slot
   ERR_WAIT_DEBUG = 0x1FF,     // the deliberate never-completing wait
 };
 
@@ -28,6 +30,14 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+
+// ------------------------------------------------------------------------------------------ dependent launch
+
+// Kernels are launched with programmatic stream serialization: a kernel may start while the previous
+// one in the stream is finishing. Every kernel waits here before it touches global memory that
+// earlier work writes, and signals early that the next kernel may be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ------------------------------------------------------------------------------------------ mbarrier
 
@@ -84,6 +94,18 @@ __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, con
   }
 }
 
+// Teardown: waits (bounded, ignoring the abort flag) until the phase with this parity has completed, so
+// that no copy or MMA is still writing shared or tensor memory when the CTA releases it.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, const WaitCtl &ctl) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > ctl.timeout_ns) {
+      if (ctl.err) atomicCAS(ctl.err, 0u, static_cast<uint32_t>(ERR_WAIT_DRAIN));
+      break;
+    }
+  }
+}
+
 // ------------------------------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
@@ -98,6 +120,14 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *m
       "[%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+
+// 1-D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16), completing tx bytes on bar.
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(smem_dst)),
+               "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 
 // ------------------------------------------------------------------------------------------ tcgen05

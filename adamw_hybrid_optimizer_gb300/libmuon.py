@@ -44,10 +44,19 @@ class adamw_hparams(ctypes.Structure):
                 ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("step", ctypes.c_int64)]
 
 
+class muon_bucket(ctypes.Structure):
+    _fields_ = [("params", ctypes.c_void_p), ("grads", ctypes.c_void_p), ("momentum", ctypes.c_void_p),
+                ("K", ctypes.c_int64), ("A", ctypes.c_int64), ("B", ctypes.c_int64), ("pdt", ctypes.c_int),
+                ("gdt", ctypes.c_int)]
+
+
 SIGNATURES = {
     "muon_workspace_bytes": (ctypes.c_size_t, [_c_int64, _c_int64, _c_int64]),
     "muon_step_batched": (ctypes.c_int, [_vp, ctypes.c_int, _vp, ctypes.c_int, _vp, _c_int64, _c_int64, _c_int64,
                                          ctypes.POINTER(muon_hparams), _vp, ctypes.c_size_t, _vp]),
+    "muon_workspace_bytes_grouped": (ctypes.c_size_t, [ctypes.POINTER(muon_bucket), ctypes.c_int]),
+    "muon_step_grouped": (ctypes.c_int, [ctypes.POINTER(muon_bucket), ctypes.c_int, ctypes.POINTER(muon_hparams), _vp,
+                                         ctypes.c_size_t, _vp]),
     "ns_orthogonalize": (ctypes.c_int, [_vp, ctypes.c_int, _vp, ctypes.c_int, _c_int64, _c_int64, _c_int64,
                                         ctypes.c_int, ctypes.POINTER(ctypes.c_float), ctypes.c_float, _vp,
                                         ctypes.c_size_t, _vp]),
@@ -148,6 +157,25 @@ def muon_step_batched(param_ptrs, pdt: int, grad_ptrs, gdt: int, momentum, K: in
     st = lib().muon_step_batched(param_ptrs.data_ptr(), pdt, grad_ptrs.data_ptr(), gdt, momentum.data_ptr(), K, A, B,
                                  ctypes.byref(hp), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream))
     _check(st, "muon_step_batched")
+
+
+def make_buckets(specs):
+    """specs: sequence of (param_ptrs, grad_ptrs, momentum, K, A, B, pdt, gdt); returns a ctypes muon_bucket array."""
+    arr = (muon_bucket * len(specs))()
+    for i, (pp, gp, mom, K, A, B, pdt, gdt) in enumerate(specs):
+        arr[i] = muon_bucket(pp.data_ptr(), gp.data_ptr(), mom.data_ptr(), K, A, B, pdt, gdt)
+    return arr
+
+
+def muon_workspace_bytes_grouped(buckets) -> int:
+    return int(lib().muon_workspace_bytes_grouped(buckets, len(buckets)))
+
+
+def muon_step_grouped(buckets, hp: muon_hparams, ws, stream=None):
+    """buckets: a ctypes muon_bucket array (see make_buckets)."""
+    st = lib().muon_step_grouped(buckets, len(buckets), ctypes.byref(hp), ws.data_ptr(),
+                                 ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "muon_step_grouped")
 
 
 def pointer_array(tensors, device):

@@ -57,7 +57,6 @@ class Workload:
         self.w = w
         plan = L.muon_plan_buckets(workloads.shape_list(w))
         self.buckets = []
-        ws_bytes = 0
         for b, (shape, K) in enumerate(zip(plan["bucket_shapes"], plan["bucket_K"])):
             A, B = shape
             members = [i for i, bid in enumerate(plan["bucket_id"]) if bid == b]
@@ -71,8 +70,9 @@ class Workload:
             self.buckets.append(dict(K=K, A=A, B=B, p=p, g=g, mom=mom,
                                      pptr=L.pointer_array([p[k] for k in range(K)], device),
                                      gptr=L.pointer_array([g[k] for k in range(K)], device)))
-            ws_bytes = max(ws_bytes, L.muon_workspace_bytes(K, A, B))
-        self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
+        self.bucket_array = L.make_buckets([(bk["pptr"], bk["gptr"], bk["mom"], bk["K"], bk["A"], bk["B"],
+                                             L.MUON_BF16, L.MUON_BF16) for bk in self.buckets])
+        self.ws = torch.zeros(L.muon_workspace_bytes_grouped(self.bucket_array), dtype=torch.uint8, device=device)
         self.hp = L.make_muon_hparams(w.muon_hp.lr, w.muon_hp.momentum, w.muon_hp.weight_decay, w.muon_hp.nesterov,
                                       w.muon_hp.cautious_wd, w.muon_hp.scale_mode, w.muon_hp.coeffs, w.muon_hp.eps)
         # AdamW: one flat buffer per weight-decay value (embedding + head; the LayerNorm vectors)
@@ -96,9 +96,7 @@ class Workload:
     def step(self, stream=None):
         L = self.L
         self.t += 1
-        for bk in self.buckets:
-            L.muon_step_batched(bk["pptr"], L.MUON_BF16, bk["gptr"], L.MUON_BF16, bk["mom"], bk["K"], bk["A"], bk["B"],
-                                self.hp, self.ws, stream)
+        L.muon_step_grouped(self.bucket_array, self.hp, self.ws, stream)
         a = self.w.adamw_hp
         for buf in self.adamw:
             L.adamw_step(buf["p"], buf["g"], buf["m"], buf["v"], a.lr, a.beta1, a.beta2, a.eps, buf["wd"], self.t,
@@ -322,7 +320,9 @@ def run_ours(args):
         d[1] += 1
     flops, nominal, bytes_ = wl.work()
     tot = {k: v[0] / args.steps for k, v in per_kind.items()}          # ms per step per kind
-    dominant = max(tot, key=tot.get)
+    # the dominant kernel among those with an algorithmic work model (the GEMMs, the two bandwidth passes)
+    modelled = [k for k in tot if k in flops or k in bytes_]
+    dominant = max(modelled, key=tot.get)
     launches_per_step = {k: v[1] / args.steps for k, v in per_kind.items()}
     ns_ms = sum(tot.get(k, 0.0) for k in ("ns_gram", "ns_poly", "ns_apply", "ns_final"))
     peak_tf = peaks["bf16_tflops"]
@@ -427,6 +427,62 @@ def _traffic_from_profiles(kernel):
     return v if isinstance(v, (int, float)) else None
 
 
+def run_ns_sweep(args):
+    """Newton-Schulz sweep: K=64 square bf16 stacks, 5 classic steps, one JSON line per size (not the bench line)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from adamw_hybrid_optimizer_gb300 import libmuon as L
+    import workloads
+    peaks, peak_src = load_peaks()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    coeffs = [workloads.CLASSIC_QUINTIC] * 5
+    K = workloads.NS_SWEEP_K
+    sizes = [int(v) for v in args.sizes.split(",")] if args.sizes else list(workloads.NS_SWEEP_SIZES)
+    for n in sizes:
+        x = workloads.ns_sweep_input(n, K, 0, device="cuda:0")
+        out = torch.empty_like(x)
+        ws = torch.empty(L.muon_workspace_bytes(K, n, n), dtype=torch.uint8, device=dev)
+        reps = 3 if n >= 4096 else 10
+        for _ in range(2):
+            L.ns_orthogonalize(x, out, coeffs, 1e-7, ws)
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(reps):
+            L.ns_orthogonalize(x, out, coeffs, 1e-7, ws)
+        s1.record()
+        torch.cuda.synchronize()
+        ms = s0.elapsed_time(s1) / reps
+        L.muon_trace_enable(True)
+        L.ns_orthogonalize(x, out, coeffs, 1e-7, ws)
+        torch.cuda.synchronize()
+        L.muon_trace_enable(False)
+        per = {}
+        for kind, t in L.muon_trace_collect():
+            per[kind] = per.get(kind, 0.0) + t
+        if L.muon_check(ws) != L.MUON_OK:
+            raise RuntimeError("device wait ran out in the sweep")
+        nominal = 5 * K * 6.0 * n ** 3
+        work = {"ns_gram": 5 * K * n ** 3, "ns_poly": 5 * K * n ** 3, "ns_apply": 4 * K * 2.0 * n ** 3,
+                "ns_final": K * 2.0 * n ** 3}
+        kern = {k: {"ms": round(per[k], 3), "tflops": round(work[k] / (per[k] * 1e-3) / 1e12, 1),
+                    "frac": round(work[k] / (per[k] * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
+                for k in work if k in per}
+        mma_ms = sum(per.get(k, 0.0) for k in work)
+        issued = sum(work.values())
+        print(json.dumps({"sweep": "ns_orthogonalize", "n": n, "K": K, "ms": round(ms, 3),
+                          "tflops_nominal": round(nominal / (ms * 1e-3) / 1e12, 1),
+                          "frac_nominal": round(nominal / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                          "tflops_gemm_kernels": round(issued / (mma_ms * 1e-3) / 1e12, 1),
+                          "frac_gemm_kernels": round(issued / (mma_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                          "kernels": kern, "peak": f"{peaks['bf16_tflops']} TFLOP/s {peak_src} burst"}), flush=True)
+        del x, out, ws
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -434,7 +490,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ns-sweep", action="store_true", help="Newton-Schulz size sweep instead of the bench line")
+    ap.add_argument("--sizes", default="", help="comma-separated n for --ns-sweep")
     args = ap.parse_args()
+    if args.ns_sweep:
+        return run_ns_sweep(args)
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":

@@ -96,6 +96,30 @@ muon_status muon_step_batched(void *const *params, muon_dtype pdt, const void *c
                               float *momentum, int64_t K, int64_t A, int64_t B, const muon_hparams *hp, void *ws,
                               size_t ws_bytes, muon_stream_t stream);
 
+/* One same-shape stack of Muon matrices for muon_step_grouped (the arguments muon_step_batched takes). */
+typedef struct {
+  void *const *params;        /* DEVICE array of K device pointers, each an A x B row-major matrix of pdt */
+  const void *const *grads;   /* DEVICE array of K device pointers, each an A x B row-major matrix of gdt */
+  float *momentum;            /* device fp32 (K, A, B), updated in place */
+  int64_t K, A, B;
+  muon_dtype pdt, gdt;
+} muon_bucket;
+
+/* Workspace bytes for muon_step_grouped: the sum over buckets of muon_workspace_bytes(K, A, B).
+ * Returns 0 if n < 1, buckets is null or a dimension is not positive. */
+size_t muon_workspace_bytes_grouped(const muon_bucket *buckets, int n);
+
+/* One Muon step on n same-shape stacks at once, all with the same hyperparameters: the computation of
+ * muon_step_batched on each bucket, with every Newton-Schulz step kind of all buckets issued as one
+ * grouped tensor-core launch ([P4] section 2.2, batching matrices of similar shapes; [P1] the stacked
+ * (K, ...) Muon groups). Results are identical to n muon_step_batched calls.
+ *   buckets   HOST array of n bucket descriptors (1 <= n <= 4096).
+ *   ws        device workspace of ws_bytes >= muon_workspace_bytes_grouped(buckets, n), 256-byte aligned;
+ *             its first 256 bytes are the control block muon_check reads.
+ * Errors as for muon_step_batched, checked for every bucket before anything is launched. */
+muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hparams *hp, void *ws, size_t ws_bytes,
+                              muon_stream_t stream);
+
 /* Newton-Schulz orthogonalisation of a stack, [P2] "Muon: orthogonalising the update" (newton_schulz):
  * out_k = NS(x_k) for k < K, with normalisation by ||x_k||_F + eps and transpose-to-wide.
  *   x    device, contiguous (K, A, B) of xdt (MUON_F32 or MUON_BF16).

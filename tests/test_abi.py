@@ -154,3 +154,24 @@ def test_other_entry_point_checks():
 def test_launch_counter_starts_at_zero_without_launches():
     assert L.muon_launch_count() >= 0
     assert L.muon_trace_collect() == []
+
+
+def test_grouped_entry_point_checks():
+    lib = L.lib()
+    hp = L.make_muon_hparams(0.02, 0.95, 0.01)
+    good = (L.muon_bucket * 2)(L.muon_bucket(FAKE, FAKE, FAKE, 4, 64, 128, 0, 0),
+                               L.muon_bucket(FAKE, FAKE, FAKE, 2, 128, 64, 1, 1))
+    need = L.muon_workspace_bytes_grouped(good)
+    assert need == L.muon_workspace_bytes(4, 64, 128) + L.muon_workspace_bytes(2, 128, 64)
+    st = lambda b, n=2, ws=FAKE, nb=need: lib.muon_step_grouped(b, n, ctypes.byref(hp), ws, nb, None)
+    assert st(good, n=0) == L.MUON_ERR_INVALID_ARG
+    assert st(good, ws=None) == L.MUON_ERR_INVALID_ARG
+    assert st(good, ws=FAKE + 8) == L.MUON_ERR_ALIGNMENT
+    assert st(good, nb=need - 1) == L.MUON_ERR_WORKSPACE
+    bad = (L.muon_bucket * 2)(good[0], L.muon_bucket(None, FAKE, FAKE, 2, 128, 64, 1, 1))
+    assert st(bad) == L.MUON_ERR_INVALID_ARG
+    bad = (L.muon_bucket * 2)(good[0], L.muon_bucket(FAKE, FAKE, FAKE, 2, 128, 0, 1, 1))
+    assert st(bad) == L.MUON_ERR_INVALID_ARG
+    bad = (L.muon_bucket * 2)(good[0], L.muon_bucket(FAKE, FAKE, FAKE, 2, 128, 64, 1, 9))
+    assert st(bad) == L.MUON_ERR_DTYPE
+    assert L.muon_workspace_bytes_grouped((L.muon_bucket * 1)(L.muon_bucket(FAKE, FAKE, FAKE, 0, 1, 1, 0, 0))) == 0

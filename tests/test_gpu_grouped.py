@@ -1,0 +1,106 @@
+"""muon_step_grouped: one grouped launch per Newton-Schulz step kind over several buckets.
+
+Grouping changes only which CTA computes which tile, never the arithmetic of a tile, so the result must
+equal, bit for bit, one muon_step_batched call per bucket on the same inputs (which the per-bucket tests
+compare with the oracle). Covered: the GPT-2-small set (4 buckets, one of them transposed), and ten
+buckets of distinct ragged shapes with fp32 and bf16 parameters (more than one launch per step kind).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle.buckets import plan_buckets
+from tests.gpu_common import DEV, build_lib, f64, hp_struct, rel_fro
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def L():
+    return build_lib()
+
+
+def _make(shapes, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    out = []
+    for (K, A, B) in shapes:
+        p = (torch.randn((K, A, B), generator=g) * 1e-3).to(dtype).to(DEV)
+        grads = [(torch.randn((K, A, B), generator=g) * 1e-3).to(dtype).to(DEV) for _ in range(2)]
+        out.append((p, grads))
+    return out
+
+
+def _run_both(L, shapes, dtype, hp, seed=0):
+    data = _make(shapes, dtype, seed)
+    code = L.MUON_F32 if dtype == torch.float32 else L.MUON_BF16
+    hps = hp_struct(L, hp)
+    # per-bucket reference: muon_step_batched
+    ref_p, ref_m = [], []
+    for (K, A, B), (p0, grads) in zip(shapes, data):
+        p = p0.clone()
+        mom = torch.zeros((K, A, B), dtype=torch.float32, device=DEV)
+        ws = torch.zeros(L.muon_workspace_bytes(K, A, B), dtype=torch.uint8, device=DEV)
+        pp = L.pointer_array([p[k] for k in range(K)], DEV)
+        for g in grads:
+            L.muon_step_batched(pp, code, L.pointer_array([g[k] for k in range(K)], DEV), code, mom, K, A, B, hps, ws)
+        assert L.muon_check(ws) == L.MUON_OK
+        ref_p.append(p)
+        ref_m.append(mom)
+    # grouped
+    ps = [p0.clone() for p0, _ in data]
+    moms = [torch.zeros(s, dtype=torch.float32, device=DEV) for s in shapes]
+    pptr = [L.pointer_array([p[k] for k in range(s[0])], DEV) for p, s in zip(ps, shapes)]
+    for step in range(2):
+        gptr = [L.pointer_array([g[step][k] for k in range(s[0])], DEV) for (_, g), s in zip(data, shapes)]
+        bk = L.make_buckets([(pp, gp, m, K, A, B, code, code) for pp, gp, m, (K, A, B) in zip(pptr, gptr, moms, shapes)])
+        ws = torch.zeros(L.muon_workspace_bytes_grouped(bk), dtype=torch.uint8, device=DEV)
+        L.muon_step_grouped(bk, hps, ws)
+        assert L.muon_check(ws) == L.MUON_OK
+    for i in range(len(shapes)):
+        assert torch.equal(ps[i], ref_p[i]), i
+        assert torch.equal(moms[i], ref_m[i]), i
+    return ps
+
+
+def test_grouped_equals_per_bucket_gpt2_small(L):
+    w = workloads.workload("gpt2s")
+    plan = plan_buckets(workloads.shape_list(w))
+    shapes = [(K, A, B) for (A, B), K in zip(plan["bucket_shapes"], plan["bucket_K"])]
+    _run_both(L, shapes, torch.bfloat16, w.muon_hp, seed=1)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_grouped_equals_per_bucket_ten_ragged_buckets(L, dtype):
+    shapes = [(3, 64, 128), (2, 136, 72), (1, 8, 24), (4, 200, 264), (2, 256, 256), (1, 520, 776),
+              (2, 40, 1), (3, 1, 96), (2, 384, 130), (1, 130, 384)]
+    hp = workloads.workload("tiny").muon_hp
+    ps = _run_both(L, shapes, dtype, hp, seed=2)
+    assert all(torch.isfinite(p.float()).all() for p in ps)
+
+
+def test_grouped_step_matches_oracle_on_one_sample(L):
+    """A direct oracle check on the grouped path too (first matrix of each GPT-2-small bucket, step 1)."""
+    from oracle import muon as omuon
+    w = workloads.workload("gpt2s")
+    hp = w.muon_hp
+    plan = plan_buckets(workloads.shape_list(w))
+    specs, keep = [], []
+    for b, ((A, B), K) in enumerate(zip(plan["bucket_shapes"], plan["bucket_K"])):
+        members = [i for i, bid in enumerate(plan["bucket_id"]) if bid == b]
+        p = torch.stack([workloads.muon_param_init(w, i) for i in members]).to(DEV)
+        g = torch.stack([workloads.muon_grad(w, 1, i) for i in members]).to(DEV)
+        m = torch.zeros((K, A, B), dtype=torch.float32, device=DEV)
+        keep.append((p, g, m, members, f64(p[0])))
+        specs.append((L.pointer_array([p[k] for k in range(K)], DEV), L.pointer_array([g[k] for k in range(K)], DEV),
+                      m, K, A, B, L.MUON_BF16, L.MUON_BF16))
+    bk = L.make_buckets(specs)
+    ws = torch.zeros(L.muon_workspace_bytes_grouped(bk), dtype=torch.uint8, device=DEV)
+    L.muon_step_grouped(bk, hp_struct(L, hp), ws)
+    assert L.muon_check(ws) == L.MUON_OK
+    for p, g, m, members, p0 in keep:
+        ref, _, _ = omuon.muon_update(p0, f64(g[0]), np.zeros_like(p0), lr=hp.lr, momentum=hp.momentum,
+                                      weight_decay=hp.weight_decay, nesterov=hp.nesterov, coeffs=hp.coeffs,
+                                      eps=hp.eps, param_dtype="bf16")
+        got = f64(p[0])
+        assert np.linalg.norm(got - ref) <= 2e-2 * np.linalg.norm(ref - p0) + 2 ** -8 * np.linalg.norm(ref)
