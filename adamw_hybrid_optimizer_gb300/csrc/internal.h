@@ -43,9 +43,10 @@ struct GemmProblem {
   int rows;
   int cols;
   int m_tiles, n_tiles;
-  int tiles_per_matrix;
+  int m_pairs;            // tile rows are processed in vertically adjacent pairs, one per CTA of a cluster
+  int tiles_per_matrix;   // tile pairs per matrix
   int k_iters;            // contraction / 64, rounded up
-  long long tile_begin;   // first tile of this problem in the launch's tile space
+  long long tile_begin;   // first tile pair of this problem in the launch's pair space
   // epilogue coefficients
   float alpha;            // gram: output = alpha * s^2 * acc (s from `scale` when given)
   float coef_a, coef_b, coef_c;

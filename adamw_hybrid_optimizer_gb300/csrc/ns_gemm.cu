@@ -13,8 +13,11 @@
 // (4 stages, 3 for the final step), one tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) per 16-slice
 // issued by one thread, fp32 accumulators in tensor memory (2 x 256 columns, so the epilogue of one
 // tile overlaps the MMAs of the next), persistent CTAs (one per SM) striding over the tiles of up to
-// GEMM_MAX_PROBLEMS stacks at once. Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM
-// owner), warps 2-5 = epilogue, warp 6 = epilogue loader: ahead of the epilogue it brings each tile's
+// GEMM_MAX_PROBLEMS stacks at once. CTAs run as clusters of two that compute vertically adjacent tiles
+// (rows 2p and 2p+1 of one tile column): both need the same B operand, so each CTA loads one half of it
+// and multicasts it to both, which cuts the operand traffic per SM by a third. Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM
+// owner), warps 2-9 = epilogue (two per tensor-memory lane quarter, each taking one 32-column half of
+// every 64-column slot), warp 10 = epilogue loader: ahead of the epilogue it brings each tile's
 // second input (G or X) and, for bf16 parameters, the parameters into a 2-slot shared-memory ring, so
 // the epilogue never waits for a global-memory round trip.
 #include <cuda.h>
@@ -40,7 +43,9 @@ constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int ACC_COLS = BN;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int NUM_THREADS = 224;
+constexpr int EPI_WARPS = 8;                                // two per TMEM lane quarter
+constexpr int LOADER_WARP = 2 + EPI_WARPS;
+constexpr int NUM_THREADS = 32 * (LOADER_WARP + 1);
 
 // Epilogue input ring: a slot holds 64 columns (two 32-column chunks) of a tile's 128 rows.
 constexpr int RING_SLOTS = 2;
@@ -95,22 +100,25 @@ __device__ __forceinline__ int find_problem(const GemmGroup &g, long long t) {
   return p;
 }
 
-// local tile index of one problem -> (matrix, tile row, tile column)
-__device__ __forceinline__ void decode_tile(const GemmProblem &a, int symmetric, long long t, int &b, int &ti,
-                                            int &tj) {
+// local tile-pair index of one problem -> (matrix, tile row of this CTA, tile column). Pair p covers tile
+// rows 2p (cluster rank 0) and 2p+1 (rank 1); a rank-1 tile past the last row computes nothing useful and
+// stores nothing.
+__device__ __forceinline__ void decode_tile(const GemmProblem &a, int symmetric, long long t, uint32_t rank, int &b,
+                                            int &ti, int &tj) {
   b = static_cast<int>(t / a.tiles_per_matrix);
   int r = static_cast<int>(t - static_cast<long long>(b) * a.tiles_per_matrix);
   if (!symmetric) {
-    tj = r / a.m_tiles;
-    ti = r - tj * a.m_tiles;
+    tj = r / a.m_pairs;
+    ti = 2 * (r - tj * a.m_pairs) + static_cast<int>(rank);
     return;
   }
-  // column-major over the tiles with 256*j + 255 >= 128*i, i.e. i < 2j + 2
+  // column-major over the pairs touching the upper triangle: tile (i, j) is needed iff 128 i <= 256 j + 255,
+  // i.e. i < 2j + 2, so pair p is needed iff p <= j
   int j = 0;
   for (;;) {
-    const int cnt = min(a.m_tiles, 2 * j + 2);
+    const int cnt = min(a.m_pairs, j + 1);
     if (r < cnt) {
-      ti = r;
+      ti = 2 * r + static_cast<int>(rank);
       tj = j;
       return;
     }
@@ -340,14 +348,15 @@ __device__ __forceinline__ uint32_t stage_params_bytes(const GemmProblem &a, int
   return a.transposed ? 64u * BM * 2u : static_cast<uint32_t>(BM) * 64u * 2u;
 }
 
+// Issued by all 32 lanes of the loader warp, each taking every 32nd row segment.
 __device__ __forceinline__ void stage_params_issue(const GemmProblem &a, const void *base, int row0, int c0,
-                                                   uint8_t *dst, uint64_t *bar) {
+                                                   uint8_t *dst, uint64_t *bar, int lane) {
   const __nv_bfloat16 *p = static_cast<const __nv_bfloat16 *>(base);
   if (!a.transposed) {
-    for (int r = 0; r < BM; ++r)
+    for (int r = lane; r < BM; r += 32)
       bulk_load(dst + r * PARAM_PITCH_WIDE, p + static_cast<long long>(row0 + r) * a.orig_cols + c0, 128, bar);
   } else {
-    for (int j = 0; j < 64; ++j)
+    for (int j = lane; j < 64; j += 32)
       bulk_load(dst + j * PARAM_PITCH_TALL, p + static_cast<long long>(c0 + j) * a.orig_cols + row0, BM * 2, bar);
   }
 }
@@ -367,15 +376,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&ctrl->full[s], 1);
-      mbar_init(&ctrl->empty[s], 1);
+      mbar_init(&ctrl->empty[s], 2);   // both CTAs' MMAs read each stage (B halves are shared)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctrl->acc_full[s], 1);
-      mbar_init(&ctrl->acc_empty[s], 4);
+      mbar_init(&ctrl->acc_empty[s], EPI_WARPS);
     }
     for (int s = 0; s < RING_SLOTS; ++s) {
       mbar_init(&ctrl->ring_full[s], 1);
-      mbar_init(&ctrl->ring_empty[s], 4);
+      mbar_init(&ctrl->ring_empty[s], EPI_WARPS);
     }
     mbar_init(&ctrl->drain, 1);
     ctrl->abort_flag = 0;
@@ -389,7 +398,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();     // the cluster barrier is warp-aligned
+  cluster_sync();   // both CTAs' barriers are initialised before either multicasts into the other
   tc_fence_after();
   // everything above touched only shared and tensor memory; operands, scales and parameters written by
   // earlier kernels are read only after the previous grid has completed
@@ -397,6 +407,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
   if (threadIdx.x == 0) pdl_launch_dependents();
   const uint32_t tmem_base = ctrl->tmem_base;
   WaitCtl ctl{&ctrl->abort_flag, args.err, args.timeout_ns};
+  const uint32_t rank = cluster_ctarank();
+  const long long first = blockIdx.x >> 1;
+  const long long stride = gridDim.x >> 1;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -405,7 +418,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       int last_parity[MAX_STAGES];
       for (int s = 0; s < MAX_STAGES; ++s) last_parity[s] = -1;
       bool ok = true;
-      for (long long t = blockIdx.x; ok && t < args.total_tiles; t += gridDim.x) {
+      for (long long t = first; ok && t < args.total_tiles; t += stride) {
         // descriptor fields copied to registers: the asm below clobbers memory, which would otherwise force a
         // reload from parameter space on every use
         const int pi = find_problem(args, t);
@@ -413,7 +426,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         const CUtensorMap *map_a = &args.map_a[pi];
         const CUtensorMap *map_b = &args.map_b[pi];
         int b, ti, tj;
-        decode_tile(P, args.symmetric, t - P.tile_begin, b, ti, tj);
+        decode_tile(P, args.symmetric, t - P.tile_begin, rank, b, ti, tj);
         const int k_iters = P.k_iters;
         for (int kk = 0; kk < k_iters; ++kk) {
           if (!wait_bounded(&ctrl->empty[stage], phase ^ 1u, ctl, ERR_WAIT_EMPTY)) {
@@ -425,12 +438,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
           uint8_t *sa = smem + stage * STAGE_BYTES;
           uint8_t *sb = sa + A_BYTES;
           tma_load_3d(sa, map_a, &ctrl->full[stage], kk * BK, ti * BM, b);
+          // this CTA's half of the shared B operand, delivered to both CTAs of the pair
           if constexpr (!B_MN) {
-            tma_load_3d(sb, map_b, &ctrl->full[stage], kk * BK, tj * BN, b);
+            // K-major: rows tj*256 + 128*rank .. +127 through the A map (same tensor, box 64 x 128)
+            tma_load_3d_mc(sb + rank * (B_BYTES / 2), map_a, &ctrl->full[stage], kk * BK,
+                           tj * BN + (BN / 2) * static_cast<int>(rank), b, 0x3);
           } else {
+            // N-major: column chunks 2*rank and 2*rank+1 (64 columns each)
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c)
-              tma_load_3d(sb + c * (64 * BK * 2), map_b, &ctrl->full[stage], tj * BN + 64 * c, kk * BK, b);
+            for (int q = 0; q < 2; ++q) {
+              const int c = 2 * static_cast<int>(rank) + q;
+              tma_load_3d_mc(sb + c * (64 * BK * 2), map_b, &ctrl->full[stage], tj * BN + 64 * c, kk * BK, b, 0x3);
+            }
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -449,7 +468,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       bool issued = false;
-      for (long long t = blockIdx.x; ok && t < args.total_tiles; t += gridDim.x) {
+      for (long long t = first; ok && t < args.total_tiles; t += stride) {
         if (!wait_bounded(&ctrl->acc_empty[acc], acc_phase ^ 1u, ctl, ERR_WAIT_ACC_EMPTY)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
@@ -470,7 +489,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
             tc_mma_bf16(d_tmem, adesc, bdesc, idesc, (kk | k) != 0 ? 1u : 0u);
           }
           issued = true;
-          tc_commit(&ctrl->empty[stage]);
+          tc_commit_mc(&ctrl->empty[stage], 0x3);   // frees the stage in both CTAs of the pair
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -487,67 +506,73 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         drain_wait(&ctrl->drain, 0u, ctl);
       }
     }
-  } else if (warp == 6) {
+  } else if (warp == LOADER_WARP) {
     if constexpr (EPI != EPI_GRAM) {
-      if (lane == 0) {
-        // ---------------------------------------------------------------- epilogue loader
-        uint32_t slot = 0, rphase = 0;
-        int last_parity[RING_SLOTS];
-        for (int s = 0; s < RING_SLOTS; ++s) last_parity[s] = -1;
-        bool ok = true;
-        for (long long t = blockIdx.x; ok && t < args.total_tiles; t += gridDim.x) {
-          const int pi = find_problem(args, t);
-          const GemmProblem P = args.prob[pi];
-          // POLY reads G through the A-operand map (box 64 x 128); APPLY / FINAL read X through the N-major
-          // B-operand map (box 64 x 64, two loads)
-          const CUtensorMap *aux_map = (EPI == EPI_POLY) ? &args.map_a[pi] : &args.map_b[pi];
-          int b, ti, tj;
-          decode_tile(P, args.symmetric, t - P.tile_begin, b, ti, tj);
-          const int row0 = ti * BM;
-          for (int s = 0; s < BN / 64; ++s) {
-            const int c0 = tj * BN + 64 * s;
-            if (c0 >= P.cols) break;
-            if (!slot_used(args.symmetric, c0, row0)) continue;
-            if (!wait_bounded(&ctrl->ring_empty[slot], rphase ^ 1u, ctl, ERR_WAIT_RING_EMPTY)) {
-              ok = false;
-              break;
-            }
-            uint8_t *dst = ring + slot * SLOT_BYTES;
-            uint32_t pbytes = 0;
-            const void *pbase = nullptr;
-            if constexpr (EPI == EPI_FINAL) pbytes = stage_params_bytes(P, b, row0, c0, pbase);
+      // ---------------------------------------------------------------- epilogue loader (whole warp: lane 0
+      // owns the ring barriers and the TMA loads, all lanes share the parameter row copies)
+      uint32_t slot = 0, rphase = 0;
+      int last_parity[RING_SLOTS];
+      for (int s = 0; s < RING_SLOTS; ++s) last_parity[s] = -1;
+      bool ok = true;
+      for (long long t = first; ok && t < args.total_tiles; t += stride) {
+        const int pi = find_problem(args, t);
+        const GemmProblem P = args.prob[pi];
+        // POLY reads G through the A-operand map (box 64 x 128); APPLY / FINAL read X through the N-major
+        // B-operand map (box 64 x 64, two loads)
+        const CUtensorMap *aux_map = (EPI == EPI_POLY) ? &args.map_a[pi] : &args.map_b[pi];
+        int b, ti, tj;
+        decode_tile(P, args.symmetric, t - P.tile_begin, rank, b, ti, tj);
+        const int row0 = ti * BM;
+        for (int s = 0; s < BN / 64; ++s) {
+          const int c0 = tj * BN + 64 * s;
+          if (c0 >= P.cols) break;
+          if (!slot_used(args.symmetric, c0, row0)) continue;
+          bool w = true;
+          if (lane == 0) w = wait_bounded(&ctrl->ring_empty[slot], rphase ^ 1u, ctl, ERR_WAIT_RING_EMPTY);
+          if (!__shfl_sync(0xffffffffu, w, 0)) {
+            ok = false;
+            break;
+          }
+          uint8_t *dst = ring + slot * SLOT_BYTES;
+          uint32_t pbytes = 0;
+          const void *pbase = nullptr;
+          if constexpr (EPI == EPI_FINAL) pbytes = stage_params_bytes(P, b, row0, c0, pbase);
+          if (lane == 0) {
             ctrl->ring_param_ok[slot] = pbytes != 0;
             mbar_arrive_expect_tx(&ctrl->ring_full[slot], RING_AUX_BYTES + pbytes);
-            last_parity[slot] = static_cast<int>(rphase);
             if constexpr (EPI == EPI_POLY) {
               tma_load_3d(dst, aux_map, &ctrl->ring_full[slot], c0, row0, b);
             } else {
               tma_load_3d(dst, aux_map, &ctrl->ring_full[slot], c0, row0, b);
               tma_load_3d(dst + 64 * 128, aux_map, &ctrl->ring_full[slot], c0, row0 + 64, b);
             }
-            if constexpr (EPI == EPI_FINAL) {
-              if (pbytes) stage_params_issue(P, pbase, row0, c0, dst + RING_AUX_BYTES, &ctrl->ring_full[slot]);
-            }
-            if (++slot == RING_SLOTS) {
-              slot = 0;
-              rphase ^= 1u;
-            }
+          }
+          __syncwarp();   // the expected byte count is registered before any lane's copy can complete
+          if constexpr (EPI == EPI_FINAL) {
+            if (pbytes) stage_params_issue(P, pbase, row0, c0, dst + RING_AUX_BYTES, &ctrl->ring_full[slot], lane);
+          }
+          last_parity[slot] = static_cast<int>(rphase);
+          if (++slot == RING_SLOTS) {
+            slot = 0;
+            rphase ^= 1u;
           }
         }
+      }
+      if (lane == 0)
         for (int s = 0; s < RING_SLOTS; ++s)
           if (last_parity[s] >= 0) drain_wait(&ctrl->ring_full[s], static_cast<uint32_t>(last_parity[s]), ctl);
-      }
     }
   } else {
-    // ---------------------------------------------------------------- epilogue (warps 2..5)
+    // ---------------------------------------------------------------- epilogue (warps 2..9)
     const int lane_base = (warp % 4) * 32;  // TMEM lanes this warp may read
     const int rloc = lane_base + lane;      // this thread's row within the tile
+    const int my_half = (warp - 2) / 4;     // which 32-column half of each 64-column slot
     uint32_t acc = 0, acc_phase = 0, slot = 0, rphase = 0;
-    for (long long t = blockIdx.x; t < args.total_tiles; t += gridDim.x) {
+    for (long long t = first; t < args.total_tiles; t += stride) {
       // by value: epilogue stores could alias a reference into parameter space and force reloads
       const GemmProblem P = args.prob[find_problem(args, t)];
       int b, ti, tj;
-      decode_tile(P, args.symmetric, t - P.tile_begin, b, ti, tj);
+      decode_tile(P, args.symmetric, t - P.tile_begin, rank, b, ti, tj);
       // every lane waits; the warp proceeds only if all of them saw the accumulator complete, so the
       // warp-collective TMEM loads below never run with part of the warp gone
       bool ok = wait_bounded(&ctrl->acc_full[acc], acc_phase, ctl, ERR_WAIT_ACC_FULL);
@@ -572,16 +597,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
           }
           staged = ctrl->ring_param_ok[slot] != 0;
         }
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
+        {
+          const int half = my_half;
           const int col0 = c0 + 32 * half;
-          if (col0 >= P.cols) break;                                     // warp-uniform
-          if (args.symmetric && col0 + 31 < warp_row0) continue;         // chunk below the diagonal for every lane
-          if (warp_row0 >= P.rows) break;                                // whole warp past the last row
-          float v[32];
-          tmem_ld_32x32b_x32(tmem_base + acc * ACC_COLS + (static_cast<uint32_t>(lane_base) << 16) + (col0 - tj * BN),
-                             v);
-          epilogue_chunk<EPI>(P, b, row, rloc, col0, half, slot_ptr, slot_ptr + RING_AUX_BYTES, staged, v);
+          // warp-uniform: chunk past the last column, below the diagonal for every lane, or past the last row
+          if (col0 < P.cols && !(args.symmetric && col0 + 31 < warp_row0) && warp_row0 < P.rows) {
+            float v[32];
+            tmem_ld_32x32b_x32(tmem_base + acc * ACC_COLS + (static_cast<uint32_t>(lane_base) << 16) +
+                                   (col0 - tj * BN),
+                               v);
+            epilogue_chunk<EPI>(P, b, row, rloc, col0, half, slot_ptr, slot_ptr + RING_AUX_BYTES, staged, v);
+          }
         }
         if constexpr (EPI != EPI_GRAM) {
           __syncwarp();
@@ -601,8 +627,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
     }
   }
 
+  // neither CTA leaves while the other may still multicast into it or arrive on its barriers
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();     // lanes that ran a role loop rejoin their warp before the warp-aligned barrier
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
@@ -654,17 +682,30 @@ muon_status launch_group(const GemmGroup &g, int32_t kind, cudaStream_t s) {
                          static_cast<int>(smem_bytes(EPI)));
   });
   if (g.total_tiles <= 0) return MUON_OK;
-  const long long sms = device_sm_count();
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(g.total_tiles < sms ? g.total_tiles : sms));
   cfg.blockDim = dim3(NUM_THREADS);
   cfg.dynamicSmemBytes = smem_bytes(EPI);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
+  // persistent: as many pairs of CTAs as can be resident at once (one CTA per SM)
+  static int max_clusters[64];
+  if (max_clusters[dev & 63] == 0) {
+    int n = 0;
+    cfg.gridDim = dim3(2 * (device_sm_count() / 2));
+    if (cudaOccupancyMaxActiveClusters(&n, ns_gemm_kernel<EPI, B_MN>, &cfg) != cudaSuccess || n < 1)
+      n = device_sm_count() / 2;
+    max_clusters[dev & 63] = n;
+  }
+  const long long ncl = g.total_tiles < max_clusters[dev & 63] ? g.total_tiles : max_clusters[dev & 63];
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * ncl));
   launch_begin(kind, s);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<EPI, B_MN>, g);
   launch_end(s);
@@ -678,12 +719,13 @@ void fill_tiles(GemmProblem &a, long long batch, long long rows, long long cols,
   a.cols = static_cast<int>(cols);
   a.m_tiles = static_cast<int>((rows + BM - 1) / BM);
   a.n_tiles = static_cast<int>((cols + BN - 1) / BN);
+  a.m_pairs = (a.m_tiles + 1) / 2;
   if (symmetric) {
     int cnt = 0;
-    for (int j = 0; j < a.n_tiles; ++j) cnt += (a.m_tiles < 2 * j + 2 ? a.m_tiles : 2 * j + 2);
+    for (int j = 0; j < a.n_tiles; ++j) cnt += (a.m_pairs < j + 1 ? a.m_pairs : j + 1);
     a.tiles_per_matrix = cnt;
   } else {
-    a.tiles_per_matrix = a.m_tiles * a.n_tiles;
+    a.tiles_per_matrix = a.m_pairs * a.n_tiles;
   }
   a.k_iters = static_cast<int>((contraction + BK - 1) / BK);
 }

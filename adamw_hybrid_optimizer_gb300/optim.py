@@ -8,8 +8,9 @@ optimizer" (Muon on hidden-layer matrices; embedding, output layer and vectors o
 caller decides by the group's kind, and a Muon group must hold 2-D tensors only.
 
 Muon matrices of one group are bucketed by shape (muon_plan_buckets); each bucket owns one fp32
-(K, A, B) momentum stack and one muon_step_batched call per step. AdamW state is one fp32
-exp_avg / exp_avg_sq pair per tensor and the group's step count. All arithmetic runs in libmuon.
+(K, A, B) momentum stack, and all buckets of a group are updated by one muon_step_grouped call per
+step. AdamW state is one fp32 exp_avg / exp_avg_sq pair per tensor and the group's step count. All
+arithmetic runs in libmuon.
 """
 from __future__ import annotations
 
@@ -80,9 +81,9 @@ class HybridMuonAdamW:
                 for shape, ps in zip(plan["bucket_shapes"], members):
                     bk = _Bucket(ps, shape, device)
                     buckets.append(bk)
-                    ws_bytes = max(ws_bytes, L.muon_workspace_bytes(bk.K, bk.A, bk.B))
                     for k, p in enumerate(ps):
                         self.state[p] = {"momentum_buffer": bk.momentum[k]}
+                ws_bytes = max(ws_bytes, sum(L.muon_workspace_bytes(bk.K, bk.A, bk.B) for bk in buckets))
             else:
                 group["step"] = 0
                 for p in group["params"]:
@@ -99,6 +100,7 @@ class HybridMuonAdamW:
                 hp = L.make_muon_hparams(group["lr"], group["momentum"], group["weight_decay"], group["nesterov"],
                                          group["cautious_wd"], group["scale_mode"], group["ns_coefficients"],
                                          group["eps"])
+                specs = []
                 for bk in buckets:
                     if any(p.grad is None for p in bk.params):
                         continue
@@ -109,8 +111,9 @@ class HybridMuonAdamW:
                         if L._dtype_code(p) != pdt or L._dtype_code(gr) != gdt or not p.is_contiguous() \
                                 or not gr.is_contiguous():
                             raise ValueError("a Muon bucket needs contiguous tensors of one dtype")
-                    L.muon_step_batched(bk.param_ptrs, pdt, bk.grad_ptrs, gdt, bk.momentum, bk.K, bk.A, bk.B, hp,
-                                        self._ws)
+                    specs.append((bk.param_ptrs, bk.grad_ptrs, bk.momentum, bk.K, bk.A, bk.B, pdt, gdt))
+                if specs:
+                    L.muon_step_grouped(L.make_buckets(specs), hp, self._ws)
             else:
                 group["step"] += 1
                 b1, b2 = group["betas"]

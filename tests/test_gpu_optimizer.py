@@ -1,0 +1,107 @@
+"""HybridMuonAdamW, the param_groups optimizer on top of the C ABI.
+
+Checks, on a GPT-2-small-shaped layout cut to 2 layers: Muon groups route 2-D hidden matrices and AdamW
+groups everything else, both match the oracle; optimizer state takes 4 bytes per Muon parameter and 8
+per AdamW parameter (the budget printed in "Optimizers: AdamW, Muon and the distributed optimizer",
+section "The optimizer's memory budget"); a run saved after step 2 and resumed in a fresh optimizer
+matches an uninterrupted run bit for bit.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import adamw as oadamw
+from oracle import muon as omuon
+from tests.conftest import read_golden
+from tests.gpu_common import DEV, build_lib, f64
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def L():
+    return build_lib()
+
+
+def _model(seed):
+    g = torch.Generator().manual_seed(seed)
+    mk = lambda *s: (torch.randn(s, generator=g) * 1e-3).to(torch.bfloat16).to(DEV)
+    hidden = [mk(768, 2304), mk(768, 768), mk(768, 3072), mk(3072, 768), mk(768, 2304), mk(768, 768)]
+    other = [mk(1000, 768), mk(768), mk(768)]
+    return hidden, other
+
+
+def _grads(params, step, seed):
+    g = torch.Generator().manual_seed(1000 * seed + step)
+    for p in params:
+        p.grad = (torch.randn(p.shape, generator=g) * 1e-3).to(torch.bfloat16).to(DEV)
+
+
+def _opt(hidden, other):
+    from adamw_hybrid_optimizer_gb300 import HybridMuonAdamW
+    m = workloads.workload("gpt2s").muon_hp
+    a = workloads.workload("gpt2s").adamw_hp
+    return HybridMuonAdamW([
+        {"params": hidden, "kind": "muon", "lr": m.lr, "momentum": m.momentum, "weight_decay": m.weight_decay},
+        {"params": other, "kind": "adamw", "lr": a.lr, "betas": (a.beta1, a.beta2), "eps": a.eps,
+         "weight_decay": a.weight_decay},
+    ])
+
+
+def test_optimizer_matches_oracle_and_state_budget(L, golden_dir):
+    hidden, other = _model(0)
+    before = [f64(p) for p in hidden + other]
+    opt = _opt(hidden, other)
+    _grads(hidden + other, 1, 0)
+    grads = [f64(p.grad) for p in hidden + other]
+    opt.step()
+    torch.cuda.synchronize()
+    m = workloads.workload("gpt2s").muon_hp
+    a = workloads.workload("gpt2s").adamw_hp
+    for i, p in enumerate(hidden):
+        ref, _, _ = omuon.muon_update(before[i], grads[i], np.zeros_like(before[i]), lr=m.lr, momentum=m.momentum,
+                                      weight_decay=m.weight_decay, coeffs=m.coeffs, eps=m.eps, param_dtype="bf16")
+        assert np.linalg.norm(f64(p) - ref) <= 2e-2 * np.linalg.norm(ref - before[i]) + 2 ** -8 * np.linalg.norm(ref)
+    for j, p in enumerate(other):
+        i = len(hidden) + j
+        ref, _, _ = oadamw.adamw_update(before[i], grads[i], 0, 0, 1, lr=a.lr, beta1=a.beta1, beta2=a.beta2,
+                                        eps=a.eps, weight_decay=a.weight_decay, param_dtype="bf16")
+        ulp = np.ldexp(1.0, np.frexp(np.maximum(np.abs(ref), 1e-30))[1] - 8)
+        assert np.all(np.abs(f64(p) - ref) <= ulp * 1.0001 + 1e-6 * (np.abs(before[i]) + a.lr))
+    fx = read_golden(os.path.join(golden_dir, "optimizer_state_bytes.txt"))
+    state_bytes = lambda ps: sum(t.numel() * t.element_size() for p in ps for t in opt.state[p].values())
+    assert state_bytes(hidden) / sum(p.numel() for p in hidden) == fx["muon"][0]
+    assert state_bytes(other) / sum(p.numel() for p in other) == fx["adamw"][0]
+
+
+def test_resume_bit_matches_uninterrupted_run(L):
+    hidden, other = _model(1)
+    params = hidden + other
+    ref_opt = _opt(hidden, other)
+    snap = [p.clone() for p in params]
+    for step in (1, 2, 3, 4):
+        _grads(params, step, 1)
+        ref_opt.step()
+    ref_final = [p.clone() for p in params]
+    # rerun: two steps, checkpoint, fresh optimizer, restore, two more steps
+    for p, s0 in zip(params, snap):
+        p.data.copy_(s0)
+    opt = _opt(hidden, other)
+    for step in (1, 2):
+        _grads(params, step, 1)
+        opt.step()
+    sd = opt.state_dict()
+    saved = [p.clone() for p in params]
+    opt2 = _opt(hidden, other)
+    opt2.load_state_dict(sd)
+    for p, s in zip(params, saved):
+        p.data.copy_(s)
+    for step in (3, 4):
+        _grads(params, step, 1)
+        opt2.step()
+    torch.cuda.synchronize()
+    for a_, b_ in zip(params, ref_final):
+        assert torch.equal(a_, b_)
