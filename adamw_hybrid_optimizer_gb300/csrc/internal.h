@@ -29,6 +29,8 @@ int device_sm_count();
 // The current device's capability check and the per-wait limit set by muon_set_timeout_ns (libmuon.cu).
 muon_status device_check();
 unsigned long long wait_timeout_ns();
+// The registered per-tile timeline buffer of the GEMM kernels (null unless muon_debug_timeline set one).
+void debug_timeline(unsigned long long **buf, int *cap_per_cta);
 
 // ------------------------------------------------------------------------------------------ tensor-core GEMMs
 

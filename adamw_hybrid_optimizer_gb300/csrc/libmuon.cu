@@ -109,6 +109,24 @@ muon_status device_check() { return check_device(); }
 
 unsigned long long wait_timeout_ns() { return g_timeout_ns; }
 
+namespace {
+unsigned long long *g_timeline = nullptr;
+int g_timeline_cap = 0;
+int64_t g_timeline_regions = 0, g_timeline_next = 0, g_timeline_region_words = 0;
+}  // namespace
+
+// Each tensor-core launch after registration takes the next region of the buffer, until it is full.
+void debug_timeline(unsigned long long **buf, int *cap_per_cta) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (g_timeline == nullptr || g_timeline_next >= g_timeline_regions) {
+    *buf = nullptr;
+    *cap_per_cta = 0;
+    return;
+  }
+  *buf = g_timeline + g_timeline_next++ * g_timeline_region_words;
+  *cap_per_cta = g_timeline_cap;
+}
+
 int device_sm_count() {
   const int d = current_device();
   if (d < 0 || d >= 64) return 1;
@@ -567,6 +585,24 @@ muon_status muon_debug_wait_timeout(void *ws, size_t ws_bytes, uint64_t timeout_
   if (timeout_ns == 0 || timeout_ns > 10000000000ull) return MUON_ERR_INVALID_ARG;
   if ((st = check_device()) != MUON_OK) return st;
   return launch_debug_wait(static_cast<uint32_t *>(ws), timeout_ns, reinterpret_cast<cudaStream_t>(stream));
+}
+
+muon_status muon_debug_timeline(void *buf, int64_t bytes, int32_t records_per_cta) {
+  if (buf == nullptr || bytes <= 0 || records_per_cta <= 0) {
+    muon::g_timeline = nullptr;
+    muon::g_timeline_cap = 0;
+    return MUON_OK;
+  }
+  if (muon::device_check() != MUON_OK) return MUON_ERR_UNSUPPORTED_DEVICE;
+  const int64_t region = static_cast<int64_t>(muon::device_sm_count()) * records_per_cta * 10;
+  if (bytes < region * 8) return MUON_ERR_WORKSPACE;
+  std::lock_guard<std::mutex> lk(muon::g_trace_mu);
+  muon::g_timeline = static_cast<unsigned long long *>(buf);
+  muon::g_timeline_cap = records_per_cta;
+  muon::g_timeline_region_words = region;
+  muon::g_timeline_regions = bytes / (region * 8);
+  muon::g_timeline_next = 0;
+  return MUON_OK;
 }
 
 int64_t muon_launch_count(void) {

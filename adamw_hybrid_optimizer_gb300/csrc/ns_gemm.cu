@@ -10,16 +10,17 @@
 //     last step: u = a X + H X, then p <- p - lr*wd*p*mask - lr*scale*u      EPI_FINAL
 //
 // Design (sm_103a): 128 x 256 output tiles, 64-deep k-slices, a TMA ring with 128-byte swizzle
-// (4 stages, 3 for the final step), one tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) per 16-slice
+// (4 stages, 3 when the contraction is short), one tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) per 16-slice
 // issued by one thread, fp32 accumulators in tensor memory (2 x 256 columns, so the epilogue of one
 // tile overlaps the MMAs of the next), persistent CTAs (one per SM) striding over the tiles of up to
 // GEMM_MAX_PROBLEMS stacks at once. CTAs run as clusters of two that compute vertically adjacent tiles
 // (rows 2p and 2p+1 of one tile column): both need the same B operand, so each CTA loads one half of it
 // and multicasts it to both, which cuts the operand traffic per SM by a third. Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM
 // owner), warps 2-9 = epilogue (two per tensor-memory lane quarter, each taking one 32-column half of
-// every 64-column slot), warp 10 = epilogue loader: ahead of the epilogue it brings each tile's
-// second input (G or X) and, for bf16 parameters, the parameters into a 2-slot shared-memory ring, so
-// the epilogue never waits for a global-memory round trip.
+// every 64-column slot), warp 10 = epilogue loader: ahead of the epilogue it TMA-loads each tile's second
+// input (G or X) into a shared-memory ring (2 or 5 slots, by contraction depth). Each epilogue warp then
+// reuses its part of the slot to reshape results, so global stores (and the final step's parameter
+// loads) are coalesced 16-byte accesses; transposed outputs go through shared memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -47,37 +48,36 @@ constexpr int EPI_WARPS = 8;                                // two per TMEM lane
 constexpr int LOADER_WARP = 2 + EPI_WARPS;
 constexpr int NUM_THREADS = 32 * (LOADER_WARP + 1);
 
-// Epilogue input ring: a slot holds 64 columns (two 32-column chunks) of a tile's 128 rows.
-constexpr int RING_SLOTS = 2;
-constexpr int RING_AUX_BYTES = BM * 64 * 2;                 // bf16, 128-byte rows, 128B-swizzled (as TMA writes)
-constexpr int PARAM_PITCH_WIDE = 64 * 2 + 16;               // stored row-major: [128 rows][64 cols] + pad
-constexpr int PARAM_PITCH_TALL = BM * 2 + 16;               // stored transposed: [64 stored rows][128] + pad
-constexpr int RING_PARAM_BYTES = BM * PARAM_PITCH_WIDE;     // >= 64 * PARAM_PITCH_TALL
-static_assert(RING_PARAM_BYTES >= 64 * PARAM_PITCH_TALL, "param slot too small");
+// Epilogue input ring: a slot holds 64 columns (two 32-column chunks) of a tile's 128 rows, bf16, 128-byte
+// lines with the 128B swizzle TMA writes. The GRAM kernel has no second input and uses one slot only as
+// the epilogue's staging space.
+constexpr int MAX_RING_SLOTS = 5;
+constexpr int RING_AUX_BYTES = BM * 64 * 2;
 
-__host__ __device__ constexpr int stages_of(int epi) { return epi == EPI_FINAL ? 3 : 4; }
-__host__ __device__ constexpr int ring_slot_bytes(int epi) {
-  return epi == EPI_GRAM ? 0 : (epi == EPI_FINAL ? RING_AUX_BYTES + RING_PARAM_BYTES : RING_AUX_BYTES);
-}
+__host__ __device__ constexpr int ring_slot_bytes(int) { return RING_AUX_BYTES; }
 
 struct Ctrl {
   uint64_t full[MAX_STAGES];
   uint64_t empty[MAX_STAGES];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
-  uint64_t ring_full[RING_SLOTS];
-  uint64_t ring_empty[RING_SLOTS];
+  uint64_t ring_full[MAX_RING_SLOTS];
+  uint64_t ring_empty[MAX_RING_SLOTS];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
-  int ring_param_ok[RING_SLOTS];
 };
 
-__host__ __device__ constexpr size_t smem_bytes(int epi) {
-  return static_cast<size_t>(stages_of(epi)) * STAGE_BYTES + static_cast<size_t>(RING_SLOTS) * ring_slot_bytes(epi) +
+// Pipeline shapes: a long contraction wants mainloop stages, a short one leaves the epilogue as the limit
+// and wants ring slots (the epilogue's second input must arrive within one tile's MMA time).
+__host__ __device__ constexpr size_t smem_bytes(int epi, int stages, int slots) {
+  return static_cast<size_t>(stages) * STAGE_BYTES + static_cast<size_t>(slots) * ring_slot_bytes(epi) +
          sizeof(Ctrl) + 1024;
 }
-static_assert(smem_bytes(EPI_APPLY) <= 232448 && smem_bytes(EPI_FINAL) <= 232448, "shared memory over budget");
+constexpr int SHORT_K_ITERS = 32;   // contractions up to 2048 take the deep-ring shape
+static_assert(smem_bytes(EPI_GRAM, 4, 1) <= 232448 && smem_bytes(EPI_APPLY, 4, 2) <= 232448 &&
+                  smem_bytes(EPI_APPLY, 3, 5) <= 232448,
+              "shared memory over budget");
 
 // Kernel parameter: up to GEMM_MAX_PROBLEMS problems of one step kind, in order of tile_begin.
 struct GemmGroup {
@@ -89,8 +89,18 @@ struct GemmGroup {
   long long total_tiles;
   uint32_t *err;
   unsigned long long timeout_ns;
+  unsigned long long *timeline;   // optional per-tile timestamps (performance analysis), or null
+  int timeline_cap;               // records per CTA
 };
 static_assert(sizeof(GemmGroup) <= 4096, "kernel parameter block too large");
+
+// Timeline record of one tile (globaltimer ns): tile index, producer first / last issue, MMA start
+// (accumulator free), first / last operands ready, last commit, epilogue start (accumulator full), end.
+constexpr int TL_WORDS = 10;
+__device__ __forceinline__ unsigned long long *tl_rec(const GemmGroup &g, int local) {
+  if (g.timeline == nullptr || local >= g.timeline_cap) return nullptr;
+  return g.timeline + (static_cast<long long>(blockIdx.x) * g.timeline_cap + local) * TL_WORDS;
+}
 
 __device__ __forceinline__ int find_problem(const GemmGroup &g, long long t) {
   int p = 0;
@@ -156,15 +166,89 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const float *s
   for (int q = 0; q < 4; ++q) d4[q] = pack8(src + 8 * q);
 }
 
-// 32 bf16 values of tile row r, columns 32*half .. 32*half+31 of a ring slot (128-byte rows, 128B swizzle:
-// the 16-byte chunk q of row r sits at chunk position q ^ (r & 7)).
-__device__ __forceinline__ void ring_aux_row(const uint8_t *slot, int r, int half, float *dst) {
-  const uint8_t *row = slot + r * 128;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int qq = (4 * half + q) ^ (r & 7);
-    unpack8(*reinterpret_cast<const uint4 *>(row + qq * 16), dst + 8 * q);
+// ------------------------------------------------------------------------------------------ epilogue staging
+//
+// Each epilogue warp owns a 32 x 32 region of the current ring slot: tile rows lane_base .. +31 (one
+// 128-byte line each) and the 64-byte half `half` of those lines, with the slot's 128-byte swizzle (16-byte
+// piece q of line L sits at piece position q ^ (L & 7)). The region first holds the warp's part of the
+// second input (as the loader's TMA wrote it); once every lane has read that, the warp reuses it to
+// reshape its results, so that every global store is a 16-byte store of 8 consecutive elements, four lanes
+// covering one 64-byte row segment. Row-wise access (a thread's own row) and segment-wise access (lane ->
+// row 8k + lane/4, piece lane%4) are both free of bank conflicts beyond the 4 wavefronts 512 bytes need.
+
+struct Region {
+  uint8_t *slot;
+  int lane_base, half;
+  __device__ __forceinline__ uint8_t *piece(int i, int q) const {
+    const int line = lane_base + i;
+    return slot + line * 128 + ((((half << 2) + q) ^ (line & 7)) << 4);
   }
+  __device__ __forceinline__ __nv_bfloat16 *elem(int i, int j) const {
+    return reinterpret_cast<__nv_bfloat16 *>(piece(i, j >> 3)) + (j & 7);
+  }
+};
+
+// the thread's own row i: 32 values in, 32 values out
+__device__ __forceinline__ void region_read_row(const Region &g, int i, float *dst) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) unpack8(*reinterpret_cast<const uint4 *>(g.piece(i, q)), dst + 8 * q);
+}
+__device__ __forceinline__ void region_write_row(const Region &g, int i, const float *src) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4 *>(g.piece(i, q)) = pack8(src + 8 * q);
+}
+// the thread's values as column i of the region (element j goes to row j): a transpose through smem
+__device__ __forceinline__ void region_write_col(const Region &g, int i, const float *src) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) *g.elem(j, i) = __float2bfloat16_rn(src[j]);
+}
+__device__ __forceinline__ void region_read_col(const Region &g, int i, float *dst) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) dst[j] = bf2f(*g.elem(j, i));
+}
+
+// Stores region row i (32 bf16) to dst_row[0..31] for each of the 32 rows, 16 bytes per lane, four lanes
+// per row. ok(i, e) says whether element e of row i may be written; full(i) whether all 32 may.
+template <typename Ok, typename Full>
+__device__ __forceinline__ void region_store(const Region &g, int lane, __nv_bfloat16 *base, long long ld, Ok ok,
+                                             Full full) {
+  const int q = lane & 3;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = 8 * k + (lane >> 2);
+    const uint4 w = *reinterpret_cast<const uint4 *>(g.piece(i, q));
+    __nv_bfloat16 *dst = base + static_cast<long long>(i) * ld + 8 * q;
+    if (full(i) && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+      *reinterpret_cast<uint4 *>(dst) = w;
+    } else {
+      const __nv_bfloat16 *h = reinterpret_cast<const __nv_bfloat16 *>(&w);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (ok(i, 8 * q + e)) dst[e] = h[e];
+    }
+  }
+}
+
+// Loads 32 rows x 32 bf16 (src row i at src + i*ld, elements 0..31) into the region, segment-wise.
+template <typename Ok, typename Full>
+__device__ __forceinline__ void region_load(const Region &g, int lane, const __nv_bfloat16 *base, long long ld, Ok ok,
+                                            Full full) {
+  const int q = lane & 3;
+  uint4 w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = 8 * k + (lane >> 2);
+    const __nv_bfloat16 *src = base + static_cast<long long>(i) * ld + 8 * q;
+    if (full(i) && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+      w[k] = *reinterpret_cast<const uint4 *>(src);
+    } else {
+      __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(&w[k]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) h[e] = ok(i, 8 * q + e) ? src[e] : __float2bfloat16_rn(0.f);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(g.piece(8 * k + (lane >> 2), q)) = w[k];
 }
 
 // Muon parameter update of one element: decoupled decay (masked where u*p <= 0 if cautious), then the
@@ -174,115 +258,35 @@ __device__ __forceinline__ float param_update(float pv, float u, const GemmProbl
   return (pv - a.lr_wd * mask * pv) - a.lr_scale * u;
 }
 
-// Final step for one thread's 32 values of wide row `row`, columns col0..col0+31.
-//   stored wide (row-major A x B): the thread's row segment; parameters from the ring (param_slot, laid out
-//   [128 rows][64 cols] with pitch PARAM_PITCH_WIDE) when the loader staged them, else loaded directly.
-//   stored tall (transposed): element (c, row); for each column the warp's lanes cover 32 consecutive stored
-//   elements; ring layout [64 stored rows][128] with pitch PARAM_PITCH_TALL.
-__device__ __forceinline__ void final_store(const GemmProblem &a, void *base, int row, int rloc, int col0, int half,
-                                            const uint8_t *param_slot, bool staged, float *v) {
+// Final step with fp32 parameters or a dense fp32 output: plain per-thread accesses (small stacks only).
+__device__ __forceinline__ void final_store_f32(const GemmProblem &a, void *base, int row, int col0, float *v) {
   const bool update = a.params != nullptr;
-  const bool f32 = a.out_dtype == MUON_F32;
-  if (!a.transposed) {
-    const long long idx = static_cast<long long>(row) * a.orig_cols + col0;
-    float pv[32];
-    if (update) {
-      if (staged) {
-        const uint8_t *src = param_slot + rloc * PARAM_PITCH_WIDE + half * 64;
+  float *p = static_cast<float *>(base);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) unpack8(*reinterpret_cast<const uint4 *>(src + 16 * q), pv + 8 * q);
-      } else if (f32) {
-        const float *p = static_cast<const float *>(base) + idx;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) pv[j] = (col0 + j < a.cols) ? p[j] : 0.f;
-      } else {
-        const __nv_bfloat16 *p = static_cast<const __nv_bfloat16 *>(base) + idx;
-        const bool vec = col0 + 32 <= a.cols && (reinterpret_cast<uintptr_t>(p) & 15) == 0;
-        if (vec) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) unpack8(reinterpret_cast<const uint4 *>(p)[q], pv + 8 * q);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) pv[j] = (col0 + j < a.cols) ? bf2f(p[j]) : 0.f;
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = param_update(pv[j], v[j], a);
-    }
-    if (f32) {
-      float *p = static_cast<float *>(base) + idx;
-      const bool vec = col0 + 32 <= a.cols && (reinterpret_cast<uintptr_t>(p) & 15) == 0;
-      if (vec) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          reinterpret_cast<float4 *>(p)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (col0 + j < a.cols) p[j] = v[j];
-      }
-    } else {
-      __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(base) + idx;
-      const bool vec = col0 + 32 <= a.cols && (reinterpret_cast<uintptr_t>(p) & 15) == 0;
-      if (vec) {
-        store_bf16x32(p, v);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (col0 + j < a.cols) p[j] = __float2bfloat16_rn(v[j]);
-      }
-    }
-    return;
-  }
-  // transposed: all loads are issued before the first store
-  if (update) {
-    float pv[32];
-    if (staged) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        pv[j] = bf2f(*reinterpret_cast<const __nv_bfloat16 *>(param_slot + (32 * half + j) * PARAM_PITCH_TALL +
-                                                              2 * rloc));
-    } else if (f32) {
-      const float *p = static_cast<const float *>(base) + row;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) pv[j] = (col0 + j < a.cols) ? p[static_cast<long long>(col0 + j) * a.orig_cols] : 0.f;
-    } else {
-      const __nv_bfloat16 *p = static_cast<const __nv_bfloat16 *>(base) + row;
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        pv[j] = (col0 + j < a.cols) ? bf2f(p[static_cast<long long>(col0 + j) * a.orig_cols]) : 0.f;
-    }
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = param_update(pv[j], v[j], a);
-  }
-  if (f32) {
-    float *p = static_cast<float *>(base) + row;
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (col0 + j < a.cols) p[static_cast<long long>(col0 + j) * a.orig_cols] = v[j];
-  } else {
-    __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(base) + row;
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (col0 + j < a.cols) p[static_cast<long long>(col0 + j) * a.orig_cols] = __float2bfloat16_rn(v[j]);
+  for (int j = 0; j < 32; ++j) {
+    const int c = col0 + j;
+    if (c >= a.cols) continue;
+    const long long idx = a.transposed ? static_cast<long long>(c) * a.orig_cols + row
+                                       : static_cast<long long>(row) * a.orig_cols + c;
+    p[idx] = update ? param_update(p[idx], v[j], a) : v[j];
   }
 }
 
-// Epilogue for one 32-column chunk held by one thread (its row `row` = tile row `rloc`, columns
-// col0..col0+31, i.e. half `half` of the ring slot). Called by every lane of the warp.
+// Epilogue for one 32 x 32 chunk: warp rows warp_row0 .. +31 (this thread: row = warp_row0 + lane), columns
+// col0 .. +31; v holds this thread's 32 accumulator values. Called by every lane of the warp; the region
+// holds the chunk's second input on entry (POLY, APPLY, FINAL) and is free for reuse on exit.
 template <int EPI>
-__device__ __forceinline__ void epilogue_chunk(const GemmProblem &a, int b, int row, int rloc, int col0, int half,
-                                               const uint8_t *aux_slot, const uint8_t *param_slot, bool param_staged,
-                                               float *v) {
+__device__ __forceinline__ void epilogue_chunk(const GemmProblem &a, int b, int warp_row0, int lane, int col0,
+                                               const Region &rg, float *v) {
+  const int row = warp_row0 + lane;
+  const int rows = a.rows, cols = a.cols;
   if constexpr (EPI == EPI_GRAM || EPI == EPI_POLY) {
-    const bool row_ok = row < a.rows;
-    const bool full = row_ok && (col0 >= row) && (col0 + 32 <= a.cols);
-    __nv_bfloat16 *out_b = a.out + static_cast<long long>(b) * a.mstride_out;
     if constexpr (EPI == EPI_POLY) {
       float gv[32];
-      ring_aux_row(aux_slot, rloc, half, gv);
+      region_read_row(rg, lane, gv);
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = a.coef_b * gv[j] + a.coef_c * v[j];
+      __syncwarp();
     } else {
       float sc = a.alpha;
       if (a.scale != nullptr) {
@@ -292,78 +296,93 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem &a, int b, int 
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] *= sc;
     }
-    // direct store of the upper-triangle part of this row
-    if (full) {
-      store_bf16x32(out_b + static_cast<long long>(row) * a.ld_out + col0, v);
-    } else if (row_ok) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int c = col0 + j;
-        if (c < a.cols && c >= row) out_b[static_cast<long long>(row) * a.ld_out + c] = __float2bfloat16_rn(v[j]);
-      }
-    }
-    // mirrored store of the strictly-upper part: lanes hold consecutive rows, so each column's
-    // 32 values land in one contiguous 64-byte segment of the mirrored row
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int c = col0 + j;
-      if (row_ok && c < a.cols && c > row) out_b[static_cast<long long>(c) * a.ld_out + row] = __float2bfloat16_rn(v[j]);
-    }
+    __nv_bfloat16 *out_b = a.out + static_cast<long long>(b) * a.mstride_out;
+    // upper triangle including the diagonal, stored as computed: element (row, c) with c >= row
+    region_write_row(rg, lane, v);
+    __syncwarp();
+    const bool below_free = col0 >= warp_row0 + 31;   // no element of the chunk lies below the diagonal
+    region_store(
+        rg, lane, out_b + static_cast<long long>(warp_row0) * a.ld_out + col0, a.ld_out,
+        [&](int i, int j) { return warp_row0 + i < rows && col0 + j < cols && col0 + j >= warp_row0 + i; },
+        [&](int i) { return warp_row0 + i < rows && col0 + 32 <= cols && (below_free || col0 >= warp_row0 + i); });
+    __syncwarp();
+    // strictly upper part mirrored: element (row, c) also stored at (c, row); the region holds the transposed
+    // chunk, whose row i is output row col0 + i, columns warp_row0 .. +31
+    region_write_col(rg, lane, v);
+    __syncwarp();
+    region_store(
+        rg, lane, out_b + static_cast<long long>(col0) * a.ld_out + warp_row0, a.ld_out,
+        [&](int i, int j) { return col0 + i < cols && warp_row0 + j < rows && col0 + i > warp_row0 + j; },
+        [&](int i) { return col0 + i < cols && warp_row0 + 32 <= rows && col0 + i > warp_row0 + 31; });
   } else {
     const float sc = a.scale != nullptr ? a.scale[b] : 1.f;
     float xv[32];
-    ring_aux_row(aux_slot, rloc, half, xv);
+    region_read_row(rg, lane, xv);
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = sc * (a.coef_a * xv[j] + v[j]);
-    if (row >= a.rows) return;
+    __syncwarp();
     if constexpr (EPI == EPI_APPLY) {
-      __nv_bfloat16 *o_row = a.out + static_cast<long long>(b) * a.mstride_out + static_cast<long long>(row) * a.ld_out;
-      if (col0 + 32 <= a.cols) {
-        store_bf16x32(o_row + col0, v);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (col0 + j < a.cols) o_row[col0 + j] = __float2bfloat16_rn(v[j]);
-      }
+      region_write_row(rg, lane, v);
+      __syncwarp();
+      region_store(
+          rg, lane, a.out + static_cast<long long>(b) * a.mstride_out + static_cast<long long>(warp_row0) * a.ld_out +
+                        col0,
+          a.ld_out, [&](int i, int j) { return warp_row0 + i < rows && col0 + j < cols; },
+          [&](int i) { return warp_row0 + i < rows && col0 + 32 <= cols; });
     } else {
-      const long long mat_elems = static_cast<long long>(a.rows) * a.cols;
+      const long long mat_elems = static_cast<long long>(rows) * cols;
       void *base = a.params != nullptr ? a.params[b]
                                        : static_cast<void *>(static_cast<char *>(a.out_dense) +
                                                              static_cast<long long>(b) * mat_elems *
                                                                  (a.out_dtype == MUON_F32 ? 4 : 2));
-      final_store(a, base, row, rloc, col0, half, param_slot, param_staged, v);
+      if (a.out_dtype == MUON_F32) {
+        if (row < rows) final_store_f32(a, base, row, col0, v);
+        return;
+      }
+      const bool update = a.params != nullptr;
+      __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(base);
+      if (!a.transposed) {
+        // stored wide: region row i = stored row warp_row0 + i, columns col0 ..
+        __nv_bfloat16 *blk = p + static_cast<long long>(warp_row0) * a.orig_cols + col0;
+        auto ok = [&](int i, int j) { return warp_row0 + i < rows && col0 + j < cols; };
+        auto full = [&](int i) { return warp_row0 + i < rows && col0 + 32 <= cols; };
+        if (update) {
+          region_load(rg, lane, blk, a.orig_cols, ok, full);
+          __syncwarp();
+          float pv[32];
+          region_read_row(rg, lane, pv);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = param_update(pv[j], v[j], a);
+          __syncwarp();
+        }
+        region_write_row(rg, lane, v);
+        __syncwarp();
+        region_store(rg, lane, blk, a.orig_cols, ok, full);
+      } else {
+        // stored tall: stored row col0 + i holds wide column col0 + i; its elements warp_row0 .. are wide rows
+        __nv_bfloat16 *blk = p + static_cast<long long>(col0) * a.orig_cols + warp_row0;
+        auto ok = [&](int i, int j) { return col0 + i < cols && warp_row0 + j < rows; };
+        auto full = [&](int i) { return col0 + i < cols && warp_row0 + 32 <= rows; };
+        if (update) {
+          region_load(rg, lane, blk, a.orig_cols, ok, full);
+          __syncwarp();
+          float pv[32];
+          region_read_col(rg, lane, pv);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = param_update(pv[j], v[j], a);
+          __syncwarp();
+        }
+        region_write_col(rg, lane, v);
+        __syncwarp();
+        region_store(rg, lane, blk, a.orig_cols, ok, full);
+      }
     }
   }
 }
 
-// Epilogue loader's parameter staging for one slot (64 columns of a tile) of the final step: 1-D bulk
-// copies of the stored rows, when every copy is a whole, 16-byte-aligned bf16 segment. Returns the
-// bytes it will deliver (0: the epilogue loads the parameters itself).
-__device__ __forceinline__ uint32_t stage_params_bytes(const GemmProblem &a, int b, int row0, int c0,
-                                                       const void *&base) {
-  if (a.params == nullptr || a.out_dtype != MUON_BF16) return 0;
-  base = a.params[b];
-  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (a.orig_cols & 7) != 0) return 0;
-  if (c0 + 64 > a.cols || row0 + BM > a.rows) return 0;
-  return a.transposed ? 64u * BM * 2u : static_cast<uint32_t>(BM) * 64u * 2u;
-}
-
-// Issued by all 32 lanes of the loader warp, each taking every 32nd row segment.
-__device__ __forceinline__ void stage_params_issue(const GemmProblem &a, const void *base, int row0, int c0,
-                                                   uint8_t *dst, uint64_t *bar, int lane) {
-  const __nv_bfloat16 *p = static_cast<const __nv_bfloat16 *>(base);
-  if (!a.transposed) {
-    for (int r = lane; r < BM; r += 32)
-      bulk_load(dst + r * PARAM_PITCH_WIDE, p + static_cast<long long>(row0 + r) * a.orig_cols + c0, 128, bar);
-  } else {
-    for (int j = lane; j < 64; j += 32)
-      bulk_load(dst + j * PARAM_PITCH_TALL, p + static_cast<long long>(c0 + j) * a.orig_cols + row0, BM * 2, bar);
-  }
-}
-
-template <int EPI, bool B_MN>
+template <int EPI, bool B_MN, int STAGES, int RING_SLOTS>
 __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_constant__ GemmGroup args) {
-  constexpr int STAGES = stages_of(EPI);
+  static_assert(STAGES <= MAX_STAGES && RING_SLOTS <= MAX_RING_SLOTS, "pipeline shape");
   constexpr int SLOT_BYTES = ring_slot_bytes(EPI);
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -382,7 +401,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       mbar_init(&ctrl->acc_full[s], 1);
       mbar_init(&ctrl->acc_empty[s], EPI_WARPS);
     }
-    for (int s = 0; s < RING_SLOTS; ++s) {
+    for (int s = 0; s < MAX_RING_SLOTS; ++s) {
       mbar_init(&ctrl->ring_full[s], 1);
       mbar_init(&ctrl->ring_empty[s], EPI_WARPS);
     }
@@ -418,7 +437,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       int last_parity[MAX_STAGES];
       for (int s = 0; s < MAX_STAGES; ++s) last_parity[s] = -1;
       bool ok = true;
-      for (long long t = first; ok && t < args.total_tiles; t += stride) {
+      int local = 0;
+      for (long long t = first; ok && t < args.total_tiles; t += stride, ++local) {
+        unsigned long long *rec = tl_rec(args, local);
+        if (rec) {
+          rec[0] = static_cast<unsigned long long>(t);
+          rec[1] = globaltimer_ns();
+        }
         // descriptor fields copied to registers: the asm below clobbers memory, which would otherwise force a
         // reload from parameter space on every use
         const int pi = find_problem(args, t);
@@ -456,6 +481,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
             phase ^= 1u;
           }
         }
+        if (rec) rec[2] = globaltimer_ns();
       }
       // every armed stage's copies have landed before the CTA may exit
       for (int s = 0; s < STAGES; ++s)
@@ -468,8 +494,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       bool issued = false;
-      for (long long t = first; ok && t < args.total_tiles; t += stride) {
+      int local = 0;
+      for (long long t = first; ok && t < args.total_tiles; t += stride, ++local) {
+        unsigned long long *rec = tl_rec(args, local);
         if (!wait_bounded(&ctrl->acc_empty[acc], acc_phase ^ 1u, ctl, ERR_WAIT_ACC_EMPTY)) break;
+        if (rec) rec[3] = globaltimer_ns();
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
         const int k_iters = args.prob[find_problem(args, t)].k_iters;
@@ -478,6 +507,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
             ok = false;
             break;
           }
+          if (rec && (kk == 0 || kk == k_iters - 1)) rec[kk == 0 ? 4 : 5] = globaltimer_ns();
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
@@ -497,6 +527,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         }
         if (!ok) break;
         tc_commit(&ctrl->acc_full[acc]);
+        if (rec) rec[6] = globaltimer_ns();
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
@@ -508,11 +539,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
     }
   } else if (warp == LOADER_WARP) {
     if constexpr (EPI != EPI_GRAM) {
-      // ---------------------------------------------------------------- epilogue loader (whole warp: lane 0
-      // owns the ring barriers and the TMA loads, all lanes share the parameter row copies)
+      // ---------------------------------------------------------------- epilogue loader (lane 0 owns the
+      // ring barriers and the TMA loads; the warp stays converged for the barrier broadcasts)
       uint32_t slot = 0, rphase = 0;
-      int last_parity[RING_SLOTS];
-      for (int s = 0; s < RING_SLOTS; ++s) last_parity[s] = -1;
+      int last_parity[MAX_RING_SLOTS];
+      for (int s = 0; s < MAX_RING_SLOTS; ++s) last_parity[s] = -1;
       bool ok = true;
       for (long long t = first; ok && t < args.total_tiles; t += stride) {
         const int pi = find_problem(args, t);
@@ -534,12 +565,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
             break;
           }
           uint8_t *dst = ring + slot * SLOT_BYTES;
-          uint32_t pbytes = 0;
-          const void *pbase = nullptr;
-          if constexpr (EPI == EPI_FINAL) pbytes = stage_params_bytes(P, b, row0, c0, pbase);
           if (lane == 0) {
-            ctrl->ring_param_ok[slot] = pbytes != 0;
-            mbar_arrive_expect_tx(&ctrl->ring_full[slot], RING_AUX_BYTES + pbytes);
+            mbar_arrive_expect_tx(&ctrl->ring_full[slot], RING_AUX_BYTES);
             if constexpr (EPI == EPI_POLY) {
               tma_load_3d(dst, aux_map, &ctrl->ring_full[slot], c0, row0, b);
             } else {
@@ -547,10 +574,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
               tma_load_3d(dst + 64 * 128, aux_map, &ctrl->ring_full[slot], c0, row0 + 64, b);
             }
           }
-          __syncwarp();   // the expected byte count is registered before any lane's copy can complete
-          if constexpr (EPI == EPI_FINAL) {
-            if (pbytes) stage_params_issue(P, pbase, row0, c0, dst + RING_AUX_BYTES, &ctrl->ring_full[slot], lane);
-          }
+          __syncwarp();
           last_parity[slot] = static_cast<int>(rphase);
           if (++slot == RING_SLOTS) {
             slot = 0;
@@ -565,10 +589,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
   } else {
     // ---------------------------------------------------------------- epilogue (warps 2..9)
     const int lane_base = (warp % 4) * 32;  // TMEM lanes this warp may read
-    const int rloc = lane_base + lane;      // this thread's row within the tile
     const int my_half = (warp - 2) / 4;     // which 32-column half of each 64-column slot
     uint32_t acc = 0, acc_phase = 0, slot = 0, rphase = 0;
-    for (long long t = first; t < args.total_tiles; t += stride) {
+    int local = 0;
+    for (long long t = first; t < args.total_tiles; t += stride, ++local) {
+      unsigned long long *rec = (warp == 2 && lane == 0) ? tl_rec(args, local) : nullptr;
       // by value: epilogue stores could alias a reference into parameter space and force reloads
       const GemmProblem P = args.prob[find_problem(args, t)];
       int b, ti, tj;
@@ -577,9 +602,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       // warp-collective TMEM loads below never run with part of the warp gone
       bool ok = wait_bounded(&ctrl->acc_full[acc], acc_phase, ctl, ERR_WAIT_ACC_FULL);
       if (!__all_sync(0xffffffffu, ok)) break;
+      if (rec) rec[7] = globaltimer_ns();
       tc_fence_after();
       const int row0 = ti * BM;
-      const int row = row0 + rloc;
       const int warp_row0 = row0 + lane_base;
       bool aborted = false;
 #pragma unroll 1
@@ -587,26 +612,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         const int c0 = tj * BN + 64 * s;
         if (c0 >= P.cols) break;
         if (EPI != EPI_GRAM && !slot_used(args.symmetric, c0, row0)) continue;
-        const uint8_t *slot_ptr = ring + slot * SLOT_BYTES;
-        bool staged = false;
+        // GRAM has no second input: slot 0 serves only as staging space
+        uint8_t *slot_ptr = ring + (EPI == EPI_GRAM ? 0 : slot) * SLOT_BYTES;
         if constexpr (EPI != EPI_GRAM) {
           ok = wait_bounded(&ctrl->ring_full[slot], rphase, ctl, ERR_WAIT_RING_FULL);
           if (!__all_sync(0xffffffffu, ok)) {
             aborted = true;
             break;
           }
-          staged = ctrl->ring_param_ok[slot] != 0;
         }
         {
-          const int half = my_half;
-          const int col0 = c0 + 32 * half;
+          const int col0 = c0 + 32 * my_half;
           // warp-uniform: chunk past the last column, below the diagonal for every lane, or past the last row
           if (col0 < P.cols && !(args.symmetric && col0 + 31 < warp_row0) && warp_row0 < P.rows) {
             float v[32];
             tmem_ld_32x32b_x32(tmem_base + acc * ACC_COLS + (static_cast<uint32_t>(lane_base) << 16) +
                                    (col0 - tj * BN),
                                v);
-            epilogue_chunk<EPI>(P, b, row, rloc, col0, half, slot_ptr, slot_ptr + RING_AUX_BYTES, staged, v);
+            const Region rg{slot_ptr, lane_base, my_half};
+            epilogue_chunk<EPI>(P, b, warp_row0, lane, col0, rg, v);
+            __syncwarp();   // every lane's region reads are done before the region is written again
           }
         }
         if constexpr (EPI != EPI_GRAM) {
@@ -619,6 +644,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         }
       }
       if (aborted) break;
+      if (rec) rec[8] = globaltimer_ns();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctrl->acc_empty[acc]);
@@ -672,19 +698,20 @@ bool make_map(CUtensorMap *map, const void *base, long long inner, long long row
   return r == CUDA_SUCCESS;
 }
 
-template <int EPI, bool B_MN>
-muon_status launch_group(const GemmGroup &g, int32_t kind, cudaStream_t s) {
+template <int EPI, bool B_MN, int STAGES, int SLOTS>
+muon_status launch_shape(const GemmGroup &g, int32_t kind, cudaStream_t s) {
+  constexpr size_t SMEM = smem_bytes(EPI, STAGES, SLOTS);
   static std::once_flag attr_once[64];
   int dev = 0;
   cudaGetDevice(&dev);
   std::call_once(attr_once[dev & 63], [] {
-    cudaFuncSetAttribute(ns_gemm_kernel<EPI, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem_bytes(EPI)));
+    cudaFuncSetAttribute(ns_gemm_kernel<EPI, B_MN, STAGES, SLOTS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(SMEM));
   });
   if (g.total_tiles <= 0) return MUON_OK;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = smem_bytes(EPI);
+  cfg.dynamicSmemBytes = SMEM;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -700,14 +727,14 @@ muon_status launch_group(const GemmGroup &g, int32_t kind, cudaStream_t s) {
   if (max_clusters[dev & 63] == 0) {
     int n = 0;
     cfg.gridDim = dim3(2 * (device_sm_count() / 2));
-    if (cudaOccupancyMaxActiveClusters(&n, ns_gemm_kernel<EPI, B_MN>, &cfg) != cudaSuccess || n < 1)
+    if (cudaOccupancyMaxActiveClusters(&n, ns_gemm_kernel<EPI, B_MN, STAGES, SLOTS>, &cfg) != cudaSuccess || n < 1)
       n = device_sm_count() / 2;
     max_clusters[dev & 63] = n;
   }
   const long long ncl = g.total_tiles < max_clusters[dev & 63] ? g.total_tiles : max_clusters[dev & 63];
   cfg.gridDim = dim3(static_cast<unsigned>(2 * ncl));
   launch_begin(kind, s);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<EPI, B_MN>, g);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<EPI, B_MN, STAGES, SLOTS>, g);
   launch_end(s);
   return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
 }
@@ -857,12 +884,25 @@ muon_status GemmBatch::launch(cudaStream_t s) {
     g.total_tiles = tiles;
     g.err = err_;
     g.timeout_ns = timeout_ns_;
+    debug_timeline(&g.timeline, &g.timeline_cap);
+    int max_k = 0;
+    for (int i = 0; i < cnt; ++i) max_k = g.prob[i].k_iters > max_k ? g.prob[i].k_iters : max_k;
+    const bool short_k = max_k <= SHORT_K_ITERS;
     muon_status st;
     switch (epi_) {
-      case EPI_GRAM: st = launch_group<EPI_GRAM, false>(g, KK_GRAM, s); break;
-      case EPI_POLY: st = launch_group<EPI_POLY, false>(g, KK_POLY, s); break;
-      case EPI_APPLY: st = launch_group<EPI_APPLY, true>(g, KK_APPLY, s); break;
-      default: st = launch_group<EPI_FINAL, true>(g, KK_FINAL, s); break;
+      case EPI_GRAM: st = launch_shape<EPI_GRAM, false, 4, 1>(g, KK_GRAM, s); break;
+      case EPI_POLY:
+        st = short_k ? launch_shape<EPI_POLY, false, 3, 5>(g, KK_POLY, s)
+                     : launch_shape<EPI_POLY, false, 4, 2>(g, KK_POLY, s);
+        break;
+      case EPI_APPLY:
+        st = short_k ? launch_shape<EPI_APPLY, true, 3, 5>(g, KK_APPLY, s)
+                     : launch_shape<EPI_APPLY, true, 4, 2>(g, KK_APPLY, s);
+        break;
+      default:
+        st = short_k ? launch_shape<EPI_FINAL, true, 3, 5>(g, KK_FINAL, s)
+                     : launch_shape<EPI_FINAL, true, 4, 2>(g, KK_FINAL, s);
+        break;
     }
     if (st != MUON_OK) return st;
   }

@@ -74,6 +74,7 @@ SIGNATURES = {
     "muon_set_timeout_ns": (None, [ctypes.c_uint64]),
     "muon_debug_wait_timeout": (ctypes.c_int, [_vp, ctypes.c_size_t, ctypes.c_uint64, _vp]),
     "muon_launch_count": (ctypes.c_int64, []),
+    "muon_debug_timeline": (ctypes.c_int, [_vp, ctypes.c_int64, ctypes.c_int32]),
     "muon_trace_enable": (None, [ctypes.c_int]),
     "muon_trace_collect": (ctypes.c_int64, [_vp, _vp, _c_int64]),
     "muon_kernel_name": (ctypes.c_char_p, [ctypes.c_int32]),
@@ -258,6 +259,15 @@ def muon_set_timeout_ns(ns: int):
 def muon_debug_wait_timeout(ws, timeout_ns: int, stream=None):
     _check(lib().muon_debug_wait_timeout(ws.data_ptr(), ws.numel() * ws.element_size(), int(timeout_ns),
                                          _stream(stream)), "muon_debug_wait_timeout")
+
+
+def muon_debug_timeline(buf, records_per_cta: int):
+    """Registers (or, with buf None, unregisters) a device buffer for per-tile GEMM timestamps."""
+    if buf is None:
+        _check(lib().muon_debug_timeline(None, 0, 0), "muon_debug_timeline")
+    else:
+        _check(lib().muon_debug_timeline(buf.data_ptr(), buf.numel() * buf.element_size(), records_per_cta),
+               "muon_debug_timeline")
 
 
 def muon_launch_count() -> int:

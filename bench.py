@@ -225,6 +225,17 @@ def oracle_sample_time(budget_s: float = 20.0):
 
 # ------------------------------------------------------------------------------------------------ arms
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest replica's value (the job's time is the max over ranks)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -276,12 +287,6 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
 
     # warm-up
     for _ in range(args.warmup):
@@ -303,7 +308,7 @@ def run_ours(args):
         torch.cuda.synchronize()
     barrier()
     launches = L.muon_launch_count() - launches0
-    ms = max_over_ranks(start.elapsed_time(end) / args.steps)
+    ms = max_over_ranks(start.elapsed_time(end) / args.steps, world, device)
     clk = clocks.summary(peaks.get("sm_max_mhz"))
 
     # traced pass: per-kernel durations from events around each launch (same steps, same stream)
@@ -377,7 +382,7 @@ def run_ours(args):
         stream.synchronize()
     end.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(1e3 * (time.perf_counter() - t0) / e2e_steps)
+    e2e_ms = max_over_ranks(1e3 * (time.perf_counter() - t0) / e2e_steps, world, device)
     barrier()
     if L.muon_check(wl.ws) != L.MUON_OK:
         raise RuntimeError("a device-side wait ran out during the timed steps")
@@ -443,7 +448,7 @@ def run_ns_sweep(args):
     for n in sizes:
         x = workloads.ns_sweep_input(n, K, 0, device="cuda:0")
         out = torch.empty_like(x)
-        ws = torch.empty(L.muon_workspace_bytes(K, n, n), dtype=torch.uint8, device=dev)
+        ws = torch.zeros(L.muon_workspace_bytes(K, n, n), dtype=torch.uint8, device=dev)
         reps = 3 if n >= 4096 else 10
         for _ in range(2):
             L.ns_orthogonalize(x, out, coeffs, 1e-7, ws)

@@ -90,7 +90,8 @@ size_t muon_workspace_bytes(int64_t K, int64_t A, int64_t B);
  *   momentum  device, fp32, contiguous (K, A, B); updated in place. Zero before the first step.
  *   pdt, gdt  MUON_F32 or MUON_BF16 each.
  *   hp        host struct; hp->coeffs host array of 3*ns_steps floats.
- *   ws        device workspace of ws_bytes >= muon_workspace_bytes(K, A, B), 256-byte aligned.
+ *   ws        device workspace of ws_bytes >= muon_workspace_bytes(K, A, B), 256-byte aligned, zero-filled
+ *             before its first use (its first bytes hold the error word, which only muon_check clears).
  * Limits: 1 <= A, B <= 65536; K * max(A,B) * min(A,B) < 2^40. */
 muon_status muon_step_batched(void *const *params, muon_dtype pdt, const void *const *grads, muon_dtype gdt,
                               float *momentum, int64_t K, int64_t A, int64_t B, const muon_hparams *hp, void *ws,
@@ -114,8 +115,8 @@ size_t muon_workspace_bytes_grouped(const muon_bucket *buckets, int n);
  * grouped tensor-core launch ([P4] section 2.2, batching matrices of similar shapes; [P1] the stacked
  * (K, ...) Muon groups). Results are identical to n muon_step_batched calls.
  *   buckets   HOST array of n bucket descriptors (1 <= n <= 4096).
- *   ws        device workspace of ws_bytes >= muon_workspace_bytes_grouped(buckets, n), 256-byte aligned;
- *             its first 256 bytes are the control block muon_check reads.
+ *   ws        device workspace of ws_bytes >= muon_workspace_bytes_grouped(buckets, n), 256-byte aligned,
+ *             zero-filled before its first use; its first 256 bytes are the control block muon_check reads.
  * Errors as for muon_step_batched, checked for every bucket before anything is launched. */
 muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hparams *hp, void *ws, size_t ws_bytes,
                               muon_stream_t stream);
@@ -195,6 +196,16 @@ void muon_set_timeout_ns(uint64_t ns);
 /* Launches one kernel that waits on a barrier nothing will complete, with the given limit,
  * so that the bounded-wait path can be exercised: afterwards muon_check returns MUON_ERR_TIMEOUT. */
 muon_status muon_debug_wait_timeout(void *ws, size_t ws_bytes, uint64_t timeout_ns, muon_stream_t stream);
+
+/* Performance analysis: while a buffer is registered, the tensor-core launches that follow write, per CTA
+ * and per tile they process (up to records_per_cta), ten 64-bit words: tile index, producer first and last
+ * copy issue, MMA start (accumulator free), first and last operands ready, last MMA commit, epilogue start
+ * and end (globaltimer nanoseconds; 0 = not reached). The buffer is cut into regions of (SM count) *
+ * records_per_cta * 10 words; the i-th launch after registration fills region i (record r of CTA c at word
+ * (c * records_per_cta + r) * 10 of it) and launches beyond the last region record nothing.
+ * buf: device memory, zero-filled by the caller. buf = NULL unregisters. Returns MUON_ERR_WORKSPACE if the
+ * buffer holds less than one region. No counterpart on the pages. */
+muon_status muon_debug_timeline(void *buf, int64_t bytes, int32_t records_per_cta);
 
 /* Number of kernels this library has launched since it was loaded. */
 int64_t muon_launch_count(void);
