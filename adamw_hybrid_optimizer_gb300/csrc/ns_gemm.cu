@@ -9,13 +9,14 @@
 //     X' = a X + H X                EPI_APPLY  B operand (X) is read N-major
 //     last step: u = a X + H X, then p <- p - lr*wd*p*mask - lr*scale*u      EPI_FINAL
 //
-// Design (sm_103a): 128 x 256 output tiles, 64-deep k-slices, a TMA ring with 128-byte swizzle
-// (4 stages, 3 when the contraction is short), one tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) per 16-slice
-// issued by one thread, fp32 accumulators in tensor memory (2 x 256 columns, so the epilogue of one
+// Design (sm_103a): 128 x 256 output tiles per CTA, 64-deep k-slices, a TMA ring with 128-byte swizzle
+// (6 stages, 4 when the contraction is short), one tcgen05.mma per 16-slice issued by one thread, fp32 accumulators in tensor memory (2 x 256 columns, so the epilogue of one
 // tile overlaps the MMAs of the next), persistent CTAs (one per SM) striding over the tiles of up to
-// GEMM_MAX_PROBLEMS stacks at once. CTAs run as clusters of two that compute vertically adjacent tiles
-// (rows 2p and 2p+1 of one tile column): both need the same B operand, so each CTA loads one half of it
-// and multicasts it to both, which cuts the operand traffic per SM by a third. Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM
+// GEMM_MAX_PROBLEMS stacks at once. CTAs run as pairs (clusters of two) on vertically adjacent tiles
+// (rows 2p and 2p+1 of one tile column) with paired-SM MMAs (tcgen05 cta_group::2, M = 256): each CTA
+// holds its 128 rows of A and one half of B, the even CTA issues the MMAs, and each CTA's tensor memory
+// receives its own 128 accumulator rows. Per SM a 64-deep stage is 32 KB instead of 48 KB, which halves
+// the shared-memory traffic per MMA and leaves room for 6 stages (or 4 stages and a 5-slot ring). Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM
 // owner), warps 2-9 = epilogue (two per tensor-memory lane quarter, each taking one 32-column half of
 // every 64-column slot), warp 10 = epilogue loader: ahead of the epilogue it TMA-loads each tile's second
 // input (G or X) into a shared-memory ring (2 or 5 slots, by contraction depth). Each epilogue warp then
@@ -38,10 +39,10 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int MAX_STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int MAX_STAGES = 6;
+constexpr int A_BYTES = BM * BK * 2;                  // this CTA's 128 rows of A
+constexpr int B_HALF_BYTES = (BN / 2) * BK * 2;       // this CTA's half (128 of 256 columns) of B
+constexpr int STAGE_BYTES = A_BYTES + B_HALF_BYTES;
 constexpr int ACC_COLS = BN;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int EPI_WARPS = 8;                                // two per TMEM lane quarter
@@ -75,8 +76,8 @@ __host__ __device__ constexpr size_t smem_bytes(int epi, int stages, int slots) 
          sizeof(Ctrl) + 1024;
 }
 constexpr int SHORT_K_ITERS = 32;   // contractions up to 2048 take the deep-ring shape
-static_assert(smem_bytes(EPI_GRAM, 4, 1) <= 232448 && smem_bytes(EPI_APPLY, 4, 2) <= 232448 &&
-                  smem_bytes(EPI_APPLY, 3, 5) <= 232448,
+static_assert(smem_bytes(EPI_GRAM, 6, 1) <= 232448 && smem_bytes(EPI_APPLY, 6, 2) <= 232448 &&
+                  smem_bytes(EPI_APPLY, 4, 5) <= 232448,
               "shared memory over budget");
 
 // Kernel parameter: up to GEMM_MAX_PROBLEMS problems of one step kind, in order of tile_begin.
@@ -395,11 +396,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&ctrl->full[s], 1);
-      mbar_init(&ctrl->empty[s], 2);   // both CTAs' MMAs read each stage (B halves are shared)
+      mbar_init(&ctrl->empty[s], 1);   // the pair MMA's commit, multicast to both CTAs
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctrl->acc_full[s], 1);
-      mbar_init(&ctrl->acc_empty[s], EPI_WARPS);
+      mbar_init(&ctrl->acc_empty[s], 2 * EPI_WARPS);   // both CTAs' epilogue warps (even CTA's copy used)
     }
     for (int s = 0; s < MAX_RING_SLOTS; ++s) {
       mbar_init(&ctrl->ring_full[s], 1);
@@ -413,8 +414,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
     tma_prefetch_desc(lane & 1 ? &args.map_b[lane >> 1] : &args.map_a[lane >> 1]);
   }
   if (warp == 1) {
-    tmem_alloc(&ctrl->tmem_base, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(&ctrl->tmem_base, TMEM_COLS);   // jointly with the peer CTA's warp 1
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncwarp();     // the cluster barrier is warp-aligned
@@ -429,6 +430,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
   const uint32_t rank = cluster_ctarank();
   const long long first = blockIdx.x >> 1;
   const long long stride = gridDim.x >> 1;
+  // the even CTA's copies of the stage-full and accumulator-free barriers, as cluster addresses
+  const uint32_t leader_full0 = mapa_shared(smem_u32(&ctrl->full[0]), 0);
+  const uint32_t leader_acc_empty0 = mapa_shared(smem_u32(&ctrl->acc_empty[0]), 0);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -458,23 +462,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&ctrl->full[stage], STAGE_BYTES);
-          last_parity[stage] = static_cast<int>(phase);
+          // both CTAs' copies complete on the even CTA's barrier, which the even CTA arms for both
+          if (rank == 0) {
+            mbar_arrive_expect_tx(&ctrl->full[stage], 2 * STAGE_BYTES);
+            last_parity[stage] = static_cast<int>(phase);
+          }
+          const uint32_t fb = leader_full0 + stage * static_cast<uint32_t>(sizeof(uint64_t));
           uint8_t *sa = smem + stage * STAGE_BYTES;
           uint8_t *sb = sa + A_BYTES;
-          tma_load_3d(sa, map_a, &ctrl->full[stage], kk * BK, ti * BM, b);
-          // this CTA's half of the shared B operand, delivered to both CTAs of the pair
+          tma_load_3d_pair(sa, map_a, fb, kk * BK, ti * BM, b);
+          // this CTA's half of B: columns tj*256 + 128*rank .. +127
           if constexpr (!B_MN) {
-            // K-major: rows tj*256 + 128*rank .. +127 through the A map (same tensor, box 64 x 128)
-            tma_load_3d_mc(sb + rank * (B_BYTES / 2), map_a, &ctrl->full[stage], kk * BK,
-                           tj * BN + (BN / 2) * static_cast<int>(rank), b, 0x3);
+            // K-major: those rows of the same tensor through the A map (box 64 x 128)
+            tma_load_3d_pair(sb, map_a, fb, kk * BK, tj * BN + (BN / 2) * static_cast<int>(rank), b);
           } else {
             // N-major: column chunks 2*rank and 2*rank+1 (64 columns each)
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              const int c = 2 * static_cast<int>(rank) + q;
-              tma_load_3d_mc(sb + c * (64 * BK * 2), map_b, &ctrl->full[stage], tj * BN + 64 * c, kk * BK, b, 0x3);
-            }
+            for (int q = 0; q < 2; ++q)
+              tma_load_3d_pair(sb + q * (64 * BK * 2), map_b, fb, tj * BN + 64 * (2 * static_cast<int>(rank) + q),
+                               kk * BK, b);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -488,9 +494,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         if (last_parity[s] >= 0) drain_wait(&ctrl->full[s], static_cast<uint32_t>(last_parity[s]), ctl);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false, B_MN);
+    if (lane == 0 && rank == 0) {
+      // ---------------------------------------------------------------- MMA issuer (even CTA: M = 256 pair MMAs)
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN, false, B_MN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       bool issued = false;
@@ -516,24 +522,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
             const uint64_t adesc = smem_desc_sw128(sa + k * 32, 16, 1024);
             const uint64_t bdesc =
                 B_MN ? smem_desc_sw128(sb + k * 16 * 128, 64 * BK * 2, 1024) : smem_desc_sw128(sb + k * 32, 16, 1024);
-            tc_mma_bf16(d_tmem, adesc, bdesc, idesc, (kk | k) != 0 ? 1u : 0u);
+            tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kk | k) != 0 ? 1u : 0u);
           }
           issued = true;
-          tc_commit_mc(&ctrl->empty[stage], 0x3);   // frees the stage in both CTAs of the pair
+          tc_commit_pair_mc(&ctrl->empty[stage], 0x3);   // frees the stage in both CTAs of the pair
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(&ctrl->acc_full[acc]);
+        tc_commit_pair_mc(&ctrl->acc_full[acc], 0x3);    // both CTAs' accumulator halves are ready
         if (rec) rec[6] = globaltimer_ns();
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
       // all MMAs this thread issued have completed before TMEM is released
       if (issued) {
-        tc_commit(&ctrl->drain);
+        tc_commit_pair_mc(&ctrl->drain, 0x1);
         drain_wait(&ctrl->drain, 0u, ctl);
       }
     }
@@ -647,7 +653,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       if (rec) rec[8] = globaltimer_ns();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctrl->acc_empty[acc]);
+      // the accumulator is free once both CTAs' epilogues have read their halves (even CTA's barrier)
+      if (lane == 0) mbar_arrive_cluster(leader_acc_empty0 + acc * static_cast<uint32_t>(sizeof(uint64_t)));
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -659,7 +666,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
   cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
@@ -890,18 +897,18 @@ muon_status GemmBatch::launch(cudaStream_t s) {
     const bool short_k = max_k <= SHORT_K_ITERS;
     muon_status st;
     switch (epi_) {
-      case EPI_GRAM: st = launch_shape<EPI_GRAM, false, 4, 1>(g, KK_GRAM, s); break;
+      case EPI_GRAM: st = launch_shape<EPI_GRAM, false, 6, 1>(g, KK_GRAM, s); break;
       case EPI_POLY:
-        st = short_k ? launch_shape<EPI_POLY, false, 3, 5>(g, KK_POLY, s)
-                     : launch_shape<EPI_POLY, false, 4, 2>(g, KK_POLY, s);
+        st = short_k ? launch_shape<EPI_POLY, false, 4, 5>(g, KK_POLY, s)
+                     : launch_shape<EPI_POLY, false, 6, 2>(g, KK_POLY, s);
         break;
       case EPI_APPLY:
-        st = short_k ? launch_shape<EPI_APPLY, true, 3, 5>(g, KK_APPLY, s)
-                     : launch_shape<EPI_APPLY, true, 4, 2>(g, KK_APPLY, s);
+        st = short_k ? launch_shape<EPI_APPLY, true, 4, 5>(g, KK_APPLY, s)
+                     : launch_shape<EPI_APPLY, true, 6, 2>(g, KK_APPLY, s);
         break;
       default:
-        st = short_k ? launch_shape<EPI_FINAL, true, 3, 5>(g, KK_FINAL, s)
-                     : launch_shape<EPI_FINAL, true, 4, 2>(g, KK_FINAL, s);
+        st = short_k ? launch_shape<EPI_FINAL, true, 4, 5>(g, KK_FINAL, s)
+                     : launch_shape<EPI_FINAL, true, 6, 2>(g, KK_FINAL, s);
         break;
     }
     if (st != MUON_OK) return st;
