@@ -252,6 +252,38 @@ __device__ __forceinline__ void region_load(const Region &g, int lane, const __n
   for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(g.piece(8 * k + (lane >> 2), q)) = w[k];
 }
 
+// A 32 x 32 block of bf16 parameters as the final step reads it: block row i at base + i*ld, elements
+// 0..31; rows below ilim and elements below jlim exist.
+struct ParamBlock {
+  const __nv_bfloat16 *base;
+  long long ld;
+  int ilim, jlim;
+  bool valid;
+};
+
+// Issues this lane's four 16-byte loads of a block (segment-wise: row 8k + lane/4, piece lane%4) into
+// registers; they complete while the caller works on something else.
+__device__ __forceinline__ void block_fetch(const ParamBlock &pb, int lane, uint4 (&w)[4]) {
+  const int q = lane & 3;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = 8 * k + (lane >> 2);
+    const __nv_bfloat16 *src = pb.base + static_cast<long long>(i) * pb.ld + 8 * q;
+    if (i < pb.ilim && pb.jlim >= 32 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+      w[k] = *reinterpret_cast<const uint4 *>(src);
+    } else {
+      __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(&w[k]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) h[e] = (i < pb.ilim && 8 * q + e < pb.jlim) ? src[e] : __float2bfloat16_rn(0.f);
+    }
+  }
+}
+
+__device__ __forceinline__ void block_commit(const Region &g, int lane, const uint4 (&w)[4]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(g.piece(8 * k + (lane >> 2), lane & 3)) = w[k];
+}
+
 // Muon parameter update of one element: decoupled decay (masked where u*p <= 0 if cautious), then the
 // scaled orthogonalised step.
 __device__ __forceinline__ float param_update(float pv, float u, const GemmProblem &a) {
@@ -379,6 +411,65 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem &a, int b, int 
       }
     }
   }
+}
+
+// The block of bf16 parameters one final-step chunk updates (stored wide: rows = wide rows; stored tall:
+// rows = wide columns).
+__device__ __forceinline__ ParamBlock param_block(const GemmProblem &a, const __nv_bfloat16 *p, int warp_row0,
+                                                  int col0) {
+  ParamBlock pb;
+  if (!a.transposed) {
+    pb.base = p + static_cast<long long>(warp_row0) * a.orig_cols + col0;
+    pb.ilim = a.rows - warp_row0;
+    pb.jlim = a.cols - col0;
+  } else {
+    pb.base = p + static_cast<long long>(col0) * a.orig_cols + warp_row0;
+    pb.ilim = a.cols - col0;
+    pb.jlim = a.rows - warp_row0;
+  }
+  pb.ld = a.orig_cols;
+  pb.valid = col0 < a.cols && warp_row0 < a.rows;
+  return pb;
+}
+
+// Final-step chunk for bf16 parameters: as epilogue_chunk, with this chunk's parameter block already in
+// flight in pf (fetched one chunk ahead); once pf is in the staging region, the next chunk's block is
+// fetched into pf.
+__device__ __forceinline__ void final_chunk_bf16(const GemmProblem &a, int b, int warp_row0, int lane, int col0,
+                                                 const Region &rg, float *v, uint4 (&pf)[4], const ParamBlock &next) {
+  const float sc = a.scale != nullptr ? a.scale[b] : 1.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float xv[8];
+    unpack8(*reinterpret_cast<const uint4 *>(rg.piece(lane, q)), xv);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[8 * q + e] = sc * (a.coef_a * xv[e] + v[8 * q + e]);
+  }
+  __syncwarp();
+  block_commit(rg, lane, pf);
+  if (next.valid) block_fetch(next, lane, pf);
+  __syncwarp();
+  if (!a.transposed) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float pv[8];
+      unpack8(*reinterpret_cast<const uint4 *>(rg.piece(lane, q)), pv);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[8 * q + e] = param_update(pv[e], v[8 * q + e], a);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = param_update(bf2f(*rg.elem(j, lane)), v[j], a);
+  }
+  __syncwarp();
+  if (!a.transposed) region_write_row(rg, lane, v);
+  else region_write_col(rg, lane, v);
+  __syncwarp();
+  __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(a.params[b]);
+  const ParamBlock pb = param_block(a, p, warp_row0, col0);
+  region_store(
+      rg, lane, const_cast<__nv_bfloat16 *>(pb.base), pb.ld, [&](int i, int j) { return i < pb.ilim && j < pb.jlim; },
+      [&](int i) { return i < pb.ilim && pb.jlim >= 32; });
 }
 
 template <int EPI, bool B_MN, int STAGES, int RING_SLOTS>
@@ -613,6 +704,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       const int row0 = ti * BM;
       const int warp_row0 = row0 + lane_base;
       bool aborted = false;
+      // final step with bf16 parameters: their blocks are fetched one chunk ahead
+      const bool prefetch_params = EPI == EPI_FINAL && P.params != nullptr && P.out_dtype == MUON_BF16;
+      const __nv_bfloat16 *pbase = prefetch_params ? static_cast<const __nv_bfloat16 *>(P.params[b]) : nullptr;
+      uint4 pf[4];
+      bool pf_ready = false;
 #pragma unroll 1
       for (int s = 0; s < BN / 64; ++s) {
         const int c0 = tj * BN + 64 * s;
@@ -636,7 +732,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
                                    (col0 - tj * BN),
                                v);
             const Region rg{slot_ptr, lane_base, my_half};
-            epilogue_chunk<EPI>(P, b, warp_row0, lane, col0, rg, v);
+            if (EPI == EPI_FINAL && prefetch_params) {
+              if (!pf_ready) block_fetch(param_block(P, pbase, warp_row0, col0), lane, pf);
+              ParamBlock next = param_block(P, pbase, warp_row0, col0 + 64);
+              next.valid = next.valid && s + 1 < BN / 64;   // only this warp's next chunk of the same tile
+              final_chunk_bf16(P, b, warp_row0, lane, col0, rg, v, pf, next);
+              pf_ready = next.valid;
+            } else {
+              epilogue_chunk<EPI>(P, b, warp_row0, lane, col0, rg, v);
+            }
             __syncwarp();   // every lane's region reads are done before the region is written again
           }
         }
