@@ -1,17 +1,18 @@
 // Bandwidth-bound kernels of the optimizer step.
 //
-//   nesterov_norm_kernel  momentum M <- mu M + G, Nesterov input U = G + mu M (or M), per-tile sums of
-//                         U^2 for the Frobenius norm, U stored bf16 in the wide orientation
+//   nesterov_norm_kernel  momentum M <- mu M + G, Nesterov input U = G + mu M (or M), U stored bf16 in
+//                         the wide orientation, and the Frobenius scale s_k = 1 / (||U_k||_F + eps)
+//                         from per-tile sums of U^2 added in a fixed order by the matrix's last tile
 //                         ("Optimizers: AdamW, Muon and the distributed optimizer", section "Muon:
 //                         orthogonalising the update": the momentum rule and newton_schulz's first lines).
-//   norm_finalize_kernel  s_k = 1 / (sqrt(sum of the tile sums) + eps), one block per matrix, fixed
-//                         summation order (the result does not depend on scheduling).
+//   counter_reset_kernel  zeroes the per-matrix counters nesterov_norm_kernel counts its tiles in.
 //   adamw kernels         AdamW with bias correction and decoupled decay (same page, section "AdamW:
 //                         decoupled weight decay"), 16-byte vector accesses when aligned.
 //   debug_wait_kernel     one bounded wait on a barrier nothing completes.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <utility>
 
 #include "internal.h"
@@ -30,23 +31,17 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Block of 256 threads on one 64 x 64 tile of the stored (A x B) matrix; thread (tx, ty) handles
-// columns 4*tx..4*tx+3 of rows ty, ty+16, ty+32, ty+48.
+// Block of 256 threads on one 64 x 64 tile (tr, tc) of matrix b of the stored (A x B) stack; thread
+// (tx, ty) handles columns 4*tx..4*tx+3 of rows ty, ty+16, ty+32, ty+48. Returns the thread's sum of U^2.
 template <typename GT, bool MOMENTUM>
-__global__ void __launch_bounds__(256) nesterov_norm_kernel(const NesterovArgs a) {
-  pdl_wait();
-  if (threadIdx.x == 0) pdl_launch_dependents();
+__device__ __forceinline__ float nesterov_tile(const NesterovArgs &a, long long b, int tr, int tc,
+                                               __nv_bfloat16 (*tile)[NESTEROV_TILE + 8]) {
   constexpr int T = NESTEROV_TILE;
-  __shared__ __nv_bfloat16 tile[T][T + 8];
-  __shared__ float red[8];
-  const int b = blockIdx.y;
-  const int tr = blockIdx.x / a.tiles_c;
-  const int tc = blockIdx.x - tr * a.tiles_c;
   const long long mat = static_cast<long long>(a.A) * a.B;
   const GT *g = a.gptrs != nullptr ? static_cast<const GT *>(a.gptrs[b])
-                                   : static_cast<const GT *>(a.gbase) + static_cast<long long>(b) * mat;
-  float *M = MOMENTUM ? a.momentum + static_cast<long long>(b) * mat : nullptr;
-  __nv_bfloat16 *u = a.u + static_cast<long long>(b) * a.mstride_u;
+                                   : static_cast<const GT *>(a.gbase) + b * mat;
+  float *M = MOMENTUM ? a.momentum + b * mat : nullptr;
+  __nv_bfloat16 *u = a.u + b * a.mstride_u;
 
   const int tx = threadIdx.x & 15;
   const int ty = threadIdx.x >> 4;
@@ -144,35 +139,68 @@ __global__ void __launch_bounds__(256) nesterov_norm_kernel(const NesterovArgs a
       }
     }
   }
+  return ss;
+}
+
+// One launch over the tiles of every matrix of up to NESTEROV_MAX_PROBLEMS stacks (blocks in problem order,
+// within a problem matrix by matrix). Each block stores its tile's sum of U^2 and counts itself in the
+// matrix's counter; the block that completes the count sums the matrix's tile sums in index order (the
+// same order whichever block finishes last) and writes s = 1 / (sqrt(sum) + eps).
+template <bool MOMENTUM>
+__global__ void __launch_bounds__(256) nesterov_norm_kernel(const __grid_constant__ NesterovGroup G) {
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  __shared__ __nv_bfloat16 tile[NESTEROV_TILE][NESTEROV_TILE + 8];
+  __shared__ float red[8];
+  __shared__ int last;
+  int pi = 0;
+  while (pi + 1 < G.nprob && static_cast<long long>(blockIdx.x) >= G.block_begin[pi + 1]) ++pi;
+  const NesterovArgs &a = G.prob[pi];
+  const long long tiles = static_cast<long long>(a.tiles_r) * a.tiles_c;
+  const long long local = static_cast<long long>(blockIdx.x) - G.block_begin[pi];
+  const long long b = local / tiles;
+  const long long t = local - b * tiles;
+  const int tr = static_cast<int>(t / a.tiles_c);
+  const int tc = static_cast<int>(t - static_cast<long long>(tr) * a.tiles_c);
+  float ss = a.gdtype == MUON_F32 ? nesterov_tile<float, MOMENTUM>(a, b, tr, tc, tile)
+                                  : nesterov_tile<__nv_bfloat16, MOMENTUM>(a, b, tr, tc, tile);
   ss = warp_sum(ss);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
+  float *partials = a.partials + b * tiles;
   if (threadIdx.x == 0) {
-    float t = 0.f;
+    float sum = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) t += red[w];
-    a.partials[static_cast<long long>(b) * gridDim.x + blockIdx.x] = t;
+    for (int w = 0; w < 8; ++w) sum += red[w];
+    partials[t] = sum;
+    __threadfence();
+    last = atomicAdd(a.counters + b, 1u) == static_cast<unsigned>(tiles - 1);
   }
-}
-
-__global__ void __launch_bounds__(256) norm_finalize_kernel(const float *partials, int tiles, float *scale,
-                                                            float eps) {
-  pdl_wait();
-  if (threadIdx.x == 0) pdl_launch_dependents();
-  __shared__ float red[8];
-  const int b = blockIdx.x;
-  const float *p = partials + static_cast<long long>(b) * tiles;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
   float s = 0.f;
-  for (int i = threadIdx.x; i < tiles; i += 256) s += p[i];
+  for (long long i = threadIdx.x; i < tiles; i += 256) s += __ldcg(partials + i);
   s = warp_sum(s);
+  __syncthreads();   // red is reused
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
   __syncthreads();
   if (threadIdx.x == 0) {
-    float t = 0.f;
+    float sum = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) t += red[w];
-    scale[b] = 1.0f / (sqrtf(t) + eps);
+    for (int w = 0; w < 8; ++w) sum += red[w];
+    a.scale[b] = 1.0f / (sqrtf(sum) + a.eps);
   }
+}
+
+// Zeroes n counters. It lets its successor launch at once, but finishes only after its predecessor
+// has: a successor that waits for this grid so also waits for everything before it.
+__global__ void __launch_bounds__(256) counter_reset_kernel(unsigned *counters, long long n) {
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  pdl_wait();
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    counters[i] = 0u;
 }
 
 // ------------------------------------------------------------------------------------------ AdamW
@@ -303,26 +331,61 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 }  // namespace
 
-muon_status launch_nesterov_norm(const NesterovArgs &a, int K, cudaStream_t s) {
-  const dim3 grid(a.tiles_r * a.tiles_c, K);
-  launch_begin(KK_NESTEROV_NORM, s);
-  const bool mom = a.momentum != nullptr;
-  cudaError_t e;
-  if (a.gdtype == MUON_F32)
-    e = mom ? launch_pdl(nesterov_norm_kernel<float, true>, grid, dim3(256), 0, s, a)
-            : launch_pdl(nesterov_norm_kernel<float, false>, grid, dim3(256), 0, s, a);
-  else
-    e = mom ? launch_pdl(nesterov_norm_kernel<__nv_bfloat16, true>, grid, dim3(256), 0, s, a)
-            : launch_pdl(nesterov_norm_kernel<__nv_bfloat16, false>, grid, dim3(256), 0, s, a);
+muon_status launch_counter_reset(unsigned *counters, long long n, cudaStream_t s) {
+  if (n < 1) return MUON_OK;
+  const long long blocks = std::min<long long>((n + 255) / 256, device_sm_count());
+  launch_begin(KK_COUNTER_RESET, s);
+  const cudaError_t e = launch_pdl(counter_reset_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                                   counters, n);
   launch_end(s);
   return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
 }
 
-muon_status launch_norm_finalize(const float *partials, int tiles, float *scale, int K, float eps, cudaStream_t s) {
-  launch_begin(KK_NORM_FINALIZE, s);
-  const cudaError_t e = launch_pdl(norm_finalize_kernel, dim3(K), dim3(256), 0, s, partials, tiles, scale, eps);
-  launch_end(s);
-  return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+muon_status launch_nesterov_norm(const NesterovArgs *probs, int n, cudaStream_t s) {
+  if (n < 1) return MUON_OK;
+  const bool mom = probs[0].momentum != nullptr;
+  NesterovGroup G{};
+  long long blocks = 0;
+  auto flush = [&]() -> muon_status {
+    if (G.nprob == 0) return MUON_OK;
+    launch_begin(KK_NESTEROV_NORM, s);
+    const dim3 grid(static_cast<unsigned>(blocks));
+    const cudaError_t e = mom ? launch_pdl(nesterov_norm_kernel<true>, grid, dim3(256), 0, s, G)
+                              : launch_pdl(nesterov_norm_kernel<false>, grid, dim3(256), 0, s, G);
+    launch_end(s);
+    G.nprob = 0;
+    blocks = 0;
+    return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+  };
+  constexpr long long MAX_GRID = (1ll << 31) - 1;
+  for (int i = 0; i < n; ++i) {
+    if ((probs[i].momentum != nullptr) != mom) return MUON_ERR_INVALID_ARG;
+    const long long tiles = static_cast<long long>(probs[i].tiles_r) * probs[i].tiles_c;
+    long long done = 0;   // matrices of stack i already placed in a launch
+    while (done < probs[i].K) {
+      if (G.nprob == NESTEROV_MAX_PROBLEMS || blocks + tiles > MAX_GRID) {
+        const muon_status st = flush();
+        if (st != MUON_OK) return st;
+      }
+      const long long fit = std::min<long long>(probs[i].K - done, (MAX_GRID - blocks) / tiles);
+      NesterovArgs p = probs[i];
+      // the launch sees matrices done .. done+fit-1 of the stack as its matrices 0 .. fit-1
+      if (p.gptrs != nullptr) p.gptrs += done;
+      else p.gbase = static_cast<const char *>(p.gbase) + done * static_cast<long long>(p.A) * p.B *
+                                                              (p.gdtype == MUON_F32 ? 4 : 2);
+      if (p.momentum != nullptr) p.momentum += done * static_cast<long long>(p.A) * p.B;
+      p.u += done * p.mstride_u;
+      p.partials += done * tiles;
+      p.scale += done;
+      p.counters += done;
+      p.K = static_cast<int>(fit);
+      G.block_begin[G.nprob] = blocks;
+      G.prob[G.nprob++] = p;
+      blocks += fit * tiles;
+      done += fit;
+    }
+  }
+  return flush();
 }
 
 muon_status launch_adamw(void *p, int pdt, const void *g, int gdt, float *m, float *v, long long n,

@@ -13,7 +13,7 @@ namespace muon {
 enum KernelKind : int32_t {
   KK_ADAMW = 0,
   KK_NESTEROV_NORM = 1,
-  KK_NORM_FINALIZE = 2,
+  KK_COUNTER_RESET = 2,
   KK_GRAM = 3,
   KK_POLY = 4,
   KK_APPLY = 5,
@@ -124,7 +124,7 @@ muon_status launch_final(const Bf16Stack &h, const Bf16Stack &x, float a, const 
 
 // ------------------------------------------------------------------------------------------ elementwise
 
-// Momentum + Nesterov + Frobenius partial sums + bf16 store in the wide orientation.
+// Momentum + Nesterov + Frobenius norm scale + bf16 store in the wide orientation, for one stack.
 struct NesterovArgs {
   const void *const *gptrs;  // device array of K pointers, or null (then gbase is used)
   const void *gbase;         // contiguous (K, A, B)
@@ -132,14 +132,26 @@ struct NesterovArgs {
   float *momentum;           // (K, A, B) fp32 or null (plain normalisation, no momentum)
   __nv_bfloat16 *u;
   long long ldu, mstride_u;
-  float *partials;           // [K][tiles]
-  int A, B, tiles_r, tiles_c, transposed;
-  float mu;
+  float *partials;           // [K][tiles_r * tiles_c]
+  float *scale;              // [K]: s_k = 1 / (||U_k||_F + eps)
+  unsigned *counters;        // [K], zero when the launch starts
+  int K, A, B, tiles_r, tiles_c, transposed;
+  float mu, eps;
   int nesterov;
 };
 constexpr int NESTEROV_TILE = 64;
-muon_status launch_nesterov_norm(const NesterovArgs &a, int K, cudaStream_t s);
-muon_status launch_norm_finalize(const float *partials, int tiles, float *scale, int K, float eps, cudaStream_t s);
+constexpr int NESTEROV_MAX_PROBLEMS = 16;
+struct NesterovGroup {
+  NesterovArgs prob[NESTEROV_MAX_PROBLEMS];
+  long long block_begin[NESTEROV_MAX_PROBLEMS];
+  int nprob;
+};
+static_assert(sizeof(NesterovGroup) <= 4096, "kernel parameter block too large");
+// All n stacks (all with momentum or all without) in as few launches as the grid and the problem table
+// allow. The counters must be zero when the call's launches start; they are left at the tile counts.
+muon_status launch_nesterov_norm(const NesterovArgs *probs, int n, cudaStream_t s);
+// Zeroes n counters in stream order (a kernel, so that the launches around it keep overlapping).
+muon_status launch_counter_reset(unsigned *counters, long long n, cudaStream_t s);
 
 struct AdamwConst {
   float decay;          // 1 - lr*wd

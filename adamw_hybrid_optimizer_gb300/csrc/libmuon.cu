@@ -143,6 +143,11 @@ constexpr size_t CTRL_BYTES = 256;
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 long long round8(long long v) { return (v + 7) / 8 * 8; }
 
+// A workspace starts with a header: the control block (error word at byte 0) and one counter per matrix
+// of the call, which the call zeroes before its first launch. Each stack's sections follow, stack after
+// stack; their offsets below are relative to the stack's own start.
+size_t header_bytes(long long total_K) { return align_up(CTRL_BYTES + static_cast<size_t>(total_K) * 4, 1024); }
+
 struct Layout {
   long long m, n, ldx, ldg, tiles_r, tiles_c;
   size_t scale, partial, x0, x1, g, h, total;
@@ -156,8 +161,7 @@ Layout layout(long long K, long long A, long long B) {
   L.ldg = round8(L.m);
   L.tiles_r = (A + NESTEROV_TILE - 1) / NESTEROV_TILE;
   L.tiles_c = (B + NESTEROV_TILE - 1) / NESTEROV_TILE;
-  size_t off = CTRL_BYTES;
-  off = align_up(off, 1024);
+  size_t off = 0;
   L.scale = off;
   off = align_up(off + static_cast<size_t>(K) * 4, 1024);
   L.partial = off;
@@ -172,6 +176,33 @@ Layout layout(long long K, long long A, long long B) {
   off = align_up(off + static_cast<size_t>(K) * L.m * L.ldg * 2, 1024);
   L.total = off;
   return L;
+}
+
+// The Nesterov/norm pass of one stack whose sections start at w; counters: the stack's K header words.
+NesterovArgs nesterov_args(char *w, const Layout &L, unsigned *counters, long long K, long long A, long long B,
+                           const void *const *gptrs, const void *gbase, int gdt, float *momentum, float mu,
+                           bool nesterov, float eps) {
+  NesterovArgs na{};
+  na.gptrs = gptrs;
+  na.gbase = gbase;
+  na.gdtype = gdt;
+  na.momentum = momentum;
+  na.u = reinterpret_cast<__nv_bfloat16 *>(w + L.x0);
+  na.ldu = L.ldx;
+  na.mstride_u = L.m * L.ldx;
+  na.partials = reinterpret_cast<float *>(w + L.partial);
+  na.scale = reinterpret_cast<float *>(w + L.scale);
+  na.counters = counters;
+  na.K = static_cast<int>(K);
+  na.A = static_cast<int>(A);
+  na.B = static_cast<int>(B);
+  na.tiles_r = static_cast<int>(L.tiles_r);
+  na.tiles_c = static_cast<int>(L.tiles_c);
+  na.transposed = A > B ? 1 : 0;
+  na.mu = mu;
+  na.eps = eps;
+  na.nesterov = nesterov ? 1 : 0;
+  return na;
 }
 
 bool valid_dtype(int d) { return d == MUON_F32 || d == MUON_BF16; }
@@ -191,11 +222,10 @@ muon_status check_coeffs(int ns_steps, const float *coeffs) {
   return MUON_OK;
 }
 
-// The Newton-Schulz chain on the wide iterate in x0 (unnormalised U; s_k in `scale`), ending in
-// launch_final. Iteration t reads X from one iterate buffer and writes the other.
-muon_status run_ns_chain(char *ws, const Layout &L, long long K, int ns_steps, const float *coeffs,
+// The Newton-Schulz chain on the wide iterate in x0 (unnormalised U; s_k in `scale`) of the stack whose
+// sections start at ws, ending in launch_final. Iteration t reads X from one iterate buffer and writes the other.
+muon_status run_ns_chain(uint32_t *err, char *ws, const Layout &L, long long K, int ns_steps, const float *coeffs,
                          const FinalSpec &fin, cudaStream_t s) {
-  uint32_t *err = reinterpret_cast<uint32_t *>(ws);
   const float *scale = reinterpret_cast<const float *>(ws + L.scale);
   __nv_bfloat16 *xb[2] = {reinterpret_cast<__nv_bfloat16 *>(ws + L.x0), reinterpret_cast<__nv_bfloat16 *>(ws + L.x1)};
   __nv_bfloat16 *G = reinterpret_cast<__nv_bfloat16 *>(ws + L.g);
@@ -230,7 +260,7 @@ extern "C" {
 
 size_t muon_workspace_bytes(int64_t K, int64_t A, int64_t B) {
   if (K < 1 || A < 1 || B < 1) return 0;
-  return layout(K, A, B).total;
+  return header_bytes(K) + layout(K, A, B).total;
 }
 
 muon_status muon_step_batched(void *const *params, muon_dtype pdt, const void *const *grads, muon_dtype gdt,
@@ -248,31 +278,17 @@ muon_status muon_step_batched(void *const *params, muon_dtype pdt, const void *c
     return MUON_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MUON_ERR_ALIGNMENT;
   const Layout L = layout(K, A, B);
-  if (ws_bytes < L.total) return MUON_ERR_WORKSPACE;
+  if (ws_bytes < header_bytes(K) + L.total) return MUON_ERR_WORKSPACE;
   if ((st = check_device()) != MUON_OK) return st;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  char *w = static_cast<char *>(ws);
-  NesterovArgs na{};
-  na.gptrs = grads;
-  na.gbase = nullptr;
-  na.gdtype = gdt;
-  na.momentum = momentum;
-  na.u = reinterpret_cast<__nv_bfloat16 *>(w + L.x0);
-  na.ldu = L.ldx;
-  na.mstride_u = L.m * L.ldx;
-  na.partials = reinterpret_cast<float *>(w + L.partial);
-  na.A = static_cast<int>(A);
-  na.B = static_cast<int>(B);
-  na.tiles_r = static_cast<int>(L.tiles_r);
-  na.tiles_c = static_cast<int>(L.tiles_c);
-  na.transposed = A > B ? 1 : 0;
-  na.mu = hp->momentum;
-  na.nesterov = hp->nesterov ? 1 : 0;
-  if ((st = launch_nesterov_norm(na, static_cast<int>(K), s)) != MUON_OK) return st;
-  if ((st = launch_norm_finalize(na.partials, static_cast<int>(L.tiles_r * L.tiles_c),
-                                 reinterpret_cast<float *>(w + L.scale), static_cast<int>(K), hp->eps, s)) != MUON_OK)
-    return st;
+  char *base = static_cast<char *>(ws);
+  char *w = base + header_bytes(K);
+  unsigned *counters = reinterpret_cast<unsigned *>(base + CTRL_BYTES);
+  if ((st = launch_counter_reset(counters, K, s)) != MUON_OK) return st;
+  const NesterovArgs na = nesterov_args(w, L, counters, K, A, B, grads, nullptr, gdt, momentum, hp->momentum,
+                                        hp->nesterov != 0, hp->eps);
+  if ((st = launch_nesterov_norm(&na, 1, s)) != MUON_OK) return st;
 
   const double scale = hp->scale_mode == 0 ? 0.2 * std::sqrt(static_cast<double>(A > B ? A : B))
                                            : std::sqrt(std::max(1.0, static_cast<double>(A) / static_cast<double>(B)));
@@ -285,7 +301,7 @@ muon_status muon_step_batched(void *const *params, muon_dtype pdt, const void *c
   fin.cautious = hp->cautious_wd ? 1 : 0;
   fin.lr_wd = static_cast<float>(static_cast<double>(hp->lr) * hp->weight_decay);
   fin.lr_scale = static_cast<float>(static_cast<double>(hp->lr) * scale);
-  return run_ns_chain(w, L, K, hp->ns_steps, hp->coeffs, fin, s);
+  return run_ns_chain(reinterpret_cast<uint32_t *>(base), w, L, K, hp->ns_steps, hp->coeffs, fin, s);
 }
 
 static muon_status check_bucket(const muon_bucket &b) {
@@ -299,11 +315,13 @@ static muon_status check_bucket(const muon_bucket &b) {
 size_t muon_workspace_bytes_grouped(const muon_bucket *buckets, int n) {
   if (buckets == nullptr || n < 1) return 0;
   size_t total = 0;
+  long long total_K = 0;
   for (int i = 0; i < n; ++i) {
     if (buckets[i].K < 1 || buckets[i].A < 1 || buckets[i].B < 1) return 0;
     total += layout(buckets[i].K, buckets[i].A, buckets[i].B).total;
+    total_K += buckets[i].K;
   }
-  return total;
+  return header_bytes(total_K) + total;
 }
 
 muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hparams *hp, void *ws, size_t ws_bytes,
@@ -327,36 +345,24 @@ muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hpar
   const unsigned long long to = g_timeout_ns;
   std::vector<Layout> L(n);
   std::vector<char *> w(n);
-  size_t off = 0;
+  long long total_K = 0;
+  for (int i = 0; i < n; ++i) total_K += buckets[i].K;
+  unsigned *counters = reinterpret_cast<unsigned *>(base + CTRL_BYTES);
+  size_t off = header_bytes(total_K);
   for (int i = 0; i < n; ++i) {
     L[i] = layout(buckets[i].K, buckets[i].A, buckets[i].B);
     w[i] = base + off;
     off += L[i].total;
   }
-  // momentum, Nesterov input, norm: one pass per bucket
-  for (int i = 0; i < n; ++i) {
+  // momentum, Nesterov input, norm: all buckets in one pass
+  if ((st = launch_counter_reset(counters, total_K, s)) != MUON_OK) return st;
+  std::vector<NesterovArgs> na(n);
+  for (long long i = 0, k0 = 0; i < n; k0 += buckets[i].K, ++i) {
     const muon_bucket &bk = buckets[i];
-    NesterovArgs na{};
-    na.gptrs = bk.grads;
-    na.gdtype = bk.gdt;
-    na.momentum = bk.momentum;
-    na.u = reinterpret_cast<__nv_bfloat16 *>(w[i] + L[i].x0);
-    na.ldu = L[i].ldx;
-    na.mstride_u = L[i].m * L[i].ldx;
-    na.partials = reinterpret_cast<float *>(w[i] + L[i].partial);
-    na.A = static_cast<int>(bk.A);
-    na.B = static_cast<int>(bk.B);
-    na.tiles_r = static_cast<int>(L[i].tiles_r);
-    na.tiles_c = static_cast<int>(L[i].tiles_c);
-    na.transposed = bk.A > bk.B ? 1 : 0;
-    na.mu = hp->momentum;
-    na.nesterov = hp->nesterov ? 1 : 0;
-    if ((st = launch_nesterov_norm(na, static_cast<int>(bk.K), s)) != MUON_OK) return st;
-    if ((st = launch_norm_finalize(na.partials, static_cast<int>(L[i].tiles_r * L[i].tiles_c),
-                                   reinterpret_cast<float *>(w[i] + L[i].scale), static_cast<int>(bk.K), hp->eps,
-                                   s)) != MUON_OK)
-      return st;
+    na[i] = nesterov_args(w[i], L[i], counters + k0, bk.K, bk.A, bk.B, bk.grads, nullptr, bk.gdt, bk.momentum,
+                          hp->momentum, hp->nesterov != 0, hp->eps);
   }
+  if ((st = launch_nesterov_norm(na.data(), n, s)) != MUON_OK) return st;
   // the Newton-Schulz chain, each step kind of all buckets in one grouped launch
   for (int t = 0; t < hp->ns_steps; ++t) {
     const float a = hp->coeffs[3 * t], b = hp->coeffs[3 * t + 1], c = hp->coeffs[3 * t + 2];
@@ -411,36 +417,23 @@ muon_status ns_orthogonalize(const void *x, muon_dtype xdt, void *out, muon_dtyp
   if (!std::isfinite(eps) || eps < 0.f) return MUON_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MUON_ERR_ALIGNMENT;
   const Layout L = layout(K, A, B);
-  if (ws_bytes < L.total) return MUON_ERR_WORKSPACE;
+  if (ws_bytes < header_bytes(K) + L.total) return MUON_ERR_WORKSPACE;
   if ((st = check_device()) != MUON_OK) return st;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  char *w = static_cast<char *>(ws);
-  NesterovArgs na{};
-  na.gptrs = nullptr;
-  na.gbase = x;
-  na.gdtype = xdt;
-  na.momentum = nullptr;
-  na.u = reinterpret_cast<__nv_bfloat16 *>(w + L.x0);
-  na.ldu = L.ldx;
-  na.mstride_u = L.m * L.ldx;
-  na.partials = reinterpret_cast<float *>(w + L.partial);
-  na.A = static_cast<int>(A);
-  na.B = static_cast<int>(B);
-  na.tiles_r = static_cast<int>(L.tiles_r);
-  na.tiles_c = static_cast<int>(L.tiles_c);
-  na.transposed = A > B ? 1 : 0;
-  if ((st = launch_nesterov_norm(na, static_cast<int>(K), s)) != MUON_OK) return st;
-  if ((st = launch_norm_finalize(na.partials, static_cast<int>(L.tiles_r * L.tiles_c),
-                                 reinterpret_cast<float *>(w + L.scale), static_cast<int>(K), eps, s)) != MUON_OK)
-    return st;
+  char *base = static_cast<char *>(ws);
+  char *w = base + header_bytes(K);
+  unsigned *counters = reinterpret_cast<unsigned *>(base + CTRL_BYTES);
+  if ((st = launch_counter_reset(counters, K, s)) != MUON_OK) return st;
+  const NesterovArgs na = nesterov_args(w, L, counters, K, A, B, nullptr, x, xdt, nullptr, 0.f, false, eps);
+  if ((st = launch_nesterov_norm(&na, 1, s)) != MUON_OK) return st;
   FinalSpec fin{};
   fin.params = nullptr;
   fin.out_dense = out;
   fin.dtype = odt;
   fin.transposed = na.transposed;
   fin.orig_cols = static_cast<int>(B);
-  return run_ns_chain(w, L, K, ns_steps, coeffs, fin, s);
+  return run_ns_chain(reinterpret_cast<uint32_t *>(base), w, L, K, ns_steps, coeffs, fin, s);
 }
 
 muon_status adamw_step(void *param, muon_dtype pdt, const void *grad, muon_dtype gdt, float *exp_avg,
@@ -639,7 +632,7 @@ const char *muon_kernel_name(int32_t kind) {
   switch (kind) {
     case KK_ADAMW: return "adamw";
     case KK_NESTEROV_NORM: return "nesterov_norm";
-    case KK_NORM_FINALIZE: return "norm_finalize";
+    case KK_COUNTER_RESET: return "counter_reset";
     case KK_GRAM: return "ns_gram";
     case KK_POLY: return "ns_poly";
     case KK_APPLY: return "ns_apply";

@@ -9,8 +9,9 @@
 // array, which every GPU that loads this code holds until the process exits.
 //
 // The array is shared by every call on a device and keeps the last call's contents. Each call clears
-// the part that must start at zero (the control block with the error word) with an asynchronous
-// memset, which allocates nothing; every other scratch byte is written before it is read. Calls whose
+// the part that must start at zero (the control block with the error word, and one counter per
+// matrix) with an asynchronous memset, which allocates nothing; every other scratch byte is written
+// before it is read. Calls whose
 // work overlaps on the GPU (different streams, or several host threads) race on the array.
 #include <cuda_runtime.h>
 
@@ -48,10 +49,11 @@ size_t up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct ScratchLayout {
   long long m, n, ldx, ldg, tiles_r, tiles_c;
-  size_t scale, partial, x0, x1, g, h, total;
+  size_t counters, scale, partial, x0, x1, g, h, total;
 };
 
-// Control block, then the same sections the workspace of ns_orthogonalize holds.
+// Control block and per-matrix counters (the zeroed part), then the same sections the workspace of
+// ns_orthogonalize holds.
 ScratchLayout scratch_layout(long long K, long long A, long long B) {
   ScratchLayout L{};
   L.m = A < B ? A : B;
@@ -60,7 +62,9 @@ ScratchLayout scratch_layout(long long K, long long A, long long B) {
   L.ldg = (L.m + 7) / 8 * 8;
   L.tiles_r = (A + NESTEROV_TILE - 1) / NESTEROV_TILE;
   L.tiles_c = (B + NESTEROV_TILE - 1) / NESTEROV_TILE;
-  size_t off = 1024;
+  size_t off = 256;
+  L.counters = off;
+  off = up(off + size_t(K) * 4, 1024);
   L.scale = off;
   off = up(off + size_t(K) * 4, 1024);
   L.partial = off;
@@ -106,7 +110,7 @@ extern "C" muon_status ns_orthogonalize_noalloc(const void *x, muon_dtype xdt, v
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char *w = static_cast<char *>(scratch);
   uint32_t *err = reinterpret_cast<uint32_t *>(w);
-  if (cudaMemsetAsync(w, 0, 1024, s) != cudaSuccess) return MUON_ERR_CUDA;
+  if (cudaMemsetAsync(w, 0, L.scale, s) != cudaSuccess) return MUON_ERR_CUDA;
 
   NesterovArgs na{};
   na.gptrs = nullptr;
@@ -117,16 +121,17 @@ extern "C" muon_status ns_orthogonalize_noalloc(const void *x, muon_dtype xdt, v
   na.ldu = L.ldx;
   na.mstride_u = L.m * L.ldx;
   na.partials = reinterpret_cast<float *>(w + L.partial);
+  na.scale = reinterpret_cast<float *>(w + L.scale);
+  na.counters = reinterpret_cast<unsigned *>(w + L.counters);
+  na.K = static_cast<int>(K);
   na.A = static_cast<int>(A);
   na.B = static_cast<int>(B);
   na.tiles_r = static_cast<int>(L.tiles_r);
   na.tiles_c = static_cast<int>(L.tiles_c);
   na.transposed = A > B ? 1 : 0;
-  float *scale = reinterpret_cast<float *>(w + L.scale);
-  if ((st = launch_nesterov_norm(na, static_cast<int>(K), s)) != MUON_OK) return st;
-  if ((st = launch_norm_finalize(na.partials, static_cast<int>(L.tiles_r * L.tiles_c), scale, static_cast<int>(K),
-                                 eps, s)) != MUON_OK)
-    return st;
+  na.eps = eps;
+  const float *scale = na.scale;
+  if ((st = launch_nesterov_norm(&na, 1, s)) != MUON_OK) return st;
 
   FinalSpec fin{};
   fin.params = nullptr;

@@ -161,12 +161,6 @@ __device__ __forceinline__ uint4 pack8(const float *src) {
   return w;
 }
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const float *src) {
-  uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) d4[q] = pack8(src + 8 * q);
-}
-
 // ------------------------------------------------------------------------------------------ epilogue staging
 //
 // Each epilogue warp owns a 32 x 32 region of the current ring slot: tile rows lane_base .. +31 (one

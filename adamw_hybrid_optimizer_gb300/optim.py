@@ -83,7 +83,9 @@ class HybridMuonAdamW:
                     buckets.append(bk)
                     for k, p in enumerate(ps):
                         self.state[p] = {"momentum_buffer": bk.momentum[k]}
-                ws_bytes = max(ws_bytes, sum(L.muon_workspace_bytes(bk.K, bk.A, bk.B) for bk in buckets))
+                shapes = (L.muon_bucket * len(buckets))(*[L.muon_bucket(None, None, None, bk.K, bk.A, bk.B, 0, 0)
+                                                           for bk in buckets])
+                ws_bytes = max(ws_bytes, L.muon_workspace_bytes_grouped(shapes) if buckets else 0)
             else:
                 group["step"] = 0
                 for p in group["params"]:
@@ -91,7 +93,8 @@ class HybridMuonAdamW:
                                      "exp_avg_sq": torch.zeros(p.shape, dtype=torch.float32, device=p.device)}
             self.param_groups.append(group)
             self._buckets.append(buckets)
-        self._ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device) if device is not None else None
+        # zero-filled: the control block's error word must start at zero
+        self._ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=device) if device is not None else None
 
     @torch.no_grad()
     def step(self):

@@ -74,7 +74,8 @@ typedef struct {
 } adamw_hparams;
 
 /* Bytes of workspace muon_step_batched / ns_orthogonalize need for a (K, A, B) stack.
- * Layout (all offsets 1024-byte aligned): a 256-byte control block (error word), K fp32
+ * Layout (all sections 1024-byte aligned): a header of a 256-byte control block (error word)
+ * and K 32-bit counters, which every call clears itself before its first launch; then K fp32
  * norm scales, per-tile norm partial sums, two bf16 iterates of (K, min, max) with rows
  * padded to a multiple of 8 elements, and two bf16 (K, min, min) Gram buffers.
  * Returns 0 if K, A or B is not positive. */
@@ -106,7 +107,8 @@ typedef struct {
   muon_dtype pdt, gdt;
 } muon_bucket;
 
-/* Workspace bytes for muon_step_grouped: the sum over buckets of muon_workspace_bytes(K, A, B).
+/* Workspace bytes for muon_step_grouped: one header (control block and one counter per matrix of all
+ * buckets), then each bucket's sections as muon_workspace_bytes lays them out.
  * Returns 0 if n < 1, buckets is null or a dimension is not positive. */
 size_t muon_workspace_bytes_grouped(const muon_bucket *buckets, int n);
 

@@ -162,7 +162,8 @@ def test_grouped_entry_point_checks():
     good = (L.muon_bucket * 2)(L.muon_bucket(FAKE, FAKE, FAKE, 4, 64, 128, 0, 0),
                                L.muon_bucket(FAKE, FAKE, FAKE, 2, 128, 64, 1, 1))
     need = L.muon_workspace_bytes_grouped(good)
-    assert need == L.muon_workspace_bytes(4, 64, 128) + L.muon_workspace_bytes(2, 128, 64)
+    # one shared 1 KiB header (control block + one counter per matrix) instead of one per stack
+    assert need == L.muon_workspace_bytes(4, 64, 128) + L.muon_workspace_bytes(2, 128, 64) - 1024
     st = lambda b, n=2, ws=FAKE, nb=need: lib.muon_step_grouped(b, n, ctypes.byref(hp), ws, nb, None)
     assert st(good, n=0) == L.MUON_ERR_INVALID_ARG
     assert st(good, ws=None) == L.MUON_ERR_INVALID_ARG

@@ -2,8 +2,10 @@
 
 Grouping changes only which CTA computes which tile, never the arithmetic of a tile, so the result must
 equal, bit for bit, one muon_step_batched call per bucket on the same inputs (which the per-bucket tests
-compare with the oracle). Covered: the GPT-2-small set (4 buckets, one of them transposed), and ten
-buckets of distinct ragged shapes with fp32 and bf16 parameters (more than one launch per step kind).
+compare with the oracle). Covered: the GPT-2-small set (4 buckets, one of them transposed), ten buckets
+of distinct ragged shapes with fp32 and bf16 parameters (more than one launch per step kind), eighteen
+buckets (more than one launch of the momentum/norm pass), and a workspace that another call with another
+layout used in between.
 """
 import numpy as np
 import pytest
@@ -104,3 +106,39 @@ def test_grouped_step_matches_oracle_on_one_sample(L):
                                       eps=hp.eps, param_dtype="bf16")
         got = f64(p[0])
         assert np.linalg.norm(got - ref) <= 2e-2 * np.linalg.norm(ref - p0) + 2 ** -8 * np.linalg.norm(ref)
+
+
+def test_grouped_equals_per_bucket_eighteen_buckets(L):
+    shapes = [(1 + i % 3, 8 * (1 + i), 16 * (1 + (i * 7) % 5)) for i in range(18)]
+    hp = workloads.workload("tiny").muon_hp
+    _run_both(L, shapes, torch.bfloat16, hp, seed=3)
+
+
+def test_workspace_reused_by_another_layout(L):
+    """A call leaves the workspace full of its own data; a later call with another layout must not read
+    any of it as state (its per-matrix counters are cleared by the call itself)."""
+    hp = hp_struct(L, workloads.workload("tiny").muon_hp)
+    shapes = [(3, 64, 128), (2, 136, 72)]
+    data = _make(shapes, torch.bfloat16, 4)
+    code = L.MUON_BF16
+
+    def grouped(ws):
+        ps = [p0.clone() for p0, _ in data]
+        moms = [torch.zeros(s, dtype=torch.float32, device=DEV) for s in shapes]
+        bk = L.make_buckets([(L.pointer_array([p[k] for k in range(K)], DEV),
+                              L.pointer_array([g[0][k] for k in range(K)], DEV), m, K, A, B, code, code)
+                             for p, m, (_, g), (K, A, B) in zip(ps, moms, data, shapes)])
+        L.muon_step_grouped(bk, hp, ws)
+        assert L.muon_check(ws) == L.MUON_OK
+        return ps
+
+    fresh = torch.zeros(L.muon_workspace_bytes(4, 256, 512), dtype=torch.uint8, device=DEV)
+    ref = grouped(torch.zeros_like(fresh))
+    # another layout writes the same bytes (counters of this call sit where the other call keeps data)
+    big = torch.randn((4, 256, 512), generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).to(DEV)
+    out = torch.empty_like(big)
+    L.ns_orthogonalize(big, out, [(3.4445, -4.775, 2.0315)] * 5, 1e-7, fresh)
+    assert L.muon_check(fresh) == L.MUON_OK
+    got = grouped(fresh)
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
