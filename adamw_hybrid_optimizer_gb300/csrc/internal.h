@@ -51,14 +51,11 @@ struct GemmProblem {
   long long tile_begin;   // first tile pair of this problem in the launch's pair space
   // epilogue coefficients
   float alpha;            // gram: output = alpha * s^2 * acc (s from `scale` when given)
-  float coef_a, coef_b, coef_c;
-  const float *scale;     // per-matrix normalisation s_k (device), or null
+  float coef_a, coef_b, coef_c;   // poly: output = a*I + b*G + c*acc, with G read by the epilogue
+  const float *scale;     // per-matrix normalisation s_k (device), or null; apply / final: output = s * acc
   // bf16 output of gram / poly / apply
   __nv_bfloat16 *out;
   long long ld_out, mstride_out;
-  // second input read by the epilogue: G for poly, X for apply / final
-  const __nv_bfloat16 *aux;
-  long long ld_aux, mstride_aux;
   // final step: parameter update (params != null) or dense store (out_dense != null)
   void *const *params;
   void *out_dense;
@@ -77,7 +74,7 @@ struct Bf16Stack {
   long long rows, cols, ld, mstride, batch;
 };
 
-// Final iteration: u = s*(a*x + h x) in the wide orientation, then either the Muon parameter update
+// Final iteration: u = s * (h x) in the wide orientation (h = a*I + b*G + c*G^2), then either the Muon parameter update
 // or a dense store, transposing back when the stored matrix is tall.
 struct FinalSpec {
   void *const *params;   // device array of K pointers (update) or null
@@ -96,9 +93,10 @@ class GemmBatch {
   GemmBatch(int epi, uint32_t *err, unsigned long long timeout_ns) : epi_(epi), err_(err), timeout_ns_(timeout_ns) {}
   muon_status add_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long ldg, long long mstride_g, float alpha,
                        const float *scale);
-  muon_status add_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float b, float c);
-  muon_status add_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, float a, const float *scale);
-  muon_status add_final(const Bf16Stack &h, const Bf16Stack &x, float a, const float *scale, const FinalSpec &f);
+  muon_status add_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float a, float b,
+                       float c);
+  muon_status add_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, const float *scale);
+  muon_status add_final(const Bf16Stack &h, const Bf16Stack &x, const float *scale, const FinalSpec &f);
   muon_status launch(cudaStream_t s);
   ~GemmBatch();
 
@@ -115,11 +113,11 @@ class GemmBatch {
 // Single-stack conveniences (a batch of one).
 muon_status launch_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long ldg, long long mstride_g, float alpha,
                         const float *scale, uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
-muon_status launch_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float b, float c,
-                        uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
-muon_status launch_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, float a, const float *scale,
+muon_status launch_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float a, float b,
+                        float c, uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
+muon_status launch_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, const float *scale,
                          uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
-muon_status launch_final(const Bf16Stack &h, const Bf16Stack &x, float a, const float *scale, const FinalSpec &f,
+muon_status launch_final(const Bf16Stack &h, const Bf16Stack &x, const float *scale, const FinalSpec &f,
                          uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
 
 // ------------------------------------------------------------------------------------------ elementwise

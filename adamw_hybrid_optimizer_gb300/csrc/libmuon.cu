@@ -240,12 +240,12 @@ muon_status run_ns_chain(uint32_t *err, char *ws, const Layout &L, long long K, 
     Bf16Stack X{xb[t & 1], L.m, L.n, L.ldx, mstride_x, K};
     if ((st = launch_gram(X, G, L.ldg, mstride_g, 1.0f, sc, err, to, s)) != MUON_OK) return st;
     Bf16Stack Gs{G, L.m, L.m, L.ldg, mstride_g, K};
-    if ((st = launch_poly(Gs, H, L.ldg, mstride_g, b, c, err, to, s)) != MUON_OK) return st;
+    if ((st = launch_poly(Gs, H, L.ldg, mstride_g, a, b, c, err, to, s)) != MUON_OK) return st;
     Bf16Stack Hs{H, L.m, L.m, L.ldg, mstride_g, K};
     if (t + 1 < ns_steps) {
-      if ((st = launch_apply(Hs, X, xb[(t + 1) & 1], a, sc, err, to, s)) != MUON_OK) return st;
+      if ((st = launch_apply(Hs, X, xb[(t + 1) & 1], sc, err, to, s)) != MUON_OK) return st;
     } else {
-      if ((st = launch_final(Hs, X, a, sc, fin, err, to, s)) != MUON_OK) return st;
+      if ((st = launch_final(Hs, X, sc, fin, err, to, s)) != MUON_OK) return st;
     }
   }
   return MUON_OK;
@@ -380,9 +380,9 @@ muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hpar
       Bf16Stack Gs{G, Li.m, Li.m, Li.ldg, msg, K};
       Bf16Stack Hs{H, Li.m, Li.m, Li.ldg, msg, K};
       if ((st = gram.add_gram(X, G, Li.ldg, msg, 1.0f, sc)) != MUON_OK) return st;
-      if ((st = poly.add_poly(Gs, H, Li.ldg, msg, b, c)) != MUON_OK) return st;
+      if ((st = poly.add_poly(Gs, H, Li.ldg, msg, a, b, c)) != MUON_OK) return st;
       if (t + 1 < hp->ns_steps) {
-        st = last.add_apply(Hs, X, xb[(t + 1) & 1], a, sc);
+        st = last.add_apply(Hs, X, xb[(t + 1) & 1], sc);
       } else {
         const muon_bucket &bk = buckets[i];
         const double scale = hp->scale_mode == 0
@@ -396,7 +396,7 @@ muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hpar
         fin.cautious = hp->cautious_wd ? 1 : 0;
         fin.lr_wd = static_cast<float>(static_cast<double>(hp->lr) * hp->weight_decay);
         fin.lr_scale = static_cast<float>(static_cast<double>(hp->lr) * scale);
-        st = last.add_final(Hs, X, a, sc, fin);
+        st = last.add_final(Hs, X, sc, fin);
       }
       if (st != MUON_OK) return st;
     }
@@ -492,32 +492,31 @@ muon_status ns_gram(const void *x, void *g, int64_t K, int64_t m, int64_t n, flo
                      g_timeout_ns, reinterpret_cast<cudaStream_t>(stream));
 }
 
-muon_status ns_poly(const void *g, void *h, int64_t K, int64_t m, float b, float c, void *ws, size_t ws_bytes,
-                    muon_stream_t stream) {
+muon_status ns_poly(const void *g, void *h, int64_t K, int64_t m, float a, float b, float c, void *ws,
+                    size_t ws_bytes, muon_stream_t stream) {
   muon_status st;
   if ((st = check_step_stack(g, K, m, m)) != MUON_OK || (st = check_step_stack(h, K, m, m)) != MUON_OK ||
       (st = check_ws_ctrl(ws, ws_bytes)) != MUON_OK)
     return st;
-  if (!std::isfinite(b) || !std::isfinite(c)) return MUON_ERR_INVALID_ARG;
+  if (!std::isfinite(a) || !std::isfinite(b) || !std::isfinite(c)) return MUON_ERR_INVALID_ARG;
   if ((st = check_device()) != MUON_OK) return st;
   Bf16Stack G{g, m, m, m, m * m, K};
-  return launch_poly(G, static_cast<__nv_bfloat16 *>(h), m, m * m, b, c, static_cast<uint32_t *>(ws), g_timeout_ns,
-                     reinterpret_cast<cudaStream_t>(stream));
+  return launch_poly(G, static_cast<__nv_bfloat16 *>(h), m, m * m, a, b, c, static_cast<uint32_t *>(ws),
+                     g_timeout_ns, reinterpret_cast<cudaStream_t>(stream));
 }
 
-muon_status ns_apply(const void *h, const void *x, void *out, int64_t K, int64_t m, int64_t n, float a, void *ws,
+muon_status ns_apply(const void *h, const void *x, void *out, int64_t K, int64_t m, int64_t n, void *ws,
                      size_t ws_bytes, muon_stream_t stream) {
   muon_status st;
   if ((st = check_step_stack(h, K, m, m)) != MUON_OK || (st = check_step_stack(x, K, m, n)) != MUON_OK ||
       (st = check_step_stack(out, K, m, n)) != MUON_OK || (st = check_ws_ctrl(ws, ws_bytes)) != MUON_OK)
     return st;
   if (out == x) return MUON_ERR_INVALID_ARG;
-  if (!std::isfinite(a)) return MUON_ERR_INVALID_ARG;
   if ((st = check_device()) != MUON_OK) return st;
   Bf16Stack Hs{h, m, m, m, m * m, K};
   Bf16Stack X{x, m, n, n, m * n, K};
   // out has x's layout: launch_apply writes with x's pitches
-  return launch_apply(Hs, X, static_cast<__nv_bfloat16 *>(out), a, nullptr, static_cast<uint32_t *>(ws),
+  return launch_apply(Hs, X, static_cast<__nv_bfloat16 *>(out), nullptr, static_cast<uint32_t *>(ws),
                       g_timeout_ns, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -150,12 +150,12 @@ extern "C" muon_status ns_orthogonalize_noalloc(const void *x, muon_dtype xdt, v
     Bf16Stack X{xb[t & 1], L.m, L.n, L.ldx, msx, K};
     if ((st = launch_gram(X, G, L.ldg, msg, 1.0f, sc, err, to, s)) != MUON_OK) return st;
     Bf16Stack Gs{G, L.m, L.m, L.ldg, msg, K};
-    if ((st = launch_poly(Gs, H, L.ldg, msg, b, c, err, to, s)) != MUON_OK) return st;
+    if ((st = launch_poly(Gs, H, L.ldg, msg, a, b, c, err, to, s)) != MUON_OK) return st;
     Bf16Stack Hs{H, L.m, L.m, L.ldg, msg, K};
     if (t + 1 < ns_steps)
-      st = launch_apply(Hs, X, xb[(t + 1) & 1], a, sc, err, to, s);
+      st = launch_apply(Hs, X, xb[(t + 1) & 1], sc, err, to, s);
     else
-      st = launch_final(Hs, X, a, sc, fin, err, to, s);
+      st = launch_final(Hs, X, sc, fin, err, to, s);
     if (st != MUON_OK) return st;
   }
   return MUON_OK;

@@ -50,12 +50,13 @@ constexpr int LOADER_WARP = 2 + EPI_WARPS;
 constexpr int NUM_THREADS = 32 * (LOADER_WARP + 1);
 
 // Epilogue input ring: a slot holds 64 columns (two 32-column chunks) of a tile's 128 rows, bf16, 128-byte
-// lines with the 128B swizzle TMA writes. The GRAM kernel has no second input and uses one slot only as
-// the epilogue's staging space.
+// lines with the 128B swizzle TMA writes. Only POLY has a second input (G, for its b*G term); the other
+// kinds use one slot only as the epilogue's staging space.
 constexpr int MAX_RING_SLOTS = 5;
 constexpr int RING_AUX_BYTES = BM * 64 * 2;
 
 __host__ __device__ constexpr int ring_slot_bytes(int) { return RING_AUX_BYTES; }
+__host__ __device__ constexpr bool has_aux(int epi) { return epi == EPI_POLY; }
 
 struct Ctrl {
   uint64_t full[MAX_STAGES];
@@ -312,7 +313,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem &a, int b, int 
       float gv[32];
       region_read_row(rg, lane, gv);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = a.coef_b * gv[j] + a.coef_c * v[j];
+      for (int j = 0; j < 32; ++j) v[j] = a.coef_b * gv[j] + a.coef_c * v[j] + (col0 + j == row ? a.coef_a : 0.f);
       __syncwarp();
     } else {
       float sc = a.alpha;
@@ -342,12 +343,11 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem &a, int b, int 
         [&](int i, int j) { return col0 + i < cols && warp_row0 + j < rows && col0 + i > warp_row0 + j; },
         [&](int i) { return col0 + i < cols && warp_row0 + 32 <= rows && col0 + i > warp_row0 + 31; });
   } else {
-    const float sc = a.scale != nullptr ? a.scale[b] : 1.f;
-    float xv[32];
-    region_read_row(rg, lane, xv);
+    if (a.scale != nullptr) {
+      const float sc = a.scale[b];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = sc * (a.coef_a * xv[j] + v[j]);
-    __syncwarp();
+      for (int j = 0; j < 32; ++j) v[j] *= sc;
+    }
     if constexpr (EPI == EPI_APPLY) {
       region_write_row(rg, lane, v);
       __syncwarp();
@@ -427,21 +427,18 @@ __device__ __forceinline__ ParamBlock param_block(const GemmProblem &a, const __
 }
 
 // Final-step chunk for bf16 parameters: as epilogue_chunk, with this chunk's parameter block already in
-// flight in pf (fetched one chunk ahead); once pf is in the staging region, the next chunk's block is
-// fetched into pf.
+// flight in pf (fetched one chunk ahead); once pf is in the staging region, the block of the chunk 64
+// columns on is fetched into pf if fetch_next.
 __device__ __forceinline__ void final_chunk_bf16(const GemmProblem &a, int b, int warp_row0, int lane, int col0,
-                                                 const Region &rg, float *v, uint4 (&pf)[4], const ParamBlock &next) {
-  const float sc = a.scale != nullptr ? a.scale[b] : 1.f;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    float xv[8];
-    unpack8(*reinterpret_cast<const uint4 *>(rg.piece(lane, q)), xv);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[8 * q + e] = sc * (a.coef_a * xv[e] + v[8 * q + e]);
-  }
-  __syncwarp();
+                                                 const Region &rg, float *v, uint4 (&pf)[4], bool fetch_next) {
+  __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(a.params[b]);
   block_commit(rg, lane, pf);
-  if (next.valid) block_fetch(next, lane, pf);
+  if (fetch_next) block_fetch(param_block(a, p, warp_row0, col0 + 64), lane, pf);
+  if (a.scale != nullptr) {
+    const float sc = a.scale[b];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= sc;
+  }
   __syncwarp();
   if (!a.transposed) {
 #pragma unroll
@@ -459,7 +456,6 @@ __device__ __forceinline__ void final_chunk_bf16(const GemmProblem &a, int b, in
   if (!a.transposed) region_write_row(rg, lane, v);
   else region_write_col(rg, lane, v);
   __syncwarp();
-  __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(a.params[b]);
   const ParamBlock pb = param_block(a, p, warp_row0, col0);
   region_store(
       rg, lane, const_cast<__nv_bfloat16 *>(pb.base), pb.ld, [&](int i, int j) { return i < pb.ilim && j < pb.jlim; },
@@ -629,7 +625,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       }
     }
   } else if (warp == LOADER_WARP) {
-    if constexpr (EPI != EPI_GRAM) {
+    if constexpr (has_aux(EPI)) {
       // ---------------------------------------------------------------- epilogue loader (lane 0 owns the
       // ring barriers and the TMA loads; the warp stays converged for the barrier broadcasts)
       uint32_t slot = 0, rphase = 0;
@@ -639,9 +635,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       for (long long t = first; ok && t < args.total_tiles; t += stride) {
         const int pi = find_problem(args, t);
         const GemmProblem P = args.prob[pi];
-        // POLY reads G through the A-operand map (box 64 x 128); APPLY / FINAL read X through the N-major
-        // B-operand map (box 64 x 64, two loads)
-        const CUtensorMap *aux_map = (EPI == EPI_POLY) ? &args.map_a[pi] : &args.map_b[pi];
+        // POLY reads G through the A-operand map (box 64 x 128)
+        const CUtensorMap *aux_map = &args.map_a[pi];
         int b, ti, tj;
         decode_tile(P, args.symmetric, t - P.tile_begin, rank, b, ti, tj);
         const int row0 = ti * BM;
@@ -658,12 +653,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
           uint8_t *dst = ring + slot * SLOT_BYTES;
           if (lane == 0) {
             mbar_arrive_expect_tx(&ctrl->ring_full[slot], RING_AUX_BYTES);
-            if constexpr (EPI == EPI_POLY) {
-              tma_load_3d(dst, aux_map, &ctrl->ring_full[slot], c0, row0, b);
-            } else {
-              tma_load_3d(dst, aux_map, &ctrl->ring_full[slot], c0, row0, b);
-              tma_load_3d(dst + 64 * 128, aux_map, &ctrl->ring_full[slot], c0, row0 + 64, b);
-            }
+            tma_load_3d(dst, aux_map, &ctrl->ring_full[slot], c0, row0, b);
           }
           __syncwarp();
           last_parity[slot] = static_cast<int>(rphase);
@@ -708,9 +698,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         const int c0 = tj * BN + 64 * s;
         if (c0 >= P.cols) break;
         if (EPI != EPI_GRAM && !slot_used(args.symmetric, c0, row0)) continue;
-        // GRAM has no second input: slot 0 serves only as staging space
-        uint8_t *slot_ptr = ring + (EPI == EPI_GRAM ? 0 : slot) * SLOT_BYTES;
-        if constexpr (EPI != EPI_GRAM) {
+        // kinds without a second input use slot 0 only as staging space
+        uint8_t *slot_ptr = ring + (has_aux(EPI) ? slot : 0) * SLOT_BYTES;
+        if constexpr (has_aux(EPI)) {
           ok = wait_bounded(&ctrl->ring_full[slot], rphase, ctl, ERR_WAIT_RING_FULL);
           if (!__all_sync(0xffffffffu, ok)) {
             aborted = true;
@@ -728,17 +718,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
             const Region rg{slot_ptr, lane_base, my_half};
             if (EPI == EPI_FINAL && prefetch_params) {
               if (!pf_ready) block_fetch(param_block(P, pbase, warp_row0, col0), lane, pf);
-              ParamBlock next = param_block(P, pbase, warp_row0, col0 + 64);
-              next.valid = next.valid && s + 1 < BN / 64;   // only this warp's next chunk of the same tile
+              // only this warp's next chunk of the same tile, if it exists
+              const bool next = s + 1 < BN / 64 && col0 + 64 < P.cols;
               final_chunk_bf16(P, b, warp_row0, lane, col0, rg, v, pf, next);
-              pf_ready = next.valid;
+              pf_ready = next;
             } else {
               epilogue_chunk<EPI>(P, b, warp_row0, lane, col0, rg, v);
             }
             __syncwarp();   // every lane's region reads are done before the region is written again
           }
         }
-        if constexpr (EPI != EPI_GRAM) {
+        if constexpr (has_aux(EPI)) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctrl->ring_empty[slot]);
           if (++slot == RING_SLOTS) {
@@ -905,8 +895,8 @@ muon_status GemmBatch::add_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long 
   return push(it);
 }
 
-muon_status GemmBatch::add_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float b,
-                                float c) {
+muon_status GemmBatch::add_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float a,
+                                float b, float c) {
   if (epi_ != EPI_POLY) return MUON_ERR_INVALID_ARG;
   Item it{};
   if (!make_map(&it.ma, g.ptr, g.cols, g.rows, g.batch, g.ld, g.mstride, BM) ||
@@ -914,45 +904,33 @@ muon_status GemmBatch::add_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long 
     return MUON_ERR_CUDA;
   fill_tiles(it.p, g.batch, g.rows, g.rows, g.cols, true);
   it.p.alpha = 1.f;
+  it.p.coef_a = a;
   it.p.coef_b = b;
   it.p.coef_c = c;
   it.p.out = h;
   it.p.ld_out = ldh;
   it.p.mstride_out = mstride_h;
-  it.p.aux = static_cast<const __nv_bfloat16 *>(g.ptr);
-  it.p.ld_aux = g.ld;
-  it.p.mstride_aux = g.mstride;
   return push(it);
 }
 
-muon_status GemmBatch::add_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, float a,
-                                 const float *scale) {
+muon_status GemmBatch::add_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, const float *scale) {
   if (epi_ != EPI_APPLY) return MUON_ERR_INVALID_ARG;
   Item it{};
   if (!apply_maps(h, x, &it.ma, &it.mb)) return MUON_ERR_CUDA;
   fill_tiles(it.p, x.batch, x.rows, x.cols, h.cols, false);
-  it.p.coef_a = a;
   it.p.scale = scale;
   it.p.out = out;
   it.p.ld_out = x.ld;
   it.p.mstride_out = x.mstride;
-  it.p.aux = static_cast<const __nv_bfloat16 *>(x.ptr);
-  it.p.ld_aux = x.ld;
-  it.p.mstride_aux = x.mstride;
   return push(it);
 }
 
-muon_status GemmBatch::add_final(const Bf16Stack &h, const Bf16Stack &x, float a, const float *scale,
-                                 const FinalSpec &f) {
+muon_status GemmBatch::add_final(const Bf16Stack &h, const Bf16Stack &x, const float *scale, const FinalSpec &f) {
   if (epi_ != EPI_FINAL) return MUON_ERR_INVALID_ARG;
   Item it{};
   if (!apply_maps(h, x, &it.ma, &it.mb)) return MUON_ERR_CUDA;
   fill_tiles(it.p, x.batch, x.rows, x.cols, h.cols, false);
-  it.p.coef_a = a;
   it.p.scale = scale;
-  it.p.aux = static_cast<const __nv_bfloat16 *>(x.ptr);
-  it.p.ld_aux = x.ld;
-  it.p.mstride_aux = x.mstride;
   it.p.params = f.params;
   it.p.out_dense = f.out_dense;
   it.p.out_dtype = f.dtype;
@@ -1000,14 +978,8 @@ muon_status GemmBatch::launch(cudaStream_t s) {
         st = short_k ? launch_shape<EPI_POLY, false, 4, 5>(g, KK_POLY, s)
                      : launch_shape<EPI_POLY, false, 6, 2>(g, KK_POLY, s);
         break;
-      case EPI_APPLY:
-        st = short_k ? launch_shape<EPI_APPLY, true, 4, 5>(g, KK_APPLY, s)
-                     : launch_shape<EPI_APPLY, true, 6, 2>(g, KK_APPLY, s);
-        break;
-      default:
-        st = short_k ? launch_shape<EPI_FINAL, true, 4, 5>(g, KK_FINAL, s)
-                     : launch_shape<EPI_FINAL, true, 6, 2>(g, KK_FINAL, s);
-        break;
+      case EPI_APPLY: st = launch_shape<EPI_APPLY, true, 6, 1>(g, KK_APPLY, s); break;
+      default: st = launch_shape<EPI_FINAL, true, 6, 1>(g, KK_FINAL, s); break;
     }
     if (st != MUON_OK) return st;
   }
@@ -1021,24 +993,24 @@ muon_status launch_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long ldg, lon
   return st != MUON_OK ? st : bt.launch(s);
 }
 
-muon_status launch_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float b, float c,
-                        uint32_t *err, unsigned long long timeout_ns, cudaStream_t s) {
+muon_status launch_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float a, float b,
+                        float c, uint32_t *err, unsigned long long timeout_ns, cudaStream_t s) {
   GemmBatch bt(EPI_POLY, err, timeout_ns);
-  muon_status st = bt.add_poly(g, h, ldh, mstride_h, b, c);
+  muon_status st = bt.add_poly(g, h, ldh, mstride_h, a, b, c);
   return st != MUON_OK ? st : bt.launch(s);
 }
 
-muon_status launch_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, float a, const float *scale,
+muon_status launch_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, const float *scale,
                          uint32_t *err, unsigned long long timeout_ns, cudaStream_t s) {
   GemmBatch bt(EPI_APPLY, err, timeout_ns);
-  muon_status st = bt.add_apply(h, x, out, a, scale);
+  muon_status st = bt.add_apply(h, x, out, scale);
   return st != MUON_OK ? st : bt.launch(s);
 }
 
-muon_status launch_final(const Bf16Stack &h, const Bf16Stack &x, float a, const float *scale, const FinalSpec &f,
+muon_status launch_final(const Bf16Stack &h, const Bf16Stack &x, const float *scale, const FinalSpec &f,
                          uint32_t *err, unsigned long long timeout_ns, cudaStream_t s) {
   GemmBatch bt(EPI_FINAL, err, timeout_ns);
-  muon_status st = bt.add_final(h, x, a, scale, f);
+  muon_status st = bt.add_final(h, x, scale, f);
   return st != MUON_OK ? st : bt.launch(s);
 }
 

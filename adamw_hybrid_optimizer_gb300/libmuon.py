@@ -65,10 +65,9 @@ SIGNATURES = {
     "adamw_step": (ctypes.c_int, [_vp, ctypes.c_int, _vp, ctypes.c_int, _vp, _vp, _c_int64,
                                   ctypes.POINTER(adamw_hparams), _vp]),
     "ns_gram": (ctypes.c_int, [_vp, _vp, _c_int64, _c_int64, _c_int64, ctypes.c_float, _vp, ctypes.c_size_t, _vp]),
-    "ns_poly": (ctypes.c_int, [_vp, _vp, _c_int64, _c_int64, ctypes.c_float, ctypes.c_float, _vp, ctypes.c_size_t,
-                               _vp]),
-    "ns_apply": (ctypes.c_int, [_vp, _vp, _vp, _c_int64, _c_int64, _c_int64, ctypes.c_float, _vp, ctypes.c_size_t,
-                                _vp]),
+    "ns_poly": (ctypes.c_int, [_vp, _vp, _c_int64, _c_int64, ctypes.c_float, ctypes.c_float, ctypes.c_float, _vp,
+                               ctypes.c_size_t, _vp]),
+    "ns_apply": (ctypes.c_int, [_vp, _vp, _vp, _c_int64, _c_int64, _c_int64, _vp, ctypes.c_size_t, _vp]),
     "muon_plan_buckets": (ctypes.c_int, [_c_int64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "muon_check": (ctypes.c_int, [_vp, _vp]),
     "muon_set_timeout_ns": (None, [ctypes.c_uint64]),
@@ -217,15 +216,17 @@ def ns_gram(x, g, alpha: float, ws, stream=None):
                          _stream(stream)), "ns_gram")
 
 
-def ns_poly(g, h, b: float, c: float, ws, stream=None):
+def ns_poly(g, h, a: float, b: float, c: float, ws, stream=None):
+    """h = a*I + b*g + c*g g."""
     K, m, _ = g.shape
-    _check(lib().ns_poly(g.data_ptr(), h.data_ptr(), K, m, b, c, ws.data_ptr(), ws.numel() * ws.element_size(),
+    _check(lib().ns_poly(g.data_ptr(), h.data_ptr(), K, m, a, b, c, ws.data_ptr(), ws.numel() * ws.element_size(),
                          _stream(stream)), "ns_poly")
 
 
-def ns_apply(h, x, out, a: float, ws, stream=None):
+def ns_apply(h, x, out, ws, stream=None):
+    """out = h x."""
     K, m, n = x.shape
-    _check(lib().ns_apply(h.data_ptr(), x.data_ptr(), out.data_ptr(), K, m, n, a, ws.data_ptr(),
+    _check(lib().ns_apply(h.data_ptr(), x.data_ptr(), out.data_ptr(), K, m, n, ws.data_ptr(),
                           ws.numel() * ws.element_size(), _stream(stream)), "ns_apply")
 
 

@@ -160,17 +160,18 @@ muon_status ns_orthogonalize_noalloc(const void *x, muon_dtype xdt, void *out, m
                                      int64_t B, int ns_steps, const float *coeffs, float eps, muon_stream_t stream);
 
 /* The three tensor-core steps of one Newton-Schulz iteration on contiguous bf16 stacks, exposed
- * one by one ([P2] newton_schulz loop body; [P4] section 2.2 symmetric Gram):
+ * one by one ([P2] newton_schulz loop body; [P4] section 2.2 symmetric Gram). The loop body's
+ * a*X + (b*A + c*A A) X is computed as (a*I + b*A + c*A A) X, with a folded into the polynomial:
  *   ns_gram:  g = alpha * x x^T,         x (K, m, n), g (K, m, m); symmetric, both halves written.
- *   ns_poly:  h = b*g + c*g g,           g, h (K, m, m); g must be symmetric.
- *   ns_apply: out = a*x + h x,           h (K, m, m), x and out (K, m, n); out may not alias x.
+ *   ns_poly:  h = a*I + b*g + c*g g,     g, h (K, m, m); g must be symmetric.
+ *   ns_apply: out = h x,                 h (K, m, m), x and out (K, m, n); out may not alias x.
  * All rows must be 16-byte aligned (m and n multiples of 8), pointers 256-byte aligned.
  * ws: any workspace of at least 256 bytes (only the control block is used). */
 muon_status ns_gram(const void *x, void *g, int64_t K, int64_t m, int64_t n, float alpha, void *ws, size_t ws_bytes,
                     muon_stream_t stream);
-muon_status ns_poly(const void *g, void *h, int64_t K, int64_t m, float b, float c, void *ws, size_t ws_bytes,
-                    muon_stream_t stream);
-muon_status ns_apply(const void *h, const void *x, void *out, int64_t K, int64_t m, int64_t n, float a, void *ws,
+muon_status ns_poly(const void *g, void *h, int64_t K, int64_t m, float a, float b, float c, void *ws,
+                    size_t ws_bytes, muon_stream_t stream);
+muon_status ns_apply(const void *h, const void *x, void *out, int64_t K, int64_t m, int64_t n, void *ws,
                      size_t ws_bytes, muon_stream_t stream);
 
 /* Shape bucketing, host only ([P1] "Parameter Processing and Padding": stacking into (K, ...);

@@ -147,7 +147,8 @@ def test_other_entry_point_checks():
     assert lib.ns_gram(FAKE, FAKE, 1, 12, 16, 1.0, FAKE, 256, None) == L.MUON_ERR_SHAPE       # m not a multiple of 8
     assert lib.ns_gram(FAKE + 8, FAKE, 1, 16, 16, 1.0, FAKE, 256, None) == L.MUON_ERR_ALIGNMENT
     assert lib.ns_gram(FAKE, FAKE, 1, 16, 16, 1.0, FAKE, 128, None) == L.MUON_ERR_WORKSPACE
-    assert lib.ns_apply(FAKE, FAKE, FAKE, 1, 16, 16, 1.0, FAKE, 256, None) == L.MUON_ERR_INVALID_ARG  # out aliases x
+    assert lib.ns_apply(FAKE, FAKE, FAKE, 1, 16, 16, FAKE, 256, None) == L.MUON_ERR_INVALID_ARG  # out aliases x
+    assert lib.ns_poly(FAKE, FAKE, 1, 16, float("nan"), 1.0, 1.0, FAKE, 256, None) == L.MUON_ERR_INVALID_ARG
     assert lib.muon_debug_wait_timeout(FAKE, 256, 0, None) == L.MUON_ERR_INVALID_ARG
 
 

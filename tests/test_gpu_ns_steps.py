@@ -1,8 +1,9 @@
 """GPU parity of the three tensor-core steps of one Newton-Schulz iteration, through the C ABI.
 
 Each step is compared element by element with its definition evaluated in fp64 on the same bf16
-inputs: G = alpha X X^T, H = b G + c G G, out = a X + H X (the loop body of newton_schulz in
-"Optimizers: AdamW, Muon and the distributed optimizer", section "Muon: orthogonalising the update").
+inputs: G = alpha X X^T, H = a I + b G + c G G, out = H X (the loop body of newton_schulz in
+"Optimizers: AdamW, Muon and the distributed optimizer", section "Muon: orthogonalising the update",
+a X + (b G + c G G) X, with a folded into the polynomial).
 Shapes span several 128 x 256 tiles, ragged edges in both dimensions, a single row, and K > 1.
 """
 import numpy as np
@@ -58,14 +59,15 @@ def test_poly(L, K, m, n):
     g = torch.from_numpy(G).to(torch.bfloat16).to(DEV)
     Gb = f64(g)
     h = torch.full((K, m, m), float("nan"), dtype=torch.bfloat16, device=DEV)
-    b, c = -4.7750, 2.0315
+    a, b, c = 3.4445, -4.7750, 2.0315
     ws = ctrl_ws()
-    L.ns_poly(g, h, b, c, ws)
+    L.ns_poly(g, h, a, b, c, ws)
     assert L.muon_check(ws) == L.MUON_OK
     got = f64(h)
     GG = Gb @ Gb
-    ref = b * Gb + c * GG
-    terms = abs(b) * np.abs(Gb) + abs(c) * np.abs(GG)
+    eye = np.eye(m)[None]
+    ref = a * eye + b * Gb + c * GG
+    terms = a * eye + abs(b) * np.abs(Gb) + abs(c) * np.abs(GG)
     _check(got, ref, 2.0 ** -8 * terms + abs(c) * 1e-5 * (np.abs(Gb) @ np.abs(Gb)) + 2.0 ** -8 * np.abs(ref))
     assert np.array_equal(got, got.transpose(0, 2, 1))
 
@@ -76,19 +78,16 @@ def test_apply(L, K, m, n):
     X = f64(x)
     gen = torch.Generator().manual_seed(5 + m)
     H = torch.randn((K, m, m), generator=gen, dtype=torch.float64) / np.sqrt(m)
-    H = (H + H.transpose(1, 2)) / 2
+    H = (H + H.transpose(1, 2)) / 2 + 3.4445 * torch.eye(m, dtype=torch.float64)   # a*I + symmetric, as ns_poly makes
     h = H.to(torch.bfloat16).to(DEV)
     Hb = f64(h)
     out = torch.full((K, m, n), float("nan"), dtype=torch.bfloat16, device=DEV)
-    a = 3.4445
     ws = ctrl_ws()
-    L.ns_apply(h, x, out, a, ws)
+    L.ns_apply(h, x, out, ws)
     assert L.muon_check(ws) == L.MUON_OK
     got = f64(out)
-    HX = Hb @ X
-    ref = a * X + HX
-    terms = abs(a) * np.abs(X) + np.abs(HX)
-    _check(got, ref, 2.0 ** -8 * terms + 1e-5 * (np.abs(Hb) @ np.abs(X)) + 2.0 ** -8 * np.abs(ref))
+    ref = Hb @ X
+    _check(got, ref, 1e-5 * (np.abs(Hb) @ np.abs(X)) + 2.0 ** -8 * np.abs(ref))
 
 
 def test_bounded_wait_reports_timeout_and_context_survives(L):
