@@ -136,6 +136,7 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.skip = 0
         self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv")
 
     def __enter__(self):
@@ -143,10 +144,19 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                          "--format=csv,noheader,nounits", "-lms", "25"], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return self
+        # the timed region starts only once the sampler is producing lines
+        t0 = time.time()
+        while time.time() - t0 < 10 and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.01)
+        with open(self.path) as f:
+            self.skip = sum(1 for _ in f)
         return self
 
     def __exit__(self, *exc):
@@ -164,18 +174,22 @@ class ClockSampler:
         sms, maxes, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sms.append(float(parts[1]))
-                    maxes.append(float(parts[2]))
-                except ValueError:
-                    continue
-                for name, val in zip(names, parts[5:9]):
-                    if val.lower() == "active":
-                        reasons.add(name)
+            lines = f.readlines()
+        # samples taken before the timed region started are dropped (unless nothing else came)
+        if len(lines) > self.skip:
+            lines = lines[self.skip:]
+        for line in lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
         os.remove(self.path)
         return {"sm_mhz": statistics.median(sms) if sms else None,
                 "sm_max_mhz": max(maxes) if maxes else sm_max_default,
@@ -491,7 +505,7 @@ def run_ns_sweep(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
