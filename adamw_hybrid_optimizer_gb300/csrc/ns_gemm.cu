@@ -169,8 +169,8 @@ __device__ __forceinline__ uint4 pack8(const float *src) {
 // piece q of line L sits at piece position q ^ (L & 7)). The region first holds the warp's part of the
 // second input (as the loader's TMA wrote it); once every lane has read that, the warp reuses it to
 // reshape its results, so that every global store is a 16-byte store of 8 consecutive elements, four lanes
-// covering one 64-byte row segment. Row-wise access (a thread's own row) and segment-wise access (lane ->
-// row 8k + lane/4, piece lane%4) are both free of bank conflicts beyond the 4 wavefronts 512 bytes need.
+// covering one 64-byte row segment. Row-wise access (a thread's own row) and segment-wise access (seg_row
+// below) are both free of bank conflicts beyond the 4 wavefronts 512 bytes need.
 
 struct Region {
   uint8_t *slot;
@@ -203,6 +203,12 @@ __device__ __forceinline__ void region_read_col(const Region &g, int i, float *d
   for (int j = 0; j < 32; ++j) dst[j] = bf2f(*g.elem(j, i));
 }
 
+// Segment-wise access: in pass k, lane l handles 16-byte piece l%4 of region row seg_row(l, k). The
+// eight lanes of each quarter-warp take rows r and r+4 of the pass, whose swizzled pieces fall on eight
+// distinct 16-byte bank groups, so every quarter-warp phase of a 16-byte shared access is conflict-free;
+// each group of four lanes still covers one contiguous 64-byte row segment in global memory.
+__device__ __forceinline__ int seg_row(int lane, int k) { return 8 * k + (lane >> 3) + 4 * ((lane >> 2) & 1); }
+
 // Stores region row i (32 bf16) to dst_row[0..31] for each of the 32 rows, 16 bytes per lane, four lanes
 // per row. ok(i, e) says whether element e of row i may be written; full(i) whether all 32 may.
 template <typename Ok, typename Full>
@@ -211,7 +217,7 @@ __device__ __forceinline__ void region_store(const Region &g, int lane, __nv_bfl
   const int q = lane & 3;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const int i = 8 * k + (lane >> 2);
+    const int i = seg_row(lane, k);
     const uint4 w = *reinterpret_cast<const uint4 *>(g.piece(i, q));
     __nv_bfloat16 *dst = base + static_cast<long long>(i) * ld + 8 * q;
     if (full(i) && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
@@ -233,7 +239,7 @@ __device__ __forceinline__ void region_load(const Region &g, int lane, const __n
   uint4 w[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const int i = 8 * k + (lane >> 2);
+    const int i = seg_row(lane, k);
     const __nv_bfloat16 *src = base + static_cast<long long>(i) * ld + 8 * q;
     if (full(i) && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
       w[k] = *reinterpret_cast<const uint4 *>(src);
@@ -244,7 +250,7 @@ __device__ __forceinline__ void region_load(const Region &g, int lane, const __n
     }
   }
 #pragma unroll
-  for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(g.piece(8 * k + (lane >> 2), q)) = w[k];
+  for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(g.piece(seg_row(lane, k), q)) = w[k];
 }
 
 // A 32 x 32 block of bf16 parameters as the final step reads it: block row i at base + i*ld, elements
@@ -256,13 +262,13 @@ struct ParamBlock {
   bool valid;
 };
 
-// Issues this lane's four 16-byte loads of a block (segment-wise: row 8k + lane/4, piece lane%4) into
+// Issues this lane's four 16-byte loads of a block (segment-wise, as region_load) into
 // registers; they complete while the caller works on something else.
 __device__ __forceinline__ void block_fetch(const ParamBlock &pb, int lane, uint4 (&w)[4]) {
   const int q = lane & 3;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const int i = 8 * k + (lane >> 2);
+    const int i = seg_row(lane, k);
     const __nv_bfloat16 *src = pb.base + static_cast<long long>(i) * pb.ld + 8 * q;
     if (i < pb.ilim && pb.jlim >= 32 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
       w[k] = *reinterpret_cast<const uint4 *>(src);
@@ -276,7 +282,7 @@ __device__ __forceinline__ void block_fetch(const ParamBlock &pb, int lane, uint
 
 __device__ __forceinline__ void block_commit(const Region &g, int lane, const uint4 (&w)[4]) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(g.piece(8 * k + (lane >> 2), lane & 3)) = w[k];
+  for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(g.piece(seg_row(lane, k), lane & 3)) = w[k];
 }
 
 // Muon parameter update of one element: decoupled decay (masked where u*p <= 0 if cautious), then the
