@@ -747,8 +747,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       if (rec) rec[8] = globaltimer_ns();
       tc_fence_before();
       __syncwarp();
-      // the accumulator is free once both CTAs' epilogues have read their halves (even CTA's barrier)
-      if (lane == 0) mbar_arrive_cluster(leader_acc_empty0 + acc * static_cast<uint32_t>(sizeof(uint64_t)));
+      // the accumulator is free once both CTAs' epilogues have read their halves (even CTA's barrier); the
+      // MMA warp reads none of this warp's global stores, so the signal need not wait for them to drain
+      if (lane == 0) mbar_arrive_cluster_relaxed(leader_acc_empty0 + acc * static_cast<uint32_t>(sizeof(uint64_t)));
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }

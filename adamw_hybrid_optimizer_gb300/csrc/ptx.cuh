@@ -151,8 +151,11 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
 }
 
 // Arrive on an mbarrier given by its cluster shared-memory address (possibly another CTA's).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+// Arrive without release semantics: orders nothing before it, so it does not wait for this thread's
+// earlier global stores to be performed. For signals whose consumer reads none of those stores (the
+// accumulator-free signal: the TMEM reads it covers have completed at tcgen05.wait::ld).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // Tiled load into this CTA's shared memory whose completion is counted on the mbarrier at bar_cluster
