@@ -68,6 +68,7 @@ struct Ctrl {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  int prod_tile;   // the producer's current tile (CTA-local count), for the final step's L2 prefetch pacing
 };
 
 // Pipeline shapes: a long contraction wants mainloop stages, a short one leaves the epilogue as the limit
@@ -287,6 +288,25 @@ __device__ __forceinline__ void block_commit(const Region &g, int lane, const ui
 
 // Muon parameter update of one element: decoupled decay (masked where u*p <= 0 if cautious), then the
 // scaled orthogonalised step.
+template <bool CAUTIOUS>
+__device__ __forceinline__ float param_update_t(float pv, float u, float lr_wd, float lr_scale) {
+  const float d = (!CAUTIOUS || u * pv > 0.f) ? lr_wd : 0.f;
+  return fmaf(-lr_scale, u, fmaf(-d, pv, pv));
+}
+
+// v[j] <- update of parameter value pv(j) with u = v[j], j < 32; the cautious test is taken once per chunk.
+template <typename PV>
+__device__ __forceinline__ void param_update_32(float *v, PV pv, const GemmProblem &a) {
+  const float lr_wd = a.lr_wd, lr_scale = a.lr_scale;
+  if (a.cautious) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = param_update_t<true>(pv(j), v[j], lr_wd, lr_scale);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = param_update_t<false>(pv(j), v[j], lr_wd, lr_scale);
+  }
+}
+
 __device__ __forceinline__ float param_update(float pv, float u, const GemmProblem &a) {
   const float mask = (!a.cautious || u * pv > 0.f) ? 1.f : 0.f;
   return (pv - a.lr_wd * mask * pv) - a.lr_scale * u;
@@ -447,16 +467,11 @@ __device__ __forceinline__ void final_chunk_bf16(const GemmProblem &a, int b, in
   }
   __syncwarp();
   if (!a.transposed) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float pv[8];
-      unpack8(*reinterpret_cast<const uint4 *>(rg.piece(lane, q)), pv);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[8 * q + e] = param_update(pv[e], v[8 * q + e], a);
-    }
+    float pv[32];
+    region_read_row(rg, lane, pv);
+    param_update_32(v, [&](int j) { return pv[j]; }, a);
   } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = param_update(bf2f(*rg.elem(j, lane)), v[j], a);
+    param_update_32(v, [&](int j) { return bf2f(*rg.elem(j, lane)); }, a);
   }
   __syncwarp();
   if (!a.transposed) region_write_row(rg, lane, v);
@@ -495,6 +510,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
     }
     mbar_init(&ctrl->drain, 1);
     ctrl->abort_flag = 0;
+    ctrl->prod_tile = -1;
     fence_mbar_init();
   }
   if (warp == 0 && lane < 2 * args.nprob) {
@@ -535,6 +551,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
           rec[0] = static_cast<unsigned long long>(t);
           rec[1] = globaltimer_ns();
         }
+        if constexpr (EPI == EPI_FINAL) *reinterpret_cast<volatile int *>(&ctrl->prod_tile) = local;
         // descriptor fields copied to registers: the asm below clobbers memory, which would otherwise force a
         // reload from parameter space on every use
         const int pi = find_problem(args, t);
@@ -672,6 +689,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       if (lane == 0)
         for (int s = 0; s < RING_SLOTS; ++s)
           if (last_parity[s] >= 0) drain_wait(&ctrl->ring_full[s], static_cast<uint32_t>(last_parity[s]), ctl);
+    } else if constexpr (EPI == EPI_FINAL) {
+      // ---------------------------------------------------------------- L2 prefetch of the parameters the
+      // epilogue will update: a tile's rows are requested when the producer starts that tile's operand
+      // loads, one to two tiles before its epilogue reads them. Only a hint: the pacing wait gives up after
+      // 50 us, and nothing waits for the prefetches.
+      volatile int *prod_tile = &ctrl->prod_tile;
+      volatile int *abort_flag = &ctrl->abort_flag;
+      int local = 0;
+      for (long long t = first; t < args.total_tiles; t += stride, ++local) {
+        const unsigned long long t0 = globaltimer_ns();
+        while (*prod_tile < local && *abort_flag == 0 && globaltimer_ns() - t0 < 50000ull) __nanosleep(256);
+        if (*abort_flag != 0) break;
+        const GemmProblem P = args.prob[find_problem(args, t)];
+        if (P.params == nullptr || P.out_dtype != MUON_BF16 || (P.orig_cols & 7) != 0) continue;
+        int b, ti, tj;
+        decode_tile(P, args.symmetric, t - P.tile_begin, rank, b, ti, tj);
+        const char *p = static_cast<const char *>(P.params[b]);
+        if ((reinterpret_cast<uintptr_t>(p) & 15) != 0) continue;
+        const int row0 = ti * BM, col0 = tj * BN;
+        if (row0 >= P.rows || col0 >= P.cols) continue;   // the pair's second tile row may lie past the end
+        if (!P.transposed) {
+          // stored wide: this CTA's rows row0 .., columns col0 .. col0 + 255
+          const int ncols = min(BN, P.cols - col0);
+          for (int r = row0 + lane; r < min(row0 + BM, P.rows); r += 32)
+            prefetch_l2_bulk(p + (static_cast<long long>(r) * P.orig_cols + col0) * 2, static_cast<uint32_t>(ncols) * 2);
+        } else {
+          // stored tall: stored rows col0 .. col0 + 255, stored columns row0 .. row0 + 127
+          const int nrows = min(BM, P.rows - row0);
+          for (int c = col0 + lane; c < min(col0 + BN, P.cols); c += 32)
+            prefetch_l2_bulk(p + (static_cast<long long>(c) * P.orig_cols + row0) * 2, static_cast<uint32_t>(nrows) * 2);
+        }
+      }
     }
   } else {
     // ---------------------------------------------------------------- epilogue (warps 2..9)

@@ -113,6 +113,12 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
 }
 
 // 3-D tiled load of one box into shared memory, completing tx bytes on bar.
+// Hint: bring bytes [src, src + bytes) into L2 (16-byte aligned address, bytes a multiple of 16). Nothing
+// waits for it and nothing depends on it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1,
                                             int c2) {
   asm volatile(
