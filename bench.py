@@ -436,8 +436,8 @@ def run_ours(args):
 
 
 def _traffic_from_profiles(kernel):
-    """DRAM bytes per launch recorded from an ncu capture of the current kernels, if committed."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch (JSON) recorded from an ncu capture of the current kernels, if committed."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic_per_launch.txt")
     if not os.path.exists(path):
         return None
     with open(path) as f:
