@@ -206,6 +206,7 @@ __global__ void __launch_bounds__(256) counter_reset_kernel(unsigned *counters, 
 // ------------------------------------------------------------------------------------------ AdamW
 
 __device__ __forceinline__ float adamw_elem(float &pf, float gf, float &mf, float &vf, const AdamwConst &c) {
+  if (c.l2) gf = fmaf(c.l2_wd, pf, gf);
   pf *= c.decay;
   mf = fmaf(c.beta1, mf, c.one_minus_beta1 * gf);
   vf = fmaf(c.beta2, vf, c.one_minus_beta2 * gf * gf);

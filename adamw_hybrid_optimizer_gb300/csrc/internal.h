@@ -152,7 +152,9 @@ muon_status launch_nesterov_norm(const NesterovArgs *probs, int n, cudaStream_t 
 muon_status launch_counter_reset(unsigned *counters, long long n, cudaStream_t s);
 
 struct AdamwConst {
-  float decay;          // 1 - lr*wd
+  int l2;               // 1: g <- g + l2_wd * p before the moments (Adam with L2); 0: decoupled decay
+  float l2_wd;
+  float decay;          // 1 - lr*wd (decoupled), 1 (L2)
   float beta1, one_minus_beta1, beta2, one_minus_beta2;
   float step_size;      // lr / (1 - beta1^t)
   float inv_sqrt_bc2;   // 1 / sqrt(1 - beta2^t)

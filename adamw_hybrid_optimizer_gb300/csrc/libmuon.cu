@@ -444,7 +444,7 @@ muon_status adamw_step(void *param, muon_dtype pdt, const void *grad, muon_dtype
   if (!valid_dtype(pdt) || !valid_dtype(gdt)) return MUON_ERR_DTYPE;
   if (hp->step < 1 || !std::isfinite(hp->lr) || !std::isfinite(hp->beta1) || !std::isfinite(hp->beta2) ||
       !std::isfinite(hp->eps) || !std::isfinite(hp->weight_decay) || hp->beta1 < 0.f || hp->beta1 >= 1.f ||
-      hp->beta2 < 0.f || hp->beta2 >= 1.f)
+      hp->beta2 < 0.f || hp->beta2 >= 1.f || (hp->l2 != 0 && hp->l2 != 1))
     return MUON_ERR_INVALID_ARG;
   muon_status st = check_device();
   if (st != MUON_OK) return st;
@@ -452,7 +452,9 @@ muon_status adamw_step(void *param, muon_dtype pdt, const void *grad, muon_dtype
   const double bc1 = 1.0 - std::pow(static_cast<double>(hp->beta1), t);
   const double bc2 = 1.0 - std::pow(static_cast<double>(hp->beta2), t);
   AdamwConst c{};
-  c.decay = static_cast<float>(1.0 - static_cast<double>(hp->lr) * hp->weight_decay);
+  c.l2 = hp->l2;
+  c.l2_wd = hp->l2 ? hp->weight_decay : 0.f;
+  c.decay = hp->l2 ? 1.f : static_cast<float>(1.0 - static_cast<double>(hp->lr) * hp->weight_decay);
   c.beta1 = hp->beta1;
   c.one_minus_beta1 = static_cast<float>(1.0 - hp->beta1);
   c.beta2 = hp->beta2;

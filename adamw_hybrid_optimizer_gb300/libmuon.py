@@ -41,7 +41,8 @@ class muon_hparams(ctypes.Structure):
 
 class adamw_hparams(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
-                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("step", ctypes.c_int64)]
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("l2", ctypes.c_int32),
+                ("step", ctypes.c_int64)]
 
 
 class muon_bucket(ctypes.Structure):
@@ -203,8 +204,11 @@ def ns_orthogonalize_noalloc(x, out, coeffs, eps: float, stream=None):
     _check(st, "ns_orthogonalize_noalloc")
 
 
-def adamw_step(param, grad, exp_avg, exp_avg_sq, lr, beta1, beta2, eps, weight_decay, step: int, stream=None):
-    hp = adamw_hparams(lr, beta1, beta2, eps, weight_decay, int(step))
+def adamw_step(param, grad, exp_avg, exp_avg_sq, lr, beta1, beta2, eps, weight_decay, step: int, stream=None,
+               l2: bool = False):
+    """l2=False: AdamW (decoupled decay). l2=True: Adam with L2 regularisation (wd*p added to the gradient)."""
+    hp = adamw_hparams(lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=weight_decay, l2=int(bool(l2)),
+                       step=int(step))
     st = lib().adamw_step(param.data_ptr(), _dtype_code(param), grad.data_ptr(), _dtype_code(grad),
                           exp_avg.data_ptr(), exp_avg_sq.data_ptr(), param.numel(), ctypes.byref(hp), _stream(stream))
     _check(st, "adamw_step")

@@ -24,7 +24,8 @@ CLASSIC = (3.4445, -4.7750, 2.0315)
 
 MUON_DEFAULTS = dict(lr=0.02, momentum=0.95, weight_decay=0.01, nesterov=True, cautious_wd=False, scale_mode=0,
                      ns_steps=5, ns_coefficients=None, eps=1e-7)
-ADAMW_DEFAULTS = dict(lr=3e-4, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1)
+# is_adamw=False: Adam with L2 regularisation instead of decoupled decay ("dtensor-muon 0.1.0", "Key options")
+ADAMW_DEFAULTS = dict(lr=3e-4, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1, is_adamw=True)
 
 
 class _Bucket:
@@ -125,7 +126,7 @@ class HybridMuonAdamW:
                         continue
                     st = self.state[p]
                     L.adamw_step(p, p.grad, st["exp_avg"], st["exp_avg_sq"], group["lr"], b1, b2, group["eps"],
-                                 group["weight_decay"], group["step"])
+                                 group["weight_decay"], group["step"], l2=not group["is_adamw"])
 
     def zero_grad(self, set_to_none: bool = True):
         for group in self.param_groups:

@@ -67,9 +67,11 @@ typedef struct {
   float eps;           /* added to the Frobenius norm before dividing, 1e-7 on the pages */
 } muon_hparams;
 
-/* AdamW hyperparameters ([P2] "AdamW: decoupled weight decay"). */
+/* AdamW hyperparameters ([P2] "AdamW: decoupled weight decay"; [P3] "Key options", is_adamw). */
 typedef struct {
   float lr, beta1, beta2, eps, weight_decay;
+  int32_t l2;   /* 0: decoupled decay (AdamW). 1: L2 regularisation, wd*p joins the gradient before the
+                 * moments and nothing decays separately (Adam; the is_adamw=False option) */
   int64_t step; /* t >= 1, the step count after this update; kept by the caller */
 } adamw_hparams;
 
@@ -135,6 +137,9 @@ muon_status ns_orthogonalize(const void *x, muon_dtype xdt, void *out, muon_dtyp
 /* One AdamW step on n elements, [P2] "AdamW: decoupled weight decay":
  * p <- p*(1 - lr*wd); m <- b1*m + (1-b1)*g; v <- b2*v + (1-b2)*g^2;
  * p <- p - lr * (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps).
+ * With hp->l2 = 1 (Adam with L2 regularisation, [P2] same section; [P3] is_adamw=False): g <- g + wd*p
+ * first, then the same moments and update with no p*(1 - lr*wd) factor. hp->l2 other than 0 or 1 is
+ * MUON_ERR_INVALID_ARG.
  *   param, grad  device, n elements of pdt / gdt (MUON_F32 or MUON_BF16 each).
  *   exp_avg, exp_avg_sq  device fp32, n elements each; zero before the first step.
  * Any alignment works; 16-byte aligned pointers take the vectorised path. */

@@ -42,6 +42,12 @@ def test_library_exports_every_declared_symbol():
     assert set(declared_functions()) == set(L.SIGNATURES)
 
 
+def test_hparam_struct_layouts():
+    # the C layout: five floats, the int32 mode, then the int64 step at offset 24
+    assert ctypes.sizeof(L.adamw_hparams) == 32 and L.adamw_hparams.step.offset == 24
+    assert L.adamw_hparams.l2.offset == 20
+
+
 def test_status_strings():
     for code in range(0, 9):
         assert L.muon_status_string(code).startswith("MUON_")
@@ -136,13 +142,15 @@ def test_other_entry_point_checks():
     assert lib.ns_orthogonalize(FAKE, 0, FAKE, 0, 2, 16, 16, 0, c, 1e-7, FAKE, ws_b, None) == L.MUON_ERR_INVALID_ARG
     assert lib.ns_orthogonalize(FAKE, 0, FAKE, 0, 2, 16, 16, n, c, -1.0, FAKE, ws_b, None) == L.MUON_ERR_INVALID_ARG
     assert lib.ns_orthogonalize(FAKE, 0, FAKE, 0, 2, 16, 16, n, c, 1e-7, FAKE, 64, None) == L.MUON_ERR_WORKSPACE
-    hp = L.adamw_hparams(1e-3, 0.9, 0.95, 1e-8, 0.1, 1)
+    hp = L.adamw_hparams(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, step=1)
     assert lib.adamw_step(None, 0, FAKE, 0, FAKE, FAKE, 8, ctypes.byref(hp), None) == L.MUON_ERR_INVALID_ARG
     assert lib.adamw_step(FAKE, 0, FAKE, 0, FAKE, FAKE, 0, ctypes.byref(hp), None) == L.MUON_ERR_INVALID_ARG
     assert lib.adamw_step(FAKE, 2, FAKE, 0, FAKE, FAKE, 8, ctypes.byref(hp), None) == L.MUON_ERR_DTYPE
-    bad = L.adamw_hparams(1e-3, 1.0, 0.95, 1e-8, 0.1, 1)
+    bad = L.adamw_hparams(lr=1e-3, beta1=1.0, beta2=0.95, eps=1e-8, weight_decay=0.1, step=1)
     assert lib.adamw_step(FAKE, 0, FAKE, 0, FAKE, FAKE, 8, ctypes.byref(bad), None) == L.MUON_ERR_INVALID_ARG
-    t0 = L.adamw_hparams(1e-3, 0.9, 0.95, 1e-8, 0.1, 0)
+    t0 = L.adamw_hparams(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, step=0)
+    assert lib.adamw_step(FAKE, 0, FAKE, 0, FAKE, FAKE, 8, ctypes.byref(t0), None) == L.MUON_ERR_INVALID_ARG
+    t0 = L.adamw_hparams(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, l2=2, step=1)
     assert lib.adamw_step(FAKE, 0, FAKE, 0, FAKE, FAKE, 8, ctypes.byref(t0), None) == L.MUON_ERR_INVALID_ARG
     assert lib.ns_gram(FAKE, FAKE, 1, 12, 16, 1.0, FAKE, 256, None) == L.MUON_ERR_SHAPE       # m not a multiple of 8
     assert lib.ns_gram(FAKE + 8, FAKE, 1, 16, 16, 1.0, FAKE, 256, None) == L.MUON_ERR_ALIGNMENT

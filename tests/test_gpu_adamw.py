@@ -1,4 +1,5 @@
-"""GPU parity of adamw_step against the fp64 oracle, through the C ABI."""
+"""GPU parity of adamw_step against the fp64 oracle, through the C ABI: AdamW (decoupled decay) and, with
+l2=True, Adam with L2 regularisation (the is_adamw=False option)."""
 import numpy as np
 import pytest
 import torch
@@ -15,8 +16,9 @@ def L():
     return build_lib()
 
 
-def _run(L, p, g_list, hp, wd, sample=None, pdt="f32"):
+def _run(L, p, g_list, hp, wd, sample=None, pdt="f32", l2=False):
     """Runs len(g_list) AdamW steps on the GPU and the oracle; compares p, m, v on `sample` indices."""
+    oracle_step = oadamw.adam_l2_update if l2 else oadamw.adamw_update
     n = p.numel()
     idx = np.arange(n) if sample is None else sample
     m = torch.zeros(n, dtype=torch.float32, device=DEV)
@@ -25,11 +27,12 @@ def _run(L, p, g_list, hp, wd, sample=None, pdt="f32"):
     # error allowance carried from step to step: the moments' earlier rounding is scaled by beta each step
     # and a new 1e-6 of this step's terms is added (independent trajectories keep each other's error)
     em, ev = np.zeros(len(idx)), np.zeros(len(idx))
+    dp = np.zeros(len(idx))   # |gpu p - oracle p| entering this step (bf16 trajectories may differ)
     for t, g in enumerate(g_list, start=1):
-        L.adamw_step(p, g, m, v, hp.lr, hp.beta1, hp.beta2, hp.eps, wd, t)
+        L.adamw_step(p, g, m, v, hp.lr, hp.beta1, hp.beta2, hp.eps, wd, t, l2=l2)
         po_prev, mo_prev = po, mo
-        po, mo, vo = oadamw.adamw_update(po, f64(g)[idx], mo, vo, t, lr=hp.lr, beta1=hp.beta1, beta2=hp.beta2,
-                                         eps=hp.eps, weight_decay=wd, param_dtype=pdt)
+        po, mo, vo = oracle_step(po, f64(g)[idx], mo, vo, t, lr=hp.lr, beta1=hp.beta1, beta2=hp.beta2,
+                                 eps=hp.eps, weight_decay=wd, param_dtype=pdt)
         torch.cuda.synchronize()
         got_p, got_m, got_v = f64(p)[idx], f64(m)[idx], f64(v)[idx]
         if pdt == "f32":
@@ -40,8 +43,15 @@ def _run(L, p, g_list, hp, wd, sample=None, pdt="f32"):
             terms = np.abs(po_prev) + hp.lr * (1 + 1e-3)
             assert np.all(np.abs(got_p - po) <= t * bf16_ulp(po) * 1.0001 + 1e-6 * terms), t
         gi = f64(g)[idx]
+        if l2:
+            # the moments see g + wd*p: its fp32 rounding adds to their budget, and so does the difference of
+            # the two parameter trajectories it starts from (wd * dp, scaled by 1 - beta into m and v)
+            gi = np.abs(gi) + abs(wd) * np.abs(po_prev)
+            em = em + (1 - hp.beta1) * abs(wd) * dp
+            ev = ev + (1 - hp.beta2) * (2 * gi * abs(wd) * dp + (wd * dp) ** 2)
         em = hp.beta1 * em + 1e-6 * (hp.beta1 * np.abs(mo_prev) + np.abs(gi))
         ev = hp.beta2 * ev + 1e-6 * (np.abs(vo) + gi * gi)
+        dp = np.abs(got_p - po)
         bound_m = em + 1e-30
         bad = np.abs(got_m - mo) > bound_m
         if bad.any():
@@ -92,3 +102,21 @@ def test_layernorm_vectors_no_decay_bf16(L):
     p = workloads.adamw_param_init(w, 5).to(DEV)
     gs = [workloads.adamw_grad(w, t, 5).to(DEV) for t in range(1, 4)]
     _run(L, p, gs, w.adamw_hp, 0.0, pdt="bf16")
+
+
+@pytest.mark.parametrize("n,offset", [(8195, 0), (8195, 1)])
+def test_adam_l2_fp32(L, n, offset):
+    g0 = torch.Generator().manual_seed(10 + n + offset)
+    base_p = torch.randn(n + offset, generator=g0).to(DEV)
+    base_g = torch.randn(n + offset, generator=g0).to(DEV)
+    p, g = base_p[offset:], base_g[offset:]
+    hp = workloads.workload("tiny").adamw_hp
+    _run(L, p, [g, g * 0.5, -g], hp, 0.1, l2=True)
+
+
+def test_adam_l2_bf16_params(L):
+    hp = workloads.workload("gpt2s").adamw_hp
+    g0 = torch.Generator().manual_seed(11)
+    p = (torch.randn(40_003, generator=g0) * 1e-3).to(torch.bfloat16).to(DEV)
+    gs = [(torch.randn(40_003, generator=g0) * 1e-3).to(torch.bfloat16).to(DEV) for _ in range(3)]
+    _run(L, p, gs, hp, 0.1, pdt="bf16", l2=True)

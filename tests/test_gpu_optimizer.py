@@ -105,3 +105,26 @@ def test_resume_bit_matches_uninterrupted_run(L):
     torch.cuda.synchronize()
     for a_, b_ in zip(params, ref_final):
         assert torch.equal(a_, b_)
+
+
+def test_is_adamw_false_group_takes_adam_with_l2(L):
+    """An AdamW group with is_adamw=False runs Adam with L2 regularisation ("dtensor-muon 0.1.0", "Key options")."""
+    from adamw_hybrid_optimizer_gb300 import HybridMuonAdamW
+    a = workloads.workload("gpt2s").adamw_hp
+    _, other = _model(3)
+    before = [f64(p) for p in other]
+    opt = HybridMuonAdamW([{"params": other, "kind": "adamw", "lr": a.lr, "betas": (a.beta1, a.beta2), "eps": a.eps,
+                            "weight_decay": 0.1, "is_adamw": False}])
+    _grads(other, 1, 3)
+    grads = [f64(p.grad) for p in other]
+    opt.step()
+    torch.cuda.synchronize()
+    for i, p in enumerate(other):
+        ref, _, _ = oadamw.adam_l2_update(before[i], grads[i], 0, 0, 1, lr=a.lr, beta1=a.beta1, beta2=a.beta2,
+                                          eps=a.eps, weight_decay=0.1, param_dtype="bf16")
+        ulp = np.ldexp(1.0, np.frexp(np.maximum(np.abs(ref), 1e-30))[1] - 8)
+        assert np.all(np.abs(f64(p) - ref) <= ulp * 1.0001 + 1e-6 * (np.abs(before[i]) + a.lr))
+        # and it is not the decoupled rule on this input
+        dec, _, _ = oadamw.adamw_update(before[i], grads[i], 0, 0, 1, lr=a.lr, beta1=a.beta1, beta2=a.beta2,
+                                        eps=a.eps, weight_decay=0.1, param_dtype="bf16")
+        assert not np.array_equal(dec, ref)
