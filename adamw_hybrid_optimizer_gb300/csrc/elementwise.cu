@@ -389,6 +389,69 @@ muon_status launch_nesterov_norm(const NesterovArgs *probs, int n, cudaStream_t 
   return flush();
 }
 
+// AdamW on fp32 master weights: the update reads and writes the master, and p receives it rounded to bf16.
+template <typename GT>
+__global__ void __launch_bounds__(256) adamw_master_kernel(float *__restrict__ master, __nv_bfloat16 *__restrict__ p,
+                                                           const GT *__restrict__ g, float *__restrict__ m,
+                                                           float *__restrict__ v, long long n, int vec,
+                                                           AdamwConst c) {
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  long long done = 0;
+  if (vec) {
+    const long long groups = n / 8;
+    for (long long i = tid; i < groups; i += stride) {
+      const long long o = i * 8;
+      float pf[8], gf[8], mf[8], vf[8];
+      load8(master + o, pf);
+      load8(g + o, gf);
+      load8(m + o, mf);
+      load8(v + o, vf);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) adamw_elem(pf[e], gf[e], mf[e], vf[e], c);
+      store8(master + o, pf);
+      store8(p + o, pf);
+      store8(m + o, mf);
+      store8(v + o, vf);
+    }
+    done = groups * 8;
+  }
+  for (long long i = done + tid; i < n; i += stride) {
+    float pf = master[i], mf = m[i], vf = v[i];
+    adamw_elem(pf, load1(g, i), mf, vf, c);
+    master[i] = pf;
+    store1(p, i, pf);
+    m[i] = mf;
+    v[i] = vf;
+  }
+}
+
+long long adamw_blocks(long long work) {
+  const long long sms = device_sm_count();
+  long long blocks = (work + 255) / 256;
+  const long long cap = sms * 8;  // 8 resident 256-thread blocks per SM, grid-stride beyond that
+  if (blocks > cap) blocks = cap;
+  return blocks < 1 ? 1 : blocks;
+}
+
+muon_status launch_adamw_master(float *master, __nv_bfloat16 *p, const void *g, int gdt, float *m, float *v,
+                                long long n, const AdamwConst &c, cudaStream_t s) {
+  auto aligned = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
+  const int vec = aligned(master) && aligned(p) && aligned(g) && aligned(m) && aligned(v);
+  const dim3 gb(static_cast<unsigned>(adamw_blocks(vec ? (n / 8 + (n % 8)) : n))), tb(256);
+  launch_begin(KK_ADAMW, s);
+  const cudaError_t e =
+      gdt == MUON_F32
+          ? launch_pdl(adamw_master_kernel<float>, gb, tb, 0, s, master, p, static_cast<const float *>(g), m, v, n,
+                       vec, c)
+          : launch_pdl(adamw_master_kernel<__nv_bfloat16>, gb, tb, 0, s, master, p,
+                       static_cast<const __nv_bfloat16 *>(g), m, v, n, vec, c);
+  launch_end(s);
+  return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+}
+
 muon_status launch_adamw(void *p, int pdt, const void *g, int gdt, float *m, float *v, long long n,
                          const AdamwConst &c, cudaStream_t s) {
   auto aligned = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };

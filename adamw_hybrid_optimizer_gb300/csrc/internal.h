@@ -56,8 +56,10 @@ struct GemmProblem {
   // bf16 output of gram / poly / apply
   __nv_bfloat16 *out;
   long long ld_out, mstride_out;
-  // final step: parameter update (params != null) or dense store (out_dense != null)
+  // final step: parameter update (params != null) or dense store (out_dense != null); with master, the
+  // update applies to the fp32 master copies and params receive them rounded to bf16
   void *const *params;
+  float *const *master;
   void *out_dense;
   int out_dtype;          // muon_dtype of params / out_dense
   int transposed;         // stored matrix is the transpose of the wide iterate
@@ -78,6 +80,7 @@ struct Bf16Stack {
 // or a dense store, transposing back when the stored matrix is tall.
 struct FinalSpec {
   void *const *params;   // device array of K pointers (update) or null
+  float *const *master;  // device array of K pointers to fp32 master copies of bf16 params, or null
   void *out_dense;       // contiguous (K, A, B) (store) or null
   int dtype;             // muon_dtype
   int transposed;
@@ -162,6 +165,8 @@ struct AdamwConst {
 };
 muon_status launch_adamw(void *p, int pdt, const void *g, int gdt, float *m, float *v, long long n,
                          const AdamwConst &c, cudaStream_t s);
+muon_status launch_adamw_master(float *master, __nv_bfloat16 *p, const void *g, int gdt, float *m, float *v,
+                                long long n, const AdamwConst &c, cudaStream_t s);
 
 muon_status launch_debug_wait(uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
 

@@ -309,6 +309,7 @@ static muon_status check_bucket(const muon_bucket &b) {
   muon_status st = check_stack_dims(b.K, b.A, b.B);
   if (st != MUON_OK) return st;
   if (!valid_dtype(b.pdt) || !valid_dtype(b.gdt)) return MUON_ERR_DTYPE;
+  if (b.master != nullptr && b.pdt != MUON_BF16) return MUON_ERR_DTYPE;
   return MUON_OK;
 }
 
@@ -390,6 +391,7 @@ muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hpar
                                  : std::sqrt(std::max(1.0, static_cast<double>(bk.A) / static_cast<double>(bk.B)));
         FinalSpec fin{};
         fin.params = bk.params;
+        fin.master = bk.master;
         fin.dtype = bk.pdt;
         fin.transposed = bk.A > bk.B ? 1 : 0;
         fin.orig_cols = static_cast<int>(bk.B);
@@ -436,22 +438,16 @@ muon_status ns_orthogonalize(const void *x, muon_dtype xdt, void *out, muon_dtyp
   return run_ns_chain(reinterpret_cast<uint32_t *>(base), w, L, K, ns_steps, coeffs, fin, s);
 }
 
-muon_status adamw_step(void *param, muon_dtype pdt, const void *grad, muon_dtype gdt, float *exp_avg,
-                       float *exp_avg_sq, int64_t n, const adamw_hparams *hp, muon_stream_t stream) {
-  if (param == nullptr || grad == nullptr || exp_avg == nullptr || exp_avg_sq == nullptr || hp == nullptr)
-    return MUON_ERR_INVALID_ARG;
-  if (n < 1) return MUON_ERR_INVALID_ARG;
-  if (!valid_dtype(pdt) || !valid_dtype(gdt)) return MUON_ERR_DTYPE;
+// Validates AdamW hyperparameters and derives the kernel constants.
+static muon_status adamw_constants(const adamw_hparams *hp, AdamwConst *out) {
   if (hp->step < 1 || !std::isfinite(hp->lr) || !std::isfinite(hp->beta1) || !std::isfinite(hp->beta2) ||
       !std::isfinite(hp->eps) || !std::isfinite(hp->weight_decay) || hp->beta1 < 0.f || hp->beta1 >= 1.f ||
       hp->beta2 < 0.f || hp->beta2 >= 1.f || (hp->l2 != 0 && hp->l2 != 1))
     return MUON_ERR_INVALID_ARG;
-  muon_status st = check_device();
-  if (st != MUON_OK) return st;
   const double t = static_cast<double>(hp->step);
   const double bc1 = 1.0 - std::pow(static_cast<double>(hp->beta1), t);
   const double bc2 = 1.0 - std::pow(static_cast<double>(hp->beta2), t);
-  AdamwConst c{};
+  AdamwConst &c = *out;
   c.l2 = hp->l2;
   c.l2_wd = hp->l2 ? hp->weight_decay : 0.f;
   c.decay = hp->l2 ? 1.f : static_cast<float>(1.0 - static_cast<double>(hp->lr) * hp->weight_decay);
@@ -462,7 +458,35 @@ muon_status adamw_step(void *param, muon_dtype pdt, const void *grad, muon_dtype
   c.step_size = static_cast<float>(hp->lr / bc1);
   c.inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(bc2));
   c.eps = hp->eps;
+  return MUON_OK;
+}
+
+muon_status adamw_step(void *param, muon_dtype pdt, const void *grad, muon_dtype gdt, float *exp_avg,
+                       float *exp_avg_sq, int64_t n, const adamw_hparams *hp, muon_stream_t stream) {
+  if (param == nullptr || grad == nullptr || exp_avg == nullptr || exp_avg_sq == nullptr || hp == nullptr)
+    return MUON_ERR_INVALID_ARG;
+  if (n < 1) return MUON_ERR_INVALID_ARG;
+  if (!valid_dtype(pdt) || !valid_dtype(gdt)) return MUON_ERR_DTYPE;
+  AdamwConst c{};
+  muon_status st = adamw_constants(hp, &c);
+  if (st != MUON_OK) return st;
+  if ((st = check_device()) != MUON_OK) return st;
   return launch_adamw(param, pdt, grad, gdt, exp_avg, exp_avg_sq, n, c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+muon_status adamw_step_master(float *master, void *param, const void *grad, muon_dtype gdt, float *exp_avg,
+                              float *exp_avg_sq, int64_t n, const adamw_hparams *hp, muon_stream_t stream) {
+  if (master == nullptr || param == nullptr || grad == nullptr || exp_avg == nullptr || exp_avg_sq == nullptr ||
+      hp == nullptr)
+    return MUON_ERR_INVALID_ARG;
+  if (n < 1) return MUON_ERR_INVALID_ARG;
+  if (!valid_dtype(gdt)) return MUON_ERR_DTYPE;
+  AdamwConst c{};
+  muon_status st = adamw_constants(hp, &c);
+  if (st != MUON_OK) return st;
+  if ((st = check_device()) != MUON_OK) return st;
+  return launch_adamw_master(master, static_cast<__nv_bfloat16 *>(param), grad, gdt, exp_avg, exp_avg_sq, n, c,
+                             reinterpret_cast<cudaStream_t>(stream));
 }
 
 static muon_status check_step_stack(const void *p, int64_t K, int64_t m, int64_t n) {

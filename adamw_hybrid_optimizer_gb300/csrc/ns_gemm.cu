@@ -5,23 +5,23 @@
 //     G = X X^T                     EPI_GRAM   symmetric: only tiles touching the upper triangle
 //                                              are computed, every value is also stored mirrored
 //                                              ("DMuon", section 2.2, symmetric Gram)
-//     H = b G + c G G               EPI_POLY   G symmetric, so G G = G G^T: same operand pattern
-//     X' = a X + H X                EPI_APPLY  B operand (X) is read N-major
-//     last step: u = a X + H X, then p <- p - lr*wd*p*mask - lr*scale*u      EPI_FINAL
+//     H = a I + b G + c G G         EPI_POLY   G symmetric, so G G = G G^T: same operand pattern
+//     X' = H X                      EPI_APPLY  (= a X + (b G + c G G) X); B operand X read N-major
+//     last step: u = H X, then p <- p - lr*wd*p*mask - lr*scale*u      EPI_FINAL (EPI_FINAL_MASTER: on fp32
+//                                                                      master copies of bf16 parameters)
 //
-// Design (sm_103a): 128 x 256 output tiles per CTA, 64-deep k-slices, a TMA ring with 128-byte swizzle
-// (6 stages, 4 when the contraction is short), one tcgen05.mma per 16-slice issued by one thread, fp32 accumulators in tensor memory (2 x 256 columns, so the epilogue of one
-// tile overlaps the MMAs of the next), persistent CTAs (one per SM) striding over the tiles of up to
-// GEMM_MAX_PROBLEMS stacks at once. CTAs run as pairs (clusters of two) on vertically adjacent tiles
-// (rows 2p and 2p+1 of one tile column) with paired-SM MMAs (tcgen05 cta_group::2, M = 256): each CTA
-// holds its 128 rows of A and one half of B, the even CTA issues the MMAs, and each CTA's tensor memory
-// receives its own 128 accumulator rows. Per SM a 64-deep stage is 32 KB instead of 48 KB, which halves
-// the shared-memory traffic per MMA and leaves room for 6 stages (or 4 stages and a 5-slot ring). Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM
-// owner), warps 2-9 = epilogue (two per tensor-memory lane quarter, each taking one 32-column half of
-// every 64-column slot), warp 10 = epilogue loader: ahead of the epilogue it TMA-loads each tile's second
-// input (G or X) into a shared-memory ring (2 or 5 slots, by contraction depth). Each epilogue warp then
-// reuses its part of the slot to reshape results, so global stores (and the final step's parameter
-// loads) are coalesced 16-byte accesses; transposed outputs go through shared memory.
+// Design (sm_103a): CTAs run as pairs (clusters of two) on vertically adjacent 128 x 256 output tiles with
+// paired-SM MMAs (tcgen05 cta_group::2, M = 256): each CTA holds its 128 rows of A and one half of B, the
+// even CTA issues the MMAs, and each CTA's tensor memory receives its own 128 accumulator rows (2 x 256
+// fp32 columns, so the epilogue of one tile overlaps the MMAs of the next). Operands arrive by TMA
+// (128-byte swizzle) through a ring of 64-deep stages of 32 KB per CTA (6 stages; POLY with a short
+// contraction: 4 stages and a 5-slot input ring). The CTAs are persistent (one per SM) and stride over
+// the tiles of up to GEMM_MAX_PROBLEMS stacks at once. Warp roles: warp 0 = TMA producer, warp 1 = MMA
+// issuer (and TMEM owner), warps 2-9 = epilogue (two per tensor-memory lane quarter, each taking one
+// 32-column half of every 64-column slot), warp 10 = epilogue loader (POLY: TMA of G's tile into the
+// ring; FINAL: L2 prefetch of the parameters a tile ahead). Each epilogue warp reshapes its results in
+// shared memory so that global stores (and the final step's parameter loads, fetched one chunk ahead)
+// are coalesced 16-byte accesses; transposed outputs go through shared memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -57,6 +57,10 @@ constexpr int RING_AUX_BYTES = BM * 64 * 2;
 
 __host__ __device__ constexpr int ring_slot_bytes(int) { return RING_AUX_BYTES; }
 __host__ __device__ constexpr bool has_aux(int epi) { return epi == EPI_POLY; }
+// The final step on fp32 master weights: a kernel of its own, so that the plain final step carries none of
+// its registers.
+constexpr int EPI_FINAL_MASTER = 4;
+__host__ __device__ constexpr bool is_final(int epi) { return epi == EPI_FINAL || epi == EPI_FINAL_MASTER; }
 
 struct Ctrl {
   uint64_t full[MAX_STAGES];
@@ -312,6 +316,42 @@ __device__ __forceinline__ float param_update(float pv, float u, const GemmProbl
   return (pv - a.lr_wd * mask * pv) - a.lr_scale * u;
 }
 
+// Final step with fp32 master weights: this thread's row (stored wide) or column (stored tall) of 32
+// master values (m: the matrix, cols x rows in the wide orientation) is updated in place, and v receives the
+// new values (the caller stores them as bf16).
+__device__ __forceinline__ void master_update(float *m, int rows, int cols, int orig_cols, int transposed, int cautious,
+                                           float lr_wd, float lr_scale, int row, int col0, float *v) {
+  if (row >= rows) return;
+  auto upd = [&](float mv, float u) {
+    return cautious ? param_update_t<true>(mv, u, lr_wd, lr_scale) : param_update_t<false>(mv, u, lr_wd, lr_scale);
+  };
+  if (!transposed) {
+    float *r = m + static_cast<long long>(row) * orig_cols + col0;
+    if (col0 + 32 <= cols && (reinterpret_cast<uintptr_t>(r) & 15) == 0) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float4 x = reinterpret_cast<float4 *>(r)[q];
+        x.x = v[4 * q] = upd(x.x, v[4 * q]);
+        x.y = v[4 * q + 1] = upd(x.y, v[4 * q + 1]);
+        x.z = v[4 * q + 2] = upd(x.z, v[4 * q + 2]);
+        x.w = v[4 * q + 3] = upd(x.w, v[4 * q + 3]);
+        reinterpret_cast<float4 *>(r)[q] = x;
+      }
+      return;
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (col0 + j < cols) v[j] = r[j] = upd(r[j], v[j]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (col0 + j >= cols) continue;
+      float *e = m + static_cast<long long>(col0 + j) * orig_cols + row;
+      v[j] = *e = upd(*e, v[j]);
+    }
+  }
+}
+
 // Final step with fp32 parameters or a dense fp32 output: plain per-thread accesses (small stacks only).
 __device__ __forceinline__ void final_store_f32(const GemmProblem &a, void *base, int row, int col0, float *v) {
   const bool update = a.params != nullptr;
@@ -392,7 +432,10 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem &a, int b, int 
         if (row < rows) final_store_f32(a, base, row, col0, v);
         return;
       }
-      const bool update = a.params != nullptr;
+      if constexpr (EPI == EPI_FINAL_MASTER)   // v <- the new master values
+        master_update(a.master[b], rows, cols, a.orig_cols, a.transposed, a.cautious, a.lr_wd, a.lr_scale, row, col0,
+                      v);
+      const bool update = EPI == EPI_FINAL && a.params != nullptr;
       __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(base);
       if (!a.transposed) {
         // stored wide: region row i = stored row warp_row0 + i, columns col0 ..
@@ -551,7 +594,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
           rec[0] = static_cast<unsigned long long>(t);
           rec[1] = globaltimer_ns();
         }
-        if constexpr (EPI == EPI_FINAL) *reinterpret_cast<volatile int *>(&ctrl->prod_tile) = local;
+        if constexpr (is_final(EPI)) *reinterpret_cast<volatile int *>(&ctrl->prod_tile) = local;
         // descriptor fields copied to registers: the asm below clobbers memory, which would otherwise force a
         // reload from parameter space on every use
         const int pi = find_problem(args, t);
@@ -689,7 +732,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       if (lane == 0)
         for (int s = 0; s < RING_SLOTS; ++s)
           if (last_parity[s] >= 0) drain_wait(&ctrl->ring_full[s], static_cast<uint32_t>(last_parity[s]), ctl);
-    } else if constexpr (EPI == EPI_FINAL) {
+    } else if constexpr (EPI == EPI_FINAL) {   // (no L2 prefetch for the master kernel: parameters are only written)
       // ---------------------------------------------------------------- L2 prefetch of the parameters the
       // epilogue will update: a tile's rows are requested when the producer starts that tile's operand
       // loads, one to two tiles before its epilogue reads them. Only a hint: the pacing wait gives up after
@@ -744,7 +787,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       const int warp_row0 = row0 + lane_base;
       bool aborted = false;
       // final step with bf16 parameters: their blocks are fetched one chunk ahead
-      const bool prefetch_params = EPI == EPI_FINAL && P.params != nullptr && P.out_dtype == MUON_BF16;
+      const bool prefetch_params =
+          EPI == EPI_FINAL && P.params != nullptr && P.out_dtype == MUON_BF16;
       const __nv_bfloat16 *pbase = prefetch_params ? static_cast<const __nv_bfloat16 *>(P.params[b]) : nullptr;
       uint4 pf[4];
       bool pf_ready = false;
@@ -988,6 +1032,7 @@ muon_status GemmBatch::add_final(const Bf16Stack &h, const Bf16Stack &x, const f
   fill_tiles(it.p, x.batch, x.rows, x.cols, h.cols, false);
   it.p.scale = scale;
   it.p.params = f.params;
+  it.p.master = f.master;
   it.p.out_dense = f.out_dense;
   it.p.out_dtype = f.dtype;
   it.p.transposed = f.transposed;
@@ -1006,8 +1051,25 @@ muon_status GemmBatch::launch(cudaStream_t s) {
       items_[j] = items_[j - 1];
       items_[j - 1] = t;
     }
-  for (int first = 0; first < n_; first += GEMM_MAX_PROBLEMS) {
-    const int cnt = (n_ - first) < GEMM_MAX_PROBLEMS ? (n_ - first) : GEMM_MAX_PROBLEMS;
+  // final steps with fp32 master weights run in launches of their own (a kernel compiled for them)
+  if (epi_ == EPI_FINAL) {
+    int w = 0;
+    for (int pass = 0; pass < 2; ++pass)
+      for (int i = w; i < n_; ++i)
+        if ((items_[i].p.master != nullptr) == (pass == 1)) {
+          Item t = items_[i];
+          for (int j = i; j > w; --j) items_[j] = items_[j - 1];
+          items_[w++] = t;
+        }
+  }
+  for (int first = 0; first < n_;) {
+    int cnt = (n_ - first) < GEMM_MAX_PROBLEMS ? (n_ - first) : GEMM_MAX_PROBLEMS;
+    for (int i = 1; i < cnt; ++i)
+      if ((items_[first + i].p.master != nullptr) != (items_[first].p.master != nullptr)) {
+        cnt = i;
+        break;
+      }
+    const bool master = items_[first].p.master != nullptr;
     GemmGroup g;
     memset(&g, 0, sizeof(g));
     long long tiles = 0;
@@ -1035,9 +1097,13 @@ muon_status GemmBatch::launch(cudaStream_t s) {
                      : launch_shape<EPI_POLY, false, 6, 2>(g, KK_POLY, s);
         break;
       case EPI_APPLY: st = launch_shape<EPI_APPLY, true, 6, 1>(g, KK_APPLY, s); break;
-      default: st = launch_shape<EPI_FINAL, true, 6, 1>(g, KK_FINAL, s); break;
+      default:
+        st = master ? launch_shape<EPI_FINAL_MASTER, true, 6, 1>(g, KK_FINAL, s)
+                    : launch_shape<EPI_FINAL, true, 6, 1>(g, KK_FINAL, s);
+        break;
     }
     if (st != MUON_OK) return st;
+    first += cnt;
   }
   return MUON_OK;
 }

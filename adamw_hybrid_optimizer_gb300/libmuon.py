@@ -48,7 +48,7 @@ class adamw_hparams(ctypes.Structure):
 class muon_bucket(ctypes.Structure):
     _fields_ = [("params", ctypes.c_void_p), ("grads", ctypes.c_void_p), ("momentum", ctypes.c_void_p),
                 ("K", ctypes.c_int64), ("A", ctypes.c_int64), ("B", ctypes.c_int64), ("pdt", ctypes.c_int),
-                ("gdt", ctypes.c_int)]
+                ("gdt", ctypes.c_int), ("master", ctypes.c_void_p)]
 
 
 SIGNATURES = {
@@ -65,6 +65,8 @@ SIGNATURES = {
                                                 ctypes.c_int, ctypes.POINTER(ctypes.c_float), ctypes.c_float, _vp]),
     "adamw_step": (ctypes.c_int, [_vp, ctypes.c_int, _vp, ctypes.c_int, _vp, _vp, _c_int64,
                                   ctypes.POINTER(adamw_hparams), _vp]),
+    "adamw_step_master": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int, _vp, _vp, _c_int64,
+                                         ctypes.POINTER(adamw_hparams), _vp]),
     "ns_gram": (ctypes.c_int, [_vp, _vp, _c_int64, _c_int64, _c_int64, ctypes.c_float, _vp, ctypes.c_size_t, _vp]),
     "ns_poly": (ctypes.c_int, [_vp, _vp, _c_int64, _c_int64, ctypes.c_float, ctypes.c_float, ctypes.c_float, _vp,
                                ctypes.c_size_t, _vp]),
@@ -161,10 +163,20 @@ def muon_step_batched(param_ptrs, pdt: int, grad_ptrs, gdt: int, momentum, K: in
 
 
 def make_buckets(specs):
-    """specs: sequence of (param_ptrs, grad_ptrs, momentum, K, A, B, pdt, gdt); returns a ctypes muon_bucket array."""
+    """specs: sequence of (param_ptrs, grad_ptrs, momentum, K, A, B, pdt, gdt[, master_ptrs]); returns a ctypes
+    muon_bucket array. master_ptrs (optional): device array of K pointers to fp32 master copies.
+
+    The array keeps the tensors it points at alive (its `tensors` attribute): a pointer array built inline
+    in the call would otherwise be freed on return, and its memory could be reused before the GPU reads it."""
     arr = (muon_bucket * len(specs))()
-    for i, (pp, gp, mom, K, A, B, pdt, gdt) in enumerate(specs):
-        arr[i] = muon_bucket(pp.data_ptr(), gp.data_ptr(), mom.data_ptr(), K, A, B, pdt, gdt)
+    keep = []
+    for i, spec in enumerate(specs):
+        pp, gp, mom, K, A, B, pdt, gdt = spec[:8]
+        mp = spec[8] if len(spec) > 8 else None
+        keep += [pp, gp, mom] + ([mp] if mp is not None else [])
+        arr[i] = muon_bucket(pp.data_ptr(), gp.data_ptr(), mom.data_ptr(), K, A, B, pdt, gdt,
+                             mp.data_ptr() if mp is not None else None)
+    arr.tensors = keep
     return arr
 
 
@@ -212,6 +224,19 @@ def adamw_step(param, grad, exp_avg, exp_avg_sq, lr, beta1, beta2, eps, weight_d
     st = lib().adamw_step(param.data_ptr(), _dtype_code(param), grad.data_ptr(), _dtype_code(grad),
                           exp_avg.data_ptr(), exp_avg_sq.data_ptr(), param.numel(), ctypes.byref(hp), _stream(stream))
     _check(st, "adamw_step")
+
+
+def adamw_step_master(master, param, grad, exp_avg, exp_avg_sq, lr, beta1, beta2, eps, weight_decay, step: int,
+                      stream=None, l2: bool = False):
+    """adamw_step on fp32 master weights; the bf16 param receives the new master rounded to bf16."""
+    if _dtype_code(param) != MUON_BF16 or _dtype_code(master) != MUON_F32 or master.numel() != param.numel():
+        raise ValueError("adamw_step_master: fp32 master and bf16 param of the same size")
+    hp = adamw_hparams(lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=weight_decay, l2=int(bool(l2)),
+                       step=int(step))
+    st = lib().adamw_step_master(master.data_ptr(), param.data_ptr(), grad.data_ptr(), _dtype_code(grad),
+                                 exp_avg.data_ptr(), exp_avg_sq.data_ptr(), param.numel(), ctypes.byref(hp),
+                                 _stream(stream))
+    _check(st, "adamw_step_master")
 
 
 def ns_gram(x, g, alpha: float, ws, stream=None):

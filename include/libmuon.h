@@ -100,13 +100,18 @@ muon_status muon_step_batched(void *const *params, muon_dtype pdt, const void *c
                               float *momentum, int64_t K, int64_t A, int64_t B, const muon_hparams *hp, void *ws,
                               size_t ws_bytes, muon_stream_t stream);
 
-/* One same-shape stack of Muon matrices for muon_step_grouped (the arguments muon_step_batched takes). */
+/* One same-shape stack of Muon matrices for muon_step_grouped (the arguments muon_step_batched takes,
+ * and optionally fp32 master weights). */
 typedef struct {
   void *const *params;        /* DEVICE array of K device pointers, each an A x B row-major matrix of pdt */
   const void *const *grads;   /* DEVICE array of K device pointers, each an A x B row-major matrix of gdt */
   float *momentum;            /* device fp32 (K, A, B), updated in place */
   int64_t K, A, B;
   muon_dtype pdt, gdt;
+  float *const *master;       /* NULL, or (pdt must be MUON_BF16) a DEVICE array of K device pointers to fp32
+                               * A x B master copies: the update (decay, cautious mask, step) is applied to
+                               * the master, and the parameter becomes the master rounded to bf16 ([P2] "The
+                               * optimizer's memory budget": fp32 master weights beside bf16 weights) */
 } muon_bucket;
 
 /* Workspace bytes for muon_step_grouped: one header (control block and one counter per matrix of all
@@ -145,6 +150,15 @@ muon_status ns_orthogonalize(const void *x, muon_dtype xdt, void *out, muon_dtyp
  * Any alignment works; 16-byte aligned pointers take the vectorised path. */
 muon_status adamw_step(void *param, muon_dtype pdt, const void *grad, muon_dtype gdt, float *exp_avg,
                        float *exp_avg_sq, int64_t n, const adamw_hparams *hp, muon_stream_t stream);
+
+/* adamw_step for bf16 parameters kept with fp32 master weights ([P2] "The optimizer's memory budget":
+ * fp32 master copy, fp32 moments, bf16 weights): the update reads and writes the master, and param
+ * receives the new master rounded to bf16 (round to nearest even).
+ *   master  device fp32, n elements (the values the update starts from).
+ *   param   device bf16, n elements (written only).
+ * Other arguments and errors as adamw_step. */
+muon_status adamw_step_master(float *master, void *param, const void *grad, muon_dtype gdt, float *exp_avg,
+                              float *exp_avg_sq, int64_t n, const adamw_hparams *hp, muon_stream_t stream);
 
 /* ns_orthogonalize without any device allocation. The pages have no counterpart to this call.
  * For callers that cannot allocate device memory and so cannot provide a workspace: code running

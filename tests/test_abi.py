@@ -185,3 +185,9 @@ def test_grouped_entry_point_checks():
     bad = (L.muon_bucket * 2)(good[0], L.muon_bucket(FAKE, FAKE, FAKE, 2, 128, 64, 1, 9))
     assert st(bad) == L.MUON_ERR_DTYPE
     assert L.muon_workspace_bytes_grouped((L.muon_bucket * 1)(L.muon_bucket(FAKE, FAKE, FAKE, 0, 1, 1, 0, 0))) == 0
+    # fp32 master weights go with bf16 parameters only
+    bad = (L.muon_bucket * 2)(good[0], L.muon_bucket(FAKE, FAKE, FAKE, 2, 128, 64, L.MUON_F32, 1, FAKE))
+    assert st(bad) == L.MUON_ERR_DTYPE
+    hp2 = L.adamw_hparams(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, step=1)
+    assert lib.adamw_step_master(None, FAKE, FAKE, 0, FAKE, FAKE, 8, ctypes.byref(hp2), None) == L.MUON_ERR_INVALID_ARG
+    assert lib.adamw_step_master(FAKE, FAKE, FAKE, 5, FAKE, FAKE, 8, ctypes.byref(hp2), None) == L.MUON_ERR_DTYPE

@@ -16,9 +16,12 @@ def L():
     return build_lib()
 
 
-def _run(L, p, g_list, hp, wd, sample=None, pdt="f32", l2=False):
-    """Runs len(g_list) AdamW steps on the GPU and the oracle; compares p, m, v on `sample` indices."""
+def _run(L, p, g_list, hp, wd, sample=None, pdt="f32", l2=False, master=False):
+    """Runs len(g_list) AdamW steps on the GPU and the oracle; compares p, m, v on `sample` indices.
+    master=True: p is an fp32 master copy updated by adamw_step_master, whose bf16 parameter must equal the
+    master rounded to bf16 after every step."""
     oracle_step = oadamw.adam_l2_update if l2 else oadamw.adamw_update
+    bf16_param = p.to(torch.bfloat16) if master else None
     n = p.numel()
     idx = np.arange(n) if sample is None else sample
     m = torch.zeros(n, dtype=torch.float32, device=DEV)
@@ -29,12 +32,17 @@ def _run(L, p, g_list, hp, wd, sample=None, pdt="f32", l2=False):
     em, ev = np.zeros(len(idx)), np.zeros(len(idx))
     dp = np.zeros(len(idx))   # |gpu p - oracle p| entering this step (bf16 trajectories may differ)
     for t, g in enumerate(g_list, start=1):
-        L.adamw_step(p, g, m, v, hp.lr, hp.beta1, hp.beta2, hp.eps, wd, t, l2=l2)
+        if master:
+            L.adamw_step_master(p, bf16_param, g, m, v, hp.lr, hp.beta1, hp.beta2, hp.eps, wd, t, l2=l2)
+        else:
+            L.adamw_step(p, g, m, v, hp.lr, hp.beta1, hp.beta2, hp.eps, wd, t, l2=l2)
         po_prev, mo_prev = po, mo
         po, mo, vo = oracle_step(po, f64(g)[idx], mo, vo, t, lr=hp.lr, beta1=hp.beta1, beta2=hp.beta2,
                                  eps=hp.eps, weight_decay=wd, param_dtype=pdt)
         torch.cuda.synchronize()
         got_p, got_m, got_v = f64(p)[idx], f64(m)[idx], f64(v)[idx]
+        if master:
+            assert torch.equal(bf16_param, p.to(torch.bfloat16)), t
         if pdt == "f32":
             scale = np.abs(po_prev) + hp.lr * (1 + 1e-3)
             assert np.max(np.abs(got_p - po) / scale) <= 1e-6, t
@@ -120,3 +128,16 @@ def test_adam_l2_bf16_params(L):
     p = (torch.randn(40_003, generator=g0) * 1e-3).to(torch.bfloat16).to(DEV)
     gs = [(torch.randn(40_003, generator=g0) * 1e-3).to(torch.bfloat16).to(DEV) for _ in range(3)]
     _run(L, p, gs, hp, 0.1, pdt="bf16", l2=True)
+
+
+@pytest.mark.parametrize("n,offset", [(40_003, 0), (8195, 1)])
+def test_adamw_fp32_master_weights(L, n, offset):
+    """adamw_step_master: the fp32 master follows the oracle's fp32-parameter AdamW; the bf16 parameter is the
+    master rounded to bf16 ("Optimizers: AdamW, Muon and the distributed optimizer", "The optimizer's memory
+    budget": fp32 master weights beside bf16 weights)."""
+    g0 = torch.Generator().manual_seed(20 + n)
+    base_p = (torch.randn(n + offset, generator=g0) * 1e-3).to(DEV)
+    base_g = (torch.randn(n + offset, generator=g0) * 1e-3).to(torch.bfloat16).to(DEV)
+    p, g = base_p[offset:], base_g[offset:]
+    hp = workloads.workload("gpt2s").adamw_hp
+    _run(L, p, [g, g * 0.5, -g], hp, 0.1, master=True)

@@ -1,0 +1,55 @@
+"""fp32 master weights for bf16 Muon parameters (muon_bucket.master), through the C ABI.
+
+The update (decay, step) is applied to the fp32 master and the bf16 parameter becomes the new master
+rounded to bf16 ("Optimizers: AdamW, Muon and the distributed optimizer", section "The optimizer's memory
+budget": fp32 master weights beside bf16 weights). The oracle is the fp32-parameter Muon update on the
+master; the bf16 parameter must equal the GPU's master rounded to bf16, bit for bit, after every step.
+Wide and tall (transposed path) ragged stacks, two steps.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import muon as omuon
+from tests.gpu_common import DEV, build_lib, f64, hp_struct
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def L():
+    return build_lib()
+
+
+@pytest.mark.parametrize("shape", [(136, 264), (264, 136)])
+def test_muon_fp32_master_two_steps(L, shape):
+    A, B = shape
+    K = 3
+    hp = workloads.workload("tiny").muon_hp
+    gen = torch.Generator().manual_seed(A * 7 + B)
+    master = [(torch.randn((A, B), generator=gen) * 0.05).to(DEV) for _ in range(K)]
+    params = [m.to(torch.bfloat16) for m in master]
+    mom = torch.zeros((K, A, B), dtype=torch.float32, device=DEV)
+    m_orc = [f64(m) for m in master]
+    mom_orc = [np.zeros((A, B)) for _ in range(K)]
+    first = [x.copy() for x in m_orc]
+    pptr, mptr = L.pointer_array(params, DEV), L.pointer_array(master, DEV)
+    hps = hp_struct(L, hp)
+    for step in range(1, 3):
+        grads = [(torch.randn((A, B), generator=gen) * 1e-3).to(torch.bfloat16).to(DEV) for _ in range(K)]
+        bk = L.make_buckets([(pptr, L.pointer_array(grads, DEV), mom, K, A, B, L.MUON_BF16, L.MUON_BF16, mptr)])
+        ws = torch.zeros(L.muon_workspace_bytes_grouped(bk), dtype=torch.uint8, device=DEV)
+        L.muon_step_grouped(bk, hps, ws)
+        assert L.muon_check(ws) == L.MUON_OK
+        for k in range(K):
+            g = f64(grads[k])
+            ref, mref, _ = omuon.muon_update(m_orc[k], g, mom_orc[k], lr=hp.lr, momentum=hp.momentum,
+                                             weight_decay=hp.weight_decay, nesterov=hp.nesterov, coeffs=hp.coeffs,
+                                             eps=hp.eps, param_dtype="f32")
+            m_orc[k], mom_orc[k] = ref, mref
+            got = f64(master[k])
+            assert np.linalg.norm(got - ref) <= 2e-2 * np.linalg.norm(ref - first[k]), (step, k)
+            assert torch.equal(params[k], master[k].to(torch.bfloat16)), (step, k)
+            assert np.all(np.abs(f64(mom[k]) - mref) <= 1e-6 * (np.abs(mref) + np.abs(g)) + 1e-30)
+
