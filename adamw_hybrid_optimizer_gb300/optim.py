@@ -9,8 +9,9 @@ caller decides by the group's kind, and a Muon group must hold 2-D tensors only.
 
 Muon matrices of one group are bucketed by shape (muon_plan_buckets); each bucket owns one fp32
 (K, A, B) momentum stack, and all buckets of a group are updated by one muon_step_grouped call per
-step. AdamW state is one fp32 exp_avg / exp_avg_sq pair per tensor and the group's step count. All
-arithmetic runs in libmuon.
+step. AdamW state is one fp32 exp_avg / exp_avg_sq pair per tensor and the group's step count. With
+master_weights=True (bf16 parameters), each parameter also keeps an fp32 master copy ("master" in its
+state) that takes the update; the parameter holds it rounded to bf16. All arithmetic runs in libmuon.
 """
 from __future__ import annotations
 
@@ -22,19 +23,29 @@ from . import libmuon as L
 
 CLASSIC = (3.4445, -4.7750, 2.0315)
 
+# master_weights=True (bf16 parameters only): an fp32 master copy per parameter takes the update and the
+# parameter holds it rounded to bf16 ("Optimizers: AdamW, Muon and the distributed optimizer", section "The
+# optimizer's memory budget")
 MUON_DEFAULTS = dict(lr=0.02, momentum=0.95, weight_decay=0.01, nesterov=True, cautious_wd=False, scale_mode=0,
-                     ns_steps=5, ns_coefficients=None, eps=1e-7)
+                     ns_steps=5, ns_coefficients=None, eps=1e-7, master_weights=False)
 # is_adamw=False: Adam with L2 regularisation instead of decoupled decay ("dtensor-muon 0.1.0", "Key options")
-ADAMW_DEFAULTS = dict(lr=3e-4, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1, is_adamw=True)
+ADAMW_DEFAULTS = dict(lr=3e-4, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1, is_adamw=True, master_weights=False)
 
 
 class _Bucket:
-    def __init__(self, params: List[torch.Tensor], shape, device):
+    def __init__(self, params: List[torch.Tensor], shape, device, master_weights: bool = False):
         self.params = params
         self.K = len(params)
         self.A, self.B = shape
         self.momentum = torch.zeros((self.K, self.A, self.B), dtype=torch.float32, device=device)
         self.param_ptrs = L.pointer_array(params, device)
+        self.master = None
+        self.master_ptrs = None
+        if master_weights:
+            if any(p.dtype != torch.bfloat16 for p in params):
+                raise ValueError("master_weights needs bf16 parameters")
+            self.master = torch.stack([p.detach().float() for p in params])
+            self.master_ptrs = L.pointer_array([self.master[k] for k in range(self.K)], device)
         self.grad_ptrs = None
         self._grad_key = None
 
@@ -80,10 +91,12 @@ class HybridMuonAdamW:
                 for p, b in zip(group["params"], plan["bucket_id"]):
                     members[b].append(p)
                 for shape, ps in zip(plan["bucket_shapes"], members):
-                    bk = _Bucket(ps, shape, device)
+                    bk = _Bucket(ps, shape, device, group["master_weights"])
                     buckets.append(bk)
                     for k, p in enumerate(ps):
                         self.state[p] = {"momentum_buffer": bk.momentum[k]}
+                        if bk.master is not None:
+                            self.state[p]["master"] = bk.master[k]
                 shapes = (L.muon_bucket * len(buckets))(*[L.muon_bucket(None, None, None, bk.K, bk.A, bk.B, 0, 0)
                                                            for bk in buckets])
                 ws_bytes = max(ws_bytes, L.muon_workspace_bytes_grouped(shapes) if buckets else 0)
@@ -92,6 +105,10 @@ class HybridMuonAdamW:
                 for p in group["params"]:
                     self.state[p] = {"exp_avg": torch.zeros(p.shape, dtype=torch.float32, device=p.device),
                                      "exp_avg_sq": torch.zeros(p.shape, dtype=torch.float32, device=p.device)}
+                    if group["master_weights"]:
+                        if p.dtype != torch.bfloat16:
+                            raise ValueError("master_weights needs bf16 parameters")
+                        self.state[p]["master"] = p.detach().float().clone()
             self.param_groups.append(group)
             self._buckets.append(buckets)
         # zero-filled: the control block's error word must start at zero
@@ -115,7 +132,7 @@ class HybridMuonAdamW:
                         if L._dtype_code(p) != pdt or L._dtype_code(gr) != gdt or not p.is_contiguous() \
                                 or not gr.is_contiguous():
                             raise ValueError("a Muon bucket needs contiguous tensors of one dtype")
-                    specs.append((bk.param_ptrs, bk.grad_ptrs, bk.momentum, bk.K, bk.A, bk.B, pdt, gdt))
+                    specs.append((bk.param_ptrs, bk.grad_ptrs, bk.momentum, bk.K, bk.A, bk.B, pdt, gdt, bk.master_ptrs))
                 if specs:
                     L.muon_step_grouped(L.make_buckets(specs), hp, self._ws)
             else:
@@ -125,8 +142,13 @@ class HybridMuonAdamW:
                     if p.grad is None:
                         continue
                     st = self.state[p]
-                    L.adamw_step(p, p.grad, st["exp_avg"], st["exp_avg_sq"], group["lr"], b1, b2, group["eps"],
-                                 group["weight_decay"], group["step"], l2=not group["is_adamw"])
+                    if "master" in st:
+                        L.adamw_step_master(st["master"], p, p.grad, st["exp_avg"], st["exp_avg_sq"], group["lr"], b1,
+                                            b2, group["eps"], group["weight_decay"], group["step"],
+                                            l2=not group["is_adamw"])
+                    else:
+                        L.adamw_step(p, p.grad, st["exp_avg"], st["exp_avg_sq"], group["lr"], b1, b2, group["eps"],
+                                     group["weight_decay"], group["step"], l2=not group["is_adamw"])
 
     def zero_grad(self, set_to_none: bool = True):
         for group in self.param_groups:

@@ -128,3 +128,36 @@ def test_is_adamw_false_group_takes_adam_with_l2(L):
         dec, _, _ = oadamw.adamw_update(before[i], grads[i], 0, 0, 1, lr=a.lr, beta1=a.beta1, beta2=a.beta2,
                                         eps=a.eps, weight_decay=0.1, param_dtype="bf16")
         assert not np.array_equal(dec, ref)
+
+
+def test_master_weights_option(L):
+    """master_weights=True: fp32 masters take the update (the oracle's fp32-parameter rules), and every bf16
+    parameter equals its master rounded to bf16."""
+    from adamw_hybrid_optimizer_gb300 import HybridMuonAdamW
+    m = workloads.workload("gpt2s").muon_hp
+    a = workloads.workload("gpt2s").adamw_hp
+    hidden, other = _model(5)
+    before = [f64(p) for p in hidden + other]
+    opt = HybridMuonAdamW([
+        {"params": hidden, "kind": "muon", "lr": m.lr, "momentum": m.momentum, "weight_decay": m.weight_decay,
+         "master_weights": True},
+        {"params": other, "kind": "adamw", "lr": a.lr, "betas": (a.beta1, a.beta2), "eps": a.eps,
+         "weight_decay": a.weight_decay, "master_weights": True},
+    ])
+    _grads(hidden + other, 1, 5)
+    grads = [f64(p.grad) for p in hidden + other]
+    opt.step()
+    torch.cuda.synchronize()
+    for i, p in enumerate(hidden):
+        master = opt.state[p]["master"]
+        ref, _, _ = omuon.muon_update(before[i], grads[i], np.zeros_like(before[i]), lr=m.lr, momentum=m.momentum,
+                                      weight_decay=m.weight_decay, coeffs=m.coeffs, eps=m.eps, param_dtype="f32")
+        assert np.linalg.norm(f64(master) - ref) <= 2e-2 * np.linalg.norm(ref - before[i])
+        assert torch.equal(p, master.to(torch.bfloat16))
+    for j, p in enumerate(other):
+        i = len(hidden) + j
+        master = opt.state[p]["master"]
+        ref, _, _ = oadamw.adamw_update(before[i], grads[i], 0, 0, 1, lr=a.lr, beta1=a.beta1, beta2=a.beta2,
+                                        eps=a.eps, weight_decay=a.weight_decay, param_dtype="f32")
+        assert np.all(np.abs(f64(master) - ref) <= 1e-6 * (np.abs(before[i]) + a.lr))
+        assert torch.equal(p, master.to(torch.bfloat16))
