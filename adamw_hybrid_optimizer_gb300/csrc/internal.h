@@ -19,7 +19,8 @@ enum KernelKind : int32_t {
   KK_APPLY = 5,
   KK_FINAL = 6,
   KK_DEBUG_WAIT = 7,
-  KK_COUNT = 8
+  KK_NS_SMALL = 8,
+  KK_COUNT = 9
 };
 
 // Launch bookkeeping (libmuon.cu): counts launches and, while tracing, records an event pair.
@@ -122,6 +123,32 @@ muon_status launch_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *
                          uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
 muon_status launch_final(const Bf16Stack &h, const Bf16Stack &x, const float *scale, const FinalSpec &f,
                          uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
+
+// ------------------------------------------------------------------------------------------ small matrices
+
+// The whole Newton-Schulz chain of each matrix of a stack in one CTA (ns_small.cu), for wide iterates of
+// at most 128 x 256: from the wide U (bf16, with the per-matrix scale s) to the parameter update or the
+// dense output of the large path's final step.
+struct SmallNsArgs {
+  const __nv_bfloat16 *u;   // wide U of matrix k at u + k * mstride_u, rows of ldu elements
+  long long ldu, mstride_u;
+  const float *scale;       // s_k, or null
+  int K, m, n;              // matrices; wide rows and columns
+  int transposed;           // stored matrix is the transpose of the wide iterate
+  int orig_cols;            // columns of the stored matrix
+  int ns_steps;
+  float coeffs[3 * MUON_MAX_NS_STEPS];
+  void *const *params;      // device array of K pointers (update), or null (dense output)
+  float *const *master;     // fp32 master copies of bf16 params, or null
+  void *out_dense;          // contiguous (K, A, B) output when params is null
+  int out_dtype;            // muon_dtype of params / out_dense
+  int cautious;
+  float lr_wd, lr_scale;
+  uint32_t *err;
+  unsigned long long timeout_ns;
+};
+bool ns_small_fits(long long m, long long n);
+muon_status launch_ns_small(const SmallNsArgs &a, cudaStream_t s);
 
 // ------------------------------------------------------------------------------------------ elementwise
 

@@ -224,8 +224,36 @@ muon_status check_coeffs(int ns_steps, const float *coeffs) {
 
 // The Newton-Schulz chain on the wide iterate in x0 (unnormalised U; s_k in `scale`) of the stack whose
 // sections start at ws, ending in launch_final. Iteration t reads X from one iterate buffer and writes the other.
+// The fused one-CTA-per-matrix chain of a stack whose wide iterate fits ns_small (sections at ws).
+SmallNsArgs small_args(uint32_t *err, char *ws, const Layout &L, long long K, int ns_steps, const float *coeffs,
+                       const FinalSpec &fin) {
+  SmallNsArgs a{};
+  a.u = reinterpret_cast<const __nv_bfloat16 *>(ws + L.x0);
+  a.ldu = L.ldx;
+  a.mstride_u = L.m * L.ldx;
+  a.scale = reinterpret_cast<const float *>(ws + L.scale);
+  a.K = static_cast<int>(K);
+  a.m = static_cast<int>(L.m);
+  a.n = static_cast<int>(L.n);
+  a.transposed = fin.transposed;
+  a.orig_cols = fin.orig_cols;
+  a.ns_steps = ns_steps;
+  for (int i = 0; i < 3 * ns_steps; ++i) a.coeffs[i] = coeffs[i];
+  a.params = fin.params;
+  a.master = fin.master;
+  a.out_dense = fin.out_dense;
+  a.out_dtype = fin.dtype;
+  a.cautious = fin.cautious;
+  a.lr_wd = fin.lr_wd;
+  a.lr_scale = fin.lr_scale;
+  a.err = err;
+  a.timeout_ns = g_timeout_ns;
+  return a;
+}
+
 muon_status run_ns_chain(uint32_t *err, char *ws, const Layout &L, long long K, int ns_steps, const float *coeffs,
                          const FinalSpec &fin, cudaStream_t s) {
+  if (ns_small_fits(L.m, L.n)) return launch_ns_small(small_args(err, ws, L, K, ns_steps, coeffs, fin), s);
   const float *scale = reinterpret_cast<const float *>(ws + L.scale);
   __nv_bfloat16 *xb[2] = {reinterpret_cast<__nv_bfloat16 *>(ws + L.x0), reinterpret_cast<__nv_bfloat16 *>(ws + L.x1)};
   __nv_bfloat16 *G = reinterpret_cast<__nv_bfloat16 *>(ws + L.g);
@@ -364,12 +392,36 @@ muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hpar
                           hp->momentum, hp->nesterov != 0, hp->eps);
   }
   if ((st = launch_nesterov_norm(na.data(), n, s)) != MUON_OK) return st;
-  // the Newton-Schulz chain, each step kind of all buckets in one grouped launch
+  auto final_spec = [&](const muon_bucket &bk) {
+    const double scale = hp->scale_mode == 0
+                             ? 0.2 * std::sqrt(static_cast<double>(bk.A > bk.B ? bk.A : bk.B))
+                             : std::sqrt(std::max(1.0, static_cast<double>(bk.A) / static_cast<double>(bk.B)));
+    FinalSpec fin{};
+    fin.params = bk.params;
+    fin.master = bk.master;
+    fin.dtype = bk.pdt;
+    fin.transposed = bk.A > bk.B ? 1 : 0;
+    fin.orig_cols = static_cast<int>(bk.B);
+    fin.cautious = hp->cautious_wd ? 1 : 0;
+    fin.lr_wd = static_cast<float>(static_cast<double>(hp->lr) * hp->weight_decay);
+    fin.lr_scale = static_cast<float>(static_cast<double>(hp->lr) * scale);
+    return fin;
+  };
+  // small buckets: the whole chain in one fused launch each
+  std::vector<char> small(n, 0);
+  for (int i = 0; i < n; ++i) {
+    if (!ns_small_fits(L[i].m, L[i].n)) continue;
+    small[i] = 1;
+    const SmallNsArgs sa = small_args(err, w[i], L[i], buckets[i].K, hp->ns_steps, hp->coeffs, final_spec(buckets[i]));
+    if ((st = launch_ns_small(sa, s)) != MUON_OK) return st;
+  }
+  // the Newton-Schulz chain of the other buckets, each step kind of all of them in one grouped launch
   for (int t = 0; t < hp->ns_steps; ++t) {
     const float a = hp->coeffs[3 * t], b = hp->coeffs[3 * t + 1], c = hp->coeffs[3 * t + 2];
     GemmBatch gram(EPI_GRAM, err, to), poly(EPI_POLY, err, to);
     GemmBatch last(t + 1 < hp->ns_steps ? EPI_APPLY : EPI_FINAL, err, to);
     for (int i = 0; i < n; ++i) {
+      if (small[i]) continue;
       const Layout &Li = L[i];
       const float *sc = t == 0 ? reinterpret_cast<const float *>(w[i] + Li.scale) : nullptr;
       __nv_bfloat16 *xb[2] = {reinterpret_cast<__nv_bfloat16 *>(w[i] + Li.x0),
@@ -385,20 +437,7 @@ muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hpar
       if (t + 1 < hp->ns_steps) {
         st = last.add_apply(Hs, X, xb[(t + 1) & 1], sc);
       } else {
-        const muon_bucket &bk = buckets[i];
-        const double scale = hp->scale_mode == 0
-                                 ? 0.2 * std::sqrt(static_cast<double>(bk.A > bk.B ? bk.A : bk.B))
-                                 : std::sqrt(std::max(1.0, static_cast<double>(bk.A) / static_cast<double>(bk.B)));
-        FinalSpec fin{};
-        fin.params = bk.params;
-        fin.master = bk.master;
-        fin.dtype = bk.pdt;
-        fin.transposed = bk.A > bk.B ? 1 : 0;
-        fin.orig_cols = static_cast<int>(bk.B);
-        fin.cautious = hp->cautious_wd ? 1 : 0;
-        fin.lr_wd = static_cast<float>(static_cast<double>(hp->lr) * hp->weight_decay);
-        fin.lr_scale = static_cast<float>(static_cast<double>(hp->lr) * scale);
-        st = last.add_final(Hs, X, sc, fin);
+        st = last.add_final(Hs, X, sc, final_spec(buckets[i]));
       }
       if (st != MUON_OK) return st;
     }
@@ -663,6 +702,7 @@ const char *muon_kernel_name(int32_t kind) {
     case KK_APPLY: return "ns_apply";
     case KK_FINAL: return "ns_final";
     case KK_DEBUG_WAIT: return "debug_wait";
+    case KK_NS_SMALL: return "ns_small";
     default: return "unknown";
   }
 }

@@ -446,6 +446,51 @@ def _traffic_from_profiles(kernel):
     return v if isinstance(v, (int, float)) else None
 
 
+def run_small_sweep(args):
+    """Small stacks (wide iterates up to 128 x 256), 5 classic steps: the fused one-CTA-per-matrix chain
+    (ns_orthogonalize) against the same chain as separate tensor-core launches per step (the no-allocation
+    entry point runs those). One JSON line per shape (not the bench line)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from adamw_hybrid_optimizer_gb300 import libmuon as L
+    import workloads
+    peaks, peak_src = load_peaks()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    coeffs = [workloads.CLASSIC_QUINTIC] * 5
+    for (K, A, B) in [(4, 64, 128), (48, 128, 256), (256, 128, 256), (64, 96, 96)]:
+        g = torch.Generator(device=dev)
+        g.manual_seed(K * 100003 + A * 101 + B)
+        x = torch.randn((K, A, B), generator=g, device=dev).to(torch.bfloat16)
+        out = torch.empty_like(x)
+        ws = torch.zeros(L.muon_workspace_bytes(K, A, B), dtype=torch.uint8, device=dev)
+        times = {}
+        for name, call in (("fused", lambda: L.ns_orthogonalize(x, out, coeffs, 1e-7, ws)),
+                           ("separate", lambda: L.ns_orthogonalize_noalloc(x, out, coeffs, 1e-7))):
+            for _ in range(5):
+                call()
+            torch.cuda.synchronize()
+            reps = 200
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record()
+            for _ in range(reps):
+                call()
+            s1.record()
+            torch.cuda.synchronize()
+            times[name] = s0.elapsed_time(s1) / reps * 1e3
+        if L.muon_check(ws) != L.MUON_OK:
+            raise RuntimeError("device wait ran out in the small sweep")
+        m, n = min(A, B), max(A, B)
+        flops = 5 * K * (4.0 * m * m * n + 2.0 * m ** 3)
+        print(json.dumps({"sweep": "ns_small", "K": K, "A": A, "B": B, "us_fused": round(times["fused"], 2),
+                          "us_separate_launches": round(times["separate"], 2),
+                          "speedup": round(times["separate"] / times["fused"], 2),
+                          "tflops_nominal_fused": round(flops / (times["fused"] * 1e-6) / 1e12, 2),
+                          "peak": f"{peaks['bf16_tflops']} TFLOP/s {peak_src} burst"}), flush=True)
+    return 0
+
+
 def run_ns_sweep(args):
     """Newton-Schulz sweep: K=64 square bf16 stacks, 5 classic steps, one JSON line per size (not the bench line)."""
     import torch
@@ -511,9 +556,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ns-sweep", action="store_true", help="Newton-Schulz size sweep instead of the bench line")
     ap.add_argument("--sizes", default="", help="comma-separated n for --ns-sweep")
+    ap.add_argument("--small-sweep", action="store_true", help="fused small-matrix chain vs separate launches")
     args = ap.parse_args()
     if args.ns_sweep:
         return run_ns_sweep(args)
+    if args.small_sweep:
+        return run_small_sweep(args)
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":

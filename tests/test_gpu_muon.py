@@ -35,6 +35,12 @@ def L():
     (2, 40, 1, torch.float32, torch.float32),         # one column
     (2, 96, 96, torch.bfloat16, torch.float32),       # square: not transposed
     (3, 768, 3072, torch.bfloat16, torch.float32),
+    # the one-CTA fused chain takes wide iterates up to 128 x 256; just past that, the grouped GEMMs
+    (2, 128, 256, torch.bfloat16, torch.float32),
+    (2, 256, 128, torch.float32, torch.bfloat16),
+    (1, 16, 16, torch.float32, torch.float32),
+    (2, 129, 256, torch.bfloat16, torch.float32),
+    (2, 128, 257, torch.bfloat16, torch.float32),
 ])
 def test_ns_orthogonalize_matches_oracle(L, K, A, B, xdt, odt):
     g = torch.Generator().manual_seed(K * 1000 + A + B)
