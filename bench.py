@@ -446,6 +446,73 @@ def _traffic_from_profiles(kernel):
     return v if isinstance(v, (int, float)) else None
 
 
+def run_config_sweep(args):
+    """The optimizer step on the other configurations (tiny, aspect-ratio Polar Express, Llama-3-8B-shaped):
+    seeded device-side inputs, 2 warm-up steps, then the device time of a few steps per configuration. One
+    JSON line each (not the bench line)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from adamw_hybrid_optimizer_gb300 import libmuon as L
+    import workloads
+    peaks, peak_src = load_peaks()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    for name, steps in (("tiny", 50), ("aspect", 5), ("llama8b", 3)):
+        w = workloads.workload(name)
+        plan = L.muon_plan_buckets(workloads.shape_list(w))
+        dt = "f32" if w.muon_dtype == "f32" else "bf16"
+        code = L.MUON_F32 if dt == "f32" else L.MUON_BF16
+        specs, keep, nominal = [], [], 0.0
+        for b, ((A, B), K) in enumerate(zip(plan["bucket_shapes"], plan["bucket_K"])):
+            p = workloads.device_stack((K, A, B), "normal", w.param_std, 5000 + b, dt, dev)
+            g = workloads.device_stack((K, A, B), w.grad_dist, w.grad_std, 5100 + b, dt, dev)
+            mom = torch.zeros((K, A, B), dtype=torch.float32, device=dev)
+            keep += [p, g, mom]
+            specs.append((L.pointer_array([p[k] for k in range(K)], dev), L.pointer_array([g[k] for k in range(K)], dev),
+                          mom, K, A, B, code, code))
+            m, n = min(A, B), max(A, B)
+            nominal += w.muon_hp.ns_steps * K * (4.0 * m * m * n + 2.0 * m ** 3)
+        arr = L.make_buckets(specs)
+        ws = torch.zeros(L.muon_workspace_bytes_grouped(arr), dtype=torch.uint8, device=dev)
+        hp = L.make_muon_hparams(w.muon_hp.lr, w.muon_hp.momentum, w.muon_hp.weight_decay, w.muon_hp.nesterov,
+                                 w.muon_hp.cautious_wd, w.muon_hp.scale_mode, w.muon_hp.coeffs, w.muon_hp.eps)
+        n_adamw = sum(t.numel for t in w.adamw)
+        adt = torch.float32 if w.adamw_dtype == "f32" else torch.bfloat16
+        ap = torch.zeros(max(n_adamw, 1), dtype=adt, device=dev)
+        ag = workloads.device_stack((1, 1, max(n_adamw, 1)), "normal", w.grad_std, 5200, w.adamw_dtype, dev).view(-1)
+        am = torch.zeros(max(n_adamw, 1), dtype=torch.float32, device=dev)
+        av = torch.zeros(max(n_adamw, 1), dtype=torch.float32, device=dev)
+        a = w.adamw_hp
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        t_muon = t_adamw = 0.0
+        for it in range(2 + steps):
+            ev[0].record()
+            L.muon_step_grouped(arr, hp, ws)
+            ev[1].record()
+            if n_adamw > 0:
+                L.adamw_step(ap, ag, am, av, a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, it + 1)
+            ev[2].record()
+            torch.cuda.synchronize()
+            if it >= 2:
+                t_muon += ev[0].elapsed_time(ev[1]) / steps
+                t_adamw += ev[1].elapsed_time(ev[2]) / steps
+        if L.muon_check(ws) != L.MUON_OK:
+            raise RuntimeError(f"device wait ran out in the {name} configuration")
+        abytes = n_adamw * (28 if w.adamw_dtype == "f32" else 22)
+        t_adamw = max(t_adamw, 1e-9)
+        print(json.dumps({"config": name, "muon_matrices": sum(plan["bucket_K"]), "buckets": len(plan["bucket_K"]),
+                          "muon_ms": round(t_muon, 4), "ns_tflops_nominal": round(nominal / (t_muon * 1e-3) / 1e12, 1),
+                          "ns_frac_nominal": round(nominal / (t_muon * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                          "adamw_ms": round(t_adamw, 4), "adamw_elems": n_adamw,
+                          "adamw_gbs": round(abytes / (t_adamw * 1e-3) / 1e9, 1),
+                          "adamw_frac_hbm": round(abytes / (t_adamw * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                          "peaks": f"{peak_src}"}), flush=True)
+        del specs, keep, arr, ws, ap, ag, am, av
+        torch.cuda.empty_cache()
+    return 0
+
+
 def run_small_sweep(args):
     """Small stacks (wide iterates up to 128 x 256), 5 classic steps: the fused one-CTA-per-matrix chain
     (ns_orthogonalize) against the same chain as separate tensor-core launches per step (the no-allocation
@@ -557,11 +624,14 @@ def main():
     ap.add_argument("--ns-sweep", action="store_true", help="Newton-Schulz size sweep instead of the bench line")
     ap.add_argument("--sizes", default="", help="comma-separated n for --ns-sweep")
     ap.add_argument("--small-sweep", action="store_true", help="fused small-matrix chain vs separate launches")
+    ap.add_argument("--config-sweep", action="store_true", help="the step on the tiny, aspect and Llama-3-8B sets")
     args = ap.parse_args()
     if args.ns_sweep:
         return run_ns_sweep(args)
     if args.small_sweep:
         return run_small_sweep(args)
+    if args.config_sweep:
+        return run_config_sweep(args)
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":
