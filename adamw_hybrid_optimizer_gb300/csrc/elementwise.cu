@@ -205,13 +205,15 @@ __global__ void __launch_bounds__(256) counter_reset_kernel(unsigned *counters, 
 
 // ------------------------------------------------------------------------------------------ AdamW
 
+// Every rounding step is spelled out (explicit fmaf and round-to-nearest multiplies and divide), so the
+// compiler has no contraction left to choose and every kernel that calls this gives the same bits.
 __device__ __forceinline__ float adamw_elem(float &pf, float gf, float &mf, float &vf, const AdamwConst &c) {
   if (c.l2) gf = fmaf(c.l2_wd, pf, gf);
-  pf *= c.decay;
-  mf = fmaf(c.beta1, mf, c.one_minus_beta1 * gf);
-  vf = fmaf(c.beta2, vf, c.one_minus_beta2 * gf * gf);
-  const float denom = sqrtf(vf) * c.inv_sqrt_bc2 + c.eps;
-  pf = pf - c.step_size * (mf / denom);
+  pf = __fmul_rn(pf, c.decay);
+  mf = fmaf(c.beta1, mf, __fmul_rn(c.one_minus_beta1, gf));
+  vf = fmaf(c.beta2, vf, __fmul_rn(__fmul_rn(c.one_minus_beta2, gf), gf));
+  const float denom = fmaf(sqrtf(vf), c.inv_sqrt_bc2, c.eps);
+  pf = fmaf(-c.step_size, __fdiv_rn(mf, denom), pf);
   return pf;
 }
 
@@ -428,12 +430,96 @@ __global__ void __launch_bounds__(256) adamw_master_kernel(float *__restrict__ m
   }
 }
 
+// One warp's share of a grouped pass: elements [e0, e1) of tensor d, 8 per lane per step when the tensor is
+// vector-aligned (e0 is a multiple of the chunk size, so the alignment holds), then the scalar rest.
+template <typename PT, typename GT, bool MASTER>
+__device__ __forceinline__ void adamw_span(const AdamwTensorDesc &d, long long e0, long long e1, int lane) {
+  PT *p = static_cast<PT *>(d.p);
+  const GT *g = static_cast<const GT *>(d.g);
+  float *m = d.m, *v = d.v, *ms = d.master;
+  long long e = e0;
+  if (d.vec) {
+    const long long ev = e0 + ((e1 - e0) & ~7LL);
+#pragma unroll 1
+    for (long long o = e0 + 8 * lane; o < ev; o += 256) {
+      float pf[8], gf[8], mf[8], vf[8];
+      if constexpr (MASTER) load8(ms + o, pf);
+      else load8(p + o, pf);
+      load8(g + o, gf);
+      load8(m + o, mf);
+      load8(v + o, vf);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) adamw_elem(pf[k], gf[k], mf[k], vf[k], d.c);
+      if constexpr (MASTER) store8(ms + o, pf);
+      store8(p + o, pf);
+      store8(m + o, mf);
+      store8(v + o, vf);
+    }
+    e = ev;
+  }
+  for (long long i = e + lane; i < e1; i += 32) {
+    float pf = MASTER ? ms[i] : load1(p, i), mf = m[i], vf = v[i];
+    adamw_elem(pf, load1(g, i), mf, vf, d.c);
+    if constexpr (MASTER) ms[i] = pf;
+    store1(p, i, pf);
+    m[i] = mf;
+    v[i] = vf;
+  }
+}
+
+// Grouped AdamW: warps take chunks from the pass's counter until none is left (see AdamwGroup). The
+// arithmetic per element is adamw_elem, as in adamw_kernel, so both give the same bits.
+__global__ void __launch_bounds__(ADAMW_THREADS, 10) adamw_grouped_kernel(const __grid_constant__ AdamwGroup G) {
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  const int lane = threadIdx.x % 32;
+  for (;;) {
+    unsigned long long chunk = 0;
+    if (lane == 0) chunk = atomicAdd(G.next, 1ull);
+    chunk = __shfl_sync(0xffffffffu, chunk, 0);
+    if (chunk >= static_cast<unsigned long long>(G.total_chunks)) break;
+    const long long ch = static_cast<long long>(chunk);
+    int lo = 0, hi = G.ntensors - 1;   // the last tensor whose first chunk is <= ch
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) / 2;
+      if (G.t[mid].chunk_begin <= ch) lo = mid;
+      else hi = mid - 1;
+    }
+    const AdamwTensorDesc &d = G.t[lo];
+    const long long e0 = (ch - d.chunk_begin) * ADAMW_CHUNK;
+    const long long e1 = min(e0 + ADAMW_CHUNK, d.n);
+    if (d.master != nullptr) {
+      if (d.gdt == MUON_F32) adamw_span<__nv_bfloat16, float, true>(d, e0, e1, lane);
+      else adamw_span<__nv_bfloat16, __nv_bfloat16, true>(d, e0, e1, lane);
+    } else if (d.pdt == MUON_F32) {
+      if (d.gdt == MUON_F32) adamw_span<float, float, false>(d, e0, e1, lane);
+      else adamw_span<float, __nv_bfloat16, false>(d, e0, e1, lane);
+    } else {
+      if (d.gdt == MUON_F32) adamw_span<__nv_bfloat16, float, false>(d, e0, e1, lane);
+      else adamw_span<__nv_bfloat16, __nv_bfloat16, false>(d, e0, e1, lane);
+    }
+  }
+}
+
 long long adamw_blocks(long long work) {
   const long long sms = device_sm_count();
   long long blocks = (work + 255) / 256;
   const long long cap = sms * 8;  // 8 resident 256-thread blocks per SM, grid-stride beyond that
   if (blocks > cap) blocks = cap;
   return blocks < 1 ? 1 : blocks;
+}
+
+muon_status launch_adamw_grouped(const AdamwGroup &G, cudaStream_t s) {
+  if (G.ntensors < 1 || G.total_chunks < 1) return MUON_OK;
+  const long long sms = device_sm_count();
+  const long long warps = ADAMW_THREADS / 32;
+  const long long need = (G.total_chunks + warps - 1) / warps;   // blocks that can all find a chunk
+  const long long blocks = std::max(1LL, std::min(need, sms * 10));
+  launch_begin(KK_ADAMW, s);
+  const dim3 grid(static_cast<unsigned>(blocks)), block(ADAMW_THREADS);
+  const cudaError_t e = launch_pdl(adamw_grouped_kernel, grid, block, 0, s, G);
+  launch_end(s);
+  return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
 }
 
 muon_status launch_adamw_master(float *master, __nv_bfloat16 *p, const void *g, int gdt, float *m, float *v,

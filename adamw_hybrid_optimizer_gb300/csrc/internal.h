@@ -195,6 +195,36 @@ muon_status launch_adamw(void *p, int pdt, const void *g, int gdt, float *m, flo
 muon_status launch_adamw_master(float *master, __nv_bfloat16 *p, const void *g, int gdt, float *m, float *v,
                                 long long n, const AdamwConst &c, cudaStream_t s);
 
+// ------------------------------------------------------------------ grouped AdamW
+// One launch updates up to ADAMW_GROUP_MAX tensors. Their elements are cut into chunks of ADAMW_CHUNK
+// (the last chunk of a tensor may be short), numbered tensor after tensor; each warp takes the next
+// chunk from a counter in the launch's region until none is left, so every chunk is updated once
+// whatever the tensors' sizes.
+constexpr int ADAMW_GROUP_MAX = 96;
+constexpr long long ADAMW_CHUNK = 8192;
+constexpr size_t ADAMW_REGION_BYTES = 256;       // per launch: the chunk counter (8 B)
+constexpr int ADAMW_THREADS = 96;
+struct AdamwTensorDesc {
+  void *p;              // parameters (pdt), or bf16 when master is set
+  const void *g;        // gradients (gdt)
+  float *m, *v;         // moments
+  float *master;        // fp32 master weights taking the update, or null
+  long long n;
+  long long chunk_begin;   // first chunk of this tensor in the launch's numbering
+  int pdt, gdt;
+  int vec;              // all pointers 16-byte aligned: 8-element vector accesses
+  AdamwConst c;
+};
+struct AdamwGroup {
+  AdamwTensorDesc t[ADAMW_GROUP_MAX];
+  int ntensors;
+  long long total_chunks;
+  unsigned long long *next;   // the chunk counter (zero when the pass starts)
+};
+static_assert(sizeof(AdamwGroup) <= 16384, "kernel parameter block too large");
+// A grid of ADAMW_THREADS-thread blocks filling the GPU (10 blocks per SM at 64 registers).
+muon_status launch_adamw_grouped(const AdamwGroup &G, cudaStream_t s);
+
 muon_status launch_debug_wait(uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
 
 }  // namespace muon

@@ -353,8 +353,9 @@ size_t muon_workspace_bytes_grouped(const muon_bucket *buckets, int n) {
   return header_bytes(total_K) + total;
 }
 
-muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hparams *hp, void *ws, size_t ws_bytes,
-                              muon_stream_t stream) {
+// Every argument check of muon_step_grouped (the device check excepted).
+static muon_status check_grouped(const muon_bucket *buckets, int n, const muon_hparams *hp, void *ws,
+                                 size_t ws_bytes) {
   if (buckets == nullptr || hp == nullptr || ws == nullptr || n < 1 || n > 4096) return MUON_ERR_INVALID_ARG;
   muon_status st;
   for (int i = 0; i < n; ++i)
@@ -366,9 +367,13 @@ muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hpar
     return MUON_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MUON_ERR_ALIGNMENT;
   if (ws_bytes < muon_workspace_bytes_grouped(buckets, n)) return MUON_ERR_WORKSPACE;
-  if ((st = check_device()) != MUON_OK) return st;
+  return MUON_OK;
+}
 
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+// The launches of one grouped Muon step, on stream s (arguments already checked).
+static muon_status enqueue_grouped(const muon_bucket *buckets, int n, const muon_hparams *hp, void *ws,
+                                   cudaStream_t s) {
+  muon_status st;
   char *base = static_cast<char *>(ws);
   uint32_t *err = reinterpret_cast<uint32_t *>(base);
   const unsigned long long to = g_timeout_ns;
@@ -445,6 +450,13 @@ muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hpar
       return st;
   }
   return MUON_OK;
+}
+
+muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hparams *hp, void *ws, size_t ws_bytes,
+                              muon_stream_t stream) {
+  muon_status st;
+  if ((st = check_grouped(buckets, n, hp, ws, ws_bytes)) != MUON_OK || (st = check_device()) != MUON_OK) return st;
+  return enqueue_grouped(buckets, n, hp, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
 muon_status ns_orthogonalize(const void *x, muon_dtype xdt, void *out, muon_dtype odt, int64_t K, int64_t A,
@@ -526,6 +538,97 @@ muon_status adamw_step_master(float *master, void *param, const void *grad, muon
   if ((st = check_device()) != MUON_OK) return st;
   return launch_adamw_master(master, static_cast<__nv_bfloat16 *>(param), grad, gdt, exp_avg, exp_avg_sq, n, c,
                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------------------------------------ grouped AdamW
+
+static int64_t adamw_passes(int64_t n) { return (n + ADAMW_GROUP_MAX - 1) / ADAMW_GROUP_MAX; }
+
+// Checks every tensor and builds one launch argument block per pass of up to ADAMW_GROUP_MAX tensors, each
+// with its counter region in ws.
+static muon_status build_adamw_groups(const adamw_tensor *t, int64_t n, void *ws, size_t ws_bytes,
+                                      std::vector<AdamwGroup> &out) {
+  if (t == nullptr || ws == nullptr || n < 1 || n > (1 << 20)) return MUON_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MUON_ERR_ALIGNMENT;
+  if (ws_bytes < adamw_workspace_bytes_grouped(n)) return MUON_ERR_WORKSPACE;
+  auto aligned = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
+  out.assign(static_cast<size_t>(adamw_passes(n)), AdamwGroup{});
+  for (int64_t i = 0; i < n; ++i) {
+    const adamw_tensor &x = t[i];
+    if (x.param == nullptr || x.grad == nullptr || x.exp_avg == nullptr || x.exp_avg_sq == nullptr ||
+        x.hp == nullptr || x.n < 1)
+      return MUON_ERR_INVALID_ARG;
+    if (!valid_dtype(x.pdt) || !valid_dtype(x.gdt)) return MUON_ERR_DTYPE;
+    if (x.master != nullptr && x.pdt != MUON_BF16) return MUON_ERR_DTYPE;
+    AdamwGroup &G = out[static_cast<size_t>(i / ADAMW_GROUP_MAX)];
+    AdamwTensorDesc &d = G.t[G.ntensors];
+    muon_status st = adamw_constants(x.hp, &d.c);
+    if (st != MUON_OK) return st;
+    d.p = x.param;
+    d.g = x.grad;
+    d.m = x.exp_avg;
+    d.v = x.exp_avg_sq;
+    d.master = x.master;
+    d.n = x.n;
+    d.pdt = x.pdt;
+    d.gdt = x.gdt;
+    d.vec = aligned(x.param) && aligned(x.grad) && aligned(x.exp_avg) && aligned(x.exp_avg_sq) &&
+            (x.master == nullptr || aligned(x.master));
+    d.chunk_begin = G.total_chunks;
+    G.total_chunks += (x.n + ADAMW_CHUNK - 1) / ADAMW_CHUNK;
+    ++G.ntensors;
+  }
+  for (size_t k = 0; k < out.size(); ++k)
+    out[k].next = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + k * ADAMW_REGION_BYTES);
+  return MUON_OK;
+}
+
+size_t adamw_workspace_bytes_grouped(int64_t n) {
+  if (n < 1) return 0;
+  return static_cast<size_t>(adamw_passes(n)) * ADAMW_REGION_BYTES;
+}
+
+static muon_status reset_adamw_regions(void *ws, size_t passes, cudaStream_t s) {
+  return launch_counter_reset(static_cast<unsigned *>(ws),
+                              static_cast<long long>(passes * ADAMW_REGION_BYTES / sizeof(unsigned)), s);
+}
+
+muon_status adamw_step_grouped(const adamw_tensor *tensors, int64_t n, void *ws, size_t ws_bytes,
+                               muon_stream_t stream) {
+  std::vector<AdamwGroup> groups;
+  muon_status st = build_adamw_groups(tensors, n, ws, ws_bytes, groups);
+  if (st != MUON_OK || (st = check_device()) != MUON_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = reset_adamw_regions(ws, groups.size(), s)) != MUON_OK) return st;
+  for (const AdamwGroup &G : groups)
+    if ((st = launch_adamw_grouped(G, s)) != MUON_OK) return st;
+  return MUON_OK;
+}
+
+// ------------------------------------------------------------------------------------------ hybrid step
+
+muon_status hybrid_step(const muon_bucket *buckets, int nb, const muon_hparams *hp, void *ws, size_t ws_bytes,
+                        const adamw_tensor *tensors, int64_t nt, void *adamw_ws, size_t adamw_ws_bytes,
+                        muon_stream_t stream) {
+  if (nb < 0 || nt < 0 || (nb == 0 && nt == 0)) return MUON_ERR_INVALID_ARG;
+  muon_status st;
+  if (nb > 0 && (st = check_grouped(buckets, nb, hp, ws, ws_bytes)) != MUON_OK) return st;
+  std::vector<AdamwGroup> groups;
+  if (nt > 0 && (st = build_adamw_groups(tensors, nt, adamw_ws, adamw_ws_bytes, groups)) != MUON_OK) return st;
+  if (nb > 0 && nt > 0) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(ws), a1 = a0 + muon_workspace_bytes_grouped(buckets, nb);
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(adamw_ws), b1 = b0 + adamw_workspace_bytes_grouped(nt);
+    if (a0 < b1 && b0 < a1) return MUON_ERR_INVALID_ARG;
+  }
+  if ((st = check_device()) != MUON_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (nb > 0 && (st = enqueue_grouped(buckets, nb, hp, ws, s)) != MUON_OK) return st;
+  if (nt > 0) {
+    if ((st = reset_adamw_regions(adamw_ws, groups.size(), s)) != MUON_OK) return st;
+    for (const AdamwGroup &G : groups)
+      if ((st = launch_adamw_grouped(G, s)) != MUON_OK) return st;
+  }
+  return MUON_OK;
 }
 
 static muon_status check_step_stack(const void *p, int64_t K, int64_t m, int64_t n) {

@@ -51,6 +51,12 @@ class muon_bucket(ctypes.Structure):
                 ("gdt", ctypes.c_int), ("master", ctypes.c_void_p)]
 
 
+class adamw_tensor(ctypes.Structure):
+    _fields_ = [("param", ctypes.c_void_p), ("grad", ctypes.c_void_p), ("exp_avg", ctypes.c_void_p),
+                ("exp_avg_sq", ctypes.c_void_p), ("master", ctypes.c_void_p), ("n", ctypes.c_int64),
+                ("pdt", ctypes.c_int), ("gdt", ctypes.c_int), ("hp", ctypes.POINTER(adamw_hparams))]
+
+
 SIGNATURES = {
     "muon_workspace_bytes": (ctypes.c_size_t, [_c_int64, _c_int64, _c_int64]),
     "muon_step_batched": (ctypes.c_int, [_vp, ctypes.c_int, _vp, ctypes.c_int, _vp, _c_int64, _c_int64, _c_int64,
@@ -67,6 +73,11 @@ SIGNATURES = {
                                   ctypes.POINTER(adamw_hparams), _vp]),
     "adamw_step_master": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int, _vp, _vp, _c_int64,
                                          ctypes.POINTER(adamw_hparams), _vp]),
+    "adamw_workspace_bytes_grouped": (ctypes.c_size_t, [_c_int64]),
+    "adamw_step_grouped": (ctypes.c_int, [ctypes.POINTER(adamw_tensor), _c_int64, _vp, ctypes.c_size_t, _vp]),
+    "hybrid_step": (ctypes.c_int, [ctypes.POINTER(muon_bucket), ctypes.c_int, ctypes.POINTER(muon_hparams), _vp,
+                                   ctypes.c_size_t, ctypes.POINTER(adamw_tensor), _c_int64, _vp, ctypes.c_size_t,
+                                   _vp]),
     "ns_gram": (ctypes.c_int, [_vp, _vp, _c_int64, _c_int64, _c_int64, ctypes.c_float, _vp, ctypes.c_size_t, _vp]),
     "ns_poly": (ctypes.c_int, [_vp, _vp, _c_int64, _c_int64, ctypes.c_float, ctypes.c_float, ctypes.c_float, _vp,
                                ctypes.c_size_t, _vp]),
@@ -237,6 +248,52 @@ def adamw_step_master(master, param, grad, exp_avg, exp_avg_sq, lr, beta1, beta2
                                  exp_avg.data_ptr(), exp_avg_sq.data_ptr(), param.numel(), ctypes.byref(hp),
                                  _stream(stream))
     _check(st, "adamw_step_master")
+
+
+def make_adamw_hparams(lr, beta1, beta2, eps, weight_decay, step: int, l2: bool = False) -> adamw_hparams:
+    return adamw_hparams(lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=weight_decay, l2=int(bool(l2)),
+                         step=int(step))
+
+
+def make_adamw_tensors(specs):
+    """specs: sequence of (param, grad, exp_avg, exp_avg_sq, hp[, master]) with hp an adamw_hparams; returns a
+    ctypes adamw_tensor array that keeps the tensors and the hparams structs it points at alive."""
+    arr = (adamw_tensor * len(specs))()
+    keep = []
+    for i, spec in enumerate(specs):
+        p, g, m, v, hp = spec[:5]
+        ms = spec[5] if len(spec) > 5 else None
+        if ms is not None and (_dtype_code(p) != MUON_BF16 or _dtype_code(ms) != MUON_F32 or ms.numel() != p.numel()):
+            raise ValueError("make_adamw_tensors: a master copy needs bf16 params and an fp32 master of their size")
+        keep += [p, g, m, v, hp] + ([ms] if ms is not None else [])
+        arr[i] = adamw_tensor(p.data_ptr(), g.data_ptr(), m.data_ptr(), v.data_ptr(),
+                              ms.data_ptr() if ms is not None else None, p.numel(), _dtype_code(p), _dtype_code(g),
+                              ctypes.pointer(hp))
+    arr.tensors = keep
+    return arr
+
+
+def adamw_workspace_bytes_grouped(n: int) -> int:
+    return int(lib().adamw_workspace_bytes_grouped(int(n)))
+
+
+def adamw_step_grouped(tensors, ws, stream=None):
+    """tensors: a ctypes adamw_tensor array (see make_adamw_tensors)."""
+    _check(lib().adamw_step_grouped(tensors, len(tensors), ws.data_ptr(), ws.numel() * ws.element_size(),
+                                    _stream(stream)), "adamw_step_grouped")
+
+
+def hybrid_step(buckets, hp, ws, tensors, adamw_ws, stream=None):
+    """buckets (make_buckets) with hp / ws as for muon_step_grouped, tensors (make_adamw_tensors) with adamw_ws as
+    for adamw_step_grouped; either list may be empty."""
+    nb = len(buckets) if buckets is not None else 0
+    nt = len(tensors) if tensors is not None else 0
+    _check(lib().hybrid_step(buckets if nb else None, nb, ctypes.byref(hp) if hp is not None else None,
+                             ws.data_ptr() if ws is not None else None,
+                             ws.numel() * ws.element_size() if ws is not None else 0, tensors if nt else None, nt,
+                             adamw_ws.data_ptr() if adamw_ws is not None else None,
+                             adamw_ws.numel() * adamw_ws.element_size() if adamw_ws is not None else 0,
+                             _stream(stream)), "hybrid_step")
 
 
 def ns_gram(x, g, alpha: float, ws, stream=None):

@@ -11,7 +11,8 @@ Muon matrices of one group are bucketed by shape (muon_plan_buckets); each bucke
 (K, A, B) momentum stack, and all buckets of a group are updated by one muon_step_grouped call per
 step. AdamW state is one fp32 exp_avg / exp_avg_sq pair per tensor and the group's step count. With
 master_weights=True (bf16 parameters), each parameter also keeps an fp32 master copy ("master" in its
-state) that takes the update; the parameter holds it rounded to bf16. All arithmetic runs in libmuon.
+state) that takes the update; the parameter holds it rounded to bf16. All arithmetic runs in libmuon: the
+AdamW tensors of all groups in one grouped pass, issued with the last Muon group by hybrid_step.
 """
 from __future__ import annotations
 
@@ -113,9 +114,14 @@ class HybridMuonAdamW:
             self._buckets.append(buckets)
         # zero-filled: the control block's error word must start at zero
         self._ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=device) if device is not None else None
+        self._adamw_ws = None   # the grouped AdamW pass's counters, sized on first use
 
     @torch.no_grad()
     def step(self):
+        """One step of every group. The AdamW tensors of all groups go through one grouped pass, issued in one
+        call (hybrid_step) with the last Muon group."""
+        muon_calls = []
+        adamw_specs = []
         for group, buckets in zip(self.param_groups, self._buckets):
             if group["kind"] == "muon":
                 hp = L.make_muon_hparams(group["lr"], group["momentum"], group["weight_decay"], group["nesterov"],
@@ -134,21 +140,35 @@ class HybridMuonAdamW:
                             raise ValueError("a Muon bucket needs contiguous tensors of one dtype")
                     specs.append((bk.param_ptrs, bk.grad_ptrs, bk.momentum, bk.K, bk.A, bk.B, pdt, gdt, bk.master_ptrs))
                 if specs:
-                    L.muon_step_grouped(L.make_buckets(specs), hp, self._ws)
+                    muon_calls.append((L.make_buckets(specs), hp))
             else:
                 group["step"] += 1
                 b1, b2 = group["betas"]
+                hp = L.make_adamw_hparams(group["lr"], b1, b2, group["eps"], group["weight_decay"], group["step"],
+                                          l2=not group["is_adamw"])
                 for p in group["params"]:
                     if p.grad is None:
                         continue
+                    if not p.is_contiguous() or not p.grad.is_contiguous():
+                        raise ValueError("AdamW needs contiguous parameters and gradients")
                     st = self.state[p]
-                    if "master" in st:
-                        L.adamw_step_master(st["master"], p, p.grad, st["exp_avg"], st["exp_avg_sq"], group["lr"], b1,
-                                            b2, group["eps"], group["weight_decay"], group["step"],
-                                            l2=not group["is_adamw"])
-                    else:
-                        L.adamw_step(p, p.grad, st["exp_avg"], st["exp_avg_sq"], group["lr"], b1, b2, group["eps"],
-                                     group["weight_decay"], group["step"], l2=not group["is_adamw"])
+                    adamw_specs.append((p, p.grad, st["exp_avg"], st["exp_avg_sq"], hp)
+                                       + ((st["master"],) if "master" in st else ()))
+        if not adamw_specs:
+            for bk, hp in muon_calls:
+                L.muon_step_grouped(bk, hp, self._ws)
+            return
+        for bk, hp in muon_calls[:-1]:
+            L.muon_step_grouped(bk, hp, self._ws)
+        tensors = L.make_adamw_tensors(adamw_specs)
+        need = L.adamw_workspace_bytes_grouped(len(adamw_specs))
+        if self._adamw_ws is None or self._adamw_ws.numel() < need:
+            self._adamw_ws = torch.zeros(need, dtype=torch.uint8, device=self._ws.device)
+        if muon_calls:
+            bk, hp = muon_calls[-1]
+            L.hybrid_step(bk, hp, self._ws, tensors, self._adamw_ws)
+        else:
+            L.adamw_step_grouped(tensors, self._adamw_ws)
 
     def zero_grad(self, set_to_none: bool = True):
         for group in self.param_groups:

@@ -91,16 +91,21 @@ class Workload:
                     off += k
             self.adamw.append(dict(wd=wd, p=p, g=g, m=torch.zeros(n, dtype=torch.float32, device=device),
                                    v=torch.zeros(n, dtype=torch.float32, device=device)))
+        a = w.adamw_hp
+        self.adamw_hps = [L.make_adamw_hparams(a.lr, a.beta1, a.beta2, a.eps, b["wd"], 1) for b in self.adamw]
+        self.adamw_tensors = L.make_adamw_tensors([(b["p"], b["g"], b["m"], b["v"], h)
+                                                   for b, h in zip(self.adamw, self.adamw_hps)])
+        self.adamw_ws = torch.zeros(L.adamw_workspace_bytes_grouped(len(self.adamw)), dtype=torch.uint8,
+                                    device=device)
         self.t = 0
 
     def step(self, stream=None):
+        """One whole optimizer step through hybrid_step: the grouped Muon step, then the grouped AdamW pass."""
         L = self.L
         self.t += 1
-        L.muon_step_grouped(self.bucket_array, self.hp, self.ws, stream)
-        a = self.w.adamw_hp
-        for buf in self.adamw:
-            L.adamw_step(buf["p"], buf["g"], buf["m"], buf["v"], a.lr, a.beta1, a.beta2, a.eps, buf["wd"], self.t,
-                         stream)
+        for h in self.adamw_hps:
+            h.step = self.t
+        L.hybrid_step(self.bucket_array, self.hp, self.ws, self.adamw_tensors, self.adamw_ws, stream)
 
     # algorithmic work of one step, per kernel kind
     def work(self):

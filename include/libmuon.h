@@ -160,6 +160,48 @@ muon_status adamw_step(void *param, muon_dtype pdt, const void *grad, muon_dtype
 muon_status adamw_step_master(float *master, void *param, const void *grad, muon_dtype gdt, float *exp_avg,
                               float *exp_avg_sq, int64_t n, const adamw_hparams *hp, muon_stream_t stream);
 
+/* One tensor of a grouped AdamW call: the arguments of adamw_step (master NULL) or of adamw_step_master
+ * (master set; pdt must then be MUON_BF16), with its own hyperparameters, so that tensors of several
+ * parameter groups (say, with and without weight decay: [P2] "AdamW: decoupled weight decay") share
+ * one pass. */
+typedef struct {
+  void *param;               /* device, n elements of pdt */
+  const void *grad;          /* device, n elements of gdt */
+  float *exp_avg;            /* device fp32, n elements */
+  float *exp_avg_sq;         /* device fp32, n elements */
+  float *master;             /* NULL, or device fp32, n elements: the master weights taking the update */
+  int64_t n;                 /* >= 1 */
+  muon_dtype pdt, gdt;
+  const adamw_hparams *hp;   /* HOST struct, read during the call only; tensors may share one */
+} adamw_tensor;
+
+/* Workspace bytes for adamw_step_grouped and for hybrid_step's adamw_ws: 256 for every 96 tensors
+ * (one chunk counter per launch). 0 if n < 1. */
+size_t adamw_workspace_bytes_grouped(int64_t n);
+
+/* AdamW on n tensors in one launch per 96 tensors. Each tensor gets exactly the arithmetic of adamw_step
+ * (or adamw_step_master), so the results are bit-identical to n separate calls; tensors must not overlap.
+ *   tensors  HOST array of n descriptors (1 <= n <= 2^20).
+ *   ws       device workspace of ws_bytes >= adamw_workspace_bytes_grouped(n), 256-byte aligned; needs no
+ *            initialisation (the call zeroes its counters in stream order). Calls that share ws must be
+ *            on one stream.
+ * Errors: each tensor's checks as for adamw_step / adamw_step_master, all run before any launch;
+ * MUON_ERR_WORKSPACE if ws_bytes is too small, MUON_ERR_ALIGNMENT if ws is not 256-byte aligned. */
+muon_status adamw_step_grouped(const adamw_tensor *tensors, int64_t n, void *ws, size_t ws_bytes,
+                               muon_stream_t stream);
+
+/* The whole hybrid optimizer step in one call ([P1] "Usage Examples": one optimizer whose step updates the
+ * hidden matrices with Muon and every other parameter with AdamW): muon_step_grouped on the buckets, then
+ * adamw_step_grouped on the AdamW tensors, on the caller's stream; the results are those of the two calls.
+ *   buckets, nb, hp, ws, ws_bytes   as for muon_step_grouped (nb may be 0: AdamW only).
+ *   tensors, nt, adamw_ws, adamw_ws_bytes   as for adamw_step_grouped (nt may be 0: Muon only); adamw_ws
+ *            may not overlap ws.
+ * Errors: every check of both calls runs before anything is launched; MUON_ERR_INVALID_ARG if nb and nt
+ * are both 0 or if the two workspaces overlap. */
+muon_status hybrid_step(const muon_bucket *buckets, int nb, const muon_hparams *hp, void *ws, size_t ws_bytes,
+                        const adamw_tensor *tensors, int64_t nt, void *adamw_ws, size_t adamw_ws_bytes,
+                        muon_stream_t stream);
+
 /* ns_orthogonalize without any device allocation. The pages have no counterpart to this call.
  * For callers that cannot allocate device memory and so cannot provide a workspace: code running
  * inside a device-memory allocator's own hooks (allocating there would re-enter the allocator),

@@ -191,3 +191,74 @@ def test_grouped_entry_point_checks():
     hp2 = L.adamw_hparams(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, step=1)
     assert lib.adamw_step_master(None, FAKE, FAKE, 0, FAKE, FAKE, 8, ctypes.byref(hp2), None) == L.MUON_ERR_INVALID_ARG
     assert lib.adamw_step_master(FAKE, FAKE, FAKE, 5, FAKE, FAKE, 8, ctypes.byref(hp2), None) == L.MUON_ERR_DTYPE
+
+
+def test_adamw_tensor_struct_layout():
+    # five pointers, the int64 count at 40, the two dtype enums, then the hparams pointer at 56
+    assert ctypes.sizeof(L.adamw_tensor) == 64
+    assert L.adamw_tensor.n.offset == 40 and L.adamw_tensor.pdt.offset == 48 and L.adamw_tensor.hp.offset == 56
+
+
+def _adamw_t(param=FAKE, grad=FAKE, m=FAKE, v=FAKE, master=None, n=8192, pdt=L.MUON_BF16, gdt=L.MUON_BF16, hp=None):
+    if hp is None:
+        hp = L.make_adamw_hparams(1e-3, 0.9, 0.95, 1e-8, 0.1, 1)
+    t = L.adamw_tensor(param, grad, m, v, master, n, pdt, gdt, ctypes.pointer(hp) if hp is not False else None)
+    t._hp = hp
+    return t
+
+
+def test_grouped_adamw_entry_point_checks():
+    lib = L.lib()
+    assert L.adamw_workspace_bytes_grouped(0) == 0
+    assert L.adamw_workspace_bytes_grouped(1) == 256
+    assert L.adamw_workspace_bytes_grouped(96) == 256 and L.adamw_workspace_bytes_grouped(97) == 512
+
+    def st(*ts, ws=FAKE, nb=256, n=None):
+        arr = (L.adamw_tensor * max(len(ts), 1))(*ts)
+        return lib.adamw_step_grouped(arr, len(ts) if n is None else n, ws, nb, None)
+
+    good = _adamw_t()
+    assert st(good, n=0) == L.MUON_ERR_INVALID_ARG
+    assert st(good, ws=None) == L.MUON_ERR_INVALID_ARG
+    assert st(good, ws=FAKE + 16) == L.MUON_ERR_ALIGNMENT
+    assert st(good, nb=255) == L.MUON_ERR_WORKSPACE
+    assert st(*([good] * 97), nb=256) == L.MUON_ERR_WORKSPACE
+    assert st(good, _adamw_t(param=None)) == L.MUON_ERR_INVALID_ARG
+    assert st(good, _adamw_t(v=None)) == L.MUON_ERR_INVALID_ARG
+    assert st(good, _adamw_t(n=0)) == L.MUON_ERR_INVALID_ARG
+    assert st(good, _adamw_t(hp=False)) == L.MUON_ERR_INVALID_ARG
+    assert st(good, _adamw_t(gdt=4)) == L.MUON_ERR_DTYPE
+    # a master copy goes with bf16 parameters only
+    assert st(good, _adamw_t(master=FAKE, pdt=L.MUON_F32)) == L.MUON_ERR_DTYPE
+    assert st(good, _adamw_t(hp=L.make_adamw_hparams(1e-3, 0.9, 0.95, 1e-8, 0.1, 0))) == L.MUON_ERR_INVALID_ARG
+    assert st(good, _adamw_t(hp=L.make_adamw_hparams(1e-3, 0.9, 1.0, 1e-8, 0.1, 1))) == L.MUON_ERR_INVALID_ARG
+
+
+def test_hybrid_step_entry_point_checks():
+    lib = L.lib()
+    hp = L.make_muon_hparams(0.02, 0.95, 0.01)
+    b = (L.muon_bucket * 1)(L.muon_bucket(FAKE, FAKE, FAKE, 4, 64, 128, 0, 0))
+    need = L.muon_workspace_bytes_grouped(b)
+    ts = (L.adamw_tensor * 1)(_adamw_t())
+    aws = 1 << 30   # far from the Muon workspace at FAKE
+
+    def st(nb=1, nt=1, ws=FAKE, wsb=need, a=aws, ab=256, bk=b, t=ts):
+        return lib.hybrid_step(bk, nb, ctypes.byref(hp), ws, wsb, t, nt, a, ab, None)
+
+    assert st(nb=0, nt=0) == L.MUON_ERR_INVALID_ARG
+    assert st(nb=-1) == L.MUON_ERR_INVALID_ARG
+    assert st(wsb=need - 1) == L.MUON_ERR_WORKSPACE
+    assert st(ab=100) == L.MUON_ERR_WORKSPACE
+    assert st(nb=0, ab=100) == L.MUON_ERR_WORKSPACE
+    assert st(nt=0, wsb=need - 1) == L.MUON_ERR_WORKSPACE
+    assert st(a=aws + 8) == L.MUON_ERR_ALIGNMENT
+    # the AdamW counters may not lie inside the Muon workspace
+    assert st(a=FAKE + 1024) == L.MUON_ERR_INVALID_ARG
+    bad = (L.adamw_tensor * 1)(_adamw_t(grad=None))
+    assert st(t=bad) == L.MUON_ERR_INVALID_ARG
+    bad_b = (L.muon_bucket * 1)(L.muon_bucket(FAKE, FAKE, FAKE, 4, 64, 0, 0, 0))
+    assert st(bk=bad_b) == L.MUON_ERR_INVALID_ARG
+    # with every argument valid, the only thing left is the device (none in a CPU-only run)
+    import torch
+    if not torch.cuda.is_available():
+        assert st() in (L.MUON_ERR_CUDA, L.MUON_ERR_UNSUPPORTED_DEVICE)
