@@ -486,8 +486,8 @@ __global__ void __launch_bounds__(ADAMW_THREADS, 10) adamw_grouped_kernel(const 
       else hi = mid - 1;
     }
     const AdamwTensorDesc &d = G.t[lo];
-    const long long e0 = (ch - d.chunk_begin) * ADAMW_CHUNK;
-    const long long e1 = min(e0 + ADAMW_CHUNK, d.n);
+    const long long e0 = (ch - d.chunk_begin) * G.chunk;
+    const long long e1 = min(e0 + G.chunk, d.n);
     if (d.master != nullptr) {
       if (d.gdt == MUON_F32) adamw_span<__nv_bfloat16, float, true>(d, e0, e1, lane);
       else adamw_span<__nv_bfloat16, __nv_bfloat16, true>(d, e0, e1, lane);

@@ -92,9 +92,22 @@ struct FinalSpec {
 
 // Collects the problems of one step kind (all grams, all polys, ...) of several stacks and launches
 // them as few grouped kernels (up to GEMM_MAX_PROBLEMS problems per launch), deepest contraction first.
+// POLY, the one step kind compiled in several pipeline shapes (mainloop stages + epilogue ring slots):
+// shape 0 = 4 + 5, 1 = 5 + 3, 2 = 6 + 2. Without a measured choice, contractions up to 2048 take shape 0 and
+// deeper ones shape 2. Every shape computes each tile the same way, so the choice changes only the time.
+constexpr int POLY_SHAPES = 3;
+// The autotune table (process-wide): the measured shape for POLY launches whose deepest contraction is
+// k_iters 64-deep steps, or -1; and a forced shape for every launch (-1: none), for tests and sweeps.
+int poly_shape_lookup(int k_iters);
+void poly_shape_record(int k_iters, int shape);
+void poly_shape_clear();
+int poly_shape_forced();
+
 class GemmBatch {
  public:
   GemmBatch(int epi, uint32_t *err, unsigned long long timeout_ns) : epi_(epi), err_(err), timeout_ns_(timeout_ns) {}
+  // POLY only: launch with this pipeline shape whatever the table or the rule says (-1: no override)
+  void force_shape(int shape) { force_ = shape; }
   muon_status add_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long ldg, long long mstride_g, float alpha,
                        const float *scale);
   muon_status add_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float a, float b,
@@ -111,6 +124,7 @@ class GemmBatch {
   unsigned long long timeout_ns_;
   Item *items_ = nullptr;
   int n_ = 0, cap_ = 0;
+  int force_ = -1;
   muon_status push(const Item &it);
 };
 
@@ -196,12 +210,13 @@ muon_status launch_adamw_master(float *master, __nv_bfloat16 *p, const void *g, 
                                 long long n, const AdamwConst &c, cudaStream_t s);
 
 // ------------------------------------------------------------------ grouped AdamW
-// One launch updates up to ADAMW_GROUP_MAX tensors. Their elements are cut into chunks of ADAMW_CHUNK
+// One launch updates up to ADAMW_GROUP_MAX tensors. Their elements are cut into chunks of `chunk` elements
 // (the last chunk of a tensor may be short), numbered tensor after tensor; each warp takes the next
 // chunk from a counter in the launch's region until none is left, so every chunk is updated once
-// whatever the tensors' sizes.
+// whatever the tensors' sizes. The chunk is ADAMW_CHUNK_MAX elements, or smaller (a multiple of 256, at
+// least 256) when the launch has too few elements to give every warp of a full grid one chunk.
 constexpr int ADAMW_GROUP_MAX = 96;
-constexpr long long ADAMW_CHUNK = 8192;
+constexpr long long ADAMW_CHUNK_MAX = 8192;
 constexpr size_t ADAMW_REGION_BYTES = 256;       // per launch: the chunk counter (8 B)
 constexpr int ADAMW_THREADS = 96;
 struct AdamwTensorDesc {
@@ -218,6 +233,7 @@ struct AdamwTensorDesc {
 struct AdamwGroup {
   AdamwTensorDesc t[ADAMW_GROUP_MAX];
   int ntensors;
+  long long chunk;            // elements per chunk: a multiple of 256
   long long total_chunks;
   unsigned long long *next;   // the chunk counter (zero when the pass starts)
 };

@@ -107,6 +107,32 @@ void launch_end(cudaStream_t s) {
 
 muon_status device_check() { return check_device(); }
 
+// ------------------------------------------------------------------------------------------ autotune table
+
+namespace {
+std::mutex g_tune_mu;
+std::map<int, int> g_poly_shape;   // deepest contraction (64-deep steps) of a POLY launch -> measured shape
+int g_poly_forced = -1;
+}  // namespace
+
+int poly_shape_lookup(int k_iters) {
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  auto it = g_poly_shape.find(k_iters);
+  return it == g_poly_shape.end() ? -1 : it->second;
+}
+void poly_shape_record(int k_iters, int shape) {
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  g_poly_shape[k_iters] = shape;
+}
+void poly_shape_clear() {
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  g_poly_shape.clear();
+}
+int poly_shape_forced() {
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  return g_poly_forced;
+}
+
 unsigned long long wait_timeout_ns() { return g_timeout_ns; }
 
 namespace {
@@ -540,6 +566,97 @@ muon_status adamw_step_master(float *master, void *param, const void *grad, muon
                              reinterpret_cast<cudaStream_t>(stream));
 }
 
+// ------------------------------------------------------------------------------------------ autotune
+
+muon_status muon_autotune(const muon_bucket *buckets, int n, void *ws, size_t ws_bytes, muon_stream_t stream) {
+  if (buckets == nullptr || ws == nullptr || n < 1 || n > 4096) return MUON_ERR_INVALID_ARG;
+  muon_status st;
+  for (int i = 0; i < n; ++i)
+    if ((st = check_bucket(buckets[i])) != MUON_OK) return st;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MUON_ERR_ALIGNMENT;
+  if (ws_bytes < muon_workspace_bytes_grouped(buckets, n)) return MUON_ERR_WORKSPACE;
+  if ((st = check_device()) != MUON_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char *base = static_cast<char *>(ws);
+  uint32_t *err = reinterpret_cast<uint32_t *>(base);
+  long long total_K = 0;
+  for (int i = 0; i < n; ++i) total_K += buckets[i].K;
+  // the POLY launch of the grouped step: every bucket that does not take the fused small-matrix chain,
+  // reading its G section and writing its H section (the values do not matter for the time)
+  std::vector<Layout> L(n);
+  std::vector<char *> w(n);
+  size_t off = header_bytes(total_K);
+  int max_k = 0;
+  bool any = false;
+  for (int i = 0; i < n; ++i) {
+    L[i] = layout(buckets[i].K, buckets[i].A, buckets[i].B);
+    w[i] = base + off;
+    off += L[i].total;
+    if (ns_small_fits(L[i].m, L[i].n)) continue;
+    any = true;
+    max_k = std::max(max_k, static_cast<int>((L[i].m + 63) / 64));
+  }
+  if (!any) return MUON_OK;
+  auto launch_poly_batch = [&](int shape) -> muon_status {
+    GemmBatch poly(EPI_POLY, err, g_timeout_ns);
+    poly.force_shape(shape);
+    for (int i = 0; i < n; ++i) {
+      if (ns_small_fits(L[i].m, L[i].n)) continue;
+      const long long K = buckets[i].K, msg = L[i].m * L[i].ldg;
+      Bf16Stack Gs{w[i] + L[i].g, L[i].m, L[i].m, L[i].ldg, msg, K};
+      muon_status r = poly.add_poly(Gs, reinterpret_cast<__nv_bfloat16 *>(w[i] + L[i].h), L[i].ldg, msg, 3.4445f,
+                                    -4.7750f, 2.0315f);
+      if (r != MUON_OK) return r;
+    }
+    return poly.launch(s);
+  };
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+    if (e0) cudaEventDestroy(e0);
+    return MUON_ERR_CUDA;
+  }
+  constexpr int REPS = 5;
+  int best = -1;
+  float best_ms = 0.f;
+  st = MUON_OK;
+  for (int shape = 0; shape < POLY_SHAPES && st == MUON_OK; ++shape) {
+    float t[REPS];
+    st = launch_poly_batch(shape);   // warm-up (first launch of this shape sets its shared-memory attribute)
+    for (int r = 0; r < REPS && st == MUON_OK; ++r) {
+      if (cudaEventRecord(e0, s) != cudaSuccess) st = MUON_ERR_CUDA;
+      if (st == MUON_OK) st = launch_poly_batch(shape);
+      if (st == MUON_OK && (cudaEventRecord(e1, s) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+                            cudaEventElapsedTime(&t[r], e0, e1) != cudaSuccess))
+        st = MUON_ERR_CUDA;
+    }
+    if (st != MUON_OK) break;
+    std::sort(t, t + REPS);
+    if (best < 0 || t[REPS / 2] < best_ms) {
+      best = shape;
+      best_ms = t[REPS / 2];
+    }
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (st != MUON_OK) return st;
+  poly_shape_record(max_k, best);
+  return MUON_OK;
+}
+
+int32_t muon_autotune_poly_shape(int64_t contraction) {
+  if (contraction < 1 || contraction > (1 << 20)) return -1;
+  return poly_shape_lookup(static_cast<int>((contraction + 63) / 64));
+}
+
+void muon_autotune_reset(void) { poly_shape_clear(); }
+
+muon_status muon_debug_poly_shape(int32_t shape) {
+  if (shape < -1 || shape >= POLY_SHAPES) return MUON_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  g_poly_forced = shape;
+  return MUON_OK;
+}
+
 // ------------------------------------------------------------------------------------------ grouped AdamW
 
 static int64_t adamw_passes(int64_t n) { return (n + ADAMW_GROUP_MAX - 1) / ADAMW_GROUP_MAX; }
@@ -574,13 +691,28 @@ static muon_status build_adamw_groups(const adamw_tensor *t, int64_t n, void *ws
     d.gdt = x.gdt;
     d.vec = aligned(x.param) && aligned(x.grad) && aligned(x.exp_avg) && aligned(x.exp_avg_sq) &&
             (x.master == nullptr || aligned(x.master));
-    d.chunk_begin = G.total_chunks;
-    G.total_chunks += (x.n + ADAMW_CHUNK - 1) / ADAMW_CHUNK;
     ++G.ntensors;
   }
   for (size_t k = 0; k < out.size(); ++k)
     out[k].next = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + k * ADAMW_REGION_BYTES);
   return MUON_OK;
+}
+
+// Chunk size and numbering per launch (after the device check, which gives the SM count): every warp of a
+// full grid (10 blocks of 3 warps per SM) gets a chunk of at least 256 elements, up to ADAMW_CHUNK_MAX.
+static void number_adamw_chunks(std::vector<AdamwGroup> &groups) {
+  const long long warps = static_cast<long long>(device_sm_count()) * 10 * (ADAMW_THREADS / 32);
+  for (AdamwGroup &G : groups) {
+    long long elems = 0;
+    for (int k = 0; k < G.ntensors; ++k) elems += G.t[k].n;
+    long long c = (elems / std::max(1LL, warps) + 255) / 256 * 256;
+    G.chunk = std::min(ADAMW_CHUNK_MAX, std::max(256LL, c));
+    G.total_chunks = 0;
+    for (int k = 0; k < G.ntensors; ++k) {
+      G.t[k].chunk_begin = G.total_chunks;
+      G.total_chunks += (G.t[k].n + G.chunk - 1) / G.chunk;
+    }
+  }
 }
 
 size_t adamw_workspace_bytes_grouped(int64_t n) {
@@ -598,6 +730,7 @@ muon_status adamw_step_grouped(const adamw_tensor *tensors, int64_t n, void *ws,
   std::vector<AdamwGroup> groups;
   muon_status st = build_adamw_groups(tensors, n, ws, ws_bytes, groups);
   if (st != MUON_OK || (st = check_device()) != MUON_OK) return st;
+  number_adamw_chunks(groups);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = reset_adamw_regions(ws, groups.size(), s)) != MUON_OK) return st;
   for (const AdamwGroup &G : groups)
@@ -621,6 +754,7 @@ muon_status hybrid_step(const muon_bucket *buckets, int nb, const muon_hparams *
     if (a0 < b1 && b0 < a1) return MUON_ERR_INVALID_ARG;
   }
   if ((st = check_device()) != MUON_OK) return st;
+  number_adamw_chunks(groups);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (nb > 0 && (st = enqueue_grouped(buckets, nb, hp, ws, s)) != MUON_OK) return st;
   if (nt > 0) {

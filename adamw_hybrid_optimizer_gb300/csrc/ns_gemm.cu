@@ -81,9 +81,9 @@ __host__ __device__ constexpr size_t smem_bytes(int epi, int stages, int slots) 
   return static_cast<size_t>(stages) * STAGE_BYTES + static_cast<size_t>(slots) * ring_slot_bytes(epi) +
          sizeof(Ctrl) + 1024;
 }
-constexpr int SHORT_K_ITERS = 32;   // contractions up to 2048 take the deep-ring shape
-static_assert(smem_bytes(EPI_GRAM, 6, 1) <= 232448 && smem_bytes(EPI_APPLY, 6, 2) <= 232448 &&
-                  smem_bytes(EPI_APPLY, 4, 5) <= 232448,
+constexpr int SHORT_K_ITERS = 32;   // without a measured choice, contractions up to 2048 take the deep-ring shape
+static_assert(smem_bytes(EPI_GRAM, 6, 1) <= 232448 && smem_bytes(EPI_POLY, 6, 2) <= 232448 &&
+                  smem_bytes(EPI_POLY, 5, 3) <= 232448 && smem_bytes(EPI_POLY, 4, 5) <= 232448,
               "shared memory over budget");
 
 // Kernel parameter: up to GEMM_MAX_PROBLEMS problems of one step kind, in order of tile_begin.
@@ -1088,13 +1088,17 @@ muon_status GemmBatch::launch(cudaStream_t s) {
     debug_timeline(&g.timeline, &g.timeline_cap);
     int max_k = 0;
     for (int i = 0; i < cnt; ++i) max_k = g.prob[i].k_iters > max_k ? g.prob[i].k_iters : max_k;
-    const bool short_k = max_k <= SHORT_K_ITERS;
+    // POLY's pipeline shape: an explicit override, else the autotune table's measured choice, else the rule
+    int shape = force_ >= 0 ? force_ : poly_shape_forced();
+    if (shape < 0) shape = poly_shape_lookup(max_k);
+    if (shape < 0) shape = max_k <= SHORT_K_ITERS ? 0 : 2;
     muon_status st;
     switch (epi_) {
       case EPI_GRAM: st = launch_shape<EPI_GRAM, false, 6, 1>(g, KK_GRAM, s); break;
       case EPI_POLY:
-        st = short_k ? launch_shape<EPI_POLY, false, 4, 5>(g, KK_POLY, s)
-                     : launch_shape<EPI_POLY, false, 6, 2>(g, KK_POLY, s);
+        st = shape == 0   ? launch_shape<EPI_POLY, false, 4, 5>(g, KK_POLY, s)
+             : shape == 1 ? launch_shape<EPI_POLY, false, 5, 3>(g, KK_POLY, s)
+                          : launch_shape<EPI_POLY, false, 6, 2>(g, KK_POLY, s);
         break;
       case EPI_APPLY: st = launch_shape<EPI_APPLY, true, 6, 1>(g, KK_APPLY, s); break;
       default:

@@ -83,6 +83,10 @@ SIGNATURES = {
                                ctypes.c_size_t, _vp]),
     "ns_apply": (ctypes.c_int, [_vp, _vp, _vp, _c_int64, _c_int64, _c_int64, _vp, ctypes.c_size_t, _vp]),
     "muon_plan_buckets": (ctypes.c_int, [_c_int64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "muon_autotune": (ctypes.c_int, [ctypes.POINTER(muon_bucket), ctypes.c_int, _vp, ctypes.c_size_t, _vp]),
+    "muon_autotune_poly_shape": (ctypes.c_int32, [_c_int64]),
+    "muon_autotune_reset": (None, []),
+    "muon_debug_poly_shape": (ctypes.c_int, [ctypes.c_int32]),
     "muon_check": (ctypes.c_int, [_vp, _vp]),
     "muon_set_timeout_ns": (None, [ctypes.c_uint64]),
     "muon_debug_wait_timeout": (ctypes.c_int, [_vp, ctypes.c_size_t, ctypes.c_uint64, _vp]),
@@ -333,6 +337,24 @@ def muon_plan_buckets(shapes: Sequence[Tuple[int, int]]):
         "bucket_K": list(K)[:b],
         "momentum_offset": list(off)[:b],
     }
+
+
+def muon_autotune(buckets, ws, stream=None):
+    """Measures the poly step's pipeline shapes on these buckets and records the fastest (synchronous)."""
+    _check(lib().muon_autotune(buckets, len(buckets), ws.data_ptr(), ws.numel() * ws.element_size(),
+                               _stream(stream)), "muon_autotune")
+
+
+def muon_autotune_poly_shape(contraction: int) -> int:
+    return int(lib().muon_autotune_poly_shape(int(contraction)))
+
+
+def muon_autotune_reset():
+    lib().muon_autotune_reset()
+
+
+def muon_debug_poly_shape(shape: int):
+    _check(lib().muon_debug_poly_shape(int(shape)), "muon_debug_poly_shape")
 
 
 def muon_check(ws, stream=None) -> int:

@@ -27,8 +27,10 @@ CLASSIC = (3.4445, -4.7750, 2.0315)
 # master_weights=True (bf16 parameters only): an fp32 master copy per parameter takes the update and the
 # parameter holds it rounded to bf16 ("Optimizers: AdamW, Muon and the distributed optimizer", section "The
 # optimizer's memory budget")
+# autotune=True: before the group's first step, the poly step's pipeline shape is measured on the group's own
+# buckets and the fastest recorded (muon_autotune; "DMuon", section 2.4, shape-adaptive kernel autotuning)
 MUON_DEFAULTS = dict(lr=0.02, momentum=0.95, weight_decay=0.01, nesterov=True, cautious_wd=False, scale_mode=0,
-                     ns_steps=5, ns_coefficients=None, eps=1e-7, master_weights=False)
+                     ns_steps=5, ns_coefficients=None, eps=1e-7, master_weights=False, autotune=False)
 # is_adamw=False: Adam with L2 regularisation instead of decoupled decay ("dtensor-muon 0.1.0", "Key options")
 ADAMW_DEFAULTS = dict(lr=3e-4, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1, is_adamw=True, master_weights=False)
 
@@ -115,6 +117,7 @@ class HybridMuonAdamW:
         # zero-filled: the control block's error word must start at zero
         self._ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=device) if device is not None else None
         self._adamw_ws = None   # the grouped AdamW pass's counters, sized on first use
+        self._tuned = set()     # Muon groups whose autotune has run
 
     @torch.no_grad()
     def step(self):
@@ -140,7 +143,11 @@ class HybridMuonAdamW:
                             raise ValueError("a Muon bucket needs contiguous tensors of one dtype")
                     specs.append((bk.param_ptrs, bk.grad_ptrs, bk.momentum, bk.K, bk.A, bk.B, pdt, gdt, bk.master_ptrs))
                 if specs:
-                    muon_calls.append((L.make_buckets(specs), hp))
+                    arr = L.make_buckets(specs)
+                    if group["autotune"] and id(group) not in self._tuned:
+                        L.muon_autotune(arr, self._ws)
+                        self._tuned.add(id(group))
+                    muon_calls.append((arr, hp))
             else:
                 group["step"] += 1
                 b1, b2 = group["betas"]

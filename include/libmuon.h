@@ -130,7 +130,27 @@ size_t muon_workspace_bytes_grouped(const muon_bucket *buckets, int n);
 muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hparams *hp, void *ws, size_t ws_bytes,
                               muon_stream_t stream);
 
-/* Newton-Schulz orthogonalisation of a stack, [P2] "Muon: orthogonalising the update" (newton_schulz):
+/* Measured per-shape choice of a kernel configuration ([P4] section 2.4, shape-adaptive kernel
+ * autotuning: a search over pipeline configurations for the shapes at hand, measured once and cached for
+ * later steps). The poly step (H = a*I + b*G + c*G^2) is compiled in three pipeline shapes (mainloop
+ * stages + epilogue input slots: 4 + 5, 5 + 3, 6 + 2). For the buckets' grouped poly launch, the call
+ * times each shape (one warm-up and five timed launches, median) and records the fastest in a
+ * process-wide table keyed by the launch's deepest contraction; later launches with that contraction use
+ * it. Without an entry, contractions up to 2048 take 4 + 5 and deeper ones 6 + 2. Every shape computes
+ * each tile the same way, so the choice changes only the time, never a result.
+ *   buckets, n, ws, ws_bytes  as for muon_step_grouped. The poly launches read and overwrite the G and
+ *            H sections of ws (any content; parameters, gradients and momentum are not touched).
+ * Synchronous: returns after the timed launches complete. Errors as for muon_step_grouped's checks. */
+muon_status muon_autotune(const muon_bucket *buckets, int n, void *ws, size_t ws_bytes, muon_stream_t stream);
+
+/* The recorded poly shape (0: 4 + 5, 1: 5 + 3, 2: 6 + 2) for launches whose deepest contraction is
+ * `contraction` (the matrices' smaller dimension), or -1 if none is recorded. */
+int32_t muon_autotune_poly_shape(int64_t contraction);
+
+/* Empties the autotune table. */
+void muon_autotune_reset(void);
+
+/* Newton-Schulz orthogonalisation of a stack, [P2] "Muon: orthogonalising the update" (newton_schulz):/* Newton-Schulz orthogonalisation of a stack, [P2] "Muon: orthogonalising the update" (newton_schulz):
  * out_k = NS(x_k) for k < K, with normalisation by ||x_k||_F + eps and transpose-to-wide.
  *   x    device, contiguous (K, A, B) of xdt (MUON_F32 or MUON_BF16).
  *   out  device, contiguous (K, A, B) of odt (MUON_F32 or MUON_BF16); may not alias x.
@@ -256,6 +276,10 @@ muon_status muon_check(void *ws, muon_stream_t stream);
 
 /* Per-wait limit for device-side waits, in nanoseconds (default 2e9). Applies to later launches. */
 void muon_set_timeout_ns(uint64_t ns);
+
+/* Forces every poly launch onto one pipeline shape (0, 1 or 2 as in muon_autotune_poly_shape), or -1
+ * to go back to the table and the rule; for tests and sweeps. MUON_ERR_INVALID_ARG outside -1..2. */
+muon_status muon_debug_poly_shape(int32_t shape);
 
 /* Launches one kernel that waits on a barrier nothing will complete, with the given limit,
  * so that the bounded-wait path can be exercised: afterwards muon_check returns MUON_ERR_TIMEOUT. */

@@ -262,3 +262,23 @@ def test_hybrid_step_entry_point_checks():
     import torch
     if not torch.cuda.is_available():
         assert st() in (L.MUON_ERR_CUDA, L.MUON_ERR_UNSUPPORTED_DEVICE)
+
+
+def test_autotune_entry_point_checks_and_table():
+    lib = L.lib()
+    good = (L.muon_bucket * 1)(L.muon_bucket(FAKE, FAKE, FAKE, 4, 768, 2304, 1, 1))
+    need = L.muon_workspace_bytes_grouped(good)
+    assert lib.muon_autotune(None, 1, FAKE, need, None) == L.MUON_ERR_INVALID_ARG
+    assert lib.muon_autotune(good, 0, FAKE, need, None) == L.MUON_ERR_INVALID_ARG
+    assert lib.muon_autotune(good, 1, None, need, None) == L.MUON_ERR_INVALID_ARG
+    assert lib.muon_autotune(good, 1, FAKE + 8, need, None) == L.MUON_ERR_ALIGNMENT
+    assert lib.muon_autotune(good, 1, FAKE, need - 1, None) == L.MUON_ERR_WORKSPACE
+    bad = (L.muon_bucket * 1)(L.muon_bucket(FAKE, FAKE, FAKE, 4, 768, 0, 1, 1))
+    assert lib.muon_autotune(bad, 1, FAKE, need, None) == L.MUON_ERR_INVALID_ARG
+    L.muon_autotune_reset()
+    assert L.muon_autotune_poly_shape(768) == -1
+    assert L.muon_autotune_poly_shape(0) == -1
+    assert lib.muon_debug_poly_shape(3) == L.MUON_ERR_INVALID_ARG
+    assert lib.muon_debug_poly_shape(-2) == L.MUON_ERR_INVALID_ARG
+    assert lib.muon_debug_poly_shape(1) == L.MUON_OK
+    assert lib.muon_debug_poly_shape(-1) == L.MUON_OK
