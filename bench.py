@@ -101,11 +101,20 @@ class Workload:
 
     def step(self, stream=None):
         """One whole optimizer step through hybrid_step: the grouped Muon step, then the grouped AdamW pass."""
-        L = self.L
+        self.begin_step()
+        self.L.hybrid_step(self.bucket_array, self.hp, self.ws, self.adamw_tensors, self.adamw_ws, stream)
+
+    # the two halves of hybrid_step as separate calls, for a caller that overlaps its own copies with them
+    def begin_step(self):
         self.t += 1
         for h in self.adamw_hps:
             h.step = self.t
-        L.hybrid_step(self.bucket_array, self.hp, self.ws, self.adamw_tensors, self.adamw_ws, stream)
+
+    def muon_part(self, stream=None):
+        self.L.muon_step_grouped(self.bucket_array, self.hp, self.ws, stream)
+
+    def adamw_part(self, stream=None):
+        self.L.adamw_step_grouped(self.adamw_tensors, self.adamw_ws, stream)
 
     # algorithmic work of one step, per kernel kind
     def work(self):
@@ -390,19 +399,38 @@ def run_ours(args):
     for hg, dg in zip(host_g, dev_g):
         hg.copy_(dg)
     torch.cuda.synchronize()
+    # the copies overlap the compute: the AdamW gradients go in while the Muon chain runs, and the Muon
+    # parameters come out while the AdamW pass runs (two copy streams, events between them and the step)
     e2e_steps = max(3, args.steps // 2)
+    nb = len(wl.buckets)
+    copy_in, copy_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev = {k: torch.cuda.Event() for k in ("muon_in", "adamw_in", "muon_done", "adamw_done")}
     barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    start.record(stream)
     for _ in range(e2e_steps):
-        for hg, dg in zip(host_g, dev_g):
-            dg.copy_(hg, non_blocking=True)
-        wl.step()
-        for hp_, dp in zip(host_p, dev_p):
-            hp_.copy_(dp, non_blocking=True)
-        stream.synchronize()
-    end.record(stream)
+        with torch.cuda.stream(copy_in):
+            for hg, dg in zip(host_g[:nb], dev_g[:nb]):
+                dg.copy_(hg, non_blocking=True)
+            ev["muon_in"].record(copy_in)
+            for hg, dg in zip(host_g[nb:], dev_g[nb:]):
+                dg.copy_(hg, non_blocking=True)
+            ev["adamw_in"].record(copy_in)
+        wl.begin_step()
+        stream.wait_event(ev["muon_in"])
+        wl.muon_part(stream)
+        ev["muon_done"].record(stream)
+        stream.wait_event(ev["adamw_in"])
+        wl.adamw_part(stream)
+        ev["adamw_done"].record(stream)
+        with torch.cuda.stream(copy_out):
+            copy_out.wait_event(ev["muon_done"])
+            for hp_, dp in zip(host_p[:nb], dev_p[:nb]):
+                hp_.copy_(dp, non_blocking=True)
+            copy_out.wait_event(ev["adamw_done"])
+            for hp_, dp in zip(host_p[nb:], dev_p[nb:]):
+                hp_.copy_(dp, non_blocking=True)
+        copy_out.synchronize()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(1e3 * (time.perf_counter() - t0) / e2e_steps, world, device)
     barrier()
