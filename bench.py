@@ -110,8 +110,25 @@ class Workload:
         for h in self.adamw_hps:
             h.step = self.t
 
-    def muon_part(self, stream=None):
-        self.L.muon_step_grouped(self.bucket_array, self.hp, self.ws, stream)
+    def muon_part(self, stream=None, which=None):
+        """which: None for every bucket, else 0 or 1 for the two halves of split_buckets()."""
+        arr = self.bucket_array if which is None else self.halves[which]
+        self.L.muon_step_grouped(arr, self.hp, self.ws, stream)
+
+    def split_buckets(self):
+        """Splits the buckets in two groups, the first holding at most 40% of the gradient bytes (at least one
+        bucket), so that a caller can start the first group's chain while the rest of the gradients come in.
+        Grouping changes no result: each bucket's tiles are computed the same way in any launch."""
+        L = self.L
+        total = sum(bk["g"].numel() for bk in self.buckets)
+        cut, acc = 1, self.buckets[0]["g"].numel()
+        while cut < len(self.buckets) - 1 and acc + self.buckets[cut]["g"].numel() <= 0.4 * total:
+            acc += self.buckets[cut]["g"].numel()
+            cut += 1
+        spec = lambda bk: (bk["pptr"], bk["gptr"], bk["mom"], bk["K"], bk["A"], bk["B"], L.MUON_BF16, L.MUON_BF16)
+        self.halves = [L.make_buckets([spec(bk) for bk in self.buckets[:cut]]),
+                       L.make_buckets([spec(bk) for bk in self.buckets[cut:]])]
+        return cut
 
     def adamw_part(self, stream=None):
         self.L.adamw_step_grouped(self.adamw_tensors, self.adamw_ws, stream)
@@ -399,37 +416,38 @@ def run_ours(args):
     for hg, dg in zip(host_g, dev_g):
         hg.copy_(dg)
     torch.cuda.synchronize()
-    # the copies overlap the compute: the AdamW gradients go in while the Muon chain runs, and the Muon
-    # parameters come out while the AdamW pass runs (two copy streams, events between them and the step)
+    # the copies overlap the compute. The step runs as three calls on the compute stream, each started as
+    # soon as its inputs are in: the Muon chain of the first bucket group, the AdamW pass, the chain of the
+    # other buckets. Inputs go in on one copy stream in that order; each call's parameters come out on a
+    # second copy stream as soon as it is done.
     e2e_steps = max(3, args.steps // 2)
     nb = len(wl.buckets)
+    cut = wl.split_buckets()
+    pieces = [(list(range(cut)), lambda: wl.muon_part(stream, 0)),
+              (list(range(nb, len(dev_g))), lambda: wl.adamw_part(stream)),
+              (list(range(cut, nb)), lambda: wl.muon_part(stream, 1))]
     copy_in, copy_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
-    ev = {k: torch.cuda.Event() for k in ("muon_in", "adamw_in", "muon_done", "adamw_done")}
+    ev_in = [torch.cuda.Event() for _ in pieces]
+    ev_done = [torch.cuda.Event() for _ in pieces]
     barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         with torch.cuda.stream(copy_in):
-            for hg, dg in zip(host_g[:nb], dev_g[:nb]):
-                dg.copy_(hg, non_blocking=True)
-            ev["muon_in"].record(copy_in)
-            for hg, dg in zip(host_g[nb:], dev_g[nb:]):
-                dg.copy_(hg, non_blocking=True)
-            ev["adamw_in"].record(copy_in)
+            for (idx, _), e in zip(pieces, ev_in):
+                for i in idx:
+                    dev_g[i].copy_(host_g[i], non_blocking=True)
+                e.record(copy_in)
         wl.begin_step()
-        stream.wait_event(ev["muon_in"])
-        wl.muon_part(stream)
-        ev["muon_done"].record(stream)
-        stream.wait_event(ev["adamw_in"])
-        wl.adamw_part(stream)
-        ev["adamw_done"].record(stream)
+        for (_, run), ei, ed in zip(pieces, ev_in, ev_done):
+            stream.wait_event(ei)
+            run()
+            ed.record(stream)
         with torch.cuda.stream(copy_out):
-            copy_out.wait_event(ev["muon_done"])
-            for hp_, dp in zip(host_p[:nb], dev_p[:nb]):
-                hp_.copy_(dp, non_blocking=True)
-            copy_out.wait_event(ev["adamw_done"])
-            for hp_, dp in zip(host_p[nb:], dev_p[nb:]):
-                hp_.copy_(dp, non_blocking=True)
+            for (idx, _), e in zip(pieces, ev_done):
+                copy_out.wait_event(e)
+                for i in idx:
+                    host_p[i].copy_(dev_p[i], non_blocking=True)
         copy_out.synchronize()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(1e3 * (time.perf_counter() - t0) / e2e_steps, world, device)
