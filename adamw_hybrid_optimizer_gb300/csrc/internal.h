@@ -213,8 +213,8 @@ muon_status launch_adamw_master(float *master, __nv_bfloat16 *p, const void *g, 
 // One launch updates up to ADAMW_GROUP_MAX tensors. Their elements are cut into chunks of `chunk` elements
 // (the last chunk of a tensor may be short), numbered tensor after tensor; each warp takes the next
 // chunk from a counter in the launch's region until none is left, so every chunk is updated once
-// whatever the tensors' sizes. The chunk is ADAMW_CHUNK_MAX elements, or smaller (a multiple of 256, at
-// least 256) when the launch has too few elements to give every warp of a full grid one chunk.
+// whatever the tensors' sizes. The chunk is about an eighth of a full grid's warps' share of the elements:
+// a multiple of 256, at least 256, at most ADAMW_CHUNK_MAX.
 constexpr int ADAMW_GROUP_MAX = 96;
 constexpr long long ADAMW_CHUNK_MAX = 8192;
 constexpr size_t ADAMW_REGION_BYTES = 256;       // per launch: the chunk counter (8 B)

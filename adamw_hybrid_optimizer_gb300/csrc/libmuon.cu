@@ -698,14 +698,15 @@ static muon_status build_adamw_groups(const adamw_tensor *t, int64_t n, void *ws
   return MUON_OK;
 }
 
-// Chunk size and numbering per launch (after the device check, which gives the SM count): every warp of a
-// full grid (10 blocks of 3 warps per SM) gets a chunk of at least 256 elements, up to ADAMW_CHUNK_MAX.
+// Chunk size and numbering per launch (after the device check, which gives the SM count): about eight
+// chunks per warp of a full grid (10 blocks of 3 warps per SM), so that the last chunks, which a few warps
+// finish alone, are a small part of the pass; at least 256 elements, at most ADAMW_CHUNK_MAX.
 static void number_adamw_chunks(std::vector<AdamwGroup> &groups) {
   const long long warps = static_cast<long long>(device_sm_count()) * 10 * (ADAMW_THREADS / 32);
   for (AdamwGroup &G : groups) {
     long long elems = 0;
     for (int k = 0; k < G.ntensors; ++k) elems += G.t[k].n;
-    long long c = (elems / std::max(1LL, warps) + 255) / 256 * 256;
+    long long c = (elems / std::max(1LL, 8 * warps) + 255) / 256 * 256;
     G.chunk = std::min(ADAMW_CHUNK_MAX, std::max(256LL, c));
     G.total_chunks = 0;
     for (int k = 0; k < G.ntensors; ++k) {
