@@ -161,7 +161,8 @@ def test_hybrid_equals_sequential(L, form):
     m_ref, m_got = _muon_set(L, SHAPES, 11), None
     m_got = [[x.clone() for x in t] for t in m_ref]
     a_specs = [(1_000_003, torch.bfloat16, torch.bfloat16, False, 0), (768, torch.bfloat16, torch.bfloat16, False, 0),
-               (5000, torch.float32, torch.float32, False, 0), (40_000, torch.bfloat16, torch.bfloat16, True, 0)]
+               (5000, torch.float32, torch.float32, False, 0), (40_000, torch.bfloat16, torch.bfloat16, True, 0),
+               (300_001, torch.bfloat16, torch.float32, False, 0), (77, torch.float32, torch.float32, False, 1)]
     a_ref = _tensor_set(12, a_specs)
     a_got = _clone(a_ref)
     b_ref, b_got = _buckets(L, m_ref, SHAPES), _buckets(L, m_got, SHAPES)
