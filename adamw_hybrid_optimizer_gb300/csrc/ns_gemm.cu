@@ -184,9 +184,6 @@ struct Region {
     const int line = lane_base + i;
     return slot + line * 128 + ((((half << 2) + q) ^ (line & 7)) << 4);
   }
-  __device__ __forceinline__ __nv_bfloat16 *elem(int i, int j) const {
-    return reinterpret_cast<__nv_bfloat16 *>(piece(i, j >> 3)) + (j & 7);
-  }
 };
 
 // the thread's own row i: 32 values in, 32 values out
@@ -198,14 +195,18 @@ __device__ __forceinline__ void region_write_row(const Region &g, int i, const f
 #pragma unroll
   for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4 *>(g.piece(i, q)) = pack8(src + 8 * q);
 }
-// the thread's values as column i of the region (element j goes to row j): a transpose through smem
-__device__ __forceinline__ void region_write_col(const Region &g, int i, const float *src) {
+// Transposes the warp's 32 x 32 region in place (element (i, j) moves to (j, i)): its sixteen 8 x 8 blocks
+// are loaded transposed into registers (ldmatrix .trans, block (p, j) by load p) and stored back at the
+// mirrored block positions (stmatrix, block (j, p) by store p). Called by every lane of the warp; the
+// caller orders other accesses to the region around it with __syncwarp.
+__device__ __forceinline__ void region_transpose(const Region &g, int lane) {
+  const int j = lane >> 3, k = lane & 7;
+  uint32_t r[4][4];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) *g.elem(j, i) = __float2bfloat16_rn(src[j]);
-}
-__device__ __forceinline__ void region_read_col(const Region &g, int i, float *dst) {
+  for (int p = 0; p < 4; ++p) ldsm_x4_trans(smem_u32(g.piece(8 * p + k, j)), r[p]);
+  __syncwarp();
 #pragma unroll
-  for (int j = 0; j < 32; ++j) dst[j] = bf2f(*g.elem(j, i));
+  for (int p = 0; p < 4; ++p) stsm_x4(smem_u32(g.piece(8 * j + k, p)), r[p]);
 }
 
 // Segment-wise access: in pass k, lane l handles 16-byte piece l%4 of region row seg_row(l, k). The
@@ -400,9 +401,9 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem &a, int b, int 
         [&](int i, int j) { return warp_row0 + i < rows && col0 + j < cols && col0 + j >= warp_row0 + i; },
         [&](int i) { return warp_row0 + i < rows && col0 + 32 <= cols && (below_free || col0 >= warp_row0 + i); });
     __syncwarp();
-    // strictly upper part mirrored: element (row, c) also stored at (c, row); the region holds the transposed
-    // chunk, whose row i is output row col0 + i, columns warp_row0 .. +31
-    region_write_col(rg, lane, v);
+    // strictly upper part mirrored: element (row, c) also stored at (c, row); the region, transposed in
+    // place, holds the transposed chunk, whose row i is output row col0 + i, columns warp_row0 .. +31
+    region_transpose(rg, lane);
     __syncwarp();
     region_store(
         rg, lane, out_b + static_cast<long long>(col0) * a.ld_out + warp_row0, a.ld_out,
@@ -462,13 +463,17 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem &a, int b, int 
         if (update) {
           region_load(rg, lane, blk, a.orig_cols, ok, full);
           __syncwarp();
+          region_transpose(rg, lane);   // region row i: wide row warp_row0 + i
+          __syncwarp();
           float pv[32];
-          region_read_col(rg, lane, pv);
+          region_read_row(rg, lane, pv);
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = param_update(pv[j], v[j], a);
           __syncwarp();
         }
-        region_write_col(rg, lane, v);
+        region_write_row(rg, lane, v);
+        __syncwarp();
+        region_transpose(rg, lane);     // region row i: stored row col0 + i
         __syncwarp();
         region_store(rg, lane, blk, a.orig_cols, ok, full);
       }
@@ -509,17 +514,24 @@ __device__ __forceinline__ void final_chunk_bf16(const GemmProblem &a, int b, in
     for (int j = 0; j < 32; ++j) v[j] *= sc;
   }
   __syncwarp();
-  if (!a.transposed) {
+  // stored tall: the block is transposed in place to the wide orientation, updated row by row, and
+  // transposed back
+  if (a.transposed) {
+    region_transpose(rg, lane);
+    __syncwarp();
+  }
+  {
     float pv[32];
     region_read_row(rg, lane, pv);
     param_update_32(v, [&](int j) { return pv[j]; }, a);
-  } else {
-    param_update_32(v, [&](int j) { return bf2f(*rg.elem(j, lane)); }, a);
   }
   __syncwarp();
-  if (!a.transposed) region_write_row(rg, lane, v);
-  else region_write_col(rg, lane, v);
+  region_write_row(rg, lane, v);
   __syncwarp();
+  if (a.transposed) {
+    region_transpose(rg, lane);
+    __syncwarp();
+  }
   const ParamBlock pb = param_block(a, p, warp_row0, col0);
   region_store(
       rg, lane, const_cast<__nv_bfloat16 *>(pb.base), pb.ld, [&](int i, int j) { return i < pb.ilim && j < pb.jlim; },

@@ -113,6 +113,26 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
 }
 
 // 3-D tiled load of one box into shared memory, completing tx bytes on bar.
+// ------------------------------------------------------------------------------------------ 8x8 b16 matrices
+
+// Four 8 x 8 b16 matrices from shared memory, transposed on the way: lanes 8j .. 8j+7 give the addresses of
+// rows 0..7 of matrix j (16 bytes each); r[j] of lane t holds elements (2(t%4), t/4) and (2(t%4)+1, t/4)
+// of matrix j.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// Four 8 x 8 b16 matrices to shared memory: r[j] of lane t holds elements (t/4, 2(t%4)) and (t/4, 2(t%4)+1)
+// of matrix j; lanes 8j .. 8j+7 give the addresses of its rows 0..7.
+__device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t (&r)[4]) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+
 // Hint: bring bytes [src, src + bytes) into L2 (16-byte aligned address, bytes a multiple of 16). Nothing
 // waits for it and nothing depends on it.
 __device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
