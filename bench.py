@@ -111,24 +111,25 @@ class Workload:
             h.step = self.t
 
     def muon_part(self, stream=None, which=None):
-        """which: None for every bucket, else 0 or 1 for the two halves of split_buckets()."""
-        arr = self.bucket_array if which is None else self.halves[which]
+        """which: None for every bucket, else an index into the groups of split_buckets()."""
+        arr = self.bucket_array if which is None else self.groups[which]
         self.L.muon_step_grouped(arr, self.hp, self.ws, stream)
 
     def split_buckets(self):
-        """Splits the buckets in two groups, the first holding at most 40% of the gradient bytes (at least one
-        bucket), so that a caller can start the first group's chain while the rest of the gradients come in.
-        Grouping changes no result: each bucket's tiles are computed the same way in any launch."""
+        """Splits the buckets into groups: a first one holding at most 40% of the gradient bytes (at least one
+        bucket), then one group per remaining bucket, so that a caller can start each group's chain as soon as
+        its gradients are in, and copy its parameters out while the next one runs. Grouping changes no
+        result: each bucket's tiles are computed the same way in any launch. Returns the bucket index lists."""
         L = self.L
         total = sum(bk["g"].numel() for bk in self.buckets)
         cut, acc = 1, self.buckets[0]["g"].numel()
         while cut < len(self.buckets) - 1 and acc + self.buckets[cut]["g"].numel() <= 0.4 * total:
             acc += self.buckets[cut]["g"].numel()
             cut += 1
+        idx = [list(range(cut))] + [[i] for i in range(cut, len(self.buckets))]
         spec = lambda bk: (bk["pptr"], bk["gptr"], bk["mom"], bk["K"], bk["A"], bk["B"], L.MUON_BF16, L.MUON_BF16)
-        self.halves = [L.make_buckets([spec(bk) for bk in self.buckets[:cut]]),
-                       L.make_buckets([spec(bk) for bk in self.buckets[cut:]])]
-        return cut
+        self.groups = [L.make_buckets([spec(self.buckets[i]) for i in g]) for g in idx]
+        return idx
 
     def adamw_part(self, stream=None):
         self.L.adamw_step_grouped(self.adamw_tensors, self.adamw_ws, stream)
@@ -416,16 +417,16 @@ def run_ours(args):
     for hg, dg in zip(host_g, dev_g):
         hg.copy_(dg)
     torch.cuda.synchronize()
-    # the copies overlap the compute. The step runs as three calls on the compute stream, each started as
-    # soon as its inputs are in: the Muon chain of the first bucket group, the AdamW pass, the chain of the
-    # other buckets. Inputs go in on one copy stream in that order; each call's parameters come out on a
+    # the copies overlap the compute. The step runs as several calls on the compute stream, each started as
+    # soon as its inputs are in: the Muon chain of the first bucket group, the AdamW pass, then the chain of
+    # each other bucket. Inputs go in on one copy stream in that order; each call's parameters come out on a
     # second copy stream as soon as it is done.
     e2e_steps = max(3, args.steps // 2)
     nb = len(wl.buckets)
-    cut = wl.split_buckets()
-    pieces = [(list(range(cut)), lambda: wl.muon_part(stream, 0)),
-              (list(range(nb, len(dev_g))), lambda: wl.adamw_part(stream)),
-              (list(range(cut, nb)), lambda: wl.muon_part(stream, 1))]
+    groups = wl.split_buckets()
+    pieces = [(groups[0], lambda: wl.muon_part(stream, 0)),
+              (list(range(nb, len(dev_g))), lambda: wl.adamw_part(stream))]
+    pieces += [(g, lambda k=k: wl.muon_part(stream, k)) for k, g in enumerate(groups) if k > 0]
     copy_in, copy_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     ev_in = [torch.cuda.Event() for _ in pieces]
     ev_done = [torch.cuda.Event() for _ in pieces]
