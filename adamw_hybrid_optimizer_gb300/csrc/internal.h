@@ -50,6 +50,10 @@ struct GemmProblem {
   int tiles_per_matrix;   // tile pairs per matrix
   int k_iters;            // contraction / 64, rounded up
   long long tile_begin;   // first tile pair of this problem in the launch's pair space
+  // per-matrix readiness counters (see TileSync), indexed by the matrix within the problem; null: none
+  const uint32_t *wait_ctr;
+  uint32_t wait_target;
+  uint32_t *sig_ctr;
   // epilogue coefficients
   float alpha;            // gram: output = alpha * s^2 * acc (s from `scale` when given)
   float coef_a, coef_b, coef_c;   // poly: output = a*I + b*G + c*acc, with G read by the epilogue
@@ -103,17 +107,35 @@ void poly_shape_record(int k_iters, int shape);
 void poly_shape_clear();
 int poly_shape_forced();
 
+// Per-matrix dependencies between the grouped launches of one Newton-Schulz chain, instead of the launch
+// order: a tile of matrix b loads its operands only once wait[b] >= target (every tile of b that the
+// previous step kind produced has been stored), and each epilogue warp adds 1 to sig[b] (release) when
+// its part of a tile is stored. A launch whose problems all have a wait skips the grid-wide dependency on
+// its predecessor, so its tiles can start on the SMs its predecessor has left while the rest finish.
+struct TileSync {
+  const uint32_t *wait;
+  uint32_t target;
+  uint32_t *sig;
+};
+// The signals one launch of this step kind adds to a matrix's counter (every CTA's epilogue warps, once
+// per tile) for a wide iterate of m rows and n columns.
+uint32_t gemm_signals_per_matrix(int epi, long long m, long long n);
+
 class GemmBatch {
  public:
   GemmBatch(int epi, uint32_t *err, unsigned long long timeout_ns) : epi_(epi), err_(err), timeout_ns_(timeout_ns) {}
   // POLY only: launch with this pipeline shape whatever the table or the rule says (-1: no override)
   void force_shape(int shape) { force_ = shape; }
   muon_status add_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long ldg, long long mstride_g, float alpha,
-                       const float *scale);
+                       const float *scale,
+                       const TileSync *sync = nullptr);
   muon_status add_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float a, float b,
-                       float c);
-  muon_status add_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, const float *scale);
-  muon_status add_final(const Bf16Stack &h, const Bf16Stack &x, const float *scale, const FinalSpec &f);
+                       float c,
+                       const TileSync *sync = nullptr);
+  muon_status add_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, const float *scale,
+                       const TileSync *sync = nullptr);
+  muon_status add_final(const Bf16Stack &h, const Bf16Stack &x, const float *scale, const FinalSpec &f,
+                       const TileSync *sync = nullptr);
   muon_status launch(cudaStream_t s);
   ~GemmBatch();
 

@@ -172,7 +172,9 @@ long long round8(long long v) { return (v + 7) / 8 * 8; }
 // A workspace starts with a header: the control block (error word at byte 0) and one counter per matrix
 // of the call, which the call zeroes before its first launch. Each stack's sections follow, stack after
 // stack; their offsets below are relative to the stack's own start.
-size_t header_bytes(long long total_K) { return align_up(CTRL_BYTES + static_cast<size_t>(total_K) * 4, 1024); }
+// Control block, then four counters per matrix: the norm pass's tile count and the grouped chain's
+// per-matrix readiness counters of G, H and the iterate X (TileSync).
+size_t header_bytes(long long total_K) { return align_up(CTRL_BYTES + static_cast<size_t>(total_K) * 16, 1024); }
 
 struct Layout {
   long long m, n, ldx, ldg, tiles_r, tiles_c;
@@ -414,8 +416,11 @@ static muon_status enqueue_grouped(const muon_bucket *buckets, int n, const muon
     w[i] = base + off;
     off += L[i].total;
   }
+  // readiness counters of the chain: G, H and X of matrix k at G_ready[k], H_ready[k], X_ready[k]; they only
+  // grow during a step (t-th launch of a kind: target t times its per-launch count) and start at zero
+  uint32_t *G_ready = counters + total_K, *H_ready = counters + 2 * total_K, *X_ready = counters + 3 * total_K;
   // momentum, Nesterov input, norm: all buckets in one pass
-  if ((st = launch_counter_reset(counters, total_K, s)) != MUON_OK) return st;
+  if ((st = launch_counter_reset(counters, 4 * total_K, s)) != MUON_OK) return st;
   std::vector<NesterovArgs> na(n);
   for (long long i = 0, k0 = 0; i < n; k0 += buckets[i].K, ++i) {
     const muon_bucket &bk = buckets[i];
@@ -451,10 +456,18 @@ static muon_status enqueue_grouped(const muon_bucket *buckets, int n, const muon
     const float a = hp->coeffs[3 * t], b = hp->coeffs[3 * t + 1], c = hp->coeffs[3 * t + 2];
     GemmBatch gram(EPI_GRAM, err, to), poly(EPI_POLY, err, to);
     GemmBatch last(t + 1 < hp->ns_steps ? EPI_APPLY : EPI_FINAL, err, to);
-    for (int i = 0; i < n; ++i) {
+    for (int i = 0, k0 = 0; i < n; k0 += static_cast<int>(buckets[i].K), ++i) {
       if (small[i]) continue;
       const Layout &Li = L[i];
       const float *sc = t == 0 ? reinterpret_cast<const float *>(w[i] + Li.scale) : nullptr;
+      const uint32_t e_gram = gemm_signals_per_matrix(EPI_GRAM, Li.m, Li.n);
+      const uint32_t e_poly = gemm_signals_per_matrix(EPI_POLY, Li.m, Li.n);
+      const uint32_t e_apply = gemm_signals_per_matrix(EPI_APPLY, Li.m, Li.n);
+      const uint32_t tt = static_cast<uint32_t>(t);
+      // GRAM of step 0 reads the norm pass's output: it keeps the launch-order dependency
+      const TileSync sync_gram{t == 0 ? nullptr : X_ready + k0, tt * e_apply, G_ready + k0};
+      const TileSync sync_poly{G_ready + k0, (tt + 1) * e_gram, H_ready + k0};
+      const TileSync sync_last{H_ready + k0, (tt + 1) * e_poly, t + 1 < hp->ns_steps ? X_ready + k0 : nullptr};
       __nv_bfloat16 *xb[2] = {reinterpret_cast<__nv_bfloat16 *>(w[i] + Li.x0),
                               reinterpret_cast<__nv_bfloat16 *>(w[i] + Li.x1)};
       __nv_bfloat16 *G = reinterpret_cast<__nv_bfloat16 *>(w[i] + Li.g);
@@ -463,12 +476,12 @@ static muon_status enqueue_grouped(const muon_bucket *buckets, int n, const muon
       Bf16Stack X{xb[t & 1], Li.m, Li.n, Li.ldx, msx, K};
       Bf16Stack Gs{G, Li.m, Li.m, Li.ldg, msg, K};
       Bf16Stack Hs{H, Li.m, Li.m, Li.ldg, msg, K};
-      if ((st = gram.add_gram(X, G, Li.ldg, msg, 1.0f, sc)) != MUON_OK) return st;
-      if ((st = poly.add_poly(Gs, H, Li.ldg, msg, a, b, c)) != MUON_OK) return st;
+      if ((st = gram.add_gram(X, G, Li.ldg, msg, 1.0f, sc, &sync_gram)) != MUON_OK) return st;
+      if ((st = poly.add_poly(Gs, H, Li.ldg, msg, a, b, c, &sync_poly)) != MUON_OK) return st;
       if (t + 1 < hp->ns_steps) {
-        st = last.add_apply(Hs, X, xb[(t + 1) & 1], sc);
+        st = last.add_apply(Hs, X, xb[(t + 1) & 1], sc, &sync_last);
       } else {
-        st = last.add_final(Hs, X, sc, final_spec(buckets[i]));
+        st = last.add_final(Hs, X, sc, final_spec(buckets[i]), &sync_last);
       }
       if (st != MUON_OK) return st;
     }

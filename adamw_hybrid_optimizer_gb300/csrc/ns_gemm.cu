@@ -98,6 +98,7 @@ struct GemmGroup {
   unsigned long long timeout_ns;
   unsigned long long *timeline;   // optional per-tile timestamps (performance analysis), or null
   int timeline_cap;               // records per CTA
+  int counter_deps;               // every problem waits on per-matrix counters: no grid-wide dependency
 };
 static_assert(sizeof(GemmGroup) <= 4096, "kernel parameter block too large");
 
@@ -580,8 +581,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
   cluster_sync();   // both CTAs' barriers are initialised before either multicasts into the other
   tc_fence_after();
   // everything above touched only shared and tensor memory; operands, scales and parameters written by
-  // earlier kernels are read only after the previous grid has completed
-  pdl_wait();
+  // earlier kernels are read only after the previous grid has completed, or, with per-matrix counters,
+  // after the tiles of the matrix they belong to have been stored (the waits below)
+  if (!args.counter_deps) pdl_wait();
   if (threadIdx.x == 0) pdl_launch_dependents();
   const uint32_t tmem_base = ctrl->tmem_base;
   WaitCtl ctl{&ctrl->abort_flag, args.err, args.timeout_ns};
@@ -600,6 +602,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       for (int s = 0; s < MAX_STAGES; ++s) last_parity[s] = -1;
       bool ok = true;
       int local = 0;
+      int ready_pi = -1, ready_b = -1;   // the last matrix whose inputs this thread has waited for
       for (long long t = first; ok && t < args.total_tiles; t += stride, ++local) {
         unsigned long long *rec = tl_rec(args, local);
         if (rec) {
@@ -615,6 +618,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         const CUtensorMap *map_b = &args.map_b[pi];
         int b, ti, tj;
         decode_tile(P, args.symmetric, t - P.tile_begin, rank, b, ti, tj);
+        if (P.wait_ctr != nullptr && (pi != ready_pi || b != ready_b)) {
+          if (!wait_counter(P.wait_ctr + b, P.wait_target, ctl)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();   // the TMA loads below read what the generic stores wrote
+          ready_pi = pi;
+          ready_b = b;
+        }
         const int k_iters = P.k_iters;
         for (int kk = 0; kk < k_iters; ++kk) {
           if (!wait_bounded(&ctrl->empty[stage], phase ^ 1u, ctl, ERR_WAIT_EMPTY)) {
@@ -710,6 +722,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       int last_parity[MAX_RING_SLOTS];
       for (int s = 0; s < MAX_RING_SLOTS; ++s) last_parity[s] = -1;
       bool ok = true;
+      int ready_pi = -1, ready_b = -1;
       for (long long t = first; ok && t < args.total_tiles; t += stride) {
         const int pi = find_problem(args, t);
         const GemmProblem P = args.prob[pi];
@@ -717,6 +730,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         const CUtensorMap *aux_map = &args.map_a[pi];
         int b, ti, tj;
         decode_tile(P, args.symmetric, t - P.tile_begin, rank, b, ti, tj);
+        if (P.wait_ctr != nullptr && (pi != ready_pi || b != ready_b)) {
+          bool w = true;
+          if (lane == 0) {
+            w = wait_counter(P.wait_ctr + b, P.wait_target, ctl);
+            if (w) fence_proxy_async_global();
+          }
+          if (!__shfl_sync(0xffffffffu, w, 0)) break;
+          ready_pi = pi;
+          ready_b = b;
+        }
         const int row0 = ti * BM;
         for (int s = 0; s < BN / 64; ++s) {
           const int c0 = tj * BN + 64 * s;
@@ -852,6 +875,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       if (rec) rec[8] = globaltimer_ns();
       tc_fence_before();
       __syncwarp();
+      // this warp's stores of the tile are done: count them for the launches that read this matrix
+      if (P.sig_ctr != nullptr && lane == 0) red_release_gpu_add(P.sig_ctr + b, 1u);
       // the accumulator is free once both CTAs' epilogues have read their halves (even CTA's barrier); the
       // MMA warp reads none of this warp's global stores, so the signal need not wait for them to drain
       if (lane == 0) mbar_arrive_cluster_relaxed(leader_acc_empty0 + acc * static_cast<uint32_t>(sizeof(uint64_t)));
@@ -978,6 +1003,13 @@ struct GemmBatch::Item {
 
 GemmBatch::~GemmBatch() { delete[] items_; }
 
+uint32_t gemm_signals_per_matrix(int epi, long long m, long long n) {
+  GemmProblem p{};
+  const bool symmetric = epi == EPI_GRAM || epi == EPI_POLY;
+  fill_tiles(p, 1, m, symmetric ? m : n, symmetric ? n : m, symmetric);
+  return static_cast<uint32_t>(p.tiles_per_matrix) * 2u * EPI_WARPS;
+}
+
 muon_status GemmBatch::push(const Item &it) {
   if (n_ == cap_) {
     const int nc = cap_ ? 2 * cap_ : GEMM_MAX_PROBLEMS;
@@ -992,7 +1024,7 @@ muon_status GemmBatch::push(const Item &it) {
 }
 
 muon_status GemmBatch::add_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long ldg, long long mstride_g, float alpha,
-                                const float *scale) {
+                                const float *scale, const TileSync *sync) {
   if (epi_ != EPI_GRAM) return MUON_ERR_INVALID_ARG;
   Item it{};
   if (!make_map(&it.ma, x.ptr, x.cols, x.rows, x.batch, x.ld, x.mstride, BM) ||
@@ -1004,11 +1036,16 @@ muon_status GemmBatch::add_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long 
   it.p.out = g;
   it.p.ld_out = ldg;
   it.p.mstride_out = mstride_g;
+  if (sync != nullptr) {
+    it.p.wait_ctr = sync->wait;
+    it.p.wait_target = sync->target;
+    it.p.sig_ctr = sync->sig;
+  }
   return push(it);
 }
 
 muon_status GemmBatch::add_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float a,
-                                float b, float c) {
+                                float b, float c, const TileSync *sync) {
   if (epi_ != EPI_POLY) return MUON_ERR_INVALID_ARG;
   Item it{};
   if (!make_map(&it.ma, g.ptr, g.cols, g.rows, g.batch, g.ld, g.mstride, BM) ||
@@ -1022,10 +1059,16 @@ muon_status GemmBatch::add_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long 
   it.p.out = h;
   it.p.ld_out = ldh;
   it.p.mstride_out = mstride_h;
+  if (sync != nullptr) {
+    it.p.wait_ctr = sync->wait;
+    it.p.wait_target = sync->target;
+    it.p.sig_ctr = sync->sig;
+  }
   return push(it);
 }
 
-muon_status GemmBatch::add_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, const float *scale) {
+muon_status GemmBatch::add_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, const float *scale,
+                                 const TileSync *sync) {
   if (epi_ != EPI_APPLY) return MUON_ERR_INVALID_ARG;
   Item it{};
   if (!apply_maps(h, x, &it.ma, &it.mb)) return MUON_ERR_CUDA;
@@ -1034,10 +1077,16 @@ muon_status GemmBatch::add_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bf
   it.p.out = out;
   it.p.ld_out = x.ld;
   it.p.mstride_out = x.mstride;
+  if (sync != nullptr) {
+    it.p.wait_ctr = sync->wait;
+    it.p.wait_target = sync->target;
+    it.p.sig_ctr = sync->sig;
+  }
   return push(it);
 }
 
-muon_status GemmBatch::add_final(const Bf16Stack &h, const Bf16Stack &x, const float *scale, const FinalSpec &f) {
+muon_status GemmBatch::add_final(const Bf16Stack &h, const Bf16Stack &x, const float *scale, const FinalSpec &f,
+                                 const TileSync *sync) {
   if (epi_ != EPI_FINAL) return MUON_ERR_INVALID_ARG;
   Item it{};
   if (!apply_maps(h, x, &it.ma, &it.mb)) return MUON_ERR_CUDA;
@@ -1052,6 +1101,11 @@ muon_status GemmBatch::add_final(const Bf16Stack &h, const Bf16Stack &x, const f
   it.p.cautious = f.cautious;
   it.p.lr_wd = f.lr_wd;
   it.p.lr_scale = f.lr_scale;
+  if (sync != nullptr) {
+    it.p.wait_ctr = sync->wait;
+    it.p.wait_target = sync->target;
+    it.p.sig_ctr = sync->sig;
+  }
   return push(it);
 }
 
@@ -1093,6 +1147,9 @@ muon_status GemmBatch::launch(cudaStream_t s) {
       tiles += static_cast<long long>(g.prob[i].tiles_per_matrix) * g.prob[i].batch;
     }
     g.nprob = cnt;
+    g.counter_deps = 1;
+    for (int i = 0; i < cnt; ++i)
+      if (g.prob[i].wait_ctr == nullptr) g.counter_deps = 0;
     g.symmetric = (epi_ == EPI_GRAM || epi_ == EPI_POLY) ? 1 : 0;
     g.total_tiles = tiles;
     g.err = err_;

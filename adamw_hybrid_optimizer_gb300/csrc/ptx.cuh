@@ -18,6 +18,7 @@ enum : uint32_t {
   ERR_WAIT_DRAIN = 0x105,     // teardown waiting for in-flight copies / MMAs
   ERR_WAIT_RING_FULL = 0x106, // epilogue waiting for its staged second input
   ERR_WAIT_RING_EMPTY = 0x107,// epilogue loader waiting for a free ring slot
+  ERR_WAIT_COUNTER = 0x108,   // a tile waiting for its matrix's input from the previous step kind
   ERR_WAIT_DEBUG = 0x1FF,     // the deliberate never-completing wait
 };
 
@@ -90,6 +91,40 @@ __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, con
         if (ctl.err) atomicCAS(ctl.err, 0u, code);
         return false;
       }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------ counters in global memory
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Adds v with release semantics at GPU scope: every write that happens before it (this thread's, and those
+// of other threads ordered before it by a barrier) is visible to a thread that acquires the new value.
+__device__ __forceinline__ void red_release_gpu_add(uint32_t *p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Orders generic-proxy writes this thread has acquired before its later async-proxy (TMA) global reads.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Waits until *ctr >= target (acquire). Returns false (and sets the abort flag and the error word) if
+// the limit runs out or another thread of the CTA already gave up.
+__device__ __forceinline__ bool wait_counter(const uint32_t *ctr, uint32_t target, const WaitCtl &ctl) {
+  if (ld_acquire_gpu(ctr) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(ctr) >= target) return true;
+    if (*ctl.abort_flag) return false;
+    if (globaltimer_ns() - t0 > ctl.timeout_ns) {
+      *ctl.abort_flag = 1;
+      if (ctl.err) atomicCAS(ctl.err, 0u, static_cast<uint32_t>(ERR_WAIT_COUNTER));
+      return false;
     }
   }
 }
