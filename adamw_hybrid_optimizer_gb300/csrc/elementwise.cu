@@ -190,6 +190,8 @@ __global__ void __launch_bounds__(256) nesterov_norm_kernel(const __grid_constan
 #pragma unroll
     for (int w = 0; w < 8; ++w) sum += red[w];
     a.scale[b] = 1.0f / (sqrtf(sum) + a.eps);
+    // one count past the tiles: matrix b's input to the chain (its tiles' U and this scale) is complete
+    red_release_gpu_add(a.counters + b, 1u);
   }
 }
 

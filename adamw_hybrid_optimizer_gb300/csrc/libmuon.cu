@@ -464,8 +464,11 @@ static muon_status enqueue_grouped(const muon_bucket *buckets, int n, const muon
       const uint32_t e_poly = gemm_signals_per_matrix(EPI_POLY, Li.m, Li.n);
       const uint32_t e_apply = gemm_signals_per_matrix(EPI_APPLY, Li.m, Li.n);
       const uint32_t tt = static_cast<uint32_t>(t);
-      // GRAM of step 0 reads the norm pass's output: it keeps the launch-order dependency
-      const TileSync sync_gram{t == 0 ? nullptr : X_ready + k0, tt * e_apply, G_ready + k0};
+      // GRAM of step 0 reads the norm pass's output: a matrix's norm counter reaches its tile count plus one
+      // once its U and scale are stored
+      const uint32_t norm_done = static_cast<uint32_t>(na[i].tiles_r * na[i].tiles_c) + 1u;
+      const TileSync sync_gram{t == 0 ? counters + k0 : X_ready + k0, t == 0 ? norm_done : tt * e_apply,
+                               G_ready + k0};
       const TileSync sync_poly{G_ready + k0, (tt + 1) * e_gram, H_ready + k0};
       const TileSync sync_last{H_ready + k0, (tt + 1) * e_poly, t + 1 < hp->ns_steps ? X_ready + k0 : nullptr};
       __nv_bfloat16 *xb[2] = {reinterpret_cast<__nv_bfloat16 *>(w[i] + Li.x0),
