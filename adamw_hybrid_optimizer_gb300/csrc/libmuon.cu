@@ -77,6 +77,9 @@ cudaEvent_t take_event() {
 }
 
 unsigned long long g_timeout_ns = 2000000000ull;
+// grouped chain: per-matrix counter dependencies between launches: -1 where the rule in enqueue_grouped
+// allows them, 0 never, 1 always
+int g_counter_deps = -1;
 
 }  // namespace
 
@@ -451,6 +454,28 @@ static muon_status enqueue_grouped(const muon_bucket *buckets, int n, const muon
     const SmallNsArgs sa = small_args(err, w[i], L[i], buckets[i].K, hp->ns_steps, hp->coeffs, final_spec(buckets[i]));
     if ((st = launch_ns_small(sa, s)) != MUON_OK) return st;
   }
+  // Counter dependencies pay where launch boundaries are a visible share of the chain: launches of a few
+  // hundred microseconds at most, and tiles of 8 or more 64-deep k-steps (each epilogue warp's release per
+  // tile is then cheap next to the tile). Measured: GPT-2-small step 1.525 -> 1.465 ms with them; the
+  // 256-wide aspect set (4-step tiles) 1.86 -> 2.03 ms and the Llama-3-8B set (launches of milliseconds)
+  // 330 -> 369 ms, so not there.
+  bool deps = g_counter_deps == 1;
+  if (g_counter_deps == -1) {
+    double est_us = 0.0;
+    long long min_k = 1LL << 40;
+    for (int kind = EPI_GRAM; kind <= EPI_APPLY; ++kind) {
+      double kiters = 0.0;
+      for (int i = 0; i < n; ++i) {
+        if (small[i]) continue;
+        const long long m = L[i].m, nn = L[i].n;
+        const long long k = (kind == EPI_GRAM ? nn + 63 : m + 63) / 64;
+        min_k = std::min(min_k, k);
+        kiters += static_cast<double>(buckets[i].K) * gemm_signals_per_matrix(kind, m, nn) / (2 * 8) * k;
+      }
+      est_us = std::max(est_us, kiters * 0.33 / std::max(1, device_sm_count() / 2));
+    }
+    deps = est_us <= 500.0 && min_k >= 8;
+  }
   // the Newton-Schulz chain of the other buckets, each step kind of all of them in one grouped launch
   for (int t = 0; t < hp->ns_steps; ++t) {
     const float a = hp->coeffs[3 * t], b = hp->coeffs[3 * t + 1], c = hp->coeffs[3 * t + 2];
@@ -479,12 +504,12 @@ static muon_status enqueue_grouped(const muon_bucket *buckets, int n, const muon
       Bf16Stack X{xb[t & 1], Li.m, Li.n, Li.ldx, msx, K};
       Bf16Stack Gs{G, Li.m, Li.m, Li.ldg, msg, K};
       Bf16Stack Hs{H, Li.m, Li.m, Li.ldg, msg, K};
-      if ((st = gram.add_gram(X, G, Li.ldg, msg, 1.0f, sc, &sync_gram)) != MUON_OK) return st;
-      if ((st = poly.add_poly(Gs, H, Li.ldg, msg, a, b, c, &sync_poly)) != MUON_OK) return st;
+      if ((st = gram.add_gram(X, G, Li.ldg, msg, 1.0f, sc, deps ? &sync_gram : nullptr)) != MUON_OK) return st;
+      if ((st = poly.add_poly(Gs, H, Li.ldg, msg, a, b, c, deps ? &sync_poly : nullptr)) != MUON_OK) return st;
       if (t + 1 < hp->ns_steps) {
-        st = last.add_apply(Hs, X, xb[(t + 1) & 1], sc, &sync_last);
+        st = last.add_apply(Hs, X, xb[(t + 1) & 1], sc, deps ? &sync_last : nullptr);
       } else {
-        st = last.add_final(Hs, X, sc, final_spec(buckets[i]), &sync_last);
+        st = last.add_final(Hs, X, sc, final_spec(buckets[i]), deps ? &sync_last : nullptr);
       }
       if (st != MUON_OK) return st;
     }
@@ -665,6 +690,12 @@ int32_t muon_autotune_poly_shape(int64_t contraction) {
 }
 
 void muon_autotune_reset(void) { poly_shape_clear(); }
+
+muon_status muon_debug_counter_deps(int32_t on) {
+  if (on < -1 || on > 1) return MUON_ERR_INVALID_ARG;
+  g_counter_deps = on;
+  return MUON_OK;
+}
 
 muon_status muon_debug_poly_shape(int32_t shape) {
   if (shape < -1 || shape >= POLY_SHAPES) return MUON_ERR_INVALID_ARG;

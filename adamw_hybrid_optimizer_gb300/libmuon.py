@@ -87,6 +87,7 @@ SIGNATURES = {
     "muon_autotune_poly_shape": (ctypes.c_int32, [_c_int64]),
     "muon_autotune_reset": (None, []),
     "muon_debug_poly_shape": (ctypes.c_int, [ctypes.c_int32]),
+    "muon_debug_counter_deps": (ctypes.c_int, [ctypes.c_int32]),
     "muon_check": (ctypes.c_int, [_vp, _vp]),
     "muon_set_timeout_ns": (None, [ctypes.c_uint64]),
     "muon_debug_wait_timeout": (ctypes.c_int, [_vp, ctypes.c_size_t, ctypes.c_uint64, _vp]),
@@ -355,6 +356,11 @@ def muon_autotune_reset():
 
 def muon_debug_poly_shape(shape: int):
     _check(lib().muon_debug_poly_shape(int(shape)), "muon_debug_poly_shape")
+
+
+def muon_debug_counter_deps(mode: int):
+    """1: counter dependencies in the grouped chain, 0: launch order, -1: the library's rule (default)."""
+    _check(lib().muon_debug_counter_deps(int(mode)), "muon_debug_counter_deps")
 
 
 def muon_check(ws, stream=None) -> int:

@@ -551,31 +551,46 @@ def run_config_sweep(args):
         atensors = L.make_adamw_tensors(aspecs) if aspecs else None
         aws = torch.zeros(max(L.adamw_workspace_bytes_grouped(len(aspecs)), 256), dtype=torch.uint8, device=dev)
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        t_muon = t_adamw = 0.0
-        for it in range(2 + steps):
-            for h in hps.values():
-                h.step = it + 1
-            ev[0].record()
-            L.muon_step_grouped(arr, hp, ws)
-            ev[1].record()
-            if atensors is not None:
-                L.adamw_step_grouped(atensors, aws)
-            ev[2].record()
-            torch.cuda.synchronize()
-            if it >= 2:
-                t_muon += ev[0].elapsed_time(ev[1]) / steps
-                t_adamw += ev[1].elapsed_time(ev[2]) / steps
-        if L.muon_check(ws) != L.MUON_OK:
-            raise RuntimeError(f"device wait ran out in the {name} configuration")
         abytes = n_adamw * (28 if w.adamw_dtype == "f32" else 22)
-        t_adamw = max(t_adamw, 1e-9)
-        print(json.dumps({"config": name, "muon_matrices": sum(plan["bucket_K"]), "buckets": len(plan["bucket_K"]),
-                          "muon_ms": round(t_muon, 4), "ns_tflops_nominal": round(nominal / (t_muon * 1e-3) / 1e12, 1),
-                          "ns_frac_nominal": round(nominal / (t_muon * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-                          "adamw_ms": round(t_adamw, 4), "adamw_elems": n_adamw,
-                          "adamw_gbs": round(abytes / (t_adamw * 1e-3) / 1e9, 1),
-                          "adamw_frac_hbm": round(abytes / (t_adamw * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-                          "peaks": f"{peak_src}"}), flush=True)
+        it = 0
+        # the chain with its launches overlapping through per-matrix counters (the default), then with each
+        # launch waiting for its whole predecessor; and a traced step for the per-kernel times
+        for deps in (1, 0):
+            L.muon_debug_counter_deps(deps)
+            t_muon = t_adamw = 0.0
+            for rep in range(2 + steps):
+                it += 1
+                for h in hps.values():
+                    h.step = it
+                ev[0].record()
+                L.muon_step_grouped(arr, hp, ws)
+                ev[1].record()
+                if atensors is not None:
+                    L.adamw_step_grouped(atensors, aws)
+                ev[2].record()
+                torch.cuda.synchronize()
+                if rep >= 2:
+                    t_muon += ev[0].elapsed_time(ev[1]) / steps
+                    t_adamw += ev[1].elapsed_time(ev[2]) / steps
+            L.muon_trace_enable(True)
+            L.muon_step_grouped(arr, hp, ws)
+            torch.cuda.synchronize()
+            L.muon_trace_enable(False)
+            per_kind = {}
+            for kind, t in L.muon_trace_collect():
+                per_kind[kind] = round(per_kind.get(kind, 0.0) + t, 4)
+            if L.muon_check(ws) != L.MUON_OK:
+                raise RuntimeError(f"device wait ran out in the {name} configuration")
+            t_adamw = max(t_adamw, 1e-9)
+            print(json.dumps({"config": name, "counter_deps": deps, "muon_matrices": sum(plan["bucket_K"]),
+                              "buckets": len(plan["bucket_K"]), "muon_ms": round(t_muon, 4),
+                              "ns_tflops_nominal": round(nominal / (t_muon * 1e-3) / 1e12, 1),
+                              "ns_frac_nominal": round(nominal / (t_muon * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                              "adamw_ms": round(t_adamw, 4), "adamw_elems": n_adamw,
+                              "adamw_gbs": round(abytes / (t_adamw * 1e-3) / 1e9, 1),
+                              "adamw_frac_hbm": round(abytes / (t_adamw * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                              "traced_ms_per_kind": per_kind, "peaks": f"{peak_src}"}), flush=True)
+        L.muon_debug_counter_deps(-1)
         del specs, keep, arr, ws, ap, ag, am, av, aspecs, atensors
         torch.cuda.empty_cache()
     return 0

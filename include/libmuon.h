@@ -281,6 +281,13 @@ void muon_set_timeout_ns(uint64_t ns);
  * to go back to the table and the rule; for tests and sweeps. MUON_ERR_INVALID_ARG outside -1..2. */
 muon_status muon_debug_poly_shape(int32_t shape);
 
+/* Grouped chain scheduling (muon_step_grouped, hybrid_step). 1: each launch of the Newton-Schulz chain
+ * waits per matrix on counters its predecessor raises, so that launches overlap. 0: each launch waits for
+ * its whole predecessor. -1 (the default): counters where the launches are short (a few hundred
+ * microseconds at most) and every tile has at least 8 64-deep k-steps, the launch order elsewhere.
+ * Results are the same in every mode; for measurements. MUON_ERR_INVALID_ARG for other values. */
+muon_status muon_debug_counter_deps(int32_t on);
+
 /* Launches one kernel that waits on a barrier nothing will complete, with the given limit,
  * so that the bounded-wait path can be exercised: afterwards muon_check returns MUON_ERR_TIMEOUT. */
 muon_status muon_debug_wait_timeout(void *ws, size_t ws_bytes, uint64_t timeout_ns, muon_stream_t stream);

@@ -282,3 +282,11 @@ def test_autotune_entry_point_checks_and_table():
     assert lib.muon_debug_poly_shape(-2) == L.MUON_ERR_INVALID_ARG
     assert lib.muon_debug_poly_shape(1) == L.MUON_OK
     assert lib.muon_debug_poly_shape(-1) == L.MUON_OK
+
+
+def test_counter_deps_switch():
+    lib = L.lib()
+    assert lib.muon_debug_counter_deps(2) == L.MUON_ERR_INVALID_ARG
+    assert lib.muon_debug_counter_deps(-2) == L.MUON_ERR_INVALID_ARG
+    for mode in (1, 0, -1):
+        assert lib.muon_debug_counter_deps(mode) == L.MUON_OK

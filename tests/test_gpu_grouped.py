@@ -73,11 +73,18 @@ def test_grouped_equals_per_bucket_gpt2_small(L):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_grouped_equals_per_bucket_ten_ragged_buckets(L, dtype):
+@pytest.mark.parametrize("deps", [1, 0])
+def test_grouped_equals_per_bucket_ten_ragged_buckets(L, dtype, deps):
+    """deps: the grouped chain's launches wait per matrix on counters (1) or on their whole predecessor (0);
+    the library's own rule would pick the launch order for these small shapes, so both are forced."""
     shapes = [(3, 64, 128), (2, 136, 72), (1, 8, 24), (4, 200, 264), (2, 256, 256), (1, 520, 776),
               (2, 40, 1), (3, 1, 96), (2, 384, 130), (1, 130, 384)]
     hp = workloads.workload("tiny").muon_hp
-    ps = _run_both(L, shapes, dtype, hp, seed=2)
+    L.muon_debug_counter_deps(deps)
+    try:
+        ps = _run_both(L, shapes, dtype, hp, seed=2)
+    finally:
+        L.muon_debug_counter_deps(-1)
     assert all(torch.isfinite(p.float()).all() for p in ps)
 
 
