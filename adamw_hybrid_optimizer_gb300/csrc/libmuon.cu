@@ -455,26 +455,22 @@ static muon_status enqueue_grouped(const muon_bucket *buckets, int n, const muon
     if ((st = launch_ns_small(sa, s)) != MUON_OK) return st;
   }
   // Counter dependencies pay where launch boundaries are a visible share of the chain: launches of a few
-  // hundred microseconds at most, and tiles of 8 or more 64-deep k-steps (each epilogue warp's release per
-  // tile is then cheap next to the tile). Measured: GPT-2-small step 1.525 -> 1.465 ms with them; the
-  // 256-wide aspect set (4-step tiles) 1.86 -> 2.03 ms and the Llama-3-8B set (launches of milliseconds)
-  // 330 -> 369 ms, so not there.
+  // hundred microseconds at most. Measured: GPT-2-small step 1.525 -> 1.457 ms and the 256-wide aspect set
+  // 1.86 -> 1.80 ms with them, but the Llama-3-8B set (launches of milliseconds) 325 -> 355 ms, so not there.
   bool deps = g_counter_deps == 1;
   if (g_counter_deps == -1) {
-    double est_us = 0.0;
-    long long min_k = 1LL << 40;
+    double est_us = 0.0;   // the longest step kind's launch: 0.33 us per 64-deep k-step of a tile pair
     for (int kind = EPI_GRAM; kind <= EPI_APPLY; ++kind) {
       double kiters = 0.0;
       for (int i = 0; i < n; ++i) {
         if (small[i]) continue;
         const long long m = L[i].m, nn = L[i].n;
         const long long k = (kind == EPI_GRAM ? nn + 63 : m + 63) / 64;
-        min_k = std::min(min_k, k);
         kiters += static_cast<double>(buckets[i].K) * gemm_signals_per_matrix(kind, m, nn) / (2 * 8) * k;
       }
       est_us = std::max(est_us, kiters * 0.33 / std::max(1, device_sm_count() / 2));
     }
-    deps = est_us <= 500.0 && min_k >= 8;
+    deps = est_us <= 500.0;
   }
   // the Newton-Schulz chain of the other buckets, each step kind of all of them in one grouped launch
   for (int t = 0; t < hp->ns_steps; ++t) {

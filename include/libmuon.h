@@ -284,7 +284,7 @@ muon_status muon_debug_poly_shape(int32_t shape);
 /* Grouped chain scheduling (muon_step_grouped, hybrid_step). 1: each launch of the Newton-Schulz chain
  * waits per matrix on counters its predecessor raises, so that launches overlap. 0: each launch waits for
  * its whole predecessor. -1 (the default): counters where the launches are short (a few hundred
- * microseconds at most) and every tile has at least 8 64-deep k-steps, the launch order elsewhere.
+ * microseconds at most), the launch order elsewhere.
  * Results are the same in every mode; for measurements. MUON_ERR_INVALID_ARG for other values. */
 muon_status muon_debug_counter_deps(int32_t on);
 
