@@ -47,7 +47,8 @@ constexpr int ACC_COLS = BN;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int EPI_WARPS = 8;                                // two per TMEM lane quarter
 constexpr int LOADER_WARP = 2 + EPI_WARPS;
-constexpr int NUM_THREADS = 32 * (LOADER_WARP + 1);
+constexpr int SIGNAL_WARP = LOADER_WARP + 1;                  // readiness counters' GPU-scope releases
+constexpr int NUM_THREADS = 32 * (SIGNAL_WARP + 1);
 
 // Epilogue input ring: a slot holds 64 columns (two 32-column chunks) of a tile's 128 rows, bf16, 128-byte
 // lines with the 128B swizzle TMA writes. Only POLY has a second input (G, for its b*G term); the other
@@ -73,7 +74,7 @@ struct Ctrl {
   uint32_t tmem_base;
   int abort_flag;
   int prod_tile;   // the producer's current tile (CTA-local count), for the final step's L2 prefetch pacing
-  uint32_t stored; // GRAM / APPLY with counters: epilogue warps whose part of a tile is stored (all tiles so far)
+  uint32_t stored; // with readiness counters: epilogue warps whose part of a tile is stored (all tiles so far)
 };
 
 // Pipeline shapes: a long contraction wants mainloop stages, a short one leaves the epilogue as the limit
@@ -769,32 +770,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       if (lane == 0)
         for (int s = 0; s < RING_SLOTS; ++s)
           if (last_parity[s] >= 0) drain_wait(&ctrl->ring_full[s], static_cast<uint32_t>(last_parity[s]), ctl);
-    } else if constexpr (EPI == EPI_GRAM || EPI == EPI_APPLY) {
-      // ---------------------------------------------------------------- readiness signals: once all eight
-      // epilogue warps have stored their parts of this CTA's j-th tile (their CTA-scope releases, acquired
-      // here), add them to the tile's matrix counter with one GPU-scope release
-      if (lane == 0) {
-        volatile int *abort_flag = &ctrl->abort_flag;
-        uint32_t j = 0;   // signalled tiles so far (the epilogue counts only those)
-        for (long long t = first; t < args.total_tiles; t += stride) {
-          const GemmProblem &P = args.prob[find_problem(args, t)];
-          if (P.sig_ctr == nullptr) continue;
-          int b, ti, tj;
-          decode_tile(P, args.symmetric, t - P.tile_begin, rank, b, ti, tj);
-          const uint32_t need = EPI_WARPS * ++j;
-          const unsigned long long t0 = globaltimer_ns();
-          bool gone = false;
-          while (ld_acquire_cta_shared(&ctrl->stored) < need) {
-            if (*abort_flag != 0 || globaltimer_ns() - t0 > args.timeout_ns) {
-              gone = true;
-              break;
-            }
-            __nanosleep(64);
-          }
-          if (gone) break;
-          red_release_gpu_add(P.sig_ctr + b, static_cast<uint32_t>(EPI_WARPS));
-        }
-      }
     } else if constexpr (EPI == EPI_FINAL) {   // (no L2 prefetch for the master kernel: parameters are only written)
       // ---------------------------------------------------------------- L2 prefetch of the parameters the
       // epilogue will update: a tile's rows are requested when the producer starts that tile's operand
@@ -826,6 +801,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
           for (int c = col0 + lane; c < min(col0 + BN, P.cols); c += 32)
             prefetch_l2_bulk(p + (static_cast<long long>(c) * P.orig_cols + row0) * 2, static_cast<uint32_t>(nrows) * 2);
         }
+      }
+    }
+  } else if (warp == SIGNAL_WARP) {
+    // ---------------------------------------------------------------- readiness signals: once all eight
+    // epilogue warps have stored their parts of this CTA's j-th signalled tile (their CTA-scope releases,
+    // acquired here), add them to the tile's matrix counter with one GPU-scope release, so that no epilogue
+    // warp waits for its stores to reach the GPU scope
+    if (lane == 0) {
+      volatile int *abort_flag = &ctrl->abort_flag;
+      uint32_t j = 0;   // signalled tiles so far (the epilogue counts only those)
+      for (long long t = first; t < args.total_tiles; t += stride) {
+        const GemmProblem &P = args.prob[find_problem(args, t)];
+        if (P.sig_ctr == nullptr) continue;
+        int b, ti, tj;
+        decode_tile(P, args.symmetric, t - P.tile_begin, rank, b, ti, tj);
+        const uint32_t need = EPI_WARPS * ++j;
+        const unsigned long long t0 = globaltimer_ns();
+        bool gone = false;
+        while (ld_acquire_cta_shared(&ctrl->stored) < need) {
+          if (*abort_flag != 0 || globaltimer_ns() - t0 > args.timeout_ns) {
+            gone = true;
+            break;
+          }
+          __nanosleep(64);
+        }
+        if (gone) break;
+        red_release_gpu_add(P.sig_ctr + b, static_cast<uint32_t>(EPI_WARPS));
       }
     }
   } else {
@@ -903,13 +905,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       if (rec) rec[8] = globaltimer_ns();
       tc_fence_before();
       __syncwarp();
-      // this warp's stores of the tile are done: count them for the launches that read this matrix. GRAM and
-      // APPLY hand the count to their idle loader warp (a CTA-scope release here, the GPU-scope one there);
-      // POLY, whose loader is busy, releases at GPU scope itself
-      if (P.sig_ctr != nullptr && lane == 0) {
-        if constexpr (EPI == EPI_GRAM || EPI == EPI_APPLY) red_release_cta_shared_add(&ctrl->stored, 1u);
-        else red_release_gpu_add(P.sig_ctr + b, 1u);
-      }
+      // this warp's stores of the tile are done: count them (CTA-scope release) for the signal warp, which
+      // passes them on to the launches that read this matrix
+      if (P.sig_ctr != nullptr && lane == 0) red_release_cta_shared_add(&ctrl->stored, 1u);
       // the accumulator is free once both CTAs' epilogues have read their halves (even CTA's barrier); the
       // MMA warp reads none of this warp's global stores, so the signal need not wait for them to drain
       if (lane == 0) mbar_arrive_cluster_relaxed(leader_acc_empty0 + acc * static_cast<uint32_t>(sizeof(uint64_t)));
