@@ -1034,6 +1034,15 @@ struct GemmBatch::Item {
 
 GemmBatch::~GemmBatch() { delete[] items_; }
 
+namespace {
+void set_sync(GemmProblem &p, const TileSync *sync) {
+  if (sync == nullptr) return;
+  p.wait_ctr = sync->wait;
+  p.wait_target = sync->target;
+  p.sig_ctr = sync->sig;
+}
+}  // namespace
+
 uint32_t gemm_signals_per_matrix(int epi, long long m, long long n) {
   GemmProblem p{};
   const bool symmetric = epi == EPI_GRAM || epi == EPI_POLY;
@@ -1067,11 +1076,7 @@ muon_status GemmBatch::add_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long 
   it.p.out = g;
   it.p.ld_out = ldg;
   it.p.mstride_out = mstride_g;
-  if (sync != nullptr) {
-    it.p.wait_ctr = sync->wait;
-    it.p.wait_target = sync->target;
-    it.p.sig_ctr = sync->sig;
-  }
+  set_sync(it.p, sync);
   return push(it);
 }
 
@@ -1090,11 +1095,7 @@ muon_status GemmBatch::add_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long 
   it.p.out = h;
   it.p.ld_out = ldh;
   it.p.mstride_out = mstride_h;
-  if (sync != nullptr) {
-    it.p.wait_ctr = sync->wait;
-    it.p.wait_target = sync->target;
-    it.p.sig_ctr = sync->sig;
-  }
+  set_sync(it.p, sync);
   return push(it);
 }
 
@@ -1108,11 +1109,7 @@ muon_status GemmBatch::add_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bf
   it.p.out = out;
   it.p.ld_out = x.ld;
   it.p.mstride_out = x.mstride;
-  if (sync != nullptr) {
-    it.p.wait_ctr = sync->wait;
-    it.p.wait_target = sync->target;
-    it.p.sig_ctr = sync->sig;
-  }
+  set_sync(it.p, sync);
   return push(it);
 }
 
@@ -1132,11 +1129,7 @@ muon_status GemmBatch::add_final(const Bf16Stack &h, const Bf16Stack &x, const f
   it.p.cautious = f.cautious;
   it.p.lr_wd = f.lr_wd;
   it.p.lr_scale = f.lr_scale;
-  if (sync != nullptr) {
-    it.p.wait_ctr = sync->wait;
-    it.p.wait_target = sync->target;
-    it.p.sig_ctr = sync->sig;
-  }
+  set_sync(it.p, sync);
   return push(it);
 }
 
