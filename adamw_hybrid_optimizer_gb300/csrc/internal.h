@@ -152,13 +152,17 @@ class GemmBatch {
 
 // Single-stack conveniences (a batch of one).
 muon_status launch_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long ldg, long long mstride_g, float alpha,
-                        const float *scale, uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
+                        const float *scale, uint32_t *err, unsigned long long timeout_ns, cudaStream_t s,
+                        const TileSync *sync = nullptr);
 muon_status launch_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float a, float b,
-                        float c, uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
+                        float c, uint32_t *err, unsigned long long timeout_ns, cudaStream_t s,
+                        const TileSync *sync = nullptr);
 muon_status launch_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, const float *scale,
-                         uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
+                         uint32_t *err, unsigned long long timeout_ns, cudaStream_t s,
+                        const TileSync *sync = nullptr);
 muon_status launch_final(const Bf16Stack &h, const Bf16Stack &x, const float *scale, const FinalSpec &f,
-                         uint32_t *err, unsigned long long timeout_ns, cudaStream_t s);
+                         uint32_t *err, unsigned long long timeout_ns, cudaStream_t s,
+                        const TileSync *sync = nullptr);
 
 // ------------------------------------------------------------------------------------------ small matrices
 

@@ -282,9 +282,34 @@ SmallNsArgs small_args(uint32_t *err, char *ws, const Layout &L, long long K, in
   return a;
 }
 
+// Estimated duration of one step kind's launch over these stacks: 0.33 us per 64-deep k-step of a 256 x 256
+// tile pair (the measured mainloop rate), spread over the clusters.
+double launch_estimate_us(int kind, long long m, long long n, long long K) {
+  const long long k = (kind == EPI_GRAM ? n + 63 : m + 63) / 64;
+  const double pairs = static_cast<double>(K) * gemm_signals_per_matrix(kind, m, n) / (2 * 8);
+  return pairs * static_cast<double>(k) * 0.33 / std::max(1, device_sm_count() / 2);
+}
+
+// Whether a chain whose longest launch is estimated at est_us uses the per-matrix readiness counters.
+// They pay where launch boundaries are a visible share of the chain: launches of a few hundred
+// microseconds at most. Measured: GPT-2-small step 1.525 -> 1.457 ms and the 256-wide aspect set
+// 1.86 -> 1.80 ms with them, but the Llama-3-8B set (launches of milliseconds) 325 -> 355 ms.
+bool counter_deps_for(double est_us) { return g_counter_deps == 1 || (g_counter_deps == -1 && est_us <= 500.0); }
+
+// The Newton-Schulz chain of one stack. counters: the workspace's four counters per matrix (the norm
+// pass's, then the readiness of G, H and X), zeroed by the caller before the norm pass; norm_tiles: the
+// norm pass's tiles per matrix. With counter dependencies (counter_deps_for), each launch waits per matrix
+// on its predecessor's counters instead of on the whole grid.
 muon_status run_ns_chain(uint32_t *err, char *ws, const Layout &L, long long K, int ns_steps, const float *coeffs,
-                         const FinalSpec &fin, cudaStream_t s) {
+                         const FinalSpec &fin, cudaStream_t s, uint32_t *counters, uint32_t norm_tiles) {
   if (ns_small_fits(L.m, L.n)) return launch_ns_small(small_args(err, ws, L, K, ns_steps, coeffs, fin), s);
+  double est = 0.0;
+  for (int kind = EPI_GRAM; kind <= EPI_APPLY; ++kind) est = std::max(est, launch_estimate_us(kind, L.m, L.n, K));
+  const bool deps = counter_deps_for(est);
+  uint32_t *G_ready = counters + K, *H_ready = counters + 2 * K, *X_ready = counters + 3 * K;
+  const uint32_t e_gram = gemm_signals_per_matrix(EPI_GRAM, L.m, L.n);
+  const uint32_t e_poly = gemm_signals_per_matrix(EPI_POLY, L.m, L.n);
+  const uint32_t e_apply = gemm_signals_per_matrix(EPI_APPLY, L.m, L.n);
   const float *scale = reinterpret_cast<const float *>(ws + L.scale);
   __nv_bfloat16 *xb[2] = {reinterpret_cast<__nv_bfloat16 *>(ws + L.x0), reinterpret_cast<__nv_bfloat16 *>(ws + L.x1)};
   __nv_bfloat16 *G = reinterpret_cast<__nv_bfloat16 *>(ws + L.g);
@@ -296,16 +321,23 @@ muon_status run_ns_chain(uint32_t *err, char *ws, const Layout &L, long long K, 
   for (int t = 0; t < ns_steps; ++t) {
     const float a = coeffs[3 * t], b = coeffs[3 * t + 1], c = coeffs[3 * t + 2];
     const float *sc = (t == 0) ? scale : nullptr;
+    const uint32_t tt = static_cast<uint32_t>(t);
+    const TileSync sync_gram{t == 0 ? counters : X_ready, t == 0 ? norm_tiles + 1u : tt * e_apply, G_ready};
+    const TileSync sync_poly{G_ready, (tt + 1) * e_gram, H_ready};
+    const TileSync sync_last{H_ready, (tt + 1) * e_poly, t + 1 < ns_steps ? X_ready : nullptr};
     Bf16Stack X{xb[t & 1], L.m, L.n, L.ldx, mstride_x, K};
-    if ((st = launch_gram(X, G, L.ldg, mstride_g, 1.0f, sc, err, to, s)) != MUON_OK) return st;
+    if ((st = launch_gram(X, G, L.ldg, mstride_g, 1.0f, sc, err, to, s, deps ? &sync_gram : nullptr)) != MUON_OK)
+      return st;
     Bf16Stack Gs{G, L.m, L.m, L.ldg, mstride_g, K};
-    if ((st = launch_poly(Gs, H, L.ldg, mstride_g, a, b, c, err, to, s)) != MUON_OK) return st;
+    if ((st = launch_poly(Gs, H, L.ldg, mstride_g, a, b, c, err, to, s, deps ? &sync_poly : nullptr)) != MUON_OK)
+      return st;
     Bf16Stack Hs{H, L.m, L.m, L.ldg, mstride_g, K};
     if (t + 1 < ns_steps) {
-      if ((st = launch_apply(Hs, X, xb[(t + 1) & 1], sc, err, to, s)) != MUON_OK) return st;
+      st = launch_apply(Hs, X, xb[(t + 1) & 1], sc, err, to, s, deps ? &sync_last : nullptr);
     } else {
-      if ((st = launch_final(Hs, X, sc, fin, err, to, s)) != MUON_OK) return st;
+      st = launch_final(Hs, X, sc, fin, err, to, s, deps ? &sync_last : nullptr);
     }
+    if (st != MUON_OK) return st;
   }
   return MUON_OK;
 }
@@ -344,7 +376,7 @@ muon_status muon_step_batched(void *const *params, muon_dtype pdt, const void *c
   char *base = static_cast<char *>(ws);
   char *w = base + header_bytes(K);
   unsigned *counters = reinterpret_cast<unsigned *>(base + CTRL_BYTES);
-  if ((st = launch_counter_reset(counters, K, s)) != MUON_OK) return st;
+  if ((st = launch_counter_reset(counters, 4 * K, s)) != MUON_OK) return st;
   const NesterovArgs na = nesterov_args(w, L, counters, K, A, B, grads, nullptr, gdt, momentum, hp->momentum,
                                         hp->nesterov != 0, hp->eps);
   if ((st = launch_nesterov_norm(&na, 1, s)) != MUON_OK) return st;
@@ -360,7 +392,8 @@ muon_status muon_step_batched(void *const *params, muon_dtype pdt, const void *c
   fin.cautious = hp->cautious_wd ? 1 : 0;
   fin.lr_wd = static_cast<float>(static_cast<double>(hp->lr) * hp->weight_decay);
   fin.lr_scale = static_cast<float>(static_cast<double>(hp->lr) * scale);
-  return run_ns_chain(reinterpret_cast<uint32_t *>(base), w, L, K, hp->ns_steps, hp->coeffs, fin, s);
+  return run_ns_chain(reinterpret_cast<uint32_t *>(base), w, L, K, hp->ns_steps, hp->coeffs, fin, s, counters,
+                      static_cast<uint32_t>(na.tiles_r * na.tiles_c));
 }
 
 static muon_status check_bucket(const muon_bucket &b) {
@@ -454,24 +487,15 @@ static muon_status enqueue_grouped(const muon_bucket *buckets, int n, const muon
     const SmallNsArgs sa = small_args(err, w[i], L[i], buckets[i].K, hp->ns_steps, hp->coeffs, final_spec(buckets[i]));
     if ((st = launch_ns_small(sa, s)) != MUON_OK) return st;
   }
-  // Counter dependencies pay where launch boundaries are a visible share of the chain: launches of a few
-  // hundred microseconds at most. Measured: GPT-2-small step 1.525 -> 1.457 ms and the 256-wide aspect set
-  // 1.86 -> 1.80 ms with them, but the Llama-3-8B set (launches of milliseconds) 325 -> 355 ms, so not there.
-  bool deps = g_counter_deps == 1;
-  if (g_counter_deps == -1) {
-    double est_us = 0.0;   // the longest step kind's launch: 0.33 us per 64-deep k-step of a tile pair
-    for (int kind = EPI_GRAM; kind <= EPI_APPLY; ++kind) {
-      double kiters = 0.0;
-      for (int i = 0; i < n; ++i) {
-        if (small[i]) continue;
-        const long long m = L[i].m, nn = L[i].n;
-        const long long k = (kind == EPI_GRAM ? nn + 63 : m + 63) / 64;
-        kiters += static_cast<double>(buckets[i].K) * gemm_signals_per_matrix(kind, m, nn) / (2 * 8) * k;
-      }
-      est_us = std::max(est_us, kiters * 0.33 / std::max(1, device_sm_count() / 2));
-    }
-    deps = est_us <= 500.0;
+  // per-matrix counter dependencies where the launches (all buckets of a step kind in one) are short
+  double est_us = 0.0;
+  for (int kind = EPI_GRAM; kind <= EPI_APPLY; ++kind) {
+    double us = 0.0;
+    for (int i = 0; i < n; ++i)
+      if (!small[i]) us += launch_estimate_us(kind, L[i].m, L[i].n, buckets[i].K);
+    est_us = std::max(est_us, us);
   }
+  const bool deps = counter_deps_for(est_us);
   // the Newton-Schulz chain of the other buckets, each step kind of all of them in one grouped launch
   for (int t = 0; t < hp->ns_steps; ++t) {
     const float a = hp->coeffs[3 * t], b = hp->coeffs[3 * t + 1], c = hp->coeffs[3 * t + 2];
@@ -540,7 +564,7 @@ muon_status ns_orthogonalize(const void *x, muon_dtype xdt, void *out, muon_dtyp
   char *base = static_cast<char *>(ws);
   char *w = base + header_bytes(K);
   unsigned *counters = reinterpret_cast<unsigned *>(base + CTRL_BYTES);
-  if ((st = launch_counter_reset(counters, K, s)) != MUON_OK) return st;
+  if ((st = launch_counter_reset(counters, 4 * K, s)) != MUON_OK) return st;
   const NesterovArgs na = nesterov_args(w, L, counters, K, A, B, nullptr, x, xdt, nullptr, 0.f, false, eps);
   if ((st = launch_nesterov_norm(&na, 1, s)) != MUON_OK) return st;
   FinalSpec fin{};
@@ -549,7 +573,8 @@ muon_status ns_orthogonalize(const void *x, muon_dtype xdt, void *out, muon_dtyp
   fin.dtype = odt;
   fin.transposed = na.transposed;
   fin.orig_cols = static_cast<int>(B);
-  return run_ns_chain(reinterpret_cast<uint32_t *>(base), w, L, K, ns_steps, coeffs, fin, s);
+  return run_ns_chain(reinterpret_cast<uint32_t *>(base), w, L, K, ns_steps, coeffs, fin, s, counters,
+                      static_cast<uint32_t>(na.tiles_r * na.tiles_c));
 }
 
 // Validates AdamW hyperparameters and derives the kernel constants.

@@ -1206,30 +1206,31 @@ muon_status GemmBatch::launch(cudaStream_t s) {
 }
 
 muon_status launch_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long ldg, long long mstride_g, float alpha,
-                        const float *scale, uint32_t *err, unsigned long long timeout_ns, cudaStream_t s) {
+                        const float *scale, uint32_t *err, unsigned long long timeout_ns, cudaStream_t s,
+                        const TileSync *sync) {
   GemmBatch bt(EPI_GRAM, err, timeout_ns);
-  muon_status st = bt.add_gram(x, g, ldg, mstride_g, alpha, scale);
+  muon_status st = bt.add_gram(x, g, ldg, mstride_g, alpha, scale, sync);
   return st != MUON_OK ? st : bt.launch(s);
 }
 
 muon_status launch_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float a, float b,
-                        float c, uint32_t *err, unsigned long long timeout_ns, cudaStream_t s) {
+                        float c, uint32_t *err, unsigned long long timeout_ns, cudaStream_t s, const TileSync *sync) {
   GemmBatch bt(EPI_POLY, err, timeout_ns);
-  muon_status st = bt.add_poly(g, h, ldh, mstride_h, a, b, c);
+  muon_status st = bt.add_poly(g, h, ldh, mstride_h, a, b, c, sync);
   return st != MUON_OK ? st : bt.launch(s);
 }
 
 muon_status launch_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, const float *scale,
-                         uint32_t *err, unsigned long long timeout_ns, cudaStream_t s) {
+                         uint32_t *err, unsigned long long timeout_ns, cudaStream_t s, const TileSync *sync) {
   GemmBatch bt(EPI_APPLY, err, timeout_ns);
-  muon_status st = bt.add_apply(h, x, out, scale);
+  muon_status st = bt.add_apply(h, x, out, scale, sync);
   return st != MUON_OK ? st : bt.launch(s);
 }
 
 muon_status launch_final(const Bf16Stack &h, const Bf16Stack &x, const float *scale, const FinalSpec &f,
-                         uint32_t *err, unsigned long long timeout_ns, cudaStream_t s) {
+                         uint32_t *err, unsigned long long timeout_ns, cudaStream_t s, const TileSync *sync) {
   GemmBatch bt(EPI_FINAL, err, timeout_ns);
-  muon_status st = bt.add_final(h, x, scale, f);
+  muon_status st = bt.add_final(h, x, scale, f, sync);
   return st != MUON_OK ? st : bt.launch(s);
 }
 
