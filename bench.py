@@ -654,6 +654,7 @@ def run_ns_sweep(args):
     coeffs = [workloads.CLASSIC_QUINTIC] * 5
     K = workloads.NS_SWEEP_K
     sizes = [int(v) for v in args.sizes.split(",")] if args.sizes else list(workloads.NS_SWEEP_SIZES)
+    L.muon_debug_counter_deps(args.counter_deps)
     for n in sizes:
         x = workloads.ns_sweep_input(n, K, 0, device="cuda:0")
         out = torch.empty_like(x)
@@ -708,6 +709,8 @@ def main():
     ap.add_argument("--sizes", default="", help="comma-separated n for --ns-sweep")
     ap.add_argument("--small-sweep", action="store_true", help="fused small-matrix chain vs separate launches")
     ap.add_argument("--config-sweep", action="store_true", help="the step on the tiny, aspect and Llama-3-8B sets")
+    ap.add_argument("--counter-deps", type=int, choices=[-1, 0, 1], default=-1,
+                    help="--ns-sweep: chain launches wait per matrix (1), per grid (0), or as the library decides (-1)")
     args = ap.parse_args()
     if args.ns_sweep:
         return run_ns_sweep(args)
