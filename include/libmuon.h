@@ -77,7 +77,9 @@ typedef struct {
 
 /* Bytes of workspace muon_step_batched / ns_orthogonalize need for a (K, A, B) stack.
  * Layout (all sections 1024-byte aligned): a header of a 256-byte control block (error word)
- * and K 32-bit counters, which every call clears itself before its first launch; then K fp32
+ * and 4*K 32-bit counters (the norm pass's per-matrix tile count, and the readiness of each
+ * matrix's Gram, polynomial and iterate, through which the Newton-Schulz launches can wait per
+ * matrix instead of per launch), which every call clears itself before its first launch; then K fp32
  * norm scales, per-tile norm partial sums, two bf16 iterates of (K, min, max) with rows
  * padded to a multiple of 8 elements, and two bf16 (K, min, min) Gram buffers.
  * Returns 0 if K, A or B is not positive. */
@@ -114,7 +116,7 @@ typedef struct {
                                * optimizer's memory budget": fp32 master weights beside bf16 weights) */
 } muon_bucket;
 
-/* Workspace bytes for muon_step_grouped: one header (control block and one counter per matrix of all
+/* Workspace bytes for muon_step_grouped: one header (control block and four counters per matrix of all
  * buckets), then each bucket's sections as muon_workspace_bytes lays them out.
  * Returns 0 if n < 1, buckets is null or a dimension is not positive. */
 size_t muon_workspace_bytes_grouped(const muon_bucket *buckets, int n);
