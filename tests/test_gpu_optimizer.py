@@ -161,3 +161,37 @@ def test_master_weights_option(L):
                                         eps=a.eps, weight_decay=a.weight_decay, param_dtype="f32")
         assert np.all(np.abs(f64(master) - ref) <= 1e-6 * (np.abs(before[i]) + a.lr))
         assert torch.equal(p, master.to(torch.bfloat16))
+
+
+def test_several_groups_equal_one_optimizer_per_group(L):
+    """Two Muon groups (different lr and decay) and two AdamW groups (with and without decay) in one optimizer:
+    the step issues muon_step_grouped for the first Muon group and one hybrid_step for the second with every
+    AdamW tensor. Groups are independent, so each parameter must end bit for bit where one optimizer per
+    group puts it."""
+    from adamw_hybrid_optimizer_gb300.optim import HybridMuonAdamW
+    gen = torch.Generator().manual_seed(77)
+    shapes = {"m1": [(256, 512), (256, 512)], "m2": [(768, 768), (512, 256)], "a1": [(5000,)], "a2": [(768,), (33,)]}
+    init = {k: [(torch.randn(s, generator=gen) * 1e-2).to(torch.bfloat16) for s in v] for k, v in shapes.items()}
+    grads = [{k: [(torch.randn(s, generator=gen) * 1e-3).to(torch.bfloat16) for s in v] for k, v in shapes.items()}
+             for _ in range(3)]
+    spec = {"m1": {"kind": "muon", "lr": 0.02, "weight_decay": 0.01},
+            "m2": {"kind": "muon", "lr": 0.01, "weight_decay": 0.0, "cautious_wd": True},
+            "a1": {"kind": "adamw", "lr": 3e-4, "weight_decay": 0.1},
+            "a2": {"kind": "adamw", "lr": 1e-3, "weight_decay": 0.0}}
+
+    def run(keys):
+        ps = {k: [t.clone().to(DEV) for t in init[k]] for k in keys}
+        opt = HybridMuonAdamW([dict(spec[k], params=ps[k]) for k in keys])
+        for g in grads:
+            for k in keys:
+                for p, gr in zip(ps[k], g[k]):
+                    p.grad = gr.to(DEV)
+            opt.step()
+        torch.cuda.synchronize()
+        return ps
+
+    together = run(["m1", "m2", "a1", "a2"])
+    for k in shapes:
+        alone = run([k])[k]
+        for a, b in zip(together[k], alone):
+            assert torch.equal(a, b), k
