@@ -142,6 +142,89 @@ __device__ __forceinline__ float nesterov_tile(const NesterovArgs &a, long long 
   return ss;
 }
 
+// As nesterov_tile for a matrix stored wide (not transposed), on a tile of 64 rows x 256 columns: thread
+// (tx, ty) handles columns 4*tx..4*tx+3 of rows ty, ty+4, .., ty+60, four rows at a time, so that a warp
+// covers 128 consecutive columns of one row. Returns the thread's sum of U^2.
+template <typename GT, bool MOMENTUM>
+__device__ __forceinline__ float nesterov_tile_wide(const NesterovArgs &a, long long b, int tr, int tc) {
+  constexpr int TR = NESTEROV_TILE, TC = NESTEROV_WIDE_TILE;
+  const long long mat = static_cast<long long>(a.A) * a.B;
+  const GT *g = a.gptrs != nullptr ? static_cast<const GT *>(a.gptrs[b])
+                                   : static_cast<const GT *>(a.gbase) + b * mat;
+  float *M = MOMENTUM ? a.momentum + b * mat : nullptr;
+  __nv_bfloat16 *u = a.u + b * a.mstride_u;
+  const int tx = threadIdx.x & 63;
+  const int ty = threadIdx.x >> 6;
+  const int c0 = tc * TC + tx * 4;
+  const bool vec = (a.B % 4 == 0) && (c0 + 4 <= a.B) &&
+                   ((reinterpret_cast<uintptr_t>(g) & (4 * sizeof(GT) - 1)) == 0) &&
+                   (!MOMENTUM || (reinterpret_cast<uintptr_t>(M) & 15) == 0);
+  float ss = 0.f;
+#pragma unroll 1
+  for (int p0 = 0; p0 < TR / 4; p0 += 4) {
+#pragma unroll
+    for (int p = p0; p < p0 + 4; ++p) {
+      const int r = tr * TR + ty + 4 * p;
+      if (r >= a.A || c0 >= a.B) continue;
+      const long long base = static_cast<long long>(r) * a.B + c0;
+      float gv[4], mv[4], uv[4];
+      if (vec) {
+        if constexpr (sizeof(GT) == 4) {
+          const float4 q = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(g) + base);
+          gv[0] = q.x; gv[1] = q.y; gv[2] = q.z; gv[3] = q.w;
+        } else {
+          const uint2 q = *reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(g) + base);
+          const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&q.x));
+          const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&q.y));
+          gv[0] = lo.x; gv[1] = lo.y; gv[2] = hi.x; gv[3] = hi.y;
+        }
+        if constexpr (MOMENTUM) {
+          const float4 q = *reinterpret_cast<const float4 *>(M + base);
+          mv[0] = q.x; mv[1] = q.y; mv[2] = q.z; mv[3] = q.w;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const bool in = c0 + q < a.B;
+          gv[q] = in ? ld_f(g, base + q) : 0.f;
+          mv[q] = (MOMENTUM && in) ? M[base + q] : 0.f;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if constexpr (MOMENTUM) {
+          const float mn = fmaf(a.mu, mv[q], gv[q]);
+          mv[q] = mn;
+          uv[q] = a.nesterov ? fmaf(a.mu, mn, gv[q]) : mn;
+        } else {
+          uv[q] = gv[q];
+        }
+        if (c0 + q >= a.B) uv[q] = 0.f;
+        ss = fmaf(uv[q], uv[q], ss);
+      }
+      if constexpr (MOMENTUM) {
+        if (vec) {
+          *reinterpret_cast<float4 *>(M + base) = make_float4(mv[0], mv[1], mv[2], mv[3]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (c0 + q < a.B) M[base + q] = mv[q];
+        }
+      }
+      __nv_bfloat16 *dst = u + static_cast<long long>(r) * a.ldu + c0;
+      if (c0 + 4 <= a.B) {
+        __nv_bfloat162 w[2] = {__floats2bfloat162_rn(uv[0], uv[1]), __floats2bfloat162_rn(uv[2], uv[3])};
+        *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<uint2 *>(w);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (c0 + q < a.B) dst[q] = __float2bfloat16_rn(uv[q]);
+      }
+    }
+  }
+  return ss;
+}
+
 // One launch over the tiles of every matrix of up to NESTEROV_MAX_PROBLEMS stacks (blocks in problem order,
 // within a problem matrix by matrix). Each block stores its tile's sum of U^2 and counts itself in the
 // matrix's counter; the block that completes the count sums the matrix's tile sums in index order (the
@@ -162,8 +245,13 @@ __global__ void __launch_bounds__(256) nesterov_norm_kernel(const __grid_constan
   const long long t = local - b * tiles;
   const int tr = static_cast<int>(t / a.tiles_c);
   const int tc = static_cast<int>(t - static_cast<long long>(tr) * a.tiles_c);
-  float ss = a.gdtype == MUON_F32 ? nesterov_tile<float, MOMENTUM>(a, b, tr, tc, tile)
-                                  : nesterov_tile<__nv_bfloat16, MOMENTUM>(a, b, tr, tc, tile);
+  float ss;
+  if (a.wide_tiles && !a.transposed)
+    ss = a.gdtype == MUON_F32 ? nesterov_tile_wide<float, MOMENTUM>(a, b, tr, tc)
+                              : nesterov_tile_wide<__nv_bfloat16, MOMENTUM>(a, b, tr, tc);
+  else
+    ss = a.gdtype == MUON_F32 ? nesterov_tile<float, MOMENTUM>(a, b, tr, tc, tile)
+                              : nesterov_tile<__nv_bfloat16, MOMENTUM>(a, b, tr, tc, tile);
   ss = warp_sum(ss);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
