@@ -124,7 +124,10 @@ size_t muon_workspace_bytes_grouped(const muon_bucket *buckets, int n);
 /* One Muon step on n same-shape stacks at once, all with the same hyperparameters: the computation of
  * muon_step_batched on each bucket, with every Newton-Schulz step kind of all buckets issued as one
  * grouped tensor-core launch ([P4] section 2.2, batching matrices of similar shapes; [P1] the stacked
- * (K, ...) Muon groups). Results are identical to n muon_step_batched calls.
+ * (K, ...) Muon groups). Results are identical to n muon_step_batched calls. Where the launches are short
+ * (muon_debug_counter_deps), each waits per matrix on counters in the workspace header that its
+ * predecessor raises, rather than on the whole predecessor, so consecutive launches overlap; this
+ * changes no result.
  *   buckets   HOST array of n bucket descriptors (1 <= n <= 4096).
  *   ws        device workspace of ws_bytes >= muon_workspace_bytes_grouped(buckets, n), 256-byte aligned,
  *             zero-filled before its first use; its first 256 bytes are the control block muon_check reads.
