@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <mutex>
 #include <map>
@@ -79,7 +80,7 @@ cudaEvent_t take_event() {
 unsigned long long g_timeout_ns = 2000000000ull;
 // grouped chain: per-matrix counter dependencies between launches: -1 where the rule in enqueue_grouped
 // allows them, 0 never, 1 always
-int g_counter_deps = -1;
+std::atomic<int> g_counter_deps{-1};
 
 }  // namespace
 
@@ -300,7 +301,10 @@ double launch_estimate_us(int kind, long long m, long long n, long long K) {
 // They pay where launch boundaries are a visible share of the chain: launches of a few hundred
 // microseconds at most. Measured: GPT-2-small step 1.525 -> 1.457 ms and the 256-wide aspect set
 // 1.86 -> 1.80 ms with them, but the Llama-3-8B set (launches of milliseconds) 325 -> 355 ms.
-bool counter_deps_for(double est_us) { return g_counter_deps == 1 || (g_counter_deps == -1 && est_us <= 500.0); }
+bool counter_deps_for(double est_us) {
+  const int mode = g_counter_deps.load();
+  return mode == 1 || (mode == -1 && est_us <= 500.0);
+}
 
 // The Newton-Schulz chain of one stack. counters: the workspace's four counters per matrix (the norm
 // pass's, then the readiness of G, H and X), zeroed by the caller before the norm pass; norm_tiles: the
@@ -720,7 +724,7 @@ void muon_autotune_reset(void) { poly_shape_clear(); }
 
 muon_status muon_debug_counter_deps(int32_t on) {
   if (on < -1 || on > 1) return MUON_ERR_INVALID_ARG;
-  g_counter_deps = on;
+  g_counter_deps.store(on);
   return MUON_OK;
 }
 
