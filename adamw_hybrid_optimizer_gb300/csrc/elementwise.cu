@@ -285,12 +285,15 @@ __global__ void __launch_bounds__(256) nesterov_norm_kernel(const __grid_constan
 
 // Zeroes n counters. It lets its successor launch at once, but finishes only after its predecessor
 // has: a successor that waits for this grid so also waits for everything before it.
-__global__ void __launch_bounds__(256) counter_reset_kernel(unsigned *counters, long long n) {
+__global__ void __launch_bounds__(256) counter_reset_kernel(unsigned *counters, long long n, unsigned *counters2,
+                                                             long long n2) {
   if (threadIdx.x == 0) pdl_launch_dependents();
   pdl_wait();
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += static_cast<long long>(gridDim.x) * blockDim.x)
-    counters[i] = 0u;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n + n2;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    if (i < n) counters[i] = 0u;
+    else counters2[i - n] = 0u;
+  }
 }
 
 // ------------------------------------------------------------------------------------------ AdamW
@@ -424,12 +427,14 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 }  // namespace
 
-muon_status launch_counter_reset(unsigned *counters, long long n, cudaStream_t s) {
-  if (n < 1) return MUON_OK;
-  const long long blocks = std::min<long long>((n + 255) / 256, device_sm_count());
+muon_status launch_counter_reset(unsigned *counters, long long n, cudaStream_t s, unsigned *counters2, long long n2) {
+  if (counters2 == nullptr || n2 < 0) n2 = 0;
+  if (n < 0) n = 0;
+  if (n + n2 < 1) return MUON_OK;
+  const long long blocks = std::min<long long>((n + n2 + 255) / 256, device_sm_count());
   launch_begin(KK_COUNTER_RESET, s);
   const cudaError_t e = launch_pdl(counter_reset_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
-                                   counters, n);
+                                   counters, n, counters2, n2);
   launch_end(s);
   return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
 }

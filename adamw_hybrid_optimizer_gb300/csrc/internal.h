@@ -221,7 +221,8 @@ static_assert(sizeof(NesterovGroup) <= 4096, "kernel parameter block too large")
 // allow. The counters must be zero when the call's launches start; they are left at the tile counts.
 muon_status launch_nesterov_norm(const NesterovArgs *probs, int n, cudaStream_t s);
 // Zeroes n counters in stream order (a kernel, so that the launches around it keep overlapping).
-muon_status launch_counter_reset(unsigned *counters, long long n, cudaStream_t s);
+muon_status launch_counter_reset(unsigned *counters, long long n, cudaStream_t s, unsigned *counters2 = nullptr,
+                                 long long n2 = 0);
 
 struct AdamwConst {
   int l2;               // 1: g <- g + l2_wd * p before the moments (Adam with L2); 0: decoupled decay

@@ -446,7 +446,7 @@ static muon_status check_grouped(const muon_bucket *buckets, int n, const muon_h
 
 // The launches of one grouped Muon step, on stream s (arguments already checked).
 static muon_status enqueue_grouped(const muon_bucket *buckets, int n, const muon_hparams *hp, void *ws,
-                                   cudaStream_t s) {
+                                   cudaStream_t s, unsigned *extra_zero = nullptr, long long extra_n = 0) {
   muon_status st;
   char *base = static_cast<char *>(ws);
   uint32_t *err = reinterpret_cast<uint32_t *>(base);
@@ -466,7 +466,8 @@ static muon_status enqueue_grouped(const muon_bucket *buckets, int n, const muon
   // grow during a step (t-th launch of a kind: target t times its per-launch count) and start at zero
   uint32_t *G_ready = counters + total_K, *H_ready = counters + 2 * total_K, *X_ready = counters + 3 * total_K;
   // momentum, Nesterov input, norm: all buckets in one pass
-  if ((st = launch_counter_reset(counters, 4 * total_K, s)) != MUON_OK) return st;
+  // (extra_zero: more counters to clear in the same launch, for a call that follows this chain)
+  if ((st = launch_counter_reset(counters, 4 * total_K, s, extra_zero, extra_n)) != MUON_OK) return st;
   std::vector<NesterovArgs> na(n);
   for (long long i = 0, k0 = 0; i < n; k0 += buckets[i].K, ++i) {
     const muon_bucket &bk = buckets[i];
@@ -835,9 +836,14 @@ muon_status hybrid_step(const muon_bucket *buckets, int nb, const muon_hparams *
   if ((st = check_device()) != MUON_OK) return st;
   number_adamw_chunks(groups);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (nb > 0 && (st = enqueue_grouped(buckets, nb, hp, ws, s)) != MUON_OK) return st;
+  // with both parts, the AdamW chunk counters are cleared by the Muon step's own counter reset
+  const long long adamw_words =
+      nt > 0 ? static_cast<long long>(groups.size() * ADAMW_REGION_BYTES / sizeof(unsigned)) : 0;
+  if (nb > 0 && (st = enqueue_grouped(buckets, nb, hp, ws, s, static_cast<unsigned *>(adamw_ws), adamw_words)) !=
+                    MUON_OK)
+    return st;
   if (nt > 0) {
-    if ((st = reset_adamw_regions(adamw_ws, groups.size(), s)) != MUON_OK) return st;
+    if (nb == 0 && (st = reset_adamw_regions(adamw_ws, groups.size(), s)) != MUON_OK) return st;
     for (const AdamwGroup &G : groups)
       if ((st = launch_adamw_grouped(G, s)) != MUON_OK) return st;
   }
