@@ -14,14 +14,16 @@
 // paired-SM MMAs (tcgen05 cta_group::2, M = 256): each CTA holds its 128 rows of A and one half of B, the
 // even CTA issues the MMAs, and each CTA's tensor memory receives its own 128 accumulator rows (2 x 256
 // fp32 columns, so the epilogue of one tile overlaps the MMAs of the next). Operands arrive by TMA
-// (128-byte swizzle) through a ring of 64-deep stages of 32 KB per CTA (6 stages; POLY with a short
-// contraction: 4 stages and a 5-slot input ring). The CTAs are persistent (one per SM) and stride over
-// the tiles of up to GEMM_MAX_PROBLEMS stacks at once. Warp roles: warp 0 = TMA producer, warp 1 = MMA
-// issuer (and TMEM owner), warps 2-9 = epilogue (two per tensor-memory lane quarter, each taking one
-// 32-column half of every 64-column slot), warp 10 = epilogue loader (POLY: TMA of G's tile into the
-// ring; FINAL: L2 prefetch of the parameters a tile ahead). Each epilogue warp reshapes its results in
-// shared memory so that global stores (and the final step's parameter loads, fetched one chunk ahead)
-// are coalesced 16-byte accesses; transposed outputs go through shared memory.
+// (128-byte swizzle) through a ring of 64-deep stages of 32 KB per CTA (6 stages; POLY in three splits of
+// stages and epilogue input slots, picked by a measured autotune or by the contraction depth). The CTAs are
+// persistent (one per SM) and stride over the tiles of up to GEMM_MAX_PROBLEMS stacks at once. Warp roles:
+// warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner), warps 2-9 = epilogue (two per
+// tensor-memory lane quarter, each taking one 32-column half of every 64-column slot), warp 10 = loader
+// (POLY: TMA of G's tile into the ring; FINAL: L2 prefetch of the parameters a tile ahead), warp 11 =
+// readiness signals (TileSync: per-matrix counters that let consecutive launches overlap). Each epilogue
+// warp reshapes its results in shared memory so that global stores (and the final step's parameter loads,
+// fetched one chunk ahead) are coalesced 16-byte accesses; transposed outputs are transposed in place
+// there (ldmatrix.trans / stmatrix).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
