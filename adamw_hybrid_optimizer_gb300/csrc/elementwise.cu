@@ -2,12 +2,16 @@
 //
 //   nesterov_norm_kernel  momentum M <- mu M + G, Nesterov input U = G + mu M (or M), U stored bf16 in
 //                         the wide orientation, and the Frobenius scale s_k = 1 / (||U_k||_F + eps)
-//                         from per-tile sums of U^2 added in a fixed order by the matrix's last tile
+//                         from per-tile sums of U^2 added in a fixed order by the matrix's last tile,
+//                         which then counts the matrix as ready for the chain
 //                         ("Optimizers: AdamW, Muon and the distributed optimizer", section "Muon:
 //                         orthogonalising the update": the momentum rule and newton_schulz's first lines).
-//   counter_reset_kernel  zeroes the per-matrix counters nesterov_norm_kernel counts its tiles in.
+//   counter_reset_kernel  zeroes counters in stream order: the norm pass's and the chain's per-matrix
+//                         counters, and the grouped AdamW pass's chunk counter.
 //   adamw kernels         AdamW with bias correction and decoupled decay (same page, section "AdamW:
-//                         decoupled weight decay"), 16-byte vector accesses when aligned.
+//                         decoupled weight decay"), or Adam with L2, 16-byte vector accesses when aligned:
+//                         one tensor per launch (adamw_kernel, adamw_master_kernel) or many, warps taking
+//                         element chunks from a counter (adamw_grouped_kernel).
 //   debug_wait_kernel     one bounded wait on a barrier nothing completes.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
