@@ -205,3 +205,26 @@ def test_aspect_polar_express_cautious_sampled(L):
     w = workloads.workload("aspect")
     for b, (shape, members) in enumerate([((256, 16384), list(range(16))), ((16384, 256), list(range(16, 32)))]):
         _run_bucket(L, w, shape, members, 3, sample=workloads.bucket_sample(16, w.cfg_id, b))
+
+
+@pytest.mark.parametrize("K,A,B", [(4, 256, 512), (3, 640, 256), (2, 1024, 1024)])
+def test_ns_orthogonalize_scheduling_modes_agree(L, K, A, B):
+    """The single-stack chain's launches wait per matrix on readiness counters (1) or on their whole
+    predecessor (0): the tiles are computed the same way, so the outputs must agree bit for bit (the default
+    rule is compared with the oracle above)."""
+    gen = torch.Generator().manual_seed(A + B + K)
+    x = torch.randn((K, A, B), generator=gen).to(torch.bfloat16).to(DEV)
+    outs = []
+    try:
+        for mode in (1, 0):
+            L.muon_debug_counter_deps(mode)
+            ws = workspace(L, K, A, B)
+            out = torch.empty((K, A, B), dtype=torch.float32, device=DEV)
+            L.ns_orthogonalize(x, out, CLASSIC5, 1e-7, ws)
+            torch.cuda.synchronize()
+            assert L.muon_check(ws) == L.MUON_OK
+            outs.append(out)
+    finally:
+        L.muon_debug_counter_deps(-1)
+    assert torch.isfinite(outs[0]).all()
+    assert torch.equal(outs[0], outs[1])
