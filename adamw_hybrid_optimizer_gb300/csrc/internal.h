@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cmath>
+
 #include "../../include/libmuon.h"
 
 namespace muon {
@@ -217,6 +219,84 @@ struct NesterovGroup {
   int nprob;
 };
 static_assert(sizeof(NesterovGroup) <= 4096, "kernel parameter block too large");
+
+// ------------------------------------------------------------------------------------------ workspace layout
+//
+// A workspace (the caller's, or the no-allocation entry point's static scratch) starts with a header: the
+// control block (error word at byte 0) and four 32-bit counters per matrix of the call (the norm pass's tile
+// count, then the readiness of each matrix's G, H and iterate X), which every call zeroes before its first
+// launch. Each stack's sections follow, stack after stack; their offsets are relative to the stack's start.
+constexpr size_t CTRL_BYTES = 256;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline long long round8(long long v) { return (v + 7) / 8 * 8; }
+inline size_t header_bytes(long long total_K) {
+  return align_up(CTRL_BYTES + static_cast<size_t>(total_K) * 16, 1024);
+}
+
+// One stack's sections (1024-byte aligned): K fp32 scales, the norm pass's per-tile partial sums, two bf16
+// iterates (K, m, ldx) and two bf16 (K, m, ldg) buffers for G and H; m = min(A, B), n = max(A, B), rows padded
+// to a multiple of 8 elements (16 bytes, as TMA requires).
+struct Layout {
+  long long m, n, ldx, ldg, tiles_r, tiles_c;
+  size_t scale, partial, x0, x1, g, h, total;
+};
+
+inline Layout layout(long long K, long long A, long long B) {
+  Layout L{};
+  L.m = A < B ? A : B;
+  L.n = A < B ? B : A;
+  L.ldx = round8(L.n);
+  L.ldg = round8(L.m);
+  L.tiles_r = (A + NESTEROV_TILE - 1) / NESTEROV_TILE;
+  L.tiles_c = (B + NESTEROV_TILE - 1) / NESTEROV_TILE;
+  size_t off = 0;
+  L.scale = off;
+  off = align_up(off + static_cast<size_t>(K) * 4, 1024);
+  L.partial = off;
+  off = align_up(off + static_cast<size_t>(K) * L.tiles_r * L.tiles_c * 4, 1024);
+  L.x0 = off;
+  off = align_up(off + static_cast<size_t>(K) * L.m * L.ldx * 2, 1024);
+  L.x1 = off;
+  off = align_up(off + static_cast<size_t>(K) * L.m * L.ldx * 2, 1024);
+  L.g = off;
+  off = align_up(off + static_cast<size_t>(K) * L.m * L.ldg * 2, 1024);
+  L.h = off;
+  off = align_up(off + static_cast<size_t>(K) * L.m * L.ldg * 2, 1024);
+  L.total = off;
+  return L;
+}
+
+// ------------------------------------------------------------------------------------------ argument checks
+
+inline bool valid_dtype(int d) { return d == MUON_F32 || d == MUON_BF16; }
+
+inline muon_status check_stack_dims(int64_t K, int64_t A, int64_t B) {
+  if (K < 1 || A < 1 || B < 1) return MUON_ERR_INVALID_ARG;
+  if (A > 65536 || B > 65536 || K > (1ll << 31)) return MUON_ERR_SHAPE;
+  const long double elems = static_cast<long double>(K) * A * B;
+  if (elems >= static_cast<long double>(1ll << 40)) return MUON_ERR_SHAPE;
+  return MUON_OK;
+}
+
+inline muon_status check_coeffs(int ns_steps, const float *coeffs) {
+  if (ns_steps < 1 || ns_steps > MUON_MAX_NS_STEPS || coeffs == nullptr) return MUON_ERR_INVALID_ARG;
+  for (int i = 0; i < 3 * ns_steps; ++i)
+    if (!std::isfinite(coeffs[i])) return MUON_ERR_INVALID_ARG;
+  return MUON_OK;
+}
+
+// Every check of ns_orthogonalize's arguments but the workspace's.
+inline muon_status check_ns_args(const void *x, int xdt, const void *out, int odt, int64_t K, int64_t A, int64_t B,
+                                 int ns_steps, const float *coeffs, float eps) {
+  if (x == nullptr || out == nullptr) return MUON_ERR_INVALID_ARG;
+  muon_status st = check_stack_dims(K, A, B);
+  if (st != MUON_OK) return st;
+  if (!valid_dtype(xdt) || !valid_dtype(odt)) return MUON_ERR_DTYPE;
+  if ((st = check_coeffs(ns_steps, coeffs)) != MUON_OK) return st;
+  if (!std::isfinite(eps) || eps < 0.f) return MUON_ERR_INVALID_ARG;
+  return MUON_OK;
+}
 // All n stacks (all with momentum or all without) in as few launches as the grid and the problem table
 // allow. The counters must be zero when the call's launches start; they are left at the tile counts.
 muon_status launch_nesterov_norm(const NesterovArgs *probs, int n, cudaStream_t s);

@@ -168,48 +168,6 @@ namespace {
 
 // ------------------------------------------------------------------------------------------ workspace
 
-constexpr size_t CTRL_BYTES = 256;
-
-size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-long long round8(long long v) { return (v + 7) / 8 * 8; }
-
-// A workspace starts with a header: the control block (error word at byte 0) and one counter per matrix
-// of the call, which the call zeroes before its first launch. Each stack's sections follow, stack after
-// stack; their offsets below are relative to the stack's own start.
-// Control block, then four counters per matrix: the norm pass's tile count and the grouped chain's
-// per-matrix readiness counters of G, H and the iterate X (TileSync).
-size_t header_bytes(long long total_K) { return align_up(CTRL_BYTES + static_cast<size_t>(total_K) * 16, 1024); }
-
-struct Layout {
-  long long m, n, ldx, ldg, tiles_r, tiles_c;
-  size_t scale, partial, x0, x1, g, h, total;
-};
-
-Layout layout(long long K, long long A, long long B) {
-  Layout L{};
-  L.m = A < B ? A : B;
-  L.n = A < B ? B : A;
-  L.ldx = round8(L.n);
-  L.ldg = round8(L.m);
-  L.tiles_r = (A + NESTEROV_TILE - 1) / NESTEROV_TILE;
-  L.tiles_c = (B + NESTEROV_TILE - 1) / NESTEROV_TILE;
-  size_t off = 0;
-  L.scale = off;
-  off = align_up(off + static_cast<size_t>(K) * 4, 1024);
-  L.partial = off;
-  off = align_up(off + static_cast<size_t>(K) * L.tiles_r * L.tiles_c * 4, 1024);
-  L.x0 = off;
-  off = align_up(off + static_cast<size_t>(K) * L.m * L.ldx * 2, 1024);
-  L.x1 = off;
-  off = align_up(off + static_cast<size_t>(K) * L.m * L.ldx * 2, 1024);
-  L.g = off;
-  off = align_up(off + static_cast<size_t>(K) * L.m * L.ldg * 2, 1024);
-  L.h = off;
-  off = align_up(off + static_cast<size_t>(K) * L.m * L.ldg * 2, 1024);
-  L.total = off;
-  return L;
-}
-
 // The Nesterov/norm pass of one stack whose sections start at w; counters: the stack's K header words.
 NesterovArgs nesterov_args(char *w, const Layout &L, unsigned *counters, long long K, long long A, long long B,
                            const void *const *gptrs, const void *gbase, int gdt, float *momentum, float mu,
@@ -241,23 +199,6 @@ NesterovArgs nesterov_args(char *w, const Layout &L, unsigned *counters, long lo
   na.eps = eps;
   na.nesterov = nesterov ? 1 : 0;
   return na;
-}
-
-bool valid_dtype(int d) { return d == MUON_F32 || d == MUON_BF16; }
-
-muon_status check_stack_dims(int64_t K, int64_t A, int64_t B) {
-  if (K < 1 || A < 1 || B < 1) return MUON_ERR_INVALID_ARG;
-  if (A > 65536 || B > 65536 || K > (1ll << 31)) return MUON_ERR_SHAPE;
-  const long double elems = static_cast<long double>(K) * A * B;
-  if (elems >= static_cast<long double>(1ll << 40)) return MUON_ERR_SHAPE;
-  return MUON_OK;
-}
-
-muon_status check_coeffs(int ns_steps, const float *coeffs) {
-  if (ns_steps < 1 || ns_steps > MUON_MAX_NS_STEPS || coeffs == nullptr) return MUON_ERR_INVALID_ARG;
-  for (int i = 0; i < 3 * ns_steps; ++i)
-    if (!std::isfinite(coeffs[i])) return MUON_ERR_INVALID_ARG;
-  return MUON_OK;
 }
 
 // The Newton-Schulz chain on the wide iterate in x0 (unnormalised U; s_k in `scale`) of the stack whose
@@ -560,12 +501,9 @@ muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hpar
 muon_status ns_orthogonalize(const void *x, muon_dtype xdt, void *out, muon_dtype odt, int64_t K, int64_t A,
                              int64_t B, int ns_steps, const float *coeffs, float eps, void *ws, size_t ws_bytes,
                              muon_stream_t stream) {
-  if (x == nullptr || out == nullptr || ws == nullptr) return MUON_ERR_INVALID_ARG;
-  muon_status st = check_stack_dims(K, A, B);
+  if (ws == nullptr) return MUON_ERR_INVALID_ARG;
+  muon_status st = check_ns_args(x, xdt, out, odt, K, A, B, ns_steps, coeffs, eps);
   if (st != MUON_OK) return st;
-  if (!valid_dtype(xdt) || !valid_dtype(odt)) return MUON_ERR_DTYPE;
-  if ((st = check_coeffs(ns_steps, coeffs)) != MUON_OK) return st;
-  if (!std::isfinite(eps) || eps < 0.f) return MUON_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MUON_ERR_ALIGNMENT;
   const Layout L = layout(K, A, B);
   if (ws_bytes < header_bytes(K) + L.total) return MUON_ERR_WORKSPACE;

@@ -8,11 +8,16 @@
 // They pass only their input and output buffers; the scratch lives in this file's static device
 // array, which every GPU that loads this code holds until the process exits.
 //
-// The array is shared by every call on a device and keeps the last call's contents. Each call clears
-// the part that must start at zero (the control block with the error word, and one counter per
-// matrix) with an asynchronous memset, which allocates nothing; every other scratch byte is written
-// before it is read. Calls whose
-// work overlaps on the GPU (different streams, or several host threads) race on the array.
+// The array holds a workspace laid out exactly as ns_orthogonalize's (internal.h: header_bytes and
+// layout), so a stack fits when muon_workspace_bytes(K, A, B) is at most its size. It is shared by every
+// call on a device and keeps the last call's contents. Each call clears the part that must start at zero
+// (the per-matrix counters of the header) with an asynchronous memset, which allocates nothing; every
+// other scratch byte is written before it is read. The error word at its start is sticky: a bounded wait
+// that runs out sets it, and only ns_orthogonalize_noalloc_check reads and clears it. Calls whose work
+// overlaps on the GPU (different streams, or several host threads) race on the array.
+//
+// This path runs the chain as separate launches per step (Gram, polynomial, apply), also for stacks that
+// ns_orthogonalize hands to the fused small-matrix kernel.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -30,8 +35,9 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH
 std::mutex g_noalloc_mu;
 void *g_noalloc_ptr[64] = {};
 
-// Once per device, with that device current: the device address of the scratch array. In host code
-// the array's name is only a host-side stand-in, never a device address.
+// Set-up, once per device, with that device current: the device address of the scratch array (in host
+// code the array's name is only a host-side stand-in, never a device address), and a zeroed control
+// block. The memset is synchronous, so the first call on a device should come before any stream capture.
 muon_status noalloc_scratch(void **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MUON_ERR_CUDA;
@@ -39,46 +45,11 @@ muon_status noalloc_scratch(void **out) {
   if (g_noalloc_ptr[dev] == nullptr) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return MUON_ERR_CUDA;
+    if (cudaMemset(p, 0, CTRL_BYTES) != cudaSuccess) return MUON_ERR_CUDA;
     g_noalloc_ptr[dev] = p;
   }
   *out = g_noalloc_ptr[dev];
   return MUON_OK;
-}
-
-size_t up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-
-struct ScratchLayout {
-  long long m, n, ldx, ldg, tiles_r, tiles_c;
-  size_t counters, scale, partial, x0, x1, g, h, total;
-};
-
-// Control block and per-matrix counters (the zeroed part), then the same sections the workspace of
-// ns_orthogonalize holds.
-ScratchLayout scratch_layout(long long K, long long A, long long B) {
-  ScratchLayout L{};
-  L.m = A < B ? A : B;
-  L.n = A < B ? B : A;
-  L.ldx = (L.n + 7) / 8 * 8;
-  L.ldg = (L.m + 7) / 8 * 8;
-  L.tiles_r = (A + NESTEROV_TILE - 1) / NESTEROV_TILE;
-  L.tiles_c = (B + NESTEROV_TILE - 1) / NESTEROV_TILE;
-  size_t off = 256;
-  L.counters = off;
-  off = up(off + size_t(K) * 4, 1024);
-  L.scale = off;
-  off = up(off + size_t(K) * 4, 1024);
-  L.partial = off;
-  off = up(off + size_t(K) * L.tiles_r * L.tiles_c * 4, 1024);
-  L.x0 = off;
-  off = up(off + size_t(K) * L.m * L.ldx * 2, 1024);
-  L.x1 = off;
-  off = up(off + size_t(K) * L.m * L.ldx * 2, 1024);
-  L.g = off;
-  off = up(off + size_t(K) * L.m * L.ldg * 2, 1024);
-  L.h = off;
-  off = up(off + size_t(K) * L.m * L.ldg * 2, 1024);
-  L.total = off;
-  return L;
 }
 
 }  // namespace
@@ -89,28 +60,26 @@ using namespace muon;
 extern "C" muon_status ns_orthogonalize_noalloc(const void *x, muon_dtype xdt, void *out, muon_dtype odt, int64_t K,
                                                 int64_t A, int64_t B, int ns_steps, const float *coeffs, float eps,
                                                 muon_stream_t stream) {
-  if (x == nullptr || out == nullptr || coeffs == nullptr) return MUON_ERR_INVALID_ARG;
-  if (K < 1 || A < 1 || B < 1) return MUON_ERR_INVALID_ARG;
-  if (A > 65536 || B > 65536 || K > (1ll << 31)) return MUON_ERR_SHAPE;
-  if ((xdt != MUON_F32 && xdt != MUON_BF16) || (odt != MUON_F32 && odt != MUON_BF16)) return MUON_ERR_DTYPE;
-  if (ns_steps < 1 || ns_steps > MUON_MAX_NS_STEPS) return MUON_ERR_INVALID_ARG;
-  for (int i = 0; i < 3 * ns_steps; ++i)
-    if (!(coeffs[i] == coeffs[i]) || coeffs[i] > 3.4e38f || coeffs[i] < -3.4e38f) return MUON_ERR_INVALID_ARG;
-  if (!(eps >= 0.f) || eps > 3.4e38f) return MUON_ERR_INVALID_ARG;
-  // checked in floating point first so that huge stacks cannot overflow the layout arithmetic
-  const long double approx = 4.0L * K * A * B + 4.0L * K * (long double)(A < B ? A : B) * (A < B ? A : B);
-  if (approx > (long double)NOALLOC_SCRATCH_BYTES) return MUON_ERR_WORKSPACE;
-  const ScratchLayout L = scratch_layout(K, A, B);
-  if (L.total > NOALLOC_SCRATCH_BYTES) return MUON_ERR_WORKSPACE;
-  muon_status st = device_check();
+  muon_status st = check_ns_args(x, xdt, out, odt, K, A, B, ns_steps, coeffs, eps);
   if (st != MUON_OK) return st;
+  // the bound in floating point first, so that huge stacks cannot overflow the layout arithmetic
+  const long double mn = static_cast<long double>(A < B ? A : B);
+  if (4.0L * K * A * B + 4.0L * K * mn * mn > static_cast<long double>(NOALLOC_SCRATCH_BYTES))
+    return MUON_ERR_WORKSPACE;
+  const Layout L = layout(K, A, B);
+  const size_t hdr = header_bytes(K);
+  if (hdr + L.total > NOALLOC_SCRATCH_BYTES) return MUON_ERR_WORKSPACE;
+  if ((st = device_check()) != MUON_OK) return st;
   void *scratch = nullptr;
   if ((st = noalloc_scratch(&scratch)) != MUON_OK) return st;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  char *w = static_cast<char *>(scratch);
-  uint32_t *err = reinterpret_cast<uint32_t *>(w);
-  if (cudaMemsetAsync(w, 0, L.scale, s) != cudaSuccess) return MUON_ERR_CUDA;
+  char *base = static_cast<char *>(scratch);
+  uint32_t *err = reinterpret_cast<uint32_t *>(base);
+  unsigned *counters = reinterpret_cast<unsigned *>(base + CTRL_BYTES);
+  char *w = base + hdr;
+  // the per-matrix counters start at zero; the error word (sticky) is left alone
+  if (cudaMemsetAsync(counters, 0, hdr - CTRL_BYTES, s) != cudaSuccess) return MUON_ERR_CUDA;
 
   NesterovArgs na{};
   na.gptrs = nullptr;
@@ -122,7 +91,7 @@ extern "C" muon_status ns_orthogonalize_noalloc(const void *x, muon_dtype xdt, v
   na.mstride_u = L.m * L.ldx;
   na.partials = reinterpret_cast<float *>(w + L.partial);
   na.scale = reinterpret_cast<float *>(w + L.scale);
-  na.counters = reinterpret_cast<unsigned *>(w + L.counters);
+  na.counters = counters;
   na.K = static_cast<int>(K);
   na.A = static_cast<int>(A);
   na.B = static_cast<int>(B);
@@ -159,4 +128,29 @@ extern "C" muon_status ns_orthogonalize_noalloc(const void *x, muon_dtype xdt, v
     if (st != MUON_OK) return st;
   }
   return MUON_OK;
+}
+
+// Reads and clears the scratch's error word after the stream's work is done. A small synchronous copy
+// into a host variable and a memset: nothing is allocated.
+extern "C" muon_status ns_orthogonalize_noalloc_check(muon_stream_t stream) {
+  muon_status st = device_check();
+  if (st != MUON_OK) return st;
+  void *scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != MUON_OK) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MUON_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return MUON_ERR_CUDA;
+  if (word == 0) return MUON_OK;
+  if (cudaMemset(scratch, 0, sizeof(word)) != cudaSuccess) return MUON_ERR_CUDA;
+  return MUON_ERR_TIMEOUT;
+}
+
+// The bounded-wait test kernel of muon_debug_wait_timeout, reporting into the scratch's error word.
+extern "C" muon_status muon_debug_wait_timeout_noalloc(uint64_t timeout_ns, muon_stream_t stream) {
+  if (timeout_ns == 0 || timeout_ns > 10000000000ull) return MUON_ERR_INVALID_ARG;
+  muon_status st = device_check();
+  if (st != MUON_OK) return st;
+  void *scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != MUON_OK) return st;
+  return launch_debug_wait(static_cast<uint32_t *>(scratch), timeout_ns, reinterpret_cast<cudaStream_t>(stream));
 }

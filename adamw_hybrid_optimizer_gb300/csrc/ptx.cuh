@@ -157,7 +157,6 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// 3-D tiled load of one box into shared memory, completing tx bytes on bar.
 // ------------------------------------------------------------------------------------------ 8x8 b16 matrices
 
 // Four 8 x 8 b16 matrices from shared memory, transposed on the way: lanes 8j .. 8j+7 give the addresses of
@@ -184,6 +183,7 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// 3-D tiled load of one box into shared memory, completing tx bytes on bar.
 __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1,
                                             int c2) {
   asm volatile(
@@ -199,17 +199,6 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
                    smem_u32(smem_dst)),
                "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
-}
-
-// The same box delivered into the shared memory of every CTA in cta_mask (same offsets in each CTA),
-// completing tx bytes on each destination CTA's barrier at bar's offset.
-__device__ __forceinline__ void tma_load_3d_mc(void *smem_dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1,
-                                               int c2, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "h"(cta_mask)
-      : "memory");
 }
 
 // ------------------------------------------------------------------------------------------ cluster

@@ -69,6 +69,8 @@ SIGNATURES = {
                                         ctypes.c_size_t, _vp]),
     "ns_orthogonalize_noalloc": (ctypes.c_int, [_vp, ctypes.c_int, _vp, ctypes.c_int, _c_int64, _c_int64, _c_int64,
                                                 ctypes.c_int, ctypes.POINTER(ctypes.c_float), ctypes.c_float, _vp]),
+    "ns_orthogonalize_noalloc_check": (ctypes.c_int, [_vp]),
+    "muon_debug_wait_timeout_noalloc": (ctypes.c_int, [ctypes.c_uint64, _vp]),
     "adamw_step": (ctypes.c_int, [_vp, ctypes.c_int, _vp, ctypes.c_int, _vp, _vp, _c_int64,
                                   ctypes.POINTER(adamw_hparams), _vp]),
     "adamw_step_master": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int, _vp, _vp, _c_int64,
@@ -230,6 +232,16 @@ def ns_orthogonalize_noalloc(x, out, coeffs, eps: float, stream=None):
     st = lib().ns_orthogonalize_noalloc(x.data_ptr(), _dtype_code(x), out.data_ptr(), _dtype_code(out), K, A, B,
                                         steps, arr, eps, _stream(stream))
     _check(st, "ns_orthogonalize_noalloc")
+
+
+def ns_orthogonalize_noalloc_check(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the built-in scratch's sticky error status:
+    MUON_ERR_TIMEOUT if a bounded wait of an ns_orthogonalize_noalloc call ran out since the last check."""
+    return int(lib().ns_orthogonalize_noalloc_check(_stream(stream)))
+
+
+def muon_debug_wait_timeout_noalloc(timeout_ns: int, stream=None):
+    _check(lib().muon_debug_wait_timeout_noalloc(int(timeout_ns), _stream(stream)), "muon_debug_wait_timeout_noalloc")
 
 
 def adamw_step(param, grad, exp_avg, exp_avg_sq, lr, beta1, beta2, eps, weight_decay, step: int, stream=None,

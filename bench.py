@@ -19,6 +19,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -169,11 +170,11 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.skip = 0
-        self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv")
+        fd, self.path = tempfile.mkstemp(prefix="muon_bench_clocks_", suffix=".csv")
+        os.close(fd)
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
                                           "--format=csv,noheader,nounits", "-lms", "25"], stdout=self.f,
@@ -202,6 +203,8 @@ class ClockSampler:
 
     def summary(self, sm_max_default):
         if self.proc is None or not os.path.exists(self.path):
+            if os.path.exists(self.path):
+                os.remove(self.path)
             return {"sm_mhz": None, "sm_max_mhz": sm_max_default, "reasons": ["nvidia-smi unavailable"]}
         sms, maxes, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]

@@ -155,7 +155,7 @@ int32_t muon_autotune_poly_shape(int64_t contraction);
 /* Empties the autotune table. */
 void muon_autotune_reset(void);
 
-/* Newton-Schulz orthogonalisation of a stack, [P2] "Muon: orthogonalising the update" (newton_schulz):/* Newton-Schulz orthogonalisation of a stack, [P2] "Muon: orthogonalising the update" (newton_schulz):
+/* Newton-Schulz orthogonalisation of a stack, [P2] "Muon: orthogonalising the update" (newton_schulz):
  * out_k = NS(x_k) for k < K, with normalisation by ||x_k||_F + eps and transpose-to-wide.
  *   x    device, contiguous (K, A, B) of xdt (MUON_F32 or MUON_BF16).
  *   out  device, contiguous (K, A, B) of odt (MUON_F32 or MUON_BF16); may not alias x.
@@ -233,17 +233,31 @@ muon_status hybrid_step(const muon_bucket *buckets, int nb, const muon_hparams *
  * plugins whose host program gives them no allocation API, runtimes whose device-memory budget is
  * fixed at start-up. Same result and arguments as ns_orthogonalize minus the workspace.
  *   Scratch: a static 64 MiB device array inside the library, held by every GPU that loads the
- *   library until the process exits. A stack fits if 4*K*A*B + 4*K*min(A,B)^2 bytes plus padding
- *   (as muon_workspace_bytes(K, A, B) counts it) is at most 64 MiB; larger stacks return
- *   MUON_ERR_WORKSPACE before anything is launched.
- *   The first call on a device looks up the array's device address (once per device, with that
- *   device current); make that first call before any stream capture.
+ *   library until the process exits, laid out as ns_orthogonalize's workspace. A stack fits if
+ *   muon_workspace_bytes(K, A, B) <= 64 MiB (about 4*K*A*B + 4*K*min(A,B)^2 bytes plus padding and
+ *   16 bytes of counters per matrix); larger stacks return MUON_ERR_WORKSPACE before anything is launched.
+ *   The first call on a device (of this function or of the two below) looks up the array's device
+ *   address and zeroes its control block (once per device, with that device current, synchronously);
+ *   make that first call before any stream capture.
  *   Every call shares the array: calls whose work overlaps on the GPU (other streams, other host
- *   threads) race and must be serialised by the caller. Each call clears the array's control block;
- *   a device-side wait that runs out is not reported by this call (muon_check needs a workspace).
+ *   threads) race and must be serialised by the caller. Each call clears the array's per-matrix counters.
+ *   The array's error word is sticky: a device-side wait that runs out sets it (the output is then
+ *   incomplete), and only ns_orthogonalize_noalloc_check reads and clears it.
+ *   The chain runs as separate launches per Newton-Schulz step for every shape.
  * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine. */
 muon_status ns_orthogonalize_noalloc(const void *x, muon_dtype xdt, void *out, muon_dtype odt, int64_t K, int64_t A,
                                      int64_t B, int ns_steps, const float *coeffs, float eps, muon_stream_t stream);
+
+/* The check that goes with ns_orthogonalize_noalloc (no counterpart on the pages): synchronises the
+ * stream the calls ran on, then reads and clears the built-in scratch's error word with a 4-byte copy into
+ * a host variable and a memset (nothing is allocated). Returns MUON_ERR_TIMEOUT if a bounded wait of an
+ * ns_orthogonalize_noalloc call on this device ran out since the last check, else MUON_OK. */
+muon_status ns_orthogonalize_noalloc_check(muon_stream_t stream);
+
+/* muon_debug_wait_timeout for the built-in scratch: one bounded wait that nothing completes, reporting into
+ * the scratch's error word, so that ns_orthogonalize_noalloc_check's report can be tested without a fault.
+ * MUON_ERR_INVALID_ARG unless 0 < timeout_ns <= 1e10. */
+muon_status muon_debug_wait_timeout_noalloc(uint64_t timeout_ns, muon_stream_t stream);
 
 /* The three tensor-core steps of one Newton-Schulz iteration on contiguous bf16 stacks, exposed
  * one by one ([P2] newton_schulz loop body; [P4] section 2.2 symmetric Gram). The loop body's

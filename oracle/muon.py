@@ -5,7 +5,7 @@ Follows [P2] "Optimizers: AdamW, Muon and the distributed optimizer", section
 Muon.step example), with the options of [P3] "dtensor-muon 0.1.0", table "Key options"
 (nesterov, use_cautious_wd, ns_steps, orthogonalization_strategy).
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent (the same readings the GPU path takes):
   * Nesterov input is the sum G + mu*M with the *updated* M; nesterov=False uses M.
   * eps = 1e-7 is added to the Frobenius norm of that one matrix.
   * Transposition happens only when rows > cols (squares are not transposed).
