@@ -141,3 +141,45 @@ def test_adamw_fp32_master_weights(L, n, offset):
     p, g = base_p[offset:], base_g[offset:]
     hp = workloads.workload("gpt2s").adamw_hp
     _run(L, p, [g, g * 0.5, -g], hp, 0.1, master=True)
+
+
+@pytest.mark.parametrize("grouped", [False, True])
+def test_bf16_each_step_within_one_ulp(L, grouped):
+    """bf16 parameters, step by step: at every step count t = 1..10 both sides start from the same seeded
+    state (p and g bf16, m and v fp32 of the size they reach by step t, zero at t = 1), so the one-step
+    bound holds without a trajectory allowance: the GPU's parameter within one bf16 ulp of the oracle's
+    (both round a value that agrees to fp32 precision; they can land on the two sides of a rounding point),
+    plus the fp32 rounding of the terms where the update cancels the decayed parameter; the moments within
+    1e-6 of their terms. Through adamw_step, or through adamw_step_grouped with the vector cut into two
+    tensors with and without decay."""
+    hp = workloads.workload("gpt2s").adamw_hp
+    n = 300_007
+    cut = 123_457
+    for t in range(1, 11):
+        rng = np.random.default_rng(1000 + t)
+        p0 = workloads.round_to(rng.standard_normal(n) * 1e-3, "bf16")
+        g0 = workloads.round_to(rng.standard_normal(n) * 1e-3, "bf16")
+        m0 = workloads.round_to(rng.standard_normal(n) * 1e-3 * (1 - hp.beta1 ** (t - 1)), "f32")
+        v0 = workloads.round_to((rng.standard_normal(n) * 1e-3) ** 2 * (1 - hp.beta2 ** (t - 1)), "f32")
+        p, g, m, v = p0.to(DEV), g0.to(DEV), m0.to(DEV), v0.to(DEV)
+        wd = np.full(n, 0.1)
+        if grouped:
+            wd[cut:] = 0.0
+            h1 = L.make_adamw_hparams(hp.lr, hp.beta1, hp.beta2, hp.eps, 0.1, t)
+            h2 = L.make_adamw_hparams(hp.lr, hp.beta1, hp.beta2, hp.eps, 0.0, t)
+            tensors = L.make_adamw_tensors([(p[:cut], g[:cut], m[:cut], v[:cut], h1),
+                                            (p[cut:], g[cut:], m[cut:], v[cut:], h2)])
+            aws = torch.zeros(L.adamw_workspace_bytes_grouped(2), dtype=torch.uint8, device=DEV)
+            L.adamw_step_grouped(tensors, aws)
+        else:
+            L.adamw_step(p, g, m, v, hp.lr, hp.beta1, hp.beta2, hp.eps, 0.1, t)
+        torch.cuda.synchronize()
+        P0, G0, M0, V0 = f64(p0), f64(g0), f64(m0), f64(v0)
+        po, mo, vo = oadamw.adamw_update(P0, G0, M0, V0, t, lr=hp.lr, beta1=hp.beta1, beta2=hp.beta2, eps=hp.eps,
+                                         weight_decay=wd, param_dtype="bf16")
+        got_p, got_m, got_v = f64(p), f64(m), f64(v)
+        terms = np.abs(P0) + hp.lr * (1 + 1e-3)
+        off = np.abs(got_p - po)
+        assert np.all(off <= bf16_ulp(po) * 1.0001 + 1e-6 * terms), (t, float(np.max(off / bf16_ulp(po))))
+        assert np.all(np.abs(got_m - mo) <= 1e-6 * (hp.beta1 * np.abs(M0) + np.abs(G0)) + 1e-30), t
+        assert np.all(np.abs(got_v - vo) <= 1e-6 * (np.abs(vo) + G0 * G0) + 1e-30), t
