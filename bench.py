@@ -1,10 +1,13 @@
 """Benchmark of the hybrid Muon + AdamW optimizer step on GB300.
 
-A step is one full optimizer step over the GPT-2-small-shaped parameter set: four Muon buckets of 12
-bf16 matrices (768x2304, 768x768, 768x3072, 3072x768; fp32 momentum; 5 classic Newton-Schulz steps)
-and AdamW over 77,285,376 bf16 elements (embedding + head with decay, 24 LayerNorm vectors without).
-Inputs are synthetic (seeded, N(0, 1e-3^2) params and grads) and resident in HBM; one gradient set
-is reused by every step. Each step touches ~2.4 GB, more than the 129 MB L2, so no separate flush.
+A step is one full optimizer step over the Llama-3-8B-shaped parameter set: four Muon buckets of bf16
+matrices (32 layers x {q, o 4096x4096; k, v 1024x4096; gate, up 14336x4096 (transposed path);
+down 4096x14336}, 224 matrices, 6,979,321,856 elements; fp32 momentum; Nesterov 0.95; 5 classic
+Newton-Schulz steps) and AdamW over 1,050,939,392 bf16 elements (embedding and head 128256x4096 with
+decay, 65 RMSNorm 4096-vectors without; fp32 moments). Inputs are synthetic (seeded N(0, 1e-3^2) params
+and grads drawn on the device) and resident in HBM; one gradient set is reused by every step. Each step
+touches well over 100 GB, far more than the 129 MB L2, so no separate flush. The GPT-2-small-shaped set
+is timed too and reported under its own key.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -28,9 +31,17 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "Muon step ms & NS TFLOP/s (frac of bf16 peak); AdamW GB/s (frac of HBM)"
-WORKLOAD = ("gpt2-small-shaped parameter set: Muon 4 buckets x K=12 bf16 (768x2304, 768x768, 768x3072, "
-            "3072x768 transposed path), fp32 momentum, Nesterov 0.95, 5 classic quintic NS steps; AdamW on "
-            "2x50304x768 bf16 (wd 0.1) + 24x768 LayerNorm bf16 (wd 0), fp32 moments")
+WORKLOADS = {
+    "llama8b": ("llama-3-8b-shaped parameter set: Muon 4 buckets bf16 (K=64 4096x4096, K=64 1024x4096, "
+                "K=64 14336x4096 transposed path, K=32 4096x14336; 6,979,321,856 elements), fp32 momentum, "
+                "Nesterov 0.95, 5 classic quintic NS steps; AdamW on 2x128256x4096 bf16 (wd 0.1) + 65x4096 "
+                "RMSNorm bf16 (wd 0), fp32 moments"),
+    "gpt2s": ("gpt2-small-shaped parameter set: Muon 4 buckets x K=12 bf16 (768x2304, 768x768, 768x3072, "
+              "3072x768 transposed path), fp32 momentum, Nesterov 0.95, 5 classic quintic NS steps; AdamW on "
+              "2x50304x768 bf16 (wd 0.1) + 24x768 LayerNorm bf16 (wd 0), fp32 moments"),
+}
+HEADLINE = "llama8b"
+WORKLOAD = WORKLOADS[HEADLINE]
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -46,59 +57,56 @@ def load_peaks():
 # ------------------------------------------------------------------------------------------------ workload
 
 class Workload:
-    """Device buffers of the bench step: Muon bucket stacks and flat AdamW buffers."""
+    """Device buffers of one bench step: Muon bucket stacks and the AdamW tensors (views of one flat buffer per
+    dtype), drawn on the device from seeded generators."""
 
-    def __init__(self, L, device, draw=True):
+    def __init__(self, L, device, name=HEADLINE):
         import torch
         import workloads
-        from adamw_hybrid_optimizer_gb300 import libmuon  # noqa: F401
         self.L = L
         self.device = device
-        w = workloads.workload("gpt2s")
+        w = workloads.workload(name)
         self.w = w
+        self.name = name
         plan = L.muon_plan_buckets(workloads.shape_list(w))
         self.buckets = []
         for b, (shape, K) in enumerate(zip(plan["bucket_shapes"], plan["bucket_K"])):
             A, B = shape
-            members = [i for i, bid in enumerate(plan["bucket_id"]) if bid == b]
-            p = torch.empty((K, A, B), dtype=torch.bfloat16, device=device)
-            g = torch.empty((K, A, B), dtype=torch.bfloat16, device=device)
-            if draw:
-                for k, i in enumerate(members):
-                    p[k].copy_(workloads.muon_param_init(w, i))
-                    g[k].copy_(workloads.muon_grad(w, 1, i))
+            p = workloads.device_stack((K, A, B), "normal", w.param_std, 7000 + b, "bf16", device)
+            g = workloads.device_stack((K, A, B), w.grad_dist, w.grad_std, 7100 + b, "bf16", device)
             mom = torch.zeros((K, A, B), dtype=torch.float32, device=device)
             self.buckets.append(dict(K=K, A=A, B=B, p=p, g=g, mom=mom,
                                      pptr=L.pointer_array([p[k] for k in range(K)], device),
                                      gptr=L.pointer_array([g[k] for k in range(K)], device)))
-        self.bucket_array = L.make_buckets([(bk["pptr"], bk["gptr"], bk["mom"], bk["K"], bk["A"], bk["B"],
-                                             L.MUON_BF16, L.MUON_BF16) for bk in self.buckets])
+        self.bucket_array = L.make_buckets([self._spec(bk) for bk in self.buckets])
         self.ws = torch.zeros(L.muon_workspace_bytes_grouped(self.bucket_array), dtype=torch.uint8, device=device)
-        self.hp = L.make_muon_hparams(w.muon_hp.lr, w.muon_hp.momentum, w.muon_hp.weight_decay, w.muon_hp.nesterov,
-                                      w.muon_hp.cautious_wd, w.muon_hp.scale_mode, w.muon_hp.coeffs, w.muon_hp.eps)
-        # AdamW: one flat buffer per weight-decay value (embedding + head; the LayerNorm vectors)
-        self.adamw = []
-        for wd in (0.1, 0.0):
-            idx = [i for i, t in enumerate(w.adamw) if t.weight_decay == wd]
-            n = sum(w.adamw[i].numel for i in idx)
-            p = torch.empty(n, dtype=torch.bfloat16, device=device)
-            g = torch.empty(n, dtype=torch.bfloat16, device=device)
-            if draw:
-                off = 0
-                for i in idx:
-                    k = w.adamw[i].numel
-                    p[off:off + k].copy_(workloads.adamw_param_init(w, i))
-                    g[off:off + k].copy_(workloads.adamw_grad(w, 1, i))
-                    off += k
-            self.adamw.append(dict(wd=wd, p=p, g=g, m=torch.zeros(n, dtype=torch.float32, device=device),
-                                   v=torch.zeros(n, dtype=torch.float32, device=device)))
+        h = w.muon_hp
+        self.hp = L.make_muon_hparams(h.lr, h.momentum, h.weight_decay, h.nesterov, h.cautious_wd, h.scale_mode,
+                                      h.coeffs, h.eps)
+        # AdamW: the workload's tensors as views of one flat bf16 buffer, each with its own weight decay
+        n = w.adamw_elems
+        self.adamw_flat = dict(p=workloads.device_stack((1, 1, n), "normal", w.param_std, 7200, "bf16",
+                                                        device).view(-1),
+                               g=workloads.device_stack((1, 1, n), "normal", w.grad_std, 7201, "bf16",
+                                                        device).view(-1),
+                               m=torch.zeros(n, dtype=torch.float32, device=device),
+                               v=torch.zeros(n, dtype=torch.float32, device=device))
         a = w.adamw_hp
-        self.adamw_hps = [L.make_adamw_hparams(a.lr, a.beta1, a.beta2, a.eps, b["wd"], 1) for b in self.adamw]
-        self.adamw_tensors = L.make_adamw_tensors([(b["p"], b["g"], b["m"], b["v"], h)
-                                                   for b, h in zip(self.adamw, self.adamw_hps)])
-        self.adamw_ws = torch.zeros(L.adamw_workspace_bytes_grouped(len(self.adamw)), dtype=torch.uint8,
-                                    device=device)
+        self.adamw_hps = {}
+        specs, off = [], 0
+        for t in w.adamw:
+            hp = self.adamw_hps.setdefault(t.weight_decay,
+                                           L.make_adamw_hparams(a.lr, a.beta1, a.beta2, a.eps, t.weight_decay, 1))
+            sl = slice(off, off + t.numel)
+            specs.append(tuple(self.adamw_flat[k][sl] for k in "pgmv") + (hp,))
+            off += t.numel
+        self.adamw_tensors = L.make_adamw_tensors(specs)
+        self.adamw_ws = torch.zeros(L.adamw_workspace_bytes_grouped(len(specs)), dtype=torch.uint8, device=device)
         self.t = 0
+
+    def _spec(self, bk):
+        L = self.L
+        return (bk["pptr"], bk["gptr"], bk["mom"], bk["K"], bk["A"], bk["B"], L.MUON_BF16, L.MUON_BF16)
 
     def step(self, stream=None):
         """One whole optimizer step through hybrid_step: the grouped Muon step, then the grouped AdamW pass."""
@@ -108,7 +116,7 @@ class Workload:
     # the two halves of hybrid_step as separate calls, for a caller that overlaps its own copies with them
     def begin_step(self):
         self.t += 1
-        for h in self.adamw_hps:
+        for h in self.adamw_hps.values():
             h.step = self.t
 
     def muon_part(self, stream=None, which=None):
@@ -128,8 +136,7 @@ class Workload:
             acc += self.buckets[cut]["g"].numel()
             cut += 1
         idx = [list(range(cut))] + [[i] for i in range(cut, len(self.buckets))]
-        spec = lambda bk: (bk["pptr"], bk["gptr"], bk["mom"], bk["K"], bk["A"], bk["B"], L.MUON_BF16, L.MUON_BF16)
-        self.groups = [L.make_buckets([spec(self.buckets[i]) for i in g]) for g in idx]
+        self.groups = [L.make_buckets([self._spec(self.buckets[i]) for i in g]) for g in idx]
         return idx
 
     def adamw_part(self, stream=None):
@@ -149,14 +156,14 @@ class Workload:
             flops["ns_final"] += K * 2 * m * m * n
             nominal += ns * K * (4 * m * m * n + 2 * m ** 3)
             bytes_["nesterov_norm"] += K * m * n * (2 + 4 + 4 + 2)
-        for buf in self.adamw:
-            bytes_["adamw"] += buf["p"].numel() * 22
+        bytes_["adamw"] = self.w.adamw_elems * 22
         return flops, nominal, bytes_
 
-    def h2d_d2h_bytes(self):
-        h = sum(bk["g"].numel() * 2 for bk in self.buckets) + sum(b["g"].numel() * 2 for b in self.adamw)
-        d = sum(bk["p"].numel() * 2 for bk in self.buckets) + sum(b["p"].numel() * 2 for b in self.adamw)
-        return h, d
+    # host <-> device views for the end-to-end leg: (gradient, parameter) device tensors per piece
+    def host_views(self):
+        dev_g = [bk["g"] for bk in self.buckets] + [self.adamw_flat["g"]]
+        dev_p = [bk["p"] for bk in self.buckets] + [self.adamw_flat["p"]]
+        return dev_g, dev_p
 
 
 # ------------------------------------------------------------------------------------------------ clocks
@@ -233,43 +240,51 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------------------------------ oracle timing
 
-def oracle_sample_time(budget_s: float = 20.0):
-    """Times the oracle on a bounded sample of the step: one matrix per Muon bucket and 2^21 AdamW elements.
-    Returns (extrapolated ms per full step, sample description, seconds spent)."""
+def oracle_sample_time(shapes_to_time, adamw_sample: int = 1 << 21):
+    """Times the oracle (fp64 NumPy, as it stands) on a bounded sample of the headline step: one Muon update
+    (momentum, Nesterov input, Newton-Schulz, decay and step) of one matrix of each bucket in shapes_to_time,
+    and AdamW on adamw_sample elements. The full step's time is extrapolated: each bucket's Muon work by its
+    nominal Newton-Schulz flops at the fp64 rate measured on the timed matrices, AdamW by element count.
+    Returns (extrapolated ms per full step, sample description, seconds spent, matrices timed)."""
     import workloads
     from oracle import adamw as oadamw
     from oracle import muon as omuon
     from oracle.buckets import plan_buckets
-    w = workloads.workload("gpt2s")
+    w = workloads.workload(HEADLINE)
     hp = w.muon_hp
     plan = plan_buckets(workloads.shape_list(w))
     t_start = time.perf_counter()
-    total_ms = 0.0
+
+    def ns_flops(A, B):
+        m, n = min(A, B), max(A, B)
+        return hp.ns_steps * (4.0 * m * m * n + 2.0 * m ** 3)
+
+    timed_flops = timed_s = 0.0
     parts = []
-    for b, (shape, K) in enumerate(zip(plan["bucket_shapes"], plan["bucket_K"])):
-        i = plan["bucket_id"].index(b)
-        p = workloads.as_f64(workloads.muon_param_init(w, i))
-        g = workloads.as_f64(workloads.muon_grad(w, 1, i))
+    rng = np.random.default_rng(17)
+    for (A, B), K in zip(plan["bucket_shapes"], plan["bucket_K"]):
+        if (A, B) not in shapes_to_time:
+            continue
+        p = rng.standard_normal((A, B)) * w.param_std
+        g = rng.standard_normal((A, B)) * w.grad_std
         t0 = time.perf_counter()
         omuon.muon_update(p, g, np.zeros_like(p), lr=hp.lr, momentum=hp.momentum, weight_decay=hp.weight_decay,
                           nesterov=hp.nesterov, coeffs=hp.coeffs, eps=hp.eps, param_dtype="bf16")
-        dt = time.perf_counter() - t0
-        total_ms += dt * 1e3 * K
-        parts.append(f"1 of {K} {shape[0]}x{shape[1]}")
-        if time.perf_counter() - t_start > budget_s:
-            break
-    n_s = 1 << 21
-    rng = np.random.default_rng(0)
-    p, g = rng.standard_normal((2, n_s)) * 1e-3
+        timed_s += time.perf_counter() - t0
+        timed_flops += ns_flops(A, B)
+        parts.append(f"1 of {K} {A}x{B}")
+    rate = timed_flops / timed_s
+    muon_ms = sum(K * ns_flops(A, B) for (A, B), K in zip(plan["bucket_shapes"], plan["bucket_K"])) / rate * 1e3
+    p, g = rng.standard_normal((2, adamw_sample)) * 1e-3
     a = w.adamw_hp
     t0 = time.perf_counter()
-    oadamw.adamw_update(p, g, np.zeros(n_s), np.zeros(n_s), 1, lr=a.lr, beta1=a.beta1, beta2=a.beta2, eps=a.eps,
-                        weight_decay=0.1, param_dtype="bf16")
-    dt = time.perf_counter() - t0
-    total_ms += dt * 1e3 * w.adamw_elems / n_s
-    desc = ("oracle (NumPy fp64) Muon update of " + ", ".join(parts) + f" matrices, AdamW on {n_s} elements; "
-            "extrapolated to the full step by matrix count and element count")
-    return total_ms, desc, time.perf_counter() - t_start
+    oadamw.adamw_update(p, g, np.zeros(adamw_sample), np.zeros(adamw_sample), 1, lr=a.lr, beta1=a.beta1,
+                        beta2=a.beta2, eps=a.eps, weight_decay=0.1, param_dtype="bf16")
+    adamw_ms = (time.perf_counter() - t0) * 1e3 * w.adamw_elems / adamw_sample
+    desc = ("oracle (NumPy fp64) Muon update of " + ", ".join(parts) + f" matrices ({rate / 1e9:.1f} GFLOP/s "
+            f"fp64 measured), AdamW on {adamw_sample} elements; the full step (224 matrices, "
+            f"{w.adamw_elems} AdamW elements) extrapolated by Newton-Schulz flop count and element count")
+    return muon_ms + adamw_ms, desc, time.perf_counter() - t_start, len(parts)
 
 
 # ------------------------------------------------------------------------------------------------ arms
@@ -293,25 +308,73 @@ def dist_env():
 
 
 def run_reference(args):
+    """The reference arm: the oracle, timed as it stands on the host cores, each step a bounded sample of the
+    headline step (one 1024x4096 Muon matrix and 2^21 AdamW elements) extrapolated to the full step."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     times = []
-    desc = ""
+    desc, timed = "", 0
     for i in range(args.warmup + args.steps):
-        ms, desc, _ = oracle_sample_time(budget_s=8.0)
+        ms, desc, _, n = oracle_sample_time({(1024, 4096)})
         if i >= args.warmup:
             times.append(ms)
+            timed += n
     value = float(np.mean(times))
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "ms",
             "higher_is_better": False, "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(value, 3), "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": WORKLOAD},
+            "extrapolated": True,
+            "oracle_samples_timed": {"muon_matrices": timed, "adamw_elements": (1 << 21) * args.steps,
+                                     "note": "each timed step is a sample of the full step, extrapolated; "
+                                             "no full step was run"},
             "cpu_baseline": {"value": round(value, 3), "unit": "ms", "cores": os.cpu_count(), "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": round(value, 3), "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def _kernel_table(L, wl, steps, peaks):
+    """Per-kernel device times of `steps` traced steps (an event pair around every launch)."""
+    import torch
+    L.muon_trace_enable(True)
+    for _ in range(steps):
+        wl.step()
+    torch.cuda.synchronize()
+    L.muon_trace_enable(False)
+    per_kind = {}
+    for kind, t in L.muon_trace_collect():
+        d = per_kind.setdefault(kind, [0.0, 0])
+        d[0] += t
+        d[1] += 1
+    flops, nominal, bytes_ = wl.work()
+    tot = {k: v[0] / steps for k, v in per_kind.items()}          # ms per step per kind
+    launches_per_step = {k: v[1] / steps for k, v in per_kind.items()}
+    kernels = {}
+    for k, t in tot.items():
+        entry = {"ms_per_step": round(t, 4), "launches_per_step": launches_per_step[k],
+                 "avg_launch_us": round(1e3 * t / launches_per_step[k], 2)}
+        if k in flops:
+            tf = flops[k] / (t * 1e-3) / 1e12
+            entry.update({"tflops": round(tf, 1), "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 4)})
+        if k in bytes_:
+            gbs = bytes_[k] / (t * 1e-3) / 1e9
+            entry.update({"gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)})
+        kernels[k] = entry
+    return tot, kernels, flops, nominal, bytes_
+
+
+def _timed_steps(wl, steps, stream):
+    import torch
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        wl.step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
 
 
 def run_ours(args):
@@ -329,16 +392,18 @@ def run_ours(args):
     from adamw_hybrid_optimizer_gb300 import libmuon as L
 
     peaks, peak_src = load_peaks()
-    wl = Workload(L, device)
+    peak_tf = peaks["bf16_tflops"]
+    peak_bw = peaks["hbm_gbs"]
+    wl = Workload(L, device, HEADLINE)
     stream = torch.cuda.current_stream(device)
     # initialisation, outside every timed region: the poly step's pipeline shape measured on these buckets
     L.muon_autotune(wl.bucket_array, wl.ws)
-    poly_shape = {0: "4+5", 1: "5+3", 2: "6+2"}.get(L.muon_autotune_poly_shape(768), "rule")
+    ms_ = sorted({min(bk["A"], bk["B"]) for bk in wl.buckets})
+    poly_shape = {m: {0: "4+5", 1: "5+3", 2: "6+2"}.get(L.muon_autotune_poly_shape(m), "rule") for m in ms_}
 
     def barrier():
         if world > 1:
             dist.barrier()
-
 
     # warm-up
     for _ in range(args.warmup):
@@ -348,53 +413,23 @@ def run_ours(args):
         raise RuntimeError("a device-side wait ran out during warm-up")
 
     # timed region: device time of K steps
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     launches0 = L.muon_launch_count()
     with ClockSampler(local) as clocks:
-        start.record(stream)
-        for _ in range(args.steps):
-            wl.step()
-        end.record(stream)
-        torch.cuda.synchronize()
+        ms = _timed_steps(wl, args.steps, stream)
     barrier()
     launches = L.muon_launch_count() - launches0
-    ms = max_over_ranks(start.elapsed_time(end) / args.steps, world, device)
+    ms = max_over_ranks(ms, world, device)
     clk = clocks.summary(peaks.get("sm_max_mhz"))
 
-    # traced pass: per-kernel durations from events around each launch (same steps, same stream)
-    L.muon_trace_enable(True)
-    for _ in range(args.steps):
-        wl.step()
-    torch.cuda.synchronize()
-    L.muon_trace_enable(False)
-    rec = L.muon_trace_collect()
-    per_kind = {}
-    for kind, t in rec:
-        d = per_kind.setdefault(kind, [0.0, 0])
-        d[0] += t
-        d[1] += 1
-    flops, nominal, bytes_ = wl.work()
-    tot = {k: v[0] / args.steps for k, v in per_kind.items()}          # ms per step per kind
+    # traced pass: per-kernel durations from events around each launch (same stream)
+    trace_steps = max(1, min(args.steps, 3))
+    tot, kernels, flops, nominal, bytes_ = _kernel_table(L, wl, trace_steps, peaks)
     # the dominant kernel among those with an algorithmic work model (the GEMMs, the two bandwidth passes)
     modelled = [k for k in tot if k in flops or k in bytes_]
     dominant = max(modelled, key=tot.get)
-    launches_per_step = {k: v[1] / args.steps for k, v in per_kind.items()}
     ns_ms = sum(tot.get(k, 0.0) for k in ("ns_gram", "ns_poly", "ns_apply", "ns_final"))
-    peak_tf = peaks["bf16_tflops"]
-    peak_bw = peaks["hbm_gbs"]
-    kernels = {}
-    for k, t in tot.items():
-        entry = {"ms_per_step": round(t, 4), "launches_per_step": launches_per_step[k],
-                 "avg_launch_us": round(1e3 * t / launches_per_step[k], 2)}
-        if k in flops:
-            tf = flops[k] / (t * 1e-3) / 1e12
-            entry.update({"tflops": round(tf, 1), "frac_bf16_peak": round(tf / peak_tf, 4)})
-        if k in bytes_:
-            gbs = bytes_[k] / (t * 1e-3) / 1e9
-            entry.update({"gbs": round(gbs, 1), "frac_hbm": round(gbs / peak_bw, 4)})
-        kernels[k] = entry
     if dominant in flops:
         ach = flops[dominant] / (tot[dominant] * 1e-3) / 1e12
         roof = {"bound": "tensor", "kernel": dominant, "achieved": round(ach, 2), "peak": peak_tf,
@@ -404,19 +439,17 @@ def run_ours(args):
         ach = bytes_[dominant] / (tot[dominant] * 1e-3) / 1e9
         roof = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": peak_bw, "unit": "GB/s",
                 "frac": round(ach / peak_bw, 4), "traffic": None, "peak_source": f"{peak_src} copy"}
-    traffic = _traffic_from_profiles(dominant)
+    traffic = _traffic_from_profiles(HEADLINE, dominant)
     if traffic is not None:
         roof["traffic"] = traffic
 
     # end to end through the C ABI with host buffers: gradients in from pinned host memory, updated
     # parameters back out, every step, inside the timed region
-    h2d, d2h = wl.h2d_d2h_bytes()
-    host_g = [torch.empty(bk["g"].shape, dtype=bk["g"].dtype, pin_memory=True) for bk in wl.buckets] + \
-             [torch.empty(b["g"].shape, dtype=b["g"].dtype, pin_memory=True) for b in wl.adamw]
-    host_p = [torch.empty(bk["p"].shape, dtype=bk["p"].dtype, pin_memory=True) for bk in wl.buckets] + \
-             [torch.empty(b["p"].shape, dtype=b["p"].dtype, pin_memory=True) for b in wl.adamw]
-    dev_g = [bk["g"] for bk in wl.buckets] + [b["g"] for b in wl.adamw]
-    dev_p = [bk["p"] for bk in wl.buckets] + [b["p"] for b in wl.adamw]
+    dev_g, dev_p = wl.host_views()
+    h2d = sum(t.numel() * t.element_size() for t in dev_g)
+    d2h = sum(t.numel() * t.element_size() for t in dev_p)
+    host_g = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_g]
+    host_p = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_p]
     for hg, dg in zip(host_g, dev_g):
         hg.copy_(dg)
     torch.cuda.synchronize()
@@ -424,11 +457,10 @@ def run_ours(args):
     # soon as its inputs are in: the Muon chain of the first bucket group, the AdamW pass, then the chain of
     # each other bucket. Inputs go in on one copy stream in that order; each call's parameters come out on a
     # second copy stream as soon as it is done.
-    e2e_steps = max(3, args.steps // 2)
+    e2e_steps = max(3, args.steps // 4)
     nb = len(wl.buckets)
     groups = wl.split_buckets()
-    pieces = [(groups[0], lambda: wl.muon_part(stream, 0)),
-              (list(range(nb, len(dev_g))), lambda: wl.adamw_part(stream))]
+    pieces = [(groups[0], lambda: wl.muon_part(stream, 0)), ([nb], lambda: wl.adamw_part(stream))]
     pieces += [(g, lambda k=k: wl.muon_part(stream, k)) for k, g in enumerate(groups) if k > 0]
     copy_in, copy_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     ev_in = [torch.cuda.Event() for _ in pieces]
@@ -458,22 +490,49 @@ def run_ours(args):
     barrier()
     if L.muon_check(wl.ws) != L.MUON_OK:
         raise RuntimeError("a device-side wait ran out during the timed steps")
+    del host_g, host_p
+    adamw_ms = tot.get("adamw", 0.0)
+    head_cfg = {"muon_matrices": sum(bk["K"] for bk in wl.buckets), "adamw_elems": wl.w.adamw_elems}
+    del wl
+    torch.cuda.empty_cache()
+
+    # the GPT-2-small-shaped set, device time only (reported under its own key)
+    small = Workload(L, device, "gpt2s")
+    L.muon_autotune(small.bucket_array, small.ws)
+    for _ in range(max(3, args.warmup)):
+        small.step()
+    torch.cuda.synchronize()
+    small_ms = _timed_steps(small, max(50, args.steps), stream)
+    s_tot, s_kernels, _, s_nominal, s_bytes = _kernel_table(L, small, 3, peaks)
+    s_ns = sum(s_tot.get(k, 0.0) for k in ("ns_gram", "ns_poly", "ns_apply", "ns_final"))
+    s_adamw = s_tot.get("adamw", 0.0)
+    if L.muon_check(small.ws) != L.MUON_OK:
+        raise RuntimeError("a device-side wait ran out during the GPT-2-small steps")
+    gpt2s = {"workload": WORKLOADS["gpt2s"], "ms_per_step": round(small_ms, 4),
+             "ns_ms": round(s_ns, 4),
+             "ns_frac_bf16_peak_nominal": round(s_nominal / (s_ns * 1e-3) / 1e12 / peak_tf, 4) if s_ns else None,
+             "adamw_gbs": round(s_bytes["adamw"] / (s_adamw * 1e-3) / 1e9, 1) if s_adamw else None,
+             "kernels": s_kernels}
+    del small
+    torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cms, desc, _ = oracle_sample_time(budget_s=20.0)
-        cpu = {"value": round(cms, 1), "unit": "ms", "cores": os.cpu_count(), "kind": "oracle", "sample": desc}
+        cms, desc, _, n = oracle_sample_time({(1024, 4096), (4096, 4096)})
+        cpu = {"value": round(cms, 1), "unit": "ms", "cores": os.cpu_count(), "kind": "oracle", "sample": desc,
+               "extrapolated": True}
 
     if rank == 0:
-        adamw_ms = tot.get("adamw", 0.0)
+        sm, smax = clk.get("sm_mhz"), clk.get("sm_max_mhz")
         line = {
             "metric": METRIC, "value": round(ms, 4), "unit": "ms", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "inputs larger than L2: ~2.4 GB touched per step, no separate flush",
-                       "muon_matrices": 48, "adamw_elems": wl.w.adamw_elems,
-                       "poly_pipeline": f"{poly_shape} stages+slots (measured at init)"},
+            "config": dict({"workload": WORKLOAD, "parallelism": "replicas" if world > 1 else "single",
+                            "l2": "inputs larger than L2: >100 GB touched per step, no separate flush",
+                            "poly_pipeline": {str(m): f"{v} stages+slots" for m, v in poly_shape.items()}},
+                           **head_cfg),
+            "ms_at_sm_max_clock": round(ms * sm / smax, 4) if sm and smax else None,
             "muon_ms": round(sum(tot.get(k, 0.0) for k in tot if k != "adamw"), 4),
             "ns_ms": round(ns_ms, 4),
             "ns_tflops_nominal": round(nominal / (ns_ms * 1e-3) / 1e12, 1) if ns_ms > 0 else None,
@@ -487,6 +546,7 @@ def run_ours(args):
             "gpu_launches": launches,
             "clocks": clk,
             "cpu_baseline": cpu,
+            "gpt2s": gpt2s,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -494,14 +554,15 @@ def run_ours(args):
     return 0
 
 
-def _traffic_from_profiles(kernel):
-    """DRAM bytes per launch (JSON) recorded from an ncu capture of the current kernels, if committed."""
+def _traffic_from_profiles(workload, kernel):
+    """DRAM bytes per launch of `kernel` on `workload`, from the committed summary of an ncu capture of the
+    current kernels ({workload: {kernel: bytes}}), if there is one."""
     path = os.path.join(ROOT, "profiles", "dram_traffic_per_launch.txt")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    v = d.get(kernel)
+    v = d.get(workload, {}).get(kernel) if isinstance(d.get(workload), dict) else None
     return v if isinstance(v, (int, float)) else None
 
 
@@ -704,7 +765,7 @@ def run_ns_sweep(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -120,6 +120,7 @@ def test_llama8b_adamw_set_grouped_sampled(L):
     po = f64(p[idx_t])
     mref, vref = np.zeros(len(allidx)), np.zeros(len(allidx))
     em, ev = np.zeros(len(allidx)), np.zeros(len(allidx))   # fp32 rounding carried from step to step
+    dp = np.zeros(len(allidx))                                # |gpu p - oracle p| after the previous step
     for step in range(1, 4):
         g.copy_(workloads.device_stack((1, 1, n_total), "normal", w.grad_std, 3300 + step, "bf16", DEV).view(-1))
         for h in hps.values():
@@ -131,9 +132,14 @@ def test_llama8b_adamw_set_grouped_sampled(L):
         po, mref, vref = oadamw.adamw_update(po, gi, mref, vref, step, lr=a.lr, beta1=a.beta1, beta2=a.beta2,
                                              eps=a.eps, weight_decay=wd, param_dtype="bf16")
         got_p, got_m, got_v = f64(p[idx_t]), f64(mo[idx_t]), f64(vo[idx_t])
-        # independent bf16 trajectories: each store may round the other way once per step
+        # independent bf16 trajectories: a parameter difference carries into the next step scaled by the decay
+        # factor (the update itself reads only m and v), and each step's two roundings add at most one ulp
         terms = np.abs(po_prev) + a.lr * (1 + 1e-3)
-        assert np.all(np.abs(got_p - po) <= step * bf16_ulp(po) * 1.0001 + 1e-6 * terms), step
+        carried = dp * (1.0 - a.lr * wd)
+        off = np.abs(got_p - po)
+        bound = carried + bf16_ulp(np.maximum(np.abs(got_p), np.abs(po))) * 1.0001 + 1e-6 * terms
+        assert np.all(off <= bound), (step, int(np.sum(off > bound)))
+        dp = off
         em = a.beta1 * em + 1e-6 * (a.beta1 * np.abs(m_prev) + np.abs(gi))
         ev = a.beta2 * ev + 1e-6 * (np.abs(vref) + gi * gi)
         assert np.all(np.abs(got_m - mref) <= em + 1e-30), step
