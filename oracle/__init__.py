@@ -10,7 +10,8 @@ written from their formulas and prose in float64 NumPy:
 
   oracle.muon          Muon: momentum, Nesterov input, Frobenius normalisation,
                        transpose-to-wide, quintic Newton-Schulz, 0.2*sqrt(max(A,B))
-                       scaling, decoupled (optionally cautious) weight decay.
+                       scaling, decoupled (optionally cautious) weight decay; and the
+                       same iteration run in the m x m Gram space (newton_schulz_gram).
   oracle.adamw         AdamW with bias correction and decoupled decay; Adam + L2.
   oracle.buckets       grouping of Muon matrices by shape into (K, A, B) stacks.
   oracle.polar_express per-step minimax odd-quintic coefficients (Polar Express).

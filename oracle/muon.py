@@ -50,6 +50,33 @@ def newton_schulz(G, coeffs: Coeffs, eps: float = 1e-7) -> np.ndarray:
     return X.T if transposed else X
 
 
+def newton_schulz_gram(G, coeffs: Coeffs, eps: float = 1e-7) -> np.ndarray:
+    """[P4] "DMuon", section 2.2 "Efficient Gram Newton-Schulz Iteration": the same iteration run in the
+    m x m Gram space (m = the smaller side), which costs O(m^3) per step instead of O(m^2 n).
+
+    The page names the recurrence but prints no formula. Reading taken (the plainest one that reaches the
+    same X_N as newton_schulz): with X_0 the normalised wide matrix and A_0 = X_0 X_0^T, every iterate is
+    X_t = R_t X_0 for an m x m matrix R_t, and X_t X_t^T = A_t; per step t
+        Q_t = a_t I + b_t A_t + c_t A_t A_t ;  R_{t+1} = Q_t R_t ;  A_{t+1} = Q_t A_t Q_t
+    (X_{t+1} = Q_t X_t is newton_schulz's step), and the output is X_N = R_N X_0, transposed back.
+    """
+    G = np.asarray(G, dtype=np.float64)
+    X0 = G / (np.linalg.norm(G) + eps)         # Frobenius norm of the whole matrix
+    transposed = G.shape[0] > G.shape[1]
+    if transposed:
+        X0 = X0.T
+    m = X0.shape[0]
+    I = np.eye(m)
+    A = X0 @ X0.T
+    R = I
+    for a, b, c in coeffs:
+        Q = a * I + b * A + c * (A @ A)
+        R = Q @ R
+        A = Q @ A @ Q
+    X = R @ X0
+    return X.T if transposed else X
+
+
 def compose_phi(x, coeffs: Coeffs) -> np.ndarray:
     """The scalar map a singular value goes through: phi = p_{N-1} o ... o p_0, p_t(s) = a s + b s^3 + c s^5.
 

@@ -43,6 +43,49 @@ def _ns_wrong_sign(G, coeffs, eps=1e-7):
 _ns_ref = omuon.newton_schulz
 
 
+def _gram_parts(G, eps):
+    G = np.asarray(G, dtype=np.float64)
+    X0 = G / (np.linalg.norm(G) + eps)
+    t = G.shape[0] > G.shape[1]
+    return (X0.T if t else X0), t
+
+
+def _gram_one_sided_update(G, coeffs, eps=1e-7):
+    X0, t = _gram_parts(G, eps)
+    I = np.eye(X0.shape[0])
+    A, R = X0 @ X0.T, I
+    for a, b, c in coeffs:
+        Q = a * I + b * A + c * A @ A
+        R = Q @ R
+        A = Q @ A                      # planted: A_{t+1} = Q A instead of Q A Q
+    X = R @ X0
+    return X.T if t else X
+
+
+def _gram_last_q_only(G, coeffs, eps=1e-7):
+    X0, t = _gram_parts(G, eps)
+    I = np.eye(X0.shape[0])
+    A, R = X0 @ X0.T, I
+    for a, b, c in coeffs:
+        Q = a * I + b * A + c * A @ A
+        R = Q                          # planted: R not accumulated
+        A = Q @ A @ Q
+    X = R @ X0
+    return X.T if t else X
+
+
+def _gram_drop_c(G, coeffs, eps=1e-7):
+    X0, t = _gram_parts(G, eps)
+    I = np.eye(X0.shape[0])
+    A, R = X0 @ X0.T, I
+    for a, b, c in coeffs:
+        Q = a * I + b * A              # planted: no c A^2 term
+        R = Q @ R
+        A = Q @ A @ Q
+    X = R @ X0
+    return X.T if t else X
+
+
 def _muon_decay_after(p, g, m, *, lr, momentum, weight_decay, nesterov=True, cautious_wd=False,
                       coeffs=(omuon.CLASSIC,) * 5, eps=1e-7, scale_mode=0, param_dtype="f64"):
     p = np.asarray(p, float)
@@ -94,6 +137,12 @@ NS_PINS = [
     lambda: pins.test_page_singular_value_example(pins.os.path.join(pins.os.path.dirname(pins.__file__), "golden")),
     lambda: pins.test_equal_singular_values_input(64),
 ]
+GRAM_PINS = [
+    lambda: pins.test_gram_ns_equals_svd_closed_form((8, 16), pins.CLASSIC5),
+    lambda: pins.test_gram_ns_page_singular_value_example(pins.os.path.join(pins.os.path.dirname(pins.__file__),
+                                                                            "golden")),
+    lambda: pins.test_gram_ns_equal_singular_values_input(64),
+]
 MUON_PINS = [pins.test_cautious_decay_hand_case, pins.test_momentum_and_nesterov_second_step,
              lambda: pins.test_first_step_update_is_ns_of_gradient(True), pins.test_zero_gradient_only_decays]
 ADAMW_PINS = [lambda: pins.test_page_adamw_decay_example(pins.os.path.join(pins.os.path.dirname(pins.__file__),
@@ -116,6 +165,12 @@ def test_ns_mutants_are_caught(monkeypatch, mutant):
     assert _some_pin_fails(NS_PINS)
 
 
+@pytest.mark.parametrize("mutant", [_gram_one_sided_update, _gram_last_q_only, _gram_drop_c])
+def test_gram_ns_mutants_are_caught(monkeypatch, mutant):
+    monkeypatch.setattr(omuon, "newton_schulz_gram", mutant)
+    assert _some_pin_fails(GRAM_PINS)
+
+
 @pytest.mark.parametrize("mutant", [_muon_decay_after, _muon_old_momentum_nesterov, _muon_min_scale])
 def test_muon_mutants_are_caught(monkeypatch, mutant):
     monkeypatch.setattr(omuon, "muon_update", mutant)
@@ -129,4 +184,4 @@ def test_adamw_mutants_are_caught(monkeypatch, mutant):
 
 
 def test_unmutated_oracle_passes_the_same_pins():
-    assert not _some_pin_fails(NS_PINS + MUON_PINS + ADAMW_PINS)
+    assert not _some_pin_fails(NS_PINS + GRAM_PINS + MUON_PINS + ADAMW_PINS)

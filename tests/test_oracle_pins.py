@@ -115,6 +115,47 @@ def test_ns_of_row_slices_is_not_ns_of_matrix():
     assert np.linalg.norm(parts - full) / np.linalg.norm(full) > 0.3
 
 
+# ------------------------------------------------------------------------------------------------ Gram-space iteration
+
+@pytest.mark.parametrize("shape", [(8, 16), (16, 8), (12, 12), (5, 9), (33, 7), (6, 40)])
+@pytest.mark.parametrize("coeffs", [CLASSIC5, PE8, [omuon.CLASSIC] * 1], ids=["classic5", "pe8", "classic1"])
+def test_gram_ns_equals_svd_closed_form(shape, coeffs):
+    """The Gram-space recurrence reaches U phi(Sigma / ||G||) V^T, the SVD closed form (not newton_schulz)."""
+    rng = np.random.default_rng(100 + sum(shape))
+    G = rng.standard_normal(shape)
+    got = omuon.newton_schulz_gram(G, coeffs)
+    ref = omuon.ns_closed_form(G, coeffs)
+    assert np.linalg.norm(got - ref) <= 1e-10 * max(1.0, np.linalg.norm(ref))
+
+
+def test_gram_ns_page_singular_value_example(golden_dir):
+    """The printed orthogonalisation example ("Muon: orthogonalising the update") through the Gram-space
+    recurrence: the same singular-value ranges and shares after 1, 3 and 5 steps."""
+    fx = read_golden(os.path.join(golden_dir, "ns_singular_value_example.txt"))
+    rng = np.random.default_rng(0)
+    U = _orth(256, 256, rng)
+    V = _orth(1024, 256, rng)
+    G = (U * np.logspace(0, -2, 256)) @ V.T
+    for steps in (1, 3, 5):
+        s = np.linalg.svd(omuon.newton_schulz_gram(G, [omuon.CLASSIC] * steps), compute_uv=False)
+        lo, hi, share = fx[str(steps)]
+        assert round(s.min(), 2) == lo and round(s.max(), 2) == hi
+        assert round(100 * np.mean((s > 0.7) & (s < 1.2))) == share
+
+
+@pytest.mark.parametrize("m", [4, 64])
+def test_gram_ns_equal_singular_values_input(m):
+    G = np.hstack([np.eye(m), np.zeros((m, 3 * m))])
+    out = omuon.newton_schulz_gram(G, PE8, eps=0.0)
+    np.testing.assert_allclose(out, omuon.compose_phi(1.0 / math.sqrt(m), PE8) * G, atol=1e-12)
+
+
+@pytest.mark.parametrize("shape", [(6, 30), (30, 6)])
+def test_gram_ns_transpose_symmetry(shape):
+    G = np.random.default_rng(7).standard_normal(shape)
+    assert np.array_equal(omuon.newton_schulz_gram(G.T, CLASSIC5), omuon.newton_schulz_gram(G, CLASSIC5).T)
+
+
 # ------------------------------------------------------------------------------------------------ Muon step
 
 HP = dict(lr=0.02, momentum=0.95, weight_decay=0.01)
