@@ -22,7 +22,9 @@ enum KernelKind : int32_t {
   KK_FINAL = 6,
   KK_DEBUG_WAIT = 7,
   KK_NS_SMALL = 8,
-  KK_COUNT = 9
+  KK_GRAM_SPACE = 9,
+  KK_GRAM32 = 10,
+  KK_COUNT = 11
 };
 
 // Launch bookkeeping (libmuon.cu): counts launches and, while tracing, records an event pair.
@@ -37,7 +39,9 @@ void debug_timeline(unsigned long long **buf, int *cap_per_cta);
 
 // ------------------------------------------------------------------------------------------ tensor-core GEMMs
 
-enum EpiKind : int { EPI_GRAM = 0, EPI_POLY = 1, EPI_APPLY = 2, EPI_FINAL = 3 };
+// EPI_GRAM32: the Gram matrix of a wide iterate with m <= 256 rows, stored in fp32 as a tf32 "hi" plane and
+// an fp32 "lo" plane (hi + lo = the value) for the Gram-space chain.
+enum EpiKind : int { EPI_GRAM = 0, EPI_POLY = 1, EPI_APPLY = 2, EPI_FINAL = 3, EPI_GRAM32 = 5 };
 
 constexpr int GEMM_MAX_PROBLEMS = 8;
 
@@ -63,6 +67,10 @@ struct GemmProblem {
   // bf16 output of gram / poly / apply
   __nv_bfloat16 *out;
   long long ld_out, mstride_out;
+  // fp32 output of the Gram-space Gram (EPI_GRAM32): hi plane at out32, lo plane at out32 + plane32, with the
+  // row and matrix pitches ld_out and mstride_out (elements)
+  float *out32;
+  long long plane32;
   // final step: parameter update (params != null) or dense store (out_dense != null); with master, the
   // update applies to the fp32 master copies and params receive them rounded to bf16
   void *const *params;
@@ -136,9 +144,15 @@ class GemmBatch {
                        const TileSync *sync = nullptr);
   muon_status add_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, const float *scale,
                        const TileSync *sync = nullptr);
+  // EPI_GRAM32 (x.rows <= 256): g = alpha * s^2 * x x^T as fp32 hi / lo planes
+  muon_status add_gram32(const Bf16Stack &x, float *g_hi, long long ldg, long long mstride_g, long long plane,
+                         float alpha, const float *scale);
   muon_status add_final(const Bf16Stack &h, const Bf16Stack &x, const float *scale, const FinalSpec &f,
                        const TileSync *sync = nullptr);
   muon_status launch(cudaStream_t s);
+  // Per-matrix counter waits replace the wait for the whole previous grid unless this is set: then the
+  // launches wait for both (used where the previous launch in the stream belongs to another branch)
+  void force_grid_wait(bool on) { grid_wait_ = on; }
   ~GemmBatch();
 
  private:
@@ -149,6 +163,7 @@ class GemmBatch {
   Item *items_ = nullptr;
   int n_ = 0, cap_ = 0;
   int force_ = -1;
+  bool grid_wait_ = false;
   muon_status push(const Item &it);
 };
 
@@ -191,6 +206,28 @@ struct SmallNsArgs {
 };
 bool ns_small_fits(long long m, long long n);
 muon_status launch_ns_small(const SmallNsArgs &a, cudaStream_t s);
+
+// ------------------------------------------------------------------------------------------ Gram-space chain
+
+// The Newton-Schulz iteration in the m x m Gram space (ns_gram_space.cu) for wide iterates with at most
+// GS_MAX_M rows that the fused small-matrix kernel does not take. Its scratch is GS_BUFFERS fp32 m x m matrices
+// per matrix of the stack (A, Q, P and two R), each as a hi and a lo plane with rows of round8(m) elements:
+// buffer b, plane p, matrix k at ((b * 2 + p) * K + k) * m * round8(m).
+constexpr int GS_MAX_M = 256;
+constexpr int GS_BUFFERS = 5;
+enum GsBuffer : int { GS_G = 0, GS_Q = 1, GS_P = 2, GS_R0 = 3, GS_R1 = 4 };
+inline bool gram_space_eligible(long long m, long long n) { return m >= 1 && m <= GS_MAX_M && !ns_small_fits(m, n); }
+size_t gram_space_plane_bytes(long long K, long long m);
+struct GramSpaceStack {
+  float *planes;             // the stack's scratch planes (16-byte aligned)
+  int K, m;
+  __nv_bfloat16 *r_out;      // R_N in bf16 for the final GEMM: matrix k at r_out + k * mstride_r, rows of ld_r
+  long long ld_r, mstride_r;
+};
+// From A_0 in buffer GS_G (written by an EPI_GRAM32 launch) to R_N in bf16, for every matrix of up to n stacks
+// (one launch per 8 stacks).
+muon_status launch_gram_space(const GramSpaceStack *stacks, int n, int ns_steps, const float *coeffs, uint32_t *err,
+                              unsigned long long timeout_ns, cudaStream_t s);
 
 // ------------------------------------------------------------------------------------------ elementwise
 
@@ -236,10 +273,11 @@ inline size_t header_bytes(long long total_K) {
 
 // One stack's sections (1024-byte aligned): K fp32 scales, the norm pass's per-tile partial sums, two bf16
 // iterates (K, m, ldx) and two bf16 (K, m, ldg) buffers for G and H; m = min(A, B), n = max(A, B), rows padded
-// to a multiple of 8 elements (16 bytes, as TMA requires).
+// to a multiple of 8 elements (16 bytes, as TMA requires); then, for shapes that can take the Gram-space path,
+// its fp32 planes (gram_space_plane_bytes).
 struct Layout {
   long long m, n, ldx, ldg, tiles_r, tiles_c;
-  size_t scale, partial, x0, x1, g, h, total;
+  size_t scale, partial, x0, x1, g, h, gs, total;   // gs: the Gram-space planes (shapes that can take that path)
 };
 
 inline Layout layout(long long K, long long A, long long B) {
@@ -263,6 +301,8 @@ inline Layout layout(long long K, long long A, long long B) {
   off = align_up(off + static_cast<size_t>(K) * L.m * L.ldg * 2, 1024);
   L.h = off;
   off = align_up(off + static_cast<size_t>(K) * L.m * L.ldg * 2, 1024);
+  L.gs = off;
+  if (gram_space_eligible(L.m, L.n)) off = align_up(off + gram_space_plane_bytes(K, L.m), 1024);
   L.total = off;
   return L;
 }

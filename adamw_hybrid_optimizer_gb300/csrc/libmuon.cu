@@ -81,6 +81,8 @@ unsigned long long g_timeout_ns = 2000000000ull;
 // grouped chain: per-matrix counter dependencies between launches: -1 where the rule in enqueue_grouped
 // allows them, 0 never, 1 always
 std::atomic<int> g_counter_deps{-1};
+// Gram-space path: -1 the rule (gram_space_route), 0 never, 1 wherever the shape is eligible
+std::atomic<int> g_gram_space{-1};
 
 }  // namespace
 
@@ -247,6 +249,41 @@ bool counter_deps_for(double est_us) {
   return mode == 1 || (mode == -1 && est_us <= 500.0);
 }
 
+// Whether a stack takes the Gram-space path: an eligible shape (m <= 256 and not the fused small-matrix
+// kernel's) whose long side is at least four times its short one, where the m x m chain (about 4 m^3 flops per
+// step in three tf32 passes) costs a fraction of the plain step's 4 m^2 n + 2 m^3 bf16 flops.
+bool gram_space_route(long long m, long long n) {
+  if (!gram_space_eligible(m, n)) return false;
+  const int mode = g_gram_space.load();
+  return mode == 1 || (mode == -1 && n >= 4 * m);
+}
+
+// The Gram-space path's launches for one stack, added to three batches: the fp32 Gram A_0 = s^2 U U^T of the
+// wide U in x0, the m x m chain (into gs), and the final step with R_N (bf16, in the H section) as its operand.
+muon_status add_gram_space(char *ws, const Layout &L, long long K, const FinalSpec &fin, GemmBatch &g32,
+                           std::vector<GramSpaceStack> &gs, GemmBatch &fin_batch) {
+  const float *scale = reinterpret_cast<const float *>(ws + L.scale);
+  float *planes = reinterpret_cast<float *>(ws + L.gs);
+  const long long ldm = round8(L.m), msm = L.m * ldm;
+  Bf16Stack X{ws + L.x0, L.m, L.n, L.ldx, L.m * L.ldx, K};
+  muon_status st = g32.add_gram32(X, planes, ldm, msm, K * msm, 1.0f, scale);
+  if (st != MUON_OK) return st;
+  __nv_bfloat16 *H = reinterpret_cast<__nv_bfloat16 *>(ws + L.h);
+  gs.push_back(GramSpaceStack{planes, static_cast<int>(K), static_cast<int>(L.m), H, L.ldg, L.m * L.ldg});
+  Bf16Stack Hs{H, L.m, L.m, L.ldg, L.m * L.ldg, K};
+  return fin_batch.add_final(Hs, X, scale, fin);
+}
+
+muon_status launch_gram_space_batches(GemmBatch &g32, const std::vector<GramSpaceStack> &gs, GemmBatch &fin_batch,
+                                      int ns_steps, const float *coeffs, uint32_t *err, cudaStream_t s) {
+  muon_status st;
+  if ((st = g32.launch(s)) != MUON_OK) return st;
+  if ((st = launch_gram_space(gs.data(), static_cast<int>(gs.size()), ns_steps, coeffs, err, g_timeout_ns, s)) !=
+      MUON_OK)
+    return st;
+  return fin_batch.launch(s);
+}
+
 // The Newton-Schulz chain of one stack. counters: the workspace's four counters per matrix (the norm
 // pass's, then the readiness of G, H and X), zeroed by the caller before the norm pass; norm_tiles: the
 // norm pass's tiles per matrix. With counter dependencies (counter_deps_for), each launch waits per matrix
@@ -254,6 +291,12 @@ bool counter_deps_for(double est_us) {
 muon_status run_ns_chain(uint32_t *err, char *ws, const Layout &L, long long K, int ns_steps, const float *coeffs,
                          const FinalSpec &fin, cudaStream_t s, uint32_t *counters, uint32_t norm_tiles) {
   if (ns_small_fits(L.m, L.n)) return launch_ns_small(small_args(err, ws, L, K, ns_steps, coeffs, fin), s);
+  if (gram_space_route(L.m, L.n)) {
+    GemmBatch g32(EPI_GRAM32, err, g_timeout_ns), fb(EPI_FINAL, err, g_timeout_ns);
+    std::vector<GramSpaceStack> gs;
+    muon_status st = add_gram_space(ws, L, K, fin, g32, gs, fb);
+    return st != MUON_OK ? st : launch_gram_space_batches(g32, gs, fb, ns_steps, coeffs, err, s);
+  }
   double est = 0.0;
   for (int kind = EPI_GRAM; kind <= EPI_APPLY; ++kind) est = std::max(est, launch_estimate_us(kind, L.m, L.n, K));
   const bool deps = counter_deps_for(est);
@@ -431,20 +474,38 @@ static muon_status enqueue_grouped(const muon_bucket *buckets, int n, const muon
     fin.lr_scale = static_cast<float>(static_cast<double>(hp->lr) * scale);
     return fin;
   };
-  // small buckets: the whole chain in one fused launch each
-  std::vector<char> small(n, 0);
+  // Launch order: the branches first (small buckets: the whole chain in one fused launch each; Gram-space
+  // buckets: fp32 Gram, m x m chain, final step), each launch waiting for the whole previous grid; then the
+  // plain chain of the other buckets. Where the plain chain's launches wait per matrix on counters, its first
+  // launch also waits for the previous grid, so that the step's last launch completes only after every branch.
+  std::vector<char> small(n, 0), gspace(n, 0);
+  bool branch = false;
   for (int i = 0; i < n; ++i) {
     if (!ns_small_fits(L[i].m, L[i].n)) continue;
     small[i] = 1;
+    branch = true;
     const SmallNsArgs sa = small_args(err, w[i], L[i], buckets[i].K, hp->ns_steps, hp->coeffs, final_spec(buckets[i]));
     if ((st = launch_ns_small(sa, s)) != MUON_OK) return st;
+  }
+  {
+    GemmBatch g32(EPI_GRAM32, err, to), fb(EPI_FINAL, err, to);
+    std::vector<GramSpaceStack> gs;
+    for (int i = 0; i < n; ++i) {
+      if (small[i] || !gram_space_route(L[i].m, L[i].n)) continue;
+      gspace[i] = 1;
+      if ((st = add_gram_space(w[i], L[i], buckets[i].K, final_spec(buckets[i]), g32, gs, fb)) != MUON_OK) return st;
+    }
+    if (!gs.empty()) {
+      branch = true;
+      if ((st = launch_gram_space_batches(g32, gs, fb, hp->ns_steps, hp->coeffs, err, s)) != MUON_OK) return st;
+    }
   }
   // per-matrix counter dependencies where the launches (all buckets of a step kind in one) are short
   double est_us = 0.0;
   for (int kind = EPI_GRAM; kind <= EPI_APPLY; ++kind) {
     double us = 0.0;
     for (int i = 0; i < n; ++i)
-      if (!small[i]) us += launch_estimate_us(kind, L[i].m, L[i].n, buckets[i].K);
+      if (!small[i] && !gspace[i]) us += launch_estimate_us(kind, L[i].m, L[i].n, buckets[i].K);
     est_us = std::max(est_us, us);
   }
   const bool deps = counter_deps_for(est_us);
@@ -453,8 +514,9 @@ static muon_status enqueue_grouped(const muon_bucket *buckets, int n, const muon
     const float a = hp->coeffs[3 * t], b = hp->coeffs[3 * t + 1], c = hp->coeffs[3 * t + 2];
     GemmBatch gram(EPI_GRAM, err, to), poly(EPI_POLY, err, to);
     GemmBatch last(t + 1 < hp->ns_steps ? EPI_APPLY : EPI_FINAL, err, to);
+    if (t == 0 && branch) gram.force_grid_wait(true);
     for (int i = 0, k0 = 0; i < n; k0 += static_cast<int>(buckets[i].K), ++i) {
-      if (small[i]) continue;
+      if (small[i] || gspace[i]) continue;
       const Layout &Li = L[i];
       const float *sc = t == 0 ? reinterpret_cast<const float *>(w[i] + Li.scale) : nullptr;
       const uint32_t e_gram = gemm_signals_per_matrix(EPI_GRAM, Li.m, Li.n);
@@ -603,7 +665,7 @@ muon_status muon_autotune(const muon_bucket *buckets, int n, void *ws, size_t ws
     L[i] = layout(buckets[i].K, buckets[i].A, buckets[i].B);
     w[i] = base + off;
     off += L[i].total;
-    if (ns_small_fits(L[i].m, L[i].n)) continue;
+    if (ns_small_fits(L[i].m, L[i].n) || gram_space_route(L[i].m, L[i].n)) continue;
     any = true;
     max_k = std::max(max_k, static_cast<int>((L[i].m + 63) / 64));
   }
@@ -612,7 +674,7 @@ muon_status muon_autotune(const muon_bucket *buckets, int n, void *ws, size_t ws
     GemmBatch poly(EPI_POLY, err, g_timeout_ns);
     poly.force_shape(shape);
     for (int i = 0; i < n; ++i) {
-      if (ns_small_fits(L[i].m, L[i].n)) continue;
+      if (ns_small_fits(L[i].m, L[i].n) || gram_space_route(L[i].m, L[i].n)) continue;
       const long long K = buckets[i].K, msg = L[i].m * L[i].ldg;
       Bf16Stack Gs{w[i] + L[i].g, L[i].m, L[i].m, L[i].ldg, msg, K};
       muon_status r = poly.add_poly(Gs, reinterpret_cast<__nv_bfloat16 *>(w[i] + L[i].h), L[i].ldg, msg, 3.4445f,
@@ -665,6 +727,17 @@ muon_status muon_debug_counter_deps(int32_t on) {
   if (on < -1 || on > 1) return MUON_ERR_INVALID_ARG;
   g_counter_deps.store(on);
   return MUON_OK;
+}
+
+muon_status muon_debug_gram_space(int32_t mode) {
+  if (mode < -1 || mode > 1) return MUON_ERR_INVALID_ARG;
+  g_gram_space.store(mode);
+  return MUON_OK;
+}
+
+int32_t muon_gram_space_route(int64_t A, int64_t B) {
+  if (A < 1 || B < 1) return 0;
+  return gram_space_route(std::min(A, B), std::max(A, B)) ? 1 : 0;
 }
 
 muon_status muon_debug_poly_shape(int32_t shape) {
@@ -963,6 +1036,8 @@ const char *muon_kernel_name(int32_t kind) {
     case KK_FINAL: return "ns_final";
     case KK_DEBUG_WAIT: return "debug_wait";
     case KK_NS_SMALL: return "ns_small";
+    case KK_GRAM_SPACE: return "ns_gram_space";
+    case KK_GRAM32: return "ns_gram_f32";
     default: return "unknown";
   }
 }

@@ -9,6 +9,7 @@
 //     X' = H X                      EPI_APPLY  (= a X + (b G + c G G) X); B operand X read N-major
 //     last step: u = H X, then p <- p - lr*wd*p*mask - lr*scale*u      EPI_FINAL (EPI_FINAL_MASTER: on fp32
 //                                                                      master copies of bf16 parameters)
+//     A_0 = s^2 X X^T for the Gram-space chain (m <= 256)  EPI_GRAM32  fp32 hi / lo planes, whole tile stored
 //
 // Design (sm_103a): CTAs run as pairs (clusters of two) on vertically adjacent 128 x 256 output tiles with
 // paired-SM MMAs (tcgen05 cta_group::2, M = 256): each CTA holds its 128 rows of A and one half of B, the
@@ -380,7 +381,39 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem &a, int b, int 
                                                const Region &rg, float *v) {
   const int row = warp_row0 + lane;
   const int rows = a.rows, cols = a.cols;
-  if constexpr (EPI == EPI_GRAM || EPI == EPI_POLY) {
+  if constexpr (EPI == EPI_GRAM32) {
+    // the whole m x m tile is computed (m <= 256: one tile pair per matrix); each lane stores its row's 32
+    // values as a tf32 hi plane (low 13 mantissa bits cleared) and an fp32 lo plane (the rest, exact)
+    float sc = a.alpha;
+    if (a.scale != nullptr) {
+      const float s = a.scale[b];
+      sc *= s * s;
+    }
+    if (row >= rows) return;
+    float *hi = a.out32 + static_cast<long long>(b) * a.mstride_out + static_cast<long long>(row) * a.ld_out + col0;
+    float *lo = hi + a.plane32;
+    auto split = [&](float x, float &h, float &l) {
+      h = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+      l = x - h;
+    };
+    if (col0 + 32 <= cols && (reinterpret_cast<uintptr_t>(hi) & 15) == 0 && (reinterpret_cast<uintptr_t>(lo) & 15) == 0) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float4 h, l;
+        split(v[4 * q] * sc, h.x, l.x);
+        split(v[4 * q + 1] * sc, h.y, l.y);
+        split(v[4 * q + 2] * sc, h.z, l.z);
+        split(v[4 * q + 3] * sc, h.w, l.w);
+        reinterpret_cast<float4 *>(hi)[q] = h;
+        reinterpret_cast<float4 *>(lo)[q] = l;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (col0 + j < cols) split(v[j] * sc, hi[j], lo[j]);
+    }
+    return;
+  } else if constexpr (EPI == EPI_GRAM || EPI == EPI_POLY) {
     if constexpr (EPI == EPI_POLY) {
       float gv[32];
       region_read_row(rg, lane, gv);
@@ -1082,6 +1115,23 @@ muon_status GemmBatch::add_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long 
   return push(it);
 }
 
+muon_status GemmBatch::add_gram32(const Bf16Stack &x, float *g_hi, long long ldg, long long mstride_g,
+                                  long long plane, float alpha, const float *scale) {
+  if (epi_ != EPI_GRAM32 || x.rows > 2 * BM) return MUON_ERR_INVALID_ARG;
+  Item it{};
+  if (!make_map(&it.ma, x.ptr, x.cols, x.rows, x.batch, x.ld, x.mstride, BM) ||
+      !make_map(&it.mb, x.ptr, x.cols, x.rows, x.batch, x.ld, x.mstride, BN))
+    return MUON_ERR_CUDA;
+  fill_tiles(it.p, x.batch, x.rows, x.rows, x.cols, false);   // one tile pair per matrix: the whole m x m
+  it.p.alpha = alpha;
+  it.p.scale = scale;
+  it.p.out32 = g_hi;
+  it.p.plane32 = plane;
+  it.p.ld_out = ldg;
+  it.p.mstride_out = mstride_g;
+  return push(it);
+}
+
 muon_status GemmBatch::add_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long ldh, long long mstride_h, float a,
                                 float b, float c, const TileSync *sync) {
   if (epi_ != EPI_POLY) return MUON_ERR_INVALID_ARG;
@@ -1176,6 +1226,7 @@ muon_status GemmBatch::launch(cudaStream_t s) {
     g.counter_deps = 1;
     for (int i = 0; i < cnt; ++i)
       if (g.prob[i].wait_ctr == nullptr) g.counter_deps = 0;
+    if (grid_wait_) g.counter_deps = 0;
     g.symmetric = (epi_ == EPI_GRAM || epi_ == EPI_POLY) ? 1 : 0;
     g.total_tiles = tiles;
     g.err = err_;
@@ -1190,6 +1241,7 @@ muon_status GemmBatch::launch(cudaStream_t s) {
     muon_status st;
     switch (epi_) {
       case EPI_GRAM: st = launch_shape<EPI_GRAM, false, 6, 1>(g, KK_GRAM, s); break;
+      case EPI_GRAM32: st = launch_shape<EPI_GRAM32, false, 6, 1>(g, KK_GRAM32, s); break;
       case EPI_POLY:
         st = shape == 0   ? launch_shape<EPI_POLY, false, 4, 5>(g, KK_POLY, s)
              : shape == 1 ? launch_shape<EPI_POLY, false, 5, 3>(g, KK_POLY, s)

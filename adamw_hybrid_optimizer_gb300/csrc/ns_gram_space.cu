@@ -1,0 +1,452 @@
+// The Newton-Schulz iteration in the Gram space ("DMuon: Efficient Distributed Muon Training with Near-Adam
+// Overhead", section 2.2 "Efficient Gram Newton-Schulz Iteration"): for a wide iterate X_0 (m x n, m <= n) the
+// chain runs on m x m matrices instead of m x n ones. With A_0 = X_0 X_0^T (computed by the tensor-core GEMM's
+// fp32 Gram epilogue before this kernel), per step t with coefficients (a, b, c):
+//     Q_t = a I + b A_t + c A_t A_t ;  R_{t+1} = Q_t R_t (R_1 = Q_0) ;  A_{t+1} = Q_t (Q_t A_t)
+// and X_N = R_N X_0, which the final-step GEMM applies with the parameter update. Every matrix here is a
+// polynomial in A_0, so all of them are symmetric and commute.
+//
+// Precision: forming A squares the condition number, so the m x m chain keeps fp32 accuracy. Each matrix is
+// stored as two fp32 planes, hi (the value with its low 13 mantissa bits cleared: exactly a tf32 number) and
+// lo (the rest, exact in fp32), and every product is three tf32 tensor-core passes, hi*hi + hi*lo + lo*hi,
+// accumulated in fp32 in tensor memory (the lo*lo term is below fp32 rounding).
+//
+// Design (sm_103a): one cluster of 4 CTAs per matrix (m in 129..256: CTA (bi, bj) owns the 128 x 128 output
+// block (bi, bj) of every product) or per 4 matrices (m <= 128: one block each). A CTA's operands are the rows
+// of its block of the left matrix and, since the right matrix is symmetric, the rows of its block column of
+// the right one (exactly the K-major B operand); TMA brings them in 32-column (128-byte) slices of hi and lo
+// planes through a 3-stage ring, one thread issues tcgen05.mma kind::tf32 (M = 128, N = 128, K = 8) into one
+// of two 128-column accumulators, and four epilogue warps (one per tensor-memory lane quarter) finish each
+// product: the polynomial Q = a I + b A + c acc, the hi / lo split, and the fp32 stores. The CTAs of a cluster
+// exchange results through global memory (L2-resident), one cluster barrier per phase:
+//     phase A: S = A A            -> Q (and R_1 = Q_0 at t = 0)
+//     phase B: P = Q A, R' = Q R  -> P, R'   (P not at the last step, R' not at t = 0)
+//     phase C: A' = Q P           -> A       (not at the last step)
+// R_N is also stored rounded to bf16 as the final GEMM's m x m operand. Every mbarrier wait is bounded; a wait
+// that runs out sets the error word, and the CTA then skips its remaining work but keeps taking part in every
+// cluster barrier (so no CTA of the cluster waits forever), drains its copies and MMAs, and frees its TMEM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace muon {
+
+namespace {
+
+constexpr int GS_THREADS = 192;          // warp 0 TMA, warp 1 MMA (+ TMEM owner), warps 2-5 epilogue
+constexpr int GS_BLOCK = 128;            // output block side, M and N of every MMA
+constexpr int GS_KC = 32;                // fp32 columns per slice: one 128-byte swizzled row
+constexpr int GS_TILE_BYTES = GS_BLOCK * GS_KC * 4;          // 16 KB
+constexpr int GS_STAGE_BYTES = 4 * GS_TILE_BYTES;            // A hi, A lo, B hi, B lo
+constexpr int GS_STAGES = 3;
+constexpr int GS_CLUSTER = 4;
+constexpr uint32_t GS_TMEM_COLS = 256;   // two 128-column accumulators
+constexpr int GS_MAX_PROBLEMS = 8;
+
+struct GsProblem {
+  float *planes;            // buffer b, plane p (0 hi, 1 lo), matrix k at ((b * 2 + p) * K + k) * m * ldm
+  __nv_bfloat16 *r_out;     // R_N in bf16: matrix k at r_out + k * mstride_r, rows of ld_r elements
+  long long ldm, ld_r, mstride_r;
+  long long unit_begin;     // first cluster of this problem in the launch
+  int K, m, mb;             // matrices, wide rows, 128-row blocks per side (1 or 2)
+};
+
+struct GsGroup {
+  CUtensorMap map[GS_MAX_PROBLEMS];   // fp32 (m, m, 10 K) over the planes, box 32 x 128, 128-byte swizzle
+  GsProblem prob[GS_MAX_PROBLEMS];
+  int nprob;
+  long long total_units;
+  int ns_steps;
+  float coeffs[3 * MUON_MAX_NS_STEPS];
+  uint32_t *err;
+  unsigned long long timeout_ns;
+};
+static_assert(sizeof(GsGroup) <= 4096, "kernel parameter block too large");
+
+struct GsCtrl {
+  uint64_t full[GS_STAGES];
+  uint64_t empty[GS_STAGES];
+  uint64_t acc_full[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+constexpr size_t GS_SMEM = static_cast<size_t>(GS_STAGES) * GS_STAGE_BYTES + sizeof(GsCtrl) + 1024;
+static_assert(GS_SMEM <= 232448, "shared memory over budget");
+
+// Epilogue kinds of one product.
+enum : int { EK_Q = 0, EK_P = 1, EK_A = 2, EK_R = 3 };
+
+struct Product {
+  int a_buf, b_buf, acc, kind, out_buf;
+};
+
+// The products of phase `ph` (0 = A, 1 = B, 2 = C) of step t; returns how many (0 if the phase is skipped).
+__device__ __forceinline__ int phase_products(int t, int ph, int N, Product *p) {
+  const int r_in = GS_R0 + ((t - 1) & 1), r_out = GS_R0 + (t & 1);
+  if (ph == 0) {
+    p[0] = {GS_G, GS_G, 0, EK_Q, GS_Q};
+    return 1;
+  }
+  if (ph == 1) {
+    int n = 0;
+    if (t < N - 1) p[n++] = {GS_Q, GS_G, 0, EK_P, GS_P};
+    if (t >= 1) p[n++] = {GS_Q, r_in, 1, EK_R, r_out};
+    return n;
+  }
+  if (t < N - 1) {
+    p[0] = {GS_Q, GS_P, 0, EK_A, GS_G};
+    return 1;
+  }
+  return 0;
+}
+
+__device__ __forceinline__ float tf32_hi(float v) { return __uint_as_float(__float_as_uint(v) & 0xFFFFE000u); }
+
+__device__ __forceinline__ int find_problem(const GsGroup &g, long long u) {
+  int p = 0;
+#pragma unroll 1
+  for (int q = 1; q < g.nprob; ++q)
+    if (u >= g.prob[q].unit_begin) p = q;
+  return p;
+}
+
+__device__ __forceinline__ float *plane(const GsProblem &P, int buf, int pl, int k) {
+  return P.planes + ((static_cast<long long>(buf) * 2 + pl) * P.K + k) * static_cast<long long>(P.m) * P.ldm;
+}
+
+// Stores 32 values of row `row`, columns col0 .. col0 + 31 of buffer `buf` as hi / lo planes (only columns < m).
+__device__ __forceinline__ void store_split(const GsProblem &P, int buf, int k, int row, int col0, const float *v) {
+  float *hi = plane(P, buf, 0, k) + static_cast<long long>(row) * P.ldm + col0;
+  float *lo = plane(P, buf, 1, k) + static_cast<long long>(row) * P.ldm + col0;
+  if (col0 + 32 <= P.m && (reinterpret_cast<uintptr_t>(hi) & 15) == 0 && (reinterpret_cast<uintptr_t>(lo) & 15) == 0) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float4 h, l;
+      h.x = tf32_hi(v[4 * q]);
+      h.y = tf32_hi(v[4 * q + 1]);
+      h.z = tf32_hi(v[4 * q + 2]);
+      h.w = tf32_hi(v[4 * q + 3]);
+      l.x = v[4 * q] - h.x;
+      l.y = v[4 * q + 1] - h.y;
+      l.z = v[4 * q + 2] - h.z;
+      l.w = v[4 * q + 3] - h.w;
+      reinterpret_cast<float4 *>(hi)[q] = h;
+      reinterpret_cast<float4 *>(lo)[q] = l;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (col0 + j >= P.m) break;
+      const float h = tf32_hi(v[j]);
+      hi[j] = h;
+      lo[j] = v[j] - h;
+    }
+  }
+}
+
+__device__ __forceinline__ void load_full(const GsProblem &P, int buf, int k, int row, int col0, float *v) {
+  const float *hi = plane(P, buf, 0, k) + static_cast<long long>(row) * P.ldm + col0;
+  const float *lo = plane(P, buf, 1, k) + static_cast<long long>(row) * P.ldm + col0;
+  if (col0 + 32 <= P.m && (reinterpret_cast<uintptr_t>(hi) & 15) == 0 && (reinterpret_cast<uintptr_t>(lo) & 15) == 0) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 h = reinterpret_cast<const float4 *>(hi)[q];
+      const float4 l = reinterpret_cast<const float4 *>(lo)[q];
+      v[4 * q] = h.x + l.x;
+      v[4 * q + 1] = h.y + l.y;
+      v[4 * q + 2] = h.z + l.z;
+      v[4 * q + 3] = h.w + l.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = col0 + j < P.m ? hi[j] + lo[j] : 0.f;
+  }
+}
+
+__global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS, 1)
+    gram_space_kernel(const __grid_constant__ GsGroup args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  GsCtrl *ctrl = reinterpret_cast<GsCtrl *>(smem + GS_STAGES * GS_STAGE_BYTES);
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < GS_STAGES; ++s) {
+      mbar_init(&ctrl->full[s], 1);
+      mbar_init(&ctrl->empty[s], 1);
+    }
+    mbar_init(&ctrl->acc_full[0], 1);
+    mbar_init(&ctrl->acc_full[1], 1);
+    mbar_init(&ctrl->drain, 1);
+    ctrl->abort_flag = 0;
+    fence_mbar_init();
+  }
+  // this CTA's matrix and output block
+  const long long unit = blockIdx.x / GS_CLUSTER;
+  const int pi = find_problem(args, unit);
+  const GsProblem P = args.prob[pi];
+  const long long lu = unit - P.unit_begin;
+  const int k = P.mb == 2 ? static_cast<int>(lu) : static_cast<int>(lu * GS_CLUSTER + rank);
+  const int bi = P.mb == 2 ? static_cast<int>(rank >> 1) : 0;
+  const int bj = P.mb == 2 ? static_cast<int>(rank & 1) : 0;
+  const bool active = k < P.K;
+  const CUtensorMap *map = &args.map[pi];
+  if (warp == 0 && lane == 0) tma_prefetch_desc(map);
+  if (warp == 1) {
+    tmem_alloc(&ctrl->tmem_base, GS_TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // A_0 (and the scratch planes) are written by the previous kernel: read only once it has completed
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  const uint32_t tmem = ctrl->tmem_base;
+  WaitCtl ctl{&ctrl->abort_flag, args.err, args.timeout_ns};
+  const int N = args.ns_steps;
+  const int kchunks = (P.m + GS_KC - 1) / GS_KC;
+  constexpr uint32_t idesc = idesc_tf32_f32(GS_BLOCK, GS_BLOCK);
+
+  // pipeline state, carried across products and phases
+  uint32_t stage = 0, sphase = 0;
+  int last_parity[GS_STAGES] = {-1, -1, -1};
+  uint32_t acc_uses[2] = {0u, 0u};
+  bool issued = false;
+
+#pragma unroll 1
+  for (int t = 0; t < N; ++t) {
+    const float ca = args.coeffs[3 * t], cb = args.coeffs[3 * t + 1], cc = args.coeffs[3 * t + 2];
+#pragma unroll 1
+    for (int ph = 0; ph < 3; ++ph) {
+      Product prods[2];
+      const int np = phase_products(t, ph, N, prods);
+      if (np == 0) continue;   // the same for every CTA of the cluster: no barrier for a skipped phase
+      const bool work = active && ctrl->abort_flag == 0;
+      if (warp == 0) {
+        if (lane == 0 && work) {
+          // ------------------------------------------------------------ TMA producer
+          fence_proxy_async_global();   // the planes were written by generic stores before the last barrier
+          bool ok = true;
+          for (int q = 0; q < np && ok; ++q) {
+            const int za = (prods[q].a_buf * 2) * P.K + k, zb = (prods[q].b_buf * 2) * P.K + k;
+            for (int c = 0; c < kchunks; ++c) {
+              if (!wait_bounded(&ctrl->empty[stage], sphase ^ 1u, ctl, ERR_WAIT_EMPTY)) {
+                ok = false;
+                break;
+              }
+              uint8_t *st = smem + stage * GS_STAGE_BYTES;
+              mbar_arrive_expect_tx(&ctrl->full[stage], GS_STAGE_BYTES);
+              last_parity[stage] = static_cast<int>(sphase);
+              tma_load_3d(st, map, &ctrl->full[stage], c * GS_KC, bi * GS_BLOCK, za);
+              tma_load_3d(st + GS_TILE_BYTES, map, &ctrl->full[stage], c * GS_KC, bi * GS_BLOCK, za + P.K);
+              tma_load_3d(st + 2 * GS_TILE_BYTES, map, &ctrl->full[stage], c * GS_KC, bj * GS_BLOCK, zb);
+              tma_load_3d(st + 3 * GS_TILE_BYTES, map, &ctrl->full[stage], c * GS_KC, bj * GS_BLOCK, zb + P.K);
+              if (++stage == GS_STAGES) {
+                stage = 0;
+                sphase ^= 1u;
+              }
+            }
+          }
+        }
+      } else if (warp == 1) {
+        if (lane == 0 && work) {
+          // ------------------------------------------------------------ MMA issuer
+          tc_fence_after();
+          bool ok = true;
+          for (int q = 0; q < np && ok; ++q) {
+            const uint32_t d = tmem + static_cast<uint32_t>(prods[q].acc * GS_BLOCK);
+            for (int c = 0; c < kchunks; ++c) {
+              if (!wait_bounded(&ctrl->full[stage], sphase, ctl, ERR_WAIT_FULL)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t a_hi = smem_u32(smem + stage * GS_STAGE_BYTES);
+              const uint32_t a_lo = a_hi + GS_TILE_BYTES, b_hi = a_hi + 2 * GS_TILE_BYTES,
+                             b_lo = a_hi + 3 * GS_TILE_BYTES;
+#pragma unroll
+              for (int kk = 0; kk < GS_KC / 8; ++kk) {
+                const uint64_t ah = smem_desc_sw128(a_hi + kk * 32, 16, 1024);
+                const uint64_t al = smem_desc_sw128(a_lo + kk * 32, 16, 1024);
+                const uint64_t bh = smem_desc_sw128(b_hi + kk * 32, 16, 1024);
+                const uint64_t bl = smem_desc_sw128(b_lo + kk * 32, 16, 1024);
+                tc_mma_tf32(d, ah, bh, idesc, (c | kk) != 0 ? 1u : 0u);
+                tc_mma_tf32(d, ah, bl, idesc, 1u);
+                tc_mma_tf32(d, al, bh, idesc, 1u);
+              }
+              issued = true;
+              tc_commit(&ctrl->empty[stage]);
+              if (++stage == GS_STAGES) {
+                stage = 0;
+                sphase ^= 1u;
+              }
+            }
+            if (ok) tc_commit(&ctrl->acc_full[prods[q].acc]);
+          }
+        }
+      } else {
+        // -------------------------------------------------------------- epilogue (warps 2..5)
+        const int quarter = warp & 3;               // tensor-memory lanes this warp may read
+        const int row = bi * GS_BLOCK + quarter * 32 + lane;
+        for (int q = 0; q < np; ++q) {
+          const Product pr = prods[q];
+          const uint32_t par = acc_uses[pr.acc] & 1u;
+          acc_uses[pr.acc] += 1u;
+          if (!work) continue;
+          const bool ok = wait_bounded(&ctrl->acc_full[pr.acc], par, ctl, ERR_WAIT_ACC_FULL);
+          if (!__all_sync(0xffffffffu, ok)) continue;
+          tc_fence_after();
+#pragma unroll 1
+          for (int cc4 = 0; cc4 < GS_BLOCK / 32; ++cc4) {
+            const int col0 = bj * GS_BLOCK + cc4 * 32;
+            if (col0 >= P.m) break;   // warp-uniform
+            float v[32];
+            tmem_ld_32x32b_x32(tmem + static_cast<uint32_t>(pr.acc * GS_BLOCK + cc4 * 32) +
+                                   (static_cast<uint32_t>(quarter * 32) << 16),
+                               v);
+            if (row >= P.m) continue;
+            if (pr.kind == EK_Q) {
+              float g[32];
+              load_full(P, GS_G, k, row, col0, g);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = fmaf(cc, v[j], fmaf(cb, g[j], col0 + j == row ? ca : 0.f));
+              if (t == 0 && N > 1) store_split(P, GS_R0, k, row, col0, v);
+            }
+            store_split(P, pr.out_buf, k, row, col0, v);
+            // R_N rounded to bf16 for the final GEMM: at t = 0 when N = 1 (R_1 = Q_0), else from the last R product
+            if ((pr.kind == EK_Q && N == 1) || (pr.kind == EK_R && t == N - 1)) {
+              __nv_bfloat16 *dst = P.r_out + static_cast<long long>(k) * P.mstride_r + static_cast<long long>(row) * P.ld_r;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (col0 + j < P.m) dst[col0 + j] = __float2bfloat16_rn(v[j]);
+            }
+          }
+        }
+        __threadfence();   // this phase's stores are visible GPU-wide before the cluster barrier releases them
+      }
+      // ---------------------------------------------------------------- phase barrier (every thread of the cluster)
+      tc_fence_before();
+      __syncwarp();
+      cluster_sync();
+      tc_fence_after();
+    }
+  }
+
+  // teardown: every armed stage's copies have landed and every MMA has completed before the CTA exits
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < GS_STAGES; ++s)
+      if (last_parity[s] >= 0) drain_wait(&ctrl->full[s], static_cast<uint32_t>(last_parity[s]), ctl);
+  }
+  if (warp == 1 && lane == 0 && issued) {
+    tc_commit(&ctrl->drain);
+    drain_wait(&ctrl->drain, 0u, ctl);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, GS_TMEM_COLS);
+  }
+}
+
+// The driver's tensor-map encoder, fetched through the runtime so the library needs no -lcuda.
+using EncodeTiledFn = decltype(&cuTensorMapEncodeTiled);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+size_t gram_space_plane_bytes(long long K, long long m) {
+  return static_cast<size_t>(GS_BUFFERS) * 2 * static_cast<size_t>(K) * static_cast<size_t>(m) *
+         static_cast<size_t>(round8(m)) * 4;
+}
+
+muon_status launch_gram_space(const GramSpaceStack *stacks, int n, int ns_steps, const float *coeffs, uint32_t *err,
+                              unsigned long long timeout_ns, cudaStream_t s) {
+  if (n < 1 || ns_steps < 1 || ns_steps > MUON_MAX_NS_STEPS) return MUON_ERR_INVALID_ARG;
+  auto enc = encode_fn();
+  if (enc == nullptr) return MUON_ERR_CUDA;
+  static std::once_flag attr_once[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::call_once(attr_once[dev & 63], [] {
+    cudaFuncSetAttribute(gram_space_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(GS_SMEM));
+  });
+  for (int first = 0; first < n; first += GS_MAX_PROBLEMS) {
+    const int cnt = n - first < GS_MAX_PROBLEMS ? n - first : GS_MAX_PROBLEMS;
+    GsGroup g;
+    memset(&g, 0, sizeof(g));
+    long long units = 0;
+    for (int i = 0; i < cnt; ++i) {
+      const GramSpaceStack &st = stacks[first + i];
+      if (st.m < 1 || st.m > GS_MAX_M || st.K < 1) return MUON_ERR_INVALID_ARG;
+      GsProblem &P = g.prob[i];
+      P.planes = st.planes;
+      P.r_out = st.r_out;
+      P.ldm = round8(st.m);
+      P.ld_r = st.ld_r;
+      P.mstride_r = st.mstride_r;
+      P.K = st.K;
+      P.m = st.m;
+      P.mb = st.m > GS_BLOCK ? 2 : 1;
+      P.unit_begin = units;
+      units += P.mb == 2 ? st.K : (st.K + GS_CLUSTER - 1) / GS_CLUSTER;
+      cuuint64_t dims[3] = {static_cast<cuuint64_t>(st.m), static_cast<cuuint64_t>(st.m),
+                            static_cast<cuuint64_t>(2 * GS_BUFFERS) * static_cast<cuuint64_t>(st.K)};
+      cuuint64_t strides[2] = {static_cast<cuuint64_t>(P.ldm) * 4,
+                               static_cast<cuuint64_t>(P.ldm) * static_cast<cuuint64_t>(st.m) * 4};
+      cuuint32_t box[3] = {static_cast<cuuint32_t>(GS_KC), static_cast<cuuint32_t>(GS_BLOCK), 1u};
+      cuuint32_t estr[3] = {1u, 1u, 1u};
+      if (enc(&g.map[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, st.planes, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return MUON_ERR_CUDA;
+    }
+    g.nprob = cnt;
+    g.total_units = units;
+    g.ns_steps = ns_steps;
+    for (int i = 0; i < 3 * ns_steps; ++i) g.coeffs[i] = coeffs[i];
+    g.err = err;
+    g.timeout_ns = timeout_ns;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(GS_CLUSTER * units));
+    cfg.blockDim = dim3(GS_THREADS);
+    cfg.dynamicSmemBytes = GS_SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    launch_begin(KK_GRAM_SPACE, s);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, gram_space_kernel, g);
+    launch_end(s);
+    if (e != cudaSuccess) return MUON_ERR_CUDA;
+  }
+  return MUON_OK;
+}
+
+}  // namespace muon

@@ -90,6 +90,8 @@ SIGNATURES = {
     "muon_autotune_reset": (None, []),
     "muon_debug_poly_shape": (ctypes.c_int, [ctypes.c_int32]),
     "muon_debug_counter_deps": (ctypes.c_int, [ctypes.c_int32]),
+    "muon_debug_gram_space": (ctypes.c_int, [ctypes.c_int32]),
+    "muon_gram_space_route": (ctypes.c_int32, [_c_int64, _c_int64]),
     "muon_check": (ctypes.c_int, [_vp, _vp]),
     "muon_set_timeout_ns": (None, [ctypes.c_uint64]),
     "muon_debug_wait_timeout": (ctypes.c_int, [_vp, ctypes.c_size_t, ctypes.c_uint64, _vp]),
@@ -373,6 +375,15 @@ def muon_debug_poly_shape(shape: int):
 def muon_debug_counter_deps(mode: int):
     """1: counter dependencies in the grouped chain, 0: launch order, -1: the library's rule (default)."""
     _check(lib().muon_debug_counter_deps(int(mode)), "muon_debug_counter_deps")
+
+
+def muon_debug_gram_space(mode: int):
+    """Gram-space Newton-Schulz path: -1 the library's rule (default), 0 never, 1 wherever the shape allows it."""
+    _check(lib().muon_debug_gram_space(int(mode)), "muon_debug_gram_space")
+
+
+def muon_gram_space_route(A: int, B: int) -> bool:
+    return bool(lib().muon_gram_space_route(int(A), int(B)))
 
 
 def muon_check(ws, stream=None) -> int:

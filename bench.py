@@ -578,7 +578,9 @@ def run_config_sweep(args):
     peaks, peak_src = load_peaks()
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
-    for name, steps in (("tiny", 50), ("aspect", 5), ("llama8b", 3)):
+    sweep = [("tiny", 50, -1), ("aspect", 5, -1), ("aspect", 5, 0), ("llama8b", 3, -1)]
+    for name, steps, gram_mode in sweep:
+        L.muon_debug_gram_space(gram_mode)
         w = workloads.workload(name)
         plan = L.muon_plan_buckets(workloads.shape_list(w))
         dt = "f32" if w.muon_dtype == "f32" else "bf16"
@@ -647,6 +649,8 @@ def run_config_sweep(args):
                 raise RuntimeError(f"device wait ran out in the {name} configuration")
             t_adamw = max(t_adamw, 1e-9)
             print(json.dumps({"config": name, "counter_deps": deps, "muon_matrices": sum(plan["bucket_K"]),
+                              "gram_space": {f"{A}x{B}": L.muon_gram_space_route(A, B)
+                                             for (A, B) in plan["bucket_shapes"]},
                               "buckets": len(plan["bucket_K"]), "muon_ms": round(t_muon, 4),
                               "ns_tflops_nominal": round(nominal / (t_muon * 1e-3) / 1e12, 1),
                               "ns_frac_nominal": round(nominal / (t_muon * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
@@ -655,6 +659,7 @@ def run_config_sweep(args):
                               "adamw_frac_hbm": round(abytes / (t_adamw * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                               "traced_ms_per_kind": per_kind, "peaks": f"{peak_src}"}), flush=True)
         L.muon_debug_counter_deps(-1)
+        L.muon_debug_gram_space(-1)
         del specs, keep, arr, ws, ap, ag, am, av, aspecs, atensors
         torch.cuda.empty_cache()
     return 0

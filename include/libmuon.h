@@ -81,7 +81,8 @@ typedef struct {
  * matrix's Gram, polynomial and iterate, through which the Newton-Schulz launches can wait per
  * matrix instead of per launch), which every call clears itself before its first launch; then K fp32
  * norm scales, per-tile norm partial sums, two bf16 iterates of (K, min, max) with rows
- * padded to a multiple of 8 elements, and two bf16 (K, min, min) Gram buffers.
+ * padded to a multiple of 8 elements, two bf16 (K, min, min) Gram buffers, and, for shapes that can take
+ * the Gram-space path (muon_debug_gram_space), its fp32 scratch.
  * Returns 0 if K, A or B is not positive. */
 size_t muon_workspace_bytes(int64_t K, int64_t A, int64_t B);
 
@@ -299,6 +300,24 @@ void muon_set_timeout_ns(uint64_t ns);
 /* Forces every poly launch onto one pipeline shape (0, 1 or 2 as in muon_autotune_poly_shape), or -1
  * to go back to the table and the rule; for tests and sweeps. MUON_ERR_INVALID_ARG outside -1..2. */
 muon_status muon_debug_poly_shape(int32_t shape);
+
+/* The Newton-Schulz iteration in the Gram space ([P4] section 2.2, "Efficient Gram Newton-Schulz Iteration"):
+ * for a wide iterate X_0 (m x n, m = min(A,B) <= n) the chain runs on m x m matrices, A_0 = X_0 X_0^T,
+ * Q_t = a_t I + b_t A_t + c_t A_t^2, R_{t+1} = Q_t R_t, A_{t+1} = Q_t A_t Q_t, and X_N = R_N X_0 -- the same
+ * result as the plain iteration, at O(m^3) instead of O(m^2 n) per step. A_0 is accumulated in fp32 from the
+ * bf16 iterate; the m x m chain keeps fp32 accuracy (three tf32 tensor-core passes per product on hi / lo
+ * splits); R_N is rounded to bf16 for the final product, which applies the parameter update as the plain
+ * path's last step does.
+ * Shapes that can take it: m <= 256 and not the fused small-matrix kernel's (m <= 128 with n <= 256); their
+ * workspace (muon_workspace_bytes) includes 40*K*m*round8(m) bytes of fp32 scratch for it.
+ * muon_step_batched, muon_step_grouped, hybrid_step and ns_orthogonalize take it where
+ * muon_gram_space_route says so: by default for those shapes with n >= 4*m.
+ * muon_debug_gram_space: -1 the default rule, 0 never, 1 for every shape that can take it (for tests and
+ * measurements). MUON_ERR_INVALID_ARG for other values. */
+muon_status muon_debug_gram_space(int32_t mode);
+
+/* 1 if a (A, B) matrix takes the Gram-space path under the current mode, else 0 (also for A or B < 1). */
+int32_t muon_gram_space_route(int64_t A, int64_t B);
 
 /* Grouped chain scheduling (muon_step_grouped, hybrid_step). 1: each launch of the Newton-Schulz chain
  * waits per matrix on counters its predecessor raises, so that launches overlap. 0: each launch waits for

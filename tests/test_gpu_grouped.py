@@ -149,3 +149,21 @@ def test_workspace_reused_by_another_layout(L):
     got = grouped(fresh)
     for a, b in zip(got, ref):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("deps", [1, 0])
+def test_grouped_equals_per_bucket_with_every_path(L, deps):
+    """Buckets on all three paths in one grouped call: the fused small-matrix chain, the Gram-space chain (one
+    and two 128-row blocks, wide and tall, a cluster left partly idle) and the plain GEMM chain, with the plain
+    chain's launches overlapping through counters (1) or in launch order (0). The branches run first and the
+    plain chain's first launch waits for them; every result equals the per-bucket calls bit for bit."""
+    shapes = [(3, 64, 128), (2, 256, 2048), (3, 100, 1000), (2, 2048, 200), (2, 512, 768), (1, 40, 1)]
+    assert L.muon_gram_space_route(256, 2048) and L.muon_gram_space_route(100, 1000)
+    assert L.muon_gram_space_route(2048, 200) and not L.muon_gram_space_route(512, 768)
+    hp = workloads.workload("aspect").muon_hp
+    L.muon_debug_counter_deps(deps)
+    try:
+        ps = _run_both(L, shapes, torch.bfloat16, hp, seed=6)
+    finally:
+        L.muon_debug_counter_deps(-1)
+    assert all(torch.isfinite(p.float()).all() for p in ps)
