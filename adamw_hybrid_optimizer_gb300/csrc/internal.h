@@ -11,6 +11,9 @@
 
 namespace muon {
 
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline long long round8(long long v) { return (v + 7) / 8 * 8; }
+
 // Kernel kinds, for launch counting and the event trace.
 enum KernelKind : int32_t {
   KK_ADAMW = 0,
@@ -55,6 +58,8 @@ struct GemmProblem {
   int m_pairs;            // tile rows are processed in vertically adjacent pairs, one per CTA of a cluster
   int tiles_per_matrix;   // tile pairs per matrix
   int k_iters;            // contraction / 64, rounded up
+  int k_wrap;             // 0, or: 64-deep steps kk >= k_wrap read B's rows from (kk - k_wrap) * 64 (the final
+                          // step of the Gram-space path: [R_hi | R_lo] times [X; X])
   long long tile_begin;   // first tile pair of this problem in the launch's pair space
   // per-matrix readiness counters (see TileSync), indexed by the matrix within the problem; null: none
   const uint32_t *wait_ctr;
@@ -148,7 +153,7 @@ class GemmBatch {
   muon_status add_gram32(const Bf16Stack &x, float *g_hi, long long ldg, long long mstride_g, long long plane,
                          float alpha, const float *scale);
   muon_status add_final(const Bf16Stack &h, const Bf16Stack &x, const float *scale, const FinalSpec &f,
-                       const TileSync *sync = nullptr);
+                       const TileSync *sync = nullptr, int k_wrap = 0);
   muon_status launch(cudaStream_t s);
   // Per-matrix counter waits replace the wait for the whole previous grid unless this is set: then the
   // launches wait for both (used where the previous launch in the stream belongs to another branch)
@@ -212,18 +217,23 @@ muon_status launch_ns_small(const SmallNsArgs &a, cudaStream_t s);
 // The Newton-Schulz iteration in the m x m Gram space (ns_gram_space.cu) for wide iterates with at most
 // GS_MAX_M rows that the fused small-matrix kernel does not take. Its scratch is GS_BUFFERS fp32 m x m matrices
 // per matrix of the stack (A, Q, P and two R), each as a hi and a lo plane with rows of round8(m) elements:
-// buffer b, plane p, matrix k at ((b * 2 + p) * K + k) * m * round8(m).
+// buffer b, plane p, matrix k at ((b * 2 + p) * K + k) * m * round8(m); then R_N for the final product as two
+// bf16 halves side by side, [R_hi | R_lo] (R_hi = R_N rounded, R_lo = the rest rounded), each half 64-column
+// padded with zeros: K matrices of m rows x 2 * round64(m) columns.
 constexpr int GS_MAX_M = 256;
 constexpr int GS_BUFFERS = 5;
 enum GsBuffer : int { GS_G = 0, GS_Q = 1, GS_P = 2, GS_R0 = 3, GS_R1 = 4 };
 inline bool gram_space_eligible(long long m, long long n) { return m >= 1 && m <= GS_MAX_M && !ns_small_fits(m, n); }
 size_t gram_space_plane_bytes(long long K, long long m);
+inline long long round64(long long v) { return (v + 63) / 64 * 64; }
 struct GramSpaceStack {
-  float *planes;             // the stack's scratch planes (16-byte aligned)
+  float *planes;             // the stack's scratch (16-byte aligned): fp32 planes, then [R_hi | R_lo]
   int K, m;
-  __nv_bfloat16 *r_out;      // R_N in bf16 for the final GEMM: matrix k at r_out + k * mstride_r, rows of ld_r
-  long long ld_r, mstride_r;
 };
+// The [R_hi | R_lo] halves of a stack's scratch.
+inline __nv_bfloat16 *gram_space_rsplit(float *planes, long long K, long long m) {
+  return reinterpret_cast<__nv_bfloat16 *>(planes + static_cast<long long>(GS_BUFFERS) * 2 * K * m * round8(m));
+}
 // From A_0 in buffer GS_G (written by an EPI_GRAM32 launch) to R_N in bf16, for every matrix of up to n stacks
 // (one launch per 8 stacks).
 muon_status launch_gram_space(const GramSpaceStack *stacks, int n, int ns_steps, const float *coeffs, uint32_t *err,
@@ -265,8 +275,6 @@ static_assert(sizeof(NesterovGroup) <= 4096, "kernel parameter block too large")
 // launch. Each stack's sections follow, stack after stack; their offsets are relative to the stack's start.
 constexpr size_t CTRL_BYTES = 256;
 
-inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-inline long long round8(long long v) { return (v + 7) / 8 * 8; }
 inline size_t header_bytes(long long total_K) {
   return align_up(CTRL_BYTES + static_cast<size_t>(total_K) * 16, 1024);
 }

@@ -259,7 +259,7 @@ bool gram_space_route(long long m, long long n) {
 }
 
 // The Gram-space path's launches for one stack, added to three batches: the fp32 Gram A_0 = s^2 U U^T of the
-// wide U in x0, the m x m chain (into gs), and the final step with R_N (bf16, in the H section) as its operand.
+// wide U in x0, the m x m chain (into gs), and the final step with [R_hi | R_lo] times [U; U] (scaled by s).
 muon_status add_gram_space(char *ws, const Layout &L, long long K, const FinalSpec &fin, GemmBatch &g32,
                            std::vector<GramSpaceStack> &gs, GemmBatch &fin_batch) {
   const float *scale = reinterpret_cast<const float *>(ws + L.scale);
@@ -268,10 +268,10 @@ muon_status add_gram_space(char *ws, const Layout &L, long long K, const FinalSp
   Bf16Stack X{ws + L.x0, L.m, L.n, L.ldx, L.m * L.ldx, K};
   muon_status st = g32.add_gram32(X, planes, ldm, msm, K * msm, 1.0f, scale);
   if (st != MUON_OK) return st;
-  __nv_bfloat16 *H = reinterpret_cast<__nv_bfloat16 *>(ws + L.h);
-  gs.push_back(GramSpaceStack{planes, static_cast<int>(K), static_cast<int>(L.m), H, L.ldg, L.m * L.ldg});
-  Bf16Stack Hs{H, L.m, L.m, L.ldg, L.m * L.ldg, K};
-  return fin_batch.add_final(Hs, X, scale, fin);
+  gs.push_back(GramSpaceStack{planes, static_cast<int>(K), static_cast<int>(L.m)});
+  const long long mp = round64(L.m);
+  Bf16Stack Rs{gram_space_rsplit(planes, K, L.m), L.m, 2 * mp, 2 * mp, L.m * 2 * mp, K};
+  return fin_batch.add_final(Rs, X, scale, fin, nullptr, static_cast<int>(mp / 64));
 }
 
 muon_status launch_gram_space_batches(GemmBatch &g32, const std::vector<GramSpaceStack> &gs, GemmBatch &fin_batch,

@@ -685,11 +685,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
             // K-major: those rows of the same tensor through the A map (box 64 x 128)
             tma_load_3d_pair(sb, map_a, fb, kk * BK, tj * BN + (BN / 2) * static_cast<int>(rank), b);
           } else {
-            // N-major: column chunks 2*rank and 2*rank+1 (64 columns each)
+            // N-major: column chunks 2*rank and 2*rank+1 (64 columns each); with k_wrap, the second half of the
+            // contraction reads B's rows again from the top
+            const int kb = (P.k_wrap > 0 && kk >= P.k_wrap) ? kk - P.k_wrap : kk;
 #pragma unroll
             for (int q = 0; q < 2; ++q)
               tma_load_3d_pair(sb + q * (64 * BK * 2), map_b, fb, tj * BN + 64 * (2 * static_cast<int>(rank) + q),
-                               kk * BK, b);
+                               kb * BK, b);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -1166,11 +1168,12 @@ muon_status GemmBatch::add_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bf
 }
 
 muon_status GemmBatch::add_final(const Bf16Stack &h, const Bf16Stack &x, const float *scale, const FinalSpec &f,
-                                 const TileSync *sync) {
-  if (epi_ != EPI_FINAL) return MUON_ERR_INVALID_ARG;
+                                 const TileSync *sync, int k_wrap) {
+  if (epi_ != EPI_FINAL || k_wrap < 0 || (k_wrap > 0 && h.cols != 2LL * k_wrap * BK)) return MUON_ERR_INVALID_ARG;
   Item it{};
   if (!apply_maps(h, x, &it.ma, &it.mb)) return MUON_ERR_CUDA;
   fill_tiles(it.p, x.batch, x.rows, x.cols, h.cols, false);
+  it.p.k_wrap = k_wrap;
   it.p.scale = scale;
   it.p.params = f.params;
   it.p.master = f.master;

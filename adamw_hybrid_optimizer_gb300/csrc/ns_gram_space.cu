@@ -3,8 +3,8 @@
 // chain runs on m x m matrices instead of m x n ones. With A_0 = X_0 X_0^T (computed by the tensor-core GEMM's
 // fp32 Gram epilogue before this kernel), per step t with coefficients (a, b, c):
 //     Q_t = a I + b A_t + c A_t A_t ;  R_{t+1} = Q_t R_t (R_1 = Q_0) ;  A_{t+1} = Q_t (Q_t A_t)
-// and X_N = R_N X_0, which the final-step GEMM applies with the parameter update. Every matrix here is a
-// polynomial in A_0, so all of them are symmetric and commute.
+// and X_N = R_N X_0, which the final-step GEMM applies with the parameter update (as R_hi X_0 + R_lo X_0).
+// Every matrix here is a polynomial in A_0, so all of them are symmetric and commute.
 //
 // Precision: forming A squares the condition number, so the m x m chain keeps fp32 accuracy. Each matrix is
 // stored as two fp32 planes, hi (the value with its low 13 mantissa bits cleared: exactly a tf32 number) and
@@ -22,7 +22,9 @@
 //     phase A: S = A A            -> Q (and R_1 = Q_0 at t = 0)
 //     phase B: P = Q A, R' = Q R  -> P, R'   (P not at the last step, R' not at t = 0)
 //     phase C: A' = Q P           -> A       (not at the last step)
-// R_N is also stored rounded to bf16 as the final GEMM's m x m operand. Every mbarrier wait is bounded; a wait
+// R_N is also stored for the final GEMM as two bf16 halves [R_hi | R_lo] (R has a wide range of magnitudes on
+// ill-conditioned inputs, and one bf16 rounding of it would cost more accuracy than the whole bf16 chain): the
+// final step contracts them with [X_0; X_0]. Every mbarrier wait is bounded; a wait
 // that runs out sets the error word, and the CTA then skips its remaining work but keeps taking part in every
 // cluster barrier (so no CTA of the cluster waits forever), drains its copies and MMAs, and frees its TMEM.
 #include <cuda.h>
@@ -51,8 +53,8 @@ constexpr int GS_MAX_PROBLEMS = 8;
 
 struct GsProblem {
   float *planes;            // buffer b, plane p (0 hi, 1 lo), matrix k at ((b * 2 + p) * K + k) * m * ldm
-  __nv_bfloat16 *r_out;     // R_N in bf16: matrix k at r_out + k * mstride_r, rows of ld_r elements
-  long long ldm, ld_r, mstride_r;
+  __nv_bfloat16 *r_out;     // [R_hi | R_lo]: matrix k at r_out + k * m * ld_r, rows of ld_r = 2 * mp elements
+  long long ldm, ld_r, mp;  // mp = round64(m): the offset of R_lo in a row
   long long unit_begin;     // first cluster of this problem in the launch
   int K, m, mb;             // matrices, wide rows, 128-row blocks per side (1 or 2)
 };
@@ -310,26 +312,33 @@ __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS,
 #pragma unroll 1
           for (int cc4 = 0; cc4 < GS_BLOCK / 32; ++cc4) {
             const int col0 = bj * GS_BLOCK + cc4 * 32;
-            if (col0 >= P.m) break;   // warp-uniform
+            if (col0 >= P.mp) break;   // warp-uniform (columns m .. mp - 1: zero padding of [R_hi | R_lo] only)
             float v[32];
             tmem_ld_32x32b_x32(tmem + static_cast<uint32_t>(pr.acc * GS_BLOCK + cc4 * 32) +
                                    (static_cast<uint32_t>(quarter * 32) << 16),
                                v);
             if (row >= P.m) continue;
-            if (pr.kind == EK_Q) {
+            if (col0 < P.m && pr.kind == EK_Q) {
               float g[32];
               load_full(P, GS_G, k, row, col0, g);
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = fmaf(cc, v[j], fmaf(cb, g[j], col0 + j == row ? ca : 0.f));
-              if (t == 0 && N > 1) store_split(P, GS_R0, k, row, col0, v);
+              if (t == 0 && N > 1) store_split(P, GS_R0, k, row, col0, v);   // R_1 = Q_0
             }
-            store_split(P, pr.out_buf, k, row, col0, v);
-            // R_N rounded to bf16 for the final GEMM: at t = 0 when N = 1 (R_1 = Q_0), else from the last R product
+            if (col0 < P.m) store_split(P, pr.out_buf, k, row, col0, v);
+            // R_N for the final GEMM as two bf16 halves, R_hi = rn(R) at column c and R_lo = rn(R - R_hi) at
+            // column mp + c, zero in the padding columns m .. mp - 1 of each half: at t = 0 when N = 1
+            // (R_1 = Q_0), else from the last R product
             if ((pr.kind == EK_Q && N == 1) || (pr.kind == EK_R && t == N - 1)) {
-              __nv_bfloat16 *dst = P.r_out + static_cast<long long>(k) * P.mstride_r + static_cast<long long>(row) * P.ld_r;
+              __nv_bfloat16 *dst = P.r_out + (static_cast<long long>(k) * P.m + row) * P.ld_r;
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (col0 + j < P.m) dst[col0 + j] = __float2bfloat16_rn(v[j]);
+              for (int j = 0; j < 32; ++j) {
+                const int c = col0 + j;
+                if (c >= P.mp) break;
+                const __nv_bfloat16 h = __float2bfloat16_rn(c < P.m ? v[j] : 0.f);
+                dst[c] = h;
+                dst[P.mp + c] = __float2bfloat16_rn(c < P.m ? v[j] - __bfloat162float(h) : 0.f);
+              }
             }
           }
         }
@@ -381,7 +390,8 @@ EncodeTiledFn encode_fn() {
 
 size_t gram_space_plane_bytes(long long K, long long m) {
   return static_cast<size_t>(GS_BUFFERS) * 2 * static_cast<size_t>(K) * static_cast<size_t>(m) *
-         static_cast<size_t>(round8(m)) * 4;
+             static_cast<size_t>(round8(m)) * 4 +
+         static_cast<size_t>(K) * static_cast<size_t>(m) * static_cast<size_t>(2 * round64(m)) * 2;
 }
 
 muon_status launch_gram_space(const GramSpaceStack *stacks, int n, int ns_steps, const float *coeffs, uint32_t *err,
@@ -405,10 +415,10 @@ muon_status launch_gram_space(const GramSpaceStack *stacks, int n, int ns_steps,
       if (st.m < 1 || st.m > GS_MAX_M || st.K < 1) return MUON_ERR_INVALID_ARG;
       GsProblem &P = g.prob[i];
       P.planes = st.planes;
-      P.r_out = st.r_out;
+      P.r_out = gram_space_rsplit(st.planes, st.K, st.m);
       P.ldm = round8(st.m);
-      P.ld_r = st.ld_r;
-      P.mstride_r = st.mstride_r;
+      P.mp = round64(st.m);
+      P.ld_r = 2 * P.mp;
       P.K = st.K;
       P.m = st.m;
       P.mb = st.m > GS_BLOCK ? 2 : 1;
