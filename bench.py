@@ -592,7 +592,7 @@ def run_profile_small(args):
     torch.cuda.set_device(dev)
     name = args.profile_small
     w = workloads.workload(name)
-    per_bucket_K = {"llama8b": 4, "aspect": 8}[name]
+    per_bucket_K = {"llama8b": 2, "aspect": 8}[name]
     plan = L.muon_plan_buckets(workloads.shape_list(w))
     specs, keep = [], []
     for b, (A, B) in enumerate(plan["bucket_shapes"]):
@@ -844,7 +844,7 @@ def main():
     ap.add_argument("--no-gpt2s", action="store_true", help="skip the GPT-2-small figures")
     ap.add_argument("--profile-small", default="",
                     help="one grouped Muon step (no warm-up, no autotune) of a small case of the named set, "
-                         "for ncu captures: 'llama8b' (K=4 per bucket) or 'aspect' (K=8 per bucket)")
+                         "for ncu captures: 'llama8b' (K=2 per bucket) or 'aspect' (K=8 per bucket)")
     ap.add_argument("--ns-sweep", action="store_true", help="Newton-Schulz size sweep instead of the bench line")
     ap.add_argument("--sizes", default="", help="comma-separated n for --ns-sweep")
     ap.add_argument("--small-sweep", action="store_true", help="fused small-matrix chain vs separate launches")
