@@ -73,9 +73,10 @@ struct GemmProblem {
   __nv_bfloat16 *out;
   long long ld_out, mstride_out;
   // fp32 output of the Gram-space Gram (EPI_GRAM32): hi plane at out32, lo plane at out32 + plane32, with the
-  // row and matrix pitches ld_out and mstride_out (elements)
+  // row and matrix pitches ld_out and mstride_out (elements); and c * G + b * I (coef_b, coef_c) at
+  // out32 + bprime32 and that + plane32
   float *out32;
-  long long plane32;
+  long long plane32, bprime32;
   // final step: parameter update (params != null) or dense store (out_dense != null); with master, the
   // update applies to the fp32 master copies and params receive them rounded to bf16
   void *const *params;
@@ -149,9 +150,9 @@ class GemmBatch {
                        const TileSync *sync = nullptr);
   muon_status add_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, const float *scale,
                        const TileSync *sync = nullptr);
-  // EPI_GRAM32 (x.rows <= 256): g = alpha * s^2 * x x^T as fp32 hi / lo planes
+  // EPI_GRAM32 (x.rows <= 256): g = alpha * s^2 * x x^T as fp32 hi / lo planes, and c g + b I at g_hi + bprime
   muon_status add_gram32(const Bf16Stack &x, float *g_hi, long long ldg, long long mstride_g, long long plane,
-                         float alpha, const float *scale);
+                         long long bprime, float b, float c, float alpha, const float *scale);
   muon_status add_final(const Bf16Stack &h, const Bf16Stack &x, const float *scale, const FinalSpec &f,
                        const TileSync *sync = nullptr, int k_wrap = 0);
   muon_status launch(cudaStream_t s);
@@ -216,13 +217,15 @@ muon_status launch_ns_small(const SmallNsArgs &a, cudaStream_t s);
 
 // The Newton-Schulz iteration in the m x m Gram space (ns_gram_space.cu) for wide iterates with at most
 // GS_MAX_M rows that the fused small-matrix kernel does not take. Its scratch is GS_BUFFERS fp32 m x m matrices
-// per matrix of the stack (A, Q, P and two R), each as a hi and a lo plane with rows of round8(m) elements:
+// per matrix of the stack (A, Q, P, two R and B), each as a hi and a lo plane with rows of round8(m) elements:
 // buffer b, plane p, matrix k at ((b * 2 + p) * K + k) * m * round8(m); then R_N for the final product as two
 // bf16 halves side by side, [R_hi | R_lo] (R_hi = R_N rounded, R_lo = the rest rounded), each half 64-column
 // padded with zeros: K matrices of m rows x 2 * round64(m) columns.
 constexpr int GS_MAX_M = 256;
-constexpr int GS_BUFFERS = 5;
-enum GsBuffer : int { GS_G = 0, GS_Q = 1, GS_P = 2, GS_R0 = 3, GS_R1 = 4 };
+constexpr int GS_BUFFERS = 6;
+// GS_B holds c_t A_t + b_t I, the right operand of phase A's product A_t (c_t A_t + b_t I) = b_t A_t + c_t A_t^2,
+// written wherever A_t is written
+enum GsBuffer : int { GS_G = 0, GS_Q = 1, GS_P = 2, GS_R0 = 3, GS_R1 = 4, GS_B = 5 };
 inline bool gram_space_eligible(long long m, long long n) { return m >= 1 && m <= GS_MAX_M && !ns_small_fits(m, n); }
 size_t gram_space_plane_bytes(long long K, long long m);
 inline long long round64(long long v) { return (v + 63) / 64 * 64; }

@@ -260,13 +260,15 @@ bool gram_space_route(long long m, long long n) {
 
 // The Gram-space path's launches for one stack, added to three batches: the fp32 Gram A_0 = s^2 U U^T of the
 // wide U in x0, the m x m chain (into gs), and the final step with [R_hi | R_lo] times [U; U] (scaled by s).
-muon_status add_gram_space(char *ws, const Layout &L, long long K, const FinalSpec &fin, GemmBatch &g32,
-                           std::vector<GramSpaceStack> &gs, GemmBatch &fin_batch) {
+muon_status add_gram_space(char *ws, const Layout &L, long long K, const float *coeffs, const FinalSpec &fin,
+                           GemmBatch &g32, std::vector<GramSpaceStack> &gs, GemmBatch &fin_batch) {
   const float *scale = reinterpret_cast<const float *>(ws + L.scale);
   float *planes = reinterpret_cast<float *>(ws + L.gs);
   const long long ldm = round8(L.m), msm = L.m * ldm;
   Bf16Stack X{ws + L.x0, L.m, L.n, L.ldx, L.m * L.ldx, K};
-  muon_status st = g32.add_gram32(X, planes, ldm, msm, K * msm, 1.0f, scale);
+  // A_0 into buffer GS_G and c_0 A_0 + b_0 I into buffer GS_B (plane p of buffer b starts at (2 b + p) K m ldm)
+  muon_status st = g32.add_gram32(X, planes, ldm, msm, K * msm, 2LL * GS_B * K * msm, coeffs[1], coeffs[2], 1.0f,
+                                  scale);
   if (st != MUON_OK) return st;
   gs.push_back(GramSpaceStack{planes, static_cast<int>(K), static_cast<int>(L.m)});
   const long long mp = round64(L.m);
@@ -294,7 +296,7 @@ muon_status run_ns_chain(uint32_t *err, char *ws, const Layout &L, long long K, 
   if (gram_space_route(L.m, L.n)) {
     GemmBatch g32(EPI_GRAM32, err, g_timeout_ns), fb(EPI_FINAL, err, g_timeout_ns);
     std::vector<GramSpaceStack> gs;
-    muon_status st = add_gram_space(ws, L, K, fin, g32, gs, fb);
+    muon_status st = add_gram_space(ws, L, K, coeffs, fin, g32, gs, fb);
     return st != MUON_OK ? st : launch_gram_space_batches(g32, gs, fb, ns_steps, coeffs, err, s);
   }
   double est = 0.0;
@@ -493,7 +495,9 @@ static muon_status enqueue_grouped(const muon_bucket *buckets, int n, const muon
     for (int i = 0; i < n; ++i) {
       if (small[i] || !gram_space_route(L[i].m, L[i].n)) continue;
       gspace[i] = 1;
-      if ((st = add_gram_space(w[i], L[i], buckets[i].K, final_spec(buckets[i]), g32, gs, fb)) != MUON_OK) return st;
+      if ((st = add_gram_space(w[i], L[i], buckets[i].K, hp->coeffs, final_spec(buckets[i]), g32, gs, fb)) !=
+          MUON_OK)
+        return st;
     }
     if (!gs.empty()) {
       branch = true;

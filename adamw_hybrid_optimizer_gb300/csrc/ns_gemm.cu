@@ -9,7 +9,8 @@
 //     X' = H X                      EPI_APPLY  (= a X + (b G + c G G) X); B operand X read N-major
 //     last step: u = H X, then p <- p - lr*wd*p*mask - lr*scale*u      EPI_FINAL (EPI_FINAL_MASTER: on fp32
 //                                                                      master copies of bf16 parameters)
-//     A_0 = s^2 X X^T for the Gram-space chain (m <= 256)  EPI_GRAM32  fp32 hi / lo planes, whole tile stored
+//     A_0 = s^2 X X^T for the Gram-space chain (m <= 256)  EPI_GRAM32  fp32 hi / lo planes of A_0 and of
+//                                                                      c_0 A_0 + b_0 I, whole tile stored
 //
 // Design (sm_103a): CTAs run as pairs (clusters of two) on vertically adjacent 128 x 256 output tiles with
 // paired-SM MMAs (tcgen05 cta_group::2, M = 256): each CTA holds its 128 rows of A and one half of B, the
@@ -390,27 +391,35 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem &a, int b, int 
       sc *= s * s;
     }
     if (row >= rows) return;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= sc;
     float *hi = a.out32 + static_cast<long long>(b) * a.mstride_out + static_cast<long long>(row) * a.ld_out + col0;
-    float *lo = hi + a.plane32;
     auto split = [&](float x, float &h, float &l) {
       h = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
       l = x - h;
     };
-    if (col0 + 32 <= cols && (reinterpret_cast<uintptr_t>(hi) & 15) == 0 && (reinterpret_cast<uintptr_t>(lo) & 15) == 0) {
+    // G, then c G + b I (the right operand of the chain's first product)
+    for (int pass = 0; pass < 2; ++pass) {
+      float *h_ = pass == 0 ? hi : hi + a.bprime32;
+      float *l_ = h_ + a.plane32;
+      auto val = [&](int j) { return pass == 0 ? v[j] : fmaf(a.coef_c, v[j], col0 + j == row ? a.coef_b : 0.f); };
+      if (col0 + 32 <= cols && (reinterpret_cast<uintptr_t>(h_) & 15) == 0 &&
+          (reinterpret_cast<uintptr_t>(l_) & 15) == 0) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float4 h, l;
-        split(v[4 * q] * sc, h.x, l.x);
-        split(v[4 * q + 1] * sc, h.y, l.y);
-        split(v[4 * q + 2] * sc, h.z, l.z);
-        split(v[4 * q + 3] * sc, h.w, l.w);
-        reinterpret_cast<float4 *>(hi)[q] = h;
-        reinterpret_cast<float4 *>(lo)[q] = l;
+        for (int q = 0; q < 8; ++q) {
+          float4 h, l;
+          split(val(4 * q), h.x, l.x);
+          split(val(4 * q + 1), h.y, l.y);
+          split(val(4 * q + 2), h.z, l.z);
+          split(val(4 * q + 3), h.w, l.w);
+          reinterpret_cast<float4 *>(h_)[q] = h;
+          reinterpret_cast<float4 *>(l_)[q] = l;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (col0 + j < cols) split(val(j), h_[j], l_[j]);
       }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (col0 + j < cols) split(v[j] * sc, hi[j], lo[j]);
     }
     return;
   } else if constexpr (EPI == EPI_GRAM || EPI == EPI_POLY) {
@@ -1118,7 +1127,8 @@ muon_status GemmBatch::add_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long 
 }
 
 muon_status GemmBatch::add_gram32(const Bf16Stack &x, float *g_hi, long long ldg, long long mstride_g,
-                                  long long plane, float alpha, const float *scale) {
+                                  long long plane, long long bprime, float b, float c, float alpha,
+                                  const float *scale) {
   if (epi_ != EPI_GRAM32 || x.rows > 2 * BM) return MUON_ERR_INVALID_ARG;
   Item it{};
   if (!make_map(&it.ma, x.ptr, x.cols, x.rows, x.batch, x.ld, x.mstride, BM) ||
@@ -1129,6 +1139,9 @@ muon_status GemmBatch::add_gram32(const Bf16Stack &x, float *g_hi, long long ldg
   it.p.scale = scale;
   it.p.out32 = g_hi;
   it.p.plane32 = plane;
+  it.p.bprime32 = bprime;
+  it.p.coef_b = b;
+  it.p.coef_c = c;
   it.p.ld_out = ldg;
   it.p.mstride_out = mstride_g;
   return push(it);

@@ -17,11 +17,12 @@
 // the right one (exactly the K-major B operand); TMA brings them in 32-column (128-byte) slices of hi and lo
 // planes through a 3-stage ring, one thread issues tcgen05.mma kind::tf32 (M = 128, N = 128, K = 8) into one
 // of two 128-column accumulators, and four epilogue warps (one per tensor-memory lane quarter) finish each
-// product: the polynomial Q = a I + b A + c acc, the hi / lo split, and the fp32 stores. The CTAs of a cluster
+// product: the diagonal term of Q, the hi / lo split, and the fp32 stores. The CTAs of a cluster
 // exchange results through global memory (L2-resident), one cluster barrier per phase:
-//     phase A: S = A A            -> Q (and R_1 = Q_0 at t = 0)
+//     phase A: A B = b A + c A A  -> Q = a I + A B (and R_1 = Q_0 at t = 0)
 //     phase B: P = Q A, R' = Q R  -> P, R'   (P not at the last step, R' not at t = 0)
-//     phase C: A' = Q P           -> A       (not at the last step)
+//     phase C: A' = Q P           -> A, and B = c' A' + b' I with the next step's coefficients (not at the last step)
+// (B = c_0 A_0 + b_0 I comes with A_0 from the Gram epilogue), so no epilogue reads global memory.
 // R_N is also stored for the final GEMM as two bf16 halves [R_hi | R_lo] (R has a wide range of magnitudes on
 // ill-conditioned inputs, and one bf16 rounding of it would cost more accuracy than the whole bf16 chain): the
 // final step contracts them with [X_0; X_0]. Every mbarrier wait is bounded; a wait
@@ -94,7 +95,7 @@ struct Product {
 __device__ __forceinline__ int phase_products(int t, int ph, int N, Product *p) {
   const int r_in = GS_R0 + ((t - 1) & 1), r_out = GS_R0 + (t & 1);
   if (ph == 0) {
-    p[0] = {GS_G, GS_G, 0, EK_Q, GS_Q};
+    p[0] = {GS_G, GS_B, 0, EK_Q, GS_Q};   // A (c A + b I) = b A + c A^2
     return 1;
   }
   if (ph == 1) {
@@ -154,22 +155,39 @@ __device__ __forceinline__ void store_split(const GsProblem &P, int buf, int k, 
   }
 }
 
-__device__ __forceinline__ void load_full(const GsProblem &P, int buf, int k, int row, int col0, float *v) {
-  const float *hi = plane(P, buf, 0, k) + static_cast<long long>(row) * P.ldm + col0;
-  const float *lo = plane(P, buf, 1, k) + static_cast<long long>(row) * P.ldm + col0;
-  if (col0 + 32 <= P.m && (reinterpret_cast<uintptr_t>(hi) & 15) == 0 && (reinterpret_cast<uintptr_t>(lo) & 15) == 0) {
+// The epilogue of one 32-column chunk of a product (this thread's row; v holds its 32 accumulator values).
+__device__ __forceinline__ void epilogue_chunk(const GsProblem &P, const Product &pr, int k, int row, int col0, int t,
+                                               int N, const float *co, float *v) {
+  if (col0 < P.m) {
+    if (pr.kind == EK_Q) {
+      // Q = a I + (b A + c A^2), the bracket from the MMA
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float4 h = reinterpret_cast<const float4 *>(hi)[q];
-      const float4 l = reinterpret_cast<const float4 *>(lo)[q];
-      v[4 * q] = h.x + l.x;
-      v[4 * q + 1] = h.y + l.y;
-      v[4 * q + 2] = h.z + l.z;
-      v[4 * q + 3] = h.w + l.w;
+      for (int j = 0; j < 32; ++j) v[j] += col0 + j == row ? co[3 * t] : 0.f;
+      if (t == 0 && N > 1) store_split(P, GS_R0, k, row, col0, v);   // R_1 = Q_0
     }
-  } else {
+    store_split(P, pr.out_buf, k, row, col0, v);
+    if (pr.kind == EK_A) {
+      // the next step's right operand c' A' + b' I
+      const float bn = co[3 * (t + 1) + 1], cn = co[3 * (t + 1) + 2];
+      float w[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = col0 + j < P.m ? hi[j] + lo[j] : 0.f;
+      for (int j = 0; j < 32; ++j) w[j] = fmaf(cn, v[j], col0 + j == row ? bn : 0.f);
+      store_split(P, GS_B, k, row, col0, w);
+    }
+  }
+  // R_N for the final GEMM as two bf16 halves, R_hi = rn(R) at column c and R_lo = rn(R - R_hi) at column
+  // mp + c, zero in the padding columns m .. mp - 1 of each half: at t = 0 when N = 1 (R_1 = Q_0), else from
+  // the last R product
+  if ((pr.kind == EK_Q && N == 1) || (pr.kind == EK_R && t == N - 1)) {
+    __nv_bfloat16 *dst = P.r_out + (static_cast<long long>(k) * P.m + row) * P.ld_r;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int c = col0 + j;
+      if (c >= P.mp) break;
+      const __nv_bfloat16 h = __float2bfloat16_rn(c < P.m ? v[j] : 0.f);
+      dst[c] = h;
+      dst[P.mp + c] = __float2bfloat16_rn(c < P.m ? v[j] - __bfloat162float(h) : 0.f);
+    }
   }
 }
 
@@ -228,7 +246,6 @@ __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS,
 
 #pragma unroll 1
   for (int t = 0; t < N; ++t) {
-    const float ca = args.coeffs[3 * t], cb = args.coeffs[3 * t + 1], cc = args.coeffs[3 * t + 2];
 #pragma unroll 1
     for (int ph = 0; ph < 3; ++ph) {
       Product prods[2];
@@ -309,42 +326,33 @@ __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS,
           const bool ok = wait_bounded(&ctrl->acc_full[pr.acc], par, ctl, ERR_WAIT_ACC_FULL);
           if (!__all_sync(0xffffffffu, ok)) continue;
           tc_fence_after();
+          // two 32-column chunks per round: both tensor-memory loads in flight before one wait
 #pragma unroll 1
-          for (int cc4 = 0; cc4 < GS_BLOCK / 32; ++cc4) {
-            const int col0 = bj * GS_BLOCK + cc4 * 32;
+          for (int cc = 0; cc < GS_BLOCK / 32; cc += 2) {
+            const int col0 = bj * GS_BLOCK + cc * 32;
             if (col0 >= P.mp) break;   // warp-uniform (columns m .. mp - 1: zero padding of [R_hi | R_lo] only)
-            float v[32];
-            tmem_ld_32x32b_x32(tmem + static_cast<uint32_t>(pr.acc * GS_BLOCK + cc4 * 32) +
-                                   (static_cast<uint32_t>(quarter * 32) << 16),
-                               v);
+            const uint32_t ta = tmem + static_cast<uint32_t>(pr.acc * GS_BLOCK + cc * 32) +
+                                (static_cast<uint32_t>(quarter * 32) << 16);
+            uint32_t r0[32], r1[32];
+            tmem_ld_32x32b_x32_async(ta, r0);
+            tmem_ld_32x32b_x32_async(ta + 32, r1);
+            tmem_ld_wait();
             if (row >= P.m) continue;
-            if (col0 < P.m && pr.kind == EK_Q) {
-              float g[32];
-              load_full(P, GS_G, k, row, col0, g);
+            float v[32];
 #pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = fmaf(cc, v[j], fmaf(cb, g[j], col0 + j == row ? ca : 0.f));
-              if (t == 0 && N > 1) store_split(P, GS_R0, k, row, col0, v);   // R_1 = Q_0
-            }
-            if (col0 < P.m) store_split(P, pr.out_buf, k, row, col0, v);
-            // R_N for the final GEMM as two bf16 halves, R_hi = rn(R) at column c and R_lo = rn(R - R_hi) at
-            // column mp + c, zero in the padding columns m .. mp - 1 of each half: at t = 0 when N = 1
-            // (R_1 = Q_0), else from the last R product
-            if ((pr.kind == EK_Q && N == 1) || (pr.kind == EK_R && t == N - 1)) {
-              __nv_bfloat16 *dst = P.r_out + (static_cast<long long>(k) * P.m + row) * P.ld_r;
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
+            epilogue_chunk(P, pr, k, row, col0, t, N, args.coeffs, v);
+            if (col0 + 32 < P.mp) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const int c = col0 + j;
-                if (c >= P.mp) break;
-                const __nv_bfloat16 h = __float2bfloat16_rn(c < P.m ? v[j] : 0.f);
-                dst[c] = h;
-                dst[P.mp + c] = __float2bfloat16_rn(c < P.m ? v[j] - __bfloat162float(h) : 0.f);
-              }
+              for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r1[j]);
+              epilogue_chunk(P, pr, k, row, col0 + 32, t, N, args.coeffs, v);
             }
           }
         }
-        __threadfence();   // this phase's stores are visible GPU-wide before the cluster barrier releases them
       }
-      // ---------------------------------------------------------------- phase barrier (every thread of the cluster)
+      // ---------------------------------------------------------------- phase barrier (every thread of the cluster):
+      // its release / acquire at cluster scope orders this phase's global stores before the next phase's reads,
+      // whose TMA copies the producer issues after a proxy fence
       tc_fence_before();
       __syncwarp();
       cluster_sync();

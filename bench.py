@@ -690,6 +690,8 @@ def run_config_sweep(args):
         for deps in (1, 0):
             L.muon_debug_counter_deps(deps)
             t_muon = t_adamw = 0.0
+            sampler = ClockSampler(0)
+            sampler.__enter__()
             for rep in range(2 + steps):
                 it += 1
                 for h in hps.values():
@@ -704,6 +706,8 @@ def run_config_sweep(args):
                 if rep >= 2:
                     t_muon += ev[0].elapsed_time(ev[1]) / steps
                     t_adamw += ev[1].elapsed_time(ev[2]) / steps
+            sampler.__exit__(None, None, None)
+            clk = sampler.summary(peaks.get("sm_max_mhz"))
             L.muon_trace_enable(True)
             L.muon_step_grouped(arr, hp, ws)
             torch.cuda.synchronize()
@@ -723,7 +727,8 @@ def run_config_sweep(args):
                               "adamw_ms": round(t_adamw, 4), "adamw_elems": n_adamw,
                               "adamw_gbs": round(abytes / (t_adamw * 1e-3) / 1e9, 1),
                               "adamw_frac_hbm": round(abytes / (t_adamw * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-                              "traced_ms_per_kind": per_kind, "peaks": f"{peak_src}"}), flush=True)
+                              "traced_ms_per_kind": per_kind, "peaks": f"{peak_src}",
+                              "clocks": clk}), flush=True)
         L.muon_debug_counter_deps(-1)
         L.muon_debug_gram_space(-1)
         del specs, keep, arr, ws, ap, ag, am, av, aspecs, atensors
