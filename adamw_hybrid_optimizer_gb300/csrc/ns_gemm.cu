@@ -89,6 +89,7 @@ __host__ __device__ constexpr size_t smem_bytes(int epi, int stages, int slots) 
 }
 constexpr int SHORT_K_ITERS = 32;   // without a measured choice, contractions up to 2048 take the deep-ring shape
 static_assert(smem_bytes(EPI_GRAM, 6, 1) <= 232448 && smem_bytes(EPI_POLY, 6, 2) <= 232448 &&
+                  smem_bytes(EPI_GRAM32, 6, 2) <= 232448 &&
                   smem_bytes(EPI_POLY, 5, 3) <= 232448 && smem_bytes(EPI_POLY, 4, 5) <= 232448,
               "shared memory over budget");
 
@@ -390,36 +391,46 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem &a, int b, int 
       const float s = a.scale[b];
       sc *= s * s;
     }
-    if (row >= rows) return;
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] *= sc;
-    float *hi = a.out32 + static_cast<long long>(b) * a.mstride_out + static_cast<long long>(row) * a.ld_out + col0;
-    auto split = [&](float x, float &h, float &l) {
-      h = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
-      l = x - h;
-    };
-    // G, then c G + b I (the right operand of the chain's first product)
-    for (int pass = 0; pass < 2; ++pass) {
-      float *h_ = pass == 0 ? hi : hi + a.bprime32;
-      float *l_ = h_ + a.plane32;
-      auto val = [&](int j) { return pass == 0 ? v[j] : fmaf(a.coef_c, v[j], col0 + j == row ? a.coef_b : 0.f); };
-      if (col0 + 32 <= cols && (reinterpret_cast<uintptr_t>(h_) & 15) == 0 &&
-          (reinterpret_cast<uintptr_t>(l_) & 15) == 0) {
+    // each warp stages its 32 x 32 fp32 chunk (4 KB of the two ring slots this kind is launched with) so that
+    // every global store writes four whole 128-byte rows: 16-byte piece q of row r at position q ^ (r & 7)
+    uint8_t *stg = rg.slot + (rg.half * 4 + rg.lane_base / 32) * 4096;
+    auto piece = [&](int r, int q) { return reinterpret_cast<float4 *>(stg + r * 128 + ((q ^ (r & 7)) << 4)); };
+    float *base = a.out32 + static_cast<long long>(b) * a.mstride_out;
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {   // G hi, G lo, then (c G + b I) hi, lo
+      const bool bp = pass >= 2, lo = pass & 1;
+      const float cm = bp ? a.coef_c : 1.f, dg = bp ? a.coef_b : 0.f;
+      const uint32_t mask = lo ? 0u : 0xFFFFE000u;
+      float w[32];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float4 h, l;
-          split(val(4 * q), h.x, l.x);
-          split(val(4 * q + 1), h.y, l.y);
-          split(val(4 * q + 2), h.z, l.z);
-          split(val(4 * q + 3), h.w, l.w);
-          reinterpret_cast<float4 *>(h_)[q] = h;
-          reinterpret_cast<float4 *>(l_)[q] = l;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (col0 + j < cols) split(val(j), h_[j], l_[j]);
+      for (int j = 0; j < 32; ++j) {
+        const float x = fmaf(cm, v[j], col0 + j == row ? dg : 0.f);
+        const float h = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+        // hi plane: h; lo plane: x - h
+        w[j] = lo ? x - h : __uint_as_float(__float_as_uint(x) & mask);
       }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) *piece(lane, q) = make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+      __syncwarp();
+      float *dst = base + (bp ? a.bprime32 : 0) + (lo ? a.plane32 : 0);
+      const int q = lane & 7, c = col0 + 4 * q;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = 4 * i + (lane >> 3);
+        if (warp_row0 + r >= rows) continue;
+        const float4 x = *piece(r, q);
+        float *d = dst + static_cast<long long>(warp_row0 + r) * a.ld_out + c;
+        if (c + 4 <= cols) {
+          *reinterpret_cast<float4 *>(d) = x;
+        } else {
+          if (c < cols) d[0] = x.x;
+          if (c + 1 < cols) d[1] = x.y;
+          if (c + 2 < cols) d[2] = x.z;
+        }
+      }
+      __syncwarp();
     }
     return;
   } else if constexpr (EPI == EPI_GRAM || EPI == EPI_POLY) {
@@ -1257,7 +1268,7 @@ muon_status GemmBatch::launch(cudaStream_t s) {
     muon_status st;
     switch (epi_) {
       case EPI_GRAM: st = launch_shape<EPI_GRAM, false, 6, 1>(g, KK_GRAM, s); break;
-      case EPI_GRAM32: st = launch_shape<EPI_GRAM32, false, 6, 1>(g, KK_GRAM32, s); break;
+      case EPI_GRAM32: st = launch_shape<EPI_GRAM32, false, 6, 2>(g, KK_GRAM32, s); break;
       case EPI_POLY:
         st = shape == 0   ? launch_shape<EPI_POLY, false, 4, 5>(g, KK_POLY, s)
              : shape == 1 ? launch_shape<EPI_POLY, false, 5, 3>(g, KK_POLY, s)

@@ -69,8 +69,15 @@ struct GsGroup {
   float coeffs[3 * MUON_MAX_NS_STEPS];
   uint32_t *err;
   unsigned long long timeout_ns;
+  unsigned long long *timeline;   // optional per-phase timestamps (performance analysis), or null
+  int timeline_cap;               // records per CTA
+  int timeline_ctas;              // CTAs that record (the region holds this many)
 };
 static_assert(sizeof(GsGroup) <= 4096, "kernel parameter block too large");
+
+// Timeline record of one phase (globaltimer ns): phase number + 1, producer first / last copy issue, MMA first
+// operands ready, last MMA commit, epilogue first accumulator ready, epilogue end, barrier passed.
+constexpr int GS_TL_WORDS = 10;
 
 struct GsCtrl {
   uint64_t full[GS_STAGES];
@@ -81,7 +88,10 @@ struct GsCtrl {
   int abort_flag;
 };
 
-constexpr size_t GS_SMEM = static_cast<size_t>(GS_STAGES) * GS_STAGE_BYTES + sizeof(GsCtrl) + 1024;
+constexpr int GS_EPI_WARPS = 4;
+constexpr int GS_STAGING_BYTES = 32 * 32 * 4;   // per epilogue warp: one 32 x 32 fp32 chunk
+constexpr size_t GS_SMEM = static_cast<size_t>(GS_STAGES) * GS_STAGE_BYTES +
+                           static_cast<size_t>(GS_EPI_WARPS) * GS_STAGING_BYTES + sizeof(GsCtrl) + 1024;
 static_assert(GS_SMEM <= 232448, "shared memory over budget");
 
 // Epilogue kinds of one product.
@@ -125,77 +135,121 @@ __device__ __forceinline__ float *plane(const GsProblem &P, int buf, int pl, int
   return P.planes + ((static_cast<long long>(buf) * 2 + pl) * P.K + k) * static_cast<long long>(P.m) * P.ldm;
 }
 
-// Stores 32 values of row `row`, columns col0 .. col0 + 31 of buffer `buf` as hi / lo planes (only columns < m).
-__device__ __forceinline__ void store_split(const GsProblem &P, int buf, int k, int row, int col0, const float *v) {
-  float *hi = plane(P, buf, 0, k) + static_cast<long long>(row) * P.ldm + col0;
-  float *lo = plane(P, buf, 1, k) + static_cast<long long>(row) * P.ldm + col0;
-  if (col0 + 32 <= P.m && (reinterpret_cast<uintptr_t>(hi) & 15) == 0 && (reinterpret_cast<uintptr_t>(lo) & 15) == 0) {
+// Epilogue stores go through a per-warp staging chunk in shared memory: each lane holds one row's 32 values,
+// writes them as 8 16-byte pieces (piece q of row r at position q ^ (r & 7), so that neither the row-wise writes
+// nor the segment-wise reads conflict beyond the 4 wavefronts 512 bytes need), and the warp then stores 4 whole
+// rows (128 bytes each) per instruction. Rows >= m and columns >= m are not stored.
+struct Staging {
+  uint8_t *base;
+  __device__ __forceinline__ float4 *piece(int r, int q) const {
+    return reinterpret_cast<float4 *>(base + r * 128 + ((q ^ (r & 7)) << 4));
+  }
+};
+
+__device__ __forceinline__ void stage_row(const Staging &sg, int lane, const float *v) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      float4 h, l;
-      h.x = tf32_hi(v[4 * q]);
-      h.y = tf32_hi(v[4 * q + 1]);
-      h.z = tf32_hi(v[4 * q + 2]);
-      h.w = tf32_hi(v[4 * q + 3]);
-      l.x = v[4 * q] - h.x;
-      l.y = v[4 * q + 1] - h.y;
-      l.z = v[4 * q + 2] - h.z;
-      l.w = v[4 * q + 3] - h.w;
-      reinterpret_cast<float4 *>(hi)[q] = h;
-      reinterpret_cast<float4 *>(lo)[q] = l;
-    }
-  } else {
+  for (int q = 0; q < 8; ++q) *sg.piece(lane, q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+
+// Stores the staged 32 x 32 chunk (rows row0 .., columns col0 ..) into fp32 matrix `dst` (rows of ld elements).
+__device__ __forceinline__ void store_staged(const Staging &sg, int lane, float *dst, long long ld, int m, int row0,
+                                             int col0) {
+  const int q = lane & 7;
+  const int c = col0 + 4 * q;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      if (col0 + j >= P.m) break;
-      const float h = tf32_hi(v[j]);
-      hi[j] = h;
-      lo[j] = v[j] - h;
+  for (int i = 0; i < 8; ++i) {
+    const int r = 4 * i + (lane >> 3);
+    if (row0 + r >= m) continue;
+    const float4 x = *sg.piece(r, q);
+    float *d = dst + static_cast<long long>(row0 + r) * ld + c;
+    if (c + 4 <= m) {
+      *reinterpret_cast<float4 *>(d) = x;
+    } else {
+      if (c < m) d[0] = x.x;
+      if (c + 1 < m) d[1] = x.y;
+      if (c + 2 < m) d[2] = x.z;
     }
   }
 }
 
-// The epilogue of one 32-column chunk of a product (this thread's row; v holds its 32 accumulator values).
-__device__ __forceinline__ void epilogue_chunk(const GsProblem &P, const Product &pr, int k, int row, int col0, int t,
-                                               int N, const float *co, float *v) {
+// Stores this warp's chunk (lane = row row0 + lane, values v) of buffer `buf` as its hi and lo planes.
+__device__ __forceinline__ void store_split(const GsProblem &P, const Staging &sg, int lane, int buf, int k, int row0,
+                                            int col0, const float *v) {
+  float h[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) h[j] = tf32_hi(v[j]);
+  stage_row(sg, lane, h);
+  __syncwarp();
+  store_staged(sg, lane, plane(P, buf, 0, k), P.ldm, P.m, row0, col0);
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 32; ++j) h[j] = v[j] - h[j];
+  stage_row(sg, lane, h);
+  __syncwarp();
+  store_staged(sg, lane, plane(P, buf, 1, k), P.ldm, P.m, row0, col0);
+  __syncwarp();
+}
+
+// R_N for the final GEMM as two bf16 halves, R_hi = rn(R) at column c and R_lo = rn(R - R_hi) at column mp + c,
+// zero in the padding columns m .. mp - 1 of each half.
+__device__ __forceinline__ void store_rsplit(const GsProblem &P, const Staging &sg, int lane, int k, int row0,
+                                             int col0, const float *v) {
+  stage_row(sg, lane, v);
+  __syncwarp();
+  const int q = lane & 7;
+  const int c = col0 + 4 * q;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = 4 * i + (lane >> 3);
+    if (row0 + r >= P.m || c >= P.mp) continue;
+    const float4 x = *sg.piece(r, q);
+    const float e[4] = {x.x, x.y, x.z, x.w};
+    __nv_bfloat16 hv[4], lv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float val = c + j < P.m ? e[j] : 0.f;
+      hv[j] = __float2bfloat16_rn(val);
+      lv[j] = __float2bfloat16_rn(val - __bfloat162float(hv[j]));
+    }
+    __nv_bfloat16 *d = P.r_out + (static_cast<long long>(k) * P.m + row0 + r) * P.ld_r + c;
+    *reinterpret_cast<uint2 *>(d) = *reinterpret_cast<const uint2 *>(hv);            // mp, c: multiples of 4
+    *reinterpret_cast<uint2 *>(d + P.mp) = *reinterpret_cast<const uint2 *>(lv);
+  }
+  __syncwarp();
+}
+
+// The epilogue of one 32-column chunk of a product: this warp's rows row0 .. row0 + 31 (lane = row), columns
+// col0 .. col0 + 31; v holds the lane's 32 accumulator values. Called by every lane of the warp.
+__device__ __forceinline__ void epilogue_chunk(const GsProblem &P, const Staging &sg, const Product &pr, int k,
+                                               int row0, int lane, int col0, int t, int N, const float *co, float *v) {
+  const int row = row0 + lane;
   if (col0 < P.m) {
     if (pr.kind == EK_Q) {
       // Q = a I + (b A + c A^2), the bracket from the MMA
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] += col0 + j == row ? co[3 * t] : 0.f;
-      if (t == 0 && N > 1) store_split(P, GS_R0, k, row, col0, v);   // R_1 = Q_0
+      if (t == 0 && N > 1) store_split(P, sg, lane, GS_R0, k, row0, col0, v);   // R_1 = Q_0
     }
-    store_split(P, pr.out_buf, k, row, col0, v);
+    store_split(P, sg, lane, pr.out_buf, k, row0, col0, v);
     if (pr.kind == EK_A) {
       // the next step's right operand c' A' + b' I
       const float bn = co[3 * (t + 1) + 1], cn = co[3 * (t + 1) + 2];
       float w[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) w[j] = fmaf(cn, v[j], col0 + j == row ? bn : 0.f);
-      store_split(P, GS_B, k, row, col0, w);
+      store_split(P, sg, lane, GS_B, k, row0, col0, w);
     }
   }
-  // R_N for the final GEMM as two bf16 halves, R_hi = rn(R) at column c and R_lo = rn(R - R_hi) at column
-  // mp + c, zero in the padding columns m .. mp - 1 of each half: at t = 0 when N = 1 (R_1 = Q_0), else from
-  // the last R product
-  if ((pr.kind == EK_Q && N == 1) || (pr.kind == EK_R && t == N - 1)) {
-    __nv_bfloat16 *dst = P.r_out + (static_cast<long long>(k) * P.m + row) * P.ld_r;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int c = col0 + j;
-      if (c >= P.mp) break;
-      const __nv_bfloat16 h = __float2bfloat16_rn(c < P.m ? v[j] : 0.f);
-      dst[c] = h;
-      dst[P.mp + c] = __float2bfloat16_rn(c < P.m ? v[j] - __bfloat162float(h) : 0.f);
-    }
-  }
+  // R_N: at t = 0 when N = 1 (R_1 = Q_0), else from the last R product
+  if ((pr.kind == EK_Q && N == 1) || (pr.kind == EK_R && t == N - 1)) store_rsplit(P, sg, lane, k, row0, col0, v);
 }
 
 __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS, 1)
     gram_space_kernel(const __grid_constant__ GsGroup args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  GsCtrl *ctrl = reinterpret_cast<GsCtrl *>(smem + GS_STAGES * GS_STAGE_BYTES);
+  uint8_t *staging = smem + GS_STAGES * GS_STAGE_BYTES;
+  GsCtrl *ctrl = reinterpret_cast<GsCtrl *>(staging + GS_EPI_WARPS * GS_STAGING_BYTES);
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const uint32_t rank = cluster_ctarank();
@@ -244,6 +298,7 @@ __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS,
   uint32_t acc_uses[2] = {0u, 0u};
   bool issued = false;
 
+  int phase_no = 0;
 #pragma unroll 1
   for (int t = 0; t < N; ++t) {
 #pragma unroll 1
@@ -252,10 +307,19 @@ __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS,
       const int np = phase_products(t, ph, N, prods);
       if (np == 0) continue;   // the same for every CTA of the cluster: no barrier for a skipped phase
       const bool work = active && ctrl->abort_flag == 0;
+      unsigned long long *rec =
+          (args.timeline != nullptr && phase_no < args.timeline_cap && static_cast<int>(blockIdx.x) < args.timeline_ctas)
+              ? args.timeline + (static_cast<long long>(blockIdx.x) * args.timeline_cap + phase_no) * GS_TL_WORDS
+              : nullptr;
+      ++phase_no;
       if (warp == 0) {
         if (lane == 0 && work) {
           // ------------------------------------------------------------ TMA producer
           fence_proxy_async_global();   // the planes were written by generic stores before the last barrier
+          if (rec) {
+            rec[0] = static_cast<unsigned long long>(phase_no);
+            rec[1] = globaltimer_ns();
+          }
           bool ok = true;
           for (int q = 0; q < np && ok; ++q) {
             const int za = (prods[q].a_buf * 2) * P.K + k, zb = (prods[q].b_buf * 2) * P.K + k;
@@ -277,6 +341,7 @@ __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS,
               }
             }
           }
+          if (rec) rec[2] = globaltimer_ns();
         }
       } else if (warp == 1) {
         if (lane == 0 && work) {
@@ -290,6 +355,7 @@ __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS,
                 ok = false;
                 break;
               }
+              if (rec && q == 0 && c == 0) rec[3] = globaltimer_ns();
               tc_fence_after();
               const uint32_t a_hi = smem_u32(smem + stage * GS_STAGE_BYTES);
               const uint32_t a_lo = a_hi + GS_TILE_BYTES, b_hi = a_hi + 2 * GS_TILE_BYTES,
@@ -313,11 +379,13 @@ __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS,
             }
             if (ok) tc_commit(&ctrl->acc_full[prods[q].acc]);
           }
+          if (rec) rec[4] = globaltimer_ns();
         }
       } else {
         // -------------------------------------------------------------- epilogue (warps 2..5)
         const int quarter = warp & 3;               // tensor-memory lanes this warp may read
-        const int row = bi * GS_BLOCK + quarter * 32 + lane;
+        const int row0 = bi * GS_BLOCK + quarter * 32;
+        const Staging sg{staging + (warp - 2) * GS_STAGING_BYTES};
         for (int q = 0; q < np; ++q) {
           const Product pr = prods[q];
           const uint32_t par = acc_uses[pr.acc] & 1u;
@@ -325,30 +393,21 @@ __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS,
           if (!work) continue;
           const bool ok = wait_bounded(&ctrl->acc_full[pr.acc], par, ctl, ERR_WAIT_ACC_FULL);
           if (!__all_sync(0xffffffffu, ok)) continue;
+          if (rec && q == 0 && warp == 2 && lane == 0) rec[5] = globaltimer_ns();
           tc_fence_after();
-          // two 32-column chunks per round: both tensor-memory loads in flight before one wait
 #pragma unroll 1
-          for (int cc = 0; cc < GS_BLOCK / 32; cc += 2) {
+          for (int cc = 0; cc < GS_BLOCK / 32; ++cc) {
             const int col0 = bj * GS_BLOCK + cc * 32;
             if (col0 >= P.mp) break;   // warp-uniform (columns m .. mp - 1: zero padding of [R_hi | R_lo] only)
-            const uint32_t ta = tmem + static_cast<uint32_t>(pr.acc * GS_BLOCK + cc * 32) +
-                                (static_cast<uint32_t>(quarter * 32) << 16);
-            uint32_t r0[32], r1[32];
-            tmem_ld_32x32b_x32_async(ta, r0);
-            tmem_ld_32x32b_x32_async(ta + 32, r1);
-            tmem_ld_wait();
-            if (row >= P.m) continue;
             float v[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
-            epilogue_chunk(P, pr, k, row, col0, t, N, args.coeffs, v);
-            if (col0 + 32 < P.mp) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r1[j]);
-              epilogue_chunk(P, pr, k, row, col0 + 32, t, N, args.coeffs, v);
-            }
+            tmem_ld_32x32b_x32(tmem + static_cast<uint32_t>(pr.acc * GS_BLOCK + cc * 32) +
+                                   (static_cast<uint32_t>(quarter * 32) << 16),
+                               v);
+            if (row0 >= P.m) continue;   // warp-uniform
+            epilogue_chunk(P, sg, pr, k, row0, lane, col0, t, N, args.coeffs, v);
           }
         }
+        if (rec && warp == 2 && lane == 0) rec[6] = globaltimer_ns();
       }
       // ---------------------------------------------------------------- phase barrier (every thread of the cluster):
       // its release / acquire at cluster scope orders this phase's global stores before the next phase's reads,
@@ -357,6 +416,7 @@ __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS,
       __syncwarp();
       cluster_sync();
       tc_fence_after();
+      if (rec && threadIdx.x == 0) rec[7] = globaltimer_ns();
     }
   }
 
@@ -449,6 +509,8 @@ muon_status launch_gram_space(const GramSpaceStack *stacks, int n, int ns_steps,
     for (int i = 0; i < 3 * ns_steps; ++i) g.coeffs[i] = coeffs[i];
     g.err = err;
     g.timeout_ns = timeout_ns;
+    debug_timeline(&g.timeline, &g.timeline_cap);
+    g.timeline_ctas = device_sm_count();
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(GS_CLUSTER * units));
     cfg.blockDim = dim3(GS_THREADS);
