@@ -876,12 +876,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         const uint32_t need = EPI_WARPS * ++j;
         const unsigned long long t0 = globaltimer_ns();
         bool gone = false;
+        // a tile takes microseconds: poll with a growing sleep (up to half a microsecond) rather than every few
+        // tens of nanoseconds for the whole launch
+        unsigned sleep_ns = 32;
         while (ld_acquire_cta_shared(&ctrl->stored) < need) {
           if (*abort_flag != 0 || globaltimer_ns() - t0 > args.timeout_ns) {
             gone = true;
             break;
           }
-          __nanosleep(64);
+          __nanosleep(sleep_ns);
+          if (sleep_ns < 512) sleep_ns <<= 1;
         }
         if (gone) break;
         red_release_gpu_add(P.sig_ctr + b, static_cast<uint32_t>(EPI_WARPS));

@@ -18,7 +18,8 @@
 // planes through a 3-stage ring, one thread issues tcgen05.mma kind::tf32 (M = 128, N = 128, K = 8) into one
 // of two 128-column accumulators, and four epilogue warps (one per tensor-memory lane quarter) finish each
 // product: the diagonal term of Q, the hi / lo split, and the fp32 stores. The CTAs of a cluster
-// exchange results through global memory (L2-resident), one cluster barrier per phase:
+// exchange results through global memory (L2-resident; every block leaves by a TMA bulk store of 128 x 32 tiles
+// staged in shared memory), one cluster barrier per phase:
 //     phase A: A B = b A + c A A  -> Q = a I + A B (and R_1 = Q_0 at t = 0)
 //     phase B: P = Q A, R' = Q R  -> P, R'   (P not at the last step, R' not at t = 0)
 //     phase C: A' = Q P           -> A, and B = c' A' + b' I with the next step's coefficients (not at the last step)
@@ -89,9 +90,10 @@ struct GsCtrl {
 };
 
 constexpr int GS_EPI_WARPS = 4;
-constexpr int GS_STAGING_BYTES = 32 * 32 * 4;   // per epilogue warp: one 32 x 32 fp32 chunk
+constexpr int GS_OUT_TILES = 2;   // double-buffered 128 x 32 fp32 output tiles for the TMA stores
 constexpr size_t GS_SMEM = static_cast<size_t>(GS_STAGES) * GS_STAGE_BYTES +
-                           static_cast<size_t>(GS_EPI_WARPS) * GS_STAGING_BYTES + sizeof(GsCtrl) + 1024;
+                           static_cast<size_t>(GS_OUT_TILES) * GS_TILE_BYTES + sizeof(GsCtrl) + 1024;
+constexpr int GS_EPI_BAR = 1;     // named barrier of the four epilogue warps
 static_assert(GS_SMEM <= 232448, "shared memory over budget");
 
 // Epilogue kinds of one product.
@@ -135,66 +137,60 @@ __device__ __forceinline__ float *plane(const GsProblem &P, int buf, int pl, int
   return P.planes + ((static_cast<long long>(buf) * 2 + pl) * P.K + k) * static_cast<long long>(P.m) * P.ldm;
 }
 
-// Epilogue stores go through a per-warp staging chunk in shared memory: each lane holds one row's 32 values,
-// writes them as 8 16-byte pieces (piece q of row r at position q ^ (r & 7), so that neither the row-wise writes
-// nor the segment-wise reads conflict beyond the 4 wavefronts 512 bytes need), and the warp then stores 4 whole
-// rows (128 bytes each) per instruction. Rows >= m and columns >= m are not stored.
-struct Staging {
-  uint8_t *base;
-  __device__ __forceinline__ float4 *piece(int r, int q) const {
-    return reinterpret_cast<float4 *>(base + r * 128 + ((q ^ (r & 7)) << 4));
-  }
+// Epilogue output: the four epilogue warps write a 128-row x 32-column fp32 tile of one plane into shared memory
+// in the layout a TMA load of that box produces (128-byte rows; 16-byte piece q of row r at position q ^ (r & 7)),
+// and one thread stores it with a TMA bulk store, which writes whole rows, leaves out rows and columns past m, and
+// runs asynchronously to the warps. Two tiles alternate; the storing thread waits, before a tile is written
+// again, until the store two tiles back has read it, and before the phase barrier until every store is done.
+struct TileOut {
+  uint8_t *tiles;          // GS_OUT_TILES tiles of GS_TILE_BYTES, 1024-byte aligned
+  const CUtensorMap *map;  // the planes' tensor map (box 32 x 128)
+  int n;                   // tiles stored so far in this kernel
+  bool issuer;             // the one thread that issues the stores
 };
 
-__device__ __forceinline__ void stage_row(const Staging &sg, int lane, const float *v) {
-#pragma unroll
-  for (int q = 0; q < 8; ++q) *sg.piece(lane, q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+__device__ __forceinline__ float4 *tile_piece(uint8_t *tile, int r, int q) {
+  return reinterpret_cast<float4 *>(tile + r * 128 + ((q ^ (r & 7)) << 4));
 }
 
-// Stores the staged 32 x 32 chunk (rows row0 .., columns col0 ..) into fp32 matrix `dst` (rows of ld elements).
-__device__ __forceinline__ void store_staged(const Staging &sg, int lane, float *dst, long long ld, int m, int row0,
-                                             int col0) {
-  const int q = lane & 7;
-  const int c = col0 + 4 * q;
+// Collective over the four epilogue warps: stores rows of block row bi (this lane's row: quarter * 32 + lane of
+// the tile), columns col0 .. col0 + 31, of plane `pl` of buffer `buf` of matrix k, values w.
+__device__ __forceinline__ void store_tile(TileOut &to, const GsProblem &P, int bi, int quarter, int lane, int buf,
+                                           int pl, int k, int col0, const float *w) {
+  uint8_t *tile = to.tiles + (to.n & 1) * GS_TILE_BYTES;
+  if (to.issuer) bulk_wait_group_read<1>();   // the store that last used this tile has read it
+  named_barrier_sync(GS_EPI_BAR, GS_EPI_WARPS * 32);
+  const int r = quarter * 32 + lane;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int r = 4 * i + (lane >> 3);
-    if (row0 + r >= m) continue;
-    const float4 x = *sg.piece(r, q);
-    float *d = dst + static_cast<long long>(row0 + r) * ld + c;
-    if (c + 4 <= m) {
-      *reinterpret_cast<float4 *>(d) = x;
-    } else {
-      if (c < m) d[0] = x.x;
-      if (c + 1 < m) d[1] = x.y;
-      if (c + 2 < m) d[2] = x.z;
-    }
+  for (int q = 0; q < 8; ++q) *tile_piece(tile, r, q) = make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  fence_proxy_async_shared();                 // the generic writes are visible to the TMA engine
+  named_barrier_sync(GS_EPI_BAR, GS_EPI_WARPS * 32);
+  if (to.issuer) {
+    tma_store_3d(to.map, tile, col0, bi * GS_BLOCK, (buf * 2 + pl) * P.K + k);
+    bulk_commit_group();
   }
+  ++to.n;
 }
 
-// Stores this warp's chunk (lane = row row0 + lane, values v) of buffer `buf` as its hi and lo planes.
-__device__ __forceinline__ void store_split(const GsProblem &P, const Staging &sg, int lane, int buf, int k, int row0,
-                                            int col0, const float *v) {
-  float h[32];
+// Both planes of one buffer: the tf32 hi part and the rest.
+__device__ __forceinline__ void store_split(TileOut &to, const GsProblem &P, int bi, int quarter, int lane, int buf,
+                                            int k, int col0, const float *v) {
+  float w[32];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) h[j] = tf32_hi(v[j]);
-  stage_row(sg, lane, h);
-  __syncwarp();
-  store_staged(sg, lane, plane(P, buf, 0, k), P.ldm, P.m, row0, col0);
-  __syncwarp();
+  for (int j = 0; j < 32; ++j) w[j] = tf32_hi(v[j]);
+  store_tile(to, P, bi, quarter, lane, buf, 0, k, col0, w);
 #pragma unroll
-  for (int j = 0; j < 32; ++j) h[j] = v[j] - h[j];
-  stage_row(sg, lane, h);
-  __syncwarp();
-  store_staged(sg, lane, plane(P, buf, 1, k), P.ldm, P.m, row0, col0);
-  __syncwarp();
+  for (int j = 0; j < 32; ++j) w[j] = v[j] - w[j];
+  store_tile(to, P, bi, quarter, lane, buf, 1, k, col0, w);
 }
 
 // R_N for the final GEMM as two bf16 halves, R_hi = rn(R) at column c and R_lo = rn(R - R_hi) at column mp + c,
-// zero in the padding columns m .. mp - 1 of each half.
-__device__ __forceinline__ void store_rsplit(const GsProblem &P, const Staging &sg, int lane, int k, int row0,
-                                             int col0, const float *v) {
-  stage_row(sg, lane, v);
+// zero in the padding columns m .. mp - 1 of each half. Per warp, through a 32 x 32 fp32 staging chunk (so that
+// lanes store consecutive columns of a row), with plain stores: it runs once per chain.
+__device__ __forceinline__ void store_rsplit(const GsProblem &P, uint8_t *stg, int lane, int k, int row0, int col0,
+                                             const float *v) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) *tile_piece(stg, lane, q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
   __syncwarp();
   const int q = lane & 7;
   const int c = col0 + 4 * q;
@@ -202,7 +198,7 @@ __device__ __forceinline__ void store_rsplit(const GsProblem &P, const Staging &
   for (int i = 0; i < 8; ++i) {
     const int r = 4 * i + (lane >> 3);
     if (row0 + r >= P.m || c >= P.mp) continue;
-    const float4 x = *sg.piece(r, q);
+    const float4 x = *tile_piece(stg, r, q);
     const float e[4] = {x.x, x.y, x.z, x.w};
     __nv_bfloat16 hv[4], lv[4];
 #pragma unroll
@@ -218,38 +214,42 @@ __device__ __forceinline__ void store_rsplit(const GsProblem &P, const Staging &
   __syncwarp();
 }
 
-// The epilogue of one 32-column chunk of a product: this warp's rows row0 .. row0 + 31 (lane = row), columns
-// col0 .. col0 + 31; v holds the lane's 32 accumulator values. Called by every lane of the warp.
-__device__ __forceinline__ void epilogue_chunk(const GsProblem &P, const Staging &sg, const Product &pr, int k,
-                                               int row0, int lane, int col0, int t, int N, const float *co, float *v) {
+// The epilogue of one 32-column chunk of a product, collective over the four epilogue warps: rows of block row
+// bi (lane = row quarter * 32 + lane of the block), columns col0 .. col0 + 31; v holds the lane's 32 values.
+// rstage: a 4 KB staging chunk of this warp for the R_N halves (in the operand ring, idle by then).
+__device__ __forceinline__ void epilogue_chunk(TileOut &to, const GsProblem &P, const Product &pr, int k, int bi,
+                                               int quarter, int lane, int col0, int t, int N, const float *co,
+                                               float *v, uint8_t *rstage) {
+  const int row0 = bi * GS_BLOCK + quarter * 32;
   const int row = row0 + lane;
   if (col0 < P.m) {
     if (pr.kind == EK_Q) {
       // Q = a I + (b A + c A^2), the bracket from the MMA
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] += col0 + j == row ? co[3 * t] : 0.f;
-      if (t == 0 && N > 1) store_split(P, sg, lane, GS_R0, k, row0, col0, v);   // R_1 = Q_0
+      if (t == 0 && N > 1) store_split(to, P, bi, quarter, lane, GS_R0, k, col0, v);   // R_1 = Q_0
     }
-    store_split(P, sg, lane, pr.out_buf, k, row0, col0, v);
+    store_split(to, P, bi, quarter, lane, pr.out_buf, k, col0, v);
     if (pr.kind == EK_A) {
       // the next step's right operand c' A' + b' I
       const float bn = co[3 * (t + 1) + 1], cn = co[3 * (t + 1) + 2];
       float w[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) w[j] = fmaf(cn, v[j], col0 + j == row ? bn : 0.f);
-      store_split(P, sg, lane, GS_B, k, row0, col0, w);
+      store_split(to, P, bi, quarter, lane, GS_B, k, col0, w);
     }
   }
-  // R_N: at t = 0 when N = 1 (R_1 = Q_0), else from the last R product
-  if ((pr.kind == EK_Q && N == 1) || (pr.kind == EK_R && t == N - 1)) store_rsplit(P, sg, lane, k, row0, col0, v);
+  // R_N: at t = 0 when N = 1 (R_1 = Q_0), else from the last R product (the phase's only product either way)
+  if (row0 < P.m && ((pr.kind == EK_Q && N == 1) || (pr.kind == EK_R && t == N - 1)))
+    store_rsplit(P, rstage, lane, k, row0, col0, v);
 }
 
 __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS, 1)
     gram_space_kernel(const __grid_constant__ GsGroup args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *staging = smem + GS_STAGES * GS_STAGE_BYTES;
-  GsCtrl *ctrl = reinterpret_cast<GsCtrl *>(staging + GS_EPI_WARPS * GS_STAGING_BYTES);
+  uint8_t *out_tiles = smem + GS_STAGES * GS_STAGE_BYTES;
+  GsCtrl *ctrl = reinterpret_cast<GsCtrl *>(out_tiles + GS_OUT_TILES * GS_TILE_BYTES);
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const uint32_t rank = cluster_ctarank();
@@ -293,6 +293,7 @@ __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS,
   constexpr uint32_t idesc = idesc_tf32_f32(GS_BLOCK, GS_BLOCK);
 
   // pipeline state, carried across products and phases
+  TileOut tout{out_tiles, map, 0, warp == 2 && lane == 0};
   uint32_t stage = 0, sphase = 0;
   int last_parity[GS_STAGES] = {-1, -1, -1};
   uint32_t acc_uses[2] = {0u, 0u};
@@ -384,15 +385,16 @@ __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS,
       } else {
         // -------------------------------------------------------------- epilogue (warps 2..5)
         const int quarter = warp & 3;               // tensor-memory lanes this warp may read
-        const int row0 = bi * GS_BLOCK + quarter * 32;
-        const Staging sg{staging + (warp - 2) * GS_STAGING_BYTES};
+        uint8_t *rstage = smem + (warp - 2) * (32 * 32 * 4);
         for (int q = 0; q < np; ++q) {
           const Product pr = prods[q];
           const uint32_t par = acc_uses[pr.acc] & 1u;
           acc_uses[pr.acc] += 1u;
           if (!work) continue;
           const bool ok = wait_bounded(&ctrl->acc_full[pr.acc], par, ctl, ERR_WAIT_ACC_FULL);
-          if (!__all_sync(0xffffffffu, ok)) continue;
+          // the output stores are collective over the four epilogue warps: they go on only if all saw the
+          // accumulator (each thread arrives here after a bounded wait)
+          if (!named_barrier_and(GS_EPI_BAR, GS_EPI_WARPS * 32, ok)) continue;
           if (rec && q == 0 && warp == 2 && lane == 0) rec[5] = globaltimer_ns();
           tc_fence_after();
 #pragma unroll 1
@@ -403,9 +405,13 @@ __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS,
             tmem_ld_32x32b_x32(tmem + static_cast<uint32_t>(pr.acc * GS_BLOCK + cc * 32) +
                                    (static_cast<uint32_t>(quarter * 32) << 16),
                                v);
-            if (row0 >= P.m) continue;   // warp-uniform
-            epilogue_chunk(P, sg, pr, k, row0, lane, col0, t, N, args.coeffs, v);
+            epilogue_chunk(tout, P, pr, k, bi, quarter, lane, col0, t, N, args.coeffs, v, rstage);
           }
+        }
+        // every store of the phase has been performed before the barrier publishes it
+        if (tout.issuer) {
+          bulk_wait_group_all();
+          fence_proxy_async_global();
         }
         if (rec && warp == 2 && lane == 0) rec[6] = globaltimer_ns();
       }
