@@ -4,7 +4,9 @@ The update (decay, step) is applied to the fp32 master and the bf16 parameter be
 rounded to bf16 ("Optimizers: AdamW, Muon and the distributed optimizer", section "The optimizer's memory
 budget": fp32 master weights beside bf16 weights). The oracle is the fp32-parameter Muon update on the
 master; the bf16 parameter must equal the GPU's master rounded to bf16, bit for bit, after every step.
-Wide and tall (transposed path) ragged stacks, two steps.
+Wide and tall (transposed path) ragged stacks, two steps, on the plain chain and (200 x 1000 and its
+transpose) on the Gram-space path, whose final step is the same master-weight kernel with the [R_hi | R_lo]
+operand.
 """
 import numpy as np
 import pytest
@@ -22,10 +24,11 @@ def L():
     return build_lib()
 
 
-@pytest.mark.parametrize("shape", [(136, 264), (264, 136)])
+@pytest.mark.parametrize("shape", [(136, 264), (264, 136), (200, 1000), (1000, 200)])
 def test_muon_fp32_master_two_steps(L, shape):
     A, B = shape
     K = 3
+    assert L.muon_gram_space_route(A, B) == (min(A, B) == 200)
     hp = workloads.workload("tiny").muon_hp
     gen = torch.Generator().manual_seed(A * 7 + B)
     master = [(torch.randn((A, B), generator=gen) * 0.05).to(DEV) for _ in range(K)]
