@@ -249,13 +249,23 @@ bool counter_deps_for(double est_us) {
   return mode == 1 || (mode == -1 && est_us <= 500.0);
 }
 
-// Whether a stack takes the Gram-space path: an eligible shape (m <= 256 and not the fused small-matrix
-// kernel's) whose long side is at least four times its short one, where the m x m chain (about 4 m^3 flops per
-// step in three tf32 passes) costs a fraction of the plain step's 4 m^2 n + 2 m^3 bf16 flops.
-bool gram_space_route(long long m, long long n) {
+// Whether a stack of K wide m x n iterates takes the Gram-space path: never for shapes that cannot (m > 256, or
+// the fused small-matrix kernel's); else as forced by muon_debug_gram_space, else as measured by muon_autotune
+// for this (m, n, K), else where the long side is at least four times the short one, where the m x m chain
+// (about 4 m^3 flops per step in three tf32 passes) costs a fraction of the plain step's 4 m^2 n + 2 m^3.
+std::mutex g_route_mu;
+std::map<std::vector<long long>, int> g_route_table;   // (m, n, K) -> measured: 1 Gram space, 0 plain chain
+
+bool gram_space_route(long long m, long long n, long long K) {
   if (!gram_space_eligible(m, n)) return false;
   const int mode = g_gram_space.load();
-  return mode == 1 || (mode == -1 && n >= 4 * m);
+  if (mode >= 0) return mode == 1;
+  {
+    std::lock_guard<std::mutex> lk(g_route_mu);
+    auto it = g_route_table.find({m, n, K});
+    if (it != g_route_table.end()) return it->second == 1;
+  }
+  return n >= 4 * m;
 }
 
 // The Gram-space path's launches for one stack, added to three batches: the fp32 Gram A_0 = s^2 U U^T of the
@@ -293,7 +303,7 @@ muon_status launch_gram_space_batches(GemmBatch &g32, const std::vector<GramSpac
 muon_status run_ns_chain(uint32_t *err, char *ws, const Layout &L, long long K, int ns_steps, const float *coeffs,
                          const FinalSpec &fin, cudaStream_t s, uint32_t *counters, uint32_t norm_tiles) {
   if (ns_small_fits(L.m, L.n)) return launch_ns_small(small_args(err, ws, L, K, ns_steps, coeffs, fin), s);
-  if (gram_space_route(L.m, L.n)) {
+  if (gram_space_route(L.m, L.n, K)) {
     GemmBatch g32(EPI_GRAM32, err, g_timeout_ns), fb(EPI_FINAL, err, g_timeout_ns);
     std::vector<GramSpaceStack> gs;
     muon_status st = add_gram_space(ws, L, K, coeffs, fin, g32, gs, fb);
@@ -431,123 +441,136 @@ static muon_status check_grouped(const muon_bucket *buckets, int n, const muon_h
 }
 
 // The launches of one grouped Muon step, on stream s (arguments already checked).
-static muon_status enqueue_grouped(const muon_bucket *buckets, int n, const muon_hparams *hp, void *ws,
-                                   cudaStream_t s, unsigned *extra_zero = nullptr, long long extra_n = 0) {
+}  // extern "C"
+
+namespace muon_grouped_detail {
+using namespace muon;
+
+// Where a stack's Newton-Schulz chain runs.
+enum : int { PATH_SMALL = 0, PATH_GRAM = 1, PATH_PLAIN = 2 };
+
+// One stack of a grouped call, as the chain issuer sees it.
+struct ChainStack {
+  Layout L;
+  char *w;               // the stack's sections
+  long long K, k0;       // matrices; the first one's index in the call's counters
+  uint32_t norm_done;    // the norm counter's value once the stack's U and scales are stored
+  FinalSpec fin;
+  int path;
+};
+
+// What the chain issuer needs besides the stacks.
+struct ChainCall {
+  uint32_t *err;
+  uint32_t *counters;    // the header's four counters per matrix
+  long long total_K;
+  int ns_steps;
+  const float *coeffs;
+  bool norm_wait;        // the first Gram launch waits on the norm counters (false: no norm pass precedes)
+  int deps;              // plain chain: -1 the table or the rule, 0 launch order, 1 per-matrix counters
+};
+
+// The plain stacks' (m, n, K) in order: the key of a grouped chain's measured scheduling mode.
+std::vector<long long> plain_signature(const std::vector<ChainStack> &cs) {
+  std::vector<long long> sig;
+  for (const ChainStack &c : cs)
+    if (c.path == PATH_PLAIN) sig.insert(sig.end(), {c.L.m, c.L.n, c.K});
+  return sig;
+}
+
+std::mutex g_sched_mu;
+std::map<std::vector<long long>, int> g_deps_table;   // plain-chain signature -> measured scheduling mode
+
+int deps_lookup(const std::vector<long long> &sig) {
+  std::lock_guard<std::mutex> lk(g_sched_mu);
+  auto it = g_deps_table.find(sig);
+  return it == g_deps_table.end() ? -1 : it->second;
+}
+
+// The chains of a grouped call, after its norm pass. Launch order: the branches first (small stacks: the whole
+// chain in one fused launch each; Gram-space stacks: fp32 Gram, m x m chain, final step), each launch waiting
+// for the whole previous grid; then the plain chain of the other stacks. Where the plain chain's launches wait
+// per matrix on counters, its first launch also waits for the previous grid, so that the step's last launch
+// completes only after every branch.
+muon_status issue_chains(const std::vector<ChainStack> &cs, const ChainCall &cc, cudaStream_t s) {
   muon_status st;
-  char *base = static_cast<char *>(ws);
-  uint32_t *err = reinterpret_cast<uint32_t *>(base);
   const unsigned long long to = g_timeout_ns;
-  std::vector<Layout> L(n);
-  std::vector<char *> w(n);
-  long long total_K = 0;
-  for (int i = 0; i < n; ++i) total_K += buckets[i].K;
-  unsigned *counters = reinterpret_cast<unsigned *>(base + CTRL_BYTES);
-  size_t off = header_bytes(total_K);
-  for (int i = 0; i < n; ++i) {
-    L[i] = layout(buckets[i].K, buckets[i].A, buckets[i].B);
-    w[i] = base + off;
-    off += L[i].total;
-  }
-  // readiness counters of the chain: G, H and X of matrix k at G_ready[k], H_ready[k], X_ready[k]; they only
-  // grow during a step (t-th launch of a kind: target t times its per-launch count) and start at zero
-  uint32_t *G_ready = counters + total_K, *H_ready = counters + 2 * total_K, *X_ready = counters + 3 * total_K;
-  // momentum, Nesterov input, norm: all buckets in one pass
-  // (extra_zero: more counters to clear in the same launch, for a call that follows this chain)
-  if ((st = launch_counter_reset(counters, 4 * total_K, s, extra_zero, extra_n)) != MUON_OK) return st;
-  std::vector<NesterovArgs> na(n);
-  for (long long i = 0, k0 = 0; i < n; k0 += buckets[i].K, ++i) {
-    const muon_bucket &bk = buckets[i];
-    na[i] = nesterov_args(w[i], L[i], counters + k0, bk.K, bk.A, bk.B, bk.grads, nullptr, bk.gdt, bk.momentum,
-                          hp->momentum, hp->nesterov != 0, hp->eps);
-  }
-  if ((st = launch_nesterov_norm(na.data(), n, s)) != MUON_OK) return st;
-  auto final_spec = [&](const muon_bucket &bk) {
-    const double scale = hp->scale_mode == 0
-                             ? 0.2 * std::sqrt(static_cast<double>(bk.A > bk.B ? bk.A : bk.B))
-                             : std::sqrt(std::max(1.0, static_cast<double>(bk.A) / static_cast<double>(bk.B)));
-    FinalSpec fin{};
-    fin.params = bk.params;
-    fin.master = bk.master;
-    fin.dtype = bk.pdt;
-    fin.transposed = bk.A > bk.B ? 1 : 0;
-    fin.orig_cols = static_cast<int>(bk.B);
-    fin.cautious = hp->cautious_wd ? 1 : 0;
-    fin.lr_wd = static_cast<float>(static_cast<double>(hp->lr) * hp->weight_decay);
-    fin.lr_scale = static_cast<float>(static_cast<double>(hp->lr) * scale);
-    return fin;
-  };
-  // Launch order: the branches first (small buckets: the whole chain in one fused launch each; Gram-space
-  // buckets: fp32 Gram, m x m chain, final step), each launch waiting for the whole previous grid; then the
-  // plain chain of the other buckets. Where the plain chain's launches wait per matrix on counters, its first
-  // launch also waits for the previous grid, so that the step's last launch completes only after every branch.
-  std::vector<char> small(n, 0), gspace(n, 0);
+  const int N = cc.ns_steps;
   bool branch = false;
-  for (int i = 0; i < n; ++i) {
-    if (!ns_small_fits(L[i].m, L[i].n)) continue;
-    small[i] = 1;
+  for (const ChainStack &c : cs) {
+    if (c.path != PATH_SMALL) continue;
     branch = true;
-    const SmallNsArgs sa = small_args(err, w[i], L[i], buckets[i].K, hp->ns_steps, hp->coeffs, final_spec(buckets[i]));
-    if ((st = launch_ns_small(sa, s)) != MUON_OK) return st;
+    if ((st = launch_ns_small(small_args(cc.err, c.w, c.L, c.K, N, cc.coeffs, c.fin), s)) != MUON_OK) return st;
   }
   {
-    GemmBatch g32(EPI_GRAM32, err, to), fb(EPI_FINAL, err, to);
+    GemmBatch g32(EPI_GRAM32, cc.err, to), fb(EPI_FINAL, cc.err, to);
     std::vector<GramSpaceStack> gs;
-    for (int i = 0; i < n; ++i) {
-      if (small[i] || !gram_space_route(L[i].m, L[i].n)) continue;
-      gspace[i] = 1;
-      if ((st = add_gram_space(w[i], L[i], buckets[i].K, hp->coeffs, final_spec(buckets[i]), g32, gs, fb)) !=
-          MUON_OK)
+    for (const ChainStack &c : cs)
+      if (c.path == PATH_GRAM && (st = add_gram_space(c.w, c.L, c.K, cc.coeffs, c.fin, g32, gs, fb)) != MUON_OK)
         return st;
-    }
     if (!gs.empty()) {
       branch = true;
-      if ((st = launch_gram_space_batches(g32, gs, fb, hp->ns_steps, hp->coeffs, err, s)) != MUON_OK) return st;
+      if ((st = launch_gram_space_batches(g32, gs, fb, N, cc.coeffs, cc.err, s)) != MUON_OK) return st;
     }
   }
-  // per-matrix counter dependencies where the launches (all buckets of a step kind in one) are short
-  double est_us = 0.0;
-  for (int kind = EPI_GRAM; kind <= EPI_APPLY; ++kind) {
-    double us = 0.0;
-    for (int i = 0; i < n; ++i)
-      if (!small[i] && !gspace[i]) us += launch_estimate_us(kind, L[i].m, L[i].n, buckets[i].K);
-    est_us = std::max(est_us, us);
+  // scheduling of the plain chain: forced, else measured for this set of stacks, else the rule (per-matrix
+  // counters where the launches, all stacks of a step kind in one, are short)
+  bool deps;
+  if (cc.deps >= 0) {
+    deps = cc.deps == 1;
+  } else if (g_counter_deps.load() >= 0) {
+    deps = g_counter_deps.load() == 1;
+  } else {
+    const int measured = deps_lookup(plain_signature(cs));
+    if (measured >= 0) {
+      deps = measured == 1;
+    } else {
+      double est_us = 0.0;
+      for (int kind = EPI_GRAM; kind <= EPI_APPLY; ++kind) {
+        double us = 0.0;
+        for (const ChainStack &c : cs)
+          if (c.path == PATH_PLAIN) us += launch_estimate_us(kind, c.L.m, c.L.n, c.K);
+        est_us = std::max(est_us, us);
+      }
+      deps = est_us <= 500.0;
+    }
   }
-  const bool deps = counter_deps_for(est_us);
-  // the Newton-Schulz chain of the other buckets, each step kind of all of them in one grouped launch
-  for (int t = 0; t < hp->ns_steps; ++t) {
-    const float a = hp->coeffs[3 * t], b = hp->coeffs[3 * t + 1], c = hp->coeffs[3 * t + 2];
-    GemmBatch gram(EPI_GRAM, err, to), poly(EPI_POLY, err, to);
-    GemmBatch last(t + 1 < hp->ns_steps ? EPI_APPLY : EPI_FINAL, err, to);
+  uint32_t *G_ready = cc.counters + cc.total_K, *H_ready = cc.counters + 2 * cc.total_K;
+  uint32_t *X_ready = cc.counters + 3 * cc.total_K;
+  for (int t = 0; t < N; ++t) {
+    const float a = cc.coeffs[3 * t], b = cc.coeffs[3 * t + 1], c3 = cc.coeffs[3 * t + 2];
+    GemmBatch gram(EPI_GRAM, cc.err, to), poly(EPI_POLY, cc.err, to);
+    GemmBatch last(t + 1 < N ? EPI_APPLY : EPI_FINAL, cc.err, to);
     if (t == 0 && branch) gram.force_grid_wait(true);
-    for (int i = 0, k0 = 0; i < n; k0 += static_cast<int>(buckets[i].K), ++i) {
-      if (small[i] || gspace[i]) continue;
-      const Layout &Li = L[i];
-      const float *sc = t == 0 ? reinterpret_cast<const float *>(w[i] + Li.scale) : nullptr;
+    for (const ChainStack &c : cs) {
+      if (c.path != PATH_PLAIN) continue;
+      const Layout &Li = c.L;
+      const long long k0 = c.k0;
+      const float *sc = t == 0 ? reinterpret_cast<const float *>(c.w + Li.scale) : nullptr;
       const uint32_t e_gram = gemm_signals_per_matrix(EPI_GRAM, Li.m, Li.n);
       const uint32_t e_poly = gemm_signals_per_matrix(EPI_POLY, Li.m, Li.n);
       const uint32_t e_apply = gemm_signals_per_matrix(EPI_APPLY, Li.m, Li.n);
       const uint32_t tt = static_cast<uint32_t>(t);
       // GRAM of step 0 reads the norm pass's output: a matrix's norm counter reaches its tile count plus one
       // once its U and scale are stored
-      const uint32_t norm_done = static_cast<uint32_t>(na[i].tiles_r * na[i].tiles_c) + 1u;
-      const TileSync sync_gram{t == 0 ? counters + k0 : X_ready + k0, t == 0 ? norm_done : tt * e_apply,
-                               G_ready + k0};
+      const TileSync sync_gram{t == 0 ? (cc.norm_wait ? cc.counters + k0 : nullptr) : X_ready + k0,
+                               t == 0 ? c.norm_done : tt * e_apply, G_ready + k0};
       const TileSync sync_poly{G_ready + k0, (tt + 1) * e_gram, H_ready + k0};
-      const TileSync sync_last{H_ready + k0, (tt + 1) * e_poly, t + 1 < hp->ns_steps ? X_ready + k0 : nullptr};
-      __nv_bfloat16 *xb[2] = {reinterpret_cast<__nv_bfloat16 *>(w[i] + Li.x0),
-                              reinterpret_cast<__nv_bfloat16 *>(w[i] + Li.x1)};
-      __nv_bfloat16 *G = reinterpret_cast<__nv_bfloat16 *>(w[i] + Li.g);
-      __nv_bfloat16 *H = reinterpret_cast<__nv_bfloat16 *>(w[i] + Li.h);
-      const long long K = buckets[i].K, msx = Li.m * Li.ldx, msg = Li.m * Li.ldg;
+      const TileSync sync_last{H_ready + k0, (tt + 1) * e_poly, t + 1 < N ? X_ready + k0 : nullptr};
+      __nv_bfloat16 *xb[2] = {reinterpret_cast<__nv_bfloat16 *>(c.w + Li.x0),
+                              reinterpret_cast<__nv_bfloat16 *>(c.w + Li.x1)};
+      __nv_bfloat16 *G = reinterpret_cast<__nv_bfloat16 *>(c.w + Li.g);
+      __nv_bfloat16 *H = reinterpret_cast<__nv_bfloat16 *>(c.w + Li.h);
+      const long long K = c.K, msx = Li.m * Li.ldx, msg = Li.m * Li.ldg;
       Bf16Stack X{xb[t & 1], Li.m, Li.n, Li.ldx, msx, K};
       Bf16Stack Gs{G, Li.m, Li.m, Li.ldg, msg, K};
       Bf16Stack Hs{H, Li.m, Li.m, Li.ldg, msg, K};
       if ((st = gram.add_gram(X, G, Li.ldg, msg, 1.0f, sc, deps ? &sync_gram : nullptr)) != MUON_OK) return st;
-      if ((st = poly.add_poly(Gs, H, Li.ldg, msg, a, b, c, deps ? &sync_poly : nullptr)) != MUON_OK) return st;
-      if (t + 1 < hp->ns_steps) {
+      if ((st = poly.add_poly(Gs, H, Li.ldg, msg, a, b, c3, deps ? &sync_poly : nullptr)) != MUON_OK) return st;
+      if (t + 1 < N) {
         st = last.add_apply(Hs, X, xb[(t + 1) & 1], sc, deps ? &sync_last : nullptr);
       } else {
-        st = last.add_final(Hs, X, sc, final_spec(buckets[i]), deps ? &sync_last : nullptr);
+        st = last.add_final(Hs, X, sc, c.fin, deps ? &sync_last : nullptr);
       }
       if (st != MUON_OK) return st;
     }
@@ -555,6 +578,99 @@ static muon_status enqueue_grouped(const muon_bucket *buckets, int n, const muon
       return st;
   }
   return MUON_OK;
+}
+
+FinalSpec final_spec_of(const muon_bucket &bk, const muon_hparams *hp) {
+  const double scale = hp->scale_mode == 0
+                           ? 0.2 * std::sqrt(static_cast<double>(bk.A > bk.B ? bk.A : bk.B))
+                           : std::sqrt(std::max(1.0, static_cast<double>(bk.A) / static_cast<double>(bk.B)));
+  FinalSpec fin{};
+  fin.params = bk.params;
+  fin.master = bk.master;
+  fin.dtype = bk.pdt;
+  fin.transposed = bk.A > bk.B ? 1 : 0;
+  fin.orig_cols = static_cast<int>(bk.B);
+  fin.cautious = hp->cautious_wd ? 1 : 0;
+  fin.lr_wd = static_cast<float>(static_cast<double>(hp->lr) * hp->weight_decay);
+  fin.lr_scale = static_cast<float>(static_cast<double>(hp->lr) * scale);
+  return fin;
+}
+
+// The stacks of a grouped call over workspace ws: layouts, sections, counters and paths (by the route rule,
+// the measured table, or the debug switch).
+std::vector<ChainStack> chain_stacks(const muon_bucket *buckets, int n, const muon_hparams *hp, char *base,
+                                     long long *total_K_out) {
+  long long total_K = 0;
+  for (int i = 0; i < n; ++i) total_K += buckets[i].K;
+  std::vector<ChainStack> cs(n);
+  size_t off = header_bytes(total_K);
+  for (long long i = 0, k0 = 0; i < n; k0 += buckets[i].K, ++i) {
+    ChainStack &c = cs[i];
+    c.L = layout(buckets[i].K, buckets[i].A, buckets[i].B);
+    c.w = base + off;
+    off += c.L.total;
+    c.K = buckets[i].K;
+    c.k0 = k0;
+    c.fin = final_spec_of(buckets[i], hp);
+    c.path = ns_small_fits(c.L.m, c.L.n) ? PATH_SMALL
+             : gram_space_route(c.L.m, c.L.n, c.K) ? PATH_GRAM
+                                                  : PATH_PLAIN;
+  }
+  *total_K_out = total_K;
+  return cs;
+}
+
+// Median device time of five runs of fn (after one warm-up run) on stream s, in ms; <0 on a CUDA error.
+template <typename F>
+float median_time(F fn, cudaStream_t s, muon_status *st) {
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+    if (e0) cudaEventDestroy(e0);
+    *st = MUON_ERR_CUDA;
+    return -1.f;
+  }
+  constexpr int REPS = 5;
+  float t[REPS];
+  *st = fn();
+  for (int r = 0; r < REPS && *st == MUON_OK; ++r) {
+    if (cudaEventRecord(e0, s) != cudaSuccess) *st = MUON_ERR_CUDA;
+    if (*st == MUON_OK) *st = fn();
+    if (*st == MUON_OK && (cudaEventRecord(e1, s) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+                           cudaEventElapsedTime(&t[r], e0, e1) != cudaSuccess))
+      *st = MUON_ERR_CUDA;
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (*st != MUON_OK) return -1.f;
+  std::sort(t, t + REPS);
+  return t[REPS / 2];
+}
+
+}  // namespace muon_grouped_detail
+
+extern "C" {
+
+static muon_status enqueue_grouped(const muon_bucket *buckets, int n, const muon_hparams *hp, void *ws,
+                                   cudaStream_t s, unsigned *extra_zero = nullptr, long long extra_n = 0) {
+  using namespace muon_grouped_detail;
+  muon_status st;
+  char *base = static_cast<char *>(ws);
+  long long total_K = 0;
+  std::vector<ChainStack> cs = chain_stacks(buckets, n, hp, base, &total_K);
+  unsigned *counters = reinterpret_cast<unsigned *>(base + CTRL_BYTES);
+  // (extra_zero: more counters to clear in the same launch, for a call that follows this chain)
+  if ((st = launch_counter_reset(counters, 4 * total_K, s, extra_zero, extra_n)) != MUON_OK) return st;
+  // momentum, Nesterov input, norm: all buckets in one pass
+  std::vector<NesterovArgs> na(n);
+  for (int i = 0; i < n; ++i) {
+    const muon_bucket &bk = buckets[i];
+    na[i] = nesterov_args(cs[i].w, cs[i].L, counters + cs[i].k0, bk.K, bk.A, bk.B, bk.grads, nullptr, bk.gdt,
+                          bk.momentum, hp->momentum, hp->nesterov != 0, hp->eps);
+    cs[i].norm_done = static_cast<uint32_t>(na[i].tiles_r * na[i].tiles_c) + 1u;
+  }
+  if ((st = launch_nesterov_norm(na.data(), n, s)) != MUON_OK) return st;
+  ChainCall cc{reinterpret_cast<uint32_t *>(base), counters, total_K, hp->ns_steps, hp->coeffs, true, -1};
+  return issue_chains(cs, cc, s);
 }
 
 muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hparams *hp, void *ws, size_t ws_bytes,
@@ -645,79 +761,131 @@ muon_status adamw_step_master(float *master, void *param, const void *grad, muon
 
 // ------------------------------------------------------------------------------------------ autotune
 
-muon_status muon_autotune(const muon_bucket *buckets, int n, void *ws, size_t ws_bytes, muon_stream_t stream) {
-  if (buckets == nullptr || ws == nullptr || n < 1 || n > 4096) return MUON_ERR_INVALID_ARG;
+muon_status muon_autotune(const muon_bucket *buckets, int n, const muon_hparams *hp, void *ws, size_t ws_bytes,
+                          muon_stream_t stream) {
+  using namespace muon_grouped_detail;
+  if (buckets == nullptr || hp == nullptr || ws == nullptr || n < 1 || n > 4096) return MUON_ERR_INVALID_ARG;
   muon_status st;
   for (int i = 0; i < n; ++i)
     if ((st = check_bucket(buckets[i])) != MUON_OK) return st;
+  if ((st = check_coeffs(hp->ns_steps, hp->coeffs)) != MUON_OK) return st;
   if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MUON_ERR_ALIGNMENT;
   if (ws_bytes < muon_workspace_bytes_grouped(buckets, n)) return MUON_ERR_WORKSPACE;
   if ((st = check_device()) != MUON_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char *base = static_cast<char *>(ws);
   uint32_t *err = reinterpret_cast<uint32_t *>(base);
+  unsigned *counters = reinterpret_cast<unsigned *>(base + CTRL_BYTES);
   long long total_K = 0;
-  for (int i = 0; i < n; ++i) total_K += buckets[i].K;
-  // the POLY launch of the grouped step: every bucket that does not take the fused small-matrix chain,
-  // reading its G section and writing its H section (the values do not matter for the time)
-  std::vector<Layout> L(n);
-  std::vector<char *> w(n);
-  size_t off = header_bytes(total_K);
-  int max_k = 0;
-  bool any = false;
-  for (int i = 0; i < n; ++i) {
-    L[i] = layout(buckets[i].K, buckets[i].A, buckets[i].B);
-    w[i] = base + off;
-    off += L[i].total;
-    if (ns_small_fits(L[i].m, L[i].n) || gram_space_route(L[i].m, L[i].n)) continue;
-    any = true;
-    max_k = std::max(max_k, static_cast<int>((L[i].m + 63) / 64));
+  std::vector<ChainStack> cs = chain_stacks(buckets, n, hp, base, &total_K);
+  const int N = hp->ns_steps;
+  // Every timed run works on the workspace alone: the chains start from whatever iterate x0 holds (no norm pass,
+  // so parameters, gradients and momentum are not read) and the final step writes a dense bf16 output into an
+  // iterate buffer the chain no longer reads, instead of updating parameters. Times do not depend on the values.
+  for (ChainStack &c : cs) {
+    c.norm_done = 0;
+    c.fin = FinalSpec{};
+    c.fin.dtype = MUON_BF16;
+    c.fin.orig_cols = static_cast<int>(c.L.n);
   }
-  if (!any) return MUON_OK;
-  auto launch_poly_batch = [&](int shape) -> muon_status {
-    GemmBatch poly(EPI_POLY, err, g_timeout_ns);
-    poly.force_shape(shape);
-    for (int i = 0; i < n; ++i) {
-      if (ns_small_fits(L[i].m, L[i].n) || gram_space_route(L[i].m, L[i].n)) continue;
-      const long long K = buckets[i].K, msg = L[i].m * L[i].ldg;
-      Bf16Stack Gs{w[i] + L[i].g, L[i].m, L[i].m, L[i].ldg, msg, K};
-      muon_status r = poly.add_poly(Gs, reinterpret_cast<__nv_bfloat16 *>(w[i] + L[i].h), L[i].ldg, msg, 3.4445f,
-                                    -4.7750f, 2.0315f);
-      if (r != MUON_OK) return r;
-    }
-    return poly.launch(s);
+  auto dense_out = [&](ChainStack &c) {
+    // plain chain: the final step reads iterate (N - 1) & 1; the Gram-space and small paths read only x0
+    const bool x0_free = c.path == PATH_PLAIN && ((N - 1) & 1) == 1;
+    c.fin.out_dense = c.w + (x0_free ? c.L.x0 : c.L.x1);
   };
-  cudaEvent_t e0 = nullptr, e1 = nullptr;
-  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
-    if (e0) cudaEventDestroy(e0);
-    return MUON_ERR_CUDA;
-  }
-  constexpr int REPS = 5;
-  int best = -1;
-  float best_ms = 0.f;
-  st = MUON_OK;
-  for (int shape = 0; shape < POLY_SHAPES && st == MUON_OK; ++shape) {
-    float t[REPS];
-    st = launch_poly_batch(shape);   // warm-up (first launch of this shape sets its shared-memory attribute)
-    for (int r = 0; r < REPS && st == MUON_OK; ++r) {
-      if (cudaEventRecord(e0, s) != cudaSuccess) st = MUON_ERR_CUDA;
-      if (st == MUON_OK) st = launch_poly_batch(shape);
-      if (st == MUON_OK && (cudaEventRecord(e1, s) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
-                            cudaEventElapsedTime(&t[r], e0, e1) != cudaSuccess))
-        st = MUON_ERR_CUDA;
+  auto run = [&](std::vector<ChainStack> &set, int deps) -> muon_status {
+    muon_status r = launch_counter_reset(counters, 4 * total_K, s);
+    if (r != MUON_OK) return r;
+    ChainCall cc{err, counters, total_K, N, hp->coeffs, false, deps};
+    return issue_chains(set, cc, s);
+  };
+  // 1. the path of each stack that can take the Gram-space chain: each way, that stack alone
+  for (ChainStack &c : cs) {
+    if (c.path == PATH_SMALL || !gram_space_eligible(c.L.m, c.L.n) || g_gram_space.load() >= 0) continue;
+    float best = -1.f;
+    int best_path = c.path;
+    for (int path : {PATH_GRAM, PATH_PLAIN}) {
+      c.path = path;
+      dense_out(c);
+      std::vector<ChainStack> one{c};
+      const float ms = median_time([&] { return run(one, -1); }, s, &st);
+      if (st != MUON_OK) return st;
+      if (best < 0.f || ms < best) {
+        best = ms;
+        best_path = path;
+      }
     }
-    if (st != MUON_OK) break;
-    std::sort(t, t + REPS);
-    if (best < 0 || t[REPS / 2] < best_ms) {
-      best = shape;
-      best_ms = t[REPS / 2];
-    }
+    c.path = best_path;
+    std::lock_guard<std::mutex> lk(g_route_mu);
+    g_route_table[{c.L.m, c.L.n, c.K}] = best_path == PATH_GRAM ? 1 : 0;
   }
-  cudaEventDestroy(e0);
-  cudaEventDestroy(e1);
-  if (st != MUON_OK) return st;
-  poly_shape_record(max_k, best);
-  return MUON_OK;
+  for (ChainStack &c : cs) dense_out(c);
+  // 2. the poly step's pipeline shape, on the plain stacks' grouped poly launch (reads G, writes H)
+  int max_k = 0;
+  bool any_plain = false;
+  for (const ChainStack &c : cs)
+    if (c.path == PATH_PLAIN) {
+      any_plain = true;
+      max_k = std::max(max_k, static_cast<int>((c.L.m + 63) / 64));
+    }
+  if (any_plain) {
+    int best = -1;
+    float best_ms = 0.f;
+    for (int shape = 0; shape < POLY_SHAPES; ++shape) {
+      const float ms = median_time(
+          [&]() -> muon_status {
+            GemmBatch poly(EPI_POLY, err, g_timeout_ns);
+            poly.force_shape(shape);
+            for (const ChainStack &c : cs) {
+              if (c.path != PATH_PLAIN) continue;
+              const long long msg = c.L.m * c.L.ldg;
+              Bf16Stack Gs{c.w + c.L.g, c.L.m, c.L.m, c.L.ldg, msg, c.K};
+              muon_status r = poly.add_poly(Gs, reinterpret_cast<__nv_bfloat16 *>(c.w + c.L.h), c.L.ldg, msg,
+                                            hp->coeffs[0], hp->coeffs[1], hp->coeffs[2]);
+              if (r != MUON_OK) return r;
+            }
+            return poly.launch(s);
+          },
+          s, &st);
+      if (st != MUON_OK) return st;
+      if (best < 0 || ms < best_ms) {
+        best = shape;
+        best_ms = ms;
+      }
+    }
+    poly_shape_record(max_k, best);
+  }
+  // 3. the plain chain's scheduling: per-matrix counters or launch order, for the whole set as it will run
+  if (any_plain && g_counter_deps.load() < 0) {
+    float t_mode[2];
+    for (int deps = 0; deps < 2; ++deps) {
+      t_mode[deps] = median_time([&] { return run(cs, deps); }, s, &st);
+      if (st != MUON_OK) return st;
+    }
+    std::lock_guard<std::mutex> lk(g_sched_mu);
+    g_deps_table[plain_signature(cs)] = t_mode[1] < t_mode[0] ? 1 : 0;
+  }
+  return muon_check(ws, stream) == MUON_ERR_TIMEOUT ? MUON_ERR_TIMEOUT : MUON_OK;
+}
+
+int32_t muon_autotune_route(int64_t K, int64_t A, int64_t B) {
+  if (K < 1 || A < 1 || B < 1) return -1;
+  std::lock_guard<std::mutex> lk(g_route_mu);
+  auto it = g_route_table.find({std::min(A, B), std::max(A, B), K});
+  return it == g_route_table.end() ? -1 : it->second;
+}
+
+int32_t muon_autotune_scheduling(const muon_bucket *buckets, int n) {
+  using namespace muon_grouped_detail;
+  if (buckets == nullptr || n < 1 || n > 4096) return -1;
+  std::vector<long long> sig;
+  for (int i = 0; i < n; ++i) {
+    const long long m = std::min(buckets[i].A, buckets[i].B), nn = std::max(buckets[i].A, buckets[i].B);
+    if (buckets[i].K < 1 || m < 1) return -1;
+    if (ns_small_fits(m, nn) || gram_space_route(m, nn, buckets[i].K)) continue;
+    sig.insert(sig.end(), {m, nn, static_cast<long long>(buckets[i].K)});
+  }
+  return deps_lookup(sig);
 }
 
 int32_t muon_autotune_poly_shape(int64_t contraction) {
@@ -725,7 +893,15 @@ int32_t muon_autotune_poly_shape(int64_t contraction) {
   return poly_shape_lookup(static_cast<int>((contraction + 63) / 64));
 }
 
-void muon_autotune_reset(void) { poly_shape_clear(); }
+void muon_autotune_reset(void) {
+  poly_shape_clear();
+  {
+    std::lock_guard<std::mutex> lk(g_route_mu);
+    g_route_table.clear();
+  }
+  std::lock_guard<std::mutex> lk(muon_grouped_detail::g_sched_mu);
+  muon_grouped_detail::g_deps_table.clear();
+}
 
 muon_status muon_debug_counter_deps(int32_t on) {
   if (on < -1 || on > 1) return MUON_ERR_INVALID_ARG;
@@ -739,9 +915,9 @@ muon_status muon_debug_gram_space(int32_t mode) {
   return MUON_OK;
 }
 
-int32_t muon_gram_space_route(int64_t A, int64_t B) {
-  if (A < 1 || B < 1) return 0;
-  return gram_space_route(std::min(A, B), std::max(A, B)) ? 1 : 0;
+int32_t muon_gram_space_route(int64_t K, int64_t A, int64_t B) {
+  if (K < 1 || A < 1 || B < 1) return 0;
+  return gram_space_route(std::min(A, B), std::max(A, B), K) ? 1 : 0;
 }
 
 muon_status muon_debug_poly_shape(int32_t shape) {

@@ -85,13 +85,16 @@ SIGNATURES = {
                                ctypes.c_size_t, _vp]),
     "ns_apply": (ctypes.c_int, [_vp, _vp, _vp, _c_int64, _c_int64, _c_int64, _vp, ctypes.c_size_t, _vp]),
     "muon_plan_buckets": (ctypes.c_int, [_c_int64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
-    "muon_autotune": (ctypes.c_int, [ctypes.POINTER(muon_bucket), ctypes.c_int, _vp, ctypes.c_size_t, _vp]),
+    "muon_autotune": (ctypes.c_int, [ctypes.POINTER(muon_bucket), ctypes.c_int, ctypes.POINTER(muon_hparams), _vp,
+                                     ctypes.c_size_t, _vp]),
+    "muon_autotune_route": (ctypes.c_int32, [_c_int64, _c_int64, _c_int64]),
+    "muon_autotune_scheduling": (ctypes.c_int32, [ctypes.POINTER(muon_bucket), ctypes.c_int]),
     "muon_autotune_poly_shape": (ctypes.c_int32, [_c_int64]),
     "muon_autotune_reset": (None, []),
     "muon_debug_poly_shape": (ctypes.c_int, [ctypes.c_int32]),
     "muon_debug_counter_deps": (ctypes.c_int, [ctypes.c_int32]),
     "muon_debug_gram_space": (ctypes.c_int, [ctypes.c_int32]),
-    "muon_gram_space_route": (ctypes.c_int32, [_c_int64, _c_int64]),
+    "muon_gram_space_route": (ctypes.c_int32, [_c_int64, _c_int64, _c_int64]),
     "muon_check": (ctypes.c_int, [_vp, _vp]),
     "muon_set_timeout_ns": (None, [ctypes.c_uint64]),
     "muon_debug_wait_timeout": (ctypes.c_int, [_vp, ctypes.c_size_t, ctypes.c_uint64, _vp]),
@@ -354,10 +357,21 @@ def muon_plan_buckets(shapes: Sequence[Tuple[int, int]]):
     }
 
 
-def muon_autotune(buckets, ws, stream=None):
-    """Measures the poly step's pipeline shapes on these buckets and records the fastest (synchronous)."""
-    _check(lib().muon_autotune(buckets, len(buckets), ws.data_ptr(), ws.numel() * ws.element_size(),
+def muon_autotune(buckets, hp, ws, stream=None):
+    """Measures, on the workspace alone, each eligible bucket's Newton-Schulz path, the poly step's pipeline shape
+    and the plain chain's scheduling for these buckets and hyperparameters, and records the fastest (synchronous)."""
+    _check(lib().muon_autotune(buckets, len(buckets), ctypes.byref(hp), ws.data_ptr(), ws.numel() * ws.element_size(),
                                _stream(stream)), "muon_autotune")
+
+
+def muon_autotune_route(K: int, A: int, B: int) -> int:
+    """The recorded path: 1 Gram space, 0 plain chain, -1 none."""
+    return int(lib().muon_autotune_route(int(K), int(A), int(B)))
+
+
+def muon_autotune_scheduling(buckets) -> int:
+    """The recorded scheduling of these buckets' plain chain: 1 counters, 0 launch order, -1 none."""
+    return int(lib().muon_autotune_scheduling(buckets, len(buckets)))
 
 
 def muon_autotune_poly_shape(contraction: int) -> int:
@@ -382,8 +396,8 @@ def muon_debug_gram_space(mode: int):
     _check(lib().muon_debug_gram_space(int(mode)), "muon_debug_gram_space")
 
 
-def muon_gram_space_route(A: int, B: int) -> bool:
-    return bool(lib().muon_gram_space_route(int(A), int(B)))
+def muon_gram_space_route(A: int, B: int, K: int = 1) -> bool:
+    return bool(lib().muon_gram_space_route(int(K), int(A), int(B)))
 
 
 def muon_check(ws, stream=None) -> int:

@@ -27,8 +27,9 @@ CLASSIC = (3.4445, -4.7750, 2.0315)
 # master_weights=True (bf16 parameters only): an fp32 master copy per parameter takes the update and the
 # parameter holds it rounded to bf16 ("Optimizers: AdamW, Muon and the distributed optimizer", section "The
 # optimizer's memory budget")
-# autotune=True: before the group's first step, the poly step's pipeline shape is measured on the group's own
-# buckets and the fastest recorded (muon_autotune; "DMuon", section 2.4, shape-adaptive kernel autotuning)
+# autotune=True: before the group's first step, the Newton-Schulz path of each bucket that can take the Gram-space
+# chain, the poly step's pipeline shape and the chain's scheduling are measured on the group's own buckets and the
+# fastest recorded (muon_autotune; "DMuon", section 2.4, shape-adaptive kernel autotuning)
 MUON_DEFAULTS = dict(lr=0.02, momentum=0.95, weight_decay=0.01, nesterov=True, cautious_wd=False, scale_mode=0,
                      ns_steps=5, ns_coefficients=None, eps=1e-7, master_weights=False, autotune=False)
 # is_adamw=False: Adam with L2 regularisation instead of decoupled decay ("dtensor-muon 0.1.0", "Key options")
@@ -145,7 +146,7 @@ class HybridMuonAdamW:
                 if specs:
                     arr = L.make_buckets(specs)
                     if group["autotune"] and id(group) not in self._tuned:
-                        L.muon_autotune(arr, self._ws)
+                        L.muon_autotune(arr, hp, self._ws)
                         self._tuned.add(id(group))
                     muon_calls.append((arr, hp))
             else:

@@ -394,6 +394,18 @@ def _run_e2e(wl, args, stream, world, device, barrier):
     for hg, dg in zip(host_g, dev_g):
         hg.copy_(dg)
     torch.cuda.synchronize()
+    # the pinned-copy bandwidth of this machine, each way, on the largest buffer (the floor of the end-to-end step)
+    big = max(range(len(dev_g)), key=lambda i: dev_g[i].numel())
+    nbytes = dev_g[big].numel() * dev_g[big].element_size()
+    c0, c1, c2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    c0.record()
+    dev_g[big].copy_(host_g[big], non_blocking=True)
+    c1.record()
+    host_p[big].copy_(dev_p[big], non_blocking=True)
+    c2.record()
+    torch.cuda.synchronize()
+    h2d_gbs = nbytes / (c0.elapsed_time(c1) * 1e-3) / 1e9
+    d2h_gbs = nbytes / (c1.elapsed_time(c2) * 1e-3) / 1e9
     e2e_steps = max(3, args.steps // 4)
     nb = len(wl.buckets)
     groups = wl.split_buckets()
@@ -426,14 +438,14 @@ def _run_e2e(wl, args, stream, world, device, barrier):
     e2e_ms = max_over_ranks(1e3 * (time.perf_counter() - t0) / e2e_steps, world, device)
     barrier()
     return {"value": round(e2e_ms, 3), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": e2e_steps}
+            "steps": e2e_steps, "pinned_copy_gbs": {"h2d": round(h2d_gbs, 1), "d2h": round(d2h_gbs, 1)}}
 
 
 def _run_gpt2s(L, device, args, stream, peaks):
     """The GPT-2-small-shaped set's step, device time only, with its per-kernel table."""
     import torch
     small = Workload(L, device, "gpt2s")
-    L.muon_autotune(small.bucket_array, small.ws)
+    L.muon_autotune(small.bucket_array, small.hp, small.ws)
     for _ in range(max(3, args.warmup)):
         small.step()
     torch.cuda.synchronize()
@@ -473,9 +485,10 @@ def run_ours(args):
     wl = Workload(L, device, HEADLINE)
     stream = torch.cuda.current_stream(device)
     # initialisation, outside every timed region: the poly step's pipeline shape measured on these buckets
-    L.muon_autotune(wl.bucket_array, wl.ws)
+    L.muon_autotune(wl.bucket_array, wl.hp, wl.ws)
     ms_ = sorted({min(bk["A"], bk["B"]) for bk in wl.buckets})
     poly_shape = {m: {0: "4+5", 1: "5+3", 2: "6+2"}.get(L.muon_autotune_poly_shape(m), "rule") for m in ms_}
+    sched = {0: "launch order", 1: "per-matrix counters"}.get(L.muon_autotune_scheduling(wl.bucket_array), "rule")
 
     def barrier():
         if world > 1:
@@ -554,7 +567,8 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": dict({"workload": WORKLOAD, "parallelism": "replicas" if world > 1 else "single",
                             "l2": "inputs larger than L2: >100 GB touched per step, no separate flush",
-                            "poly_pipeline": {str(m): f"{v} stages+slots" for m, v in poly_shape.items()}},
+                            "poly_pipeline": {str(m): f"{v} stages+slots" for m, v in poly_shape.items()},
+                            "chain_scheduling": f"{sched} (measured at init)"},
                            **head_cfg),
             "ms_at_sm_max_clock": round(ms * sm / smax, 4) if sm and smax else None,
             "muon_ms": round(sum(tot.get(k, 0.0) for k in tot if k != "adamw"), 4),
@@ -719,8 +733,8 @@ def run_config_sweep(args):
                 raise RuntimeError(f"device wait ran out in the {name} configuration")
             t_adamw = max(t_adamw, 1e-9)
             print(json.dumps({"config": name, "counter_deps": deps, "muon_matrices": sum(plan["bucket_K"]),
-                              "gram_space": {f"{A}x{B}": L.muon_gram_space_route(A, B)
-                                             for (A, B) in plan["bucket_shapes"]},
+                              "gram_space": {f"{A}x{B}": L.muon_gram_space_route(A, B, K)
+                                             for (A, B), K in zip(plan["bucket_shapes"], plan["bucket_K"])},
                               "buckets": len(plan["bucket_K"]), "muon_ms": round(t_muon, 4),
                               "ns_tflops_nominal": round(nominal / (t_muon * 1e-3) / 1e12, 1),
                               "ns_frac_nominal": round(nominal / (t_muon * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),

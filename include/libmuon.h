@@ -136,24 +136,39 @@ size_t muon_workspace_bytes_grouped(const muon_bucket *buckets, int n);
 muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hparams *hp, void *ws, size_t ws_bytes,
                               muon_stream_t stream);
 
-/* Measured per-shape choice of a kernel configuration ([P4] section 2.4, shape-adaptive kernel
- * autotuning: a search over pipeline configurations for the shapes at hand, measured once and cached for
- * later steps). The poly step (H = a*I + b*G + c*G^2) is compiled in three pipeline shapes (mainloop
- * stages + epilogue input slots: 4 + 5, 5 + 3, 6 + 2). For the buckets' grouped poly launch, the call
- * times each shape (one warm-up and five timed launches, median) and records the fastest in a
- * process-wide table keyed by the launch's deepest contraction; later launches with that contraction use
- * it. Without an entry, contractions up to 2048 take 4 + 5 and deeper ones 6 + 2. Every shape computes
- * each tile the same way, so the choice changes only the time, never a result.
- *   buckets, n, ws, ws_bytes  as for muon_step_grouped. The poly launches read and overwrite the G and
- *            H sections of ws (any content; parameters, gradients and momentum are not touched).
- * Synchronous: returns after the timed launches complete. Errors as for muon_step_grouped's checks. */
-muon_status muon_autotune(const muon_bucket *buckets, int n, void *ws, size_t ws_bytes, muon_stream_t stream);
+/* Measured per-shape choices ([P4] section 2.4, shape-adaptive kernel autotuning: configurations searched
+ * for the shapes at hand, measured once and cached for later steps). For the buckets of a grouped step with
+ * these hyperparameters (the step count and coefficients set the chain's length), the call measures, on the
+ * workspace alone, and records in process-wide tables:
+ *   1. the Newton-Schulz path of every bucket that can take the Gram-space chain (muon_gram_space_route):
+ *      that bucket's chain timed each way, keyed by (min(A,B), max(A,B), K);
+ *   2. the poly step's pipeline shape (mainloop stages + epilogue input slots: 4 + 5, 5 + 3, 6 + 2) for the
+ *      plain buckets' grouped poly launch, keyed by its deepest contraction (without an entry, contractions
+ *      up to 2048 take 4 + 5 and deeper ones 6 + 2);
+ *   3. the plain chain's scheduling (per-matrix readiness counters or launch order), the whole set timed
+ *      each way, keyed by the plain buckets' shapes and counts.
+ * Each candidate runs once as a warm-up and five times timed (median). Later calls use the recorded choices
+ * unless a debug switch forces one. The shapes and the scheduling never change a result; the path changes
+ * the arithmetic (both paths are checked against the oracle by the tests).
+ *   buckets, n, hp, ws, ws_bytes  as for muon_step_grouped. The timed chains start from whatever the
+ *            workspace's iterate holds and write only workspace sections: parameters, gradients and momentum
+ *            are neither read nor written.
+ * Synchronous: returns after the timed launches complete. Errors as for muon_step_grouped's checks;
+ * MUON_ERR_TIMEOUT if a bounded wait ran out during the measurements. */
+muon_status muon_autotune(const muon_bucket *buckets, int n, const muon_hparams *hp, void *ws, size_t ws_bytes,
+                          muon_stream_t stream);
+
+/* The recorded path of K matrices of A x B: 1 Gram space, 0 plain chain, -1 none recorded. */
+int32_t muon_autotune_route(int64_t K, int64_t A, int64_t B);
+
+/* The recorded scheduling of these buckets' plain chain: 1 per-matrix counters, 0 launch order, -1 none. */
+int32_t muon_autotune_scheduling(const muon_bucket *buckets, int n);
 
 /* The recorded poly shape (0: 4 + 5, 1: 5 + 3, 2: 6 + 2) for launches whose deepest contraction is
  * `contraction` (the matrices' smaller dimension), or -1 if none is recorded. */
 int32_t muon_autotune_poly_shape(int64_t contraction);
 
-/* Empties the autotune table. */
+/* Empties the autotune tables. */
 void muon_autotune_reset(void);
 
 /* Newton-Schulz orthogonalisation of a stack, [P2] "Muon: orthogonalising the update" (newton_schulz):
@@ -311,13 +326,14 @@ muon_status muon_debug_poly_shape(int32_t shape);
  * Shapes that can take it: m <= 256 and not the fused small-matrix kernel's (m <= 128 with n <= 256); their
  * workspace (muon_workspace_bytes) includes 40*K*m*round8(m) bytes of fp32 scratch for it.
  * muon_step_batched, muon_step_grouped, hybrid_step and ns_orthogonalize take it where
- * muon_gram_space_route says so: by default for those shapes with n >= 4*m.
+ * muon_gram_space_route says so: as measured by muon_autotune for that (m, n, K), else for n >= 4*m.
  * muon_debug_gram_space: -1 the default rule, 0 never, 1 for every shape that can take it (for tests and
  * measurements). MUON_ERR_INVALID_ARG for other values. */
 muon_status muon_debug_gram_space(int32_t mode);
 
-/* 1 if a (A, B) matrix takes the Gram-space path under the current mode, else 0 (also for A or B < 1). */
-int32_t muon_gram_space_route(int64_t A, int64_t B);
+/* 1 if a stack of K matrices of A x B takes the Gram-space path under the current mode and the autotune
+ * table, else 0 (also for K, A or B < 1). */
+int32_t muon_gram_space_route(int64_t K, int64_t A, int64_t B);
 
 /* Grouped chain scheduling (muon_step_grouped, hybrid_step). 1: each launch of the Newton-Schulz chain
  * waits per matrix on counters its predecessor raises, so that launches overlap. 0: each launch waits for

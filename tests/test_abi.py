@@ -268,16 +268,21 @@ def test_autotune_entry_point_checks_and_table():
     lib = L.lib()
     good = (L.muon_bucket * 1)(L.muon_bucket(FAKE, FAKE, FAKE, 4, 768, 2304, 1, 1))
     need = L.muon_workspace_bytes_grouped(good)
-    assert lib.muon_autotune(None, 1, FAKE, need, None) == L.MUON_ERR_INVALID_ARG
-    assert lib.muon_autotune(good, 0, FAKE, need, None) == L.MUON_ERR_INVALID_ARG
-    assert lib.muon_autotune(good, 1, None, need, None) == L.MUON_ERR_INVALID_ARG
-    assert lib.muon_autotune(good, 1, FAKE + 8, need, None) == L.MUON_ERR_ALIGNMENT
-    assert lib.muon_autotune(good, 1, FAKE, need - 1, None) == L.MUON_ERR_WORKSPACE
+    hp = ctypes.byref(L.make_muon_hparams(0.02, 0.95, 0.01))
+    assert lib.muon_autotune(None, 1, hp, FAKE, need, None) == L.MUON_ERR_INVALID_ARG
+    assert lib.muon_autotune(good, 0, hp, FAKE, need, None) == L.MUON_ERR_INVALID_ARG
+    assert lib.muon_autotune(good, 1, None, FAKE, need, None) == L.MUON_ERR_INVALID_ARG
+    assert lib.muon_autotune(good, 1, hp, None, need, None) == L.MUON_ERR_INVALID_ARG
+    assert lib.muon_autotune(good, 1, hp, FAKE + 8, need, None) == L.MUON_ERR_ALIGNMENT
+    assert lib.muon_autotune(good, 1, hp, FAKE, need - 1, None) == L.MUON_ERR_WORKSPACE
     bad = (L.muon_bucket * 1)(L.muon_bucket(FAKE, FAKE, FAKE, 4, 768, 0, 1, 1))
-    assert lib.muon_autotune(bad, 1, FAKE, need, None) == L.MUON_ERR_INVALID_ARG
+    assert lib.muon_autotune(bad, 1, hp, FAKE, need, None) == L.MUON_ERR_INVALID_ARG
     L.muon_autotune_reset()
     assert L.muon_autotune_poly_shape(768) == -1
     assert L.muon_autotune_poly_shape(0) == -1
+    assert L.muon_autotune_route(16, 256, 16384) == -1 and L.muon_autotune_route(0, 256, 16384) == -1
+    assert L.muon_autotune_scheduling(good) == -1
+    assert lib.muon_autotune_scheduling(None, 1) == -1
     assert lib.muon_debug_poly_shape(3) == L.MUON_ERR_INVALID_ARG
     assert lib.muon_debug_poly_shape(-2) == L.MUON_ERR_INVALID_ARG
     assert lib.muon_debug_poly_shape(1) == L.MUON_OK

@@ -1,10 +1,13 @@
-"""The per-shape autotune of the poly step's pipeline shape, through the C ABI.
+"""The per-shape autotune, through the C ABI: the poly step's pipeline shape, the plain chain's scheduling,
+and the Newton-Schulz path of stacks that can take the Gram-space chain.
 
-The three compiled shapes (4 + 5, 5 + 3, 6 + 2 mainloop stages + epilogue slots) compute every tile the
+The three compiled poly shapes (4 + 5, 5 + 3, 6 + 2 mainloop stages + epilogue slots) compute every tile the
 same way, so each must give the same bits as the others on the same input (the shape the rule picks is
 compared with the oracle in test_gpu_ns_steps); covered at a short, a long and a ragged contraction.
-muon_autotune must record a shape for the grouped launch's contraction, and a grouped step after it must
-equal, bit for bit, the same step with the table empty.
+muon_autotune must record a shape for the grouped launch's contraction and a scheduling for the set, leave
+parameters and momentum untouched, and a grouped step after it must equal, bit for bit, the same step with the
+tables empty (shapes and scheduling never change a result). On the aspect set it must record a path for both
+buckets, and the step after it must match the oracle.
 """
 import pytest
 import torch
@@ -66,10 +69,12 @@ def test_autotune_records_a_shape_and_keeps_results(L):
     ws_ref = torch.zeros(L.muon_workspace_bytes_grouped(ref_b), dtype=torch.uint8, device=DEV)
     ws_got = torch.zeros_like(ws_ref)
     L.muon_step_grouped(ref_b, hp, ws_ref)          # table empty: the rule's shape
-    L.muon_autotune(got_b, ws_got)
+    L.muon_autotune(got_b, hp, ws_got)
     shape = L.muon_autotune_poly_shape(768)
     assert shape in (0, 1, 2)
     assert L.muon_autotune_poly_shape(1024) == -1
+    assert L.muon_autotune_scheduling(got_b) in (0, 1)
+    print(f"GPT-2-small set: poly shape {shape}, scheduling {L.muon_autotune_scheduling(got_b)} (1 = counters)")
     # the autotune touched only the workspace: parameters and momentum are as they were
     for (p, _, mom), (p0, _, mom0) in zip(got, ref):
         assert torch.count_nonzero(mom) == 0
@@ -80,6 +85,48 @@ def test_autotune_records_a_shape_and_keeps_results(L):
         assert torch.equal(p, p0) and torch.equal(mom, mom0)
     L.muon_autotune_reset()
     assert L.muon_autotune_poly_shape(768) == -1
+    assert L.muon_autotune_scheduling(got_b) == -1
+
+
+def test_autotune_chooses_a_path_on_the_aspect_set(L):
+    """Both aspect-set buckets can take the Gram-space chain; the autotune times each way and records a path
+    (the Gram space, measured about twice as fast on these shapes). The step after it matches the oracle."""
+    import numpy as np
+    from oracle import muon as omuon
+    from tests.gpu_common import f64
+    L.muon_autotune_reset()
+    w = workloads.workload("aspect")
+    hp = w.muon_hp
+    shapes = [(16, 256, 16384), (16, 16384, 256)]
+    specs, keep = [], []
+    for b, (K, A, B) in enumerate(shapes):
+        p = workloads.device_stack((K, A, B), "normal", w.param_std, 8300 + b, "bf16", DEV)
+        g = workloads.device_stack((K, A, B), "student_t3", 1.0, 8400 + b, "bf16", DEV)
+        m = torch.zeros((K, A, B), dtype=torch.float32, device=DEV)
+        keep.append((p, g, m, p[0].clone()))
+        specs.append((L.pointer_array([p[k] for k in range(K)], DEV), L.pointer_array([g[k] for k in range(K)], DEV),
+                      m, K, A, B, L.MUON_BF16, L.MUON_BF16))
+    bk = L.make_buckets(specs)
+    ws = torch.zeros(L.muon_workspace_bytes_grouped(bk), dtype=torch.uint8, device=DEV)
+    hps = hp_struct(L, hp)
+    L.muon_autotune(bk, hps, ws)
+    routes = [L.muon_autotune_route(K, A, B) for K, A, B in shapes]
+    print(f"aspect set: recorded paths {routes} (1 = Gram space)")
+    assert routes == [1, 1]
+    assert all(torch.count_nonzero(m) == 0 for _, _, m, _ in keep)
+    L.muon_step_grouped(bk, hps, ws)
+    assert L.muon_check(ws) == L.MUON_OK
+    for (K, A, B), (p, g, m, p0) in zip(shapes, keep):
+        P0, G0 = f64(p0), f64(g[0])
+        ref, _, u = omuon.muon_update(P0, G0, np.zeros_like(P0), lr=hp.lr, momentum=hp.momentum,
+                                      weight_decay=hp.weight_decay, nesterov=hp.nesterov, cautious_wd=False,
+                                      coeffs=hp.coeffs, eps=hp.eps, param_dtype="bf16")
+        # cautious decay changes only the decay term (lr * wd * p): compare the step with it allowed for
+        step_gpu, step_orc = P0 - f64(p[0]), hp.lr * omuon.update_scale(A, B) * u
+        err = np.linalg.norm(np.maximum(np.abs(step_gpu - step_orc) - hp.lr * hp.weight_decay * np.abs(P0), 0.0))
+        assert err <= 2e-2 * np.linalg.norm(step_orc) + 2 ** -8 * np.linalg.norm(f64(p[0]))
+    L.muon_autotune_reset()
+    assert L.muon_autotune_route(16, 256, 16384) == -1
 
 
 def test_optimizer_autotune_option(L):
