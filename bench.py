@@ -485,7 +485,8 @@ def run_ours(args):
     wl = Workload(L, device, HEADLINE)
     stream = torch.cuda.current_stream(device)
     # initialisation, outside every timed region: the poly step's pipeline shape measured on these buckets
-    L.muon_autotune(wl.bucket_array, wl.hp, wl.ws)
+    if not args.no_autotune:
+        L.muon_autotune(wl.bucket_array, wl.hp, wl.ws)
     ms_ = sorted({min(bk["A"], bk["B"]) for bk in wl.buckets})
     poly_shape = {m: {0: "4+5", 1: "5+3", 2: "6+2"}.get(L.muon_autotune_poly_shape(m), "rule") for m in ms_}
     sched = {0: "launch order", 1: "per-matrix counters"}.get(L.muon_autotune_scheduling(wl.bucket_array), "rule")
@@ -861,6 +862,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (host buffers)")
     ap.add_argument("--no-gpt2s", action="store_true", help="skip the GPT-2-small figures")
+    ap.add_argument("--no-autotune", action="store_true",
+                    help="skip the measured choices at initialisation (the rules decide; for launch-list captures)")
     ap.add_argument("--profile-small", default="",
                     help="one grouped Muon step (no warm-up, no autotune) of a small case of the named set, "
                          "for ncu captures: 'llama8b' (K=2 per bucket) or 'aspect' (K=8 per bucket)")
