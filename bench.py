@@ -389,6 +389,16 @@ def _run_e2e(wl, args, stream, world, device, barrier):
     dev_g, dev_p = wl.host_views()
     h2d = sum(t.numel() * t.element_size() for t in dev_g)
     d2h = sum(t.numel() * t.element_size() for t in dev_p)
+    # every local replica pins its own host buffers: stay within half of the host's memory
+    local_world = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+    try:
+        host_bytes = os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")
+    except (ValueError, OSError, AttributeError):
+        host_bytes = 0
+    if host_bytes and (h2d + d2h) * local_world > host_bytes // 2:
+        return {"value": None, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "skipped": f"{local_world} replicas would pin {(h2d + d2h) * local_world / 1e9:.0f} GB of "
+                           f"{host_bytes / 1e9:.0f} GB host memory"}
     host_g = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_g]
     host_p = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_p]
     for hg, dg in zip(host_g, dev_g):
