@@ -6,6 +6,8 @@
 #include <stdint.h>
 
 #include <cmath>
+#include <utility>
+#include <vector>
 
 #include "../../include/libmuon.h"
 
@@ -27,7 +29,8 @@ enum KernelKind : int32_t {
   KK_NS_SMALL = 8,
   KK_GRAM_SPACE = 9,
   KK_GRAM32 = 10,
-  KK_COUNT = 11
+  KK_GRAM32_REDUCE = 11,
+  KK_COUNT = 12
 };
 
 // Launch bookkeeping (libmuon.cu): counts launches and, while tracing, records an event pair.
@@ -77,6 +80,10 @@ struct GemmProblem {
   // out32 + bprime32 and that + plane32
   float *out32;
   long long plane32, bprime32;
+  // EPI_GRAM32 split along the contraction: ksplit (>= 1) slices of kper 64-deep steps, each slice a tile pair of
+  // its own; slice j stores its raw fp32 sum in plane 2 + j (out32 + (2 + j) * plane32), and a reduce kernel
+  // adds the slices in index order and forms the outputs above
+  int ksplit, kper;
   // final step: parameter update (params != null) or dense store (out_dense != null); with master, the
   // update applies to the fp32 master copies and params receive them rounded to bf16
   void *const *params;
@@ -123,6 +130,19 @@ void poly_shape_record(int k_iters, int shape);
 void poly_shape_clear();
 int poly_shape_forced();
 
+// The fp32 Gram of the Gram-space path (EPI_GRAM32) has one tile pair per matrix, which leaves most SMs idle when
+// a launch holds fewer matrices than there are SM pairs. Its contraction (the iterate's long side) is then split
+// into up to GRAM32_MAX_SPLIT slices, each computed by a tile pair of its own. Without a measured choice the
+// launch takes the most slices that still fit one wave and keep each slice at least GRAM32_MIN_SLICE_K 64-deep
+// steps; the autotune table holds measured counts keyed by the launch's matrices and deepest contraction; a
+// forced count (-1: none) serves tests and sweeps. The count changes only the order of the fp32 additions.
+constexpr int GRAM32_MAX_SPLIT = 8;
+constexpr int GRAM32_MIN_SLICE_K = 16;
+int gram_split_lookup(long long matrices, int k_iters);
+void gram_split_record(long long matrices, int k_iters, int split);
+void gram_split_clear();
+int gram_split_forced();
+
 // Per-matrix dependencies between the grouped launches of one Newton-Schulz chain, instead of the launch
 // order: a tile of matrix b loads its operands only once wait[b] >= target (every tile of b that the
 // previous step kind produced has been stored), and each epilogue warp adds 1 to sig[b] (release) when
@@ -150,9 +170,16 @@ class GemmBatch {
                        const TileSync *sync = nullptr);
   muon_status add_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, const float *scale,
                        const TileSync *sync = nullptr);
-  // EPI_GRAM32 (x.rows <= 256): g = alpha * s^2 * x x^T as fp32 hi / lo planes, and c g + b I at g_hi + bprime
+  // EPI_GRAM32 (x.rows <= 256): g = alpha * s^2 * x x^T as fp32 hi / lo planes, and c g + b I at g_hi + bprime;
+  // planes 2 .. bprime / plane - 1 are scratch for the slices of a split contraction
   muon_status add_gram32(const Bf16Stack &x, float *g_hi, long long ldg, long long mstride_g, long long plane,
                          long long bprime, float b, float c, float alpha, const float *scale);
+  // EPI_GRAM32 only: split every contraction into this many slices (clipped to what each problem allows), whatever
+  // the table or the rule says (0: no override)
+  void force_split(int split) { split_ = split; }
+  // EPI_GRAM32: the autotune table's keys (matrices, deepest contraction in 64-deep steps) of the launches that
+  // launch() would issue, in order
+  std::vector<std::pair<long long, int>> split_keys();
   muon_status add_final(const Bf16Stack &h, const Bf16Stack &x, const float *scale, const FinalSpec &f,
                        const TileSync *sync = nullptr, int k_wrap = 0);
   muon_status launch(cudaStream_t s);
@@ -169,8 +196,11 @@ class GemmBatch {
   Item *items_ = nullptr;
   int n_ = 0, cap_ = 0;
   int force_ = -1;
+  int split_ = 0;
   bool grid_wait_ = false;
   muon_status push(const Item &it);
+  void order();                        // launch order of the items (stable for a given set)
+  int group_size(int first) const;     // items from first that share one launch
 };
 
 // Single-stack conveniences (a batch of one).

@@ -139,6 +139,29 @@ int poly_shape_forced() {
   return g_poly_forced;
 }
 
+namespace {
+std::map<std::pair<long long, int>, int> g_gram_split;   // (matrices, deepest contraction) -> measured slices
+int g_gram_split_forced = -1;
+}  // namespace
+
+int gram_split_lookup(long long matrices, int k_iters) {
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  auto it = g_gram_split.find({matrices, k_iters});
+  return it == g_gram_split.end() ? -1 : it->second;
+}
+void gram_split_record(long long matrices, int k_iters, int split) {
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  g_gram_split[{matrices, k_iters}] = split;
+}
+void gram_split_clear() {
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  g_gram_split.clear();
+}
+int gram_split_forced() {
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  return g_gram_split_forced;
+}
+
 unsigned long long wait_timeout_ns() { return g_timeout_ns; }
 
 namespace {
@@ -820,6 +843,47 @@ muon_status muon_autotune(const muon_bucket *buckets, int n, const muon_hparams 
     g_route_table[{c.L.m, c.L.n, c.K}] = best_path == PATH_GRAM ? 1 : 0;
   }
   for (ChainStack &c : cs) dense_out(c);
+  // 1b. the slices of the Gram-space stacks' fp32 Gram launch (reads the iterate, writes the Gram-space planes)
+  bool any_gram = false;
+  for (const ChainStack &c : cs) any_gram = any_gram || c.path == PATH_GRAM;
+  if (any_gram && gram_split_forced() < 0) {
+    auto gram32_batch = [&](GemmBatch &g32) -> muon_status {
+      for (const ChainStack &c : cs) {
+        if (c.path != PATH_GRAM) continue;
+        float *planes = reinterpret_cast<float *>(c.w + c.L.gs);
+        const long long ldm = round8(c.L.m), msm = c.L.m * ldm;
+        Bf16Stack X{c.w + c.L.x0, c.L.m, c.L.n, c.L.ldx, c.L.m * c.L.ldx, c.K};
+        muon_status r = g32.add_gram32(X, planes, ldm, msm, c.K * msm, 2LL * GS_B * c.K * msm, hp->coeffs[1],
+                                       hp->coeffs[2], 1.0f, nullptr);
+        if (r != MUON_OK) return r;
+      }
+      return MUON_OK;
+    };
+    std::vector<std::pair<long long, int>> keys;
+    {
+      GemmBatch g32(EPI_GRAM32, err, g_timeout_ns);
+      if ((st = gram32_batch(g32)) != MUON_OK) return st;
+      keys = g32.split_keys();
+    }
+    int best = 1;
+    float best_ms = -1.f;
+    for (int split : {1, 2, 3, 4, 6, 8}) {
+      const float ms = median_time(
+          [&]() -> muon_status {
+            GemmBatch g32(EPI_GRAM32, err, g_timeout_ns);
+            g32.force_split(split);
+            muon_status r = gram32_batch(g32);
+            return r != MUON_OK ? r : g32.launch(s);
+          },
+          s, &st);
+      if (st != MUON_OK) return st;
+      if (best_ms < 0.f || ms < best_ms) {
+        best = split;
+        best_ms = ms;
+      }
+    }
+    for (const auto &k : keys) gram_split_record(k.first, k.second, best);
+  }
   // 2. the poly step's pipeline shape, on the plain stacks' grouped poly launch (reads G, writes H)
   int max_k = 0;
   bool any_plain = false;
@@ -893,8 +957,14 @@ int32_t muon_autotune_poly_shape(int64_t contraction) {
   return poly_shape_lookup(static_cast<int>((contraction + 63) / 64));
 }
 
+int32_t muon_autotune_gram_split(int64_t matrices, int64_t contraction) {
+  if (matrices < 1 || contraction < 1 || contraction > (1 << 26)) return -1;
+  return gram_split_lookup(matrices, static_cast<int>((contraction + 63) / 64));
+}
+
 void muon_autotune_reset(void) {
   poly_shape_clear();
+  gram_split_clear();
   {
     std::lock_guard<std::mutex> lk(g_route_mu);
     g_route_table.clear();
@@ -918,6 +988,13 @@ muon_status muon_debug_gram_space(int32_t mode) {
 int32_t muon_gram_space_route(int64_t K, int64_t A, int64_t B) {
   if (K < 1 || A < 1 || B < 1) return 0;
   return gram_space_route(std::min(A, B), std::max(A, B), K) ? 1 : 0;
+}
+
+muon_status muon_debug_gram_split(int32_t split) {
+  if (split < -1 || split == 0 || split > GRAM32_MAX_SPLIT) return MUON_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  g_gram_split_forced = split;
+  return MUON_OK;
 }
 
 muon_status muon_debug_poly_shape(int32_t shape) {
@@ -1218,6 +1295,7 @@ const char *muon_kernel_name(int32_t kind) {
     case KK_NS_SMALL: return "ns_small";
     case KK_GRAM_SPACE: return "ns_gram_space";
     case KK_GRAM32: return "ns_gram_f32";
+    case KK_GRAM32_REDUCE: return "ns_gram_f32_reduce";
     default: return "unknown";
   }
 }

@@ -30,6 +30,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -43,10 +44,13 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int MAX_STAGES = 6;
+constexpr int MAX_STAGES = 12;
 constexpr int A_BYTES = BM * BK * 2;                  // this CTA's 128 rows of A
 constexpr int B_HALF_BYTES = (BN / 2) * BK * 2;       // this CTA's half (128 of 256 columns) of B
 constexpr int STAGE_BYTES = A_BYTES + B_HALF_BYTES;
+// A mainloop stage holds this CTA's A tile and its half of B, except in the fp32 Gram (EPI_GRAM32), whose B is
+// its A: there a stage is the A tile alone, and twice as many stages fit.
+__host__ __device__ constexpr int stage_bytes(int epi) { return epi == EPI_GRAM32 ? A_BYTES : STAGE_BYTES; }
 constexpr int ACC_COLS = BN;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int EPI_WARPS = 8;                                // two per TMEM lane quarter
@@ -84,12 +88,12 @@ struct Ctrl {
 // Pipeline shapes: a long contraction wants mainloop stages, a short one leaves the epilogue as the limit
 // and wants ring slots (the epilogue's second input must arrive within one tile's MMA time).
 __host__ __device__ constexpr size_t smem_bytes(int epi, int stages, int slots) {
-  return static_cast<size_t>(stages) * STAGE_BYTES + static_cast<size_t>(slots) * ring_slot_bytes(epi) +
+  return static_cast<size_t>(stages) * stage_bytes(epi) + static_cast<size_t>(slots) * ring_slot_bytes(epi) +
          sizeof(Ctrl) + 1024;
 }
 constexpr int SHORT_K_ITERS = 32;   // without a measured choice, contractions up to 2048 take the deep-ring shape
 static_assert(smem_bytes(EPI_GRAM, 6, 1) <= 232448 && smem_bytes(EPI_POLY, 6, 2) <= 232448 &&
-                  smem_bytes(EPI_GRAM32, 6, 2) <= 232448 &&
+                  smem_bytes(EPI_GRAM32, 12, 2) <= 232448 &&
                   smem_bytes(EPI_POLY, 5, 3) <= 232448 && smem_bytes(EPI_POLY, 4, 5) <= 232448,
               "shared memory over budget");
 
@@ -133,6 +137,7 @@ __device__ __forceinline__ void decode_tile(const GemmProblem &a, int symmetric,
   b = static_cast<int>(t / a.tiles_per_matrix);
   int r = static_cast<int>(t - static_cast<long long>(b) * a.tiles_per_matrix);
   if (!symmetric) {
+    if (a.ksplit > 1) r %= a.tiles_per_matrix / a.ksplit;   // the slice index is tile_k_range's
     tj = r / a.m_pairs;
     ti = 2 * (r - tj * a.m_pairs) + static_cast<int>(rank);
     return;
@@ -150,6 +155,22 @@ __device__ __forceinline__ void decode_tile(const GemmProblem &a, int symmetric,
     r -= cnt;
     ++j;
   }
+}
+
+// The contraction slice of local tile pair t and its 64-deep steps k0 .. k1 - 1: the whole contraction unless the
+// problem is split, where a matrix's pairs run slice ksplit - 1 first and slice 0 last.
+__device__ __forceinline__ int tile_k_range(const GemmProblem &a, long long t, int &k0, int &k1) {
+  if (a.ksplit <= 1) {
+    k0 = 0;
+    k1 = a.k_iters;
+    return 0;
+  }
+  const int per_slice = a.tiles_per_matrix / a.ksplit;
+  const int r = static_cast<int>(t % a.tiles_per_matrix);
+  const int slice = a.ksplit - 1 - r / per_slice;
+  k0 = slice * a.kper;
+  k1 = min(a.k_iters, k0 + a.kper);
+  return slice;
 }
 
 // A ring slot pair of chunks is used unless the whole tile lies below the diagonal for those 64 columns.
@@ -380,10 +401,24 @@ __device__ __forceinline__ void final_store_f32(const GemmProblem &a, void *base
 // holds the chunk's second input on entry (POLY, APPLY, FINAL) and is free for reuse on exit.
 template <int EPI>
 __device__ __forceinline__ void epilogue_chunk(const GemmProblem &a, int b, int warp_row0, int lane, int col0,
-                                               const Region &rg, float *v) {
+                                               const Region &rg, float *v, int slice = 0) {
   const int row = warp_row0 + lane;
   const int rows = a.rows, cols = a.cols;
   if constexpr (EPI == EPI_GRAM32) {
+    if (a.ksplit > 1) {
+      // one slice of a split contraction: the raw sum, row by row (each lane 128 bytes of its row), into the
+      // slice's plane; the reduce kernel scales and splits the total. Whole 16-byte pieces: a piece that starts
+      // inside the row ends inside its padding (the pitch is a multiple of 8), where the sum is zero (the
+      // operand's rows past m load as zeros) and nothing reads
+      if (row >= rows) return;
+      float *d = a.out32 + (2 + slice) * a.plane32 + static_cast<long long>(b) * a.mstride_out +
+                 static_cast<long long>(row) * a.ld_out + col0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (col0 + 4 * q < cols)
+          *reinterpret_cast<float4 *>(d + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      return;
+    }
     // the whole m x m tile is computed (m <= 256: one tile pair per matrix); each lane stores its row's 32
     // values as a tf32 hi plane (low 13 mantissa bits cleared) and an fp32 lo plane (the rest, exact)
     float sc = a.alpha;
@@ -600,9 +635,13 @@ template <int EPI, bool B_MN, int STAGES, int RING_SLOTS>
 __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_constant__ GemmGroup args) {
   static_assert(STAGES <= MAX_STAGES && RING_SLOTS <= MAX_RING_SLOTS, "pipeline shape");
   constexpr int SLOT_BYTES = ring_slot_bytes(EPI);
+  // The fp32 Gram's one tile pair per matrix (m <= 256) lies on the diagonal: each CTA's half of B is the same
+  // 128 rows of the same tensor as its A tile, so only A is loaded and the MMA reads B from it.
+  constexpr bool SHARED_B = EPI == EPI_GRAM32;
+  constexpr int SB = stage_bytes(EPI);
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *ring = smem + STAGES * STAGE_BYTES;
+  uint8_t *ring = smem + STAGES * SB;
   Ctrl *ctrl = reinterpret_cast<Ctrl *>(ring + RING_SLOTS * SLOT_BYTES);
 
   const int warp = threadIdx.x / 32;
@@ -685,33 +724,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
           ready_pi = pi;
           ready_b = b;
         }
-        const int k_iters = P.k_iters;
-        for (int kk = 0; kk < k_iters; ++kk) {
+        int k0, k1;
+        tile_k_range(P, t - P.tile_begin, k0, k1);
+        for (int kk = k0; kk < k1; ++kk) {
           if (!wait_bounded(&ctrl->empty[stage], phase ^ 1u, ctl, ERR_WAIT_EMPTY)) {
             ok = false;
             break;
           }
           // both CTAs' copies complete on the even CTA's barrier, which the even CTA arms for both
           if (rank == 0) {
-            mbar_arrive_expect_tx(&ctrl->full[stage], 2 * STAGE_BYTES);
+            mbar_arrive_expect_tx(&ctrl->full[stage], 2 * SB);
             last_parity[stage] = static_cast<int>(phase);
           }
           const uint32_t fb = leader_full0 + stage * static_cast<uint32_t>(sizeof(uint64_t));
-          uint8_t *sa = smem + stage * STAGE_BYTES;
+          uint8_t *sa = smem + stage * SB;
           uint8_t *sb = sa + A_BYTES;
           tma_load_3d_pair(sa, map_a, fb, kk * BK, ti * BM, b);
-          // this CTA's half of B: columns tj*256 + 128*rank .. +127
-          if constexpr (!B_MN) {
-            // K-major: those rows of the same tensor through the A map (box 64 x 128)
-            tma_load_3d_pair(sb, map_a, fb, kk * BK, tj * BN + (BN / 2) * static_cast<int>(rank), b);
-          } else {
-            // N-major: column chunks 2*rank and 2*rank+1 (64 columns each); with k_wrap, the second half of the
-            // contraction reads B's rows again from the top
-            const int kb = (P.k_wrap > 0 && kk >= P.k_wrap) ? kk - P.k_wrap : kk;
+          if constexpr (!SHARED_B) {
+            // this CTA's half of B: columns tj*256 + 128*rank .. +127
+            if constexpr (!B_MN) {
+              // K-major: those rows of the same tensor through the A map (box 64 x 128)
+              tma_load_3d_pair(sb, map_a, fb, kk * BK, tj * BN + (BN / 2) * static_cast<int>(rank), b);
+            } else {
+              // N-major: column chunks 2*rank and 2*rank+1 (64 columns each); with k_wrap, the second half of the
+              // contraction reads B's rows again from the top
+              const int kb = (P.k_wrap > 0 && kk >= P.k_wrap) ? kk - P.k_wrap : kk;
 #pragma unroll
-            for (int q = 0; q < 2; ++q)
-              tma_load_3d_pair(sb + q * (64 * BK * 2), map_b, fb, tj * BN + 64 * (2 * static_cast<int>(rank) + q),
-                               kb * BK, b);
+              for (int q = 0; q < 2; ++q)
+                tma_load_3d_pair(sb + q * (64 * BK * 2), map_b, fb, tj * BN + 64 * (2 * static_cast<int>(rank) + q),
+                                 kb * BK, b);
+            }
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -738,22 +780,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         if (rec) rec[3] = globaltimer_ns();
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-        const int k_iters = args.prob[find_problem(args, t)].k_iters;
-        for (int kk = 0; kk < k_iters; ++kk) {
+        const GemmProblem &P = args.prob[find_problem(args, t)];
+        int k0, k1;
+        tile_k_range(P, t - P.tile_begin, k0, k1);
+        for (int kk = k0; kk < k1; ++kk) {
           if (!wait_bounded(&ctrl->full[stage], phase, ctl, ERR_WAIT_FULL)) {
             ok = false;
             break;
           }
-          if (rec && (kk == 0 || kk == k_iters - 1)) rec[kk == 0 ? 4 : 5] = globaltimer_ns();
+          if (rec && (kk == k0 || kk == k1 - 1)) rec[kk == k0 ? 4 : 5] = globaltimer_ns();
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t sb = sa + A_BYTES;
+          const uint32_t sa = smem_u32(smem + stage * SB);
+          const uint32_t sb = SHARED_B ? sa : sa + A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t adesc = smem_desc_sw128(sa + k * 32, 16, 1024);
             const uint64_t bdesc =
                 B_MN ? smem_desc_sw128(sb + k * 16 * 128, 64 * BK * 2, 1024) : smem_desc_sw128(sb + k * 32, 16, 1024);
-            tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kk | k) != 0 ? 1u : 0u);
+            tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, ((kk - k0) | k) != 0 ? 1u : 0u);
           }
           issued = true;
           tc_commit_pair_mc(&ctrl->empty[stage], 0x3);   // frees the stage in both CTAs of the pair
@@ -911,6 +955,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       tc_fence_after();
       const int row0 = ti * BM;
       const int warp_row0 = row0 + lane_base;
+      int k0, k1;
+      const int slice = EPI == EPI_GRAM32 ? tile_k_range(P, t - P.tile_begin, k0, k1) : 0;
       bool aborted = false;
       // final step with bf16 parameters: their blocks are fetched one chunk ahead
       const bool prefetch_params =
@@ -948,7 +994,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
               final_chunk_bf16(P, b, warp_row0, lane, col0, rg, v, pf, next);
               pf_ready = next;
             } else {
-              epilogue_chunk<EPI>(P, b, warp_row0, lane, col0, rg, v);
+              epilogue_chunk<EPI>(P, b, warp_row0, lane, col0, rg, v, slice);
             }
             __syncwarp();   // every lane's region reads are done before the region is written again
           }
@@ -1063,6 +1109,138 @@ muon_status launch_shape(const GemmGroup &g, int32_t kind, cudaStream_t s) {
   return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
 }
 
+// ------------------------------------------------------------------------------------------ split fp32 Gram
+
+// One problem of a split EPI_GRAM32 launch, for the reduce kernel: ksplit raw slice sums in planes 2 .. 2 +
+// ksplit - 1 of out32 (rows x rows, row pitch ld, matrix pitch mstride, plane pitch plane32).
+struct Gram32Reduce {
+  float *out32;
+  const float *scale;
+  long long plane32, bprime32, ld, mstride, block_begin;
+  int rows, ksplit, row_blocks;
+  float alpha, coef_b, coef_c;
+};
+struct Gram32ReduceGroup {
+  Gram32Reduce prob[GEMM_MAX_PROBLEMS];
+  int nprob;
+};
+static_assert(sizeof(Gram32ReduceGroup) <= 4096, "kernel parameter block too large");
+
+// The outputs of the fp32 Gram from its slices: A = alpha * s^2 * (slice 0 + slice 1 + ...), added in slice
+// order, as a tf32 hi plane (low 13 mantissa bits cleared) and an fp32 lo plane (the rest), and c A + b I the
+// same way: what the unsplit epilogue stores. Blocks of 256 threads: 8 rows of one matrix, 32 lanes per row,
+// lane l the 4 columns at 4 l and 4 l + 128 (rows <= 256).
+__global__ void __launch_bounds__(256) gram32_reduce_kernel(const __grid_constant__ Gram32ReduceGroup G) {
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  int pi = 0;
+  while (pi + 1 < G.nprob && static_cast<long long>(blockIdx.x) >= G.prob[pi + 1].block_begin) ++pi;
+  const Gram32Reduce &a = G.prob[pi];
+  const long long local = static_cast<long long>(blockIdx.x) - a.block_begin;
+  const long long b = local / a.row_blocks;
+  const int row = static_cast<int>(local - b * a.row_blocks) * 8 + static_cast<int>(threadIdx.x >> 5);
+  if (row >= a.rows) return;
+  float sc = a.alpha;
+  if (a.scale != nullptr) {
+    const float sv = a.scale[b];
+    sc *= sv * sv;
+  }
+  const long long base = b * a.mstride + static_cast<long long>(row) * a.ld;
+#pragma unroll 1
+  for (int h = 0; h < 2; ++h) {
+    const int c = 4 * static_cast<int>(threadIdx.x & 31) + 128 * h;
+    if (c >= a.rows) break;
+    const bool full = c + 4 <= a.rows;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+    for (int j = 0; j < a.ksplit; ++j) {
+      const float *src = a.out32 + (2 + j) * a.plane32 + base + c;
+      if (full) {
+        const float4 q = __ldcg(reinterpret_cast<const float4 *>(src));
+        v[0] += q.x;
+        v[1] += q.y;
+        v[2] += q.z;
+        v[3] += q.w;
+      } else {
+        for (int e = 0; e < 4; ++e)
+          if (c + e < a.rows) v[e] += __ldcg(src + e);
+      }
+    }
+    float o[4][4];   // G hi, G lo, B' hi, B' lo
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x = v[e] * sc;
+      const float xb = fmaf(a.coef_c, x, c + e == row ? a.coef_b : 0.f);
+      const float xh = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+      const float bh = __uint_as_float(__float_as_uint(xb) & 0xFFFFE000u);
+      o[0][e] = xh;
+      o[1][e] = x - xh;
+      o[2][e] = bh;
+      o[3][e] = xb - bh;
+    }
+    const long long off[4] = {0, a.plane32, a.bprime32, a.bprime32 + a.plane32};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      float *d = a.out32 + off[w] + base + c;
+      if (full) {
+        *reinterpret_cast<float4 *>(d) = make_float4(o[w][0], o[w][1], o[w][2], o[w][3]);
+      } else {
+        for (int e = 0; e < 4; ++e)
+          if (c + e < a.rows) d[e] = o[w][e];
+      }
+    }
+  }
+}
+
+muon_status launch_gram32_reduce(const Gram32ReduceGroup &g, long long blocks, cudaStream_t s) {
+  if (blocks <= 0) return MUON_OK;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  launch_begin(KK_GRAM32_REDUCE, s);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gram32_reduce_kernel, g);
+  launch_end(s);
+  return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+}
+
+// The slices of each EPI_GRAM32 problem of one launch (matrices in total, deepest contraction max_k): an
+// explicit count, else the measured one, else the most that fit one wave of SM pairs with slices at least
+// GRAM32_MIN_SLICE_K deep; clipped per problem to its scratch planes and its contraction, and evened out so
+// that no slice is empty. Sets ksplit, kper and the problem's tile pairs per matrix.
+void choose_gram_split(GemmProblem *probs, int cnt, int forced) {
+  long long matrices = 0;
+  int max_k = 0;
+  for (int i = 0; i < cnt; ++i) {
+    matrices += probs[i].batch;
+    max_k = probs[i].k_iters > max_k ? probs[i].k_iters : max_k;
+  }
+  int want = forced > 0 ? forced : gram_split_forced();
+  bool rule = false;
+  if (want <= 0) want = gram_split_lookup(matrices, max_k);
+  if (want <= 0) {
+    rule = true;
+    const long long pairs = device_sm_count() / 2;
+    want = matrices > 0 ? static_cast<int>(pairs / matrices) : 1;
+  }
+  for (int i = 0; i < cnt; ++i) {
+    GemmProblem &p = probs[i];
+    const long long planes = p.plane32 > 0 ? p.bprime32 / p.plane32 - 2 : 0;
+    long long sp = want;
+    if (rule) sp = std::min<long long>(sp, p.k_iters / GRAM32_MIN_SLICE_K);
+    sp = std::min<long long>({sp, GRAM32_MAX_SPLIT, planes, p.k_iters});
+    if (sp < 1) sp = 1;
+    p.kper = static_cast<int>((p.k_iters + sp - 1) / sp);
+    p.ksplit = (p.k_iters + p.kper - 1) / p.kper;
+    p.tiles_per_matrix = p.m_pairs * p.n_tiles * p.ksplit;
+  }
+}
+
 void fill_tiles(GemmProblem &a, long long batch, long long rows, long long cols, long long contraction,
                 bool symmetric) {
   a.batch = static_cast<int>(batch);
@@ -1079,6 +1257,8 @@ void fill_tiles(GemmProblem &a, long long batch, long long rows, long long cols,
     a.tiles_per_matrix = a.m_pairs * a.n_tiles;
   }
   a.k_iters = static_cast<int>((contraction + BK - 1) / BK);
+  a.ksplit = 1;
+  a.kper = a.k_iters;
 }
 
 bool apply_maps(const Bf16Stack &h, const Bf16Stack &x, CUtensorMap *ma, CUtensorMap *mb) {
@@ -1216,7 +1396,31 @@ muon_status GemmBatch::add_final(const Bf16Stack &h, const Bf16Stack &x, const f
   return push(it);
 }
 
-muon_status GemmBatch::launch(cudaStream_t s) {
+std::vector<std::pair<long long, int>> GemmBatch::split_keys() {
+  order();
+  std::vector<std::pair<long long, int>> keys;
+  for (int first = 0; first < n_;) {
+    const int cnt = group_size(first);
+    long long matrices = 0;
+    int max_k = 0;
+    for (int i = first; i < first + cnt; ++i) {
+      matrices += items_[i].p.batch;
+      max_k = std::max(max_k, items_[i].p.k_iters);
+    }
+    keys.emplace_back(matrices, max_k);
+    first += cnt;
+  }
+  return keys;
+}
+
+int GemmBatch::group_size(int first) const {
+  int cnt = (n_ - first) < GEMM_MAX_PROBLEMS ? (n_ - first) : GEMM_MAX_PROBLEMS;
+  for (int i = 1; i < cnt; ++i)
+    if ((items_[first + i].p.master != nullptr) != (items_[first].p.master != nullptr)) return i;
+  return cnt;
+}
+
+void GemmBatch::order() {
   // deepest contraction first, so that the longest tiles start in the first wave of the persistent CTAs
   for (int i = 1; i < n_; ++i)
     for (int j = i; j > 0 && items_[j].p.k_iters > items_[j - 1].p.k_iters; --j) {
@@ -1235,21 +1439,21 @@ muon_status GemmBatch::launch(cudaStream_t s) {
           items_[w++] = t;
         }
   }
+}
+
+muon_status GemmBatch::launch(cudaStream_t s) {
+  order();
   for (int first = 0; first < n_;) {
-    int cnt = (n_ - first) < GEMM_MAX_PROBLEMS ? (n_ - first) : GEMM_MAX_PROBLEMS;
-    for (int i = 1; i < cnt; ++i)
-      if ((items_[first + i].p.master != nullptr) != (items_[first].p.master != nullptr)) {
-        cnt = i;
-        break;
-      }
+    const int cnt = group_size(first);
     const bool master = items_[first].p.master != nullptr;
     GemmGroup g;
     memset(&g, 0, sizeof(g));
+    for (int i = 0; i < cnt; ++i) g.prob[i] = items_[first + i].p;
+    if (epi_ == EPI_GRAM32) choose_gram_split(g.prob, cnt, split_);
     long long tiles = 0;
     for (int i = 0; i < cnt; ++i) {
       g.map_a[i] = items_[first + i].ma;
       g.map_b[i] = items_[first + i].mb;
-      g.prob[i] = items_[first + i].p;
       g.prob[i].tile_begin = tiles;
       tiles += static_cast<long long>(g.prob[i].tiles_per_matrix) * g.prob[i].batch;
     }
@@ -1272,7 +1476,35 @@ muon_status GemmBatch::launch(cudaStream_t s) {
     muon_status st;
     switch (epi_) {
       case EPI_GRAM: st = launch_shape<EPI_GRAM, false, 6, 1>(g, KK_GRAM, s); break;
-      case EPI_GRAM32: st = launch_shape<EPI_GRAM32, false, 6, 2>(g, KK_GRAM32, s); break;
+      case EPI_GRAM32:
+        st = launch_shape<EPI_GRAM32, false, 12, 2>(g, KK_GRAM32, s);
+        if (st == MUON_OK) {
+          // the split problems' slices, added up
+          Gram32ReduceGroup rg;
+          memset(&rg, 0, sizeof(rg));
+          long long blocks = 0;
+          for (int i = 0; i < cnt; ++i) {
+            const GemmProblem &p = g.prob[i];
+            if (p.ksplit <= 1) continue;
+            Gram32Reduce &r = rg.prob[rg.nprob++];
+            r.out32 = p.out32;
+            r.scale = p.scale;
+            r.plane32 = p.plane32;
+            r.bprime32 = p.bprime32;
+            r.ld = p.ld_out;
+            r.mstride = p.mstride_out;
+            r.rows = p.rows;
+            r.ksplit = p.ksplit;
+            r.row_blocks = (p.rows + 7) / 8;
+            r.alpha = p.alpha;
+            r.coef_b = p.coef_b;
+            r.coef_c = p.coef_c;
+            r.block_begin = blocks;
+            blocks += static_cast<long long>(p.batch) * r.row_blocks;
+          }
+          st = launch_gram32_reduce(rg, blocks, s);
+        }
+        break;
       case EPI_POLY:
         st = shape == 0   ? launch_shape<EPI_POLY, false, 4, 5>(g, KK_POLY, s)
              : shape == 1 ? launch_shape<EPI_POLY, false, 5, 3>(g, KK_POLY, s)

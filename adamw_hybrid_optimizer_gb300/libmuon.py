@@ -90,7 +90,9 @@ SIGNATURES = {
     "muon_autotune_route": (ctypes.c_int32, [_c_int64, _c_int64, _c_int64]),
     "muon_autotune_scheduling": (ctypes.c_int32, [ctypes.POINTER(muon_bucket), ctypes.c_int]),
     "muon_autotune_poly_shape": (ctypes.c_int32, [_c_int64]),
+    "muon_autotune_gram_split": (ctypes.c_int32, [_c_int64, _c_int64]),
     "muon_autotune_reset": (None, []),
+    "muon_debug_gram_split": (ctypes.c_int, [ctypes.c_int32]),
     "muon_debug_poly_shape": (ctypes.c_int, [ctypes.c_int32]),
     "muon_debug_counter_deps": (ctypes.c_int, [ctypes.c_int32]),
     "muon_debug_gram_space": (ctypes.c_int, [ctypes.c_int32]),
@@ -378,6 +380,11 @@ def muon_autotune_poly_shape(contraction: int) -> int:
     return int(lib().muon_autotune_poly_shape(int(contraction)))
 
 
+def muon_autotune_gram_split(matrices: int, contraction: int) -> int:
+    """The recorded contraction slices of a Gram-space fp32 Gram launch, or -1."""
+    return int(lib().muon_autotune_gram_split(int(matrices), int(contraction)))
+
+
 def muon_autotune_reset():
     lib().muon_autotune_reset()
 
@@ -394,6 +401,11 @@ def muon_debug_counter_deps(mode: int):
 def muon_debug_gram_space(mode: int):
     """Gram-space Newton-Schulz path: -1 the library's rule (default), 0 never, 1 wherever the shape allows it."""
     _check(lib().muon_debug_gram_space(int(mode)), "muon_debug_gram_space")
+
+
+def muon_debug_gram_split(split: int):
+    """Contraction slices of the Gram-space fp32 Gram: 1 .. 8 forced, -1 the table and the rule (default)."""
+    _check(lib().muon_debug_gram_split(int(split)), "muon_debug_gram_split")
 
 
 def muon_gram_space_route(A: int, B: int, K: int = 1) -> bool:

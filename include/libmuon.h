@@ -142,14 +142,18 @@ muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hpar
  * workspace alone, and records in process-wide tables:
  *   1. the Newton-Schulz path of every bucket that can take the Gram-space chain (muon_gram_space_route):
  *      that bucket's chain timed each way, keyed by (min(A,B), max(A,B), K);
+ *   1b. the number of contraction slices (1, 2, 3, 4, 6 or 8) of the Gram-space buckets' fp32 Gram launch,
+ *      which has one tile pair per matrix: keyed by the launch's matrices and deepest contraction (see
+ *      muon_autotune_gram_split);
  *   2. the poly step's pipeline shape (mainloop stages + epilogue input slots: 4 + 5, 5 + 3, 6 + 2) for the
  *      plain buckets' grouped poly launch, keyed by its deepest contraction (without an entry, contractions
  *      up to 2048 take 4 + 5 and deeper ones 6 + 2);
  *   3. the plain chain's scheduling (per-matrix readiness counters or launch order), the whole set timed
  *      each way, keyed by the plain buckets' shapes and counts.
  * Each candidate runs once as a warm-up and five times timed (median). Later calls use the recorded choices
- * unless a debug switch forces one. The shapes and the scheduling never change a result; the path changes
- * the arithmetic (both paths are checked against the oracle by the tests).
+ * unless a debug switch forces one. The shapes and the scheduling never change a result; the slice count
+ * changes only the order of the Gram's fp32 additions; the path changes the arithmetic (both paths are
+ * checked against the oracle by the tests).
  *   buckets, n, hp, ws, ws_bytes  as for muon_step_grouped. The timed chains start from whatever the
  *            workspace's iterate holds and write only workspace sections: parameters, gradients and momentum
  *            are neither read nor written.
@@ -167,6 +171,12 @@ int32_t muon_autotune_scheduling(const muon_bucket *buckets, int n);
 /* The recorded poly shape (0: 4 + 5, 1: 5 + 3, 2: 6 + 2) for launches whose deepest contraction is
  * `contraction` (the matrices' smaller dimension), or -1 if none is recorded. */
 int32_t muon_autotune_poly_shape(int64_t contraction);
+
+/* The recorded number of contraction slices for fp32 Gram launches of the Gram-space path holding `matrices`
+ * matrices whose deepest contraction is `contraction` (the iterates' long side), or -1 if none is recorded.
+ * Without an entry a launch takes the most slices (up to 8) that fit one wave of SM pairs while each slice
+ * stays at least 1024 deep. */
+int32_t muon_autotune_gram_split(int64_t matrices, int64_t contraction);
 
 /* Empties the autotune tables. */
 void muon_autotune_reset(void);
@@ -330,6 +340,12 @@ muon_status muon_debug_poly_shape(int32_t shape);
  * muon_debug_gram_space: -1 the default rule, 0 never, 1 for every shape that can take it (for tests and
  * measurements). MUON_ERR_INVALID_ARG for other values. */
 muon_status muon_debug_gram_space(int32_t mode);
+
+/* Forces the fp32 Gram of the Gram-space path into `split` contraction slices (1 .. 8, clipped per stack to
+ * its contraction) in every launch, or -1 to go back to the table and the rule; for tests and sweeps. The
+ * slices are added in index order by a second kernel, so a given split always gives the same bits.
+ * MUON_ERR_INVALID_ARG for other values. */
+muon_status muon_debug_gram_split(int32_t split);
 
 /* 1 if a stack of K matrices of A x B takes the Gram-space path under the current mode and the autotune
  * table, else 0 (also for K, A or B < 1). */

@@ -8,7 +8,8 @@ the orthogonalised output (against both the oracle's plain iteration and its Gra
 agree in fp64), and of the parameter change for the Muon step. Shapes cover one and two 128-row blocks per
 side, ragged m, tall stacks (transposed to wide and back), stacks whose matrix count leaves part of a
 cluster idle, and very small m; inputs cover Gaussian, Student-t(3) and a rank-16 spike on noise, with the
-classic quintic and the 8-step Polar Express table.
+classic quintic and the 8-step Polar Express table. The fp32 Gram that starts the path is also run with its
+contraction split into slices (muon_debug_gram_split), against the unsplit result and the oracle.
 """
 import numpy as np
 import pytest
@@ -29,6 +30,7 @@ def L():
     lib = build_lib()
     yield lib
     lib.muon_debug_gram_space(-1)
+    lib.muon_debug_gram_split(-1)
 
 
 def _spike(K, A, B, seed):
@@ -100,6 +102,39 @@ def test_gram_space_forced_on_shapes_the_rule_leaves_plain(L, K, A, B):
         ref = omuon.newton_schulz(X[k], PE8, 1e-7)
         assert rel_fro(outs[1][k], ref) <= 2e-2
         assert rel_fro(outs[0][k], ref) <= 2e-2
+
+
+@pytest.mark.parametrize("K,A,B", [
+    (4, 256, 1024),    # 16 contraction steps of 64: slices of 8, 6 + 6 + 4, 2
+    (2, 200, 1000),    # ragged m and a ragged last step
+    (3, 1024, 256),    # tall
+    (2, 64, 300),      # 5 steps: 8 slices clip to 5 of one step each
+])
+def test_gram_split_matches_unsplit_and_oracle(L, K, A, B):
+    """The Gram-space path's fp32 Gram with its contraction split into 2, 3 and 8 slices (summed in slice order
+    by the reduce kernel): each within the bar of the oracle, within 1e-3 of the unsplit result (only the order
+    of the fp32 additions differs), and the same bits when run again."""
+    assert L.muon_gram_space_route(A, B)
+    x = _input("t3", K, A, B, 7 * K + A).to(DEV)
+    X = f64(x)
+    outs = {}
+    try:
+        for split in (1, 2, 3, 8, 3):
+            L.muon_debug_gram_split(split)
+            out = torch.full((K, A, B), float("nan"), dtype=torch.float32, device=DEV)
+            ws = workspace(L, K, A, B)
+            L.ns_orthogonalize(x, out, PE8, 1e-7, ws)
+            assert L.muon_check(ws) == L.MUON_OK
+            if split in outs:
+                assert torch.equal(out, outs[split]), split
+            outs[split] = out
+    finally:
+        L.muon_debug_gram_split(-1)
+    for split in (2, 3, 8):
+        for k in range(K):
+            got, base = f64(outs[split][k]), f64(outs[1][k])
+            assert rel_fro(got, base) <= 1e-3, (split, k, rel_fro(got, base))
+            assert rel_fro(got, omuon.newton_schulz(X[k], PE8, 1e-7)) <= 2e-2
 
 
 def test_gram_space_routing_rule(L):
