@@ -75,14 +75,14 @@ struct GemmProblem {
   // bf16 output of gram / poly / apply
   __nv_bfloat16 *out;
   long long ld_out, mstride_out;
-  // fp32 output of the Gram-space Gram (EPI_GRAM32): hi plane at out32, lo plane at out32 + plane32, with the
-  // row and matrix pitches ld_out and mstride_out (elements); and c * G + b * I (coef_b, coef_c) at
-  // out32 + bprime32 and that + plane32
-  float *out32;
-  long long plane32, bprime32;
+  // output of the Gram-space Gram (EPI_GRAM32), bf16 planes: G's hi plane (G rounded) at out, its lo plane (the
+  // rest, rounded) at out + gs_plane, with the row and matrix pitches ld_out and mstride_out (elements); and
+  // c * G + b * I (coef_b, coef_c) the same way at out + gs_bprime and that + gs_plane
+  long long gs_plane, gs_bprime;
   // EPI_GRAM32 split along the contraction: ksplit (>= 1) slices of kper 64-deep steps, each slice a tile pair of
-  // its own; slice j stores its raw fp32 sum in plane 2 + j (out32 + (2 + j) * plane32), and a reduce kernel
-  // adds the slices in index order and forms the outputs above
+  // its own; slice j stores its raw fp32 sum over the two bf16 planes 2 + 2 j and 3 + 2 j (as fp32 with the same
+  // element pitches, from out + (2 + 2 j) * gs_plane), and a reduce kernel adds the slices in index order and
+  // forms the outputs above
   int ksplit, kper;
   // final step: parameter update (params != null) or dense store (out_dense != null); with master, the
   // update applies to the fp32 master copies and params receive them rounded to bf16
@@ -136,7 +136,7 @@ int poly_shape_forced();
 // launch takes the most slices that still fit one wave and keep each slice at least GRAM32_MIN_SLICE_K 64-deep
 // steps; the autotune table holds measured counts keyed by the launch's matrices and deepest contraction; a
 // forced count (-1: none) serves tests and sweeps. The count changes only the order of the fp32 additions.
-constexpr int GRAM32_MAX_SPLIT = 8;
+constexpr int GRAM32_MAX_SPLIT = 4;
 constexpr int GRAM32_MIN_SLICE_K = 16;
 int gram_split_lookup(long long matrices, int k_iters);
 void gram_split_record(long long matrices, int k_iters, int split);
@@ -170,9 +170,9 @@ class GemmBatch {
                        const TileSync *sync = nullptr);
   muon_status add_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bfloat16 *out, const float *scale,
                        const TileSync *sync = nullptr);
-  // EPI_GRAM32 (x.rows <= 256): g = alpha * s^2 * x x^T as fp32 hi / lo planes, and c g + b I at g_hi + bprime;
-  // planes 2 .. bprime / plane - 1 are scratch for the slices of a split contraction
-  muon_status add_gram32(const Bf16Stack &x, float *g_hi, long long ldg, long long mstride_g, long long plane,
+  // EPI_GRAM32 (x.rows <= 256): g = alpha * s^2 * x x^T as bf16 hi / lo planes, and c g + b I at g_hi + bprime;
+  // planes 2 .. bprime / plane - 1 are scratch for the slices of a split contraction (two planes per slice)
+  muon_status add_gram32(const Bf16Stack &x, __nv_bfloat16 *g_hi, long long ldg, long long mstride_g, long long plane,
                          long long bprime, float b, float c, float alpha, const float *scale);
   // EPI_GRAM32 only: split every contraction into this many slices (clipped to what each problem allows), whatever
   // the table or the rule says (0: no override)
@@ -246,9 +246,11 @@ muon_status launch_ns_small(const SmallNsArgs &a, cudaStream_t s);
 // ------------------------------------------------------------------------------------------ Gram-space chain
 
 // The Newton-Schulz iteration in the m x m Gram space (ns_gram_space.cu) for wide iterates with at most
-// GS_MAX_M rows that the fused small-matrix kernel does not take. Its scratch is GS_BUFFERS fp32 m x m matrices
-// per matrix of the stack (A, Q, P, two R and B), each as a hi and a lo plane with rows of round8(m) elements:
-// buffer b, plane p, matrix k at ((b * 2 + p) * K + k) * m * round8(m); then R_N for the final product as two
+// GS_MAX_M rows that the fused small-matrix kernel does not take. Its scratch is GS_BUFFERS m x m matrices per
+// matrix of the stack (A, Q, P, two R and B), each as two bf16 planes, hi (the value rounded) and lo (the rest,
+// rounded), with rows of round8(m) elements: buffer b, plane p, matrix k at ((b * 2 + p) * K + k) * m *
+// round8(m) elements; before the chain runs, buffers Q .. R1 hold the fp32 Gram's slice sums when its
+// contraction is split (slice j, fp32, over planes 2 + 2 j and 3 + 2 j); then R_N for the final product as two
 // bf16 halves side by side, [R_hi | R_lo] (R_hi = R_N rounded, R_lo = the rest rounded), each half 64-column
 // padded with zeros: K matrices of m rows x 2 * round64(m) columns.
 constexpr int GS_MAX_M = 256;
@@ -260,12 +262,12 @@ inline bool gram_space_eligible(long long m, long long n) { return m >= 1 && m <
 size_t gram_space_plane_bytes(long long K, long long m);
 inline long long round64(long long v) { return (v + 63) / 64 * 64; }
 struct GramSpaceStack {
-  float *planes;             // the stack's scratch (16-byte aligned): fp32 planes, then [R_hi | R_lo]
+  __nv_bfloat16 *planes;     // the stack's scratch (16-byte aligned): the buffers' planes, then [R_hi | R_lo]
   int K, m;
 };
 // The [R_hi | R_lo] halves of a stack's scratch.
-inline __nv_bfloat16 *gram_space_rsplit(float *planes, long long K, long long m) {
-  return reinterpret_cast<__nv_bfloat16 *>(planes + static_cast<long long>(GS_BUFFERS) * 2 * K * m * round8(m));
+inline __nv_bfloat16 *gram_space_rsplit(__nv_bfloat16 *planes, long long K, long long m) {
+  return planes + static_cast<long long>(GS_BUFFERS) * 2 * K * m * round8(m);
 }
 // From A_0 in buffer GS_G (written by an EPI_GRAM32 launch) to R_N in bf16, for every matrix of up to n stacks
 // (one launch per 8 stacks).

@@ -296,7 +296,7 @@ bool gram_space_route(long long m, long long n, long long K) {
 muon_status add_gram_space(char *ws, const Layout &L, long long K, const float *coeffs, const FinalSpec &fin,
                            GemmBatch &g32, std::vector<GramSpaceStack> &gs, GemmBatch &fin_batch) {
   const float *scale = reinterpret_cast<const float *>(ws + L.scale);
-  float *planes = reinterpret_cast<float *>(ws + L.gs);
+  __nv_bfloat16 *planes = reinterpret_cast<__nv_bfloat16 *>(ws + L.gs);
   const long long ldm = round8(L.m), msm = L.m * ldm;
   Bf16Stack X{ws + L.x0, L.m, L.n, L.ldx, L.m * L.ldx, K};
   // A_0 into buffer GS_G and c_0 A_0 + b_0 I into buffer GS_B (plane p of buffer b starts at (2 b + p) K m ldm)
@@ -850,7 +850,7 @@ muon_status muon_autotune(const muon_bucket *buckets, int n, const muon_hparams 
     auto gram32_batch = [&](GemmBatch &g32) -> muon_status {
       for (const ChainStack &c : cs) {
         if (c.path != PATH_GRAM) continue;
-        float *planes = reinterpret_cast<float *>(c.w + c.L.gs);
+        __nv_bfloat16 *planes = reinterpret_cast<__nv_bfloat16 *>(c.w + c.L.gs);
         const long long ldm = round8(c.L.m), msm = c.L.m * ldm;
         Bf16Stack X{c.w + c.L.x0, c.L.m, c.L.n, c.L.ldx, c.L.m * c.L.ldx, c.K};
         muon_status r = g32.add_gram32(X, planes, ldm, msm, c.K * msm, 2LL * GS_B * c.K * msm, hp->coeffs[1],
@@ -867,7 +867,7 @@ muon_status muon_autotune(const muon_bucket *buckets, int n, const muon_hparams 
     }
     int best = 1;
     float best_ms = -1.f;
-    for (int split : {1, 2, 3, 4, 6, 8}) {
+    for (int split = 1; split <= GRAM32_MAX_SPLIT; ++split) {
       const float ms = median_time(
           [&]() -> muon_status {
             GemmBatch g32(EPI_GRAM32, err, g_timeout_ns);

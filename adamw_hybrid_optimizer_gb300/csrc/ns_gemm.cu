@@ -405,22 +405,23 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem &a, int b, int 
   const int row = warp_row0 + lane;
   const int rows = a.rows, cols = a.cols;
   if constexpr (EPI == EPI_GRAM32) {
+    // Each lane writes its own row's 32 values in whole 16-byte pieces: a piece that starts inside the row ends
+    // inside its padding (the pitch is a multiple of 8 elements), where every output is zero (the operand's rows
+    // past m load as zeros, and the diagonal term lies inside) and nothing reads.
+    if (row >= rows) return;
+    const long long at = static_cast<long long>(b) * a.mstride_out + static_cast<long long>(row) * a.ld_out + col0;
     if (a.ksplit > 1) {
-      // one slice of a split contraction: the raw sum, row by row (each lane 128 bytes of its row), into the
-      // slice's plane; the reduce kernel scales and splits the total. Whole 16-byte pieces: a piece that starts
-      // inside the row ends inside its padding (the pitch is a multiple of 8), where the sum is zero (the
-      // operand's rows past m load as zeros) and nothing reads
-      if (row >= rows) return;
-      float *d = a.out32 + (2 + slice) * a.plane32 + static_cast<long long>(b) * a.mstride_out +
-                 static_cast<long long>(row) * a.ld_out + col0;
+      // one slice of a split contraction: the raw fp32 sum into the slice's scratch; the reduce kernel scales and
+      // splits the total
+      float *d = reinterpret_cast<float *>(a.out + (2 + 2 * slice) * a.gs_plane) + at;
 #pragma unroll
       for (int q = 0; q < 8; ++q)
         if (col0 + 4 * q < cols)
           *reinterpret_cast<float4 *>(d + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
       return;
     }
-    // the whole m x m tile is computed (m <= 256: one tile pair per matrix); each lane stores its row's 32
-    // values as a tf32 hi plane (low 13 mantissa bits cleared) and an fp32 lo plane (the rest, exact)
+    // the whole m x m tile is computed (m <= 256: one tile pair per matrix): G = alpha s^2 acc and c G + b I,
+    // each as a bf16 hi plane (rounded) and a bf16 lo plane (the rest, rounded)
     float sc = a.alpha;
     if (a.scale != nullptr) {
       const float s = a.scale[b];
@@ -428,44 +429,28 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem &a, int b, int 
     }
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] *= sc;
-    // each warp stages its 32 x 32 fp32 chunk (4 KB of the two ring slots this kind is launched with) so that
-    // every global store writes four whole 128-byte rows: 16-byte piece q of row r at position q ^ (r & 7)
-    uint8_t *stg = rg.slot + (rg.half * 4 + rg.lane_base / 32) * 4096;
-    auto piece = [&](int r, int q) { return reinterpret_cast<float4 *>(stg + r * 128 + ((q ^ (r & 7)) << 4)); };
-    float *base = a.out32 + static_cast<long long>(b) * a.mstride_out;
+    __nv_bfloat16 *base = a.out + at;
 #pragma unroll 1
-    for (int pass = 0; pass < 4; ++pass) {   // G hi, G lo, then (c G + b I) hi, lo
-      const bool bp = pass >= 2, lo = pass & 1;
+    for (int bp = 0; bp < 2; ++bp) {   // G, then c G + b I
       const float cm = bp ? a.coef_c : 1.f, dg = bp ? a.coef_b : 0.f;
-      const uint32_t mask = lo ? 0u : 0xFFFFE000u;
-      float w[32];
+      __nv_bfloat16 *dh = base + (bp ? a.gs_bprime : 0), *dl = dh + a.gs_plane;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float x = fmaf(cm, v[j], col0 + j == row ? dg : 0.f);
-        const float h = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
-        // hi plane: h; lo plane: x - h
-        w[j] = lo ? x - h : __uint_as_float(__float_as_uint(x) & mask);
-      }
+      for (int q = 0; q < 4; ++q) {
+        if (col0 + 8 * q >= cols) break;
+        uint4 wh, wl;
+        __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&wh), *l = reinterpret_cast<__nv_bfloat162 *>(&wl);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) *piece(lane, q) = make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-      __syncwarp();
-      float *dst = base + (bp ? a.bprime32 : 0) + (lo ? a.plane32 : 0);
-      const int q = lane & 7, c = col0 + 4 * q;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = 4 * i + (lane >> 3);
-        if (warp_row0 + r >= rows) continue;
-        const float4 x = *piece(r, q);
-        float *d = dst + static_cast<long long>(warp_row0 + r) * a.ld_out + c;
-        if (c + 4 <= cols) {
-          *reinterpret_cast<float4 *>(d) = x;
-        } else {
-          if (c < cols) d[0] = x.x;
-          if (c + 1 < cols) d[1] = x.y;
-          if (c + 2 < cols) d[2] = x.z;
+        for (int e = 0; e < 4; ++e) {
+          const int j = 8 * q + 2 * e;
+          const float x0 = fmaf(cm, v[j], col0 + j == row ? dg : 0.f);
+          const float x1 = fmaf(cm, v[j + 1], col0 + j + 1 == row ? dg : 0.f);
+          h[e] = __floats2bfloat162_rn(x0, x1);
+          const float2 r = __bfloat1622float2(h[e]);
+          l[e] = __floats2bfloat162_rn(x0 - r.x, x1 - r.y);
         }
+        *reinterpret_cast<uint4 *>(dh + 8 * q) = wh;
+        *reinterpret_cast<uint4 *>(dl + 8 * q) = wl;
       }
-      __syncwarp();
     }
     return;
   } else if constexpr (EPI == EPI_GRAM || EPI == EPI_POLY) {
@@ -1111,12 +1096,13 @@ muon_status launch_shape(const GemmGroup &g, int32_t kind, cudaStream_t s) {
 
 // ------------------------------------------------------------------------------------------ split fp32 Gram
 
-// One problem of a split EPI_GRAM32 launch, for the reduce kernel: ksplit raw slice sums in planes 2 .. 2 +
-// ksplit - 1 of out32 (rows x rows, row pitch ld, matrix pitch mstride, plane pitch plane32).
+// One problem of a split EPI_GRAM32 launch, for the reduce kernel: ksplit raw fp32 slice sums, slice j over the
+// bf16 planes 2 + 2 j and 3 + 2 j from out (rows x rows, row pitch ld and matrix pitch mstride in elements, plane
+// pitch plane); the outputs as the unsplit epilogue writes them.
 struct Gram32Reduce {
-  float *out32;
+  __nv_bfloat16 *out;
   const float *scale;
-  long long plane32, bprime32, ld, mstride, block_begin;
+  long long plane, bprime, ld, mstride, block_begin;
   int rows, ksplit, row_blocks;
   float alpha, coef_b, coef_c;
 };
@@ -1126,10 +1112,10 @@ struct Gram32ReduceGroup {
 };
 static_assert(sizeof(Gram32ReduceGroup) <= 4096, "kernel parameter block too large");
 
-// The outputs of the fp32 Gram from its slices: A = alpha * s^2 * (slice 0 + slice 1 + ...), added in slice
-// order, as a tf32 hi plane (low 13 mantissa bits cleared) and an fp32 lo plane (the rest), and c A + b I the
-// same way: what the unsplit epilogue stores. Blocks of 256 threads: 8 rows of one matrix, 32 lanes per row,
-// lane l the 4 columns at 4 l and 4 l + 128 (rows <= 256).
+// The outputs of the fp32 Gram from its slices: G = alpha * s^2 * (slice 0 + slice 1 + ...), added in slice
+// order, and c G + b I, each as a bf16 hi plane (rounded) and a bf16 lo plane (the rest, rounded): what the
+// unsplit epilogue stores. Blocks of 256 threads: 8 rows of one matrix, 32 lanes per row, lane l the 4 columns
+// at 4 l and 4 l + 128 (rows <= 256).
 __global__ void __launch_bounds__(256) gram32_reduce_kernel(const __grid_constant__ Gram32ReduceGroup G) {
   pdl_wait();
   if (threadIdx.x == 0) pdl_launch_dependents();
@@ -1154,7 +1140,7 @@ __global__ void __launch_bounds__(256) gram32_reduce_kernel(const __grid_constan
     float v[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
     for (int j = 0; j < a.ksplit; ++j) {
-      const float *src = a.out32 + (2 + j) * a.plane32 + base + c;
+      const float *src = reinterpret_cast<const float *>(a.out + (2 + 2 * j) * a.plane) + base + c;
       if (full) {
         const float4 q = __ldcg(reinterpret_cast<const float4 *>(src));
         v[0] += q.x;
@@ -1166,24 +1152,22 @@ __global__ void __launch_bounds__(256) gram32_reduce_kernel(const __grid_constan
           if (c + e < a.rows) v[e] += __ldcg(src + e);
       }
     }
-    float o[4][4];   // G hi, G lo, B' hi, B' lo
+    __nv_bfloat16 o[4][4];   // G hi, G lo, (c G + b I) hi, lo
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float x = v[e] * sc;
       const float xb = fmaf(a.coef_c, x, c + e == row ? a.coef_b : 0.f);
-      const float xh = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
-      const float bh = __uint_as_float(__float_as_uint(xb) & 0xFFFFE000u);
-      o[0][e] = xh;
-      o[1][e] = x - xh;
-      o[2][e] = bh;
-      o[3][e] = xb - bh;
+      o[0][e] = __float2bfloat16_rn(x);
+      o[1][e] = __float2bfloat16_rn(x - __bfloat162float(o[0][e]));
+      o[2][e] = __float2bfloat16_rn(xb);
+      o[3][e] = __float2bfloat16_rn(xb - __bfloat162float(o[2][e]));
     }
-    const long long off[4] = {0, a.plane32, a.bprime32, a.bprime32 + a.plane32};
+    const long long off[4] = {0, a.plane, a.bprime, a.bprime + a.plane};
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-      float *d = a.out32 + off[w] + base + c;
+      __nv_bfloat16 *d = a.out + off[w] + base + c;
       if (full) {
-        *reinterpret_cast<float4 *>(d) = make_float4(o[w][0], o[w][1], o[w][2], o[w][3]);
+        *reinterpret_cast<uint2 *>(d) = *reinterpret_cast<const uint2 *>(o[w]);
       } else {
         for (int e = 0; e < 4; ++e)
           if (c + e < a.rows) d[e] = o[w][e];
@@ -1230,7 +1214,7 @@ void choose_gram_split(GemmProblem *probs, int cnt, int forced) {
   }
   for (int i = 0; i < cnt; ++i) {
     GemmProblem &p = probs[i];
-    const long long planes = p.plane32 > 0 ? p.bprime32 / p.plane32 - 2 : 0;
+    const long long planes = p.gs_plane > 0 ? (p.gs_bprime / p.gs_plane - 2) / 2 : 0;   // two per slice
     long long sp = want;
     if (rule) sp = std::min<long long>(sp, p.k_iters / GRAM32_MIN_SLICE_K);
     sp = std::min<long long>({sp, GRAM32_MAX_SPLIT, planes, p.k_iters});
@@ -1321,7 +1305,7 @@ muon_status GemmBatch::add_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long 
   return push(it);
 }
 
-muon_status GemmBatch::add_gram32(const Bf16Stack &x, float *g_hi, long long ldg, long long mstride_g,
+muon_status GemmBatch::add_gram32(const Bf16Stack &x, __nv_bfloat16 *g_hi, long long ldg, long long mstride_g,
                                   long long plane, long long bprime, float b, float c, float alpha,
                                   const float *scale) {
   if (epi_ != EPI_GRAM32 || x.rows > 2 * BM) return MUON_ERR_INVALID_ARG;
@@ -1332,9 +1316,9 @@ muon_status GemmBatch::add_gram32(const Bf16Stack &x, float *g_hi, long long ldg
   fill_tiles(it.p, x.batch, x.rows, x.rows, x.cols, false);   // one tile pair per matrix: the whole m x m
   it.p.alpha = alpha;
   it.p.scale = scale;
-  it.p.out32 = g_hi;
-  it.p.plane32 = plane;
-  it.p.bprime32 = bprime;
+  it.p.out = g_hi;
+  it.p.gs_plane = plane;
+  it.p.gs_bprime = bprime;
   it.p.coef_b = b;
   it.p.coef_c = c;
   it.p.ld_out = ldg;
@@ -1487,10 +1471,10 @@ muon_status GemmBatch::launch(cudaStream_t s) {
             const GemmProblem &p = g.prob[i];
             if (p.ksplit <= 1) continue;
             Gram32Reduce &r = rg.prob[rg.nprob++];
-            r.out32 = p.out32;
+            r.out = p.out;
             r.scale = p.scale;
-            r.plane32 = p.plane32;
-            r.bprime32 = p.bprime32;
+            r.plane = p.gs_plane;
+            r.bprime = p.gs_bprime;
             r.ld = p.ld_out;
             r.mstride = p.mstride_out;
             r.rows = p.rows;

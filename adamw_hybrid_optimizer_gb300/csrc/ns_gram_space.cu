@@ -6,20 +6,26 @@
 // and X_N = R_N X_0, which the final-step GEMM applies with the parameter update (as R_hi X_0 + R_lo X_0).
 // Every matrix here is a polynomial in A_0, so all of them are symmetric and commute.
 //
-// Precision: forming A squares the condition number, so the m x m chain keeps fp32 accuracy. Each matrix is
-// stored as two fp32 planes, hi (the value with its low 13 mantissa bits cleared: exactly a tf32 number) and
-// lo (the rest, exact in fp32), and every product is three tf32 tensor-core passes, hi*hi + hi*lo + lo*hi,
-// accumulated in fp32 in tensor memory (the lo*lo term is below fp32 rounding).
+// Precision: forming A squares the condition number, so the m x m chain keeps more than bf16 accuracy. Each
+// matrix is stored as two bf16 planes, hi = the value rounded to bf16 and lo = the rest rounded to bf16 (16
+// significant bits together), and every product is three bf16 tensor-core passes, hi*hi + hi*lo + lo*hi,
+// accumulated in fp32 in tensor memory (the lo*lo term is below that precision). The error of the result is
+// then set by the bf16 iterate X_0 and by the bf16 halves of R_N, not by the chain: in fp64 simulations of the
+// recurrence on the test inputs (Gaussian, Student-t(3), rank-16 spikes, log-spaced spectra) the bf16 split
+// gave the same error against the plain fp64 iteration as fp32-accurate products, to three or four digits.
 //
 // Design (sm_103a): one cluster of 4 CTAs per matrix (m in 129..256: CTA (bi, bj) owns the 128 x 128 output
 // block (bi, bj) of every product) or per 4 matrices (m <= 128: one block each). A CTA's operands are the rows
-// of its block of the left matrix and, since the right matrix is symmetric, the rows of its block column of
-// the right one (exactly the K-major B operand); TMA brings them in 32-column (128-byte) slices of hi and lo
-// planes through a 3-stage ring, one thread issues tcgen05.mma kind::tf32 (M = 128, N = 128, K = 8) into one
-// of two 128-column accumulators, and four epilogue warps (one per tensor-memory lane quarter) finish each
-// product: the diagonal term of Q, the hi / lo split, and the fp32 stores. The CTAs of a cluster
-// exchange results through global memory (L2-resident; every block leaves by a TMA bulk store of 128 x 32 tiles
-// staged in shared memory), one cluster barrier per phase:
+// of its block row of the left matrix (K-major) and the columns of its block column of the right one, read as
+// 64-row slices of that block column (MN-major). The matrices are symmetric only up to rounding, and the
+// iteration amplifies the asymmetric part, so every product takes its right operand as stored, never its
+// transpose: in fp64 simulations of the recurrence on square Gaussian inputs, reading the right operand
+// transposed (exact for symmetric matrices) raised the error ten times. TMA brings the operands in 64-deep
+// (128-byte) slices of hi and lo planes through a 3-stage ring, one thread issues tcgen05.mma kind::f16 (bf16, M = 128, N = 128, K = 16) into
+// one of two 128-column accumulators, and four epilogue warps (one per tensor-memory lane quarter) finish each
+// product 64 columns at a time: the diagonal term of Q, the hi / lo split, and the stores. The CTAs of a cluster
+// exchange results through global memory (L2-resident; every block leaves by TMA bulk stores of 128 x 64 bf16
+// tiles staged in shared memory), one cluster barrier per phase:
 //     phase A: A B = b A + c A A  -> Q = a I + A B (and R_1 = Q_0 at t = 0)
 //     phase B: P = Q A, R' = Q R  -> P, R'   (P not at the last step, R' not at t = 0)
 //     phase C: A' = Q P           -> A, and B = c' A' + b' I with the next step's coefficients (not at the last step)
@@ -45,8 +51,8 @@ namespace {
 
 constexpr int GS_THREADS = 192;          // warp 0 TMA, warp 1 MMA (+ TMEM owner), warps 2-5 epilogue
 constexpr int GS_BLOCK = 128;            // output block side, M and N of every MMA
-constexpr int GS_KC = 32;                // fp32 columns per slice: one 128-byte swizzled row
-constexpr int GS_TILE_BYTES = GS_BLOCK * GS_KC * 4;          // 16 KB
+constexpr int GS_KC = 64;                // bf16 columns per slice: one 128-byte swizzled row
+constexpr int GS_TILE_BYTES = GS_BLOCK * GS_KC * 2;          // 16 KB
 constexpr int GS_STAGE_BYTES = 4 * GS_TILE_BYTES;            // A hi, A lo, B hi, B lo
 constexpr int GS_STAGES = 3;
 constexpr int GS_CLUSTER = 4;
@@ -54,7 +60,7 @@ constexpr uint32_t GS_TMEM_COLS = 256;   // two 128-column accumulators
 constexpr int GS_MAX_PROBLEMS = 8;
 
 struct GsProblem {
-  float *planes;            // buffer b, plane p (0 hi, 1 lo), matrix k at ((b * 2 + p) * K + k) * m * ldm
+  __nv_bfloat16 *planes;    // buffer b, plane p (0 hi, 1 lo), matrix k at ((b * 2 + p) * K + k) * m * ldm
   __nv_bfloat16 *r_out;     // [R_hi | R_lo]: matrix k at r_out + k * m * ld_r, rows of ld_r = 2 * mp elements
   long long ldm, ld_r, mp;  // mp = round64(m): the offset of R_lo in a row
   long long unit_begin;     // first cluster of this problem in the launch
@@ -62,7 +68,8 @@ struct GsProblem {
 };
 
 struct GsGroup {
-  CUtensorMap map[GS_MAX_PROBLEMS];   // fp32 (m, m, 10 K) over the planes, box 32 x 128, 128-byte swizzle
+  CUtensorMap map[GS_MAX_PROBLEMS];   // bf16 (m, m, 12 K) over the planes, box 64 x 128, 128-byte swizzle
+  CUtensorMap map_b[GS_MAX_PROBLEMS]; // the same tensor, box 64 x 64: a right-operand slice is two of them
   GsProblem prob[GS_MAX_PROBLEMS];
   int nprob;
   long long total_units;
@@ -90,7 +97,7 @@ struct GsCtrl {
 };
 
 constexpr int GS_EPI_WARPS = 4;
-constexpr int GS_OUT_TILES = 2;   // double-buffered 128 x 32 fp32 output tiles for the TMA stores
+constexpr int GS_OUT_TILES = 2;   // double-buffered 128 x 64 bf16 output tiles for the TMA stores
 constexpr size_t GS_SMEM = static_cast<size_t>(GS_STAGES) * GS_STAGE_BYTES +
                            static_cast<size_t>(GS_OUT_TILES) * GS_TILE_BYTES + sizeof(GsCtrl) + 1024;
 constexpr int GS_EPI_BAR = 1;     // named barrier of the four epilogue warps
@@ -123,7 +130,24 @@ __device__ __forceinline__ int phase_products(int t, int ph, int N, Product *p) 
   return 0;
 }
 
-__device__ __forceinline__ float tf32_hi(float v) { return __uint_as_float(__float_as_uint(v) & 0xFFFFE000u); }
+// Eight values as bf16: rounded (hi), or what rounding left over, rounded (lo).
+__device__ __forceinline__ uint4 pack8_hi(const float *x) {
+  uint4 w;
+  __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+  return w;
+}
+__device__ __forceinline__ uint4 pack8_lo(const float *x) {
+  uint4 w;
+  __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 r = __bfloat1622float2(__floats2bfloat162_rn(x[2 * e], x[2 * e + 1]));
+    h[e] = __floats2bfloat162_rn(x[2 * e] - r.x, x[2 * e + 1] - r.y);
+  }
+  return w;
+}
 
 __device__ __forceinline__ int find_problem(const GsGroup &g, long long u) {
   int p = 0;
@@ -133,18 +157,15 @@ __device__ __forceinline__ int find_problem(const GsGroup &g, long long u) {
   return p;
 }
 
-__device__ __forceinline__ float *plane(const GsProblem &P, int buf, int pl, int k) {
-  return P.planes + ((static_cast<long long>(buf) * 2 + pl) * P.K + k) * static_cast<long long>(P.m) * P.ldm;
-}
 
-// Epilogue output: the four epilogue warps write a 128-row x 32-column fp32 tile of one plane into shared memory
+// Epilogue output: the four epilogue warps write a 128-row x 64-column bf16 tile of one plane into shared memory
 // in the layout a TMA load of that box produces (128-byte rows; 16-byte piece q of row r at position q ^ (r & 7)),
 // and one thread stores it with a TMA bulk store, which writes whole rows, leaves out rows and columns past m, and
 // runs asynchronously to the warps. Two tiles alternate; the storing thread waits, before a tile is written
 // again, until the store two tiles back has read it, and before the phase barrier until every store is done.
 struct TileOut {
   uint8_t *tiles;          // GS_OUT_TILES tiles of GS_TILE_BYTES, 1024-byte aligned
-  const CUtensorMap *map;  // the planes' tensor map (box 32 x 128)
+  const CUtensorMap *map;  // the planes' tensor map (box 64 x 128)
   int n;                   // tiles stored so far in this kernel
   bool issuer;             // the one thread that issues the stores
 };
@@ -154,15 +175,17 @@ __device__ __forceinline__ float4 *tile_piece(uint8_t *tile, int r, int q) {
 }
 
 // Collective over the four epilogue warps: stores rows of block row bi (this lane's row: quarter * 32 + lane of
-// the tile), columns col0 .. col0 + 31, of plane `pl` of buffer `buf` of matrix k, values w.
+// the tile), columns col0 .. col0 + 63, of plane `pl` of buffer `buf` of matrix k; piece(q) gives the lane's
+// 16-byte piece q (columns col0 + 8 q .. + 7).
+template <typename Piece>
 __device__ __forceinline__ void store_tile(TileOut &to, const GsProblem &P, int bi, int quarter, int lane, int buf,
-                                           int pl, int k, int col0, const float *w) {
+                                           int pl, int k, int col0, Piece piece) {
   uint8_t *tile = to.tiles + (to.n & 1) * GS_TILE_BYTES;
   if (to.issuer) bulk_wait_group_read<1>();   // the store that last used this tile has read it
   named_barrier_sync(GS_EPI_BAR, GS_EPI_WARPS * 32);
   const int r = quarter * 32 + lane;
 #pragma unroll
-  for (int q = 0; q < 8; ++q) *tile_piece(tile, r, q) = make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4 *>(tile_piece(tile, r, q)) = piece(q);
   fence_proxy_async_shared();                 // the generic writes are visible to the TMA engine
   named_barrier_sync(GS_EPI_BAR, GS_EPI_WARPS * 32);
   if (to.issuer) {
@@ -172,16 +195,11 @@ __device__ __forceinline__ void store_tile(TileOut &to, const GsProblem &P, int 
   ++to.n;
 }
 
-// Both planes of one buffer: the tf32 hi part and the rest.
+// Both planes of one buffer from the lane's 64 values: the bf16 rounding and the rounded rest.
 __device__ __forceinline__ void store_split(TileOut &to, const GsProblem &P, int bi, int quarter, int lane, int buf,
                                             int k, int col0, const float *v) {
-  float w[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) w[j] = tf32_hi(v[j]);
-  store_tile(to, P, bi, quarter, lane, buf, 0, k, col0, w);
-#pragma unroll
-  for (int j = 0; j < 32; ++j) w[j] = v[j] - w[j];
-  store_tile(to, P, bi, quarter, lane, buf, 1, k, col0, w);
+  store_tile(to, P, bi, quarter, lane, buf, 0, k, col0, [&](int q) { return pack8_hi(v + 8 * q); });
+  store_tile(to, P, bi, quarter, lane, buf, 1, k, col0, [&](int q) { return pack8_lo(v + 8 * q); });
 }
 
 // R_N for the final GEMM as two bf16 halves, R_hi = rn(R) at column c and R_lo = rn(R - R_hi) at column mp + c,
@@ -214,8 +232,8 @@ __device__ __forceinline__ void store_rsplit(const GsProblem &P, uint8_t *stg, i
   __syncwarp();
 }
 
-// The epilogue of one 32-column chunk of a product, collective over the four epilogue warps: rows of block row
-// bi (lane = row quarter * 32 + lane of the block), columns col0 .. col0 + 31; v holds the lane's 32 values.
+// The epilogue of one 64-column chunk of a product, collective over the four epilogue warps: rows of block row
+// bi (lane = row quarter * 32 + lane of the block), columns col0 .. col0 + 63; v holds the lane's 64 values.
 // rstage: a 4 KB staging chunk of this warp for the R_N halves (in the operand ring, idle by then).
 __device__ __forceinline__ void epilogue_chunk(TileOut &to, const GsProblem &P, const Product &pr, int k, int bi,
                                                int quarter, int lane, int col0, int t, int N, const float *co,
@@ -226,22 +244,34 @@ __device__ __forceinline__ void epilogue_chunk(TileOut &to, const GsProblem &P, 
     if (pr.kind == EK_Q) {
       // Q = a I + (b A + c A^2), the bracket from the MMA
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] += col0 + j == row ? co[3 * t] : 0.f;
+      for (int j = 0; j < 64; ++j) v[j] += col0 + j == row ? co[3 * t] : 0.f;
       if (t == 0 && N > 1) store_split(to, P, bi, quarter, lane, GS_R0, k, col0, v);   // R_1 = Q_0
     }
     store_split(to, P, bi, quarter, lane, pr.out_buf, k, col0, v);
     if (pr.kind == EK_A) {
       // the next step's right operand c' A' + b' I
       const float bn = co[3 * (t + 1) + 1], cn = co[3 * (t + 1) + 2];
-      float w[32];
+      auto bprime8 = [&](int q, float *w) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) w[j] = fmaf(cn, v[j], col0 + j == row ? bn : 0.f);
-      store_split(to, P, bi, quarter, lane, GS_B, k, col0, w);
+        for (int j = 0; j < 8; ++j) w[j] = fmaf(cn, v[8 * q + j], col0 + 8 * q + j == row ? bn : 0.f);
+      };
+      store_tile(to, P, bi, quarter, lane, GS_B, 0, k, col0, [&](int q) {
+        float w[8];
+        bprime8(q, w);
+        return pack8_hi(w);
+      });
+      store_tile(to, P, bi, quarter, lane, GS_B, 1, k, col0, [&](int q) {
+        float w[8];
+        bprime8(q, w);
+        return pack8_lo(w);
+      });
     }
   }
   // R_N: at t = 0 when N = 1 (R_1 = Q_0), else from the last R product (the phase's only product either way)
-  if (row0 < P.m && ((pr.kind == EK_Q && N == 1) || (pr.kind == EK_R && t == N - 1)))
+  if (row0 < P.m && ((pr.kind == EK_Q && N == 1) || (pr.kind == EK_R && t == N - 1))) {
     store_rsplit(P, rstage, lane, k, row0, col0, v);
+    store_rsplit(P, rstage, lane, k, row0, col0 + 32, v + 32);
+  }
 }
 
 __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS, 1)
@@ -275,7 +305,11 @@ __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS,
   const int bj = P.mb == 2 ? static_cast<int>(rank & 1) : 0;
   const bool active = k < P.K;
   const CUtensorMap *map = &args.map[pi];
-  if (warp == 0 && lane == 0) tma_prefetch_desc(map);
+  const CUtensorMap *map_b = &args.map_b[pi];
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(map);
+    tma_prefetch_desc(map_b);
+  }
   if (warp == 1) {
     tmem_alloc(&ctrl->tmem_base, GS_TMEM_COLS);
     tmem_relinquish();
@@ -290,7 +324,7 @@ __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS,
   WaitCtl ctl{&ctrl->abort_flag, args.err, args.timeout_ns};
   const int N = args.ns_steps;
   const int kchunks = (P.m + GS_KC - 1) / GS_KC;
-  constexpr uint32_t idesc = idesc_tf32_f32(GS_BLOCK, GS_BLOCK);
+  constexpr uint32_t idesc = idesc_bf16_f32(GS_BLOCK, GS_BLOCK, false, true);
 
   // pipeline state, carried across products and phases
   TileOut tout{out_tiles, map, 0, warp == 2 && lane == 0};
@@ -334,8 +368,15 @@ __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS,
               last_parity[stage] = static_cast<int>(sphase);
               tma_load_3d(st, map, &ctrl->full[stage], c * GS_KC, bi * GS_BLOCK, za);
               tma_load_3d(st + GS_TILE_BYTES, map, &ctrl->full[stage], c * GS_KC, bi * GS_BLOCK, za + P.K);
-              tma_load_3d(st + 2 * GS_TILE_BYTES, map, &ctrl->full[stage], c * GS_KC, bj * GS_BLOCK, zb);
-              tma_load_3d(st + 3 * GS_TILE_BYTES, map, &ctrl->full[stage], c * GS_KC, bj * GS_BLOCK, zb + P.K);
+              // right operand: rows c * 64 .. + 63, columns of block column bj, as two 64-column halves
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int x = bj * GS_BLOCK + 64 * h;
+                tma_load_3d(st + 2 * GS_TILE_BYTES + h * (GS_TILE_BYTES / 2), map_b, &ctrl->full[stage], x, c * GS_KC,
+                            zb);
+                tma_load_3d(st + 3 * GS_TILE_BYTES + h * (GS_TILE_BYTES / 2), map_b, &ctrl->full[stage], x, c * GS_KC,
+                            zb + P.K);
+              }
               if (++stage == GS_STAGES) {
                 stage = 0;
                 sphase ^= 1u;
@@ -362,14 +403,15 @@ __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS,
               const uint32_t a_lo = a_hi + GS_TILE_BYTES, b_hi = a_hi + 2 * GS_TILE_BYTES,
                              b_lo = a_hi + 3 * GS_TILE_BYTES;
 #pragma unroll
-              for (int kk = 0; kk < GS_KC / 8; ++kk) {
+              for (int kk = 0; kk < GS_KC / 16; ++kk) {
                 const uint64_t ah = smem_desc_sw128(a_hi + kk * 32, 16, 1024);
                 const uint64_t al = smem_desc_sw128(a_lo + kk * 32, 16, 1024);
-                const uint64_t bh = smem_desc_sw128(b_hi + kk * 32, 16, 1024);
-                const uint64_t bl = smem_desc_sw128(b_lo + kk * 32, 16, 1024);
-                tc_mma_tf32(d, ah, bh, idesc, (c | kk) != 0 ? 1u : 0u);
-                tc_mma_tf32(d, ah, bl, idesc, 1u);
-                tc_mma_tf32(d, al, bh, idesc, 1u);
+                // MN-major: 16 rows of 128 bytes per step; the second 64-column half 8 KB on
+                const uint64_t bh = smem_desc_sw128(b_hi + kk * 16 * 128, GS_TILE_BYTES / 2, 1024);
+                const uint64_t bl = smem_desc_sw128(b_lo + kk * 16 * 128, GS_TILE_BYTES / 2, 1024);
+                tc_mma_bf16(d, ah, bh, idesc, (c | kk) != 0 ? 1u : 0u);
+                tc_mma_bf16(d, ah, bl, idesc, 1u);
+                tc_mma_bf16(d, al, bh, idesc, 1u);
               }
               issued = true;
               tc_commit(&ctrl->empty[stage]);
@@ -398,13 +440,21 @@ __global__ void __cluster_dims__(GS_CLUSTER, 1, 1) __launch_bounds__(GS_THREADS,
           if (rec && q == 0 && warp == 2 && lane == 0) rec[5] = globaltimer_ns();
           tc_fence_after();
 #pragma unroll 1
-          for (int cc = 0; cc < GS_BLOCK / 32; ++cc) {
-            const int col0 = bj * GS_BLOCK + cc * 32;
+          for (int cc = 0; cc < GS_BLOCK / 64; ++cc) {
+            const int col0 = bj * GS_BLOCK + cc * 64;
             if (col0 >= P.mp) break;   // warp-uniform (columns m .. mp - 1: zero padding of [R_hi | R_lo] only)
-            float v[32];
-            tmem_ld_32x32b_x32(tmem + static_cast<uint32_t>(pr.acc * GS_BLOCK + cc * 32) +
-                                   (static_cast<uint32_t>(quarter * 32) << 16),
-                               v);
+            const uint32_t ta = tmem + static_cast<uint32_t>(pr.acc * GS_BLOCK + cc * 64) +
+                                (static_cast<uint32_t>(quarter * 32) << 16);
+            uint32_t r0[32], r1[32];
+            tmem_ld_32x32b_x32_async(ta, r0);
+            tmem_ld_32x32b_x32_async(ta + 32, r1);
+            tmem_ld_wait();
+            float v[64];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              v[j] = __uint_as_float(r0[j]);
+              v[32 + j] = __uint_as_float(r1[j]);
+            }
             epilogue_chunk(tout, P, pr, k, bi, quarter, lane, col0, t, N, args.coeffs, v, rstage);
           }
         }
@@ -464,7 +514,7 @@ EncodeTiledFn encode_fn() {
 
 size_t gram_space_plane_bytes(long long K, long long m) {
   return static_cast<size_t>(GS_BUFFERS) * 2 * static_cast<size_t>(K) * static_cast<size_t>(m) *
-             static_cast<size_t>(round8(m)) * 4 +
+             static_cast<size_t>(round8(m)) * 2 +
          static_cast<size_t>(K) * static_cast<size_t>(m) * static_cast<size_t>(2 * round64(m)) * 2;
 }
 
@@ -500,11 +550,15 @@ muon_status launch_gram_space(const GramSpaceStack *stacks, int n, int ns_steps,
       units += P.mb == 2 ? st.K : (st.K + GS_CLUSTER - 1) / GS_CLUSTER;
       cuuint64_t dims[3] = {static_cast<cuuint64_t>(st.m), static_cast<cuuint64_t>(st.m),
                             static_cast<cuuint64_t>(2 * GS_BUFFERS) * static_cast<cuuint64_t>(st.K)};
-      cuuint64_t strides[2] = {static_cast<cuuint64_t>(P.ldm) * 4,
-                               static_cast<cuuint64_t>(P.ldm) * static_cast<cuuint64_t>(st.m) * 4};
+      cuuint64_t strides[2] = {static_cast<cuuint64_t>(P.ldm) * 2,
+                               static_cast<cuuint64_t>(P.ldm) * static_cast<cuuint64_t>(st.m) * 2};
       cuuint32_t box[3] = {static_cast<cuuint32_t>(GS_KC), static_cast<cuuint32_t>(GS_BLOCK), 1u};
+      cuuint32_t box_b[3] = {64u, static_cast<cuuint32_t>(GS_KC), 1u};
       cuuint32_t estr[3] = {1u, 1u, 1u};
-      if (enc(&g.map[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, st.planes, dims, strides, box, estr,
+      if (enc(&g.map[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, st.planes, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+          enc(&g.map_b[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, st.planes, dims, strides, box_b, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return MUON_ERR_CUDA;

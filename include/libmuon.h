@@ -82,7 +82,7 @@ typedef struct {
  * matrix instead of per launch), which every call clears itself before its first launch; then K fp32
  * norm scales, per-tile norm partial sums, two bf16 iterates of (K, min, max) with rows
  * padded to a multiple of 8 elements, two bf16 (K, min, min) Gram buffers, and, for shapes that can take
- * the Gram-space path (muon_debug_gram_space), its fp32 scratch.
+ * the Gram-space path (muon_debug_gram_space), its scratch.
  * Returns 0 if K, A or B is not positive. */
 size_t muon_workspace_bytes(int64_t K, int64_t A, int64_t B);
 
@@ -142,7 +142,7 @@ muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hpar
  * workspace alone, and records in process-wide tables:
  *   1. the Newton-Schulz path of every bucket that can take the Gram-space chain (muon_gram_space_route):
  *      that bucket's chain timed each way, keyed by (min(A,B), max(A,B), K);
- *   1b. the number of contraction slices (1, 2, 3, 4, 6 or 8) of the Gram-space buckets' fp32 Gram launch,
+ *   1b. the number of contraction slices (1 to 4) of the Gram-space buckets' fp32 Gram launch,
  *      which has one tile pair per matrix: keyed by the launch's matrices and deepest contraction (see
  *      muon_autotune_gram_split);
  *   2. the poly step's pipeline shape (mainloop stages + epilogue input slots: 4 + 5, 5 + 3, 6 + 2) for the
@@ -174,7 +174,7 @@ int32_t muon_autotune_poly_shape(int64_t contraction);
 
 /* The recorded number of contraction slices for fp32 Gram launches of the Gram-space path holding `matrices`
  * matrices whose deepest contraction is `contraction` (the iterates' long side), or -1 if none is recorded.
- * Without an entry a launch takes the most slices (up to 8) that fit one wave of SM pairs while each slice
+ * Without an entry a launch takes the most slices (up to 4) that fit one wave of SM pairs while each slice
  * stays at least 1024 deep. */
 int32_t muon_autotune_gram_split(int64_t matrices, int64_t contraction);
 
@@ -330,18 +330,18 @@ muon_status muon_debug_poly_shape(int32_t shape);
  * for a wide iterate X_0 (m x n, m = min(A,B) <= n) the chain runs on m x m matrices, A_0 = X_0 X_0^T,
  * Q_t = a_t I + b_t A_t + c_t A_t^2, R_{t+1} = Q_t R_t, A_{t+1} = Q_t A_t Q_t, and X_N = R_N X_0 -- the same
  * result as the plain iteration, at O(m^3) instead of O(m^2 n) per step. A_0 is accumulated in fp32 from the
- * bf16 iterate; the m x m chain keeps fp32 accuracy (three tf32 tensor-core passes per product on hi / lo
- * splits); R_N is rounded to bf16 for the final product, which applies the parameter update as the plain
- * path's last step does.
+ * bf16 iterate; the m x m chain stores every matrix as a bf16 hi / lo pair (16 significant bits) and forms
+ * each product in three bf16 tensor-core passes accumulated in fp32; R_N goes to the final product as a bf16
+ * hi / lo pair too, and that product applies the parameter update as the plain path's last step does.
  * Shapes that can take it: m <= 256 and not the fused small-matrix kernel's (m <= 128 with n <= 256); their
- * workspace (muon_workspace_bytes) includes 40*K*m*round8(m) bytes of fp32 scratch for it.
+ * workspace (muon_workspace_bytes) includes 24*K*m*round8(m) + 4*K*m*round64(m) bytes of scratch for it.
  * muon_step_batched, muon_step_grouped, hybrid_step and ns_orthogonalize take it where
  * muon_gram_space_route says so: as measured by muon_autotune for that (m, n, K), else for n >= 4*m.
  * muon_debug_gram_space: -1 the default rule, 0 never, 1 for every shape that can take it (for tests and
  * measurements). MUON_ERR_INVALID_ARG for other values. */
 muon_status muon_debug_gram_space(int32_t mode);
 
-/* Forces the fp32 Gram of the Gram-space path into `split` contraction slices (1 .. 8, clipped per stack to
+/* Forces the fp32 Gram of the Gram-space path into `split` contraction slices (1 .. 4, clipped per stack to
  * its contraction) in every launch, or -1 to go back to the table and the rule; for tests and sweeps. The
  * slices are added in index order by a second kernel, so a given split always gives the same bits.
  * MUON_ERR_INVALID_ARG for other values. */
