@@ -7,7 +7,7 @@ different inputs, and check each result against the fp64 oracle's Newton-Schulz 
 ns_orthogonalize (which uses a caller-provided workspace), both within the tests' bound for
 orthogonalised outputs (relative Frobenius error 2e-2). The shapes cover the fused small-matrix range
 (where ns_orthogonalize runs another kernel), one stack above it (the same GEMM kernels on both sides),
-and a tall fp32 stack stored as bf16. They also check that a stack too large for the built-in scratch is
+a tall fp32 stack stored as bf16, and a wide stack that takes the Gram-space path. They also check that a stack too large for the built-in scratch is
 refused before anything runs, and that a bounded wait that runs out is reported by
 ns_orthogonalize_noalloc_check (and only once), with the context still usable afterwards.
 This file is collected last on purpose.
@@ -28,6 +28,7 @@ CASES = [
     ((3, 200, 72), torch.bfloat16, torch.bfloat16, 2),
     ((2, 512, 1024), torch.bfloat16, torch.float32, 3),     # above the fused small-matrix limit
     ((2, 640, 256), torch.float32, torch.bfloat16, 4),      # tall: transposed to wide and back
+    ((3, 128, 2048), torch.bfloat16, torch.bfloat16, 5),    # the Gram-space path, its fp32 Gram split
 ]
 
 
