@@ -120,24 +120,34 @@ class Workload:
             h.step = self.t
 
     def muon_part(self, stream=None, which=None):
-        """which: None for every bucket, else an index into the groups of split_buckets()."""
-        arr = self.bucket_array if which is None else self.groups[which]
+        """which: None for every bucket, else an index into the pieces of split_pieces()."""
+        arr = self.bucket_array if which is None else self.piece_arrays[which]
         self.L.muon_step_grouped(arr, self.hp, self.ws, stream)
 
-    def split_buckets(self):
-        """Splits the buckets into groups: a first one holding at most 40% of the gradient bytes (at least one
-        bucket), then one group per remaining bucket, so that a caller can start each group's chain as soon as
-        its gradients are in, and copy its parameters out while the next one runs. Grouping changes no
-        result: each bucket's tiles are computed the same way in any launch. Returns the bucket index lists."""
+    def split_pieces(self, max_bytes=1.5e9):
+        """Cuts the Muon buckets along K into pieces of at most max_bytes of gradients (at least one matrix), so
+        that a caller can start each piece's chain as soon as its gradients are in and copy its parameters out
+        while the next one runs. Every piece's copy is shorter than its compute, so the pieces go smallest
+        first (the order that keeps a two-stage copy-then-compute pipeline busy) and the AdamW pass, whose copy
+        is far longer than its compute, goes last. A piece is (bucket, k0, k1). Cutting and ordering change no
+        result: each matrix's chain is computed the same way in any launch. Returns the pieces in order."""
         L = self.L
-        total = sum(bk["g"].numel() for bk in self.buckets)
-        cut, acc = 1, self.buckets[0]["g"].numel()
-        while cut < len(self.buckets) - 1 and acc + self.buckets[cut]["g"].numel() <= 0.4 * total:
-            acc += self.buckets[cut]["g"].numel()
-            cut += 1
-        idx = [list(range(cut))] + [[i] for i in range(cut, len(self.buckets))]
-        self.groups = [L.make_buckets([self._spec(self.buckets[i]) for i in g]) for g in idx]
-        return idx
+        pieces = []
+        for b, bk in enumerate(self.buckets):
+            per = bk["A"] * bk["B"] * bk["g"].element_size()
+            n = min(bk["K"], max(1, -(-bk["K"] * per // int(max_bytes))))   # equal parts, none above max_bytes
+            cuts = [round(i * bk["K"] / n) for i in range(n + 1)]
+            pieces += [(b, cuts[i], cuts[i + 1]) for i in range(n)]
+        size = lambda pc: (pc[2] - pc[1]) * self.buckets[pc[0]]["A"] * self.buckets[pc[0]]["B"]
+        pieces.sort(key=size)   # stable: equal pieces keep bucket order
+        self.piece_arrays = []
+        for b, k0, k1 in pieces:
+            bk = self.buckets[b]
+            self.piece_arrays.append(L.make_buckets([(
+                L.pointer_array([bk["p"][k] for k in range(k0, k1)], self.device),
+                L.pointer_array([bk["g"][k] for k in range(k0, k1)], self.device),
+                bk["mom"][k0:k1], k1 - k0, bk["A"], bk["B"], L.MUON_BF16, L.MUON_BF16)]))
+        return pieces
 
     def adamw_part(self, stream=None):
         self.L.adamw_step_grouped(self.adamw_tensors, self.adamw_ws, stream)
@@ -159,7 +169,7 @@ class Workload:
         bytes_["adamw"] = self.w.adamw_elems * 22
         return flops, nominal, bytes_
 
-    # host <-> device views for the end-to-end leg: (gradient, parameter) device tensors per piece
+    # host <-> device views for the end-to-end leg: (gradient, parameter) device tensors, per bucket, then AdamW
     def host_views(self):
         dev_g = [bk["g"] for bk in self.buckets] + [self.adamw_flat["g"]]
         dev_p = [bk["p"] for bk in self.buckets] + [self.adamw_flat["p"]]
@@ -383,8 +393,8 @@ def _run_e2e(wl, args, stream, world, device, barrier):
     """The step through the C ABI with host buffers: every step, the gradients go in from pinned host memory
     and the updated parameters come back out, inside the timed region. The copies overlap the compute: the
     step runs as several calls on the compute stream, each started as soon as its inputs are in (the Muon
-    chain of the first bucket group, the AdamW pass, then the chain of each other bucket); inputs go in on one
-    copy stream in that order, and each call's parameters come out on a second copy stream once it is done."""
+    chains of the pieces of split_pieces(), smallest first, then the AdamW pass); inputs go in on one copy
+    stream in that order, and each call's parameters come out on a second copy stream once it is done."""
     import torch
     dev_g, dev_p = wl.host_views()
     h2d = sum(t.numel() * t.element_size() for t in dev_g)
@@ -418,9 +428,9 @@ def _run_e2e(wl, args, stream, world, device, barrier):
     d2h_gbs = nbytes / (c1.elapsed_time(c2) * 1e-3) / 1e9
     e2e_steps = max(3, args.steps // 4)
     nb = len(wl.buckets)
-    groups = wl.split_buckets()
-    pieces = [(groups[0], lambda: wl.muon_part(stream, 0)), ([nb], lambda: wl.adamw_part(stream))]
-    pieces += [(g, lambda k=k: wl.muon_part(stream, k)) for k, g in enumerate(groups) if k > 0]
+    # (tensor index, k0, k1) slices to copy, and the call, per piece; AdamW's flat tensors are index nb
+    pieces = [([(b, k0, k1)], lambda j=j: wl.muon_part(stream, j)) for j, (b, k0, k1) in enumerate(wl.split_pieces())]
+    pieces.append(([(nb, 0, None)], lambda: wl.adamw_part(stream)))
     copy_in, copy_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     ev_in = [torch.cuda.Event() for _ in pieces]
     ev_done = [torch.cuda.Event() for _ in pieces]
@@ -430,8 +440,8 @@ def _run_e2e(wl, args, stream, world, device, barrier):
     for _ in range(e2e_steps):
         with torch.cuda.stream(copy_in):
             for (idx, _), e in zip(pieces, ev_in):
-                for i in idx:
-                    dev_g[i].copy_(host_g[i], non_blocking=True)
+                for i, k0, k1 in idx:
+                    dev_g[i][k0:k1].copy_(host_g[i][k0:k1], non_blocking=True)
                 e.record(copy_in)
         wl.begin_step()
         for (_, run), ei, ed in zip(pieces, ev_in, ev_done):
@@ -441,8 +451,8 @@ def _run_e2e(wl, args, stream, world, device, barrier):
         with torch.cuda.stream(copy_out):
             for (idx, _), e in zip(pieces, ev_done):
                 copy_out.wait_event(e)
-                for i in idx:
-                    host_p[i].copy_(dev_p[i], non_blocking=True)
+                for i, k0, k1 in idx:
+                    host_p[i][k0:k1].copy_(dev_p[i][k0:k1], non_blocking=True)
         copy_out.synchronize()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(1e3 * (time.perf_counter() - t0) / e2e_steps, world, device)
