@@ -45,8 +45,8 @@ void debug_timeline(unsigned long long **buf, int *cap_per_cta);
 
 // ------------------------------------------------------------------------------------------ tensor-core GEMMs
 
-// EPI_GRAM32: the Gram matrix of a wide iterate with m <= 256 rows, stored in fp32 as a tf32 "hi" plane and
-// an fp32 "lo" plane (hi + lo = the value) for the Gram-space chain.
+// EPI_GRAM32: the Gram matrix of a wide iterate with m <= 256 rows, accumulated in fp32 and stored as a bf16 "hi"
+// plane (the value rounded) and a bf16 "lo" plane (the rest, rounded) for the Gram-space chain.
 enum EpiKind : int { EPI_GRAM = 0, EPI_POLY = 1, EPI_APPLY = 2, EPI_FINAL = 3, EPI_GRAM32 = 5 };
 
 constexpr int GEMM_MAX_PROBLEMS = 8;
@@ -317,7 +317,7 @@ inline size_t header_bytes(long long total_K) {
 // One stack's sections (1024-byte aligned): K fp32 scales, the norm pass's per-tile partial sums, two bf16
 // iterates (K, m, ldx) and two bf16 (K, m, ldg) buffers for G and H; m = min(A, B), n = max(A, B), rows padded
 // to a multiple of 8 elements (16 bytes, as TMA requires); then, for shapes that can take the Gram-space path,
-// its fp32 planes (gram_space_plane_bytes).
+// its scratch (gram_space_plane_bytes).
 struct Layout {
   long long m, n, ldx, ldg, tiles_r, tiles_c;
   size_t scale, partial, x0, x1, g, h, gs, total;   // gs: the Gram-space planes (shapes that can take that path)

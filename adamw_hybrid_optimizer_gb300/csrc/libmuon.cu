@@ -275,7 +275,7 @@ bool counter_deps_for(double est_us) {
 // Whether a stack of K wide m x n iterates takes the Gram-space path: never for shapes that cannot (m > 256, or
 // the fused small-matrix kernel's); else as forced by muon_debug_gram_space, else as measured by muon_autotune
 // for this (m, n, K), else where the long side is at least four times the short one, where the m x m chain
-// (about 4 m^3 flops per step in three tf32 passes) costs a fraction of the plain step's 4 m^2 n + 2 m^3.
+// (about 4 m^3 flops per step in three bf16 passes) costs a fraction of the plain step's 4 m^2 n + 2 m^3.
 std::mutex g_route_mu;
 std::map<std::vector<long long>, int> g_route_table;   // (m, n, K) -> measured: 1 Gram space, 0 plain chain
 

@@ -9,8 +9,9 @@
 //     X' = H X                      EPI_APPLY  (= a X + (b G + c G G) X); B operand X read N-major
 //     last step: u = H X, then p <- p - lr*wd*p*mask - lr*scale*u      EPI_FINAL (EPI_FINAL_MASTER: on fp32
 //                                                                      master copies of bf16 parameters)
-//     A_0 = s^2 X X^T for the Gram-space chain (m <= 256)  EPI_GRAM32  fp32 hi / lo planes of A_0 and of
-//                                                                      c_0 A_0 + b_0 I, whole tile stored
+//     A_0 = s^2 X X^T for the Gram-space chain (m <= 256)  EPI_GRAM32  bf16 hi / lo planes of A_0 and of
+//                                                                      c_0 A_0 + b_0 I, whole tile stored;
+//                                                                      or fp32 sums of contraction slices
 //
 // Design (sm_103a): CTAs run as pairs (clusters of two) on vertically adjacent 128 x 256 output tiles with
 // paired-SM MMAs (tcgen05 cta_group::2, M = 256): each CTA holds its 128 rows of A and one half of B, the
