@@ -132,14 +132,15 @@ int poly_shape_forced();
 
 // The fp32 Gram of the Gram-space path (EPI_GRAM32) has one tile pair per matrix, which leaves most SMs idle when
 // a launch holds fewer matrices than there are SM pairs. Its contraction (the iterate's long side) is then split
-// into up to GRAM32_MAX_SPLIT slices, each computed by a tile pair of its own. Without a measured choice the
-// launch takes the most slices that still fit one wave and keep each slice at least GRAM32_MIN_SLICE_K 64-deep
-// steps; the autotune table holds measured counts keyed by the launch's matrices and deepest contraction; a
-// forced count (-1: none) serves tests and sweeps. The count changes only the order of the fp32 additions.
+// into up to GRAM32_MAX_SPLIT slices, each computed by a tile pair of its own. The count is a property of the
+// stack, so that a stack gets the same bits in any launch it shares: the autotune table's measured count for
+// its (m, contraction steps, K), else the most slices that would fill one wave of SM pairs with this stack
+// alone while each slice keeps at least GRAM32_MIN_SLICE_K 64-deep steps; a forced count (-1: none) serves
+// tests and sweeps. The count changes only the order of the fp32 additions.
 constexpr int GRAM32_MAX_SPLIT = 4;
 constexpr int GRAM32_MIN_SLICE_K = 16;
-int gram_split_lookup(long long matrices, int k_iters);
-void gram_split_record(long long matrices, int k_iters, int split);
+int gram_split_lookup(long long m, int k_iters, long long K);
+void gram_split_record(long long m, int k_iters, long long K, int split);
 void gram_split_clear();
 int gram_split_forced();
 
@@ -177,9 +178,6 @@ class GemmBatch {
   // EPI_GRAM32 only: split every contraction into this many slices (clipped to what each problem allows), whatever
   // the table or the rule says (0: no override)
   void force_split(int split) { split_ = split; }
-  // EPI_GRAM32: the autotune table's keys (matrices, deepest contraction in 64-deep steps) of the launches that
-  // launch() would issue, in order
-  std::vector<std::pair<long long, int>> split_keys();
   muon_status add_final(const Bf16Stack &h, const Bf16Stack &x, const float *scale, const FinalSpec &f,
                        const TileSync *sync = nullptr, int k_wrap = 0);
   muon_status launch(cudaStream_t s);

@@ -1194,30 +1194,18 @@ muon_status launch_gram32_reduce(const Gram32ReduceGroup &g, long long blocks, c
   return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
 }
 
-// The slices of each EPI_GRAM32 problem of one launch (matrices in total, deepest contraction max_k): an
-// explicit count, else the measured one, else the most that fit one wave of SM pairs with slices at least
-// GRAM32_MIN_SLICE_K deep; clipped per problem to its scratch planes and its contraction, and evened out so
-// that no slice is empty. Sets ksplit, kper and the problem's tile pairs per matrix.
+// The slices of each EPI_GRAM32 problem: an explicit count, else the measured one for the stack, else the most
+// that would fill one wave of SM pairs with that stack alone while each slice keeps GRAM32_MIN_SLICE_K 64-deep
+// steps; clipped to the problem's scratch planes and contraction, and evened out so that no slice is empty.
+// Sets ksplit, kper and the problem's tile pairs per matrix. Depends on the problem alone.
 void choose_gram_split(GemmProblem *probs, int cnt, int forced) {
-  long long matrices = 0;
-  int max_k = 0;
-  for (int i = 0; i < cnt; ++i) {
-    matrices += probs[i].batch;
-    max_k = probs[i].k_iters > max_k ? probs[i].k_iters : max_k;
-  }
-  int want = forced > 0 ? forced : gram_split_forced();
-  bool rule = false;
-  if (want <= 0) want = gram_split_lookup(matrices, max_k);
-  if (want <= 0) {
-    rule = true;
-    const long long pairs = device_sm_count() / 2;
-    want = matrices > 0 ? static_cast<int>(pairs / matrices) : 1;
-  }
+  const long long pairs = device_sm_count() / 2;
   for (int i = 0; i < cnt; ++i) {
     GemmProblem &p = probs[i];
+    long long sp = forced > 0 ? forced : gram_split_forced();
+    if (sp <= 0) sp = gram_split_lookup(p.rows, p.k_iters, p.batch);
+    if (sp <= 0) sp = std::min<long long>(pairs / std::max(1, p.batch), p.k_iters / GRAM32_MIN_SLICE_K);
     const long long planes = p.gs_plane > 0 ? (p.gs_bprime / p.gs_plane - 2) / 2 : 0;   // two per slice
-    long long sp = want;
-    if (rule) sp = std::min<long long>(sp, p.k_iters / GRAM32_MIN_SLICE_K);
     sp = std::min<long long>({sp, GRAM32_MAX_SPLIT, planes, p.k_iters});
     if (sp < 1) sp = 1;
     p.kper = static_cast<int>((p.k_iters + sp - 1) / sp);
@@ -1379,23 +1367,6 @@ muon_status GemmBatch::add_final(const Bf16Stack &h, const Bf16Stack &x, const f
   it.p.lr_scale = f.lr_scale;
   set_sync(it.p, sync);
   return push(it);
-}
-
-std::vector<std::pair<long long, int>> GemmBatch::split_keys() {
-  order();
-  std::vector<std::pair<long long, int>> keys;
-  for (int first = 0; first < n_;) {
-    const int cnt = group_size(first);
-    long long matrices = 0;
-    int max_k = 0;
-    for (int i = first; i < first + cnt; ++i) {
-      matrices += items_[i].p.batch;
-      max_k = std::max(max_k, items_[i].p.k_iters);
-    }
-    keys.emplace_back(matrices, max_k);
-    first += cnt;
-  }
-  return keys;
 }
 
 int GemmBatch::group_size(int first) const {

@@ -90,7 +90,8 @@ SIGNATURES = {
     "muon_autotune_route": (ctypes.c_int32, [_c_int64, _c_int64, _c_int64]),
     "muon_autotune_scheduling": (ctypes.c_int32, [ctypes.POINTER(muon_bucket), ctypes.c_int]),
     "muon_autotune_poly_shape": (ctypes.c_int32, [_c_int64]),
-    "muon_autotune_gram_split": (ctypes.c_int32, [_c_int64, _c_int64]),
+    "muon_autotune_gram_split": (ctypes.c_int32, [_c_int64, _c_int64, _c_int64]),
+    "muon_debug_piece_elems": (ctypes.c_int, [_c_int64]),
     "muon_autotune_reset": (None, []),
     "muon_debug_gram_split": (ctypes.c_int, [ctypes.c_int32]),
     "muon_debug_poly_shape": (ctypes.c_int, [ctypes.c_int32]),
@@ -380,9 +381,14 @@ def muon_autotune_poly_shape(contraction: int) -> int:
     return int(lib().muon_autotune_poly_shape(int(contraction)))
 
 
-def muon_autotune_gram_split(matrices: int, contraction: int) -> int:
-    """The recorded contraction slices of a Gram-space fp32 Gram launch, or -1."""
-    return int(lib().muon_autotune_gram_split(int(matrices), int(contraction)))
+def muon_autotune_gram_split(K: int, A: int, B: int) -> int:
+    """The recorded contraction slices of the Gram-space fp32 Gram of a K x A x B stack, or -1."""
+    return int(lib().muon_autotune_gram_split(int(K), int(A), int(B)))
+
+
+def muon_debug_piece_elems(elems: int):
+    """Matrix elements per piece of every Muon call (0: the default)."""
+    _check(lib().muon_debug_piece_elems(int(elems)), "muon_debug_piece_elems")
 
 
 def muon_autotune_reset():

@@ -125,7 +125,11 @@ size_t muon_workspace_bytes_grouped(const muon_bucket *buckets, int n);
 /* One Muon step on n same-shape stacks at once, all with the same hyperparameters: the computation of
  * muon_step_batched on each bucket, with every Newton-Schulz step kind of all buckets issued as one
  * grouped tensor-core launch ([P4] section 2.2, batching matrices of similar shapes; [P1] the stacked
- * (K, ...) Muon groups). Results are identical to n muon_step_batched calls. Where the launches are short
+ * (K, ...) Muon groups). Results are identical to n muon_step_batched calls. The step runs in pieces of at
+ * most 512 Mi matrix elements (a larger bucket cut along K into equal slices, as muon_step_batched cuts it;
+ * smaller consecutive buckets packed into one piece), each piece's whole step before the next: with fewer
+ * matrices in flight, consecutive launches find more of their operands in L2 and the power-capped GPU runs
+ * faster (muon_debug_piece_elems). Where the launches are short
  * (muon_debug_counter_deps), each waits per matrix on counters in the workspace header that its
  * predecessor raises, rather than on the whole predecessor, so consecutive launches overlap; this
  * changes no result.
@@ -142,9 +146,9 @@ muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hpar
  * workspace alone, and records in process-wide tables:
  *   1. the Newton-Schulz path of every bucket that can take the Gram-space chain (muon_gram_space_route):
  *      that bucket's chain timed each way, keyed by (min(A,B), max(A,B), K);
- *   1b. the number of contraction slices (1 to 4) of the Gram-space buckets' fp32 Gram launch,
- *      which has one tile pair per matrix: keyed by the launch's matrices and deepest contraction (see
- *      muon_autotune_gram_split);
+ *   1b. the number of contraction slices (1 to 4) of the Gram-space buckets' fp32 Gram, which has one tile
+ *      pair per matrix: their fp32 Gram launch timed with each count, keyed by each bucket's
+ *      (min(A,B), max(A,B), K) (see muon_autotune_gram_split);
  *   2. the poly step's pipeline shape (mainloop stages + epilogue input slots: 4 + 5, 5 + 3, 6 + 2) for the
  *      plain buckets' grouped poly launch, keyed by its deepest contraction (without an entry, contractions
  *      up to 2048 take 4 + 5 and deeper ones 6 + 2);
@@ -172,11 +176,11 @@ int32_t muon_autotune_scheduling(const muon_bucket *buckets, int n);
  * `contraction` (the matrices' smaller dimension), or -1 if none is recorded. */
 int32_t muon_autotune_poly_shape(int64_t contraction);
 
-/* The recorded number of contraction slices for fp32 Gram launches of the Gram-space path holding `matrices`
- * matrices whose deepest contraction is `contraction` (the iterates' long side), or -1 if none is recorded.
- * Without an entry a launch takes the most slices (up to 4) that fit one wave of SM pairs while each slice
- * stays at least 1024 deep. */
-int32_t muon_autotune_gram_split(int64_t matrices, int64_t contraction);
+/* The recorded number of contraction slices of the Gram-space path's fp32 Gram for a stack of K matrices of
+ * A x B, or -1 if none is recorded. Without an entry a stack takes the most slices (up to 4) that would fill
+ * one wave of SM pairs with that stack alone while each slice stays at least 1024 deep. The count belongs to
+ * the stack, so a stack gets the same bits in any grouped launch and in a call of its own. */
+int32_t muon_autotune_gram_split(int64_t K, int64_t A, int64_t B);
 
 /* Empties the autotune tables. */
 void muon_autotune_reset(void);
@@ -340,6 +344,13 @@ muon_status muon_debug_poly_shape(int32_t shape);
  * muon_debug_gram_space: -1 the default rule, 0 never, 1 for every shape that can take it (for tests and
  * measurements). MUON_ERR_INVALID_ARG for other values. */
 muon_status muon_debug_gram_space(int32_t mode);
+
+/* Runs every Muon call's steps in pieces of at most `elems` matrix elements (a larger stack cut along K into
+ * equal slices, smaller consecutive buckets packed together), or the default (512 Mi elements) for 0. Each
+ * piece runs its whole step before the next starts; results are the same for any piece size (the fp32 Gram's
+ * slice count, which depends on a stack's K, aside: force it with muon_debug_gram_split to compare). For tests
+ * and measurements. MUON_ERR_INVALID_ARG for negative values. */
+muon_status muon_debug_piece_elems(int64_t elems);
 
 /* Forces the fp32 Gram of the Gram-space path into `split` contraction slices (1 .. 4, clipped per stack to
  * its contraction) in every launch, or -1 to go back to the table and the rule; for tests and sweeps. The

@@ -287,8 +287,10 @@ def test_autotune_entry_point_checks_and_table():
     assert lib.muon_debug_poly_shape(-2) == L.MUON_ERR_INVALID_ARG
     assert lib.muon_debug_poly_shape(1) == L.MUON_OK
     assert lib.muon_debug_poly_shape(-1) == L.MUON_OK
-    assert L.muon_autotune_gram_split(32, 16384) == -1
-    assert L.muon_autotune_gram_split(0, 16384) == -1 and L.muon_autotune_gram_split(32, 0) == -1
+    assert L.muon_autotune_gram_split(16, 256, 16384) == -1
+    assert L.muon_autotune_gram_split(0, 256, 16384) == -1 and L.muon_autotune_gram_split(16, 0, 16384) == -1
+    assert lib.muon_debug_piece_elems(-1) == L.MUON_ERR_INVALID_ARG
+    assert lib.muon_debug_piece_elems(1 << 20) == L.MUON_OK and lib.muon_debug_piece_elems(0) == L.MUON_OK
     for bad_split in (0, 5, -2):
         assert lib.muon_debug_gram_split(bad_split) == L.MUON_ERR_INVALID_ARG
     assert lib.muon_debug_gram_split(4) == L.MUON_OK

@@ -4,8 +4,8 @@ Grouping changes only which CTA computes which tile, never the arithmetic of a t
 equal, bit for bit, one muon_step_batched call per bucket on the same inputs (which the per-bucket tests
 compare with the oracle). Covered: the GPT-2-small set (4 buckets, one of them transposed), ten buckets
 of distinct ragged shapes with fp32 and bf16 parameters (more than one launch per step kind), eighteen
-buckets (more than one launch of the momentum/norm pass), and a workspace that another call with another
-layout used in between.
+buckets (more than one launch of the momentum/norm pass), a workspace that another call with another
+layout used in between, and steps cut into pieces of different sizes.
 """
 import numpy as np
 import pytest
@@ -167,3 +167,32 @@ def test_grouped_equals_per_bucket_with_every_path(L, deps):
     finally:
         L.muon_debug_counter_deps(-1)
     assert all(torch.isfinite(p.float()).all() for p in ps)
+
+
+@pytest.mark.parametrize("elems", [1, 300_000])
+def test_pieces_change_no_result(L, elems):
+    """Every call runs its step in pieces (muon_debug_piece_elems): with one matrix per piece (1), or with stacks
+    cut along K and small buckets packed together (300 000 elements), parameters equal the default's (one piece)
+    bit for bit on every path, grouped and per bucket alike, and so does ns_orthogonalize. The fp32 Gram's slice
+    count, which depends on a stack's K, is forced to 2 in both runs."""
+    shapes = [(3, 64, 128), (4, 256, 2048), (2, 2048, 200), (3, 512, 768), (5, 100, 1000)]
+    hp = workloads.workload("aspect").muon_hp
+    results, ns = {}, {}
+    gen = torch.Generator().manual_seed(12)
+    x = torch.randn((4, 256, 2048), generator=gen).to(torch.bfloat16).to(DEV)
+    L.muon_debug_gram_split(2)
+    try:
+        for e in (0, elems):
+            L.muon_debug_piece_elems(e)
+            results[e] = _run_both(L, shapes, torch.bfloat16, hp, seed=9)
+            out = torch.empty_like(x)
+            ws = torch.zeros(L.muon_workspace_bytes(4, 256, 2048), dtype=torch.uint8, device=DEV)
+            L.ns_orthogonalize(x, out, hp.coeffs, 1e-7, ws)
+            assert L.muon_check(ws) == L.MUON_OK
+            ns[e] = out
+    finally:
+        L.muon_debug_piece_elems(0)
+        L.muon_debug_gram_split(-1)
+    for a, b in zip(results[0], results[elems]):
+        assert torch.equal(a, b)
+    assert torch.equal(ns[0], ns[elems])
