@@ -1058,14 +1058,24 @@ int32_t muon_autotune_route(int64_t K, int64_t A, int64_t B) {
 int32_t muon_autotune_scheduling(const muon_bucket *buckets, int n) {
   using namespace muon_grouped_detail;
   if (buckets == nullptr || n < 1 || n > 4096) return -1;
-  std::vector<long long> sig;
-  for (int i = 0; i < n; ++i) {
-    const long long m = std::min(buckets[i].A, buckets[i].B), nn = std::max(buckets[i].A, buckets[i].B);
-    if (buckets[i].K < 1 || m < 1) return -1;
-    if (ns_small_fits(m, nn) || gram_space_route(m, nn, buckets[i].K)) continue;
-    sig.insert(sig.end(), {m, nn, static_cast<long long>(buckets[i].K)});
+  for (int i = 0; i < n; ++i)
+    if (buckets[i].K < 1 || buckets[i].A < 1 || buckets[i].B < 1) return -1;
+  // the step's pieces: the record of each piece that has a plain chain
+  int found = -3;   // none seen yet
+  for (const auto &piece : grouped_pieces(buckets, n)) {
+    std::vector<long long> sig;
+    for (const muon_bucket &b : piece) {
+      const long long m = std::min(b.A, b.B), nn = std::max(b.A, b.B);
+      if (ns_small_fits(m, nn) || gram_space_route(m, nn, b.K)) continue;
+      sig.insert(sig.end(), {m, nn, static_cast<long long>(b.K)});
+    }
+    if (sig.empty()) continue;
+    const int r = deps_lookup(sig);
+    if (r < 0) return -1;
+    if (found == -3) found = r;
+    else if (found != r) return 2;
   }
-  return deps_lookup(sig);
+  return found == -3 ? -1 : found;
 }
 
 int32_t muon_autotune_poly_shape(int64_t contraction) {

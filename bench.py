@@ -509,7 +509,8 @@ def run_ours(args):
         L.muon_autotune(wl.bucket_array, wl.hp, wl.ws)
     ms_ = sorted({min(bk["A"], bk["B"]) for bk in wl.buckets})
     poly_shape = {m: {0: "4+5", 1: "5+3", 2: "6+2"}.get(L.muon_autotune_poly_shape(m), "rule") for m in ms_}
-    sched = {0: "launch order", 1: "per-matrix counters"}.get(L.muon_autotune_scheduling(wl.bucket_array), "rule")
+    sched = {0: "launch order", 1: "per-matrix counters", 2: "per piece"}.get(
+        L.muon_autotune_scheduling(wl.bucket_array), "rule")
 
     def barrier():
         if world > 1:

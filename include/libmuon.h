@@ -169,7 +169,9 @@ muon_status muon_autotune(const muon_bucket *buckets, int n, const muon_hparams 
 /* The recorded path of K matrices of A x B: 1 Gram space, 0 plain chain, -1 none recorded. */
 int32_t muon_autotune_route(int64_t K, int64_t A, int64_t B);
 
-/* The recorded scheduling of these buckets' plain chain: 1 per-matrix counters, 0 launch order, -1 none. */
+/* The recorded scheduling of these buckets' plain chain, as a grouped step runs them (in pieces): 1 per-matrix
+ * counters, 0 launch order, for every piece with a plain chain; 2 if the pieces' records differ; -1 if a piece
+ * has none (or no bucket takes the plain chain). */
 int32_t muon_autotune_scheduling(const muon_bucket *buckets, int n);
 
 /* The recorded poly shape (0: 4 + 5, 1: 5 + 3, 2: 6 + 2) for launches whose deepest contraction is
