@@ -737,6 +737,20 @@ float median_time(F fn, cudaStream_t s, muon_status *st) {
   return t[REPS / 2];
 }
 
+// Every timed run of the autotune works on the workspace alone: the chains start from whatever iterate x0 holds
+// (no norm pass, so parameters, gradients and momentum are not read) and the final step writes a dense bf16
+// output into an iterate buffer the chain no longer reads, instead of updating parameters. Times do not depend
+// on the values. This sets a stack up that way for its current path (call again after changing the path).
+void timing_final(ChainStack &c, int ns_steps) {
+  c.norm_done = 0;
+  c.fin = FinalSpec{};
+  c.fin.dtype = MUON_BF16;
+  c.fin.orig_cols = static_cast<int>(c.L.n);
+  // plain chain: the final step reads iterate (N - 1) & 1; the Gram-space and small paths read only x0
+  const bool x0_free = c.path == PATH_PLAIN && ((ns_steps - 1) & 1) == 1;
+  c.fin.out_dense = c.w + (x0_free ? c.L.x0 : c.L.x1);
+}
+
 }  // namespace muon_grouped_detail
 
 extern "C" {
@@ -898,12 +912,58 @@ muon_status muon_autotune(const muon_bucket *buckets, int n, const muon_hparams 
   if ((st = check_device()) != MUON_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the pieces the step runs (grouped_pieces), each measured once per distinct (A, B, K) list
+  const auto pieces = grouped_pieces(buckets, n);
   std::set<std::vector<long long>> seen;
-  for (const auto &piece : grouped_pieces(buckets, n)) {
+  for (const auto &piece : pieces) {
     std::vector<long long> sig;
     for (const muon_bucket &b : piece) sig.insert(sig.end(), {b.A, b.B, b.K});
     if (!seen.insert(sig).second) continue;
     if ((st = autotune_piece(piece.data(), static_cast<int>(piece.size()), hp, ws, s)) != MUON_OK) return st;
+  }
+  // 3. the plain chain's scheduling, per-matrix counters or launch order, for a step that runs as one piece: its
+  // chains timed each way. A step of several pieces keeps the rule: the timed runs leave out the norm pass (they
+  // may not read the state), and on the Llama-3-8B set they found the counters faster, by piece and over every
+  // piece in turn, while the real step, whose first Gram launches then overlap the norm pass at the power cap,
+  // was 2% slower with them.
+  if (g_counter_deps.load() < 0 && pieces.size() == 1) {
+    char *base = static_cast<char *>(ws);
+    uint32_t *err = reinterpret_cast<uint32_t *>(base);
+    unsigned *counters = reinterpret_cast<unsigned *>(base + CTRL_BYTES);
+    const int N = hp->ns_steps;
+    std::vector<std::vector<ChainStack>> sets;
+    std::vector<long long> ks;
+    bool any_plain = false;
+    for (const auto &piece : pieces) {
+      long long tk = 0;
+      sets.push_back(chain_stacks(piece.data(), static_cast<int>(piece.size()), hp, base, &tk));
+      ks.push_back(tk);
+      for (ChainStack &c : sets.back()) {
+        timing_final(c, N);
+        any_plain = any_plain || c.path == PATH_PLAIN;
+      }
+    }
+    if (any_plain) {
+      float t_mode[2];
+      for (int deps = 0; deps < 2; ++deps) {
+        t_mode[deps] = median_time(
+            [&]() -> muon_status {
+              for (size_t i = 0; i < sets.size(); ++i) {
+                muon_status r = launch_counter_reset(counters, 4 * ks[i], s);
+                if (r != MUON_OK) return r;
+                ChainCall cc{err, counters, ks[i], N, hp->coeffs, false, deps};
+                if ((r = issue_chains(sets[i], cc, s)) != MUON_OK) return r;
+              }
+              return MUON_OK;
+            },
+            s, &st);
+        if (st != MUON_OK) return st;
+      }
+      std::lock_guard<std::mutex> lk(g_sched_mu);
+      for (const auto &set : sets) {
+        const auto sig = plain_signature(set);
+        if (!sig.empty()) g_deps_table[sig] = t_mode[1] < t_mode[0] ? 1 : 0;
+      }
+    }
   }
   return muon_check(ws, stream) == MUON_ERR_TIMEOUT ? MUON_ERR_TIMEOUT : MUON_OK;
 }
@@ -921,20 +981,8 @@ static muon_status autotune_piece(const muon_bucket *buckets, int n, const muon_
   long long total_K = 0;
   std::vector<ChainStack> cs = chain_stacks(buckets, n, hp, base, &total_K);
   const int N = hp->ns_steps;
-  // Every timed run works on the workspace alone: the chains start from whatever iterate x0 holds (no norm pass,
-  // so parameters, gradients and momentum are not read) and the final step writes a dense bf16 output into an
-  // iterate buffer the chain no longer reads, instead of updating parameters. Times do not depend on the values.
-  for (ChainStack &c : cs) {
-    c.norm_done = 0;
-    c.fin = FinalSpec{};
-    c.fin.dtype = MUON_BF16;
-    c.fin.orig_cols = static_cast<int>(c.L.n);
-  }
-  auto dense_out = [&](ChainStack &c) {
-    // plain chain: the final step reads iterate (N - 1) & 1; the Gram-space and small paths read only x0
-    const bool x0_free = c.path == PATH_PLAIN && ((N - 1) & 1) == 1;
-    c.fin.out_dense = c.w + (x0_free ? c.L.x0 : c.L.x1);
-  };
+  for (ChainStack &c : cs) timing_final(c, N);
+  auto dense_out = [&](ChainStack &c) { timing_final(c, N); };
   auto run = [&](std::vector<ChainStack> &set, int deps) -> muon_status {
     muon_status r = launch_counter_reset(counters, 4 * total_K, s);
     if (r != MUON_OK) return r;
@@ -1032,16 +1080,6 @@ static muon_status autotune_piece(const muon_bucket *buckets, int n, const muon_
       }
     }
     poly_shape_record(max_k, best);
-  }
-  // 3. the plain chain's scheduling: per-matrix counters or launch order, for the whole set as it will run
-  if (any_plain && g_counter_deps.load() < 0) {
-    float t_mode[2];
-    for (int deps = 0; deps < 2; ++deps) {
-      t_mode[deps] = median_time([&] { return run(cs, deps); }, s, &st);
-      if (st != MUON_OK) return st;
-    }
-    std::lock_guard<std::mutex> lk(g_sched_mu);
-    g_deps_table[plain_signature(cs)] = t_mode[1] < t_mode[0] ? 1 : 0;
   }
   return MUON_OK;
 }

@@ -152,8 +152,9 @@ muon_status muon_step_grouped(const muon_bucket *buckets, int n, const muon_hpar
  *   2. the poly step's pipeline shape (mainloop stages + epilogue input slots: 4 + 5, 5 + 3, 6 + 2) for the
  *      plain buckets' grouped poly launch, keyed by its deepest contraction (without an entry, contractions
  *      up to 2048 take 4 + 5 and deeper ones 6 + 2);
- *   3. the plain chain's scheduling (per-matrix readiness counters or launch order), the whole set timed
- *      each way, keyed by the plain buckets' shapes and counts.
+ *   3. the plain chain's scheduling (per-matrix readiness counters or launch order) of a step that runs as one
+ *      piece: its chains timed each way, keyed by the plain buckets' shapes and counts (a step of several pieces
+ *      keeps the rule). Steps 1, 1b and 2 measure each distinct piece on its own.
  * Each candidate runs once as a warm-up and five times timed (median). Later calls use the recorded choices
  * unless a debug switch forces one. The shapes and the scheduling never change a result; the slice count
  * changes only the order of the Gram's fp32 additions; the path changes the arithmetic (both paths are
