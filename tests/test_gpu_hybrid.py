@@ -219,3 +219,32 @@ def test_hybrid_gpt2_small_full_size(L):
     for t, u in zip(m_got, m_ref):
         assert torch.equal(t[0], u[0]) and torch.equal(t[2], u[2])
     _assert_same(a_got, a_ref, "gpt2s adamw")
+
+
+def test_hybrid_in_pieces(L):
+    """hybrid_step with its Muon step cut into pieces of one matrix each (muon_debug_piece_elems): the AdamW pass's
+    counters are cleared with the first piece's, and every result equals the uncut step's bit for bit."""
+    hp = hp_struct(L, workloads.workload("gpt2s").muon_hp)
+    a_specs = [(1_000_003, torch.bfloat16, torch.bfloat16, False, 0), (5000, torch.float32, torch.float32, False, 0)]
+    runs = []
+    try:
+        for elems in (0, 1):
+            L.muon_debug_piece_elems(elems)
+            mset = _muon_set(L, SHAPES, 21)
+            aset = _tensor_set(22, a_specs)
+            bk = _buckets(L, mset, SHAPES)
+            ws = torch.zeros(L.muon_workspace_bytes_grouped(bk), dtype=torch.uint8, device=DEV)
+            aws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+            for step in (1, 2):
+                hps = _hps(L, step, len(a_specs))
+                arr = L.make_adamw_tensors([(p, g, m, v, h) + ((ms,) if ms is not None else ())
+                                            for (p, g, m, v, ms), h in zip(aset, hps)])
+                L.hybrid_step(bk, hp, ws, arr, aws)
+            torch.cuda.synchronize()
+            assert L.muon_check(ws) == L.MUON_OK
+            runs.append((mset, aset))
+    finally:
+        L.muon_debug_piece_elems(0)
+    (m0, a0), (m1, a1) = runs
+    assert all(torch.equal(x, y) for t, u in zip(m0, m1) for x, y in zip(t, u))
+    _assert_same(a1, a0, "adamw in pieces")

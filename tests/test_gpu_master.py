@@ -6,7 +6,7 @@ budget": fp32 master weights beside bf16 weights). The oracle is the fp32-parame
 master; the bf16 parameter must equal the GPU's master rounded to bf16, bit for bit, after every step.
 Wide and tall (transposed path) ragged stacks, two steps, on the plain chain and (200 x 1000 and its
 transpose) on the Gram-space path, whose final step is the same master-weight kernel with the [R_hi | R_lo]
-operand.
+operand; and a step cut into pieces of one matrix each, against the uncut step.
 """
 import numpy as np
 import pytest
@@ -56,3 +56,43 @@ def test_muon_fp32_master_two_steps(L, shape):
             assert torch.equal(params[k], master[k].to(torch.bfloat16)), (step, k)
             assert np.all(np.abs(f64(mom[k]) - mref) <= 1e-6 * (np.abs(mref) + np.abs(g)) + 1e-30)
 
+
+
+def test_master_weights_in_pieces(L):
+    """A grouped step cut into pieces of one matrix each (muon_debug_piece_elems) gives the masters and the bf16
+    parameters of the uncut step bit for bit, on the plain and the Gram-space paths (the fp32 Gram's slice count
+    forced, since it depends on a stack's K)."""
+    hp = hp_struct(L, workloads.workload("tiny").muon_hp)
+    shapes = [(3, 136, 264), (3, 200, 1000)]
+    gen = torch.Generator().manual_seed(31)
+    base = []
+    for K, A, B in shapes:
+        master = (torch.randn((K, A, B), generator=gen) * 0.05).to(DEV)
+        grad = (torch.randn((K, A, B), generator=gen) * 1e-3).to(torch.bfloat16).to(DEV)
+        base.append((master, grad))
+    results = {}
+    L.muon_debug_gram_split(2)
+    try:
+        for elems in (0, 1):
+            L.muon_debug_piece_elems(elems)
+            specs, keep = [], []
+            for (K, A, B), (m0, g) in zip(shapes, base):
+                master = m0.clone()
+                params = master.to(torch.bfloat16)
+                mom = torch.zeros((K, A, B), dtype=torch.float32, device=DEV)
+                keep.append((master, params, mom))
+                specs.append((L.pointer_array([params[k] for k in range(K)], DEV),
+                              L.pointer_array([g[k] for k in range(K)], DEV), mom, K, A, B, L.MUON_BF16, L.MUON_BF16,
+                              L.pointer_array([master[k] for k in range(K)], DEV)))
+            bk = L.make_buckets(specs)
+            ws = torch.zeros(L.muon_workspace_bytes_grouped(bk), dtype=torch.uint8, device=DEV)
+            for _ in range(2):
+                L.muon_step_grouped(bk, hp, ws)
+            assert L.muon_check(ws) == L.MUON_OK
+            results[elems] = keep
+    finally:
+        L.muon_debug_piece_elems(0)
+        L.muon_debug_gram_split(-1)
+    for a, b in zip(results[0], results[1]):
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
