@@ -18,7 +18,9 @@
 // even CTA issues the MMAs, and each CTA's tensor memory receives its own 128 accumulator rows (2 x 256
 // fp32 columns, so the epilogue of one tile overlaps the MMAs of the next). Operands arrive by TMA
 // (128-byte swizzle) through a ring of 64-deep stages of 32 KB per CTA (6 stages; POLY in three splits of
-// stages and epilogue input slots, picked by a measured autotune or by the contraction depth). The CTAs are
+// stages and epilogue input slots, picked by a measured autotune or by the contraction depth; EPI_GRAM32, whose
+// one tile pair per matrix lies on the diagonal, reads B from its A tile and keeps 12 A-only stages of 16 KB,
+// and may split its contraction into slices that a small reduce kernel adds in order). The CTAs are
 // persistent (one per SM) and stride over the tiles of up to GEMM_MAX_PROBLEMS stacks at once. Warp roles:
 // warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner), warps 2-9 = epilogue (two per
 // tensor-memory lane quarter, each taking one 32-column half of every 64-column slot), warp 10 = loader
