@@ -157,6 +157,9 @@ struct TileSync {
 // The signals one launch of this step kind adds to a matrix's counter (every CTA's epilogue warps, once
 // per tile) for a wide iterate of m rows and n columns.
 uint32_t gemm_signals_per_matrix(int epi, long long m, long long n);
+// The 256 x 256 tile pairs one launch of this step kind computes per matrix (symmetric kinds: on or above
+// the diagonal only).
+long long gemm_tiles_per_matrix(int epi, long long m, long long n);
 
 class GemmBatch {
  public:

@@ -260,7 +260,7 @@ SmallNsArgs small_args(uint32_t *err, char *ws, const Layout &L, long long K, in
 // tile pair (the measured mainloop rate), spread over the clusters.
 double launch_estimate_us(int kind, long long m, long long n, long long K) {
   const long long k = (kind == EPI_GRAM ? n + 63 : m + 63) / 64;
-  const double pairs = static_cast<double>(K) * gemm_signals_per_matrix(kind, m, n) / (2 * 8);
+  const double pairs = static_cast<double>(K) * gemm_tiles_per_matrix(kind, m, n);
   return pairs * static_cast<double>(k) * 0.33 / std::max(1, device_sm_count() / 2);
 }
 

@@ -1259,11 +1259,15 @@ void set_sync(GemmProblem &p, const TileSync *sync) {
 }
 }  // namespace
 
-uint32_t gemm_signals_per_matrix(int epi, long long m, long long n) {
+long long gemm_tiles_per_matrix(int epi, long long m, long long n) {
   GemmProblem p{};
   const bool symmetric = epi == EPI_GRAM || epi == EPI_POLY;
   fill_tiles(p, 1, m, symmetric ? m : n, symmetric ? n : m, symmetric);
-  return static_cast<uint32_t>(p.tiles_per_matrix) * 2u * EPI_WARPS;
+  return p.tiles_per_matrix;
+}
+
+uint32_t gemm_signals_per_matrix(int epi, long long m, long long n) {
+  return static_cast<uint32_t>(gemm_tiles_per_matrix(epi, m, n)) * 2u * EPI_WARPS;
 }
 
 muon_status GemmBatch::push(const Item &it) {
