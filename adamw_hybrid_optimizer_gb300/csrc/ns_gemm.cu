@@ -724,6 +724,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
             mbar_arrive_expect_tx(&ctrl->full[stage], 2 * SB);
             last_parity[stage] = static_cast<int>(phase);
           }
+          if (rec && kk == k0) rec[9] = globaltimer_ns();
           const uint32_t fb = leader_full0 + stage * static_cast<uint32_t>(sizeof(uint64_t));
           uint8_t *sa = smem + stage * SB;
           uint8_t *sb = sa + A_BYTES;

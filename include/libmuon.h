@@ -377,9 +377,9 @@ muon_status muon_debug_counter_deps(int32_t on);
 muon_status muon_debug_wait_timeout(void *ws, size_t ws_bytes, uint64_t timeout_ns, muon_stream_t stream);
 
 /* Performance analysis: while a buffer is registered, the tensor-core launches that follow write, per CTA
- * and per tile they process (up to records_per_cta), ten 64-bit words: tile index, producer first and last
- * copy issue, MMA start (accumulator free), first and last operands ready, last MMA commit, epilogue start
- * and end (globaltimer nanoseconds; 0 = not reached). The buffer is cut into regions of (SM count) *
+ * and per tile they process (up to records_per_cta), ten 64-bit words: tile index, producer start (before
+ * its waits) and last copy issue, MMA start (accumulator free), first and last operands ready, last MMA
+ * commit, epilogue start and end, producer first copy issue (globaltimer nanoseconds; 0 = not reached). The buffer is cut into regions of (SM count) *
  * records_per_cta * 10 words; the i-th launch after registration fills region i (record r of CTA c at word
  * (c * records_per_cta + r) * 10 of it) and launches beyond the last region record nothing.
  * buf: device memory, zero-filled by the caller. buf = NULL unregisters. Returns MUON_ERR_WORKSPACE if the
