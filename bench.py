@@ -127,10 +127,15 @@ class Workload:
     def split_pieces(self, max_bytes=1.5e9):
         """Cuts the Muon buckets along K into pieces of at most max_bytes of gradients (at least one matrix), so
         that a caller can start each piece's chain as soon as its gradients are in and copy its parameters out
-        while the next one runs. Every piece's copy is shorter than its compute, so the pieces go smallest
-        first (the order that keeps a two-stage copy-then-compute pipeline busy) and the AdamW pass, whose copy
-        is far longer than its compute, goes last. A piece is (bucket, k0, k1). Cutting and ordering change no
-        result: each matrix's chain is computed the same way in any launch. Returns the pieces in order."""
+        while the next one runs. A Muon piece computes longer than its copies take, the AdamW pass far shorter,
+        so the order keeps the three streams (copy in, compute, copy out) busy with little waiting at either
+        end: the smallest piece first, in two halves (the first compute waits for half of it only), the AdamW
+        pass after the next piece (Muon chains on both sides hide its copies), the rest by size, and the
+        largest piece last, cut into parts that halve down to one matrix (each part's compute covers the
+        previous part's copy out, so what is left after the last compute is one matrix's copy). Cutting and
+        ordering change no result: each matrix's chain is computed the same way in any launch. Returns
+        (pieces, adamw_at): the (bucket, k0, k1) pieces in order, and the index in that order before which
+        the AdamW pass runs."""
         L = self.L
         pieces = []
         for b, bk in enumerate(self.buckets):
@@ -140,14 +145,26 @@ class Workload:
             pieces += [(b, cuts[i], cuts[i + 1]) for i in range(n)]
         size = lambda pc: (pc[2] - pc[1]) * self.buckets[pc[0]]["A"] * self.buckets[pc[0]]["B"]
         pieces.sort(key=size)   # stable: equal pieces keep bucket order
+        b, k0, k1 = pieces.pop(0)
+        head = [(b, k0, (k0 + k1 + 1) // 2), (b, (k0 + k1 + 1) // 2, k1)] if k1 - k0 > 1 else [(b, k0, k1)]
+        tail = []
+        if pieces:
+            b, k0, k1 = pieces.pop()
+            while k1 - k0 > 1:
+                k = k0 + (k1 - k0 + 1) // 2
+                tail.append((b, k0, k))
+                k0 = k
+            tail.append((b, k0, k1))
+        order = head + pieces + tail
+        adamw_at = min(len(order), len(head) + 1)
         self.piece_arrays = []
-        for b, k0, k1 in pieces:
+        for b, k0, k1 in order:
             bk = self.buckets[b]
             self.piece_arrays.append(L.make_buckets([(
                 L.pointer_array([bk["p"][k] for k in range(k0, k1)], self.device),
                 L.pointer_array([bk["g"][k] for k in range(k0, k1)], self.device),
                 bk["mom"][k0:k1], k1 - k0, bk["A"], bk["B"], L.MUON_BF16, L.MUON_BF16)]))
-        return pieces
+        return order, adamw_at
 
     def adamw_part(self, stream=None):
         self.L.adamw_step_grouped(self.adamw_tensors, self.adamw_ws, stream)
@@ -393,8 +410,9 @@ def _run_e2e(wl, args, stream, world, device, barrier):
     """The step through the C ABI with host buffers: every step, the gradients go in from pinned host memory
     and the updated parameters come back out, inside the timed region. The copies overlap the compute: the
     step runs as several calls on the compute stream, each started as soon as its inputs are in (the Muon
-    chains of the pieces of split_pieces(), smallest first, then the AdamW pass); inputs go in on one copy
-    stream in that order, and each call's parameters come out on a second copy stream once it is done."""
+    chains of the pieces of split_pieces() with the AdamW pass among them, in the order it gives); inputs go in
+    on one copy stream in that order, and each call's parameters come out on a second copy stream once it is
+    done."""
     import torch
     dev_g, dev_p = wl.host_views()
     h2d = sum(t.numel() * t.element_size() for t in dev_g)
@@ -429,8 +447,9 @@ def _run_e2e(wl, args, stream, world, device, barrier):
     e2e_steps = max(3, args.steps // 4)
     nb = len(wl.buckets)
     # (tensor index, k0, k1) slices to copy, and the call, per piece; AdamW's flat tensors are index nb
-    pieces = [([(b, k0, k1)], lambda j=j: wl.muon_part(stream, j)) for j, (b, k0, k1) in enumerate(wl.split_pieces())]
-    pieces.append(([(nb, 0, None)], lambda: wl.adamw_part(stream)))
+    order, adamw_at = wl.split_pieces()
+    pieces = [([(b, k0, k1)], lambda j=j: wl.muon_part(stream, j)) for j, (b, k0, k1) in enumerate(order)]
+    pieces.insert(adamw_at, ([(nb, 0, None)], lambda: wl.adamw_part(stream)))
     copy_in, copy_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     ev_in = [torch.cuda.Event() for _ in pieces]
     ev_done = [torch.cuda.Event() for _ in pieces]
