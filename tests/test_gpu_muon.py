@@ -190,7 +190,8 @@ def test_tiny_set_three_steps(L):
     _run_bucket(L, w, (64, 128), list(range(4)), w.steps)
 
 
-@pytest.mark.parametrize("variant", ["no_nesterov", "cautious_big_wd", "scale_mode_1", "tall"])
+@pytest.mark.parametrize("variant", ["no_nesterov", "cautious_big_wd", "scale_mode_1", "tall", "tall_ragged",
+                                     "tall_ragged_vec"])
 def test_step_variants(L, variant):
     import dataclasses
     w = workloads.workload("tiny")
@@ -209,6 +210,13 @@ def test_step_variants(L, variant):
     elif variant == "tall":
         w = dataclasses.replace(w, muon=tuple(workloads.MuonTensor(f"t{i}", (128, 64)) for i in range(4)))
         shape = (128, 64)
+    elif variant.startswith("tall_ragged"):
+        # momentum on a stack stored tall, its norm pass's 64 x 64 transposed tiles cut ragged on both sides:
+        # 258 columns (not a multiple of 4: scalar loads) or 260 (vector loads, a 4-column last tile)
+        shape = (333, 258) if variant == "tall_ragged" else (200, 260)
+        w = dataclasses.replace(w, muon=tuple(workloads.MuonTensor(f"t{i}", shape) for i in range(3)))
+        _run_bucket(L, w, shape, list(range(3)), 2, hp=hp)
+        return
     _run_bucket(L, w, shape, list(range(4)), 3, hp=hp)
 
 
