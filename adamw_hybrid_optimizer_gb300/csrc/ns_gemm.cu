@@ -137,11 +137,15 @@ __device__ __forceinline__ int find_problem(const GemmGroup &g, long long t) {
 // stores nothing.
 __device__ __forceinline__ void decode_tile(const GemmProblem &a, int symmetric, long long t, uint32_t rank, int &b,
                                             int &ti, int &tj) {
-  b = static_cast<int>(t / a.tiles_per_matrix);
-  int r = static_cast<int>(t - static_cast<long long>(b) * a.tiles_per_matrix);
+  // a problem's tile pairs number below 2^31 (checked at launch): 32-bit divisions, which take a fraction of the
+  // 64-bit ones' instructions on the producer's path between two tiles
+  const uint32_t tl = static_cast<uint32_t>(t);
+  const uint32_t tpm = static_cast<uint32_t>(a.tiles_per_matrix);
+  b = static_cast<int>(tl / tpm);
+  int r = static_cast<int>(tl - static_cast<uint32_t>(b) * tpm);
   if (!symmetric) {
-    if (a.ksplit > 1) r %= a.tiles_per_matrix / a.ksplit;   // the slice index is tile_k_range's
-    tj = r / a.m_pairs;
+    if (a.ksplit > 1) r = static_cast<int>(static_cast<uint32_t>(r) % (tpm / static_cast<uint32_t>(a.ksplit)));
+    tj = static_cast<int>(static_cast<uint32_t>(r) / static_cast<uint32_t>(a.m_pairs));
     ti = 2 * (r - tj * a.m_pairs) + static_cast<int>(rank);
     return;
   }
@@ -169,7 +173,7 @@ __device__ __forceinline__ int tile_k_range(const GemmProblem &a, long long t, i
     return 0;
   }
   const int per_slice = a.tiles_per_matrix / a.ksplit;
-  const int r = static_cast<int>(t % a.tiles_per_matrix);
+  const int r = static_cast<int>(static_cast<uint32_t>(t) % static_cast<uint32_t>(a.tiles_per_matrix));
   const int slice = a.ksplit - 1 - r / per_slice;
   k0 = slice * a.kper;
   k1 = min(a.k_iters, k0 + a.kper);
@@ -1418,7 +1422,9 @@ muon_status GemmBatch::launch(cudaStream_t s) {
       g.map_a[i] = items_[first + i].ma;
       g.map_b[i] = items_[first + i].mb;
       g.prob[i].tile_begin = tiles;
-      tiles += static_cast<long long>(g.prob[i].tiles_per_matrix) * g.prob[i].batch;
+      const long long own = static_cast<long long>(g.prob[i].tiles_per_matrix) * g.prob[i].batch;
+      if (own >= (1ll << 31)) return MUON_ERR_SHAPE;   // the kernel decodes a problem's tiles in 32 bits
+      tiles += own;
     }
     g.nprob = cnt;
     g.counter_deps = 1;
