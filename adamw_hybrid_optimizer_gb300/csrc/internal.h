@@ -84,6 +84,12 @@ struct GemmProblem {
   // element pitches, from out + (2 + 2 j) * gs_plane), and a reduce kernel adds the slices in index order and
   // forms the outputs above
   int ksplit, kper;
+  // Symmetric m x m matrices (G, H) stored as their upper 256-blocks only: block (i, j), rows 256 i .., columns
+  // 256 j .., is stored when j >= i, a diagonal block whole. half_out (GRAM, POLY): store only those blocks (the
+  // mirrored half only inside diagonal blocks). half_a (POLY, APPLY, FINAL) / half_b (POLY): the A / B operand is
+  // such a matrix; a 64-deep step whose 256-block lies left of the operand rows' block reads the stored block
+  // above the diagonal transposed (an MN-major operand through map_t), which holds the same values.
+  int half_out, half_a, half_b;
   // final step: parameter update (params != null) or dense store (out_dense != null); with master, the
   // update applies to the fp32 master copies and params receive them rounded to bf16
   void *const *params;
@@ -187,6 +193,10 @@ class GemmBatch {
   // Per-matrix counter waits replace the wait for the whole previous grid unless this is set: then the
   // launches wait for both (used where the previous launch in the stream belongs to another branch)
   void force_grid_wait(bool on) { grid_wait_ = on; }
+  // Items added after this read and write the symmetric G and H as their upper 256-blocks only (GemmProblem's
+  // half_out, half_a, half_b): GRAM and POLY store no mirrored blocks, POLY, APPLY and the final step read the
+  // blocks below the diagonal transposed. Results are the same bits either way.
+  void half_symmetric(bool on) { half_ = on; }
   ~GemmBatch();
 
  private:
@@ -199,6 +209,7 @@ class GemmBatch {
   int force_ = -1;
   int split_ = 0;
   bool grid_wait_ = false;
+  bool half_ = false;
   muon_status push(const Item &it);
   void order();                        // launch order of the items (stable for a given set)
   int group_size(int first) const;     // items from first that share one launch

@@ -84,6 +84,8 @@ unsigned long long g_timeout_ns = 2000000000ull;
 std::atomic<int> g_counter_deps{-1};
 // Gram-space path: -1 the rule (gram_space_route), 0 never, 1 wherever the shape is eligible
 std::atomic<int> g_gram_space{-1};
+// plain chain: G and H stored as their upper 256-blocks only (1, the default) or whole (0)
+std::atomic<int> g_half_sym{1};
 
 }  // namespace
 
@@ -632,6 +634,10 @@ muon_status issue_chains(const std::vector<ChainStack> &cs, const ChainCall &cc,
     const float a = cc.coeffs[3 * t], b = cc.coeffs[3 * t + 1], c3 = cc.coeffs[3 * t + 2];
     GemmBatch gram(EPI_GRAM, cc.err, to), poly(EPI_POLY, cc.err, to);
     GemmBatch last(t + 1 < N ? EPI_APPLY : EPI_FINAL, cc.err, to);
+    const bool half = g_half_sym.load() != 0;
+    gram.half_symmetric(half);
+    poly.half_symmetric(half);
+    last.half_symmetric(half);
     if (t == 0 && branch) gram.force_grid_wait(true);
     for (const ChainStack &c : cs) {
       if (c.path != PATH_PLAIN) continue;
@@ -1062,6 +1068,7 @@ static muon_status autotune_piece(const muon_bucket *buckets, int n, const muon_
           [&]() -> muon_status {
             GemmBatch poly(EPI_POLY, err, g_timeout_ns);
             poly.force_shape(shape);
+            poly.half_symmetric(g_half_sym.load() != 0);   // as the chain runs it
             for (const ChainStack &c : cs) {
               if (c.path != PATH_PLAIN) continue;
               const long long msg = c.L.m * c.L.ldg;
@@ -1140,6 +1147,12 @@ void muon_autotune_reset(void) {
 muon_status muon_debug_counter_deps(int32_t on) {
   if (on < -1 || on > 1) return MUON_ERR_INVALID_ARG;
   g_counter_deps.store(on);
+  return MUON_OK;
+}
+
+muon_status muon_debug_half_symmetric(int32_t on) {
+  if (on < 0 || on > 1) return MUON_ERR_INVALID_ARG;
+  g_half_sym.store(on);
   return MUON_OK;
 }
 

@@ -3,8 +3,12 @@
 // One Newton-Schulz step ("Optimizers: AdamW, Muon and the distributed optimizer", section
 // "Muon: orthogonalising the update") on a wide iterate X (m x n, m <= n):
 //     G = X X^T                     EPI_GRAM   symmetric: only tiles touching the upper triangle
-//                                              are computed, every value is also stored mirrored
-//                                              ("DMuon", section 2.2, symmetric Gram)
+//                                              are computed ("DMuon", section 2.2, symmetric Gram);
+//                                              G and H are stored as their upper 256-blocks (a diagonal
+//                                              block whole) and their readers take a block below the
+//                                              diagonal as the transpose of the one above it (half_out,
+//                                              half_a, half_b), or, for the single-step entry points,
+//                                              every value is also stored mirrored
 //     H = a I + b G + c G G         EPI_POLY   G symmetric, so G G = G G^T: same operand pattern
 //     X' = H X                      EPI_APPLY  (= a X + (b G + c G G) X); B operand X read N-major
 //     last step: u = H X, then p <- p - lr*wd*p*mask - lr*scale*u      EPI_FINAL (EPI_FINAL_MASTER: on fp32
@@ -104,6 +108,8 @@ static_assert(smem_bytes(EPI_GRAM, 6, 1) <= 232448 && smem_bytes(EPI_POLY, 6, 2)
 struct GemmGroup {
   CUtensorMap map_a[GEMM_MAX_PROBLEMS];
   CUtensorMap map_b[GEMM_MAX_PROBLEMS];
+  // the half-stored symmetric operand (half_a / half_b) as 64 x 64 boxes, for its blocks read transposed
+  CUtensorMap map_t[GEMM_MAX_PROBLEMS];
   GemmProblem prob[GEMM_MAX_PROBLEMS];
   int nprob;
   int symmetric;
@@ -114,7 +120,8 @@ struct GemmGroup {
   int timeline_cap;               // records per CTA
   int counter_deps;               // every problem waits on per-matrix counters: no grid-wide dependency
 };
-static_assert(sizeof(GemmGroup) <= 4096, "kernel parameter block too large");
+// kernel parameters up to 32764 bytes (CUDA 12.1 and later)
+static_assert(sizeof(GemmGroup) <= 32764, "kernel parameter block too large");
 
 // Timeline record of one tile (globaltimer ns): tile index, producer first / last issue, MMA start
 // (accumulator free), first / last operands ready, last commit, epilogue start (accumulator full), end.
@@ -486,6 +493,8 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem &a, int b, int 
         [&](int i, int j) { return warp_row0 + i < rows && col0 + j < cols && col0 + j >= warp_row0 + i; },
         [&](int i) { return warp_row0 + i < rows && col0 + 32 <= cols && (below_free || col0 >= warp_row0 + i); });
     __syncwarp();
+    // half-stored output: no mirrored half outside the diagonal 256-blocks (readers take the transpose)
+    if (a.half_out && (warp_row0 >> 8) != (col0 >> 8)) return;
     // strictly upper part mirrored: element (row, c) also stored at (c, row); the region, transposed in
     // place, holds the transposed chunk, whose row i is output row col0 + i, columns warp_row0 .. +31
     region_transpose(rg, lane);
@@ -732,12 +741,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
           const uint32_t fb = leader_full0 + stage * static_cast<uint32_t>(sizeof(uint64_t));
           uint8_t *sa = smem + stage * SB;
           uint8_t *sb = sa + A_BYTES;
-          tma_load_3d_pair(sa, map_a, fb, kk * BK, ti * BM, b);
+          // half-stored symmetric operands: this step's 256-block (kk / 4) left of the rows' block is read as
+          // the transpose of the stored block above the diagonal, in two 64-wide MN-major chunks
+          const int kblk = kk >> 2;
+          if (P.half_a && kblk < (ti >> 1)) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+              tma_load_3d_pair(sa + q * (64 * BK * 2), &args.map_t[pi], fb, ti * BM + 64 * q, kk * BK, b);
+          } else {
+            tma_load_3d_pair(sa, map_a, fb, kk * BK, ti * BM, b);
+          }
           if constexpr (!SHARED_B) {
             // this CTA's half of B: columns tj*256 + 128*rank .. +127
             if constexpr (!B_MN) {
-              // K-major: those rows of the same tensor through the A map (box 64 x 128)
-              tma_load_3d_pair(sb, map_a, fb, kk * BK, tj * BN + (BN / 2) * static_cast<int>(rank), b);
+              if (P.half_b && kblk < tj) {
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                  tma_load_3d_pair(sb + q * (64 * BK * 2), &args.map_t[pi], fb,
+                                   tj * BN + (BN / 2) * static_cast<int>(rank) + 64 * q, kk * BK, b);
+              } else {
+                // K-major: those rows of the same tensor through the A map (box 64 x 128)
+                tma_load_3d_pair(sb, map_a, fb, kk * BK, tj * BN + (BN / 2) * static_cast<int>(rank), b);
+              }
             } else {
               // N-major: column chunks 2*rank and 2*rank+1 (64 columns each); with k_wrap, the second half of the
               // contraction reads B's rows again from the top
@@ -763,6 +788,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
     if (lane == 0 && rank == 0) {
       // ---------------------------------------------------------------- MMA issuer (even CTA: M = 256 pair MMAs)
       constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN, false, B_MN);
+      // with a half-stored symmetric operand: A transposed (MN-major) and / or B MN-major for some steps
+      constexpr uint32_t idesc_kt = idesc_bf16_f32(2 * BM, BN, false, true);
+      constexpr uint32_t idesc_tk = idesc_bf16_f32(2 * BM, BN, true, false);
+      constexpr uint32_t idesc_tt = idesc_bf16_f32(2 * BM, BN, true, true);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       bool issued = false;
@@ -776,6 +805,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         const GemmProblem &P = args.prob[find_problem(args, t)];
         int k0, k1;
         tile_k_range(P, t - P.tile_begin, k0, k1);
+        // 256-blocks of the contraction read transposed (half-stored symmetric operands): A's below its rows'
+        // block, B's below its columns' block
+        int a_tblk = 0, b_tblk = 0;
+        if (P.half_a || P.half_b) {
+          int mb, mti, mtj;
+          decode_tile(P, args.symmetric, t - P.tile_begin, rank, mb, mti, mtj);
+          a_tblk = P.half_a ? (mti >> 1) : 0;
+          b_tblk = P.half_b ? mtj : 0;
+        }
         for (int kk = k0; kk < k1; ++kk) {
           if (!wait_bounded(&ctrl->full[stage], phase, ctl, ERR_WAIT_FULL)) {
             ok = false;
@@ -785,12 +823,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * SB);
           const uint32_t sb = SHARED_B ? sa : sa + A_BYTES;
+          const bool a_t = (kk >> 2) < a_tblk;
+          const bool b_mn = B_MN || (kk >> 2) < b_tblk;
+          const uint32_t id = a_t ? (b_mn ? idesc_tt : idesc_tk) : (b_mn ? idesc_kt : idesc);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t adesc = smem_desc_sw128(sa + k * 32, 16, 1024);
+            const uint64_t adesc =
+                a_t ? smem_desc_sw128(sa + k * 16 * 128, 64 * BK * 2, 1024) : smem_desc_sw128(sa + k * 32, 16, 1024);
             const uint64_t bdesc =
-                B_MN ? smem_desc_sw128(sb + k * 16 * 128, 64 * BK * 2, 1024) : smem_desc_sw128(sb + k * 32, 16, 1024);
-            tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, ((kk - k0) | k) != 0 ? 1u : 0u);
+                b_mn ? smem_desc_sw128(sb + k * 16 * 128, 64 * BK * 2, 1024) : smem_desc_sw128(sb + k * 32, 16, 1024);
+            tc_mma_bf16_pair(d_tmem, adesc, bdesc, id, ((kk - k0) | k) != 0 ? 1u : 0u);
           }
           issued = true;
           tc_commit_pair_mc(&ctrl->empty[stage], 0x3);   // frees the stage in both CTAs of the pair
@@ -1249,7 +1291,7 @@ bool apply_maps(const Bf16Stack &h, const Bf16Stack &x, CUtensorMap *ma, CUtenso
 }  // namespace
 
 struct GemmBatch::Item {
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mt;
   GemmProblem p;
 };
 
@@ -1301,6 +1343,7 @@ muon_status GemmBatch::add_gram(const Bf16Stack &x, __nv_bfloat16 *g, long long 
   it.p.out = g;
   it.p.ld_out = ldg;
   it.p.mstride_out = mstride_g;
+  it.p.half_out = half_ ? 1 : 0;
   set_sync(it.p, sync);
   return push(it);
 }
@@ -1341,6 +1384,10 @@ muon_status GemmBatch::add_poly(const Bf16Stack &g, __nv_bfloat16 *h, long long 
   it.p.out = h;
   it.p.ld_out = ldh;
   it.p.mstride_out = mstride_h;
+  if (half_) {
+    if (!make_map(&it.mt, g.ptr, g.cols, g.rows, g.batch, g.ld, g.mstride, 64)) return MUON_ERR_CUDA;
+    it.p.half_out = it.p.half_a = it.p.half_b = 1;
+  }
   set_sync(it.p, sync);
   return push(it);
 }
@@ -1351,6 +1398,10 @@ muon_status GemmBatch::add_apply(const Bf16Stack &h, const Bf16Stack &x, __nv_bf
   Item it{};
   if (!apply_maps(h, x, &it.ma, &it.mb)) return MUON_ERR_CUDA;
   fill_tiles(it.p, x.batch, x.rows, x.cols, h.cols, false);
+  if (half_) {
+    if (!make_map(&it.mt, h.ptr, h.cols, h.rows, h.batch, h.ld, h.mstride, 64)) return MUON_ERR_CUDA;
+    it.p.half_a = 1;
+  }
   it.p.scale = scale;
   it.p.out = out;
   it.p.ld_out = x.ld;
@@ -1365,6 +1416,10 @@ muon_status GemmBatch::add_final(const Bf16Stack &h, const Bf16Stack &x, const f
   Item it{};
   if (!apply_maps(h, x, &it.ma, &it.mb)) return MUON_ERR_CUDA;
   fill_tiles(it.p, x.batch, x.rows, x.cols, h.cols, false);
+  if (half_ && k_wrap == 0) {   // [R_hi | R_lo] of the Gram-space path is stored whole
+    if (!make_map(&it.mt, h.ptr, h.cols, h.rows, h.batch, h.ld, h.mstride, 64)) return MUON_ERR_CUDA;
+    it.p.half_a = 1;
+  }
   it.p.k_wrap = k_wrap;
   it.p.scale = scale;
   it.p.params = f.params;
@@ -1421,6 +1476,7 @@ muon_status GemmBatch::launch(cudaStream_t s) {
     for (int i = 0; i < cnt; ++i) {
       g.map_a[i] = items_[first + i].ma;
       g.map_b[i] = items_[first + i].mb;
+      g.map_t[i] = items_[first + i].mt;
       g.prob[i].tile_begin = tiles;
       const long long own = static_cast<long long>(g.prob[i].tiles_per_matrix) * g.prob[i].batch;
       if (own >= (1ll << 31)) return MUON_ERR_SHAPE;   // the kernel decodes a problem's tiles in 32 bits

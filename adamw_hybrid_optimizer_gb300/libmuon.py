@@ -96,6 +96,7 @@ SIGNATURES = {
     "muon_debug_gram_split": (ctypes.c_int, [ctypes.c_int32]),
     "muon_debug_poly_shape": (ctypes.c_int, [ctypes.c_int32]),
     "muon_debug_counter_deps": (ctypes.c_int, [ctypes.c_int32]),
+    "muon_debug_half_symmetric": (ctypes.c_int, [ctypes.c_int32]),
     "muon_debug_gram_space": (ctypes.c_int, [ctypes.c_int32]),
     "muon_gram_space_route": (ctypes.c_int32, [_c_int64, _c_int64, _c_int64]),
     "muon_check": (ctypes.c_int, [_vp, _vp]),
@@ -402,6 +403,11 @@ def muon_debug_poly_shape(shape: int):
 def muon_debug_counter_deps(mode: int):
     """1: counter dependencies in the grouped chain, 0: launch order, -1: the library's rule (default)."""
     _check(lib().muon_debug_counter_deps(int(mode)), "muon_debug_counter_deps")
+
+
+def muon_debug_half_symmetric(on: int):
+    """1: the chain stores G and H as their upper 256-blocks only (default), 0: whole. Same results."""
+    _check(lib().muon_debug_half_symmetric(int(on)), "muon_debug_half_symmetric")
 
 
 def muon_debug_gram_space(mode: int):
