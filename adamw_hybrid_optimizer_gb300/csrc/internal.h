@@ -85,10 +85,10 @@ struct GemmProblem {
   // forms the outputs above
   int ksplit, kper;
   // Symmetric m x m matrices (G, H) stored as their upper 256-blocks only: block (i, j), rows 256 i .., columns
-  // 256 j .., is stored when j >= i, a diagonal block whole. half_out (GRAM, POLY): store only those blocks (the
-  // mirrored half only inside diagonal blocks). half_a (POLY, APPLY, FINAL) / half_b (POLY): the A / B operand is
-  // such a matrix; a 64-deep step whose 256-block lies left of the operand rows' block reads the stored block
-  // above the diagonal transposed (an MN-major operand through map_t), which holds the same values.
+  // 256 j .., is stored when j >= i, a diagonal block whole. half_out (GRAM, POLY): store only those blocks, every
+  // element as computed, nothing mirrored. half_a (POLY, APPLY, FINAL) / half_b (POLY): the A / B operand is such
+  // a matrix; a 64-deep step whose 256-block lies left of the operand rows' block reads the stored block above the
+  // diagonal transposed (an MN-major operand through map_t), which holds the same values.
   int half_out, half_a, half_b;
   // final step: parameter update (params != null) or dense store (out_dense != null); with master, the
   // update applies to the fp32 master copies and params receive them rounded to bf16

@@ -484,6 +484,18 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem &a, int b, int 
       for (int j = 0; j < 32; ++j) v[j] *= sc;
     }
     __nv_bfloat16 *out_b = a.out + static_cast<long long>(b) * a.mstride_out;
+    if (a.half_out) {
+      // upper 256-blocks only, every element as computed: an off-diagonal block lies above the diagonal, and a
+      // diagonal block's pair tile computed both of its halves; readers take the blocks below the diagonal
+      // transposed, so nothing is mirrored
+      region_write_row(rg, lane, v);
+      __syncwarp();
+      region_store(
+          rg, lane, out_b + static_cast<long long>(warp_row0) * a.ld_out + col0, a.ld_out,
+          [&](int i, int j) { return warp_row0 + i < rows && col0 + j < cols; },
+          [&](int i) { return warp_row0 + i < rows && col0 + 32 <= cols; });
+      return;
+    }
     // upper triangle including the diagonal, stored as computed: element (row, c) with c >= row
     region_write_row(rg, lane, v);
     __syncwarp();
@@ -493,8 +505,6 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem &a, int b, int 
         [&](int i, int j) { return warp_row0 + i < rows && col0 + j < cols && col0 + j >= warp_row0 + i; },
         [&](int i) { return warp_row0 + i < rows && col0 + 32 <= cols && (below_free || col0 >= warp_row0 + i); });
     __syncwarp();
-    // half-stored output: no mirrored half outside the diagonal 256-blocks (readers take the transpose)
-    if (a.half_out && (warp_row0 >> 8) != (col0 >> 8)) return;
     // strictly upper part mirrored: element (row, c) also stored at (c, row); the region, transposed in
     // place, holds the transposed chunk, whose row i is output row col0 + i, columns warp_row0 .. +31
     region_transpose(rg, lane);
@@ -883,7 +893,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         for (int s = 0; s < BN / 64; ++s) {
           const int c0 = tj * BN + 64 * s;
           if (c0 >= P.cols) break;
-          if (!slot_used(args.symmetric, c0, row0)) continue;
+          if (!slot_used(args.symmetric && !P.half_out, c0, row0)) continue;
           bool w = true;
           if (lane == 0) w = wait_bounded(&ctrl->ring_empty[slot], rphase ^ 1u, ctl, ERR_WAIT_RING_EMPTY);
           if (!__shfl_sync(0xffffffffu, w, 0)) {
@@ -1003,7 +1013,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
       for (int s = 0; s < BN / 64; ++s) {
         const int c0 = tj * BN + 64 * s;
         if (c0 >= P.cols) break;
-        if (EPI != EPI_GRAM && !slot_used(args.symmetric, c0, row0)) continue;
+        if (EPI != EPI_GRAM && !slot_used(args.symmetric && !P.half_out, c0, row0)) continue;
         // kinds without a second input use slot 0 only as staging space
         uint8_t *slot_ptr = ring + (has_aux(EPI) ? slot : 0) * SLOT_BYTES;
         if constexpr (has_aux(EPI)) {
@@ -1016,7 +1026,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         {
           const int col0 = c0 + 32 * my_half;
           // warp-uniform: chunk past the last column, below the diagonal for every lane, or past the last row
-          if (col0 < P.cols && !(args.symmetric && col0 + 31 < warp_row0) && warp_row0 < P.rows) {
+          if (col0 < P.cols && !(args.symmetric && !P.half_out && col0 + 31 < warp_row0) && warp_row0 < P.rows) {
             float v[32];
             tmem_ld_32x32b_x32(tmem_base + acc * ACC_COLS + (static_cast<uint32_t>(lane_base) << 16) +
                                    (col0 - tj * BN),

@@ -373,9 +373,10 @@ int32_t muon_gram_space_route(int64_t K, int64_t A, int64_t B);
 muon_status muon_debug_counter_deps(int32_t on);
 
 /* Storage of the symmetric m x m matrices of the Newton-Schulz chain (G = X X^T and the polynomial H).
- * 1 (the default): only their upper 256-blocks are stored (a diagonal block whole); the steps that read G
- * or H take a block below the diagonal as the transpose of the stored block above it. 0: both halves are
- * stored and read directly. The same values are read either way, so results are identical; for tests and
+ * 1 (the default): only their upper 256-blocks are stored, as computed (a diagonal block whole); the steps
+ * that read G or H take a block below the diagonal as the transpose of the stored block above it. 0: the
+ * strictly upper part is stored and mirrored, and every block is read directly. The tensor cores compute both
+ * halves of a diagonal block identically, so results are the same bits either way; for tests and
  * measurements. MUON_ERR_INVALID_ARG for other values. No counterpart on the pages. */
 muon_status muon_debug_half_symmetric(int32_t on);
 
