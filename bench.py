@@ -638,8 +638,9 @@ def run_ours(args):
 def run_profile_small(args):
     """One grouped Muon step, with no warm-up and no autotune, on a small case of a parameter set, so that an ncu
     capture can pick its launches by position: counter reset, norm pass, then per Newton-Schulz step the Gram,
-    polynomial and apply (final at the last step) launches (Gram-space buckets: fp32 Gram, m x m chain, final).
-    The stacks are larger than L2, so DRAM figures mean something; prints the launches and the work per kernel."""
+    polynomial and apply (final at the last step) launches (Gram-space buckets: fp32 Gram, m x m chain, final);
+    for the GPT-2-small set, the whole set and then its AdamW pass. The stacks are larger than L2, so DRAM figures
+    mean something; prints the launches."""
     import torch
     import __graft_entry__
     __graft_entry__.build()
@@ -648,6 +649,21 @@ def run_profile_small(args):
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
     name = args.profile_small
+    if name == "gpt2s":
+        # the whole set, small enough: its grouped Muon step, then its AdamW pass
+        wl = Workload(L, dev, name)
+        torch.cuda.synchronize()
+        n0 = L.muon_launch_count()
+        wl.begin_step()
+        wl.muon_part()
+        wl.adamw_part()
+        torch.cuda.synchronize()
+        if L.muon_check(wl.ws) != L.MUON_OK:
+            raise RuntimeError("a device-side wait ran out")
+        print(json.dumps({"profile_small": name, "matrices_per_bucket": "all",
+                          "buckets": [f"{bk['A']}x{bk['B']}" for bk in wl.buckets], "adamw_elems": wl.w.adamw_elems,
+                          "launches": L.muon_launch_count() - n0}), flush=True)
+        return 0
     w = workloads.workload(name)
     per_bucket_K = {"llama8b": 2, "aspect": 8}[name]
     plan = L.muon_plan_buckets(workloads.shape_list(w))
@@ -908,7 +924,8 @@ def main():
                     help="skip the measured choices at initialisation (the rules decide; for launch-list captures)")
     ap.add_argument("--profile-small", default="",
                     help="one grouped Muon step (no warm-up, no autotune) of a small case of the named set, "
-                         "for ncu captures: 'llama8b' (K=2 per bucket) or 'aspect' (K=8 per bucket)")
+                         "for ncu captures: 'llama8b' (K=2 per bucket), 'aspect' (K=8 per bucket) or 'gpt2s' "
+                         "(the whole set, then its AdamW pass)")
     ap.add_argument("--ns-sweep", action="store_true", help="Newton-Schulz size sweep instead of the bench line")
     ap.add_argument("--sizes", default="", help="comma-separated n for --ns-sweep")
     ap.add_argument("--small-sweep", action="store_true", help="fused small-matrix chain vs separate launches")
