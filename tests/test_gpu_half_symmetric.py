@@ -3,8 +3,9 @@ both halves stored.
 
 A step that reads G or H takes a block below the diagonal as the transpose of the stored block above it. That
 block holds the values the mirrored store would have written there, so the two modes must agree bit for bit:
-in ns_orthogonalize on wide, tall, square and ragged stacks (m a multiple of 256 or not, one or several 256-blocks),
-and in grouped momentum steps with fp32 and bf16 parameters, cautious decay and both launch-scheduling modes.
+in ns_orthogonalize on wide, tall, square and ragged stacks (m a multiple of 256 or not, one or several
+256-blocks), in every POLY pipeline shape, and in grouped momentum steps with fp32 and bf16 parameters,
+cautious decay and both launch-scheduling modes.
 """
 import dataclasses
 
@@ -86,3 +87,20 @@ def test_half_stored_grouped_steps_are_bitwise_the_whole_ones(L, dtype, deps):
     for a, b in zip(mh, mw):
         assert torch.equal(a, b)
     assert any(not torch.equal(a, b) for a, b in zip(ph, p0))   # the steps moved the parameters
+
+
+@pytest.mark.parametrize("shape", [0, 1, 2])
+def test_half_stored_chain_in_every_poly_pipeline_shape(L, shape):
+    # each POLY shape has its own ring of G blocks for b·G, which in upper-block mode also carries the blocks
+    # below the diagonal of the diagonal pair tiles
+    g = torch.Generator().manual_seed(40 + shape)
+    x = torch.randn((2, 640, 1536), generator=g, dtype=torch.float64).to(torch.bfloat16).to(DEV)
+    L.muon_debug_poly_shape(shape)
+    try:
+        half = _ns(L, x, torch.float32, 1)
+        whole = _ns(L, x, torch.float32, 0)
+    finally:
+        L.muon_debug_poly_shape(-1)
+        L.muon_debug_half_symmetric(1)
+    assert torch.isfinite(half).all()
+    assert torch.equal(half, whole)
