@@ -412,7 +412,7 @@ def _run_e2e(wl, args, stream, world, device, barrier):
     step runs as several calls on the compute stream, each started as soon as its inputs are in (the Muon
     chains of the pieces of split_pieces() with the AdamW pass among them, in the order it gives); inputs go in
     on one copy stream in that order, and each call's parameters come out on a second copy stream once it is
-    done."""
+    done. The host issues the calls and copies interleaved, each copy after the call it should overlap."""
     import torch
     dev_g, dev_p = wl.host_views()
     h2d = sum(t.numel() * t.element_size() for t in dev_g)
@@ -456,22 +456,33 @@ def _run_e2e(wl, args, stream, world, device, barrier):
     barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
+    def put(j):   # call j's gradients in, on the input copy stream
         with torch.cuda.stream(copy_in):
-            for (idx, _), e in zip(pieces, ev_in):
-                for i, k0, k1 in idx:
-                    dev_g[i][k0:k1].copy_(host_g[i][k0:k1], non_blocking=True)
-                e.record(copy_in)
-        wl.begin_step()
-        for (_, run), ei, ed in zip(pieces, ev_in, ev_done):
-            stream.wait_event(ei)
-            run()
-            ed.record(stream)
+            for i, k0, k1 in pieces[j][0]:
+                dev_g[i][k0:k1].copy_(host_g[i][k0:k1], non_blocking=True)
+            ev_in[j].record(copy_in)
+
+    def get(j):   # call j's parameters out, on the output copy stream, once the call is done
         with torch.cuda.stream(copy_out):
-            for (idx, _), e in zip(pieces, ev_done):
-                copy_out.wait_event(e)
-                for i, k0, k1 in idx:
-                    host_p[i][k0:k1].copy_(dev_p[i][k0:k1], non_blocking=True)
+            copy_out.wait_event(ev_done[j])
+            for i, k0, k1 in pieces[j][0]:
+                host_p[i][k0:k1].copy_(dev_p[i][k0:k1], non_blocking=True)
+
+    for _ in range(e2e_steps):
+        wl.begin_step()
+        # issued in pipeline order: a host whose copy calls return only once the data has moved (on some boxes
+        # the host-to-device path stages through the driver) still has call j queued on the GPU while it copies
+        # call j + 1's inputs and call j - 1's outputs; where copies are asynchronous the order changes nothing
+        put(0)
+        for j, (_, run) in enumerate(pieces):
+            stream.wait_event(ev_in[j])
+            run()
+            ev_done[j].record(stream)
+            if j + 1 < len(pieces):
+                put(j + 1)
+            if j > 0:
+                get(j - 1)
+        get(len(pieces) - 1)
         copy_out.synchronize()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(1e3 * (time.perf_counter() - t0) / e2e_steps, world, device)
