@@ -453,9 +453,6 @@ def _run_e2e(wl, args, stream, world, device, barrier):
     copy_in, copy_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     ev_in = [torch.cuda.Event() for _ in pieces]
     ev_done = [torch.cuda.Event() for _ in pieces]
-    barrier()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
     def put(j):   # call j's gradients in, on the input copy stream
         with torch.cuda.stream(copy_in):
             for i, k0, k1 in pieces[j][0]:
@@ -468,11 +465,14 @@ def _run_e2e(wl, args, stream, world, device, barrier):
             for i, k0, k1 in pieces[j][0]:
                 host_p[i][k0:k1].copy_(dev_p[i][k0:k1], non_blocking=True)
 
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
     for _ in range(e2e_steps):
         wl.begin_step()
-        # issued in pipeline order: a host whose copy calls return only once the data has moved (on some boxes
-        # the host-to-device path stages through the driver) still has call j queued on the GPU while it copies
-        # call j + 1's inputs and call j - 1's outputs; where copies are asynchronous the order changes nothing
+        # issued in pipeline order: a host whose copy calls return only once the data has moved (as on some
+        # boxes) still has call j queued on the GPU while it copies call j + 1's inputs and call j - 1's
+        # outputs; where copies are asynchronous the order changes nothing
         put(0)
         for j, (_, run) in enumerate(pieces):
             stream.wait_event(ev_in[j])
