@@ -453,6 +453,7 @@ def _run_e2e(wl, args, stream, world, device, barrier):
     copy_in, copy_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     ev_in = [torch.cuda.Event() for _ in pieces]
     ev_done = [torch.cuda.Event() for _ in pieces]
+
     def put(j):   # call j's gradients in, on the input copy stream
         with torch.cuda.stream(copy_in):
             for i, k0, k1 in pieces[j][0]:
