@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <utility>
 
 #include "internal.h"
@@ -37,10 +38,10 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // Block of 256 threads on one 64 x 64 tile (tr, tc) of matrix b of the stored (A x B) stack; thread
 // (tx, ty) handles columns 4*tx..4*tx+3 of rows ty, ty+16, ty+32, ty+48. Returns the thread's sum of U^2.
-template <typename GT, bool MOMENTUM>
+template <typename GT, bool MOMENTUM, int TR>
 __device__ __forceinline__ float nesterov_tile(const NesterovArgs &a, long long b, int tr, int tc,
-                                               __nv_bfloat16 (*tile)[NESTEROV_TILE + 8]) {
-  constexpr int T = NESTEROV_TILE;
+                                               __nv_bfloat16 (*tile)[TR + 8]) {
+  constexpr int T = NESTEROV_TILE;   // columns; TR rows
   const long long mat = static_cast<long long>(a.A) * a.B;
   const GT *g = a.gptrs != nullptr ? static_cast<const GT *>(a.gptrs[b])
                                    : static_cast<const GT *>(a.gbase) + b * mat;
@@ -55,10 +56,12 @@ __device__ __forceinline__ float nesterov_tile(const NesterovArgs &a, long long 
                    ((reinterpret_cast<uintptr_t>(g) & (4 * sizeof(GT) - 1)) == 0) &&
                    (!MOMENTUM || (reinterpret_cast<uintptr_t>(M) & 15) == 0);
   float ss = 0.f;
+#pragma unroll 1
+  for (int p0 = 0; p0 < TR / 16; p0 += 4) {
 #pragma unroll
-  for (int p = 0; p < 4; ++p) {
+  for (int p = p0; p < p0 + 4; ++p) {
     const int lrow = ty + 16 * p;
-    const int r = tr * T + lrow;
+    const int r = tr * TR + lrow;
     float uv[4] = {0.f, 0.f, 0.f, 0.f};
     if (r < a.A) {
       const long long base = static_cast<long long>(r) * a.B + c0;
@@ -123,22 +126,25 @@ __device__ __forceinline__ float nesterov_tile(const NesterovArgs &a, long long 
       for (int q = 0; q < 4; ++q) tile[tx * 4 + q][lrow] = __float2bfloat16_rn(uv[q]);
     }
   }
+  }
   if (a.transposed) {
     __syncthreads();
-    // wide row = stored column, wide column = stored row
+    // wide row = stored column, wide column = stored row: thread tx writes TR/16 consecutive elements of it
+    constexpr int E = TR / 16;
+    using Vec = typename std::conditional<E == 8, uint4, uint2>::type;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
       const int lc = ty + 16 * p;
       const int c = tc * T + lc;
-      const int r0 = tr * T + tx * 4;
+      const int r0 = tr * TR + tx * E;
       if (c < a.B) {
         __nv_bfloat16 *dst = u + static_cast<long long>(c) * a.ldu + r0;
-        if (r0 + 4 <= a.A) {
-          *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(&tile[lc][tx * 4]);
+        if (r0 + E <= a.A) {
+          *reinterpret_cast<Vec *>(dst) = *reinterpret_cast<const Vec *>(&tile[lc][tx * E]);
         } else {
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (r0 + q < a.A) dst[q] = tile[lc][tx * 4 + q];
+          for (int q = 0; q < E; ++q)
+            if (r0 + q < a.A) dst[q] = tile[lc][tx * E + q];
         }
       }
     }
@@ -234,10 +240,13 @@ __device__ __forceinline__ float nesterov_tile_wide(const NesterovArgs &a, long 
 // matrix's counter; the block that completes the count sums the matrix's tile sums in index order (the
 // same order whichever block finishes last) and writes s = 1 / (sqrt(sum) + eps).
 template <bool MOMENTUM>
-__global__ void __launch_bounds__(256) nesterov_norm_kernel(const __grid_constant__ NesterovGroup G) {
+// at most 32 registers (8 blocks of 256 threads per SM): the pass needs every block it can keep resident to have
+// enough loads in flight, and the two tile shapes of a transposed store would otherwise cost 48
+__global__ void __launch_bounds__(256, 8) nesterov_norm_kernel(const __grid_constant__ NesterovGroup G) {
   pdl_wait();
   if (threadIdx.x == 0) pdl_launch_dependents();
-  __shared__ __nv_bfloat16 tile[NESTEROV_TILE][NESTEROV_TILE + 8];
+  // the transposing tiles' buffer: 64 columns of up to NESTEROV_TALL_ROWS rows (+8 of padding)
+  __shared__ __align__(16) __nv_bfloat16 tile_buf[NESTEROV_TILE * (NESTEROV_TALL_ROWS + 8)];
   __shared__ float red[8];
   __shared__ int last;
   int pi = 0;
@@ -250,12 +259,18 @@ __global__ void __launch_bounds__(256) nesterov_norm_kernel(const __grid_constan
   const int tr = static_cast<int>(t / a.tiles_c);
   const int tc = static_cast<int>(t - static_cast<long long>(tr) * a.tiles_c);
   float ss;
-  if (a.wide_tiles && !a.transposed)
+  if (a.wide_tiles && !a.transposed) {
     ss = a.gdtype == MUON_F32 ? nesterov_tile_wide<float, MOMENTUM>(a, b, tr, tc)
                               : nesterov_tile_wide<__nv_bfloat16, MOMENTUM>(a, b, tr, tc);
-  else
-    ss = a.gdtype == MUON_F32 ? nesterov_tile<float, MOMENTUM>(a, b, tr, tc, tile)
-                              : nesterov_tile<__nv_bfloat16, MOMENTUM>(a, b, tr, tc, tile);
+  } else if (a.wide_tiles) {   // stored tall: 128-row tiles, so that each row of U gets 256 bytes at a time
+    auto tile = reinterpret_cast<__nv_bfloat16 (*)[NESTEROV_TALL_ROWS + 8]>(tile_buf);
+    ss = a.gdtype == MUON_F32 ? nesterov_tile<float, MOMENTUM, NESTEROV_TALL_ROWS>(a, b, tr, tc, tile)
+                              : nesterov_tile<__nv_bfloat16, MOMENTUM, NESTEROV_TALL_ROWS>(a, b, tr, tc, tile);
+  } else {
+    auto tile = reinterpret_cast<__nv_bfloat16 (*)[NESTEROV_TILE + 8]>(tile_buf);
+    ss = a.gdtype == MUON_F32 ? nesterov_tile<float, MOMENTUM, NESTEROV_TILE>(a, b, tr, tc, tile)
+                              : nesterov_tile<__nv_bfloat16, MOMENTUM, NESTEROV_TILE>(a, b, tr, tc, tile);
+  }
   ss = warp_sum(ss);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();

@@ -302,9 +302,11 @@ struct NesterovArgs {
   int K, A, B, tiles_r, tiles_c, transposed;
   float mu, eps;
   int nesterov;
-  int wide_tiles;   // 1 (not transposed only): tiles of 64 rows x NESTEROV_WIDE_TILE columns; 0: 64 x 64
+  int wide_tiles;   // 1: tiles of 64 rows x NESTEROV_WIDE_TILE columns, or of NESTEROV_TALL_ROWS x 64 where stored
+                    // tall; 0: 64 x 64
 };
 constexpr int NESTEROV_TILE = 64;
+constexpr int NESTEROV_TALL_ROWS = 128;   // rows of a tile of a matrix stored tall (wide_tiles)
 constexpr int NESTEROV_WIDE_TILE = 256;
 constexpr int NESTEROV_MAX_PROBLEMS = 16;
 struct NesterovGroup {

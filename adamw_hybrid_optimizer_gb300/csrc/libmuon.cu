@@ -217,12 +217,14 @@ NesterovArgs nesterov_args(char *w, const Layout &L, unsigned *counters, long lo
   na.tiles_r = static_cast<int>(L.tiles_r);
   na.tiles_c = static_cast<int>(L.tiles_c);
   na.transposed = A > B ? 1 : 0;
-  if (!na.transposed) {
-    // rows of 256 columns per block: longer contiguous segments, and a quarter of the blocks (and of
-    // their per-block reduction, fence and count) of 64 x 64 tiles; the partial sums need less room
-    na.wide_tiles = 1;
+  // rows of 256 columns per block where stored wide: longer contiguous segments, and a quarter of the blocks
+  // (and of their per-block reduction, fence and count) of 64 x 64 tiles; 128 x 64 tiles where stored tall,
+  // so that each row of the transposed U is written 256 bytes at a time; the partial sums need less room
+  na.wide_tiles = 1;
+  if (!na.transposed)
     na.tiles_c = static_cast<int>((B + NESTEROV_WIDE_TILE - 1) / NESTEROV_WIDE_TILE);
-  }
+  else
+    na.tiles_r = static_cast<int>((A + NESTEROV_TALL_ROWS - 1) / NESTEROV_TALL_ROWS);
   na.mu = mu;
   na.eps = eps;
   na.nesterov = nesterov ? 1 : 0;
